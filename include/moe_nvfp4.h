@@ -1,0 +1,211 @@
+/*
+ * moe_nvfp4.h -- C ABI of the GB300 (sm_103a) NVFP4-weight mixture-of-experts
+ * layer: FP16 activations, E2M1 weights with one E4M3 scale per 16 elements
+ * along K and one FP32 scale per tensor, FP32 accumulation.
+ *
+ * The layer, as described by the page "[Kernel][SM70] Improve Qwen3.8 no-MTP
+ * concurrency" (section "Scope and related PRs"): a router, expert dispatch by
+ * one integer plan shared by the grouped W13 and grouped W2 GEMMs, W13 (gate
+ * and up projections) fused with SwiGLU, W2 fused with the weighted top-k
+ * reduction, and an optional always-on shared expert scaled by a sigmoid gate.
+ * Top-10 routing over 512 experts is the workload of "[Perf][SM70] Optimize
+ * Qwen3.8 Flash Next prefill", section "SM70 QSA indexer hotspot update".
+ *
+ * Conventions common to every entry point
+ * ---------------------------------------
+ * - Pointers named "device" are CUDA device pointers owned by the caller and
+ *   borrowed for the duration of the call's stream work; the library keeps no
+ *   reference after the work completes.  The library allocates no memory.
+ * - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *   All GPU work is enqueued on it; no entry point synchronises the host, so
+ *   every call may be captured in a CUDA graph.
+ * - Return value: MOE_OK (0) or a negative MOE_ERR_* code.  Arguments are
+ *   validated on the host before anything is enqueued: on any error nothing
+ *   is launched and no output is touched (fail closed).  No C++ exception
+ *   crosses the ABI.
+ * - `status` (device, uint32_t, may be NULL) collects asynchronous conditions
+ *   as OR-ed MOE_ST_* bits.  The library never clears it: the caller zeroes it
+ *   and reads it after synchronising.
+ * - FP16 tensors are passed as `const void*` to raw IEEE binary16 data.
+ * - Every device pointer must be 16-byte aligned (MOE_ERR_ALIGNMENT).
+ */
+#ifndef MOE_NVFP4_H
+#define MOE_NVFP4_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MOE_NVFP4_ABI_VERSION 1
+
+/* ---- return codes ---- */
+#define MOE_OK 0
+#define MOE_ERR_INVALID_ARG (-1)        /* NULL where required, bad flag, M < 0 */
+#define MOE_ERR_SHAPE (-2)              /* unsupported sizes (see each call) */
+#define MOE_ERR_ALIGNMENT (-3)          /* a device pointer not 16-byte aligned */
+#define MOE_ERR_WORKSPACE (-4)          /* plan or workspace buffer too small */
+#define MOE_ERR_UNSUPPORTED_DEVICE (-5) /* current device is not compute capability 10.3 */
+#define MOE_ERR_CUDA (-6)               /* a CUDA runtime call or launch failed */
+#define MOE_ERR_LAYOUT (-7)             /* weights not in the layout the path needs */
+
+/* ---- asynchronous status bits (OR-ed into *status on the device) ---- */
+#define MOE_ST_INVALID_ID 0x1u /* a given expert id was outside [0, n_experts): pair dropped */
+#define MOE_ST_NONFINITE 0x2u  /* quantiser input held NaN or infinity */
+#define MOE_ST_TIMEOUT 0x4u    /* a bounded device-side wait gave up; outputs are invalid */
+
+/* ---- configuration flags ---- */
+#define MOE_FLAG_IDS_GIVEN 0x1u /* moe_nvfp4_plan: take ids and weights from the caller */
+#define MOE_FLAG_SHARED 0x2u    /* the layer has a shared expert (gate w_g + shared MLP) */
+
+/* ---- weight layouts (moe_nvfp4_quantize `layout`, moe_nvfp4_weights.layout) ----
+ *
+ * A quantised matrix has `rows` rows of `k` elements; n_mats matrices are
+ * stored back to back.  Scales are E4M3 ("fn": 0x7F/0xFF NaN, max 448), one
+ * per 16 consecutive elements of a row.
+ *
+ * MOE_LAYOUT_CANONICAL (0): q is [n_mats][rows][k/2] bytes, byte i of a row
+ *   holding element 2i in its low nibble and element 2i+1 in its high nibble;
+ *   s is [n_mats][rows][k/16].
+ *
+ * MOE_LAYOUT_FRAGMENT (1): rows % 16 == 0 and k % 64 == 0.  The matrix is cut
+ *   into 16-row tiles rt and 64-element segments ks.  Tile rt, segment ks of
+ *   matrix m owns the 512-byte q block at byte
+ *       ((m * rows/16 + rt) * k/64 + ks) * 512
+ *   and the 64-byte s block at ((m * rows/16 + rt) * k/64 + ks) * 64.
+ *   For L = 4*g + c (g = 0..7, c = 0..3): q block bytes [16L, 16L+8) are row
+ *   16*rt+g, elements [64*ks+16*c, +16) in canonical byte order, and bytes
+ *   [16L+8, 16L+16) the same elements of row 16*rt+g+8; s block bytes 2L and
+ *   2L+1 are the scales of those two 16-element runs.  One warp reads one
+ *   block with one 16-byte load per thread and holds an MMA operand fragment.
+ *
+ * MOE_LAYOUT_FRAGMENT_W13 (2): for a W13 matrix (rows = 2*I: rows 0..I-1 the
+ *   gate projection, rows I..2I-1 the up projection; rows % 32 == 0): the
+ *   fragment layout of the row-permuted matrix whose tile 2j is gate rows
+ *   [16j, 16j+16) and tile 2j+1 is up rows [I+16j, I+16j+16).
+ *
+ * moe_nvfp4_forward needs W13 in layout 2 and W2 in layout 1.
+ */
+#define MOE_LAYOUT_CANONICAL 0
+#define MOE_LAYOUT_FRAGMENT 1
+#define MOE_LAYOUT_FRAGMENT_W13 2
+
+typedef struct moe_nvfp4_config {
+  int32_t hidden;       /* H: model width; H % 128 == 0, 128 <= H <= 8192 */
+  int32_t n_experts;    /* E: routed experts; E % 8 == 0, 8 <= E <= 512 */
+  int32_t top_k;        /* k: experts per token; 1 <= k <= min(E, 32) */
+  int32_t intermediate; /* I: expert intermediate size; I % 64 == 0, 64 <= I <= 4096 */
+  uint32_t flags;       /* MOE_FLAG_* */
+  int32_t reserved[3];  /* must be zero */
+} moe_nvfp4_config;
+
+/* One NVFP4 weight tensor set (device pointers).  For the routed experts the
+ * arrays hold n_experts matrices back to back and g has n_experts entries; for
+ * the shared expert they hold one matrix and g one entry. */
+typedef struct moe_nvfp4_weights {
+  const uint8_t* q; /* packed E2M1 codes, layout as above */
+  const uint8_t* s; /* E4M3 block scales, layout as above */
+  const float* g;   /* FP32 per-matrix global scale */
+  int32_t layout;   /* MOE_LAYOUT_* */
+  int32_t reserved; /* must be zero */
+} moe_nvfp4_weights;
+
+/* ABI capability check: returns MOE_NVFP4_ABI_VERSION.  Callers refuse to use
+ * a library whose version differs from the header they were built with. */
+int32_t moe_nvfp4_abi_version(void);
+
+/* Static text for a return code or a single MOE_ST_* bit; never NULL. */
+const char* moe_nvfp4_status_string(int32_t code);
+
+/* Sizes, in bytes, of the plan buffer (for moe_nvfp4_plan) and of the
+ * forward workspace (for moe_nvfp4_forward) for any M <= max_tokens.
+ * Host-only arithmetic; also checks that the current device is an sm_103
+ * part (MOE_ERR_UNSUPPORTED_DEVICE otherwise) unless `plan_bytes` and
+ * `ws_bytes` are both NULL, in which case only `cfg` is validated. */
+int32_t moe_nvfp4_query(const moe_nvfp4_config* cfg, int64_t max_tokens, size_t* plan_bytes,
+                        size_t* ws_bytes);
+
+/* Quantises FP32 weights to NVFP4 (the layer's load-time step; the page
+ * "[Kernel][SM70] Improve Qwen3.8 no-MTP concurrency", section "Scope and
+ * related PRs", names native NVFP4 weights with raw E4M3 scale storage).
+ *
+ *   w      device FP32 [n_mats][rows][k], row-major.
+ *   q      device out, n_mats*rows*k/2 bytes in `layout`.
+ *   s      device out, n_mats*rows*k/16 bytes in `layout`.
+ *   g      device out, FP32 [n_mats].
+ * Per matrix, with every step one correctly rounded FP32 operation:
+ *   g = amax / 2688 (6 * 448; g = 1 for an all-zero matrix),
+ *   s = E4M3_rne_satfinite((amax_of_16_block / g) / 6),
+ *   q = E2M1_rne_satfinite(x / (value(s) * g)), a zero keeping the sign of x
+ *       (x / 0 is not formed: q = +-0 when value(s) * g == 0).
+ * Requires k % 64 == 0, rows % 16 == 0 (rows % 32 == 0 for layout 2),
+ * 1 <= n_mats, rows * k < 2^31.  NaN or infinite input sets MOE_ST_NONFINITE
+ * in *status and is quantised as zero.  Uses `g` as scratch while running. */
+int32_t moe_nvfp4_quantize(const float* w, int64_t n_mats, int64_t rows, int64_t k,
+                           int32_t layout, uint8_t* q, uint8_t* s, float* g, uint32_t* status,
+                           void* stream);
+
+/* Router and routing plan (steps "router" and "one integer plan" of the page
+ * "[Kernel][SM70] Improve Qwen3.8 no-MTP concurrency", section "Scope and
+ * related PRs").
+ *
+ *   M        tokens, 0 <= M <= 2^20 (M == 0 launches nothing).
+ *   x        device FP16 [M][H].
+ *   w_router device FP16 [H][E] (expert index fastest).
+ *   bias     device FP32 [E] or NULL: added to the logits before selection.
+ *   w_gate   device FP16 [H]; required with MOE_FLAG_SHARED, else ignored.
+ *   ids      device int32 [M][k]: out (expert ids, descending logit, ties to
+ *            the lower id) or, with MOE_FLAG_IDS_GIVEN, in.
+ *   topk_w   device FP32 [M][k]: out (softmax of the selected logits) or, with
+ *            MOE_FLAG_IDS_GIVEN, in.
+ *   plan     device buffer of plan_bytes >= moe_nvfp4_query(...).plan_bytes
+ *            for this M; its contents are private to the library.  It must be
+ *            zero-filled once before its first use; the library leaves its
+ *            internal counters at zero after every call.
+ * Logits are FP32 sums of FP16 x FP16 products.  With MOE_FLAG_SHARED the
+ * plan also holds gamma = sigmoid(x . w_g) and one extra pair per token for
+ * the shared expert.  Given ids outside [0, E) are dropped from the plan and
+ * set MOE_ST_INVALID_ID.  Plan calls on one plan buffer must not overlap on
+ * the GPU. */
+int32_t moe_nvfp4_plan(const moe_nvfp4_config* cfg, int64_t M, const void* x,
+                       const void* w_router, const float* bias, const void* w_gate, int32_t* ids,
+                       float* topk_w, void* plan, size_t plan_bytes, uint32_t* status,
+                       void* stream);
+
+/* The layer forward over a plan made by moe_nvfp4_plan with the same cfg and
+ * M (steps "W13/SwiGLU fusion" and "W2/reduction fusion" of the same page):
+ *
+ *   y[t] = fp16( sum_{j<k} w[t,j] * MLP_{ids[t,j]}(x[t])  +  gamma_t * MLP_shared(x[t]) )
+ *   MLP_e(x) = g2_e * W2_e . h,  h = fp16( silu(g13_e * W13_gate_e . x) * (g13_e * W13_up_e . x) )
+ *
+ * with FP32 accumulation and the slot sum in order j = 0..k-1, then the shared
+ * term.  M <= 16 runs the weight-streaming GEMV path, larger M the grouped
+ * tcgen05 GEMMs; both give the same results up to FP32 summation order.
+ *
+ *   w13      routed W13, layout MOE_LAYOUT_FRAGMENT_W13, E matrices [2I][H].
+ *   w2       routed W2, layout MOE_LAYOUT_FRAGMENT, E matrices [H][I].
+ *   shared13, shared2  shared expert (one matrix each, same layouts); required
+ *            with MOE_FLAG_SHARED, else ignored.
+ *   y        device FP16 [M][H] out.
+ *   ws       device workspace of ws_bytes >= moe_nvfp4_query(...).ws_bytes.
+ * Weight pointers need 16-byte alignment; q and s need the sizes above. */
+int32_t moe_nvfp4_forward(const moe_nvfp4_config* cfg, int64_t M, const void* x, const void* plan,
+                          const moe_nvfp4_weights* w13, const moe_nvfp4_weights* w2,
+                          const moe_nvfp4_weights* shared13, const moe_nvfp4_weights* shared2,
+                          void* y, void* ws, size_t ws_bytes, uint32_t* status, void* stream);
+
+/* Dequantises NVFP4 matrices to FP16 (exact: every E2M1 x E4M3 product is an
+ * FP16 value), applying no global scale.  q, s in `layout`; out FP16
+ * [n_mats][rows][k] in canonical row order.  Same shape rules as
+ * moe_nvfp4_quantize.  A diagnostic of the decode that every GEMM kernel
+ * applies to its weight operand. */
+int32_t moe_nvfp4_dequantize(const uint8_t* q, const uint8_t* s, int64_t n_mats, int64_t rows,
+                             int64_t k, int32_t layout, void* out, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_NVFP4_H */

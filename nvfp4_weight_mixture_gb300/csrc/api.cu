@@ -1,0 +1,252 @@
+// C ABI of the NVFP4 MoE library (declared in include/moe_nvfp4.h).
+//
+// Every entry point validates its arguments on the host before anything is
+// enqueued and returns a negative code without launching on any failure
+// ("fails closed for tensor metadata": "[Kernel][SM70] Improve Qwen3.8 no-MTP
+// concurrency", sections "Scope and related PRs" and "Guarded production
+// engine result").  No exception crosses the boundary.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "kernels.h"
+
+using namespace moe;
+
+namespace {
+
+struct DevInfo {
+  bool init = false;
+  bool supported = false;
+  int num_sms = 0;
+};
+
+std::mutex g_dev_mu;
+DevInfo g_dev[64];
+
+// Validates the current device (compute capability 10.3) and caches its SM
+// count.  Returns MOE_OK or an error code.
+int32_t current_device(int* num_sms) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return MOE_ERR_UNSUPPORTED_DEVICE;
+  }
+  if (dev < 0 || dev >= 64) return MOE_ERR_UNSUPPORTED_DEVICE;
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  DevInfo& di = g_dev[dev];
+  if (!di.init) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      cudaGetLastError();
+      return MOE_ERR_UNSUPPORTED_DEVICE;
+    }
+    di.supported = (major == 10 && minor == 3);
+    di.num_sms = sms;
+    di.init = true;
+  }
+  if (!di.supported) return MOE_ERR_UNSUPPORTED_DEVICE;
+  *num_sms = di.num_sms;
+  return MOE_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int32_t check_cfg(const moe_nvfp4_config* cfg, LayerDims* d) {
+  if (!cfg) return MOE_ERR_INVALID_ARG;
+  if (cfg->reserved[0] || cfg->reserved[1] || cfg->reserved[2]) return MOE_ERR_INVALID_ARG;
+  if (cfg->flags & ~(MOE_FLAG_IDS_GIVEN | MOE_FLAG_SHARED)) return MOE_ERR_INVALID_ARG;
+  const int H = cfg->hidden, E = cfg->n_experts, k = cfg->top_k, I = cfg->intermediate;
+  if (H < 256 || H > 4096 || H % 256) return MOE_ERR_SHAPE;
+  if (E < 8 || E > 512 || E % 8) return MOE_ERR_SHAPE;
+  if (k < 1 || k > 32 || k > E) return MOE_ERR_SHAPE;
+  if (I < 128 || I > 4096 || I % 128) return MOE_ERR_SHAPE;
+  d->H = H;
+  d->E = E;
+  d->k = k;
+  d->I = I;
+  d->shared = (cfg->flags & MOE_FLAG_SHARED) != 0;
+  d->k_eff = k + (d->shared ? 1 : 0);
+  d->e_eff = E + (d->shared ? 1 : 0);
+  return MOE_OK;
+}
+
+constexpr int64_t kMaxTokens = int64_t(1) << 20;
+
+size_t plan_bytes_for(const LayerDims& d, int64_t M) {
+  return plan_layout(nullptr, M, d.k_eff, d.e_eff, d.E, d.H, nullptr);
+}
+
+size_t ws_bytes_for(const LayerDims& d, int64_t M) {
+  const int64_t P = M * d.k_eff;
+  return align_up((size_t)P * d.I * sizeof(__half), 256) + (size_t)P * d.H * sizeof(float);
+}
+
+int32_t check_weights(const moe_nvfp4_weights* w, int32_t layout) {
+  if (!w || !w->q || !w->s || !w->g) return MOE_ERR_INVALID_ARG;
+  if (w->reserved) return MOE_ERR_INVALID_ARG;
+  if (w->layout != layout) return MOE_ERR_LAYOUT;
+  if (!aligned16(w->q) || !aligned16(w->s) || (reinterpret_cast<uintptr_t>(w->g) & 3u))
+    return MOE_ERR_ALIGNMENT;
+  return MOE_OK;
+}
+
+int32_t cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return MOE_OK;
+  cudaGetLastError();
+  return MOE_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t moe_nvfp4_abi_version(void) { return MOE_NVFP4_ABI_VERSION; }
+
+const char* moe_nvfp4_status_string(int32_t code) {
+  switch (code) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_SHAPE: return "unsupported shape";
+    case MOE_ERR_ALIGNMENT: return "device pointer not 16-byte aligned";
+    case MOE_ERR_WORKSPACE: return "plan or workspace buffer too small";
+    case MOE_ERR_UNSUPPORTED_DEVICE: return "current device is not compute capability 10.3";
+    case MOE_ERR_CUDA: return "CUDA runtime or launch failure";
+    case MOE_ERR_LAYOUT: return "weights not in the required layout";
+    case (int32_t)MOE_ST_INVALID_ID: return "status: expert id out of range (pair dropped)";
+    case (int32_t)MOE_ST_NONFINITE: return "status: non-finite quantiser input";
+    case (int32_t)MOE_ST_TIMEOUT: return "status: device-side wait timed out";
+    default: return "unknown code";
+  }
+}
+
+int32_t moe_nvfp4_query(const moe_nvfp4_config* cfg, int64_t max_tokens, size_t* plan_bytes,
+                        size_t* ws_bytes) {
+  LayerDims d;
+  int32_t rc = check_cfg(cfg, &d);
+  if (rc) return rc;
+  if (max_tokens < 0 || max_tokens > kMaxTokens) return MOE_ERR_SHAPE;
+  if (!plan_bytes && !ws_bytes) return MOE_OK;
+  int sms = 0;
+  rc = current_device(&sms);
+  if (rc) return rc;
+  if (plan_bytes) *plan_bytes = plan_bytes_for(d, max_tokens);
+  if (ws_bytes) *ws_bytes = ws_bytes_for(d, max_tokens);
+  return MOE_OK;
+}
+
+int32_t moe_nvfp4_quantize(const float* w, int64_t n_mats, int64_t rows, int64_t k,
+                           int32_t layout, uint8_t* q, uint8_t* s, float* g, uint32_t* status,
+                           void* stream) {
+  if (!w || !q || !s || !g) return MOE_ERR_INVALID_ARG;
+  if (layout < MOE_LAYOUT_CANONICAL || layout > MOE_LAYOUT_FRAGMENT_W13) return MOE_ERR_LAYOUT;
+  if (n_mats < 1 || n_mats > 65535 || rows < 16 || k < 64) return MOE_ERR_SHAPE;
+  if (k % 64 || rows % 16) return MOE_ERR_SHAPE;
+  if (layout == MOE_LAYOUT_FRAGMENT_W13 && rows % 32) return MOE_ERR_SHAPE;
+  if (rows * k >= (int64_t(1) << 31)) return MOE_ERR_SHAPE;
+  if (!aligned16(w) || !aligned16(q) || !aligned16(s) || !aligned16(g)) return MOE_ERR_ALIGNMENT;
+  if (status && (reinterpret_cast<uintptr_t>(status) & 3u)) return MOE_ERR_ALIGNMENT;
+  int sms = 0;
+  int32_t rc = current_device(&sms);
+  if (rc) return rc;
+  return cuda_status(launch_quantize(w, n_mats, rows, k, layout, q, s, g, status,
+                                     static_cast<cudaStream_t>(stream), sms));
+}
+
+int32_t moe_nvfp4_dequantize(const uint8_t* q, const uint8_t* s, int64_t n_mats, int64_t rows,
+                             int64_t k, int32_t layout, void* out, void* stream) {
+  if (!q || !s || !out) return MOE_ERR_INVALID_ARG;
+  if (layout < MOE_LAYOUT_CANONICAL || layout > MOE_LAYOUT_FRAGMENT_W13) return MOE_ERR_LAYOUT;
+  if (n_mats < 1 || rows < 16 || k < 64 || k % 64 || rows % 16) return MOE_ERR_SHAPE;
+  if (layout == MOE_LAYOUT_FRAGMENT_W13 && rows % 32) return MOE_ERR_SHAPE;
+  if (n_mats * rows * k >= (int64_t(1) << 40)) return MOE_ERR_SHAPE;
+  if (!aligned16(q) || !aligned16(s) || !aligned16(out)) return MOE_ERR_ALIGNMENT;
+  int sms = 0;
+  int32_t rc = current_device(&sms);
+  if (rc) return rc;
+  return cuda_status(
+      launch_dequantize(q, s, n_mats, rows, k, layout, out, static_cast<cudaStream_t>(stream), sms));
+}
+
+int32_t moe_nvfp4_plan(const moe_nvfp4_config* cfg, int64_t M, const void* x,
+                       const void* w_router, const float* bias, const void* w_gate, int32_t* ids,
+                       float* topk_w, void* plan, size_t plan_bytes, uint32_t* status,
+                       void* stream) {
+  LayerDims d;
+  int32_t rc = check_cfg(cfg, &d);
+  if (rc) return rc;
+  if (M < 0 || M > kMaxTokens) return MOE_ERR_SHAPE;
+  const bool given = (cfg->flags & MOE_FLAG_IDS_GIVEN) != 0;
+  if (!x || !ids || !topk_w || !plan) return MOE_ERR_INVALID_ARG;
+  if (!given && !w_router) return MOE_ERR_INVALID_ARG;
+  if (d.shared && !w_gate) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(ids) || !aligned16(topk_w) || !aligned16(plan))
+    return MOE_ERR_ALIGNMENT;
+  if ((w_router && !aligned16(w_router)) || (bias && !aligned16(bias)) ||
+      (d.shared && !aligned16(w_gate)))
+    return MOE_ERR_ALIGNMENT;
+  if (status && (reinterpret_cast<uintptr_t>(status) & 3u)) return MOE_ERR_ALIGNMENT;
+  if (plan_bytes < plan_bytes_for(d, M)) return MOE_ERR_WORKSPACE;
+  if (M == 0) return MOE_OK;
+  int sms = 0;
+  rc = current_device(&sms);
+  if (rc) return rc;
+  PlanView pv;
+  plan_layout(static_cast<char*>(plan), M, d.k_eff, d.e_eff, d.E, d.H, &pv);
+  return cuda_status(launch_plan(d, M, static_cast<const __half*>(x),
+                                 static_cast<const __half*>(w_router), bias,
+                                 static_cast<const __half*>(w_gate), ids, topk_w, given, pv,
+                                 status, static_cast<cudaStream_t>(stream), sms));
+}
+
+int32_t moe_nvfp4_forward(const moe_nvfp4_config* cfg, int64_t M, const void* x, const void* plan,
+                          const moe_nvfp4_weights* w13, const moe_nvfp4_weights* w2,
+                          const moe_nvfp4_weights* shared13, const moe_nvfp4_weights* shared2,
+                          void* y, void* ws, size_t ws_bytes, uint32_t* status, void* stream) {
+  LayerDims d;
+  int32_t rc = check_cfg(cfg, &d);
+  if (rc) return rc;
+  if (M < 0 || M > kMaxTokens) return MOE_ERR_SHAPE;
+  if (!x || !plan || !y || !ws) return MOE_ERR_INVALID_ARG;
+  if ((rc = check_weights(w13, MOE_LAYOUT_FRAGMENT_W13))) return rc;
+  if ((rc = check_weights(w2, MOE_LAYOUT_FRAGMENT))) return rc;
+  if (d.shared) {
+    if ((rc = check_weights(shared13, MOE_LAYOUT_FRAGMENT_W13))) return rc;
+    if ((rc = check_weights(shared2, MOE_LAYOUT_FRAGMENT))) return rc;
+  }
+  if (!aligned16(x) || !aligned16(plan) || !aligned16(y) || !aligned16(ws))
+    return MOE_ERR_ALIGNMENT;
+  if (status && (reinterpret_cast<uintptr_t>(status) & 3u)) return MOE_ERR_ALIGNMENT;
+  if (ws_bytes < ws_bytes_for(d, M)) return MOE_ERR_WORKSPACE;
+  if (M == 0) return MOE_OK;
+  int sms = 0;
+  rc = current_device(&sms);
+  if (rc) return rc;
+  PlanView pv;
+  plan_layout(static_cast<char*>(const_cast<void*>(plan)), M, d.k_eff, d.e_eff, d.E, d.H, &pv);
+  const int64_t P = M * d.k_eff;
+  __half* h = static_cast<__half*>(ws);
+  float* partial = reinterpret_cast<float*>(static_cast<char*>(ws) +
+                                            align_up((size_t)P * d.I * sizeof(__half), 256));
+  Weights W13{w13->q, w13->s, w13->g}, W2{w2->q, w2->s, w2->g};
+  Weights S13{nullptr, nullptr, nullptr}, S2{nullptr, nullptr, nullptr};
+  if (d.shared) {
+    S13 = Weights{shared13->q, shared13->s, shared13->g};
+    S2 = Weights{shared2->q, shared2->s, shared2->g};
+  }
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (M <= kDecodeMaxTokens)
+    e = launch_decode_forward(d, M, static_cast<const __half*>(x), pv, W13, W2, S13, S2,
+                              static_cast<__half*>(y), h, partial, status, st, sms);
+  else
+    e = launch_prefill_forward(d, M, static_cast<const __half*>(x), pv, W13, W2, S13, S2,
+                               static_cast<__half*>(y), h, partial, status, st, sms);
+  return cuda_status(e);
+}
+
+}  // extern "C"

@@ -1,0 +1,379 @@
+// Decode path (M <= 16): weight-streaming, split-K GEMV kernels and the
+// fixed-order combine.
+//
+// The layer is HBM-bound here: every touched expert's NVFP4 bytes are read
+// once.  Weights are stored in the fragment layout, so each warp reads one
+// 512-byte block per 16-row x 64-element piece with a single 16-byte load per
+// thread; the thread dequantises its 32 codes in registers (exact E2M1 x E4M3
+// products in FP16) straight into mma.sync m16n8k16 A fragments, and the
+// tokens of the expert are the N = 8 / 16 columns.
+//
+// Pages: "[Kernel][SM70] Improve Qwen3.8 no-MTP concurrency", sections "Scope
+// and related PRs" (expert-grouped multi-row W13/SiLU with intra-CTA split-K;
+// grouped W2 reusing the integer plan; M2-M16 dynamic dispatch) and "Latest
+// grouped-MoE screen" (the complete C16 decode call).
+#include <math.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+
+// Dequantised A fragment of k-step `s` (0..3) of a 16x64 fragment-layout block:
+// q = {row g codes 0-7, row g codes 8-15, row g+8 codes 0-7, row g+8 codes 8-15}
+// of this thread's 16-element run; sg / sg8 the FP16 scale splats.
+__device__ __forceinline__ void a_frag(const uint4& q, uint32_t sg, uint32_t sg8, int s,
+                                       uint32_t a[4]) {
+  const uint32_t wg = (s < 2) ? q.x : q.y;
+  const uint32_t wg8 = (s < 2) ? q.z : q.w;
+  const int sh = 16 * (s & 1);
+  a[0] = hmul2_u32(e2m1x2_to_f16x2((wg >> sh) & 0xFF), sg);
+  a[2] = hmul2_u32(e2m1x2_to_f16x2((wg >> (sh + 8)) & 0xFF), sg);
+  a[1] = hmul2_u32(e2m1x2_to_f16x2((wg8 >> sh) & 0xFF), sg8);
+  a[3] = hmul2_u32(e2m1x2_to_f16x2((wg8 >> (sh + 8)) & 0xFF), sg8);
+}
+
+__device__ __forceinline__ void scale_splats(uint32_t sc16, uint32_t* sg, uint32_t* sg8) {
+  const uint32_t f = e4m3x2_to_f16x2(sc16);
+  *sg = __byte_perm(f, f, 0x1010);
+  *sg8 = __byte_perm(f, f, 0x3232);
+}
+
+__device__ __forceinline__ uint16_t ldg_u16(const uint8_t* p) {
+  return __ldg(reinterpret_cast<const unsigned short*>(p));
+}
+
+// ---------------------------------------------------------------------------
+// W13 + SwiGLU.  One block per (active expert, pair of gate/up 16-row tiles);
+// the 8 warps split K; fixed-order reduction over warps in shared memory.
+// h[pos][i] = fp16(silu(g13 * G) * (g13 * U)) for the expert's plan positions.
+// ---------------------------------------------------------------------------
+template <int NT>
+__global__ void __launch_bounds__(256) decode_w13_kernel(LayerDims d, PlanView pv,
+                                                         const __half* __restrict__ x,
+                                                         Weights w13, Weights s13,
+                                                         __half* __restrict__ h) {
+  extern __shared__ __align__(16) char xs_raw[];  // [NT*8][H*2 + 16] token rows
+  __shared__ float red[8][2][NT][32][4];
+  __shared__ int s_tok[NT * 8];
+  pdl_wait();
+  pdl_launch_dependents();
+  const int H = d.H, I = d.I;
+  const int n_rtp = I / 16;
+  const int unit = blockIdx.x;
+  const int n_active = __ldcg(&pv.hdr->n_active);
+  if (unit >= n_active * n_rtp) return;
+  const int a = unit / n_rtp, rp = unit - a * n_rtp;
+  const int e = __ldcg(pv.active + a);
+  const int count = __ldcg(pv.counts + e);
+  const int base = __ldcg(pv.offsets + e);
+  const bool sh = (e == d.E);
+  const uint8_t* qe = sh ? s13.q : w13.q + (size_t)e * I * H;
+  const uint8_t* se = sh ? s13.s : w13.s + (size_t)e * I * H / 8;
+  const float gsc = sh ? s13.g[0] : w13.g[e];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g = lane >> 2, t4 = lane & 3;
+  const int S = H / 64;
+  // gate tile 2*rp and up tile 2*rp+1 are adjacent in the W13 fragment layout
+  const uint8_t* qt = qe + (size_t)(2 * rp) * S * 512;
+  const uint8_t* st = se + (size_t)(2 * rp) * S * 64;
+  const int xstride = H * 2 + 16;
+  const int cpr = H / 8;  // 16-byte chunks per row
+
+  uint4 qv[4][2];
+  uint32_t sv[4][2];
+  // this warp's segments: ks = warp + 8 * j, in groups of 4 (32 segments)
+  auto load_group = [&](int ks0) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int ks = ks0 + 8 * j;
+      if (ks < S) {
+#pragma unroll
+        for (int tt = 0; tt < 2; ++tt) {
+          qv[j][tt] = ldg_nc_v4(qt + ((size_t)tt * S + ks) * 512 + lane * 16);
+          sv[j][tt] = ldg_u16(st + ((size_t)tt * S + ks) * 64 + lane * 2);
+        }
+      }
+    }
+  };
+
+  // rows of the expert in chunks of NT*8 (one chunk unless given ids repeat
+  // an expert within a token)
+  for (int n0 = 0; n0 < count; n0 += NT * 8) {
+    const int n_e = min(count - n0, NT * 8);
+    const int pos0 = base + n0;
+    if (tid < n_e) s_tok[tid] = __ldcg(pv.perm + pos0 + tid) / d.k_eff;
+    __syncthreads();
+    for (int i = tid; i < n_e * cpr; i += 256) {
+      const int n = i / cpr, c = i - n * cpr;
+      cp_async16(smem_u32(xs_raw + n * xstride + c * 16), x + (int64_t)s_tok[n] * H + c * 8,
+                 16u);
+    }
+    cp_async_commit();
+
+    float acc[2][NT][4];
+#pragma unroll
+    for (int t = 0; t < 2; ++t)
+#pragma unroll
+      for (int n = 0; n < NT; ++n)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) acc[t][n][c] = 0.f;
+
+    load_group(warp);
+    cp_async_wait<0>();
+    __syncthreads();  // token rows staged
+    for (int ks0 = warp; ks0 < S; ks0 += 32) {
+      if (ks0 != warp) load_group(ks0);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int ks = ks0 + 8 * j;
+        if (ks >= S) break;
+        uint32_t xw[NT][8];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          const int n = nt * 8 + g;
+          if (n < n_e) {
+            const char* src = xs_raw + n * xstride + (ks * 64 + 16 * t4) * 2;
+            const uint4 v0 = *reinterpret_cast<const uint4*>(src);
+            const uint4 v1 = *reinterpret_cast<const uint4*>(src + 16);
+            xw[nt][0] = v0.x; xw[nt][1] = v0.y; xw[nt][2] = v0.z; xw[nt][3] = v0.w;
+            xw[nt][4] = v1.x; xw[nt][5] = v1.y; xw[nt][6] = v1.z; xw[nt][7] = v1.w;
+          } else {
+#pragma unroll
+            for (int u = 0; u < 8; ++u) xw[nt][u] = 0u;
+          }
+        }
+#pragma unroll
+        for (int tt = 0; tt < 2; ++tt) {
+          uint32_t sg, sg8;
+          scale_splats(sv[j][tt], &sg, &sg8);
+#pragma unroll
+          for (int s = 0; s < 4; ++s) {
+            uint32_t af[4];
+            a_frag(qv[j][tt], sg, sg8, s, af);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+              mma_16816(acc[tt][nt], af, xw[nt][2 * s], xw[nt][2 * s + 1]);
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int tt = 0; tt < 2; ++tt)
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) red[warp][tt][nt][lane][c] = acc[tt][nt][c];
+    __syncthreads();
+    if (tid < NT * 128) {
+      const int nt = tid >> 7, ln = (tid >> 2) & 31, c = tid & 3;
+      float G = 0.f, U = 0.f;
+#pragma unroll
+      for (int w = 0; w < 8; ++w) {
+        G += red[w][0][nt][ln][c];
+        U += red[w][1][nt][ln][c];
+      }
+      // c0: (row g, col 2t4), c1: (g, 2t4+1), c2: (g+8, 2t4), c3: (g+8, 2t4+1)
+      const int row = (ln >> 2) + ((c & 2) ? 8 : 0);
+      const int n = nt * 8 + 2 * (ln & 3) + (c & 1);
+      if (n < n_e) {
+        G *= gsc;
+        U *= gsc;
+        const float hv = G / (1.f + expf(-G)) * U;
+        h[(int64_t)(pos0 + n) * I + 16 * rp + row] = __float2half_rn(hv);
+      }
+    }
+    __syncthreads();  // red / s_tok / xs reused by the next chunk
+  }
+}
+
+// ---------------------------------------------------------------------------
+// W2.  One block per (active expert, 128-row block of H); warp w owns the
+// 16-row tile w of the block over the full K = I.  Each output is scaled by
+// g2 and the pair's combine weight and written to partial[pair][H] (FP32).
+// The first weights are fetched before waiting on the W13 grid.
+// ---------------------------------------------------------------------------
+template <int NT>
+__global__ void __launch_bounds__(256) decode_w2_kernel(LayerDims d, PlanView pv,
+                                                        const __half* __restrict__ h,
+                                                        Weights w2, Weights s2,
+                                                        float* __restrict__ partial) {
+  extern __shared__ __align__(16) char hs_raw[];  // [NT*8][I*2 + 16] h rows
+  const int H = d.H, I = d.I;
+  const int nhb = H / 128;
+  const int unit = blockIdx.x;
+  const int n_active = __ldcg(&pv.hdr->n_active);
+  if (unit >= n_active * nhb) {
+    pdl_wait();
+    return;
+  }
+  const int a = unit / nhb, hb = unit - a * nhb;
+  const int e = __ldcg(pv.active + a);
+  const int count = __ldcg(pv.counts + e);
+  const int base = __ldcg(pv.offsets + e);
+  const bool sh = (e == d.E);
+  const uint8_t* qe = sh ? s2.q : w2.q + (size_t)e * H * I / 2;
+  const uint8_t* se = sh ? s2.s : w2.s + (size_t)e * H * I / 16;
+  const float gsc = sh ? s2.g[0] : w2.g[e];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g = lane >> 2, t4 = lane & 3;
+  const int S = I / 64;
+  const int rt = hb * 8 + warp;
+  const uint8_t* qt = qe + (size_t)rt * S * 512;
+  const uint8_t* st = se + (size_t)rt * S * 64;
+  const int hstride = I * 2 + 16;
+  const int cpr = I / 8;
+
+  uint4 qv[8];
+  uint32_t sv[8];
+  auto load_group = [&](int ks0) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (ks0 + j < S) {
+        qv[j] = ldg_nc_v4(qt + (size_t)(ks0 + j) * 512 + lane * 16);
+        sv[j] = ldg_u16(st + (size_t)(ks0 + j) * 64 + lane * 2);
+      }
+    }
+  };
+  load_group(0);  // weights depend only on the plan, complete before W13 ran
+  pdl_wait();
+  pdl_launch_dependents();
+
+  for (int n0 = 0; n0 < count; n0 += NT * 8) {
+    const int n_e = min(count - n0, NT * 8);
+    const int pos0 = base + n0;
+    for (int i = tid; i < n_e * cpr; i += 256) {
+      const int n = i / cpr, c = i - n * cpr;
+      cp_async16(smem_u32(hs_raw + n * hstride + c * 16), h + (int64_t)(pos0 + n) * I + c * 8,
+                 16u);
+    }
+    cp_async_commit();
+    cp_async_wait<0>();
+    __syncthreads();
+
+    float acc[NT][4];
+#pragma unroll
+    for (int n = 0; n < NT; ++n)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) acc[n][c] = 0.f;
+
+    for (int ks0 = 0; ks0 < S; ks0 += 8) {
+      if (ks0 > 0 || n0 > 0) load_group(ks0);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int ks = ks0 + j;
+        if (ks >= S) break;
+        uint32_t sg, sg8;
+        scale_splats(sv[j], &sg, &sg8);
+        uint32_t xw[NT][8];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          const int n = nt * 8 + g;
+          if (n < n_e) {
+            const char* src = hs_raw + n * hstride + (ks * 64 + 16 * t4) * 2;
+            const uint4 v0 = *reinterpret_cast<const uint4*>(src);
+            const uint4 v1 = *reinterpret_cast<const uint4*>(src + 16);
+            xw[nt][0] = v0.x; xw[nt][1] = v0.y; xw[nt][2] = v0.z; xw[nt][3] = v0.w;
+            xw[nt][4] = v1.x; xw[nt][5] = v1.y; xw[nt][6] = v1.z; xw[nt][7] = v1.w;
+          } else {
+#pragma unroll
+            for (int u = 0; u < 8; ++u) xw[nt][u] = 0u;
+          }
+        }
+#pragma unroll
+        for (int s = 0; s < 4; ++s) {
+          uint32_t af[4];
+          a_frag(qv[j], sg, sg8, s, af);
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt)
+            mma_16816(acc[nt], af, xw[nt][2 * s], xw[nt][2 * s + 1]);
+        }
+      }
+    }
+    // c0: (row g, col 2t4), c1: (g, 2t4+1), c2: (g+8, 2t4), c3: (g+8, 2t4+1)
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const int n = nt * 8 + 2 * t4 + (c & 1);
+        if (n < n_e) {
+          const int pair = __ldcg(pv.perm + pos0 + n);
+          const float wsc = gsc * __ldcg(pv.w + pair);
+          const int row = rt * 16 + g + ((c & 2) ? 8 : 0);
+          partial[(int64_t)pair * H + row] = acc[nt][c] * wsc;
+        }
+      }
+    __syncthreads();  // hs reused by the next chunk
+  }
+}
+
+// ---------------------------------------------------------------------------
+// y[t] = fp16( sum_{j < k_eff} partial[t * k_eff + j] ), slots in order; pairs
+// dropped from the plan (invalid ids) contribute nothing.
+// ---------------------------------------------------------------------------
+__global__ void combine_kernel(int M, int H, int k_eff, const int32_t* __restrict__ inv,
+                               const float* __restrict__ partial, __half* __restrict__ y) {
+  pdl_wait();
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;  // one float4 of y
+  const int64_t n4 = (int64_t)M * H / 4;
+  if (i >= n4) return;
+  const int64_t t = (i * 4) / H;
+  const int c = (int)(i * 4 - t * H);
+  float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int j = 0; j < k_eff; ++j) {
+    const int64_t pair = t * k_eff + j;
+    if (__ldcg(inv + pair) < 0) continue;
+    const float4 v = __ldcs(reinterpret_cast<const float4*>(partial + pair * H + c));
+    s.x += v.x;
+    s.y += v.y;
+    s.z += v.z;
+    s.w += v.w;
+  }
+  __half2 lo = __floats2half2_rn(s.x, s.y), hi = __floats2half2_rn(s.z, s.w);
+  uint2 out;
+  out.x = *reinterpret_cast<uint32_t*>(&lo);
+  out.y = *reinterpret_cast<uint32_t*>(&hi);
+  *reinterpret_cast<uint2*>(y + t * H + c) = out;
+}
+
+cudaError_t launch_combine(const LayerDims& d, int64_t M, const PlanView& pv,
+                           const float* partial, __half* y, cudaStream_t stream, bool pdl) {
+  const int64_t n4 = M * d.H / 4;
+  const unsigned blocks = (unsigned)((n4 + 255) / 256);
+  return launch_k(combine_kernel, dim3(blocks), dim3(256), 0, stream, pdl, (int)M, d.H, d.k_eff,
+                  (const int32_t*)pv.inv, partial, y);
+}
+
+template <int NT>
+static cudaError_t decode_impl(const LayerDims& d, int64_t M, const __half* x, const PlanView& pv,
+                               Weights w13, Weights w2, Weights s13, Weights s2, __half* y,
+                               __half* h, float* partial, cudaStream_t stream) {
+  const int max_active = (int)((M * d.k_eff < d.e_eff) ? M * d.k_eff : d.e_eff);
+  const size_t xs_smem = (size_t)NT * 8 * (d.H * 2 + 16);
+  cudaError_t e = cudaFuncSetAttribute(decode_w13_kernel<NT>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)xs_smem);
+  if (e != cudaSuccess) return e;
+  e = launch_k(decode_w13_kernel<NT>, dim3(max_active * (d.I / 16)), dim3(256), xs_smem, stream,
+               true, d, pv, x, w13, s13, h);
+  if (e != cudaSuccess) return e;
+  const size_t hs_smem = (size_t)NT * 8 * (d.I * 2 + 16);
+  e = cudaFuncSetAttribute(decode_w2_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)hs_smem);
+  if (e != cudaSuccess) return e;
+  e = launch_k(decode_w2_kernel<NT>, dim3(max_active * (d.H / 128)), dim3(256), hs_smem, stream,
+               true, d, pv, (const __half*)h, w2, s2, partial);
+  if (e != cudaSuccess) return e;
+  return launch_combine(d, M, pv, partial, y, stream, true);
+}
+
+cudaError_t launch_decode_forward(const LayerDims& d, int64_t M, const __half* x,
+                                  const PlanView& pv, Weights w13, Weights w2, Weights s13,
+                                  Weights s2, __half* y, __half* h, float* partial,
+                                  uint32_t* status, cudaStream_t stream, int num_sms) {
+  (void)status;
+  (void)num_sms;
+  if (M <= 8) return decode_impl<1>(d, M, x, pv, w13, w2, s13, s2, y, h, partial, stream);
+  return decode_impl<2>(d, M, x, pv, w13, w2, s13, s2, y, h, partial, stream);
+}
+
+}  // namespace moe

@@ -1,0 +1,65 @@
+// Host-side launcher declarations shared by the C-ABI layer (api.cu) and the
+// kernel translation units.  Launchers assume validated arguments.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace moe {
+
+struct LayerDims {
+  int H, E, k, I;
+  int k_eff, e_eff;  // with the shared expert folded in as slot k / expert E
+  bool shared;
+};
+
+struct Weights {
+  const uint8_t* q;
+  const uint8_t* s;
+  const float* g;
+};
+
+cudaError_t launch_quantize(const float* w, int64_t n_mats, int64_t rows, int64_t k, int layout,
+                            uint8_t* q, uint8_t* s, float* g, uint32_t* status,
+                            cudaStream_t stream, int num_sms);
+cudaError_t launch_dequantize(const uint8_t* q, const uint8_t* s, int64_t n_mats, int64_t rows,
+                              int64_t k, int layout, void* out, cudaStream_t stream, int num_sms);
+
+// Router + plan.  ids_user / w_user are outputs unless ids_given.
+cudaError_t launch_plan(const LayerDims& d, int64_t M, const __half* x, const __half* w_router,
+                        const float* bias, const __half* w_gate, int32_t* ids_user,
+                        float* w_user, bool ids_given, const PlanView& pv, uint32_t* status,
+                        cudaStream_t stream, int num_sms);
+
+// Forward paths.  partial: FP32 [M * k_eff][H]; h: FP16 [M * k_eff][I].
+cudaError_t launch_decode_forward(const LayerDims& d, int64_t M, const __half* x,
+                                  const PlanView& pv, Weights w13, Weights w2, Weights s13,
+                                  Weights s2, __half* y, __half* h, float* partial,
+                                  uint32_t* status, cudaStream_t stream, int num_sms);
+cudaError_t launch_prefill_forward(const LayerDims& d, int64_t M, const __half* x,
+                                   const PlanView& pv, Weights w13, Weights w2, Weights s13,
+                                   Weights s2, __half* y, __half* h, float* partial,
+                                   uint32_t* status, cudaStream_t stream, int num_sms);
+cudaError_t launch_combine(const LayerDims& d, int64_t M, const PlanView& pv,
+                           const float* partial, __half* y, cudaStream_t stream, bool pdl);
+
+// Launch helper: programmatic dependent launch when `pdl` is set.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                     cudaStream_t stream, bool pdl, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
+}  // namespace moe

@@ -1,0 +1,676 @@
+// Router (FP32 logits, top-k, renormalised softmax weights, shared-expert
+// gate) and the integer routing plan (per-expert histogram, prefix scan,
+// stable permutation, inverse, tile schedule).
+//
+// "[Kernel][SM70] Improve Qwen3.8 no-MTP concurrency", section "Scope and
+// related PRs": the router is batched, and one integer plan is built once and
+// reused by grouped W13 and grouped W2 ("avoids repeated planning").
+//
+// Two shapes:
+//  * M <= 16 (decode): one kernel.  Blocks own (64-expert slice, 256-row
+//    chunk of H) and stream W_r once; arrival tickets make the last block of
+//    each slice reduce the chunk partials in a fixed order, and the last slice
+//    finaliser runs top-k, the weights, the gate and the whole plan.
+//  * M > 16 (prefill): a 64-token x all-experts mma.sync GEMM with the top-k
+//    in its epilogue, then a three-kernel stable counting sort.
+#include <math.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+
+constexpr int kMaxEEff = 520;  // >= 512 routed experts + the shared expert
+
+// A pair's expert id is valid if it names a routed expert in a routed slot,
+// or the shared expert in the shared slot.
+__device__ __forceinline__ bool pair_valid(int e, int slot, const LayerDims& d) {
+  return slot < d.k ? (e >= 0 && e < d.E) : (e == d.E);
+}
+
+// ---------------------------------------------------------------------------
+// Warp top-k over a row of E logits.  Lane j < k receives slot j: the j-th
+// largest logit, ties broken towards the lower expert id.  E <= 512.
+// ---------------------------------------------------------------------------
+template <bool kGlobal>
+__device__ __forceinline__ void warp_topk(const float* row, int E, int k, int* out_id,
+                                          float* out_l) {
+  const int lane = threadIdx.x & 31;
+  float v[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const int e = lane + 32 * i;
+    v[i] = (e < E) ? (kGlobal ? __ldcg(row + e) : row[e]) : -INFINITY;
+  }
+  int my_id = -1;
+  float my_l = -INFINITY;
+  for (int j = 0; j < k; ++j) {
+    float bv = v[0];
+    int bi = lane;
+#pragma unroll
+    for (int i = 1; i < 16; ++i)
+      if (v[i] > bv) {
+        bv = v[i];
+        bi = lane + 32 * i;
+      }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+      if (ov > bv || (ov == bv && oi < bi)) {
+        bv = ov;
+        bi = oi;
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      if (lane + 32 * i == bi) v[i] = -INFINITY;
+    if (lane == j) {
+      my_id = bi;
+      my_l = bv;
+    }
+  }
+  *out_id = my_id;
+  *out_l = my_l;
+}
+
+// softmax of the k selected logits held by lanes 0..k-1 (lane 0 holds the max)
+__device__ __forceinline__ float warp_topk_weight(float my_l, int k) {
+  const int lane = threadIdx.x & 31;
+  const float lmax = __shfl_sync(0xffffffffu, my_l, 0);
+  const float e = (lane < k) ? expf(my_l - lmax) : 0.f;
+  float s = e;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  return e / s;
+}
+
+// gamma = sigmoid(x . w_g), one warp, x and w_g FP16 of length H (H % 64 == 0)
+__device__ __forceinline__ float warp_gate(const __half* xr, const __half* wg, int H) {
+  const int lane = threadIdx.x & 31;
+  float z = 0.f;
+  for (int c = 2 * lane; c < H; c += 64) {
+    const float2 a = __half22float2(*reinterpret_cast<const __half2*>(xr + c));
+    const float2 b = __half22float2(*reinterpret_cast<const __half2*>(wg + c));
+    z = fmaf(a.x, b.x, z);
+    z = fmaf(a.y, b.y, z);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+  return 1.f / (1.f + expf(-z));
+}
+
+// Writes slot values of token t (lanes < k), plus the shared slot.
+__device__ __forceinline__ void store_route(const LayerDims& d, int t, int id, float w,
+                                            float gamma, int32_t* ids_user, float* w_user,
+                                            const PlanView& pv) {
+  const int lane = threadIdx.x & 31;
+  if (lane < d.k) {
+    ids_user[(int64_t)t * d.k + lane] = id;
+    w_user[(int64_t)t * d.k + lane] = w;
+    pv.ids[(int64_t)t * d.k_eff + lane] = id;
+    pv.w[(int64_t)t * d.k_eff + lane] = w;
+  }
+  if (d.shared && lane == 0) {
+    pv.ids[(int64_t)t * d.k_eff + d.k] = d.E;
+    pv.w[(int64_t)t * d.k_eff + d.k] = gamma;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Plan of up to kDecodeMaxTokens * (32 + 1) pairs by one block of 256 threads.
+// ---------------------------------------------------------------------------
+__device__ void plan_small_block(const LayerDims& d, int M, const PlanView& pv,
+                                 uint32_t* status) {
+  __shared__ int s_ids[kDecodeMaxTokens * 33];
+  __shared__ int s_cnt[kMaxEEff];
+  __shared__ int s_off[kMaxEEff];
+  __shared__ int s_tb[kMaxEEff];
+  __shared__ int s_tot[3];
+  const int tid = threadIdx.x, nthr = blockDim.x;
+  const int P = M * d.k_eff;
+  for (int i = tid; i < d.e_eff; i += nthr) s_cnt[i] = 0;
+  __syncthreads();
+  bool bad = false;
+  for (int p = tid; p < P; p += nthr) {
+    const int e = pv.ids[p];
+    const bool ok = pair_valid(e, p % d.k_eff, d);
+    s_ids[p] = ok ? e : -1;
+    if (ok)
+      atomicAdd(&s_cnt[e], 1);
+    else
+      bad = true;
+  }
+  if (bad) set_status(status, MOE_ST_INVALID_ID);
+  __syncthreads();
+  if (tid < 32) {
+    const int lane = tid, n = d.e_eff;
+    const int per = (n + 31) / 32, b = lane * per, end = min(b + per, n);
+    int cs = 0, as = 0, ts = 0;
+    for (int i = b; i < end; ++i) {
+      const int c = s_cnt[i];
+      cs += c;
+      as += c > 0;
+      ts += (c + kTileRows - 1) / kTileRows;
+    }
+    int ci = cs, ai = as, ti = ts;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int a1 = __shfl_up_sync(0xffffffffu, ci, o);
+      const int a2 = __shfl_up_sync(0xffffffffu, ai, o);
+      const int a3 = __shfl_up_sync(0xffffffffu, ti, o);
+      if (lane >= o) {
+        ci += a1;
+        ai += a2;
+        ti += a3;
+      }
+    }
+    if (lane == 31) {
+      s_tot[0] = ci;
+      s_tot[1] = ai;
+      s_tot[2] = ti;
+    }
+    ci -= cs;
+    ai -= as;
+    ti -= ts;
+    for (int i = b; i < end; ++i) {
+      const int c = s_cnt[i];
+      s_off[i] = ci;
+      s_tb[i] = ti;
+      pv.counts[i] = c;
+      pv.offsets[i] = ci;
+      if (c > 0) pv.active[ai] = i;
+      ci += c;
+      ai += c > 0;
+      ti += (c + kTileRows - 1) / kTileRows;
+    }
+  }
+  __syncthreads();
+  if (tid == 0) {
+    pv.offsets[d.e_eff] = s_tot[0];
+    pv.hdr->M = M;
+    pv.hdr->k_eff = d.k_eff;
+    pv.hdr->e_eff = d.e_eff;
+    pv.hdr->n_valid = s_tot[0];
+    pv.hdr->n_active = s_tot[1];
+    pv.hdr->n_tiles = s_tot[2];
+  }
+  for (int p = tid; p < P; p += nthr) {
+    const int e = s_ids[p];
+    if (e < 0) {
+      pv.inv[p] = -1;
+      continue;
+    }
+    int r = 0;
+    for (int q = 0; q < p; ++q) r += (s_ids[q] == e);
+    const int pos = s_off[e] + r;
+    pv.perm[pos] = p;
+    pv.inv[p] = pos;
+  }
+  for (int e = tid; e < d.e_eff; e += nthr) {
+    const int c = s_cnt[e];
+    int t = s_tb[e];
+    for (int r0 = 0; r0 < c; r0 += kTileRows, ++t) {
+      int4 tl = make_int4(e, r0, min(kTileRows, c - r0), 0);
+      reinterpret_cast<int4*>(pv.tiles)[t] = tl;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Small-M router + plan (one launch).
+// grid = (ceil(E / 64), ceil(H / 256)), block = 256.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) router_small_kernel(LayerDims d, int M,
+                                                           const __half* __restrict__ x,
+                                                           const __half* __restrict__ wr,
+                                                           const float* __restrict__ bias,
+                                                           const __half* __restrict__ wg,
+                                                           int32_t* ids_user, float* w_user,
+                                                           PlanView pv, uint32_t* status) {
+  __shared__ float xs[kDecodeMaxTokens][256];
+  __shared__ float red[8][kDecodeMaxTokens][64];
+  __shared__ int is_last;
+  const int s = blockIdx.x, hc = blockIdx.y;
+  const int E = d.E, H = d.H;
+  const int h0 = hc * 256, hn = min(256, H - h0);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  for (int i = tid; i < kDecodeMaxTokens * 256; i += 256) {
+    const int m = i >> 8, c = i & 255;
+    xs[m][c] = (m < M && c < hn) ? __half2float(x[(int64_t)m * H + h0 + c]) : 0.f;
+  }
+  const int e0 = s * 64 + 2 * lane;
+  const bool ev = e0 < E;
+  __half2 wv[32];
+#pragma unroll
+  for (int r = 0; r < 32; ++r) {
+    const int hr = warp * 32 + r;
+    wv[r] = (ev && hr < hn)
+                ? *reinterpret_cast<const __half2*>(wr + (int64_t)(h0 + hr) * E + e0)
+                : __float2half2_rn(0.f);
+  }
+  __syncthreads();
+  float acc[kDecodeMaxTokens][2];
+#pragma unroll
+  for (int m = 0; m < kDecodeMaxTokens; ++m) acc[m][0] = acc[m][1] = 0.f;
+#pragma unroll
+  for (int r = 0; r < 32; ++r) {
+    const float2 f = __half22float2(wv[r]);
+#pragma unroll
+    for (int m = 0; m < kDecodeMaxTokens; ++m) {
+      if (m < M) {
+        const float xv = xs[m][warp * 32 + r];
+        acc[m][0] = fmaf(xv, f.x, acc[m][0]);
+        acc[m][1] = fmaf(xv, f.y, acc[m][1]);
+      }
+    }
+  }
+#pragma unroll
+  for (int m = 0; m < kDecodeMaxTokens; ++m) {
+    if (m < M) {
+      red[warp][m][2 * lane] = acc[m][0];
+      red[warp][m][2 * lane + 1] = acc[m][1];
+    }
+  }
+  __syncthreads();
+  for (int i = tid; i < M * 64; i += 256) {
+    const int m = i >> 6, c = i & 63, e = s * 64 + c;
+    float t = 0.f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) t += red[w][m][c];
+    if (e < E) pv.partial[((int64_t)hc * kDecodeMaxTokens + m) * E + e] = t;
+  }
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) {
+    const unsigned t = atomicAdd(&pv.tickets[s], 1u);
+    is_last = (t == gridDim.y - 1);
+    if (is_last) pv.tickets[s] = 0u;
+  }
+  __syncthreads();
+  if (!is_last) return;
+  __threadfence();
+  // slice finaliser: fixed-order sum over H chunks, + bias
+  for (int i = tid; i < M * 64; i += 256) {
+    const int m = i >> 6, c = i & 63, e = s * 64 + c;
+    if (e >= E) continue;
+    float t = 0.f;
+    for (int q = 0; q < (int)gridDim.y; ++q)
+      t += __ldcg(pv.partial + ((int64_t)q * kDecodeMaxTokens + m) * E + e);
+    if (bias) t += bias[e];
+    pv.logits[(int64_t)m * E + e] = t;
+  }
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) {
+    const unsigned t = atomicAdd(&pv.tickets[63], 1u);
+    is_last = (t == gridDim.x - 1);
+    if (is_last) pv.tickets[63] = 0u;
+  }
+  __syncthreads();
+  if (!is_last) return;
+  __threadfence();
+  for (int m = warp; m < M; m += 8) {
+    int id;
+    float l;
+    warp_topk<true>(pv.logits + (int64_t)m * E, E, d.k, &id, &l);
+    const float w = warp_topk_weight(l, d.k);
+    const float gamma = d.shared ? warp_gate(x + (int64_t)m * H, wg, H) : 0.f;
+    store_route(d, m, id, w, gamma, ids_user, w_user, pv);
+  }
+  __syncthreads();
+  plan_small_block(d, M, pv, status);
+}
+
+// Caller-given ids and weights: copy into the plan (plus the shared slot).
+// grid = ceil(M / 8), block = 256 (one warp per token).
+__global__ void route_given_kernel(LayerDims d, int M, const __half* __restrict__ x,
+                                   const __half* __restrict__ wg, const int32_t* ids_user,
+                                   const float* w_user, PlanView pv) {
+  const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (t >= M) return;
+  if (lane < d.k) {
+    pv.ids[(int64_t)t * d.k_eff + lane] = ids_user[(int64_t)t * d.k + lane];
+    pv.w[(int64_t)t * d.k_eff + lane] = w_user[(int64_t)t * d.k + lane];
+  }
+  if (d.shared) {
+    const float gamma = warp_gate(x + (int64_t)t * d.H, wg, d.H);
+    if (lane == 0) {
+      pv.ids[(int64_t)t * d.k_eff + d.k] = d.E;
+      pv.w[(int64_t)t * d.k_eff + d.k] = gamma;
+    }
+  }
+}
+
+__global__ void __launch_bounds__(256) plan_small_kernel(LayerDims d, int M, PlanView pv,
+                                                         uint32_t* status) {
+  plan_small_block(d, M, pv, status);
+}
+
+// ---------------------------------------------------------------------------
+// Large-M router: 64 tokens x all experts per block, mma.sync m16n8k16 with
+// FP32 accumulation, top-k in the epilogue.  block = 512 (16 warps: 2 token
+// halves x 8 groups of 64 experts).
+// ---------------------------------------------------------------------------
+constexpr int kRtTok = 64;
+constexpr int kRtK = 32;
+
+__device__ __forceinline__ void ldsm_x4(uint32_t r[4], const void* p) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(smem_u32(p)));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t r[4], const void* p) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(smem_u32(p)));
+}
+
+size_t router_mma_smem(int E) {
+  const int Ep = (E + 63) / 64 * 64;
+  const size_t pipe = 2 * (size_t)(kRtTok * (kRtK + 8) + kRtK * (Ep + 8)) * sizeof(__half);
+  const size_t logits = (size_t)kRtTok * (Ep + 1) * sizeof(float);
+  return pipe > logits ? pipe : logits;
+}
+
+__global__ void __launch_bounds__(512) router_mma_kernel(LayerDims d, int M,
+                                                         const __half* __restrict__ x,
+                                                         const __half* __restrict__ wr,
+                                                         const float* __restrict__ bias,
+                                                         const __half* __restrict__ wg,
+                                                         int32_t* ids_user, float* w_user,
+                                                         PlanView pv) {
+  extern __shared__ __align__(16) char smem[];
+  const int E = d.E, H = d.H;
+  const int Ep = (E + 63) / 64 * 64;
+  const int xst = kRtK + 8, wst = Ep + 8, lst = Ep + 1;
+  __half* xs = reinterpret_cast<__half*>(smem);
+  __half* ws = xs + 2 * kRtTok * xst;
+  float* ls = reinterpret_cast<float*>(smem);
+  const int t0 = blockIdx.x * kRtTok;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int tg = warp >> 3, eg = warp & 7;
+  const int cpr = Ep / 8;
+
+  auto load_stage = [&](int st, int kk) {
+    for (int i = tid; i < kRtTok * 4; i += 512) {
+      const int r = i >> 2, c = i & 3, t = t0 + r;
+      const __half* src = x + (int64_t)(t < M ? t : 0) * H + kk + c * 8;
+      cp_async16(smem_u32(xs + (st * kRtTok + r) * xst + c * 8), src, t < M ? 16u : 0u);
+    }
+    for (int i = tid; i < kRtK * cpr; i += 512) {
+      const int r = i / cpr, c = i - r * cpr;
+      const bool in = c * 8 < E;
+      const __half* src = wr + (int64_t)(kk + r) * E + (in ? c * 8 : 0);
+      cp_async16(smem_u32(ws + (st * kRtK + r) * wst + c * 8), src, in ? 16u : 0u);
+    }
+  };
+
+  float acc[2][8][4];
+#pragma unroll
+  for (int a = 0; a < 2; ++a)
+#pragma unroll
+    for (int b = 0; b < 8; ++b)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) acc[a][b][c] = 0.f;
+
+  const int nk = H / kRtK;
+  load_stage(0, 0);
+  cp_async_commit();
+  for (int it = 0; it < nk; ++it) {
+    if (it + 1 < nk) load_stage((it + 1) & 1, (it + 1) * kRtK);
+    cp_async_commit();
+    cp_async_wait<1>();
+    __syncthreads();
+    const int st = it & 1;
+    if (eg * 64 < E) {
+#pragma unroll
+      for (int k16 = 0; k16 < 2; ++k16) {
+        uint32_t a[2][4];
+#pragma unroll
+        for (int mi = 0; mi < 2; ++mi)
+          ldsm_x4(a[mi], xs + (st * kRtTok + tg * 32 + mi * 16 + (lane & 15)) * xst + k16 * 16 +
+                             (lane >> 4) * 8);
+#pragma unroll
+        for (int nj = 0; nj < 4; ++nj) {
+          const int n0 = eg * 64 + nj * 16;
+          uint32_t b[4];
+          ldsm_x4_t(b, ws + (st * kRtK + k16 * 16 + (lane & 7) + ((lane >> 3) & 1) * 8) * wst +
+                           n0 + (lane >> 4) * 8);
+#pragma unroll
+          for (int mi = 0; mi < 2; ++mi) {
+            mma_16816(acc[mi][2 * nj], a[mi], b[0], b[1]);
+            mma_16816(acc[mi][2 * nj + 1], a[mi], b[2], b[3]);
+          }
+        }
+      }
+    }
+    __syncthreads();
+  }
+  // logits -> shared memory (the pipeline buffers are dead now)
+  const int g = lane >> 2, t4 = lane & 3;
+  if (eg * 64 < E) {
+#pragma unroll
+    for (int mi = 0; mi < 2; ++mi)
+#pragma unroll
+      for (int nt = 0; nt < 8; ++nt) {
+        const int e = eg * 64 + nt * 8 + 2 * t4;
+        const int r = tg * 32 + mi * 16 + g;
+        if (e < E) {
+          const float b0 = bias ? bias[e] : 0.f, b1 = bias ? bias[e + 1] : 0.f;
+          ls[r * lst + e] = acc[mi][nt][0] + b0;
+          ls[r * lst + e + 1] = acc[mi][nt][1] + b1;
+          ls[(r + 8) * lst + e] = acc[mi][nt][2] + b0;
+          ls[(r + 8) * lst + e + 1] = acc[mi][nt][3] + b1;
+        }
+      }
+  }
+  __syncthreads();
+  for (int r = warp; r < kRtTok; r += 16) {
+    const int t = t0 + r;
+    if (t >= M) break;
+    int id;
+    float l;
+    warp_topk<false>(ls + r * lst, E, d.k, &id, &l);
+    const float w = warp_topk_weight(l, d.k);
+    const float gamma = d.shared ? warp_gate(x + (int64_t)t * H, wg, H) : 0.f;
+    store_route(d, t, id, w, gamma, ids_user, w_user, pv);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Large-M plan: stable counting sort in three kernels.
+// ---------------------------------------------------------------------------
+// 1. Per chunk of kPlanChunk pairs: per-expert counts and each pair's rank
+//    among the earlier pairs of its expert inside the chunk.  block = 1024.
+__global__ void __launch_bounds__(1024) plan_hist_kernel(LayerDims d, int64_t P, PlanView pv,
+                                                         uint32_t* status) {
+  extern __shared__ uint16_t wcnt[];  // [32 warps][e_eff]: counts, then exclusive prefixes
+  __shared__ int run[kMaxEEff];       // count of each expert in earlier sub-chunks
+  __shared__ int subtot[kMaxEEff];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int ne = d.e_eff;
+  for (int i = tid; i < ne; i += 1024) run[i] = 0;
+  bool bad = false;
+  const int64_t base = (int64_t)blockIdx.x * kPlanChunk;
+  for (int sub = 0; sub < kPlanChunk / 1024; ++sub) {
+    for (int i = tid; i < 32 * ne; i += 1024) wcnt[i] = 0;
+    __syncthreads();
+    const int64_t p = base + sub * 1024 + tid;
+    int e = -1;
+    if (p < P) {
+      e = pv.ids[p];
+      if (!pair_valid(e, (int)(p % d.k_eff), d)) {
+        e = -1;
+        bad = true;
+      }
+    }
+    const unsigned mask = __match_any_sync(0xffffffffu, e);
+    const unsigned lt = mask & ((1u << lane) - 1u);
+    if (e >= 0 && lt == 0) wcnt[warp * ne + e] = (uint16_t)__popc(mask);
+    __syncthreads();
+    for (int ee = tid; ee < ne; ee += 1024) {
+      int r = 0;
+      for (int w = 0; w < 32; ++w) {
+        const int c = wcnt[w * ne + ee];
+        wcnt[w * ne + ee] = (uint16_t)r;
+        r += c;
+      }
+      subtot[ee] = r;
+    }
+    __syncthreads();
+    if (p < P) pv.rank[p] = (e >= 0) ? run[e] + (int)wcnt[warp * ne + e] + __popc(lt) : -1;
+    __syncthreads();
+    for (int ee = tid; ee < ne; ee += 1024) run[ee] += subtot[ee];
+    __syncthreads();
+  }
+  if (bad) set_status(status, MOE_ST_INVALID_ID);
+  for (int ee = tid; ee < ne; ee += 1024) pv.chunk_hist[(int64_t)blockIdx.x * ne + ee] = run[ee];
+}
+
+// 2. One block: per-expert prefix over chunks, expert offsets, active list,
+//    tile schedule and header.  block = 1024.
+__global__ void __launch_bounds__(1024) plan_scan_kernel(LayerDims d, int M, int n_chunks,
+                                                         PlanView pv) {
+  __shared__ int s_cnt[kMaxEEff];
+  __shared__ int s_tb[kMaxEEff];
+  __shared__ int s_tot[3];
+  const int tid = threadIdx.x, ne = d.e_eff;
+  for (int e = tid; e < ne; e += 1024) {
+    int r = 0;
+    int c = 0;
+    for (; c + 8 <= n_chunks; c += 8) {
+      int h[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) h[u] = pv.chunk_hist[(int64_t)(c + u) * ne + e];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        pv.chunk_hist[(int64_t)(c + u) * ne + e] = r;
+        r += h[u];
+      }
+    }
+    for (; c < n_chunks; ++c) {
+      const int h = pv.chunk_hist[(int64_t)c * ne + e];
+      pv.chunk_hist[(int64_t)c * ne + e] = r;
+      r += h;
+    }
+    s_cnt[e] = r;
+  }
+  __syncthreads();
+  if (tid < 32) {
+    const int lane = tid;
+    const int per = (ne + 31) / 32, b = lane * per, end = min(b + per, ne);
+    int cs = 0, as = 0, ts = 0;
+    for (int i = b; i < end; ++i) {
+      const int c = s_cnt[i];
+      cs += c;
+      as += c > 0;
+      ts += (c + kTileRows - 1) / kTileRows;
+    }
+    int ci = cs, ai = as, ti = ts;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int a1 = __shfl_up_sync(0xffffffffu, ci, o);
+      const int a2 = __shfl_up_sync(0xffffffffu, ai, o);
+      const int a3 = __shfl_up_sync(0xffffffffu, ti, o);
+      if (lane >= o) {
+        ci += a1;
+        ai += a2;
+        ti += a3;
+      }
+    }
+    if (lane == 31) {
+      s_tot[0] = ci;
+      s_tot[1] = ai;
+      s_tot[2] = ti;
+    }
+    ci -= cs;
+    ai -= as;
+    ti -= ts;
+    for (int i = b; i < end; ++i) {
+      const int c = s_cnt[i];
+      s_tb[i] = ti;
+      pv.counts[i] = c;
+      pv.offsets[i] = ci;
+      if (c > 0) pv.active[ai] = i;
+      ci += c;
+      ai += c > 0;
+      ti += (c + kTileRows - 1) / kTileRows;
+    }
+  }
+  __syncthreads();
+  if (tid == 0) {
+    pv.offsets[ne] = s_tot[0];
+    pv.hdr->M = M;
+    pv.hdr->k_eff = d.k_eff;
+    pv.hdr->e_eff = ne;
+    pv.hdr->n_valid = s_tot[0];
+    pv.hdr->n_active = s_tot[1];
+    pv.hdr->n_tiles = s_tot[2];
+  }
+  for (int e = tid; e < ne; e += 1024) {
+    const int c = s_cnt[e];
+    int t = s_tb[e];
+    for (int r0 = 0; r0 < c; r0 += kTileRows, ++t)
+      reinterpret_cast<int4*>(pv.tiles)[t] = make_int4(e, r0, min(kTileRows, c - r0), 0);
+  }
+}
+
+// 3. Positions: offset of the expert + rank over earlier chunks + rank in chunk.
+__global__ void plan_scatter_kernel(LayerDims d, int64_t P, PlanView pv) {
+  const int64_t p = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (p >= P) return;
+  const int r = pv.rank[p];
+  if (r < 0) {
+    pv.inv[p] = -1;
+    return;
+  }
+  const int e = pv.ids[p];
+  const int64_t c = p / kPlanChunk;
+  const int pos = pv.offsets[e] + pv.chunk_hist[c * d.e_eff + e] + r;
+  pv.perm[pos] = (int)p;
+  pv.inv[p] = pos;
+}
+
+// ---------------------------------------------------------------------------
+cudaError_t launch_plan(const LayerDims& d, int64_t M, const __half* x, const __half* w_router,
+                        const float* bias, const __half* w_gate, int32_t* ids_user,
+                        float* w_user, bool ids_given, const PlanView& pv, uint32_t* status,
+                        cudaStream_t stream, int num_sms) {
+  (void)num_sms;
+  const int Mi = (int)M;
+  if (M <= kDecodeMaxTokens) {
+    if (ids_given) {
+      route_given_kernel<<<(Mi + 7) / 8, 256, 0, stream>>>(d, Mi, x, w_gate, ids_user, w_user, pv);
+      plan_small_kernel<<<1, 256, 0, stream>>>(d, Mi, pv, status);
+    } else {
+      dim3 grid((d.E + 63) / 64, (d.H + 255) / 256);
+      router_small_kernel<<<grid, 256, 0, stream>>>(d, Mi, x, w_router, bias, w_gate, ids_user,
+                                                     w_user, pv, status);
+    }
+    return cudaGetLastError();
+  }
+  if (ids_given) {
+    route_given_kernel<<<(Mi + 7) / 8, 256, 0, stream>>>(d, Mi, x, w_gate, ids_user, w_user, pv);
+  } else {
+    const size_t smem = router_mma_smem(d.E);
+    cudaError_t e = cudaFuncSetAttribute(router_mma_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    router_mma_kernel<<<(Mi + kRtTok - 1) / kRtTok, 512, smem, stream>>>(
+        d, Mi, x, w_router, bias, w_gate, ids_user, w_user, pv);
+  }
+  const int64_t P = M * d.k_eff;
+  const int n_chunks = (int)((P + kPlanChunk - 1) / kPlanChunk);
+  const size_t hsmem = sizeof(uint16_t) * 32 * d.e_eff;
+  cudaError_t e = cudaFuncSetAttribute(plan_hist_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)hsmem);
+  if (e != cudaSuccess) return e;
+  plan_hist_kernel<<<n_chunks, 1024, hsmem, stream>>>(d, P, pv, status);
+  plan_scan_kernel<<<1, 1024, 0, stream>>>(d, Mi, n_chunks, pv);
+  plan_scatter_kernel<<<(unsigned)((P + 255) / 256), 256, 0, stream>>>(d, P, pv);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,268 @@
+"""Python binding of ``libmoe_nvfp4.so`` (C ABI in ``include/moe_nvfp4.h``).
+
+Argument marshalling only: torch supplies device memory and the current CUDA
+stream; every step of the layer runs in the library's CUDA kernels.  There is
+no CPU or PyTorch fallback: if the library is missing or its ABI version
+differs, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmoe_nvfp4.so")
+ABI_VERSION = 1
+
+OK = 0
+ERR = {
+    -1: "MOE_ERR_INVALID_ARG", -2: "MOE_ERR_SHAPE", -3: "MOE_ERR_ALIGNMENT",
+    -4: "MOE_ERR_WORKSPACE", -5: "MOE_ERR_UNSUPPORTED_DEVICE", -6: "MOE_ERR_CUDA",
+    -7: "MOE_ERR_LAYOUT",
+}
+ST_INVALID_ID = 0x1
+ST_NONFINITE = 0x2
+ST_TIMEOUT = 0x4
+FLAG_IDS_GIVEN = 0x1
+FLAG_SHARED = 0x2
+LAYOUT_CANONICAL = 0
+LAYOUT_FRAGMENT = 1
+LAYOUT_FRAGMENT_W13 = 2
+DECODE_MAX_TOKENS = 16
+
+EXPORTS = ["moe_nvfp4_abi_version", "moe_nvfp4_status_string", "moe_nvfp4_query",
+           "moe_nvfp4_quantize", "moe_nvfp4_plan", "moe_nvfp4_forward", "moe_nvfp4_dequantize"]
+
+
+class Config(ctypes.Structure):
+    _fields_ = [("hidden", ctypes.c_int32), ("n_experts", ctypes.c_int32),
+                ("top_k", ctypes.c_int32), ("intermediate", ctypes.c_int32),
+                ("flags", ctypes.c_uint32), ("reserved", ctypes.c_int32 * 3)]
+
+
+class WeightsC(ctypes.Structure):
+    _fields_ = [("q", ctypes.c_void_p), ("s", ctypes.c_void_p), ("g", ctypes.c_void_p),
+                ("layout", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+
+
+class MoEError(RuntimeError):
+    def __init__(self, fn, code):
+        self.code = code
+        super().__init__(f"{fn} failed: {ERR.get(code, code)} ({status_string(code)})")
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def load_library(path: str = LIB_PATH):
+    """Opens the CUDA library (once) and checks its ABI version."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(path):
+            raise RuntimeError(f"CUDA library {path} is missing: run __graft_entry__.build()")
+        lib = ctypes.CDLL(path)
+        P, I32, I64, SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+        lib.moe_nvfp4_abi_version.argtypes = []
+        lib.moe_nvfp4_abi_version.restype = I32
+        lib.moe_nvfp4_status_string.argtypes = [I32]
+        lib.moe_nvfp4_status_string.restype = ctypes.c_char_p
+        lib.moe_nvfp4_query.argtypes = [P, I64, ctypes.POINTER(SZ), ctypes.POINTER(SZ)]
+        lib.moe_nvfp4_query.restype = I32
+        lib.moe_nvfp4_quantize.argtypes = [P, I64, I64, I64, I32, P, P, P, P, P]
+        lib.moe_nvfp4_quantize.restype = I32
+        lib.moe_nvfp4_dequantize.argtypes = [P, P, I64, I64, I64, I32, P, P]
+        lib.moe_nvfp4_dequantize.restype = I32
+        lib.moe_nvfp4_plan.argtypes = [P, I64, P, P, P, P, P, P, P, SZ, P, P]
+        lib.moe_nvfp4_plan.restype = I32
+        lib.moe_nvfp4_forward.argtypes = [P, I64, P, P, P, P, P, P, P, P, SZ, P, P]
+        lib.moe_nvfp4_forward.restype = I32
+        v = lib.moe_nvfp4_abi_version()
+        if v != ABI_VERSION:
+            raise RuntimeError(f"libmoe_nvfp4 ABI version {v}, binding expects {ABI_VERSION}")
+        _lib = lib
+        return lib
+
+
+def status_string(code: int) -> str:
+    return load_library().moe_nvfp4_status_string(int(code)).decode()
+
+
+def _check(fn, rc):
+    if rc != OK:
+        raise MoEError(fn, rc)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream():
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def _need(t, dtype, name):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name}: expected a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name}: must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: must be contiguous")
+    return t
+
+
+def make_config(hidden, n_experts, top_k, intermediate, shared=False, ids_given=False):
+    c = Config()
+    c.hidden, c.n_experts, c.top_k, c.intermediate = hidden, n_experts, top_k, intermediate
+    c.flags = (FLAG_SHARED if shared else 0) | (FLAG_IDS_GIVEN if ids_given else 0)
+    return c
+
+
+def query(cfg: Config, max_tokens: int):
+    pb, wb = ctypes.c_size_t(0), ctypes.c_size_t(0)
+    _check("moe_nvfp4_query", load_library().moe_nvfp4_query(
+        ctypes.byref(cfg), int(max_tokens), ctypes.byref(pb), ctypes.byref(wb)))
+    return pb.value, wb.value
+
+
+# ---- quantise / dequantise ---------------------------------------------------------
+
+def quantize(w: torch.Tensor, layout: int, status: torch.Tensor | None = None, q=None, s=None,
+             g=None):
+    """FP32 CUDA [n_mats, rows, k] -> (q uint8, s uint8, g float32 [n_mats]).
+
+    q, s, g may be given (contiguous CUDA tensors of the right sizes) to write
+    into, e.g. a slice of a larger per-layer buffer."""
+    if w.dim() == 2:
+        w = w.unsqueeze(0)
+    _need(w, torch.float32, "w")
+    n, rows, k = w.shape
+    if q is None:
+        q = torch.empty((n, rows * k // 2), dtype=torch.uint8, device=w.device)
+    if s is None:
+        s = torch.empty((n, rows * k // 16), dtype=torch.uint8, device=w.device)
+    if g is None:
+        g = torch.empty((n,), dtype=torch.float32, device=w.device)
+    _need(q, torch.uint8, "q")
+    _need(s, torch.uint8, "s")
+    _need(g, torch.float32, "g")
+    if q.numel() != n * rows * k // 2 or s.numel() != n * rows * k // 16 or g.numel() != n:
+        raise ValueError("quantize: output sizes do not match the input")
+    if status is not None:
+        _need(status, torch.int32, "status")
+    _check("moe_nvfp4_quantize", load_library().moe_nvfp4_quantize(
+        _ptr(w), n, rows, k, int(layout), _ptr(q), _ptr(s), _ptr(g), _ptr(status), _stream()))
+    return q, s, g
+
+
+def dequantize(q, s, n_mats, rows, k, layout):
+    out = torch.empty((n_mats, rows, k), dtype=torch.float16, device=q.device)
+    _check("moe_nvfp4_dequantize", load_library().moe_nvfp4_dequantize(
+        _ptr(_need(q, torch.uint8, "q")), _ptr(_need(s, torch.uint8, "s")), n_mats, rows, k,
+        int(layout), _ptr(out), _stream()))
+    return out
+
+
+# ---- plan / forward ---------------------------------------------------------------------
+
+def _weights_c(w, layout):
+    if w is None:
+        return None
+    q, s, g = w
+    wc = WeightsC()
+    wc.q = q.data_ptr()
+    wc.s = s.data_ptr()
+    wc.g = g.data_ptr()
+    wc.layout = layout
+    wc.reserved = 0
+    return wc
+
+
+def plan(cfg: Config, x, w_router, bias, w_gate, ids, topk_w, plan_buf, status=None):
+    M = x.shape[0]
+    _need(x, torch.float16, "x")
+    _need(ids, torch.int32, "ids")
+    _need(topk_w, torch.float32, "topk_w")
+    _need(plan_buf, torch.uint8, "plan")
+    _check("moe_nvfp4_plan", load_library().moe_nvfp4_plan(
+        ctypes.byref(cfg), M, _ptr(x), _ptr(w_router), _ptr(bias), _ptr(w_gate), _ptr(ids),
+        _ptr(topk_w), _ptr(plan_buf), plan_buf.numel(), _ptr(status), _stream()))
+
+
+def forward(cfg: Config, x, plan_buf, w13, w2, shared13, shared2, y, ws, status=None):
+    M = x.shape[0]
+    _need(x, torch.float16, "x")
+    _need(y, torch.float16, "y")
+    _need(ws, torch.uint8, "ws")
+    a = _weights_c(w13, LAYOUT_FRAGMENT_W13)
+    b = _weights_c(w2, LAYOUT_FRAGMENT)
+    c = _weights_c(shared13, LAYOUT_FRAGMENT_W13)
+    d = _weights_c(shared2, LAYOUT_FRAGMENT)
+    _check("moe_nvfp4_forward", load_library().moe_nvfp4_forward(
+        ctypes.byref(cfg), M, _ptr(x), _ptr(plan_buf), ctypes.byref(a), ctypes.byref(b),
+        ctypes.byref(c) if c is not None else None, ctypes.byref(d) if d is not None else None,
+        _ptr(y), _ptr(ws), ws.numel(), _ptr(status), _stream()))
+
+
+class MoELayer:
+    """Owns the quantised weights and the plan / workspace buffers of one layer.
+
+    w13 / w2: (q, s, g) CUDA tensors in the fragment layouts (W13 interleaved).
+    """
+
+    def __init__(self, hidden, n_experts, top_k, intermediate, w_router, w13, w2,
+                 shared13=None, shared2=None, w_gate=None, bias=None, max_tokens=1,
+                 device="cuda"):
+        self.shared = shared13 is not None
+        self.cfg = make_config(hidden, n_experts, top_k, intermediate, shared=self.shared)
+        self.cfg_given = make_config(hidden, n_experts, top_k, intermediate, shared=self.shared,
+                                     ids_given=True)
+        self.H, self.E, self.k, self.I = hidden, n_experts, top_k, intermediate
+        self.w_router, self.w13, self.w2 = w_router, w13, w2
+        self.shared13, self.shared2, self.w_gate, self.bias = shared13, shared2, w_gate, bias
+        self.max_tokens = 0
+        self.device = torch.device(device)
+        self.status = torch.zeros(1, dtype=torch.int32, device=self.device)
+        self.reserve(max_tokens)
+
+    def reserve(self, max_tokens):
+        if max_tokens <= self.max_tokens:
+            return
+        pb, wb = query(self.cfg, max_tokens)
+        self.plan_buf = torch.zeros(pb, dtype=torch.uint8, device=self.device)
+        self.ws = torch.empty(max(wb, 16), dtype=torch.uint8, device=self.device)
+        self.max_tokens = max_tokens
+
+    def route(self, x, ids=None, topk_w=None, out_ids=None, out_w=None):
+        """Router + plan; with ids/topk_w given, plans those instead."""
+        M = x.shape[0]
+        self.reserve(M)
+        if ids is not None:
+            plan(self.cfg_given, x, None, None, self.w_gate, ids, topk_w, self.plan_buf,
+                 self.status)
+            return ids, topk_w
+        ids = out_ids if out_ids is not None else torch.empty((M, self.k), dtype=torch.int32,
+                                                              device=self.device)
+        tw = out_w if out_w is not None else torch.empty((M, self.k), dtype=torch.float32,
+                                                         device=self.device)
+        plan(self.cfg, x, self.w_router, self.bias, self.w_gate, ids, tw, self.plan_buf,
+             self.status)
+        return ids, tw
+
+    def forward_planned(self, x, y=None):
+        M = x.shape[0]
+        y = y if y is not None else torch.empty((M, self.H), dtype=torch.float16, device=self.device)
+        forward(self.cfg, x, self.plan_buf, self.w13, self.w2, self.shared13, self.shared2, y,
+                self.ws, self.status)
+        return y
+
+    def __call__(self, x, y=None):
+        self.route(x)
+        return self.forward_planned(x, y)

@@ -303,20 +303,24 @@ void oracle_router(const uint16_t *x, const uint16_t *wr, const float *bias,
                    int64_t M, int64_t H, int64_t E, int64_t k, float *logits,
                    int32_t *ids, float *w)
 {
+    /* tokens are independent; each logit is summed in ascending h order.
+     * Built without fast-math and with -ffp-contract=off, so every product
+     * and sum below is one IEEE FP32 operation in program order. */
+#pragma omp parallel for schedule(dynamic, 1)
     for (int64_t t = 0; t < M; ++t) {
         float *lt = logits + t * E;
+        float *xf = (float *)malloc(sizeof(float) * H);
+        for (int64_t h = 0; h < H; ++h)
+            xf[h] = (float)oracle_f16_to_double(x[t * H + h]);
         for (int64_t e = 0; e < E; ++e) {
-            volatile float acc = 0.0f;
+            float acc = 0.0f;
             for (int64_t h = 0; h < H; ++h) {
-                volatile float p = (float)oracle_f16_to_double(x[t * H + h]) *
-                                   (float)oracle_f16_to_double(wr[h * E + e]);
+                float p = xf[h] * (float)oracle_f16_to_double(wr[h * E + e]);
                 acc = acc + p;
             }
-            volatile float l = acc;
-            if (bias)
-                l = acc + bias[e];
-            lt[e] = l;
+            lt[e] = bias ? acc + bias[e] : acc;
         }
+        free(xf);
         /* selection: repeatedly take the largest remaining logit, the lowest
          * id winning ties (a stable descending sort, truncated to k) */
         unsigned char *taken = (unsigned char *)calloc((size_t)E, 1);

@@ -1,0 +1,251 @@
+"""GPU router, plan and layer forward vs the CPU oracle.
+
+Acceptance (the layer's stated parity bar):
+  * plan: bit-exact given the same expert ids;
+  * router: top-k id sets agree except where the oracle's gap between the
+    k-th and (k+1)-th logit is below 1e-5; weights within 1e-5;
+  * layer output: rel-L2 <= 1e-3 and max-abs <= 2e-2 against the oracle.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from harness import (MAX_ABS_TOL, REL_L2_TOL, ROUTER_GAP, ROUTER_W_TOL, TILE_ROWS, Case,
+                     compare)
+from nvfp4_weight_mixture_gb300 import moe, synth
+
+pytestmark = pytest.mark.gpu
+
+TINY = synth.WORKLOADS["tiny_m8"]
+DEC1 = synth.WORKLOADS["decode_m1"]
+DEC16 = synth.WORKLOADS["decode_m16_bias"]
+PRE = synth.WORKLOADS["prefill_m8192"]
+PRE_Z = synth.WORKLOADS["prefill_m8192_zipf_shared"]
+
+
+def _check_router(case, tokens=None):
+    ids_g, w_g = case.gpu_route()
+    tok = np.arange(case.wl.M) if tokens is None else np.asarray(tokens)
+    logits, ids_o, w_o, _ = case.oracle_route(tok)
+    k = case.wl.k
+    mismatched = 0
+    for i, t in enumerate(tok):
+        srt = np.sort(logits[i])[::-1]
+        gap = srt[k - 1] - srt[k] if k < len(srt) else np.inf
+        if set(ids_g[t]) != set(ids_o[i]):
+            assert gap < ROUTER_GAP, (t, ids_g[t], ids_o[i], gap)
+            mismatched += 1
+            continue
+        # same set: same order unless logits tie within the gap tolerance
+        if not np.array_equal(ids_g[t], ids_o[i]):
+            assert np.min(np.abs(np.diff(logits[i][ids_o[i]]))) < ROUTER_GAP
+            continue
+        assert np.max(np.abs(w_g[t] - w_o[i])) <= ROUTER_W_TOL, t
+        assert abs(float(w_g[t].sum()) - 1.0) < 1e-5
+    assert mismatched <= max(1, len(tok) // 1000)
+    return ids_g, w_g
+
+
+def _check_plan(case, ids):
+    """GPU plan of `ids` vs the oracle plan of the same ids: bit-exact."""
+    wl = case.wl
+    k_eff = wl.k + int(wl.shared)
+    e_eff = wl.E + int(wl.shared)
+    ids_eff = np.asarray(ids, np.int32)
+    if wl.shared:
+        ids_eff = np.concatenate([ids_eff, np.full((wl.M, 1), wl.E, np.int32)], 1)
+    ref = oracle.plan(ids_eff, e_eff, TILE_ROWS)
+    got = case.plan_arrays()
+    np.testing.assert_array_equal(got["ids"], ids_eff.reshape(-1))
+    np.testing.assert_array_equal(got["counts"], ref["counts"])
+    np.testing.assert_array_equal(got["offsets"], ref["offsets"])
+    np.testing.assert_array_equal(got["perm"], ref["perm"])
+    np.testing.assert_array_equal(got["inv"], ref["inv"])
+    np.testing.assert_array_equal(got["tiles"], ref["tiles"])
+    np.testing.assert_array_equal(got["active"], np.nonzero(ref["counts"])[0])
+    assert int(got["hdr"][0]) == wl.M and int(got["hdr"][1]) == k_eff
+    return ref
+
+
+# ---- router ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("wl,M", [(TINY, 8), (TINY, 1), (TINY, 77), (DEC1, 1), (DEC16, 16),
+                                  (DEC16, 9), (PRE, 300)])
+def test_router_vs_oracle(wl, M):
+    case = Case(synth.with_tokens(wl, M))
+    _check_router(case)
+    assert int(case.layer.status.item()) == 0
+
+
+def test_router_full_prefill_sampled():
+    case = Case(PRE_Z)
+    rng = np.random.default_rng(3)
+    tok = np.sort(rng.choice(PRE_Z.M, 256, replace=False))
+    _check_router(case, tok)
+
+
+# ---- plan ------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("wl,M", [(TINY, 8), (TINY, 16), (TINY, 500), (DEC16, 16),
+                                  (PRE, 9000)])
+def test_plan_bit_exact_given_ids(wl, M):
+    case = Case(synth.with_tokens(wl, M))
+    ids = synth.random_ids(case.wl, variant=1)
+    w = np.full(ids.shape, 1.0 / wl.k, np.float32)
+    case.layer.route(case.x_t, torch.from_numpy(ids).cuda(), torch.from_numpy(w).cuda())
+    torch.cuda.synchronize()
+    _check_plan(case, ids)
+    assert int(case.layer.status.item()) == 0
+
+
+@pytest.mark.parametrize("M", [5, 3000])
+def test_plan_edge_cases(M):
+    wl = synth.custom("edge", M, 256, 64, 4, 128)
+    case = Case(wl)
+    # all tokens on the same four experts (one hot expert per slot)
+    ids = np.tile(np.array([[3, 9, 40, 63]], np.int32), (M, 1))
+    w = np.full(ids.shape, 0.25, np.float32)
+    case.layer.route(case.x_t, torch.from_numpy(ids).cuda(), torch.from_numpy(w).cuda())
+    torch.cuda.synchronize()
+    _check_plan(case, ids)
+    # invalid ids: dropped, flagged
+    bad = ids.copy()
+    bad[0, 1] = -1
+    bad[M - 1, 3] = 64
+    case.layer.status.zero_()
+    case.layer.route(case.x_t, torch.from_numpy(bad).cuda(), torch.from_numpy(w).cuda())
+    torch.cuda.synchronize()
+    _check_plan(case, bad)
+    assert int(case.layer.status.item()) & moe.ST_INVALID_ID
+
+
+@pytest.mark.parametrize("M", [12, 600])
+def test_plan_with_shared_expert(M):
+    wl = synth.custom("sh", M, 256, 16, 2, 128, bias="zipf", shared=True)
+    case = Case(wl)
+    ids = synth.random_ids(wl, variant=2)
+    w = np.full(ids.shape, 0.5, np.float32)
+    case.layer.route(case.x_t, torch.from_numpy(ids).cuda(), torch.from_numpy(w).cuda())
+    torch.cuda.synchronize()
+    _check_plan(case, ids)
+
+
+# ---- layer forward -----------------------------------------------------------------------
+
+def _forward_check(case, tokens=None, ids_from_oracle=True):
+    if ids_from_oracle:
+        y = case.gpu_forward(ids_from_oracle=True)
+        ref = case.oracle_forward()
+        rel, mx = compare(y, ref)
+    else:
+        y = case.gpu_forward()
+        ref = case.oracle_forward(tokens=tokens)
+        rel, mx = compare(y[np.asarray(tokens)], ref)
+    assert rel <= REL_L2_TOL and mx <= MAX_ABS_TOL, (rel, mx)
+    assert int(case.layer.status.item()) == 0
+    return y
+
+
+@pytest.mark.parametrize("M", [1, 3, 8, 16])
+def test_forward_tiny_decode(M):
+    _forward_check(Case(synth.with_tokens(TINY, M)))
+
+
+@pytest.mark.parametrize("M", [17, 40, 300, 777])
+def test_forward_tiny_prefill(M):
+    _forward_check(Case(synth.with_tokens(TINY, M)))
+
+
+def test_forward_tiny_shared_expert():
+    wl = synth.custom("sh", 8, 256, 16, 2, 128, bias="zipf", shared=True)
+    _forward_check(Case(wl))
+    wl = synth.custom("sh", 200, 256, 16, 2, 128, bias="zipf", shared=True)
+    _forward_check(Case(wl))
+
+
+def test_forward_decode_m1_full():
+    _forward_check(Case(DEC1))
+
+
+def test_forward_decode_m16_full():
+    _forward_check(Case(DEC16))
+
+
+def test_forward_prefill_midsize():
+    _forward_check(Case(synth.with_tokens(PRE, 300)))
+
+
+@pytest.mark.parametrize("wl", [PRE, PRE_Z])
+def test_forward_full_prefill_sampled(wl):
+    case = Case(wl)
+    rng = np.random.default_rng(5)
+    tok = np.sort(rng.choice(wl.M, 24, replace=False))
+    _forward_check(case, tokens=tok, ids_from_oracle=False)
+
+
+def test_forward_zero_tokens():
+    case = Case(synth.with_tokens(TINY, 8))
+    x0 = case.x_t[:0]
+    ids, w = case.layer.route(x0)
+    y = case.layer.forward_planned(x0)
+    assert y.shape == (0, TINY.H)
+
+
+def test_forward_repeat_bitwise_and_graph_replay():
+    case = Case(synth.with_tokens(TINY, 40))
+    y1 = case.gpu_forward()
+    y2 = case.gpu_forward()
+    np.testing.assert_array_equal(y1.view(np.uint16), y2.view(np.uint16))
+    # CUDA graph with changing inputs: capture once, replay on new x
+    layer = case.layer
+    x_static = case.x_t.clone()
+    y_static = torch.empty_like(x_static)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        layer(x_static, y_static)
+    torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        layer(x_static, y_static)
+    for variant in (1, 2):
+        x_new = torch.from_numpy(synth.activations(case.wl, variant)).cuda()
+        x_static.copy_(x_new)
+        y_static.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        y_eager = layer(x_new)
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(y_static.cpu().numpy().view(np.uint16),
+                                      y_eager.cpu().numpy().view(np.uint16))
+
+
+def test_decode_batch_invariance():
+    """Inside the decode bucket a token's output does not depend on its batch:
+    M=16 equals two M=8 calls bitwise."""
+    case = Case(synth.with_tokens(DEC16, 16))
+    y16 = case.gpu_forward()
+    parts = []
+    for sl in (slice(0, 8), slice(8, 16)):
+        xs = case.x_t[sl].contiguous()
+        parts.append(case.layer(xs).cpu().numpy())
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(y16.view(np.uint16), np.concatenate(parts).view(np.uint16))
+
+
+@pytest.mark.parametrize("M", [16, 40])
+def test_forward_given_repeated_ids(M):
+    """Given ids that repeat an expert inside a token (more than 16 rows of one
+    expert even in the decode bucket) against the oracle on the same ids."""
+    wl = synth.custom("rep", M, 256, 16, 2, 128)
+    case = Case(wl)
+    ids = np.zeros((M, 2), np.int32)
+    ids[:, 0] = 3
+    ids[:, 1] = 3
+    ids[::3, 1] = 7
+    w = np.full(ids.shape, 0.5, np.float32)
+    y = case.gpu_forward(ids=ids, w=w)
+    ref = case.oracle_forward(ids=ids, w=w)
+    rel, mx = compare(y, ref)
+    assert rel <= REL_L2_TOL and mx <= MAX_ABS_TOL, (rel, mx)
