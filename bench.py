@@ -1,0 +1,527 @@
+#!/usr/bin/env python3
+"""Benchmark of the NVFP4-weight MoE layer on GB300: MoE-layer tokens/s.
+
+One step = one complete layer call (router + plan + W13/SwiGLU + W2 + combine,
+i.e. moe_nvfp4_plan + moe_nvfp4_forward) over one batch of seeded synthetic
+tokens, replayed from a CUDA graph with every input resident in HBM.  The L2
+cache is flushed (a 2x-L2 buffer is written) before every timed step, outside
+the step's events, and the routes change from step to step (16 different token
+batches), so weights stream from HBM as in a real layer stack.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+    python bench.py --impl reference ...   # the CPU oracle arm
+
+Workloads (seeded; see nvfp4_weight_mixture_gb300/synth.py): decode_m1 (the
+default: 1 token, H 2048, 512 experts, top-10, I 512), decode_m16_bias,
+prefill_m8192, prefill_m8192_zipf_shared, tiny_m8.
+
+Under torchrun each rank runs the same workload on its own GPU (token-parallel
+replicas, no collective on the data path); value = all ranks' tokens / the
+slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = "MoE-layer tokens/s"
+UNIT = "tokens/s"
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=None)
+    p.add_argument("--warmup", type=int, default=None)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default="decode_m1")
+    p.add_argument("--tokens", type=int, default=None,
+                   help="override the workload's token count (same shapes and seeds)")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=12.0,
+                   help="target CPU time of the oracle sample")
+    return p.parse_args()
+
+
+def dist_info():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+# ---------------------------------------------------------------------------
+# accounting (algorithmic bytes and FLOPs)
+# ---------------------------------------------------------------------------
+def w13_expert_bytes(wl):
+    return 2 * wl.I * wl.H // 2 + 2 * wl.I * wl.H // 16 + 4
+
+
+def w2_expert_bytes(wl):
+    return wl.H * wl.I // 2 + wl.H * wl.I // 16 + 4
+
+
+def layer_accounting(wl, n_active, n_pairs):
+    """Algorithmic bytes / FLOPs of one layer call: weights of the touched
+    experts (routed + shared), router weight, x, y, bias; FLOPs of the router,
+    gate and every pair's MLP.  Intermediates (h, partials) are not counted."""
+    bytes_ = n_active * (w13_expert_bytes(wl) + w2_expert_bytes(wl))
+    bytes_ += wl.H * wl.E * 2 + wl.M * wl.H * 2 * 2
+    if wl.bias != "none":
+        bytes_ += wl.E * 4
+    if wl.shared:
+        bytes_ += wl.H * 2
+    flops = 2 * wl.M * wl.H * wl.E + n_pairs * (2 * wl.H * 2 * wl.I + 2 * wl.I * wl.H)
+    if wl.shared:
+        flops += 2 * wl.M * wl.H
+    return bytes_, flops
+
+
+def kernel_accounting(wl, step, n_active, n_pairs, decode):
+    """(bound, algorithmic bytes, algorithmic FLOPs) of one launch of a traced step."""
+    H, I, M = wl.H, wl.I, wl.M
+    if step == "w13":
+        b = n_active * w13_expert_bytes(wl) + M * H * 2 + n_pairs * I * 2
+        f = n_pairs * 2 * H * 2 * I
+    elif step == "w2":
+        b = n_active * w2_expert_bytes(wl) + n_pairs * I * 2 + n_pairs * H * 4
+        f = n_pairs * 2 * I * H
+    elif step == "combine":
+        b = n_pairs * H * 4 + M * H * 2
+        f = n_pairs * H
+    else:  # plan: router weight + x + ids / weights
+        b = H * wl.E * 2 + M * H * 2 + n_pairs * 8
+        f = 2 * M * H * wl.E
+    bound = "hbm" if (decode or step in ("combine", "plan")) else "tensor"
+    return bound, b, f
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
+
+
+def load_traffic(workload, kernel):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, or None
+    when the summary is missing or the kernel sources changed since it was taken."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    src = os.path.join(ROOT, "nvfp4_weight_mixture_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in sorted(os.listdir(src)):
+        with open(os.path.join(src, f), "rb") as fh:
+            h.update(fh.read())
+    sha = h.hexdigest()[:16]
+    with open(path) as f:
+        for line in f:
+            parts = line.split()
+            if len(parts) >= 4 and parts[0] == workload and parts[1] == kernel:
+                return float(parts[2]) if parts[3] == sha else None
+    return None
+
+
+# ---------------------------------------------------------------------------
+# clocks sampler (nvidia-smi during the timed region)
+# ---------------------------------------------------------------------------
+class Clocks:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.proc = None
+        self.gpu = gpu_index
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.splitlines():
+            v = [x.strip() for x in line.split(",")]
+            if len(v) < 8:
+                continue
+            try:
+                sm.append(float(v[0]))
+                mx.append(float(v[1]))
+            except ValueError:
+                continue
+            for n, flag in zip(names, v[4:8]):
+                if flag.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (cpu_baseline and the reference arm)
+# ---------------------------------------------------------------------------
+def oracle_sample(wl, seconds, max_tokens=None):
+    """Times the oracle (router + plan-free forward, as it stands) on sampled
+    tokens of the workload, batched so that all host cores are used.  Weights
+    of the touched experts are quantised by the oracle before timing."""
+    import oracle
+    from nvfp4_weight_mixture_gb300 import synth
+    cores = len(os.sched_getaffinity(0))
+    os.environ.setdefault("OMP_NUM_THREADS", str(cores))
+    # token pool: decode workloads draw fresh token batches (variants)
+    pool = []
+    v = 0
+    while sum(len(p) for p in pool) < max(4 * cores, 64):
+        pool.append(synth.activations(wl, 100 + v))
+        v += 1
+    x = np.concatenate(pool)[: max(4 * cores, 64)]
+    wr = synth.router_weight(wl)
+    bias = synth.router_bias(wl)
+    wg = synth.gate_weight(wl)
+    E, H, I = wl.E, wl.H, wl.I
+
+    def route(xb):
+        _, ids, w = oracle.router(xb, wr, bias, wl.k)
+        gm = oracle.shared_gate(xb, wg) if wl.shared else None
+        return ids, w, gm
+
+    # quantise the experts of the first batch (outside timing)
+    o13 = (np.zeros((E, 2 * I, H // 2), np.uint8), np.zeros((E, 2 * I, H // 16), np.uint8),
+           np.ones((E,), np.float32))
+    o2 = (np.zeros((E, H, I // 2), np.uint8), np.zeros((E, H, I // 16), np.uint8),
+          np.ones((E,), np.float32))
+    have = set()
+    shared = None
+    if wl.shared:
+        a = oracle.quantize(synth.shared_w13(wl)[None])
+        b = oracle.quantize(synth.shared_w2(wl)[None])
+        shared = ((a[0][0], a[1][0], a[2][0]), (b[0][0], b[1][0], b[2][0]))
+
+    def ensure(ids):
+        for e in set(int(e) for e in ids.ravel()) - have:
+            a = oracle.quantize(synth.expert_w13(wl, e)[None])
+            b = oracle.quantize(synth.expert_w2(wl, e)[None])
+            for i in range(3):
+                o13[i][e] = a[i][0]
+                o2[i][e] = b[i][0]
+            have.add(e)
+
+    batch = cores
+    done = 0
+    elapsed = 0.0
+    idx = 0
+    while True:
+        sel = np.arange(idx, idx + batch) % len(x)
+        idx += batch
+        xb = np.ascontiguousarray(x[sel])
+        # expert weights are prepared outside the timed region
+        ids_pre, _, _ = route(xb)
+        ensure(ids_pre)
+        t0 = time.perf_counter()
+        ids, w, gm = route(xb)
+        oracle.forward(xb, ids, w, o13, o2, shared=shared, gamma=gm)
+        elapsed += time.perf_counter() - t0
+        done += len(sel)
+        if elapsed >= seconds or (max_tokens is not None and done >= max_tokens):
+            break
+    return done / elapsed, cores, done, elapsed
+
+
+def run_reference(args, wl):
+    ws, rank, _ = dist_info()
+    if rank != 0:
+        return 0
+    steps = args.steps or 10
+    warmup = args.warmup if args.warmup is not None else 1
+    per_step = max(1, min(wl.M, len(os.sched_getaffinity(0))))
+    budget = 150.0 / max(steps + warmup, 1)
+    if warmup:
+        oracle_sample(wl, 0.0, max_tokens=per_step * warmup)
+    rate, cores, done, el = oracle_sample(wl, budget * steps, max_tokens=per_step * steps)
+    ms = 1000.0 * wl.M / rate
+    line = {
+        "impl": "reference", "metric": METRIC, "value": rate, "unit": UNIT,
+        "n_gpus": args.gpus, "steps": steps, "warmup": warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": workload_config(wl),
+        "cpu_baseline": {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"{done} tokens of {wl.name} in {el:.1f} s (batches of "
+                                   f"{cores}), C oracle as it stands"},
+        "e2e": {"value": rate, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config(wl):
+    return {"workload": wl.name, "tokens": wl.M, "hidden": wl.H, "experts": wl.E,
+            "top_k": wl.k, "intermediate": wl.I, "router_bias": wl.bias,
+            "shared_expert": wl.shared,
+            "weights": "NVFP4 (E2M1, E4M3 per 16 along K, FP32 per tensor) from N(0,0.02)",
+            "activations": "FP16 N(0,1), 16 rotating token batches",
+            "l2": "flushed before every timed step (2x L2 buffer written)",
+            "parallelism": "token-parallel replicas, no collective"}
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+def build_layer(wl, dev, moe, synth):
+    import torch
+    from concurrent.futures import ThreadPoolExecutor
+    E, H, I = wl.E, wl.H, wl.I
+    q13 = torch.empty((E, I * H), dtype=torch.uint8, device=dev)
+    s13 = torch.empty((E, I * H // 8), dtype=torch.uint8, device=dev)
+    g13 = torch.empty((E,), dtype=torch.float32, device=dev)
+    q2 = torch.empty((E, H * I // 2), dtype=torch.uint8, device=dev)
+    s2 = torch.empty((E, H * I // 16), dtype=torch.uint8, device=dev)
+    g2 = torch.empty((E,), dtype=torch.float32, device=dev)
+    chunk = 32
+    with ThreadPoolExecutor(min(16, os.cpu_count() or 4)) as pool:
+        for e0 in range(0, E, chunk):
+            e1 = min(E, e0 + chunk)
+            a = np.stack(list(pool.map(lambda e: synth.expert_w13(wl, e), range(e0, e1))))
+            moe.quantize(torch.from_numpy(a).to(dev), moe.LAYOUT_FRAGMENT_W13, q=q13[e0:e1],
+                         s=s13[e0:e1], g=g13[e0:e1])
+            b = np.stack(list(pool.map(lambda e: synth.expert_w2(wl, e), range(e0, e1))))
+            moe.quantize(torch.from_numpy(b).to(dev), moe.LAYOUT_FRAGMENT, q=q2[e0:e1],
+                         s=s2[e0:e1], g=g2[e0:e1])
+    sh13 = sh2 = None
+    if wl.shared:
+        sh13 = moe.quantize(torch.from_numpy(synth.shared_w13(wl)).to(dev), moe.LAYOUT_FRAGMENT_W13)
+        sh2 = moe.quantize(torch.from_numpy(synth.shared_w2(wl)).to(dev), moe.LAYOUT_FRAGMENT)
+    wr = torch.from_numpy(synth.router_weight(wl)).to(dev)
+    bias = synth.router_bias(wl)
+    wg = synth.gate_weight(wl)
+    layer = moe.MoELayer(H, E, wl.k, I, wr, (q13, s13, g13), (q2, s2, g2), sh13, sh2,
+                         None if wg is None else torch.from_numpy(wg).to(dev),
+                         None if bias is None else torch.from_numpy(bias).to(dev),
+                         max_tokens=wl.M, device=dev)
+    return layer
+
+
+def run_gpu(args, wl):
+    import torch
+    from nvfp4_weight_mixture_gb300 import moe, synth
+
+    ws, rank, local = dist_info()
+    dist = None
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    moe.load_library()
+    decode = wl.M <= moe.DECODE_MAX_TOKENS
+    steps = args.steps or (200 if decode else 30)
+    warmup = max(3, args.warmup if args.warmup is not None else 10)
+
+    layer = build_layer(wl, dev, moe, synth)
+    n_var = 16
+    xs = [torch.from_numpy(synth.activations(wl, v)).to(dev) for v in range(n_var)]
+    ys = [torch.empty((wl.M, wl.H), dtype=torch.float16, device=dev) for _ in range(n_var)]
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    # warm-up (eager) and graph capture: one graph per token batch
+    with torch.cuda.stream(stream):
+        for i in range(warmup):
+            layer(xs[i % n_var], ys[i % n_var])
+    stream.synchronize()
+    graphs = []
+    for v in range(n_var):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            layer(xs[v], ys[v])
+        graphs.append(g)
+    with torch.cuda.stream(stream):
+        for i in range(warmup):
+            flush.zero_()
+            graphs[i % n_var].replay()
+    stream.synchronize()
+    launches_per_step = 4 if decode else 7
+
+    # ---- timed region: graph replays, L2 flushed before each step ------------------
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    clocks = Clocks(local)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    t_wall = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for i in range(steps):
+            flush.zero_()
+            ev[i][0].record(stream)
+            graphs[i % n_var].replay()
+            ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t_wall
+    ck = clocks.stop()
+    times = [a.elapsed_time(b) for a, b in ev]
+    total_ms = sum(times)
+    if dist:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+        dist.barrier()
+    ms_per_step = total_ms / steps
+    value = ws * wl.M * steps / (total_ms / 1e3)
+
+    # ---- per-kernel durations (traced eager steps, same protocol) ----------------
+    tr = [torch.cuda.Event(enable_timing=True) for _ in range(8)]
+    moe.set_trace_events(tr)
+    kt = {s: [] for s in moe.TRACE_STEPS}
+    n_tr = min(steps, 50)
+    with torch.cuda.stream(stream):
+        for i in range(n_tr):
+            flush.zero_()
+            layer(xs[i % n_var], ys[i % n_var])
+            stream.synchronize()
+            for j, s in enumerate(moe.TRACE_STEPS):
+                kt[s].append(tr[2 * j].elapsed_time(tr[2 * j + 1]))
+    moe.set_trace_events(None)
+    kernel_ms = {s: statistics.mean(v) for s, v in kt.items()}
+
+    # plan statistics of the last traced step (read after timing)
+    k_eff = wl.k + int(wl.shared)
+    hdr = layer.plan_buf[:64].view(torch.int32).cpu().numpy()
+    n_active, n_valid = int(hdr[3]), int(hdr[5])
+    st = int(layer.status.item())
+
+    # ---- end to end through the public API: pinned H2D + layer + D2H ------------
+    xh = [torch.from_numpy(synth.activations(wl, v)).pin_memory() for v in range(n_var)]
+    yh = torch.empty((wl.M, wl.H), dtype=torch.float16).pin_memory()
+    xd = torch.empty_like(xs[0])
+    yd = torch.empty_like(ys[0])
+    eev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    with torch.cuda.stream(stream):
+        for i in range(warmup):
+            xd.copy_(xh[i % n_var], non_blocking=True)
+            layer(xd, yd)
+            yh.copy_(yd, non_blocking=True)
+    stream.synchronize()
+    if dist:
+        dist.barrier()
+    with torch.cuda.stream(stream):
+        for i in range(steps):
+            flush.zero_()
+            eev[i][0].record(stream)
+            xd.copy_(xh[i % n_var], non_blocking=True)
+            layer(xd, yd)
+            yh.copy_(yd, non_blocking=True)
+            eev[i][1].record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = sum(a.elapsed_time(b) for a, b in eev)
+    if dist:
+        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_value = ws * wl.M * steps / (e2e_ms / 1e3)
+
+    if rank != 0:
+        if dist:
+            dist.destroy_process_group()
+        return 0
+
+    # ---- roofline of the dominant kernel -------------------------------------------
+    hbm, tflops, peak_src = load_peaks()
+    dom = max(("w13", "w2", "combine", "plan"), key=lambda s: kernel_ms[s])
+    bound, kb, kf = kernel_accounting(wl, dom, n_active, n_valid, decode)
+    dur = kernel_ms[dom] / 1e3
+    if bound == "hbm":
+        achieved, peak, unit = kb / dur / 1e9, hbm, "GB/s"
+    else:
+        achieved, peak, unit = kf / dur / 1e12, tflops, "TFLOP/s"
+    traffic = load_traffic(wl.name, dom)
+    lb, lf = layer_accounting(wl, n_active, n_valid)
+    step_s = ms_per_step / 1e3
+    layer_roof = max(lb / (hbm * 1e9), lf / (tflops * 1e12))
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": steps,
+        "warmup": warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+        "config": workload_config(wl),
+        "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
+                     "frac": achieved / peak, "traffic": traffic, "kernel": dom,
+                     "peak_source": f"{peak_src} ({'hbm_gbs' if bound == 'hbm' else 'bf16_tflops'}"
+                                    f"{', fp16 = bf16 nominal rate' if bound == 'tensor' else ''})",
+                     "algorithmic": {"bytes": kb, "flops": kf, "kernel_ms": kernel_ms[dom]}},
+        "layer": {"algorithmic_bytes": lb, "flops": lf, "touched_experts": n_active,
+                  "pairs": n_valid, "roofline_us": layer_roof * 1e6,
+                  "frac_of_roofline": layer_roof / step_s,
+                  "hbm_gbs_achieved": lb / step_s / 1e9,
+                  "step_ms_p10_p50_p90": [float(np.percentile(times, q)) for q in (10, 50, 90)],
+                  "kernel_ms_traced": kernel_ms, "status": st},
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": wl.M * wl.H * 2,
+                "d2h_bytes_per_step": wl.M * wl.H * 2},
+        "gpu_launches": launches_per_step * steps,
+        "clocks": ck,
+        "wall_s_timed_region": wall,
+    }
+    if ws == 1 and not args.no_cpu_baseline:
+        rate, cores, done, el = oracle_sample(wl, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle",
+                                "sample": f"{done} tokens of {wl.name} in {el:.1f} s (batches of"
+                                          f" {cores} tokens; router + forward), C oracle as it "
+                                          f"stands"}
+    print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse_args()
+    from nvfp4_weight_mixture_gb300 import synth
+    if args.workload not in synth.WORKLOADS:
+        raise SystemExit(f"unknown workload {args.workload}; one of {list(synth.WORKLOADS)}")
+    wl = synth.WORKLOADS[args.workload]
+    if args.tokens is not None:
+        wl = synth.with_tokens(wl, args.tokens)
+    if args.impl == "reference":
+        return run_reference(args, wl)
+    return run_gpu(args, wl)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

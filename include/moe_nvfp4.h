@@ -93,10 +93,10 @@ extern "C" {
 #define MOE_LAYOUT_FRAGMENT_W13 2
 
 typedef struct moe_nvfp4_config {
-  int32_t hidden;       /* H: model width; H % 128 == 0, 128 <= H <= 8192 */
+  int32_t hidden;       /* H: model width; H % 256 == 0, 256 <= H <= 4096 */
   int32_t n_experts;    /* E: routed experts; E % 8 == 0, 8 <= E <= 512 */
   int32_t top_k;        /* k: experts per token; 1 <= k <= min(E, 32) */
-  int32_t intermediate; /* I: expert intermediate size; I % 64 == 0, 64 <= I <= 4096 */
+  int32_t intermediate; /* I: expert intermediate size; I % 128 == 0, 128 <= I <= 4096 */
   uint32_t flags;       /* MOE_FLAG_* */
   int32_t reserved[3];  /* must be zero */
 } moe_nvfp4_config;
@@ -151,7 +151,8 @@ int32_t moe_nvfp4_quantize(const float* w, int64_t n_mats, int64_t rows, int64_t
  * "[Kernel][SM70] Improve Qwen3.8 no-MTP concurrency", section "Scope and
  * related PRs").
  *
- *   M        tokens, 0 <= M <= 2^20 (M == 0 launches nothing).
+ *   M        tokens, 0 <= M <= 2^20.  M == 0 returns MOE_OK at once, launching
+ *            nothing and ignoring every buffer argument (which may be NULL).
  *   x        device FP16 [M][H].
  *   w_router device FP16 [H][E] (expert index fastest).
  *   bias     device FP32 [E] or NULL: added to the logits before selection.
@@ -183,6 +184,7 @@ int32_t moe_nvfp4_plan(const moe_nvfp4_config* cfg, int64_t M, const void* x,
  * with FP32 accumulation and the slot sum in order j = 0..k-1, then the shared
  * term.  M <= 16 runs the weight-streaming GEMV path, larger M the grouped
  * tcgen05 GEMMs; both give the same results up to FP32 summation order.
+ * M == 0 returns MOE_OK at once and ignores every buffer argument.
  *
  *   w13      routed W13, layout MOE_LAYOUT_FRAGMENT_W13, E matrices [2I][H].
  *   w2       routed W2, layout MOE_LAYOUT_FRAGMENT, E matrices [H][I].
@@ -203,6 +205,19 @@ int32_t moe_nvfp4_forward(const moe_nvfp4_config* cfg, int64_t M, const void* x,
  * applies to its weight operand. */
 int32_t moe_nvfp4_dequantize(const uint8_t* q, const uint8_t* s, int64_t n_mats, int64_t rows,
                              int64_t k, int32_t layout, void* out, void* stream);
+
+/* Diagnostic kernel timing.  With `events` non-NULL, every later plan and
+ * forward call records events[2*i] on its stream just before and
+ * events[2*i+1] just after step i, for i < n_steps:
+ *   i = 0  the whole plan call (router and plan kernels),
+ *   i = 1  the W13 kernel (decode GEMV or grouped tcgen05 GEMM),
+ *   i = 2  the W2 kernel,
+ *   i = 3  the combine kernel.
+ * `events` are cudaEvent_t handles created by the caller (with timing
+ * enabled).  The records separate the kernels on the stream, so a traced call
+ * does not overlap its kernels through programmatic dependent launch.  NULL
+ * turns tracing off.  Process-wide setting; not thread-safe. */
+int32_t moe_nvfp4_set_trace_events(void* const* events, int32_t n_steps);
 
 #ifdef __cplusplus
 }

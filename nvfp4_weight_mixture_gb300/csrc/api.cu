@@ -95,6 +95,9 @@ int32_t check_weights(const moe_nvfp4_weights* w, int32_t layout) {
   return MOE_OK;
 }
 
+void* const* g_trace_events = nullptr;
+int32_t g_trace_steps = 0;
+
 int32_t cuda_status(cudaError_t e) {
   if (e == cudaSuccess) return MOE_OK;
   cudaGetLastError();
@@ -103,7 +106,22 @@ int32_t cuda_status(cudaError_t e) {
 
 }  // namespace
 
+namespace moe {
+bool trace_on() { return g_trace_events != nullptr; }
+void trace_mark(cudaStream_t stream, int step, bool end) {
+  if (!g_trace_events || step >= g_trace_steps) return;
+  cudaEventRecord(static_cast<cudaEvent_t>(g_trace_events[2 * step + (end ? 1 : 0)]), stream);
+}
+}  // namespace moe
+
 extern "C" {
+
+int32_t moe_nvfp4_set_trace_events(void* const* events, int32_t n_steps) {
+  if (events && (n_steps < 1 || n_steps > 4)) return MOE_ERR_INVALID_ARG;
+  g_trace_events = events;
+  g_trace_steps = events ? n_steps : 0;
+  return MOE_OK;
+}
 
 int32_t moe_nvfp4_abi_version(void) { return MOE_NVFP4_ABI_VERSION; }
 
@@ -180,6 +198,7 @@ int32_t moe_nvfp4_plan(const moe_nvfp4_config* cfg, int64_t M, const void* x,
   int32_t rc = check_cfg(cfg, &d);
   if (rc) return rc;
   if (M < 0 || M > kMaxTokens) return MOE_ERR_SHAPE;
+  if (M == 0) return MOE_OK;  // nothing to route; buffers of empty tensors may be NULL
   const bool given = (cfg->flags & MOE_FLAG_IDS_GIVEN) != 0;
   if (!x || !ids || !topk_w || !plan) return MOE_ERR_INVALID_ARG;
   if (!given && !w_router) return MOE_ERR_INVALID_ARG;
@@ -191,16 +210,19 @@ int32_t moe_nvfp4_plan(const moe_nvfp4_config* cfg, int64_t M, const void* x,
     return MOE_ERR_ALIGNMENT;
   if (status && (reinterpret_cast<uintptr_t>(status) & 3u)) return MOE_ERR_ALIGNMENT;
   if (plan_bytes < plan_bytes_for(d, M)) return MOE_ERR_WORKSPACE;
-  if (M == 0) return MOE_OK;
   int sms = 0;
   rc = current_device(&sms);
   if (rc) return rc;
   PlanView pv;
   plan_layout(static_cast<char*>(plan), M, d.k_eff, d.e_eff, d.E, d.H, &pv);
-  return cuda_status(launch_plan(d, M, static_cast<const __half*>(x),
-                                 static_cast<const __half*>(w_router), bias,
-                                 static_cast<const __half*>(w_gate), ids, topk_w, given, pv,
-                                 status, static_cast<cudaStream_t>(stream), sms));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  trace_mark(st, kTracePlan, false);
+  cudaError_t e = launch_plan(d, M, static_cast<const __half*>(x),
+                              static_cast<const __half*>(w_router), bias,
+                              static_cast<const __half*>(w_gate), ids, topk_w, given, pv, status,
+                              st, sms);
+  trace_mark(st, kTracePlan, true);
+  return cuda_status(e);
 }
 
 int32_t moe_nvfp4_forward(const moe_nvfp4_config* cfg, int64_t M, const void* x, const void* plan,
@@ -211,6 +233,7 @@ int32_t moe_nvfp4_forward(const moe_nvfp4_config* cfg, int64_t M, const void* x,
   int32_t rc = check_cfg(cfg, &d);
   if (rc) return rc;
   if (M < 0 || M > kMaxTokens) return MOE_ERR_SHAPE;
+  if (M == 0) return MOE_OK;  // nothing to compute; buffers of empty tensors may be NULL
   if (!x || !plan || !y || !ws) return MOE_ERR_INVALID_ARG;
   if ((rc = check_weights(w13, MOE_LAYOUT_FRAGMENT_W13))) return rc;
   if ((rc = check_weights(w2, MOE_LAYOUT_FRAGMENT))) return rc;
@@ -222,7 +245,6 @@ int32_t moe_nvfp4_forward(const moe_nvfp4_config* cfg, int64_t M, const void* x,
     return MOE_ERR_ALIGNMENT;
   if (status && (reinterpret_cast<uintptr_t>(status) & 3u)) return MOE_ERR_ALIGNMENT;
   if (ws_bytes < ws_bytes_for(d, M)) return MOE_ERR_WORKSPACE;
-  if (M == 0) return MOE_OK;
   int sms = 0;
   rc = current_device(&sms);
   if (rc) return rc;

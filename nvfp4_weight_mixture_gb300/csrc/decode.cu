@@ -350,20 +350,34 @@ static cudaError_t decode_impl(const LayerDims& d, int64_t M, const __half* x, c
                                __half* h, float* partial, cudaStream_t stream) {
   const int max_active = (int)((M * d.k_eff < d.e_eff) ? M * d.k_eff : d.e_eff);
   const size_t xs_smem = (size_t)NT * 8 * (d.H * 2 + 16);
-  cudaError_t e = cudaFuncSetAttribute(decode_w13_kernel<NT>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)xs_smem);
-  if (e != cudaSuccess) return e;
-  e = launch_k(decode_w13_kernel<NT>, dim3(max_active * (d.I / 16)), dim3(256), xs_smem, stream,
-               true, d, pv, x, w13, s13, h);
-  if (e != cudaSuccess) return e;
   const size_t hs_smem = (size_t)NT * 8 * (d.I * 2 + 16);
-  e = cudaFuncSetAttribute(decode_w2_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)hs_smem);
+  static bool attr_done = false;
+  if (!attr_done) {
+    // the largest sizes the shape limits allow (H, I <= 4096)
+    const int big = NT * 8 * (4096 * 2 + 16);
+    cudaError_t e = cudaFuncSetAttribute(decode_w13_kernel<NT>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, big);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(decode_w2_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             big);
+    if (e != cudaSuccess) return e;
+    attr_done = true;
+  }
+  const bool pdl = !trace_on();
+  trace_mark(stream, kTraceW13, false);
+  cudaError_t e = launch_k(decode_w13_kernel<NT>, dim3(max_active * (d.I / 16)), dim3(256),
+                           xs_smem, stream, pdl, d, pv, x, w13, s13, h);
   if (e != cudaSuccess) return e;
+  trace_mark(stream, kTraceW13, true);
+  trace_mark(stream, kTraceW2, false);
   e = launch_k(decode_w2_kernel<NT>, dim3(max_active * (d.H / 128)), dim3(256), hs_smem, stream,
-               true, d, pv, (const __half*)h, w2, s2, partial);
+               pdl, d, pv, (const __half*)h, w2, s2, partial);
   if (e != cudaSuccess) return e;
-  return launch_combine(d, M, pv, partial, y, stream, true);
+  trace_mark(stream, kTraceW2, true);
+  trace_mark(stream, kTraceCombine, false);
+  e = launch_combine(d, M, pv, partial, y, stream, pdl);
+  trace_mark(stream, kTraceCombine, true);
+  return e;
 }
 
 cudaError_t launch_decode_forward(const LayerDims& d, int64_t M, const __half* x,

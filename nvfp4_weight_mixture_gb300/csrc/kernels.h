@@ -45,6 +45,11 @@ cudaError_t launch_prefill_forward(const LayerDims& d, int64_t M, const __half* 
 cudaError_t launch_combine(const LayerDims& d, int64_t M, const PlanView& pv,
                            const float* partial, __half* y, cudaStream_t stream, bool pdl);
 
+// Diagnostic per-step event records (moe_nvfp4_set_trace_events).
+enum TraceStep { kTracePlan = 0, kTraceW13 = 1, kTraceW2 = 2, kTraceCombine = 3 };
+void trace_mark(cudaStream_t stream, int step, bool end);
+bool trace_on();
+
 // Launch helper: programmatic dependent launch when `pdl` is set.
 template <typename... KArgs, typename... Args>
 cudaError_t launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,

@@ -333,19 +333,32 @@ cudaError_t launch_prefill_forward(const LayerDims& d, int64_t M, const __half* 
   const int64_t P = M * d.k_eff;
   const int max_tiles = max_tiles_for(P, d.e_eff);
   const size_t smem = gemm_smem_bytes();
-  cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<true>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  static bool attr_done = false;
+  if (!attr_done) {
+    cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<true>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(grouped_gemm_kernel<false>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    attr_done = true;
+  }
+  const bool pdl = !trace_on();
+  trace_mark(stream, kTraceW13, false);
+  cudaError_t e = launch_k(grouped_gemm_kernel<true>, dim3(max_tiles * ((2 * d.I) / 256)),
+                           dim3(kGemmThreads), smem, stream, pdl, d, pv, x, w13, s13, h, partial,
+                           status);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(grouped_gemm_kernel<false>,
-                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
-  e = launch_k(grouped_gemm_kernel<true>, dim3(max_tiles * ((2 * d.I) / 256)),
-               dim3(kGemmThreads), smem, stream, true, d, pv, x, w13, s13, h, partial, status);
-  if (e != cudaSuccess) return e;
+  trace_mark(stream, kTraceW13, true);
+  trace_mark(stream, kTraceW2, false);
   e = launch_k(grouped_gemm_kernel<false>, dim3(max_tiles * (d.H / 256)), dim3(kGemmThreads),
-               smem, stream, true, d, pv, (const __half*)h, w2, s2, h, partial, status);
+               smem, stream, pdl, d, pv, (const __half*)h, w2, s2, h, partial, status);
   if (e != cudaSuccess) return e;
-  return launch_combine(d, M, pv, partial, y, stream, true);
+  trace_mark(stream, kTraceW2, true);
+  trace_mark(stream, kTraceCombine, false);
+  e = launch_combine(d, M, pv, partial, y, stream, pdl);
+  trace_mark(stream, kTraceCombine, true);
+  return e;
 }
 
 }  // namespace moe

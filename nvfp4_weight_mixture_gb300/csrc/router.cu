@@ -655,18 +655,28 @@ cudaError_t launch_plan(const LayerDims& d, int64_t M, const __half* x, const __
     route_given_kernel<<<(Mi + 7) / 8, 256, 0, stream>>>(d, Mi, x, w_gate, ids_user, w_user, pv);
   } else {
     const size_t smem = router_mma_smem(d.E);
-    cudaError_t e = cudaFuncSetAttribute(router_mma_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
+    static bool attr_done = false;
+    if (!attr_done) {
+      cudaError_t e = cudaFuncSetAttribute(router_mma_kernel,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           (int)router_mma_smem(512));
+      if (e != cudaSuccess) return e;
+      attr_done = true;
+    }
     router_mma_kernel<<<(Mi + kRtTok - 1) / kRtTok, 512, smem, stream>>>(
         d, Mi, x, w_router, bias, w_gate, ids_user, w_user, pv);
   }
   const int64_t P = M * d.k_eff;
   const int n_chunks = (int)((P + kPlanChunk - 1) / kPlanChunk);
   const size_t hsmem = sizeof(uint16_t) * 32 * d.e_eff;
-  cudaError_t e = cudaFuncSetAttribute(plan_hist_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)hsmem);
-  if (e != cudaSuccess) return e;
+  static bool attr_done = false;
+  if (!attr_done) {
+    cudaError_t e = cudaFuncSetAttribute(plan_hist_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)(sizeof(uint16_t) * 32 * 520));
+    if (e != cudaSuccess) return e;
+    attr_done = true;
+  }
   plan_hist_kernel<<<n_chunks, 1024, hsmem, stream>>>(d, P, pv, status);
   plan_scan_kernel<<<1, 1024, 0, stream>>>(d, Mi, n_chunks, pv);
   plan_scatter_kernel<<<(unsigned)((P + 255) / 256), 256, 0, stream>>>(d, P, pv);

@@ -34,7 +34,9 @@ LAYOUT_FRAGMENT_W13 = 2
 DECODE_MAX_TOKENS = 16
 
 EXPORTS = ["moe_nvfp4_abi_version", "moe_nvfp4_status_string", "moe_nvfp4_query",
-           "moe_nvfp4_quantize", "moe_nvfp4_plan", "moe_nvfp4_forward", "moe_nvfp4_dequantize"]
+           "moe_nvfp4_quantize", "moe_nvfp4_plan", "moe_nvfp4_forward", "moe_nvfp4_dequantize",
+           "moe_nvfp4_set_trace_events"]
+TRACE_STEPS = ("plan", "w13", "w2", "combine")
 
 
 class Config(ctypes.Structure):
@@ -82,6 +84,8 @@ def load_library(path: str = LIB_PATH):
         lib.moe_nvfp4_plan.restype = I32
         lib.moe_nvfp4_forward.argtypes = [P, I64, P, P, P, P, P, P, P, P, SZ, P, P]
         lib.moe_nvfp4_forward.restype = I32
+        lib.moe_nvfp4_set_trace_events.argtypes = [P, I32]
+        lib.moe_nvfp4_set_trace_events.restype = I32
         v = lib.moe_nvfp4_abi_version()
         if v != ABI_VERSION:
             raise RuntimeError(f"libmoe_nvfp4 ABI version {v}, binding expects {ABI_VERSION}")
@@ -130,6 +134,28 @@ def query(cfg: Config, max_tokens: int):
     _check("moe_nvfp4_query", load_library().moe_nvfp4_query(
         ctypes.byref(cfg), int(max_tokens), ctypes.byref(pb), ctypes.byref(wb)))
     return pb.value, wb.value
+
+
+_trace_keep = None
+
+
+def set_trace_events(events):
+    """Per-step CUDA event records inside plan/forward (diagnostic).
+
+    events: list of 2 * n torch.cuda.Event(enable_timing=True) for the first n
+    of TRACE_STEPS, or None to stop tracing."""
+    global _trace_keep
+    lib = load_library()
+    if events is None:
+        _check("moe_nvfp4_set_trace_events", lib.moe_nvfp4_set_trace_events(None, 0))
+        _trace_keep = None
+        return
+    for e in events:      # torch creates the CUDA event on its first record
+        e.record()
+    torch.cuda.synchronize()
+    arr = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
+    _trace_keep = (arr, events)
+    _check("moe_nvfp4_set_trace_events", lib.moe_nvfp4_set_trace_events(arr, len(events) // 2))
 
 
 # ---- quantise / dequantise ---------------------------------------------------------

@@ -74,6 +74,7 @@ def test_plan_and_forward_fail_closed(lib):
     plan = lib.moe_nvfp4_plan
     # M = 0 with valid arguments: OK, nothing launched, no device needed
     assert plan(ctypes.byref(c), 0, a, a, None, None, a, a, a, 1 << 20, None, None) == 0
+    assert plan(ctypes.byref(c), 0, None, None, None, None, None, None, None, 0, None, None) == 0
     assert plan(ctypes.byref(c), 1, None, a, None, None, a, a, a, 1 << 20, None, None) == -1
     assert plan(ctypes.byref(c), 1, odd, a, None, None, a, a, a, 1 << 20, None, None) == -3
     assert plan(ctypes.byref(c), 1, a, a, None, None, a, a, a, 16, None, None) == -4
