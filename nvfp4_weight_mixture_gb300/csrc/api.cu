@@ -107,6 +107,9 @@ int32_t cuda_status(cudaError_t e) {
 }  // namespace
 
 namespace moe {
+#ifdef MOE_TIMELINE
+__device__ unsigned long long g_timeline[32];
+#endif
 bool trace_on() { return g_trace_events != nullptr; }
 void trace_mark(cudaStream_t stream, int step, bool end) {
   if (!g_trace_events || step >= g_trace_steps) return;
@@ -115,6 +118,29 @@ void trace_mark(cudaStream_t stream, int step, bool end) {
 }  // namespace moe
 
 extern "C" {
+
+#ifdef MOE_TIMELINE
+// Timeline build only (not part of the public header): reset / read the
+// per-kernel globaltimer stamps.
+int32_t moe_nvfp4_timeline_reset(void* stream) {
+  unsigned long long h[32];
+  for (int s = 0; s < 8; ++s) {
+    h[4 * s] = ~0ull;
+    h[4 * s + 1] = ~0ull;
+    h[4 * s + 2] = 0ull;
+    h[4 * s + 3] = 0ull;
+  }
+  // raw cells: 21, 23, 24 take minima; 20, 22, 25 maxima
+  for (int c : {20, 22, 25}) h[c] = 0ull;
+  for (int c : {21, 23, 24}) h[c] = ~0ull;
+  return cuda_status(cudaMemcpyToSymbolAsync(moe::g_timeline, h, sizeof(h), 0,
+                                             cudaMemcpyHostToDevice,
+                                             static_cast<cudaStream_t>(stream)));
+}
+int32_t moe_nvfp4_timeline_read(unsigned long long* out) {
+  return cuda_status(cudaMemcpyFromSymbol(out, moe::g_timeline, sizeof(unsigned long long) * 32));
+}
+#endif
 
 int32_t moe_nvfp4_set_trace_events(void* const* events, int32_t n_steps) {
   if (events && (n_steps < 1 || n_steps > 4)) return MOE_ERR_INVALID_ARG;
@@ -219,8 +245,8 @@ int32_t moe_nvfp4_plan(const moe_nvfp4_config* cfg, int64_t M, const void* x,
   trace_mark(st, kTracePlan, false);
   cudaError_t e = launch_plan(d, M, static_cast<const __half*>(x),
                               static_cast<const __half*>(w_router), bias,
-                              static_cast<const __half*>(w_gate), ids, topk_w, given, pv, status,
-                              st, sms);
+                              static_cast<const __half*>(w_gate), ids, topk_w, given, pv,
+                              status, st, sms);
   trace_mark(st, kTracePlan, true);
   return cuda_status(e);
 }

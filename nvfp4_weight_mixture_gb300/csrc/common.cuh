@@ -15,6 +15,11 @@ constexpr int kDecodeMaxTokens = 16;     // M <= this runs the streaming GEMV pa
 constexpr int kTileRows = 256;           // plan tile height (N of the grouped MMAs)
 constexpr int kPlanChunk = 4096;         // pairs per histogram block in the plan
 constexpr uint64_t kWaitTimeoutNs = 200ull * 1000 * 1000;  // bounded spins: 200 ms
+// Decode work table entry (one per active expert, M <= 16): expert, first plan
+// position, rows, then the token of each of the first 16 rows; entries past
+// the active experts hold expert -1.
+constexpr int kDtabInts = 20;
+constexpr int kDtabEntries = kDecodeMaxTokens * 33;
 
 // ---------------------------------------------------------------------------
 // Plan buffer: a header followed by int32/float arrays, all carved by
@@ -44,7 +49,9 @@ struct PlanView {
   int32_t* rank;      // [M * k_eff] scratch: rank of a pair inside its chunk
   float* partial;     // [n_hchunks][kDecodeMaxTokens][n_experts] scratch (small-M router)
   float* logits;      // [kDecodeMaxTokens][n_experts] scratch (small-M router)
-  uint32_t* tickets;  // [64] self-resetting arrival counters (small-M router)
+  uint32_t* tickets;  // [64] self-resetting arrival counters: [0, 8) router slices,
+                      // [16, 48) decode W2 row blocks, 63 router finaliser
+  int32_t* dtab;      // [kDecodeMaxTokens * 33][kDtabInts] decode work table (M <= 16)
 };
 
 __host__ __device__ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
@@ -66,7 +73,7 @@ __host__ __device__ inline size_t plan_layout(char* base, int64_t M, int k_eff, 
   int64_t P = M * k_eff;
   int64_t Pc = P > 0 ? P : 1;
   int n_chunks = (int)((Pc + kPlanChunk - 1) / kPlanChunk);
-  int n_hchunks = (hidden + 255) / 256;
+  int n_hchunks = (hidden + 127) / 128;
   PlanView t;
   t.hdr = (PlanHeader*)take(sizeof(PlanHeader));
   t.tickets = (uint32_t*)take(64 * sizeof(uint32_t));
@@ -82,6 +89,7 @@ __host__ __device__ inline size_t plan_layout(char* base, int64_t M, int k_eff, 
   t.rank = (int32_t*)take(sizeof(int32_t) * Pc);
   t.partial = (float*)take(sizeof(float) * (size_t)n_hchunks * kDecodeMaxTokens * n_experts);
   t.logits = (float*)take(sizeof(float) * (size_t)kDecodeMaxTokens * n_experts);
+  t.dtab = (int32_t*)take(sizeof(int32_t) * kDtabEntries * kDtabInts);
   if (v) *v = t;
   return off;
 }
@@ -102,6 +110,48 @@ __device__ __forceinline__ uint64_t globaltimer() {
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
 }
+
+// ---- timeline instrumentation (built only with -DMOE_TIMELINE) -------------
+// Per kernel slot: [0] earliest block start, [1] earliest block past its
+// programmatic-launch wait, [2] latest block end, [3] blocks that ran.  Read
+// with moe_nvfp4_timeline_read() in that build; compiled out otherwise.
+enum TimelineSlot { kTlRouter = 0, kTlPlan = 1, kTlW13 = 2, kTlW2 = 3, kTlCombine = 4 };
+#ifdef MOE_TIMELINE
+extern __device__ unsigned long long g_timeline[32];
+struct TlScope {
+  int slot;
+  __device__ explicit TlScope(int s) : slot(s) {
+    if (threadIdx.x == 0) {
+      atomicMin(&g_timeline[4 * s], (unsigned long long)globaltimer());
+      atomicAdd(&g_timeline[4 * s + 3], 1ull);
+    }
+  }
+  __device__ void waited() const {
+    if (threadIdx.x == 0) atomicMin(&g_timeline[4 * slot + 1], (unsigned long long)globaltimer());
+  }
+  __device__ ~TlScope() {
+    if (threadIdx.x == 0) atomicMax(&g_timeline[4 * slot + 2], (unsigned long long)globaltimer());
+  }
+};
+#define MOE_TL(slot) ::moe::TlScope tl_scope_(slot)
+#define MOE_TL_WAITED() tl_scope_.waited()
+// raw stamps on timeline cells 20..31 (earliest / latest over the threads that pass)
+#define MOE_TL_MIN(cell) atomicMin(&::moe::g_timeline[cell], (unsigned long long)::moe::globaltimer())
+#define MOE_TL_MAX(cell) atomicMax(&::moe::g_timeline[cell], (unsigned long long)::moe::globaltimer())
+#else
+#define MOE_TL_MIN(cell) \
+  do {                   \
+  } while (0)
+#define MOE_TL_MAX(cell) \
+  do {                   \
+  } while (0)
+#define MOE_TL(slot) \
+  do {               \
+  } while (0)
+#define MOE_TL_WAITED() \
+  do {                  \
+  } while (0)
+#endif
 
 // ---- mbarrier ------------------------------------------------------------
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
@@ -184,6 +234,12 @@ __device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Starts an HBM -> L2 transfer of [p, p + bytes) (16-byte aligned, bytes a
+// multiple of 16) on the TMA engine; no completion is tracked.
+__device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
 
 // ---- NVFP4 decode ----------------------------------------------------------

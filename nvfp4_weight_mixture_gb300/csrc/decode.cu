@@ -49,24 +49,29 @@ __device__ __forceinline__ uint16_t ldg_u16(const uint8_t* p) {
 // h[pos][i] = fp16(silu(g13 * G) * (g13 * U)) for the expert's plan positions.
 // ---------------------------------------------------------------------------
 template <int NT>
-__global__ void __launch_bounds__(256) decode_w13_kernel(LayerDims d, PlanView pv,
-                                                         const __half* __restrict__ x,
-                                                         Weights w13, Weights s13,
-                                                         __half* __restrict__ h) {
+__global__ void __launch_bounds__(256, 3) decode_w13_kernel(LayerDims d, PlanView pv,
+                                                            const __half* __restrict__ x,
+                                                            Weights w13, Weights s13, Weights w2,
+                                                            Weights s2, __half* __restrict__ h) {
   extern __shared__ __align__(16) char xs_raw[];  // [NT*8][H*2 + 16] token rows
   __shared__ float red[8][2][NT][32][4];
   __shared__ int s_tok[NT * 8];
+  MOE_TL(kTlW13);
   pdl_wait();
+  MOE_TL_WAITED();
   pdl_launch_dependents();
+  __shared__ int s_ent[kDtabInts];
   const int H = d.H, I = d.I;
   const int n_rtp = I / 16;
   const int unit = blockIdx.x;
-  const int n_active = __ldcg(&pv.hdr->n_active);
-  if (unit >= n_active * n_rtp) return;
   const int a = unit / n_rtp, rp = unit - a * n_rtp;
-  const int e = __ldcg(pv.active + a);
-  const int count = __ldcg(pv.counts + e);
-  const int base = __ldcg(pv.offsets + e);
+  // one round trip for the unit's metadata: the decode work-table entry
+  if (threadIdx.x < kDtabInts) s_ent[threadIdx.x] = __ldcg(pv.dtab + a * kDtabInts + threadIdx.x);
+  __syncthreads();
+  const int e = s_ent[0];
+  if (e < 0) return;
+  const int base = s_ent[1];
+  const int count = s_ent[2];
   const bool sh = (e == d.E);
   const uint8_t* qe = sh ? s13.q : w13.q + (size_t)e * I * H;
   const uint8_t* se = sh ? s13.s : w13.s + (size_t)e * I * H / 8;
@@ -79,6 +84,15 @@ __global__ void __launch_bounds__(256) decode_w13_kernel(LayerDims d, PlanView p
   const uint8_t* st = se + (size_t)(2 * rp) * S * 64;
   const int xstride = H * 2 + 16;
   const int cpr = H / 8;  // 16-byte chunks per row
+  if (tid == 0) {
+    // start this unit's share (1 / n_rtp) of the expert's W2 bytes towards L2,
+    // so that the W2 kernel finds them there
+    const size_t q2 = (size_t)H * I / 2, s2b = (size_t)H * I / 16;
+    const uint8_t* q2e = sh ? s2.q : w2.q + (size_t)e * q2;
+    const uint8_t* s2e = sh ? s2.s : w2.s + (size_t)e * s2b;
+    prefetch_l2_bulk(q2e + (size_t)rp * (q2 / n_rtp), (uint32_t)(q2 / n_rtp));
+    prefetch_l2_bulk(s2e + (size_t)rp * (s2b / n_rtp), (uint32_t)(s2b / n_rtp));
+  }
 
   uint4 qv[4][2];
   uint32_t sv[4][2];
@@ -102,7 +116,8 @@ __global__ void __launch_bounds__(256) decode_w13_kernel(LayerDims d, PlanView p
   for (int n0 = 0; n0 < count; n0 += NT * 8) {
     const int n_e = min(count - n0, NT * 8);
     const int pos0 = base + n0;
-    if (tid < n_e) s_tok[tid] = __ldcg(pv.perm + pos0 + tid) / d.k_eff;
+    if (tid < n_e)
+      s_tok[tid] = (n0 + tid < 16) ? s_ent[4 + n0 + tid] : __ldcg(pv.perm + pos0 + tid) / d.k_eff;
     __syncthreads();
     for (int i = tid; i < n_e * cpr; i += 256) {
       const int n = i / cpr, c = i - n * cpr;
@@ -197,20 +212,27 @@ template <int NT>
 __global__ void __launch_bounds__(256) decode_w2_kernel(LayerDims d, PlanView pv,
                                                         const __half* __restrict__ h,
                                                         Weights w2, Weights s2,
-                                                        float* __restrict__ partial) {
+                                                        float* __restrict__ partial,
+                                                        __half* __restrict__ y) {
   extern __shared__ __align__(16) char hs_raw[];  // [NT*8][I*2 + 16] h rows
+  __shared__ int is_last;
+  MOE_TL(kTlW2);
+  __shared__ int s_ent[kDtabInts + 1];
   const int H = d.H, I = d.I;
   const int nhb = H / 128;
   const int unit = blockIdx.x;
-  const int n_active = __ldcg(&pv.hdr->n_active);
-  if (unit >= n_active * nhb) {
+  const int a = unit / nhb, hb = unit - a * nhb;
+  if (threadIdx.x < kDtabInts) s_ent[threadIdx.x] = __ldcg(pv.dtab + a * kDtabInts + threadIdx.x);
+  if (threadIdx.x == kDtabInts) s_ent[kDtabInts] = __ldcg(&pv.hdr->n_active);
+  __syncthreads();
+  const int e = s_ent[0];
+  if (e < 0) {
     pdl_wait();
     return;
   }
-  const int a = unit / nhb, hb = unit - a * nhb;
-  const int e = __ldcg(pv.active + a);
-  const int count = __ldcg(pv.counts + e);
-  const int base = __ldcg(pv.offsets + e);
+  const int n_active = s_ent[kDtabInts];
+  const int base = s_ent[1];
+  const int count = s_ent[2];
   const bool sh = (e == d.E);
   const uint8_t* qe = sh ? s2.q : w2.q + (size_t)e * H * I / 2;
   const uint8_t* se = sh ? s2.s : w2.s + (size_t)e * H * I / 16;
@@ -235,13 +257,35 @@ __global__ void __launch_bounds__(256) decode_w2_kernel(LayerDims d, PlanView pv
       }
     }
   };
-  load_group(0);  // weights depend only on the plan, complete before W13 ran
+  // Plan data (complete before the W13 grid started) is read before waiting on
+  // the W13 grid: the weights, the first row chunk's pairs and combine scales,
+  // and which pairs of the batch are valid (for the fused combine).
+  __shared__ int s_pair[NT * 8];
+  __shared__ float s_wsc[NT * 8];
+  __shared__ unsigned char s_valid[kDtabEntries];
+  load_group(0);
+  const int P_all = __ldcg(&pv.hdr->M) * d.k_eff;
+  for (int p = tid; p < P_all; p += 256) s_valid[p] = __ldcg(pv.inv + p) >= 0;
+  if (tid < min(count, NT * 8)) {
+    const int pair = __ldcg(pv.perm + base + tid);
+    s_pair[tid] = pair;
+    s_wsc[tid] = gsc * __ldcg(pv.w + pair);
+  }
   pdl_wait();
+  MOE_TL_WAITED();
   pdl_launch_dependents();
 
   for (int n0 = 0; n0 < count; n0 += NT * 8) {
     const int n_e = min(count - n0, NT * 8);
     const int pos0 = base + n0;
+    if (n0 > 0) {
+      __syncthreads();
+      if (tid < n_e) {
+        const int pair = __ldcg(pv.perm + pos0 + tid);
+        s_pair[tid] = pair;
+        s_wsc[tid] = gsc * __ldcg(pv.w + pair);
+      }
+    }
     for (int i = tid; i < n_e * cpr; i += 256) {
       const int n = i / cpr, c = i - n * cpr;
       cp_async16(smem_u32(hs_raw + n * hstride + c * 16), h + (int64_t)(pos0 + n) * I + c * 8,
@@ -297,13 +341,42 @@ __global__ void __launch_bounds__(256) decode_w2_kernel(LayerDims d, PlanView pv
       for (int c = 0; c < 4; ++c) {
         const int n = nt * 8 + 2 * t4 + (c & 1);
         if (n < n_e) {
-          const int pair = __ldcg(pv.perm + pos0 + n);
-          const float wsc = gsc * __ldcg(pv.w + pair);
           const int row = rt * 16 + g + ((c & 2) ? 8 : 0);
-          partial[(int64_t)pair * H + row] = acc[nt][c] * wsc;
+          partial[(int64_t)s_pair[n] * H + row] = acc[nt][c] * s_wsc[n];
         }
       }
     __syncthreads();  // hs reused by the next chunk
+  }
+  // The last of the n_active blocks of this row block sums the slots of every
+  // token in order: y[t][rows] = fp16(sum_j partial[t * k_eff + j][rows]).
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) {
+    const unsigned t = atomicAdd(&pv.tickets[16 + hb], 1u);
+    is_last = (t == (unsigned)n_active - 1);
+    if (is_last) pv.tickets[16 + hb] = 0u;
+  }
+  __syncthreads();
+  if (!is_last) return;
+  __threadfence();
+  const int k_eff = d.k_eff, M = P_all / k_eff;
+  for (int i = tid; i < M * 32; i += 256) {
+    const int t = i >> 5, c = hb * 128 + (i & 31) * 4;
+    float4 acc4 = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int j = 0; j < k_eff; ++j) {
+      const int64_t pair = (int64_t)t * k_eff + j;
+      if (!s_valid[pair]) continue;
+      const float4 v = __ldcg(reinterpret_cast<const float4*>(partial + pair * H + c));
+      acc4.x += v.x;
+      acc4.y += v.y;
+      acc4.z += v.z;
+      acc4.w += v.w;
+    }
+    __half2 lo = __floats2half2_rn(acc4.x, acc4.y), hi = __floats2half2_rn(acc4.z, acc4.w);
+    uint2 out;
+    out.x = *reinterpret_cast<uint32_t*>(&lo);
+    out.y = *reinterpret_cast<uint32_t*>(&hi);
+    *reinterpret_cast<uint2*>(y + (int64_t)t * H + c) = out;
   }
 }
 
@@ -313,7 +386,9 @@ __global__ void __launch_bounds__(256) decode_w2_kernel(LayerDims d, PlanView pv
 // ---------------------------------------------------------------------------
 __global__ void combine_kernel(int M, int H, int k_eff, const int32_t* __restrict__ inv,
                                const float* __restrict__ partial, __half* __restrict__ y) {
+  MOE_TL(kTlCombine);
   pdl_wait();
+  MOE_TL_WAITED();
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;  // one float4 of y
   const int64_t n4 = (int64_t)M * H / 4;
   if (i >= n4) return;
@@ -366,16 +441,16 @@ static cudaError_t decode_impl(const LayerDims& d, int64_t M, const __half* x, c
   const bool pdl = !trace_on();
   trace_mark(stream, kTraceW13, false);
   cudaError_t e = launch_k(decode_w13_kernel<NT>, dim3(max_active * (d.I / 16)), dim3(256),
-                           xs_smem, stream, pdl, d, pv, x, w13, s13, h);
+                           xs_smem, stream, pdl, d, pv, x, w13, s13, w2, s2, h);
   if (e != cudaSuccess) return e;
   trace_mark(stream, kTraceW13, true);
   trace_mark(stream, kTraceW2, false);
   e = launch_k(decode_w2_kernel<NT>, dim3(max_active * (d.H / 128)), dim3(256), hs_smem, stream,
-               pdl, d, pv, (const __half*)h, w2, s2, partial);
+               pdl, d, pv, (const __half*)h, w2, s2, partial, y);
   if (e != cudaSuccess) return e;
   trace_mark(stream, kTraceW2, true);
+  // the combine is fused into the W2 kernel on this path
   trace_mark(stream, kTraceCombine, false);
-  e = launch_combine(d, M, pv, partial, y, stream, pdl);
   trace_mark(stream, kTraceCombine, true);
   return e;
 }

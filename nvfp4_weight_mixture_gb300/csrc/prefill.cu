@@ -91,7 +91,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const int K = kW13 ? d.H : d.I;            // reduction length
   const int S = K / kBK;                      // k-steps
   const int units_per_tile = kW13 ? (2 * d.I) / 256 : d.H / 256;
+  MOE_TL(kW13 ? kTlW13 : kTlW2);
   pdl_wait();
+  MOE_TL_WAITED();
   const int n_tiles = __ldcg(&pv.hdr->n_tiles);
   const int tile = blockIdx.x / units_per_tile;
   const int u = blockIdx.x - tile * units_per_tile;

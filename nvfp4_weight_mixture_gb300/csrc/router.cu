@@ -30,44 +30,49 @@ __device__ __forceinline__ bool pair_valid(int e, int slot, const LayerDims& d) 
 
 // ---------------------------------------------------------------------------
 // Warp top-k over a row of E logits.  Lane j < k receives slot j: the j-th
-// largest logit, ties broken towards the lower expert id.  E <= 512.
+// largest logit, ties broken towards the lower expert id.  E <= 512.  Each
+// round takes the warp maximum of order-preserving integer keys and then the
+// lowest expert id holding it (two single-instruction warp reductions).
 // ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t f2key(float f) {
+  const uint32_t b = __float_as_uint(f);
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ float key2f(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
 template <bool kGlobal>
 __device__ __forceinline__ void warp_topk(const float* row, int E, int k, int* out_id,
                                           float* out_l) {
   const int lane = threadIdx.x & 31;
-  float v[16];
+  uint32_t v[16];  // key 0 = absent or taken (below every finite or infinite logit)
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
     const int e = lane + 32 * i;
-    v[i] = (e < E) ? (kGlobal ? __ldcg(row + e) : row[e]) : -INFINITY;
+    v[i] = (e < E) ? f2key(kGlobal ? __ldcg(row + e) : row[e]) : 0u;
   }
   int my_id = -1;
   float my_l = -INFINITY;
   for (int j = 0; j < k; ++j) {
-    float bv = v[0];
-    int bi = lane;
+    uint32_t m8[8];
 #pragma unroll
-    for (int i = 1; i < 16; ++i)
-      if (v[i] > bv) {
-        bv = v[i];
-        bi = lane + 32 * i;
-      }
+    for (int i = 0; i < 8; ++i) m8[i] = max(v[i], v[i + 8]);
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-      if (ov > bv || (ov == bv && oi < bi)) {
-        bv = ov;
-        bi = oi;
-      }
-    }
+    for (int i = 0; i < 4; ++i) m8[i] = max(m8[i], m8[i + 4]);
+    const uint32_t lm = max(max(m8[0], m8[2]), max(m8[1], m8[3]));
+    const uint32_t gm = __reduce_max_sync(0xffffffffu, lm);
+    uint32_t li = 0xffffffffu;
+#pragma unroll
+    for (int i = 15; i >= 0; --i)
+      if (v[i] == gm) li = (uint32_t)(lane + 32 * i);
+    const uint32_t gi = __reduce_min_sync(0xffffffffu, li);
 #pragma unroll
     for (int i = 0; i < 16; ++i)
-      if (lane + 32 * i == bi) v[i] = -INFINITY;
+      if ((uint32_t)(lane + 32 * i) == gi) v[i] = 0u;
     if (lane == j) {
-      my_id = bi;
-      my_l = bv;
+      my_id = (int)gi;
+      my_l = key2f(gm);
     }
   }
   *out_id = my_id;
@@ -117,23 +122,68 @@ __device__ __forceinline__ void store_route(const LayerDims& d, int t, int id, f
   }
 }
 
+// Exclusive block scan of three counters (blockDim.x == 256).
+__device__ __forceinline__ void block_scan3(int& a, int& b, int& c, int* tot) {
+  __shared__ int ws[8][3];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int ia = a, ib = b, ic = c;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int ta = __shfl_up_sync(0xffffffffu, ia, o);
+    const int tb = __shfl_up_sync(0xffffffffu, ib, o);
+    const int tc = __shfl_up_sync(0xffffffffu, ic, o);
+    if (lane >= o) {
+      ia += ta;
+      ib += tb;
+      ic += tc;
+    }
+  }
+  if (lane == 31) {
+    ws[warp][0] = ia;
+    ws[warp][1] = ib;
+    ws[warp][2] = ic;
+  }
+  __syncthreads();
+  int oa = 0, ob = 0, oc = 0, sa = 0, sb = 0, sc = 0;
+#pragma unroll
+  for (int w = 0; w < 8; ++w) {
+    if (w < warp) {
+      oa += ws[w][0];
+      ob += ws[w][1];
+      oc += ws[w][2];
+    }
+    sa += ws[w][0];
+    sb += ws[w][1];
+    sc += ws[w][2];
+  }
+  a = oa + ia - a;
+  b = ob + ib - b;
+  c = oc + ic - c;
+  tot[0] = sa;
+  tot[1] = sb;
+  tot[2] = sc;
+  __syncthreads();
+}
+
 // ---------------------------------------------------------------------------
 // Plan of up to kDecodeMaxTokens * (32 + 1) pairs by one block of 256 threads.
+// `src` (shared memory) holds the M * k_eff expert ids of the pairs.  Also
+// writes the decode work table.
 // ---------------------------------------------------------------------------
-__device__ void plan_small_block(const LayerDims& d, int M, const PlanView& pv,
+__device__ void plan_small_block(const LayerDims& d, int M, const int* src, const PlanView& pv,
                                  uint32_t* status) {
-  __shared__ int s_ids[kDecodeMaxTokens * 33];
-  __shared__ int s_cnt[kMaxEEff];
-  __shared__ int s_off[kMaxEEff];
-  __shared__ int s_tb[kMaxEEff];
-  __shared__ int s_tot[3];
+  __shared__ int s_ids[kDtabEntries];
+  __shared__ int s_perm[kDtabEntries];
+  __shared__ int s_cnt[768];
+  __shared__ int s_off[768];
+  __shared__ int s_act[kDtabEntries];
   const int tid = threadIdx.x, nthr = blockDim.x;
-  const int P = M * d.k_eff;
-  for (int i = tid; i < d.e_eff; i += nthr) s_cnt[i] = 0;
+  const int P = M * d.k_eff, ne = d.e_eff;
+  for (int i = tid; i < 768; i += nthr) s_cnt[i] = 0;
   __syncthreads();
   bool bad = false;
   for (int p = tid; p < P; p += nthr) {
-    const int e = pv.ids[p];
+    const int e = src[p];
     const bool ok = pair_valid(e, p % d.k_eff, d);
     s_ids[p] = ok ? e : -1;
     if (ok)
@@ -143,58 +193,44 @@ __device__ void plan_small_block(const LayerDims& d, int M, const PlanView& pv,
   }
   if (bad) set_status(status, MOE_ST_INVALID_ID);
   __syncthreads();
-  if (tid < 32) {
-    const int lane = tid, n = d.e_eff;
-    const int per = (n + 31) / 32, b = lane * per, end = min(b + per, n);
-    int cs = 0, as = 0, ts = 0;
-    for (int i = b; i < end; ++i) {
-      const int c = s_cnt[i];
-      cs += c;
-      as += c > 0;
-      ts += (c + kTileRows - 1) / kTileRows;
-    }
-    int ci = cs, ai = as, ti = ts;
+  // experts [3 tid, 3 tid + 3): counts, active flags, tiles -> block scan
+  int c3[3], sc = 0, sa = 0, st = 0;
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int a1 = __shfl_up_sync(0xffffffffu, ci, o);
-      const int a2 = __shfl_up_sync(0xffffffffu, ai, o);
-      const int a3 = __shfl_up_sync(0xffffffffu, ti, o);
-      if (lane >= o) {
-        ci += a1;
-        ai += a2;
-        ti += a3;
-      }
-    }
-    if (lane == 31) {
-      s_tot[0] = ci;
-      s_tot[1] = ai;
-      s_tot[2] = ti;
-    }
-    ci -= cs;
-    ai -= as;
-    ti -= ts;
-    for (int i = b; i < end; ++i) {
-      const int c = s_cnt[i];
-      s_off[i] = ci;
-      s_tb[i] = ti;
-      pv.counts[i] = c;
-      pv.offsets[i] = ci;
-      if (c > 0) pv.active[ai] = i;
-      ci += c;
-      ai += c > 0;
-      ti += (c + kTileRows - 1) / kTileRows;
-    }
+  for (int j = 0; j < 3; ++j) {
+    c3[j] = s_cnt[3 * tid + j];
+    sc += c3[j];
+    sa += c3[j] > 0;
+    st += (c3[j] + kTileRows - 1) / kTileRows;
   }
-  __syncthreads();
+  int tot[3];
+  block_scan3(sc, sa, st, tot);
+#pragma unroll
+  for (int j = 0; j < 3; ++j) {
+    const int e = 3 * tid + j;
+    if (e < ne) {
+      s_off[e] = sc;
+      pv.counts[e] = c3[j];
+      pv.offsets[e] = sc;
+      if (c3[j] > 0) {
+        pv.active[sa] = e;
+        s_act[sa] = e;
+      }
+      for (int r0 = 0; r0 < c3[j]; r0 += kTileRows, ++st)
+        reinterpret_cast<int4*>(pv.tiles)[st] = make_int4(e, r0, min(kTileRows, c3[j] - r0), 0);
+    }
+    sc += c3[j];
+    sa += c3[j] > 0;
+  }
   if (tid == 0) {
-    pv.offsets[d.e_eff] = s_tot[0];
+    pv.offsets[ne] = tot[0];
     pv.hdr->M = M;
     pv.hdr->k_eff = d.k_eff;
-    pv.hdr->e_eff = d.e_eff;
-    pv.hdr->n_valid = s_tot[0];
-    pv.hdr->n_active = s_tot[1];
-    pv.hdr->n_tiles = s_tot[2];
+    pv.hdr->e_eff = ne;
+    pv.hdr->n_valid = tot[0];
+    pv.hdr->n_active = tot[1];
+    pv.hdr->n_tiles = tot[2];
   }
+  __syncthreads();
   for (int p = tid; p < P; p += nthr) {
     const int e = s_ids[p];
     if (e < 0) {
@@ -205,22 +241,39 @@ __device__ void plan_small_block(const LayerDims& d, int M, const PlanView& pv,
     for (int q = 0; q < p; ++q) r += (s_ids[q] == e);
     const int pos = s_off[e] + r;
     pv.perm[pos] = p;
+    s_perm[pos] = p;
     pv.inv[p] = pos;
   }
-  for (int e = tid; e < d.e_eff; e += nthr) {
-    const int c = s_cnt[e];
-    int t = s_tb[e];
-    for (int r0 = 0; r0 < c; r0 += kTileRows, ++t) {
-      int4 tl = make_int4(e, r0, min(kTileRows, c - r0), 0);
-      reinterpret_cast<int4*>(pv.tiles)[t] = tl;
+  __syncthreads();
+  // decode work table: every entry up to the largest active-expert count
+  const int n_active = tot[1];
+  const int max_active = min(P, ne);
+  for (int i = tid; i < max_active * kDtabInts; i += nthr) {
+    const int a = i / kDtabInts, f = i - a * kDtabInts;
+    int v = -1;
+    if (a < n_active) {
+      const int e = s_act[a];
+      const int off = s_off[e];
+      if (f == 0)
+        v = e;
+      else if (f == 1)
+        v = off;
+      else if (f == 2)
+        v = s_cnt[e];
+      else if (f >= 4 && f - 4 < s_cnt[e])
+        v = s_perm[off + f - 4] / d.k_eff;
     }
+    pv.dtab[i] = v;
   }
 }
 
 // ---------------------------------------------------------------------------
 // Small-M router + plan (one launch).
-// grid = (ceil(E / 64), ceil(H / 256)), block = 256.
+// grid = (ceil(E / 64), H / kRsRows), block = 256: warp w of block (s, c)
+// streams rows [c*kRsRows + 16w, +16) of W_r for experts [64s, 64s+64).
 // ---------------------------------------------------------------------------
+constexpr int kRsRows = 128;
+
 __global__ void __launch_bounds__(256) router_small_kernel(LayerDims d, int M,
                                                            const __half* __restrict__ x,
                                                            const __half* __restrict__ wr,
@@ -228,58 +281,71 @@ __global__ void __launch_bounds__(256) router_small_kernel(LayerDims d, int M,
                                                            const __half* __restrict__ wg,
                                                            int32_t* ids_user, float* w_user,
                                                            PlanView pv, uint32_t* status) {
-  __shared__ float xs[kDecodeMaxTokens][256];
-  __shared__ float red[8][kDecodeMaxTokens][64];
+  __shared__ float xs[kDecodeMaxTokens][kRsRows];
+  __shared__ float red[4][kDecodeMaxTokens][64];
+  __shared__ int s_ids[kDecodeMaxTokens * 33];
   __shared__ int is_last;
+  MOE_TL(kTlRouter);
+  // the forward kernels may become resident now; they wait for this grid
+  pdl_launch_dependents();
   const int s = blockIdx.x, hc = blockIdx.y;
   const int E = d.E, H = d.H;
-  const int h0 = hc * 256, hn = min(256, H - h0);
+  const int h0 = hc * kRsRows;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  for (int i = tid; i < kDecodeMaxTokens * 256; i += 256) {
-    const int m = i >> 8, c = i & 255;
-    xs[m][c] = (m < M && c < hn) ? __half2float(x[(int64_t)m * H + h0 + c]) : 0.f;
-  }
   const int e0 = s * 64 + 2 * lane;
   const bool ev = e0 < E;
-  __half2 wv[32];
+  __half2 wv[16];
 #pragma unroll
-  for (int r = 0; r < 32; ++r) {
-    const int hr = warp * 32 + r;
-    wv[r] = (ev && hr < hn)
-                ? *reinterpret_cast<const __half2*>(wr + (int64_t)(h0 + hr) * E + e0)
-                : __float2half2_rn(0.f);
+  for (int r = 0; r < 16; ++r)
+    wv[r] = ev ? *reinterpret_cast<const __half2*>(wr + (int64_t)(h0 + warp * 16 + r) * E + e0)
+               : __float2half2_rn(0.f);
+  for (int i = tid; i < kDecodeMaxTokens * kRsRows; i += 256) {
+    const int m = i / kRsRows, c = i % kRsRows;
+    xs[m][c] = (m < M) ? __half2float(x[(int64_t)m * H + h0 + c]) : 0.f;
   }
   __syncthreads();
   float acc[kDecodeMaxTokens][2];
 #pragma unroll
   for (int m = 0; m < kDecodeMaxTokens; ++m) acc[m][0] = acc[m][1] = 0.f;
 #pragma unroll
-  for (int r = 0; r < 32; ++r) {
+  for (int r = 0; r < 16; ++r) {
     const float2 f = __half22float2(wv[r]);
 #pragma unroll
     for (int m = 0; m < kDecodeMaxTokens; ++m) {
       if (m < M) {
-        const float xv = xs[m][warp * 32 + r];
+        const float xv = xs[m][warp * 16 + r];
         acc[m][0] = fmaf(xv, f.x, acc[m][0]);
         acc[m][1] = fmaf(xv, f.y, acc[m][1]);
       }
     }
   }
+  // fixed-order reduction over the 8 warps: (w, w + 4) pairs, then w = 0..3
+  if (warp >= 4) {
 #pragma unroll
-  for (int m = 0; m < kDecodeMaxTokens; ++m) {
-    if (m < M) {
-      red[warp][m][2 * lane] = acc[m][0];
-      red[warp][m][2 * lane + 1] = acc[m][1];
+    for (int m = 0; m < kDecodeMaxTokens; ++m) {
+      if (m < M) {
+        red[warp - 4][m][2 * lane] = acc[m][0];
+        red[warp - 4][m][2 * lane + 1] = acc[m][1];
+      }
+    }
+  }
+  __syncthreads();
+  if (warp < 4) {
+#pragma unroll
+    for (int m = 0; m < kDecodeMaxTokens; ++m) {
+      if (m < M) {
+        red[warp][m][2 * lane] += acc[m][0];
+        red[warp][m][2 * lane + 1] += acc[m][1];
+      }
     }
   }
   __syncthreads();
   for (int i = tid; i < M * 64; i += 256) {
     const int m = i >> 6, c = i & 63, e = s * 64 + c;
-    float t = 0.f;
-#pragma unroll
-    for (int w = 0; w < 8; ++w) t += red[w][m][c];
+    const float t = (red[0][m][c] + red[1][m][c]) + (red[2][m][c] + red[3][m][c]);
     if (e < E) pv.partial[((int64_t)hc * kDecodeMaxTokens + m) * E + e] = t;
   }
+  if (tid == 0) MOE_TL_MAX(20);
   __threadfence();
   __syncthreads();
   if (tid == 0) {
@@ -290,16 +356,28 @@ __global__ void __launch_bounds__(256) router_small_kernel(LayerDims d, int M,
   __syncthreads();
   if (!is_last) return;
   __threadfence();
-  // slice finaliser: fixed-order sum over H chunks, + bias
+  if (tid == 0) MOE_TL_MIN(21);
+  // slice finaliser: fixed-order sum over the H chunks, + bias
+  const int nh = gridDim.y;
   for (int i = tid; i < M * 64; i += 256) {
     const int m = i >> 6, c = i & 63, e = s * 64 + c;
     if (e >= E) continue;
+    const float* src = pv.partial + (int64_t)m * E + e;
+    const int64_t stride = (int64_t)kDecodeMaxTokens * E;
     float t = 0.f;
-    for (int q = 0; q < (int)gridDim.y; ++q)
-      t += __ldcg(pv.partial + ((int64_t)q * kDecodeMaxTokens + m) * E + e);
+    int q = 0;
+    for (; q + 8 <= nh; q += 8) {
+      float v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) v[u] = __ldcg(src + (q + u) * stride);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) t += v[u];
+    }
+    for (; q < nh; ++q) t += __ldcg(src + q * stride);
     if (bias) t += bias[e];
     pv.logits[(int64_t)m * E + e] = t;
   }
+  if (tid == 0) MOE_TL_MAX(22);
   __threadfence();
   __syncthreads();
   if (tid == 0) {
@@ -310,6 +388,7 @@ __global__ void __launch_bounds__(256) router_small_kernel(LayerDims d, int M,
   __syncthreads();
   if (!is_last) return;
   __threadfence();
+  if (tid == 0) MOE_TL_MIN(23);
   for (int m = warp; m < M; m += 8) {
     int id;
     float l;
@@ -317,9 +396,13 @@ __global__ void __launch_bounds__(256) router_small_kernel(LayerDims d, int M,
     const float w = warp_topk_weight(l, d.k);
     const float gamma = d.shared ? warp_gate(x + (int64_t)m * H, wg, H) : 0.f;
     store_route(d, m, id, w, gamma, ids_user, w_user, pv);
+    if (lane < d.k) s_ids[m * d.k_eff + lane] = id;
+    if (d.shared && lane == 0) s_ids[m * d.k_eff + d.k] = d.E;
   }
   __syncthreads();
-  plan_small_block(d, M, pv, status);
+  if (tid == 0) MOE_TL_MIN(24);
+  plan_small_block(d, M, s_ids, pv, status);
+  if (tid == 0) MOE_TL_MAX(25);
 }
 
 // Caller-given ids and weights: copy into the plan (plus the shared slot).
@@ -327,6 +410,7 @@ __global__ void __launch_bounds__(256) router_small_kernel(LayerDims d, int M,
 __global__ void route_given_kernel(LayerDims d, int M, const __half* __restrict__ x,
                                    const __half* __restrict__ wg, const int32_t* ids_user,
                                    const float* w_user, PlanView pv) {
+  MOE_TL(kTlRouter);
   const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (t >= M) return;
@@ -345,7 +429,12 @@ __global__ void route_given_kernel(LayerDims d, int M, const __half* __restrict_
 
 __global__ void __launch_bounds__(256) plan_small_kernel(LayerDims d, int M, PlanView pv,
                                                          uint32_t* status) {
-  plan_small_block(d, M, pv, status);
+  __shared__ int s_src[kDecodeMaxTokens * 33];
+  MOE_TL(kTlPlan);
+  pdl_launch_dependents();
+  for (int p = threadIdx.x; p < M * d.k_eff; p += blockDim.x) s_src[p] = pv.ids[p];
+  __syncthreads();
+  plan_small_block(d, M, s_src, pv, status);
 }
 
 // ---------------------------------------------------------------------------
@@ -382,6 +471,7 @@ __global__ void __launch_bounds__(512) router_mma_kernel(LayerDims d, int M,
                                                          int32_t* ids_user, float* w_user,
                                                          PlanView pv) {
   extern __shared__ __align__(16) char smem[];
+  MOE_TL(kTlRouter);
   const int E = d.E, H = d.H;
   const int Ep = (E + 63) / 64 * 64;
   const int xst = kRtK + 8, wst = Ep + 8, lst = Ep + 1;
@@ -489,6 +579,7 @@ __global__ void __launch_bounds__(1024) plan_hist_kernel(LayerDims d, int64_t P,
   extern __shared__ uint16_t wcnt[];  // [32 warps][e_eff]: counts, then exclusive prefixes
   __shared__ int run[kMaxEEff];       // count of each expert in earlier sub-chunks
   __shared__ int subtot[kMaxEEff];
+  MOE_TL(kTlPlan);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int ne = d.e_eff;
   for (int i = tid; i < ne; i += 1024) run[i] = 0;
@@ -536,6 +627,7 @@ __global__ void __launch_bounds__(1024) plan_scan_kernel(LayerDims d, int M, int
   __shared__ int s_cnt[kMaxEEff];
   __shared__ int s_tb[kMaxEEff];
   __shared__ int s_tot[3];
+  MOE_TL(kTlPlan);
   const int tid = threadIdx.x, ne = d.e_eff;
   for (int e = tid; e < ne; e += 1024) {
     int r = 0;
@@ -619,6 +711,7 @@ __global__ void __launch_bounds__(1024) plan_scan_kernel(LayerDims d, int M, int
 
 // 3. Positions: offset of the expert + rank over earlier chunks + rank in chunk.
 __global__ void plan_scatter_kernel(LayerDims d, int64_t P, PlanView pv) {
+  MOE_TL(kTlPlan);
   const int64_t p = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (p >= P) return;
   const int r = pv.rank[p];
@@ -645,7 +738,7 @@ cudaError_t launch_plan(const LayerDims& d, int64_t M, const __half* x, const __
       route_given_kernel<<<(Mi + 7) / 8, 256, 0, stream>>>(d, Mi, x, w_gate, ids_user, w_user, pv);
       plan_small_kernel<<<1, 256, 0, stream>>>(d, Mi, pv, status);
     } else {
-      dim3 grid((d.E + 63) / 64, (d.H + 255) / 256);
+      dim3 grid((d.E + 63) / 64, d.H / kRsRows);
       router_small_kernel<<<grid, 256, 0, stream>>>(d, Mi, x, w_router, bias, w_gate, ids_user,
                                                      w_user, pv, status);
     }
