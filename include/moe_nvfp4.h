@@ -198,6 +198,28 @@ int32_t moe_nvfp4_forward(const moe_nvfp4_config* cfg, int64_t M, const void* x,
                           const moe_nvfp4_weights* shared13, const moe_nvfp4_weights* shared2,
                           void* y, void* ws, size_t ws_bytes, uint32_t* status, void* stream);
 
+/* moe_nvfp4_forward without a workspace argument, for callers that cannot
+ * allocate device memory (a host runtime that owns every allocation, a phase
+ * in which a framework forbids allocation, a fixed C signature with no room
+ * for a workspace).  The pages have no counterpart: this is an interface
+ * addition of this library, not a step of the method.
+ *
+ * Same arguments, results and rules as moe_nvfp4_forward, except that the
+ * workspace is a 4 MiB array inside the library (allocated when the library
+ * is loaded and held by every GPU that loads it until the process exits).
+ * Calls whose workspace would exceed it (M * k_eff * (2*I + 4*H) bytes plus
+ * alignment; e.g. M <= 16 at H 2048, I 512, top-10) return MOE_ERR_WORKSPACE
+ * and launch nothing.  The first call on a device looks the array's device
+ * address up (cudaGetSymbolAddress) with that device current; make that first
+ * call before any stream capture.  All calls share the array and it keeps the
+ * last call's contents (nothing in it needs to start at zero), so calls whose
+ * GPU work overlaps race: order them on one stream.  Allocates nothing. */
+int32_t moe_nvfp4_forward_noalloc(const moe_nvfp4_config* cfg, int64_t M, const void* x,
+                                  const void* plan, const moe_nvfp4_weights* w13,
+                                  const moe_nvfp4_weights* w2, const moe_nvfp4_weights* shared13,
+                                  const moe_nvfp4_weights* shared2, void* y, uint32_t* status,
+                                  void* stream);
+
 /* Dequantises NVFP4 matrices to FP16 (exact: every E2M1 x E4M3 product is an
  * FP16 value), applying no global scale.  q, s in `layout`; out FP16
  * [n_mats][rows][k] in canonical row order.  Same shape rules as

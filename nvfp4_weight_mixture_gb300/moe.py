@@ -35,7 +35,7 @@ DECODE_MAX_TOKENS = 16
 
 EXPORTS = ["moe_nvfp4_abi_version", "moe_nvfp4_status_string", "moe_nvfp4_query",
            "moe_nvfp4_quantize", "moe_nvfp4_plan", "moe_nvfp4_forward", "moe_nvfp4_dequantize",
-           "moe_nvfp4_set_trace_events"]
+           "moe_nvfp4_set_trace_events", "moe_nvfp4_forward_noalloc"]
 TRACE_STEPS = ("plan", "w13", "w2", "combine")
 
 
@@ -84,6 +84,8 @@ def load_library(path: str = LIB_PATH):
         lib.moe_nvfp4_plan.restype = I32
         lib.moe_nvfp4_forward.argtypes = [P, I64, P, P, P, P, P, P, P, P, SZ, P, P]
         lib.moe_nvfp4_forward.restype = I32
+        lib.moe_nvfp4_forward_noalloc.argtypes = [P, I64, P, P, P, P, P, P, P, P, P]
+        lib.moe_nvfp4_forward_noalloc.restype = I32
         lib.moe_nvfp4_set_trace_events.argtypes = [P, I32]
         lib.moe_nvfp4_set_trace_events.restype = I32
         v = lib.moe_nvfp4_abi_version()
@@ -235,6 +237,22 @@ def forward(cfg: Config, x, plan_buf, w13, w2, shared13, shared2, y, ws, status=
         ctypes.byref(cfg), M, _ptr(x), _ptr(plan_buf), ctypes.byref(a), ctypes.byref(b),
         ctypes.byref(c) if c is not None else None, ctypes.byref(d) if d is not None else None,
         _ptr(y), _ptr(ws), ws.numel(), _ptr(status), _stream()))
+
+
+def forward_noalloc(cfg: Config, x, plan_buf, w13, w2, shared13, shared2, y, status=None):
+    """moe_nvfp4_forward_noalloc: the forward with the library's own static
+    workspace (for callers that cannot allocate; see the header)."""
+    M = x.shape[0]
+    _need(x, torch.float16, "x")
+    _need(y, torch.float16, "y")
+    a = _weights_c(w13, LAYOUT_FRAGMENT_W13)
+    b = _weights_c(w2, LAYOUT_FRAGMENT)
+    c = _weights_c(shared13, LAYOUT_FRAGMENT_W13)
+    d = _weights_c(shared2, LAYOUT_FRAGMENT)
+    _check("moe_nvfp4_forward_noalloc", load_library().moe_nvfp4_forward_noalloc(
+        ctypes.byref(cfg), M, _ptr(x), _ptr(plan_buf), ctypes.byref(a), ctypes.byref(b),
+        ctypes.byref(c) if c is not None else None, ctypes.byref(d) if d is not None else None,
+        _ptr(y), _ptr(status), _stream()))
 
 
 class MoELayer:
