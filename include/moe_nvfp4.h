@@ -70,11 +70,13 @@ extern "C" {
  *   holding element 2i in its low nibble and element 2i+1 in its high nibble;
  *   s is [n_mats][rows][k/16].
  *
- * MOE_LAYOUT_FRAGMENT (1): rows % 16 == 0 and k % 64 == 0.  The matrix is cut
- *   into 16-row tiles rt and 64-element segments ks.  Tile rt, segment ks of
- *   matrix m owns the 512-byte q block at byte
- *       ((m * rows/16 + rt) * k/64 + ks) * 512
- *   and the 64-byte s block at ((m * rows/16 + rt) * k/64 + ks) * 64.
+ * MOE_LAYOUT_FRAGMENT (1): rows % 256 == 0 and k % 64 == 0.  The matrix is cut
+ *   into 16-row tiles rt (grouped 16 to a 256-row group G = rt / 16, j =
+ *   rt % 16) and 64-element segments ks.  Tile rt, segment ks of matrix m owns
+ *   the 512-byte q block number
+ *       b = ((m * rows/256 + G) * k/64 + ks) * 16 + j
+ *   (at byte 512 * b of q) and the 64-byte s block b (at byte 64 * b of s), so
+ *   the 16 tiles of a group are contiguous for each segment.
  *   For L = 4*g + c (g = 0..7, c = 0..3): q block bytes [16L, 16L+8) are row
  *   16*rt+g, elements [64*ks+16*c, +16) in canonical byte order, and bytes
  *   [16L+8, 16L+16) the same elements of row 16*rt+g+8; s block bytes 2L and
@@ -82,7 +84,7 @@ extern "C" {
  *   block with one 16-byte load per thread and holds an MMA operand fragment.
  *
  * MOE_LAYOUT_FRAGMENT_W13 (2): for a W13 matrix (rows = 2*I: rows 0..I-1 the
- *   gate projection, rows I..2I-1 the up projection; rows % 32 == 0): the
+ *   gate projection, rows I..2I-1 the up projection; rows % 256 == 0): the
  *   fragment layout of the row-permuted matrix whose tile 2j is gate rows
  *   [16j, 16j+16) and tile 2j+1 is up rows [I+16j, I+16j+16).
  *
@@ -140,7 +142,7 @@ int32_t moe_nvfp4_query(const moe_nvfp4_config* cfg, int64_t max_tokens, size_t*
  *   s = E4M3_rne_satfinite((amax_of_16_block / g) / 6),
  *   q = E2M1_rne_satfinite(x / (value(s) * g)), a zero keeping the sign of x
  *       (x / 0 is not formed: q = +-0 when value(s) * g == 0).
- * Requires k % 64 == 0, rows % 16 == 0 (rows % 32 == 0 for layout 2),
+ * Requires k % 64 == 0, rows % 16 == 0 (rows % 256 == 0 for layouts 1, 2),
  * 1 <= n_mats, rows * k < 2^31.  NaN or infinite input sets MOE_ST_NONFINITE
  * in *status and is quantised as zero.  Uses `g` as scratch while running. */
 int32_t moe_nvfp4_quantize(const float* w, int64_t n_mats, int64_t rows, int64_t k,

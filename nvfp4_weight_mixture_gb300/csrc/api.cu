@@ -109,6 +109,7 @@ int32_t cuda_status(cudaError_t e) {
 namespace moe {
 #ifdef MOE_TIMELINE
 __device__ unsigned long long g_timeline[32];
+__device__ unsigned long long g_prof[32];
 #endif
 bool trace_on() { return g_trace_events != nullptr; }
 void trace_mark(cudaStream_t stream, int step, bool end) {
@@ -139,6 +140,14 @@ int32_t moe_nvfp4_timeline_reset(void* stream) {
 }
 int32_t moe_nvfp4_timeline_read(unsigned long long* out) {
   return cuda_status(cudaMemcpyFromSymbol(out, moe::g_timeline, sizeof(unsigned long long) * 32));
+}
+int32_t moe_nvfp4_prof_read(unsigned long long* out, int reset) {
+  cudaError_t e = cudaMemcpyFromSymbol(out, moe::g_prof, sizeof(unsigned long long) * 32);
+  if (e == cudaSuccess && reset) {
+    unsigned long long z[32] = {};
+    e = cudaMemcpyToSymbol(moe::g_prof, z, sizeof(z));
+  }
+  return cuda_status(e);
 }
 #endif
 
@@ -190,7 +199,7 @@ int32_t moe_nvfp4_quantize(const float* w, int64_t n_mats, int64_t rows, int64_t
   if (layout < MOE_LAYOUT_CANONICAL || layout > MOE_LAYOUT_FRAGMENT_W13) return MOE_ERR_LAYOUT;
   if (n_mats < 1 || n_mats > 65535 || rows < 16 || k < 64) return MOE_ERR_SHAPE;
   if (k % 64 || rows % 16) return MOE_ERR_SHAPE;
-  if (layout == MOE_LAYOUT_FRAGMENT_W13 && rows % 32) return MOE_ERR_SHAPE;
+  if (layout != MOE_LAYOUT_CANONICAL && rows % 256) return MOE_ERR_SHAPE;
   if (rows * k >= (int64_t(1) << 31)) return MOE_ERR_SHAPE;
   if (!aligned16(w) || !aligned16(q) || !aligned16(s) || !aligned16(g)) return MOE_ERR_ALIGNMENT;
   if (status && (reinterpret_cast<uintptr_t>(status) & 3u)) return MOE_ERR_ALIGNMENT;
@@ -206,7 +215,7 @@ int32_t moe_nvfp4_dequantize(const uint8_t* q, const uint8_t* s, int64_t n_mats,
   if (!q || !s || !out) return MOE_ERR_INVALID_ARG;
   if (layout < MOE_LAYOUT_CANONICAL || layout > MOE_LAYOUT_FRAGMENT_W13) return MOE_ERR_LAYOUT;
   if (n_mats < 1 || rows < 16 || k < 64 || k % 64 || rows % 16) return MOE_ERR_SHAPE;
-  if (layout == MOE_LAYOUT_FRAGMENT_W13 && rows % 32) return MOE_ERR_SHAPE;
+  if (layout != MOE_LAYOUT_CANONICAL && rows % 256) return MOE_ERR_SHAPE;
   if (n_mats * rows * k >= (int64_t(1) << 40)) return MOE_ERR_SHAPE;
   if (!aligned16(q) || !aligned16(s) || !aligned16(out)) return MOE_ERR_ALIGNMENT;
   int sms = 0;

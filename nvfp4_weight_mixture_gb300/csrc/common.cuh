@@ -135,10 +135,14 @@ struct TlScope {
 };
 #define MOE_TL(slot) ::moe::TlScope tl_scope_(slot)
 #define MOE_TL_WAITED() tl_scope_.waited()
+// per-role cycle accounting of the grouped GEMM (summed over blocks)
+extern __device__ unsigned long long g_prof[32];
+#define MOE_PROF(stmt) stmt
 // raw stamps on timeline cells 20..31 (earliest / latest over the threads that pass)
 #define MOE_TL_MIN(cell) atomicMin(&::moe::g_timeline[cell], (unsigned long long)::moe::globaltimer())
 #define MOE_TL_MAX(cell) atomicMax(&::moe::g_timeline[cell], (unsigned long long)::moe::globaltimer())
 #else
+#define MOE_PROF(stmt)
 #define MOE_TL_MIN(cell) \
   do {                   \
   } while (0)

@@ -79,9 +79,11 @@ __global__ void __launch_bounds__(256, 3) decode_w13_kernel(LayerDims d, PlanVie
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, t4 = lane & 3;
   const int S = H / 64;
-  // gate tile 2*rp and up tile 2*rp+1 are adjacent in the W13 fragment layout
-  const uint8_t* qt = qe + (size_t)(2 * rp) * S * 512;
-  const uint8_t* st = se + (size_t)(2 * rp) * S * 64;
+  // gate tile 2*rp and up tile 2*rp+1: tiles j0, j0 + 1 of 256-row group rp / 8;
+  // block (tile j, segment ks) of a group is number ks * 16 + j within it
+  const int j0 = 2 * (rp & 7);
+  const uint8_t* qt = qe + (size_t)(rp >> 3) * S * 16 * 512 + j0 * 512;
+  const uint8_t* st = se + (size_t)(rp >> 3) * S * 16 * 64 + j0 * 64;
   const int xstride = H * 2 + 16;
   const int cpr = H / 8;  // 16-byte chunks per row
   if (tid == 0) {
@@ -104,8 +106,8 @@ __global__ void __launch_bounds__(256, 3) decode_w13_kernel(LayerDims d, PlanVie
       if (ks < S) {
 #pragma unroll
         for (int tt = 0; tt < 2; ++tt) {
-          qv[j][tt] = ldg_nc_v4(qt + ((size_t)tt * S + ks) * 512 + lane * 16);
-          sv[j][tt] = ldg_u16(st + ((size_t)tt * S + ks) * 64 + lane * 2);
+          qv[j][tt] = ldg_nc_v4(qt + ((size_t)ks * 16 + tt) * 512 + lane * 16);
+          sv[j][tt] = ldg_u16(st + ((size_t)ks * 16 + tt) * 64 + lane * 2);
         }
       }
     }
@@ -240,9 +242,9 @@ __global__ void __launch_bounds__(256) decode_w2_kernel(LayerDims d, PlanView pv
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, t4 = lane & 3;
   const int S = I / 64;
-  const int rt = hb * 8 + warp;
-  const uint8_t* qt = qe + (size_t)rt * S * 512;
-  const uint8_t* st = se + (size_t)rt * S * 64;
+  const int rt = hb * 8 + warp;  // tile rt % 16 of 256-row group rt / 16
+  const uint8_t* qt = qe + (size_t)(rt >> 4) * S * 16 * 512 + (rt & 15) * 512;
+  const uint8_t* st = se + (size_t)(rt >> 4) * S * 16 * 64 + (rt & 15) * 64;
   const int hstride = I * 2 + 16;
   const int cpr = I / 8;
 
@@ -252,8 +254,8 @@ __global__ void __launch_bounds__(256) decode_w2_kernel(LayerDims d, PlanView pv
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       if (ks0 + j < S) {
-        qv[j] = ldg_nc_v4(qt + (size_t)(ks0 + j) * 512 + lane * 16);
-        sv[j] = ldg_u16(st + (size_t)(ks0 + j) * 64 + lane * 2);
+        qv[j] = ldg_nc_v4(qt + (size_t)(ks0 + j) * 16 * 512 + lane * 16);
+        sv[j] = ldg_u16(st + (size_t)(ks0 + j) * 16 * 64 + lane * 2);
       }
     }
   };

@@ -3,20 +3,27 @@
 //
 // "[Kernel][SM70] Improve Qwen3.8 no-MTP concurrency", section "Scope and
 // related PRs": grouped W13 with SwiGLU and grouped W2 with the reduction,
-// both driven by the same integer plan.  Here each block takes one plan tile
-// (one expert, up to 256 of its routed rows) and 256 weight rows:
+// both driven by the same integer plan.  A work unit is one plan tile (one
+// expert, up to 256 of its routed rows) times 256 weight rows:
 //
 //   D[weight row][token] = sum_k W[weight row][k] * X[token][k]     (swap-AB)
 //
-// so the weight rows are the MMA's M = 128 (two accumulators) and the tokens
-// are N <= 256.  Warp roles:
-//   warps 0-3  dequantise NVFP4 weight blocks (fragment layout, 16-byte loads)
-//              to FP16 in 128-byte-swizzled K-major shared tiles, then run the
-//              epilogue (TMEM -> registers);
-//   warps 4-7  gather the tile's token rows with 16-byte cp.async into the
-//              same swizzled layout;
-//   warp 8     allocates tensor memory, and one lane issues the MMAs.
-// A 3-stage ring of (A0, A1, B) tiles of K = 64 is synchronised with mbarriers.
+// so the weight rows are the MMA's M = 128 (two accumulators of N <= 256
+// columns fill the 512 tensor-memory columns) and the tokens are N.  Blocks
+// are persistent (one per SM) and walk the units with a static stride.
+// Warp roles, each running ahead as far as its ring allows:
+//   warp 9     one lane streams the unit's raw NVFP4 blocks (fragment layout:
+//              16 blocks of 512 + 64 bytes per K step of 64) into a 6-deep
+//              shared ring with two bulk asynchronous copies per K step;
+//   warps 0-3  dequantise each raw stage into 128-byte-swizzled K-major FP16
+//              A tiles (2-deep ring), then run the unit's epilogue;
+//   warps 4-7  gather the unit's token rows with 16-byte cp.async into the
+//              same swizzled layout, in chunks of 64 rows (a 12-slot ring);
+//              warp 4 + (c % 4) owns chunk c and keeps two of its own chunks
+//              in flight, so up to eight chunks load ahead of the MMAs;
+//   warp 8     allocates tensor memory; one lane issues the MMAs: per K step and
+//              A tile one MMA with N = all of the tile's rows, split in two only
+//              where the step's chunks wrap around the end of the B ring.
 //
 // W13: the fragment layout interleaves 16-row gate and up tiles, so TMEM lanes
 // [32q, 32q+16) hold gate rows and [32q+16, 32q+32) the matching up rows; the
@@ -25,35 +32,48 @@
 // FP32 partial row of each pair; a separate pass sums the slots in order.
 #include <math.h>
 
+#include <algorithm>
+
 #include "common.cuh"
 #include "kernels.h"
 
 namespace moe {
 
-constexpr int kStages = 3;
-constexpr int kBK = 64;                       // K per stage (128 bytes of FP16)
-constexpr int kATile = 128 * 128;             // one 128-row A tile, bytes
-constexpr int kBTile = kTileRows * 128;       // the B tile, bytes
-constexpr int kStageBytes = 2 * kATile + kBTile;
-constexpr int kGemmThreads = 288;
+constexpr int kBK = 64;                   // K per step (128 bytes of FP16)
+constexpr int kATile = 128 * 128;         // one 128-row FP16 A tile, bytes
+constexpr int kBTile = kTileRows * 128;   // the B tile, bytes
+constexpr int kAS = 2;                    // A (dequantised) stages
+constexpr int kBChunkRows = 64;           // B ring slot: 64 token rows x 128 bytes
+constexpr int kBChunk = kBChunkRows * 128;
+constexpr int kBSlots = 12;               // B ring slots (96 KiB)
+constexpr int kRS = 5;                    // raw weight stages
+constexpr int kRawQ = 16 * 512;           // raw q bytes per K step (16 fragment blocks)
+constexpr int kRawBytes = kRawQ + 16 * 64;
+constexpr int kGemmThreads = 320;
 constexpr int kTmemCols = 512;
+constexpr int kOffA = 0;
+constexpr int kOffB = kOffA + kAS * 2 * kATile;
+constexpr int kOffRaw = kOffB + kBSlots * kBChunk;
+constexpr int kOffMeta = kOffRaw + kRS * kRawBytes;
 
 struct GemmSmem {
-  uint64_t full_a[kStages];
-  uint64_t full_b[kStages];
-  uint64_t empty[kStages];
-  uint64_t accf;
+  uint64_t raw_full[kRS], raw_empty[kRS];
+  uint64_t a_full[kAS], a_empty[kAS];
+  uint64_t b_full[kBSlots], b_empty[kBSlots];
+  uint64_t accf, tmem_empty, drain;
   uint32_t tmem;
   int abort;
-  int ep_ok;    // epilogue go/no-go, sampled once
-  int rows;     // rows of this tile
-  int pos0;     // plan position of the tile's first row
-  int src[kTileRows];   // W13: token of each row; W2: pair id of each row
-  float wsc[kTileRows]; // W2: g2 * combine weight of each row
+  int n_units;
+  int bsrc[2][kTileRows];    // B warps: token (W13) of each row, by unit parity
+  int epair[2][kTileRows];   // epilogue (W2): pair id of each row
+  float ewsc[2][kTileRows];  // epilogue (W2): g2 * combine weight of each row
+  // epilogue staging, 2 KiB per warp: W13 h values [32 tokens][16 i] (FP16),
+  // W2 partial values [16 pairs][32 rows] (FP32)
+  __align__(16) float stage[4][512];
 };
 
 constexpr size_t gemm_smem_bytes() {
-  return 1024 /* alignment slack */ + (size_t)kStages * kStageBytes + sizeof(GemmSmem);
+  return 1024 /* alignment slack */ + (size_t)kOffMeta + sizeof(GemmSmem);
 }
 
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, uint32_t* status,
@@ -76,6 +96,41 @@ __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
+// Profiling cells (timeline build): [0..3] raw producer wait/issue, [4..7]
+// MMA wait-A / wait-B / issue / wait-TMEM, [8..9] B wait/issue, [10..14]
+// dequant wait-raw / wait-A / work, epilogue wait / work; [16 + 2k] = calls.
+#ifdef MOE_TIMELINE
+#define PROF_ADD(cell, t0) atomicAdd(&g_prof[cell], (unsigned long long)(clock64() - (t0)))
+#else
+#define PROF_ADD(cell, t0)
+#endif
+
+struct Unit {
+  int e, rows, npad, sub, pos0;
+  const uint8_t* q;  // the expert's q bytes
+  const uint8_t* s;  // the expert's s bytes
+  float g;
+};
+
+template <bool kW13>
+__device__ __forceinline__ Unit load_unit(const LayerDims& d, const PlanView& pv, Weights w,
+                                          Weights ws, int u, int upt) {
+  Unit un;
+  const int tile = u / upt;
+  un.sub = u - tile * upt;
+  const int4 tl = __ldcg(reinterpret_cast<const int4*>(pv.tiles) + tile);
+  un.e = tl.x;
+  un.rows = tl.z;
+  un.npad = (tl.z + 15) & ~15;
+  un.pos0 = __ldcg(pv.offsets + tl.x) + tl.y;
+  const bool sh = (un.e == d.E);
+  const size_t mat_q = kW13 ? (size_t)d.I * d.H : (size_t)d.H * d.I / 2;
+  un.q = sh ? ws.q : w.q + (size_t)un.e * mat_q;
+  un.s = sh ? ws.s : w.s + (size_t)un.e * mat_q / 8;
+  un.g = sh ? ws.g[0] : w.g[un.e];
+  return un;
+}
+
 template <bool kW13>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     grouped_gemm_kernel(LayerDims d, PlanView pv, const __half* __restrict__ bsrc, Weights w,
@@ -84,239 +139,352 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   extern __shared__ __align__(1024) char smem_raw[];
   char* base = reinterpret_cast<char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                        ~uintptr_t(1023));
-  GemmSmem* sm = reinterpret_cast<GemmSmem*>(base + (size_t)kStages * kStageBytes);
+  GemmSmem* sm = reinterpret_cast<GemmSmem*>(base + kOffMeta);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-
-  // ---- work unit ------------------------------------------------------------
-  const int K = kW13 ? d.H : d.I;            // reduction length
-  const int S = K / kBK;                      // k-steps
-  const int units_per_tile = kW13 ? (2 * d.I) / 256 : d.H / 256;
   MOE_TL(kW13 ? kTlW13 : kTlW2);
-  pdl_wait();
-  MOE_TL_WAITED();
-  const int n_tiles = __ldcg(&pv.hdr->n_tiles);
-  const int tile = blockIdx.x / units_per_tile;
-  const int u = blockIdx.x - tile * units_per_tile;
-  if (tile >= n_tiles) return;
-  const int4 tl = __ldcg(reinterpret_cast<const int4*>(pv.tiles) + tile);
-  const int e = tl.x, r0 = tl.y, rows = tl.z;
-  const int npad = (rows + 15) & ~15;
-  const bool sh = (e == d.E);
-  const size_t mat_q = kW13 ? (size_t)d.I * d.H : (size_t)d.H * d.I / 2;
-  const uint8_t* qe = sh ? ws.q : w.q + (size_t)e * mat_q;
-  const uint8_t* se = sh ? ws.s : w.s + (size_t)e * mat_q / 8;
-  const float gsc = sh ? ws.g[0] : w.g[e];
+  MOE_PROF(constexpr int poff = kW13 ? 0 : 16);
+
+  const int K = kW13 ? d.H : d.I;           // reduction length
+  const int S = K / kBK;                     // K steps per unit
+  const int upt = kW13 ? (2 * d.I) / 256 : d.H / 256;  // units per plan tile
 
   if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(&sm->full_a[s], 128);
-      mbar_init(&sm->full_b[s], 128);
-      mbar_init(&sm->empty[s], 1);
+    for (int i = 0; i < kRS; ++i) {
+      mbar_init(&sm->raw_full[i], 1);
+      mbar_init(&sm->raw_empty[i], 128);
+    }
+    for (int i = 0; i < kAS; ++i) {
+      mbar_init(&sm->a_full[i], 128);
+      mbar_init(&sm->a_empty[i], 1);
+    }
+    for (int i = 0; i < kBSlots; ++i) {
+      mbar_init(&sm->b_full[i], 32);   // the one gather warp that owns the chunk
+      mbar_init(&sm->b_empty[i], 1);
     }
     mbar_init(&sm->accf, 1);
+    mbar_init(&sm->tmem_empty, 128);
+    mbar_init(&sm->drain, 1);
     sm->abort = 0;
-    sm->rows = rows;
-    sm->pos0 = __ldcg(pv.offsets + e) + r0;
     fence_mbar_init();
   }
   if (warp == 8) tmem_alloc(&sm->tmem, kTmemCols);
-  __syncthreads();
-  if (tid >= 128 && tid < 256) {
-    for (int n = tid - 128; n < rows; n += 128) {
-      const int pair = __ldcg(pv.perm + sm->pos0 + n);
-      sm->src[n] = kW13 ? pair / d.k_eff : pair;
-      if (!kW13) sm->wsc[n] = gsc * __ldcg(pv.w + pair);
-    }
-  }
+  // everything above is independent of the previous grid's results
+  pdl_wait();
+  MOE_TL_WAITED();
+  if (tid == 0) sm->n_units = __ldcg(&pv.hdr->n_tiles) * upt;
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = sm->tmem;
+  const int n_units = sm->n_units;
   volatile int* abort = &sm->abort;
 
-  if (warp < 4) {
-    // ---- dequantising producer: 16 fragment blocks (2 A tiles x 8) per stage,
-    //      4 per warp; raw bytes of the next stage are loaded ahead.
-    const int g = lane >> 2, c = lane & 3;
-    // packed row tile of block j of this warp: A tile at = j / 8 (j = 4w + jj)
-    auto blk_q = [&](int jj, int ks) -> const uint8_t* {
-      const int j = warp * 4 + jj;
-      const int rt = u * 16 + j;  // A tile j/8, local tile j%8
-      return qe + ((size_t)rt * S + ks) * 512 + lane * 16;
-    };
-    auto blk_s = [&](int jj, int ks) -> const uint8_t* {
-      const int j = warp * 4 + jj;
-      const int rt = u * 16 + j;
-      return se + ((size_t)rt * S + ks) * 64 + lane * 2;
-    };
-    uint4 qn[4];
-    uint32_t sn[4];
-#pragma unroll
-    for (int jj = 0; jj < 4; ++jj) {
-      qn[jj] = ldg_nc_v4(blk_q(jj, 0));
-      sn[jj] = __ldg(reinterpret_cast<const unsigned short*>(blk_s(jj, 0)));
-    }
-    for (int ks = 0; ks < S; ++ks) {
-      const int st = ks % kStages;
-      uint4 qc[4];
-      uint32_t sc[4];
-#pragma unroll
-      for (int jj = 0; jj < 4; ++jj) {
-        qc[jj] = qn[jj];
-        sc[jj] = sn[jj];
+  if (warp == 9) {
+    // ---- raw weight producer (one lane) ---------------------------------------
+    if (lane == 0) {
+      uint32_t kr = 0;
+      for (int u = blockIdx.x; u < n_units && !*abort; u += gridDim.x) {
+        const Unit un = load_unit<kW13>(d, pv, w, ws, u, upt);
+        const int grp = un.sub;  // the unit's 256 weight rows are one fragment group
+        bool ok = true;
+        for (int ks = 0; ks < S; ++ks) {
+          const int slot = kr % kRS;
+          MOE_PROF(long long t0 = clock64());
+          if (!wait_or_abort(&sm->raw_empty[slot], ((kr / kRS) & 1) ^ 1, status, abort)) {
+            ok = false;
+            break;
+          }
+          MOE_PROF(PROF_ADD(poff + 0, t0); t0 = clock64());
+          char* dst = base + kOffRaw + slot * kRawBytes;
+          mbar_expect_tx(&sm->raw_full[slot], kRawBytes);
+          // the group's 16 tiles are contiguous for each segment: two copies
+          const size_t blk = ((size_t)grp * S + ks) * 16;
+          bulk_g2s(dst, un.q + blk * 512, kRawQ, &sm->raw_full[slot]);
+          bulk_g2s(dst + kRawQ, un.s + blk * 64, kRawBytes - kRawQ, &sm->raw_full[slot]);
+          MOE_PROF(PROF_ADD(poff + 1, t0));
+          ++kr;
+        }
+        if (!ok) break;
       }
-      if (ks + 1 < S) {
+      // copies still in flight must land before the block exits: wait for the
+      // most recent stages (consumed ones completed long ago)
+      for (uint32_t k = (kr > (uint32_t)kRS ? kr - kRS : 0); k < kr; ++k)
+        wait_or_abort(&sm->raw_full[k % kRS], (k / kRS) & 1, status, abort);
+    }
+  } else if (warp == 8) {
+    // ---- MMA issuer (one lane) --------------------------------------------------
+    if (lane == 0) {
+      uint32_t ka = 0, kc = 0, it = 0;
+      for (int u = blockIdx.x; u < n_units && !*abort; u += gridDim.x, ++it) {
+        const Unit un = load_unit<kW13>(d, pv, w, ws, u, upt);
+        const int nch = (un.npad + kBChunkRows - 1) / kBChunkRows;
+        MOE_PROF(long long t0 = clock64());
+        if (it > 0 && !wait_or_abort(&sm->tmem_empty, (it - 1) & 1, status, abort)) break;
+        MOE_PROF(PROF_ADD(poff + 7, t0));
+        tc_fence_after();
+        bool ok = true;
+        for (int ks = 0; ks < S && ok; ++ks, ++ka) {
+          const int as = ka % kAS;
+          MOE_PROF(t0 = clock64());
+          if (!wait_or_abort(&sm->a_full[as], (ka / kAS) & 1, status, abort)) {
+            ok = false;
+            break;
+          }
+          MOE_PROF(PROF_ADD(poff + 4, t0));
+          tc_fence_after();
+          const uint64_t da0 = sdesc_sw128(smem_u32(base + kOffA + as * 2 * kATile));
+          const uint64_t da1 = sdesc_sw128(smem_u32(base + kOffA + as * 2 * kATile + kATile));
+          // the step's chunks in runs of contiguous ring slots (at most two)
+          int ch = 0;
+          while (ch < nch && ok) {
+            const int slot0 = kc % kBSlots;
+            const int run = min(nch - ch, kBSlots - slot0);
+            MOE_PROF(t0 = clock64());
+            for (int r = 0; r < run; ++r) {
+              const uint32_t kcr = kc + r;
+              if (!wait_or_abort(&sm->b_full[kcr % kBSlots], (kcr / kBSlots) & 1, status, abort)) {
+                ok = false;
+                break;
+              }
+            }
+            if (!ok) break;
+            MOE_PROF(PROF_ADD(poff + 5, t0); t0 = clock64());
+            tc_fence_after();
+            const int n = min(run * kBChunkRows, un.npad - ch * kBChunkRows);
+            const uint32_t idesc = idesc_f16_f32(128, n);
+            const uint64_t db = sdesc_sw128(smem_u32(base + kOffB + slot0 * kBChunk));
+            const uint32_t col = ch * kBChunkRows;
 #pragma unroll
-        for (int jj = 0; jj < 4; ++jj) {
-          qn[jj] = ldg_nc_v4(blk_q(jj, ks + 1));
-          sn[jj] = __ldg(reinterpret_cast<const unsigned short*>(blk_s(jj, ks + 1)));
+            for (int kk = 0; kk < kBK / 16; ++kk) {
+              const uint32_t acc = (ks | kk) ? 1u : 0u;
+              // +32 bytes along K inside the 128-byte swizzle atom: start address + 2
+              tc_mma_f16(tmem + col, da0 + 2 * kk, db + 2 * kk, idesc, acc);
+              tc_mma_f16(tmem + 256 + col, da1 + 2 * kk, db + 2 * kk, idesc, acc);
+            }
+            for (int r = 0; r < run; ++r) tc_commit(&sm->b_empty[(kc + r) % kBSlots]);
+            MOE_PROF(PROF_ADD(poff + 6, t0));
+            kc += run;
+            ch += run;
+          }
+          if (ok) tc_commit(&sm->a_empty[as]);
+        }
+        if (!ok) break;
+        tc_commit(&sm->accf);
+      }
+      // every MMA issued has completed before tensor memory is released
+      tc_commit(&sm->drain);
+      const uint64_t t0 = globaltimer();
+      while (!mbar_try_wait(&sm->drain, 0) && globaltimer() - t0 < kWaitTimeoutNs) {
+      }
+    }
+  } else if (warp >= 4) {
+    // ---- B producer: gather the unit's rows with cp.async -------------------------
+    // Chunk kc (64 rows of one K step) belongs to warp 4 + kc % 4.  A warp
+    // announces its chunk j once chunk j + 2 is issued (its own two-deep
+    // cp.async window), after its copies landed and were fenced for tcgen05.
+    const int bw = warp - 4;
+    uint32_t kc = 0, it = 0;
+    uint32_t pend[3];  // this warp's chunk slots not yet announced (oldest first)
+    int npend = 0;
+    for (int u = blockIdx.x; u < n_units && !*abort; u += gridDim.x, ++it) {
+      const Unit un = load_unit<kW13>(d, pv, w, ws, u, upt);
+      int* src = sm->bsrc[it & 1];
+      if (kW13)
+        for (int n = tid - 128; n < un.rows; n += 128)
+          src[n] = __ldcg(pv.perm + un.pos0 + n) / d.k_eff;
+      named_bar_sync(2, 128);
+      const int nch = (un.npad + kBChunkRows - 1) / kBChunkRows;
+      bool ok = true;
+      for (int ks = 0; ks < S && ok; ++ks) {
+        for (int ch = 0; ch < nch; ++ch, ++kc) {
+          if ((int)(kc & 3) != bw) continue;
+          const int bs = kc % kBSlots;
+          MOE_PROF(long long t0 = clock64());
+          if (!wait_or_abort(&sm->b_empty[bs], ((kc / kBSlots) & 1) ^ 1, status, abort)) {
+            ok = false;
+            break;
+          }
+          MOE_PROF(if (lane == 0) PROF_ADD(poff + 8, t0); t0 = clock64());
+          const uint32_t bt = smem_u32(base + kOffB + bs * kBChunk);
+          const int r0 = ch * kBChunkRows;
+          const int rows = min(kBChunkRows, un.npad - r0);
+#pragma unroll 4
+          for (int i = lane; i < rows * 8; i += 32) {
+            const int n = i >> 3, c = i & 7;
+            const int row = r0 + n;
+            const bool in = row < un.rows;
+            const __half* p;
+            if (kW13)
+              p = bsrc + (int64_t)(in ? src[row] : 0) * d.H + ks * kBK + c * 8;
+            else
+              p = bsrc + (int64_t)(in ? un.pos0 + row : 0) * d.I + ks * kBK + c * 8;
+            cp_async16(bt + sw128_off(n, c), p, in ? 16u : 0u);
+          }
+          cp_async_commit();
+          pend[npend++] = bs;
+          if (npend == 3) {
+            cp_async_wait<2>();
+            fence_proxy_async();
+            mbar_arrive(&sm->b_full[pend[0]]);
+            pend[0] = pend[1];
+            pend[1] = pend[2];
+            npend = 2;
+          }
+          MOE_PROF(if (lane == 0) PROF_ADD(poff + 9, t0));
         }
       }
-      if (!wait_or_abort(&sm->empty[st], ((ks / kStages) & 1) ^ 1, status, abort)) break;
-      char* stage = base + (size_t)st * kStageBytes;
-#pragma unroll
-      for (int jj = 0; jj < 4; ++jj) {
-        const int j = warp * 4 + jj;
-        char* at = stage + (j >> 3) * kATile;
-        const int r = (j & 7) * 16 + g;
-        const uint32_t f = e4m3x2_to_f16x2(sc[jj]);
-        const uint32_t sg = __byte_perm(f, f, 0x1010), sg8 = __byte_perm(f, f, 0x3232);
-        uint32_t o[4];
-        dequant8(qc[jj].x, sg, o);
-        *reinterpret_cast<uint4*>(at + sw128_off(r, 2 * c)) = make_uint4(o[0], o[1], o[2], o[3]);
-        dequant8(qc[jj].y, sg, o);
-        *reinterpret_cast<uint4*>(at + sw128_off(r, 2 * c + 1)) =
-            make_uint4(o[0], o[1], o[2], o[3]);
-        dequant8(qc[jj].z, sg8, o);
-        *reinterpret_cast<uint4*>(at + sw128_off(r + 8, 2 * c)) =
-            make_uint4(o[0], o[1], o[2], o[3]);
-        dequant8(qc[jj].w, sg8, o);
-        *reinterpret_cast<uint4*>(at + sw128_off(r + 8, 2 * c + 1)) =
-            make_uint4(o[0], o[1], o[2], o[3]);
-      }
-      fence_proxy_async();
-      mbar_arrive(&sm->full_a[st]);
-    }
-  } else if (warp < 8) {
-    // ---- B producer: gather rows with cp.async; stage ks is announced once
-    //      the copies of ks have landed (two stages kept in flight).
-    const int t = tid - 128;
-    const int chunks = npad * 8;
-    int issued = 0, announced = 0;
-    bool ok = true;
-    for (int ks = 0; ks < S && ok; ++ks) {
-      const int st = ks % kStages;
-      if (!wait_or_abort(&sm->empty[st], ((ks / kStages) & 1) ^ 1, status, abort)) {
-        ok = false;
-        break;
-      }
-      const uint32_t bt = smem_u32(base + (size_t)st * kStageBytes + 2 * kATile);
-      for (int i = t; i < chunks; i += 128) {
-        const int n = i >> 3, c = i & 7;
-        const bool in = n < rows;
-        const __half* src;
-        if (kW13)
-          src = bsrc + (int64_t)(in ? sm->src[n] : 0) * d.H + ks * kBK + c * 8;
-        else
-          src = bsrc + (int64_t)(in ? sm->pos0 + n : 0) * d.I + ks * kBK + c * 8;
-        cp_async16(bt + sw128_off(n, c), src, in ? 16u : 0u);
-      }
-      cp_async_commit();
-      ++issued;
-      if (issued - announced > 2) {
-        cp_async_wait<2>();
-        fence_proxy_async();
-        mbar_arrive(&sm->full_b[announced % kStages]);
-        ++announced;
-      }
+      // the row list of this parity is rewritten two units later
+      named_bar_sync(2, 128);
+      if (!ok) break;
     }
     cp_async_wait<0>();
     fence_proxy_async();
-    for (; announced < issued; ++announced) mbar_arrive(&sm->full_b[announced % kStages]);
-  } else if (lane == 0) {
-    // ---- MMA issuer
-    const uint32_t idesc = idesc_f16_f32(128, npad);
-    for (int ks = 0; ks < S; ++ks) {
-      const int st = ks % kStages;
-      const uint32_t par = (ks / kStages) & 1;
-      if (!wait_or_abort(&sm->full_a[st], par, status, abort)) break;
-      if (!wait_or_abort(&sm->full_b[st], par, status, abort)) break;
-      tc_fence_after();
-      const uint32_t a0 = smem_u32(base + (size_t)st * kStageBytes);
-      const uint32_t a1 = a0 + kATile;
-      const uint32_t b0 = a0 + 2 * kATile;
-#pragma unroll
-      for (int kk = 0; kk < kBK / 16; ++kk) {
-        const uint32_t acc = (ks | kk) ? 1u : 0u;
-        tc_mma_f16(tmem, sdesc_sw128(a0 + kk * 32), sdesc_sw128(b0 + kk * 32), idesc, acc);
-        tc_mma_f16(tmem + 256, sdesc_sw128(a1 + kk * 32), sdesc_sw128(b0 + kk * 32), idesc, acc);
+    for (int i = 0; i < npend; ++i) mbar_arrive(&sm->b_full[pend[i]]);
+  } else {
+    // ---- warps 0-3: dequantise, then the unit's epilogue ---------------------------
+    const int g = lane >> 2, c = lane & 3;
+    uint32_t kd = 0, it = 0;
+    for (int u = blockIdx.x; u < n_units && !*abort; u += gridDim.x, ++it) {
+      const Unit un = load_unit<kW13>(d, pv, w, ws, u, upt);
+      if (!kW13) {
+        for (int n = tid; n < un.rows; n += 128) {
+          const int pair = __ldcg(pv.perm + un.pos0 + n);
+          sm->epair[it & 1][n] = pair;
+          sm->ewsc[it & 1][n] = un.g * __ldcg(pv.w + pair);
+        }
       }
-      tc_commit(&sm->empty[st]);
-    }
-    tc_commit(&sm->accf);
-  }
-
-  // ---- epilogue (warps 0-3: TMEM lanes 32*warp .. +31) -----------------------
-  if (warp < 4) {
-    wait_or_abort(&sm->accf, 0, status, abort);
-    named_bar_sync(1, 128);
-    if (tid == 0) sm->ep_ok = !*abort;
-    named_bar_sync(1, 128);
-    tc_fence_after();
-    if (sm->ep_ok) {
+      bool ok = true;
+      for (int ks = 0; ks < S; ++ks, ++kd) {
+        const int rs = kd % kRS, as = kd % kAS;
+        MOE_PROF(long long t0 = clock64());
+        if (!wait_or_abort(&sm->raw_full[rs], (kd / kRS) & 1, status, abort)) {
+          ok = false;
+          break;
+        }
+        MOE_PROF(if (tid == 0) PROF_ADD(poff + 10, t0); t0 = clock64());
+        if (!wait_or_abort(&sm->a_empty[as], ((kd / kAS) & 1) ^ 1, status, abort)) {
+          ok = false;
+          break;
+        }
+        MOE_PROF(if (tid == 0) PROF_ADD(poff + 11, t0); t0 = clock64());
+        const char* raw = base + kOffRaw + rs * kRawBytes;
+        char* stage = base + kOffA + as * 2 * kATile;
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+          const int j = warp * 4 + jj;  // fragment block: A tile j / 8, local row tile j % 8
+          const uint4 q = *reinterpret_cast<const uint4*>(raw + j * 512 + lane * 16);
+          const uint32_t sc =
+              *reinterpret_cast<const unsigned short*>(raw + kRawQ + j * 64 + lane * 2);
+          char* at = stage + (j >> 3) * kATile;
+          const int r = (j & 7) * 16 + g;
+          const uint32_t f = e4m3x2_to_f16x2(sc);
+          const uint32_t sg = __byte_perm(f, f, 0x1010), sg8 = __byte_perm(f, f, 0x3232);
+          uint32_t o[4];
+          dequant8(q.x, sg, o);
+          *reinterpret_cast<uint4*>(at + sw128_off(r, 2 * c)) = make_uint4(o[0], o[1], o[2], o[3]);
+          dequant8(q.y, sg, o);
+          *reinterpret_cast<uint4*>(at + sw128_off(r, 2 * c + 1)) =
+              make_uint4(o[0], o[1], o[2], o[3]);
+          dequant8(q.z, sg8, o);
+          *reinterpret_cast<uint4*>(at + sw128_off(r + 8, 2 * c)) =
+              make_uint4(o[0], o[1], o[2], o[3]);
+          dequant8(q.w, sg8, o);
+          *reinterpret_cast<uint4*>(at + sw128_off(r + 8, 2 * c + 1)) =
+              make_uint4(o[0], o[1], o[2], o[3]);
+        }
+        fence_proxy_async();
+        mbar_arrive(&sm->a_full[as]);
+        mbar_arrive(&sm->raw_empty[rs]);
+        MOE_PROF(if (tid == 0) PROF_ADD(poff + 12, t0));
+      }
+      if (!ok) break;
+      // ---- epilogue of this unit (TMEM lanes 32*warp .. +31) ----
+      named_bar_sync(1, 128);  // epair / ewsc of this unit visible to all four warps
+      MOE_PROF(long long te = clock64());
+      if (!wait_or_abort(&sm->accf, it & 1, status, abort)) break;
+      MOE_PROF(if (tid == 0) PROF_ADD(poff + 13, te); te = clock64());
+      tc_fence_after();
       if (kW13) {
-        // h staging: [rows][128 i-values] FP16, 272-byte rows, in the dead ring
-        __half* hs = reinterpret_cast<__half*>(base);
-        const int hst = 136;
+        // Lane r < 16 of warp q holds gate row (16q + r) and lane r + 16 the
+        // matching up row, for 32 token columns per load.  One exchange per
+        // pair of columns gives each lane 16 (G, U) pairs: gate lanes take
+        // columns 0-15, up lanes 16-31.  h goes through a per-warp staging
+        // tile so that each token row leaves as two 16-byte stores.
+        const int I = d.I;
         const int r16 = lane & 15;
         const bool is_gate = lane < 16;
+        __half(*stg)[16] = reinterpret_cast<__half(*)[16]>(sm->stage[warp]);
 #pragma unroll 1
         for (int at = 0; at < 2; ++at) {
-          const int il = at * 64 + warp * 16 + r16;
+          const int i0 = un.sub * 128 + at * 64 + warp * 16;
 #pragma unroll 1
-          for (int c0 = 0; c0 < npad; c0 += 32) {
+          for (int c0 = 0; c0 < un.npad; c0 += 32) {
             uint32_t v[32];
             tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + at * 256 + c0, v);
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              const float mine = __uint_as_float(v[j]);
-              const float other = __shfl_xor_sync(0xffffffffu, mine, 16);
-              // gate lanes take columns 0..15, up lanes 16..31
-              const bool take = is_gate ? (j < 16) : (j >= 16);
-              if (take) {
-                const float G = (is_gate ? mine : other) * gsc;
-                const float U = (is_gate ? other : mine) * gsc;
-                const int n = c0 + j;
-                if (n < rows) hs[n * hst + il] = __float2half_rn(G / (1.f + expf(-G)) * U);
-              }
+            for (int jj = 0; jj < 16; ++jj) {
+              const float lo = __uint_as_float(v[jj]), hi = __uint_as_float(v[jj + 16]);
+              const float recv = __shfl_xor_sync(0xffffffffu, is_gate ? hi : lo, 16);
+              const float G = (is_gate ? lo : recv) * un.g;
+              const float U = (is_gate ? recv : hi) * un.g;
+              const float hv = __fdividef(G, 1.f + __expf(-G)) * U;
+              stg[is_gate ? jj : jj + 16][r16] = __float2half_rn(hv);
             }
+            __syncwarp();
+            const int n = c0 + lane;
+            if (n < un.rows) {
+              const uint4* s4 = reinterpret_cast<const uint4*>(stg[lane]);
+              uint4* dst = reinterpret_cast<uint4*>(h_out + (int64_t)(un.pos0 + n) * I + i0);
+              dst[0] = s4[0];
+              dst[1] = s4[1];
+            }
+            __syncwarp();
           }
         }
-        named_bar_sync(1, 128);
-        const int I = d.I;
-        for (int i = tid; i < rows * 16; i += 128) {
-          const int n = i >> 4, c = i & 15;
-          const uint4 v = *reinterpret_cast<const uint4*>(hs + n * hst + c * 8);
-          *reinterpret_cast<uint4*>(h_out + (int64_t)(sm->pos0 + n) * I + u * 128 + c * 8) = v;
-        }
       } else {
+        // Lane r of warp q holds output row hd = ... + 32q + r for 32 pair
+        // columns per load; a per-warp staging tile turns 16 columns at a time
+        // into rows of 32 contiguous FP32 values, written as 16-byte stores.
         const int H = d.H;
+        const int* pr = sm->epair[it & 1];
+        const float* wsc = sm->ewsc[it & 1];
+        float(*stg)[32] = reinterpret_cast<float(*)[32]>(sm->stage[warp]);
 #pragma unroll 1
         for (int at = 0; at < 2; ++at) {
-          const int hd = u * 256 + at * 128 + warp * 32 + lane;
+          const int hd0 = un.sub * 256 + at * 128 + warp * 32;
 #pragma unroll 1
-          for (int c0 = 0; c0 < npad; c0 += 32) {
+          for (int c0 = 0; c0 < un.npad; c0 += 32) {
             uint32_t v[32];
             tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + at * 256 + c0, v);
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              const int n = c0 + j;
-              if (n < rows)
-                __stcs(partial + (int64_t)sm->src[n] * H + hd, __uint_as_float(v[j]) * sm->wsc[n]);
+            for (int hf = 0; hf < 2; ++hf) {
+#pragma unroll
+              for (int j = 0; j < 16; ++j) stg[j][lane] = __uint_as_float(v[16 * hf + j]);
+              __syncwarp();
+              // lanes 8p .. 8p+7 write column (pair) p0 + p: 8 x 16 bytes
+              const int cl = lane >> 3, part = lane & 7;
+#pragma unroll
+              for (int p4 = 0; p4 < 4; ++p4) {
+                const int j = p4 * 4 + cl;
+                const int n = c0 + 16 * hf + j;
+                if (n < un.rows) {
+                  float4 o = reinterpret_cast<const float4*>(stg[j])[part];
+                  const float sc = wsc[n];
+                  o.x *= sc;
+                  o.y *= sc;
+                  o.z *= sc;
+                  o.w *= sc;
+                  __stcs(reinterpret_cast<float4*>(partial + (int64_t)pr[n] * H + hd0) + part, o);
+                }
+              }
+              __syncwarp();
             }
           }
         }
       }
+      tc_fence_before();
+      mbar_arrive(&sm->tmem_empty);
+      MOE_PROF(if (tid == 0) PROF_ADD(poff + 14, te));
     }
   }
   tc_fence_before();
@@ -331,7 +499,6 @@ cudaError_t launch_prefill_forward(const LayerDims& d, int64_t M, const __half* 
                                    const PlanView& pv, Weights w13, Weights w2, Weights s13,
                                    Weights s2, __half* y, __half* h, float* partial,
                                    uint32_t* status, cudaStream_t stream, int num_sms) {
-  (void)num_sms;
   const int64_t P = M * d.k_eff;
   const int max_tiles = max_tiles_for(P, d.e_eff);
   const size_t smem = gemm_smem_bytes();
@@ -345,16 +512,17 @@ cudaError_t launch_prefill_forward(const LayerDims& d, int64_t M, const __half* 
     if (e != cudaSuccess) return e;
     attr_done = true;
   }
+  const int g13 = (int)std::min<int64_t>((int64_t)max_tiles * ((2 * d.I) / 256), num_sms);
+  const int g2 = (int)std::min<int64_t>((int64_t)max_tiles * (d.H / 256), num_sms);
   const bool pdl = !trace_on();
   trace_mark(stream, kTraceW13, false);
-  cudaError_t e = launch_k(grouped_gemm_kernel<true>, dim3(max_tiles * ((2 * d.I) / 256)),
-                           dim3(kGemmThreads), smem, stream, pdl, d, pv, x, w13, s13, h, partial,
-                           status);
+  cudaError_t e = launch_k(grouped_gemm_kernel<true>, dim3(g13), dim3(kGemmThreads), smem,
+                           stream, pdl, d, pv, x, w13, s13, h, partial, status);
   if (e != cudaSuccess) return e;
   trace_mark(stream, kTraceW13, true);
   trace_mark(stream, kTraceW2, false);
-  e = launch_k(grouped_gemm_kernel<false>, dim3(max_tiles * (d.H / 256)), dim3(kGemmThreads),
-               smem, stream, pdl, d, pv, (const __half*)h, w2, s2, h, partial, status);
+  e = launch_k(grouped_gemm_kernel<false>, dim3(g2), dim3(kGemmThreads), smem, stream, pdl, d,
+               pv, (const __half*)h, w2, s2, h, partial, status);
   if (e != cudaSuccess) return e;
   trace_mark(stream, kTraceW2, true);
   trace_mark(stream, kTraceCombine, false);

@@ -12,14 +12,15 @@
 namespace moe {
 
 // Byte offset of the 8 q bytes and the s byte of (packed row rp, 16-element
-// block b) of matrix m in the fragment layout.
+// block b) of matrix m in the fragment layout: 256-row groups, then 64-element
+// segments, then the group's 16 row tiles (512 q bytes + 64 s bytes each).
 struct FragPos {
   int64_t q, s;
 };
 __device__ __forceinline__ FragPos frag_pos(int64_t m, int64_t rows, int64_t k, int64_t rp,
                                             int64_t b) {
   int64_t rt = rp >> 4, r16 = rp & 15, ks = b >> 2, c = b & 3;
-  int64_t blk = (m * (rows >> 4) + rt) * (k >> 6) + ks;
+  int64_t blk = ((m * (rows >> 8) + (rt >> 4)) * (k >> 6) + ks) * 16 + (rt & 15);
   int64_t L = 4 * (r16 & 7) + c;
   FragPos p;
   p.q = blk * 512 + 16 * L + ((r16 >= 8) ? 8 : 0);

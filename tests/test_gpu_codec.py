@@ -13,20 +13,22 @@ pytestmark = pytest.mark.gpu
 
 
 def frag_to_canonical(q, s, n, rows, k, w13=False):
-    """Undo the fragment layout (as documented in include/moe_nvfp4.h)."""
-    q = q.reshape(n, rows // 16, k // 64, 32, 2, 8)       # [m][rt][ks][L][half][8 bytes]
-    s = s.reshape(n, rows // 16, k // 64, 32, 2)
+    """Undo the fragment layout (as documented in include/moe_nvfp4.h): block
+    b = ((m * rows/256 + G) * k/64 + ks) * 16 + j holds tile rt = 16 G + j."""
+    q = q.reshape(n, rows // 256, k // 64, 16, 32, 2, 8)   # [m][G][ks][j][L][half][8 bytes]
+    s = s.reshape(n, rows // 256, k // 64, 16, 32, 2)
     L = np.arange(32)
     g, c = L // 4, L % 4
     qc = np.zeros((n, rows, k // 2), np.uint8)
     sc = np.zeros((n, rows, k // 16), np.uint8)
     for rt in range(rows // 16):
+        G, j = divmod(rt, 16)
         for ks in range(k // 64):
             for half in range(2):
                 r = rt * 16 + g + 8 * half
                 for b in range(8):
-                    qc[:, r, ks * 32 + 8 * c + b] = q[:, rt, ks, L, half, b]
-                sc[:, r, ks * 4 + c] = s[:, rt, ks, L, half]
+                    qc[:, r, ks * 32 + 8 * c + b] = q[:, G, ks, j, L, half, b]
+                sc[:, r, ks * 4 + c] = s[:, G, ks, j, L, half]
     if w13:
         I = rows // 2
         canon_rows = []
@@ -57,7 +59,7 @@ def _weights(seed, n, rows, k):
 
 @pytest.mark.parametrize("layout", [moe.LAYOUT_CANONICAL, moe.LAYOUT_FRAGMENT,
                                     moe.LAYOUT_FRAGMENT_W13])
-@pytest.mark.parametrize("shape", [(3, 64, 256), (2, 32, 2048), (1, 1024, 128)])
+@pytest.mark.parametrize("shape", [(3, 256, 256), (2, 256, 2048), (1, 1024, 128)])
 def test_quantize_bit_exact(layout, shape):
     n, rows, k = shape
     w = _weights(7 + rows, n, rows, k)
@@ -73,6 +75,16 @@ def test_quantize_bit_exact(layout, shape):
         qc, sc = frag_to_canonical(q, s, n, rows, k, w13=(layout == moe.LAYOUT_FRAGMENT_W13))
         np.testing.assert_array_equal(qc, qo)
         np.testing.assert_array_equal(sc, so)
+
+
+def test_quantize_small_canonical_shapes():
+    """Canonical layout only needs rows % 16 == 0."""
+    w = _weights(3, 2, 48, 128)
+    qo, so, go, st = oracle.quantize(w)
+    q, s, g = moe.quantize(torch.from_numpy(w).cuda(), moe.LAYOUT_CANONICAL)
+    np.testing.assert_array_equal(q.cpu().numpy().reshape(qo.shape), qo)
+    np.testing.assert_array_equal(s.cpu().numpy().reshape(so.shape), so)
+    np.testing.assert_array_equal(g.cpu().numpy().view(np.uint32), go.view(np.uint32))
 
 
 def test_quantize_worked_case(golden_dir):
@@ -118,8 +130,8 @@ def test_dequantize_bit_exact_all_codes(layout):
     ref = oracle.dequant(q, s).view(np.uint16)
     if layout != moe.LAYOUT_CANONICAL:
         # build the fragment layout from the canonical bytes (the inverse map)
-        qf = np.zeros((rows // 16, k // 64, 32, 2, 8), np.uint8)
-        sf = np.zeros((rows // 16, k // 64, 32, 2), np.uint8)
+        qf = np.zeros((rows // 256, k // 64, 16, 32, 2, 8), np.uint8)
+        sf = np.zeros((rows // 256, k // 64, 16, 32, 2), np.uint8)
         L = np.arange(32)
         g, c = L // 4, L % 4
         if layout == moe.LAYOUT_FRAGMENT_W13:
@@ -133,12 +145,13 @@ def test_dequantize_bit_exact_all_codes(layout):
         else:
             qp, sp = q, s
         for rt in range(rows // 16):
+            G, j = divmod(rt, 16)
             for ks in range(k // 64):
                 for half in range(2):
                     r = rt * 16 + g + 8 * half
                     for b in range(8):
-                        qf[rt, ks, L, half, b] = qp[r, ks * 32 + 8 * c + b]
-                    sf[rt, ks, L, half] = sp[r, ks * 4 + c]
+                        qf[G, ks, j, L, half, b] = qp[r, ks * 32 + 8 * c + b]
+                    sf[G, ks, j, L, half] = sp[r, ks * 4 + c]
         qd, sd = qf.reshape(-1), sf.reshape(-1)
     else:
         qd, sd = q.reshape(-1), s.reshape(-1)
