@@ -108,7 +108,7 @@ int32_t cuda_status(cudaError_t e) {
 
 namespace moe {
 #ifdef MOE_TIMELINE
-__device__ unsigned long long g_timeline[32];
+__device__ unsigned long long g_timeline[64];
 __device__ unsigned long long g_prof[32];
 #endif
 bool trace_on() { return g_trace_events != nullptr; }
@@ -124,22 +124,21 @@ extern "C" {
 // Timeline build only (not part of the public header): reset / read the
 // per-kernel globaltimer stamps.
 int32_t moe_nvfp4_timeline_reset(void* stream) {
-  unsigned long long h[32];
-  for (int s = 0; s < 8; ++s) {
+  unsigned long long h[64];
+  for (int s = 0; s < 5; ++s) {
     h[4 * s] = ~0ull;
     h[4 * s + 1] = ~0ull;
     h[4 * s + 2] = 0ull;
     h[4 * s + 3] = 0ull;
   }
-  // raw cells: 21, 23, 24 take minima; 20, 22, 25 maxima
-  for (int c : {20, 22, 25}) h[c] = 0ull;
-  for (int c : {21, 23, 24}) h[c] = ~0ull;
+  // raw cells 20..63: odd cells take minima, even cells maxima
+  for (int c = 20; c < 64; ++c) h[c] = (c & 1) ? ~0ull : 0ull;
   return cuda_status(cudaMemcpyToSymbolAsync(moe::g_timeline, h, sizeof(h), 0,
                                              cudaMemcpyHostToDevice,
                                              static_cast<cudaStream_t>(stream)));
 }
 int32_t moe_nvfp4_timeline_read(unsigned long long* out) {
-  return cuda_status(cudaMemcpyFromSymbol(out, moe::g_timeline, sizeof(unsigned long long) * 32));
+  return cuda_status(cudaMemcpyFromSymbol(out, moe::g_timeline, sizeof(unsigned long long) * 64));
 }
 int32_t moe_nvfp4_prof_read(unsigned long long* out, int reset) {
   cudaError_t e = cudaMemcpyFromSymbol(out, moe::g_prof, sizeof(unsigned long long) * 32);

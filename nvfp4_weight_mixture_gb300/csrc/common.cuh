@@ -16,7 +16,7 @@ constexpr int kTileRows = 256;           // plan tile height (N of the grouped M
 constexpr int kPlanChunk = 4096;         // pairs per histogram block in the plan
 constexpr uint64_t kWaitTimeoutNs = 200ull * 1000 * 1000;  // bounded spins: 200 ms
 // Decode work table entry (one per active expert, M <= 16): expert, first plan
-// position, rows, then the token of each of the first 16 rows; entries past
+// position, rows, then the pair id of each of the first 16 rows; entries past
 // the active experts hold expert -1.
 constexpr int kDtabInts = 20;
 constexpr int kDtabEntries = kDecodeMaxTokens * 33;
@@ -50,7 +50,7 @@ struct PlanView {
   float* partial;     // [n_hchunks][kDecodeMaxTokens][n_experts] scratch (small-M router)
   float* logits;      // [kDecodeMaxTokens][n_experts] scratch (small-M router)
   uint32_t* tickets;  // [64] self-resetting arrival counters: [0, 8) router slices,
-                      // [16, 48) decode W2 row blocks, 63 router finaliser
+                      // [48, 51) decode forward grid barriers, 63 router finaliser
   int32_t* dtab;      // [kDecodeMaxTokens * 33][kDtabInts] decode work table (M <= 16)
 };
 
@@ -117,7 +117,7 @@ __device__ __forceinline__ uint64_t globaltimer() {
 // with moe_nvfp4_timeline_read() in that build; compiled out otherwise.
 enum TimelineSlot { kTlRouter = 0, kTlPlan = 1, kTlW13 = 2, kTlW2 = 3, kTlCombine = 4 };
 #ifdef MOE_TIMELINE
-extern __device__ unsigned long long g_timeline[32];
+extern __device__ unsigned long long g_timeline[64];
 struct TlScope {
   int slot;
   __device__ explicit TlScope(int s) : slot(s) {
@@ -138,7 +138,7 @@ struct TlScope {
 // per-role cycle accounting of the grouped GEMM (summed over blocks)
 extern __device__ unsigned long long g_prof[32];
 #define MOE_PROF(stmt) stmt
-// raw stamps on timeline cells 20..31 (earliest / latest over the threads that pass)
+// raw stamps on timeline cells 20..63 (earliest / latest over the threads that pass)
 #define MOE_TL_MIN(cell) atomicMin(&::moe::g_timeline[cell], (unsigned long long)::moe::globaltimer())
 #define MOE_TL_MAX(cell) atomicMax(&::moe::g_timeline[cell], (unsigned long long)::moe::globaltimer())
 #else

@@ -1,5 +1,5 @@
-// Decode path (M <= 16): weight-streaming, split-K GEMV kernels and the
-// fixed-order combine.
+// Decode path (M <= 16): the weight-streaming forward as one cooperative
+// kernel, and the fixed-order combine kernel of the prefill path.
 //
 // The layer is HBM-bound here: every touched expert's NVFP4 bytes are read
 // once.  Weights are stored in the fragment layout, so each warp reads one
@@ -13,6 +13,8 @@
 // grouped W2 reusing the integer plan; M2-M16 dynamic dispatch) and "Latest
 // grouped-MoE screen" (the complete C16 decode call).
 #include <math.h>
+
+#include <algorithm>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -44,39 +46,50 @@ __device__ __forceinline__ uint16_t ldg_u16(const uint8_t* p) {
 }
 
 // ---------------------------------------------------------------------------
-// W13 + SwiGLU.  One block per (active expert, pair of gate/up 16-row tiles);
-// the 8 warps split K; fixed-order reduction over warps in shared memory.
-// h[pos][i] = fp16(silu(g13 * G) * (g13 * U)) for the expert's plan positions.
+// Decode forward = two kernels in programmatic dependent launch:
+//   W13 + SwiGLU: persistent blocks walk the items (active expert, pair of
+//     gate / up 16-row tiles); the block's 8 warps split K, reduce in shared
+//     memory in a fixed order and write h[pos][i] = fp16(silu(g13 G) * (g13 U)).
+//   W2 + combine: one block per 16-row tile of H; its 16 warps take the active
+//     experts in turn, each computing o = g2 * W2[tile] . h for the expert's
+//     pairs into shared memory; the block then sums every token's slots in
+//     order, y[t][tile] = fp16(sum_j w_j o_j).  Weights, pair ids and combine
+//     weights of a warp's first expert are loaded before waiting on the W13
+//     grid, so only the h rows are read after it.
 // ---------------------------------------------------------------------------
+struct DecodeArgs {
+  LayerDims d;
+  PlanView pv;
+  const __half* x;
+  Weights w13, s13, w2, s2;
+  __half* h;
+  __half* y;
+  int M;
+  int max_active;  // work-table entries that can be valid (min(M * k_eff, e_eff))
+};
+
+// A work-table entry names a routed expert (or the shared one) and a run of
+// plan positions inside [0, M * k_eff); anything else is skipped.
+__device__ __forceinline__ bool entry_ok(const DecodeArgs& p, int e, int base, int count) {
+  const int P = p.M * p.d.k_eff;
+  return e >= 0 && (e < p.d.E || (e == p.d.E && p.d.shared)) && base >= 0 && count >= 0 &&
+         base + count <= P;
+}
+
+// W13 item (a, rp) for one block of 256 threads.  xs: staged token rows
+// (stride 2H + 16).
 template <int NT>
-__global__ void __launch_bounds__(256, 3) decode_w13_kernel(LayerDims d, PlanView pv,
-                                                            const __half* __restrict__ x,
-                                                            Weights w13, Weights s13, Weights w2,
-                                                            Weights s2, __half* __restrict__ h) {
-  extern __shared__ __align__(16) char xs_raw[];  // [NT*8][H*2 + 16] token rows
-  __shared__ float red[8][2][NT][32][4];
-  __shared__ int s_tok[NT * 8];
-  MOE_TL(kTlW13);
-  pdl_wait();
-  MOE_TL_WAITED();
-  pdl_launch_dependents();
-  __shared__ int s_ent[kDtabInts];
+__device__ __forceinline__ void w13_item(const DecodeArgs& p, const int* en, int rp,
+                                         const char* xs, float* red, int* s_tok) {
+  const LayerDims& d = p.d;
   const int H = d.H, I = d.I;
-  const int n_rtp = I / 16;
-  const int unit = blockIdx.x;
-  const int a = unit / n_rtp, rp = unit - a * n_rtp;
-  // one round trip for the unit's metadata: the decode work-table entry
-  if (threadIdx.x < kDtabInts) s_ent[threadIdx.x] = __ldcg(pv.dtab + a * kDtabInts + threadIdx.x);
-  __syncthreads();
-  const int e = s_ent[0];
-  if (e < 0) return;
-  const int base = s_ent[1];
-  const int count = s_ent[2];
+  const int e = en[0], base = en[1], count = en[2];
+  if (!entry_ok(p, e, base, count)) return;
   const bool sh = (e == d.E);
-  const uint8_t* qe = sh ? s13.q : w13.q + (size_t)e * I * H;
-  const uint8_t* se = sh ? s13.s : w13.s + (size_t)e * I * H / 8;
-  const float gsc = sh ? s13.g[0] : w13.g[e];
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint8_t* qe = sh ? p.s13.q : p.w13.q + (size_t)e * I * H;
+  const uint8_t* se = sh ? p.s13.s : p.w13.s + (size_t)e * I * H / 8;
+  const float gsc = sh ? p.s13.g[0] : p.w13.g[e];
+  const int ttid = threadIdx.x, warp = ttid >> 5, lane = ttid & 31;
   const int g = lane >> 2, t4 = lane & 3;
   const int S = H / 64;
   // gate tile 2*rp and up tile 2*rp+1: tiles j0, j0 + 1 of 256-row group rp / 8;
@@ -85,20 +98,10 @@ __global__ void __launch_bounds__(256, 3) decode_w13_kernel(LayerDims d, PlanVie
   const uint8_t* qt = qe + (size_t)(rp >> 3) * S * 16 * 512 + j0 * 512;
   const uint8_t* st = se + (size_t)(rp >> 3) * S * 16 * 64 + j0 * 64;
   const int xstride = H * 2 + 16;
-  const int cpr = H / 8;  // 16-byte chunks per row
-  if (tid == 0) {
-    // start this unit's share (1 / n_rtp) of the expert's W2 bytes towards L2,
-    // so that the W2 kernel finds them there
-    const size_t q2 = (size_t)H * I / 2, s2b = (size_t)H * I / 16;
-    const uint8_t* q2e = sh ? s2.q : w2.q + (size_t)e * q2;
-    const uint8_t* s2e = sh ? s2.s : w2.s + (size_t)e * s2b;
-    prefetch_l2_bulk(q2e + (size_t)rp * (q2 / n_rtp), (uint32_t)(q2 / n_rtp));
-    prefetch_l2_bulk(s2e + (size_t)rp * (s2b / n_rtp), (uint32_t)(s2b / n_rtp));
-  }
 
   uint4 qv[4][2];
   uint32_t sv[4][2];
-  // this warp's segments: ks = warp + 8 * j, in groups of 4 (32 segments)
+  // this warp's segments: ks = warp + 8 * j, in groups of 4
   auto load_group = [&](int ks0) {
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
@@ -113,21 +116,17 @@ __global__ void __launch_bounds__(256, 3) decode_w13_kernel(LayerDims d, PlanVie
     }
   };
 
-  // rows of the expert in chunks of NT*8 (one chunk unless given ids repeat
+  // the expert's rows in chunks of NT * 8 (one chunk unless given ids repeat
   // an expert within a token)
   for (int n0 = 0; n0 < count; n0 += NT * 8) {
     const int n_e = min(count - n0, NT * 8);
     const int pos0 = base + n0;
-    if (tid < n_e)
-      s_tok[tid] = (n0 + tid < 16) ? s_ent[4 + n0 + tid] : __ldcg(pv.perm + pos0 + tid) / d.k_eff;
-    __syncthreads();
-    for (int i = tid; i < n_e * cpr; i += 256) {
-      const int n = i / cpr, c = i - n * cpr;
-      cp_async16(smem_u32(xs_raw + n * xstride + c * 16), x + (int64_t)s_tok[n] * H + c * 8,
-                 16u);
+    load_group(warp);
+    if (ttid < n_e) {
+      const int pair = (n0 + ttid < 16) ? en[4 + n0 + ttid] : __ldcg(p.pv.perm + pos0 + ttid);
+      s_tok[ttid] = min(max(pair / d.k_eff, 0), p.M - 1);
     }
-    cp_async_commit();
-
+    __syncthreads();
     float acc[2][NT][4];
 #pragma unroll
     for (int t = 0; t < 2; ++t)
@@ -135,10 +134,6 @@ __global__ void __launch_bounds__(256, 3) decode_w13_kernel(LayerDims d, PlanVie
       for (int n = 0; n < NT; ++n)
 #pragma unroll
         for (int c = 0; c < 4; ++c) acc[t][n][c] = 0.f;
-
-    load_group(warp);
-    cp_async_wait<0>();
-    __syncthreads();  // token rows staged
     for (int ks0 = warp; ks0 < S; ks0 += 32) {
       if (ks0 != warp) load_group(ks0);
 #pragma unroll
@@ -150,7 +145,7 @@ __global__ void __launch_bounds__(256, 3) decode_w13_kernel(LayerDims d, PlanVie
         for (int nt = 0; nt < NT; ++nt) {
           const int n = nt * 8 + g;
           if (n < n_e) {
-            const char* src = xs_raw + n * xstride + (ks * 64 + 16 * t4) * 2;
+            const char* src = xs + s_tok[n] * xstride + (ks * 64 + 16 * t4) * 2;
             const uint4 v0 = *reinterpret_cast<const uint4*>(src);
             const uint4 v1 = *reinterpret_cast<const uint4*>(src + 16);
             xw[nt][0] = v0.x; xw[nt][1] = v0.y; xw[nt][2] = v0.z; xw[nt][3] = v0.w;
@@ -175,20 +170,22 @@ __global__ void __launch_bounds__(256, 3) decode_w13_kernel(LayerDims d, PlanVie
         }
       }
     }
+    // red[warp][tt][nt][lane][c]
 #pragma unroll
     for (int tt = 0; tt < 2; ++tt)
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-        for (int c = 0; c < 4; ++c) red[warp][tt][nt][lane][c] = acc[tt][nt][c];
+        for (int c = 0; c < 4; ++c)
+          red[(((warp * 2 + tt) * NT + nt) * 32 + lane) * 4 + c] = acc[tt][nt][c];
     __syncthreads();
-    if (tid < NT * 128) {
-      const int nt = tid >> 7, ln = (tid >> 2) & 31, c = tid & 3;
+    if (ttid < NT * 128) {
+      const int nt = ttid >> 7, ln = (ttid >> 2) & 31, c = ttid & 3;
       float G = 0.f, U = 0.f;
 #pragma unroll
       for (int w = 0; w < 8; ++w) {
-        G += red[w][0][nt][ln][c];
-        U += red[w][1][nt][ln][c];
+        G += red[(((w * 2 + 0) * NT + nt) * 32 + ln) * 4 + c];
+        U += red[(((w * 2 + 1) * NT + nt) * 32 + ln) * 4 + c];
       }
       // c0: (row g, col 2t4), c1: (g, 2t4+1), c2: (g+8, 2t4), c3: (g+8, 2t4+1)
       const int row = (ln >> 2) + ((c & 2) ? 8 : 0);
@@ -197,188 +194,207 @@ __global__ void __launch_bounds__(256, 3) decode_w13_kernel(LayerDims d, PlanVie
         G *= gsc;
         U *= gsc;
         const float hv = G / (1.f + expf(-G)) * U;
-        h[(int64_t)(pos0 + n) * I + 16 * rp + row] = __float2half_rn(hv);
+        p.h[(int64_t)(pos0 + n) * I + 16 * rp + row] = __float2half_rn(hv);
       }
     }
-    __syncthreads();  // red / s_tok / xs reused by the next chunk
+    __syncthreads();  // red / s_tok reused by the next chunk or item
   }
 }
 
-// ---------------------------------------------------------------------------
-// W2.  One block per (active expert, 128-row block of H); warp w owns the
-// 16-row tile w of the block over the full K = I.  Each output is scaled by
-// g2 and the pair's combine weight and written to partial[pair][H] (FP32).
-// The first weights are fetched before waiting on the W13 grid.
-// ---------------------------------------------------------------------------
-template <int NT>
-__global__ void __launch_bounds__(256) decode_w2_kernel(LayerDims d, PlanView pv,
-                                                        const __half* __restrict__ h,
-                                                        Weights w2, Weights s2,
-                                                        float* __restrict__ partial,
-                                                        __half* __restrict__ y) {
-  extern __shared__ __align__(16) char hs_raw[];  // [NT*8][I*2 + 16] h rows
-  __shared__ int is_last;
-  MOE_TL(kTlW2);
-  __shared__ int s_ent[kDtabInts + 1];
-  const int H = d.H, I = d.I;
-  const int nhb = H / 128;
-  const int unit = blockIdx.x;
-  const int a = unit / nhb, hb = unit - a * nhb;
-  if (threadIdx.x < kDtabInts) s_ent[threadIdx.x] = __ldcg(pv.dtab + a * kDtabInts + threadIdx.x);
-  if (threadIdx.x == kDtabInts) s_ent[kDtabInts] = __ldcg(&pv.hdr->n_active);
-  __syncthreads();
-  const int e = s_ent[0];
-  if (e < 0) {
-    pdl_wait();
-    return;
-  }
-  const int n_active = s_ent[kDtabInts];
-  const int base = s_ent[1];
-  const int count = s_ent[2];
+// Starts the item's share (1 / n_rtp) of its expert's W2 bytes towards L2,
+// so that the W2 kernel finds them there (one thread).
+__device__ __forceinline__ void w2_share_prefetch(const DecodeArgs& p, const int* en, int rp) {
+  const LayerDims& d = p.d;
+  const int e = en[0];
+  if (!entry_ok(p, e, en[1], en[2])) return;
   const bool sh = (e == d.E);
-  const uint8_t* qe = sh ? s2.q : w2.q + (size_t)e * H * I / 2;
-  const uint8_t* se = sh ? s2.s : w2.s + (size_t)e * H * I / 16;
-  const float gsc = sh ? s2.g[0] : w2.g[e];
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int g = lane >> 2, t4 = lane & 3;
-  const int S = I / 64;
-  const int rt = hb * 8 + warp;  // tile rt % 16 of 256-row group rt / 16
-  const uint8_t* qt = qe + (size_t)(rt >> 4) * S * 16 * 512 + (rt & 15) * 512;
-  const uint8_t* st = se + (size_t)(rt >> 4) * S * 16 * 64 + (rt & 15) * 64;
-  const int hstride = I * 2 + 16;
-  const int cpr = I / 8;
+  const size_t q2 = (size_t)d.H * d.I / 2, s2b = (size_t)d.H * d.I / 16;
+  const int n_rtp = d.I / 16;
+  const uint8_t* q2e = sh ? p.s2.q : p.w2.q + (size_t)e * q2;
+  const uint8_t* s2e = sh ? p.s2.s : p.w2.s + (size_t)e * s2b;
+  prefetch_l2_bulk(q2e + (size_t)rp * (q2 / n_rtp), (uint32_t)(q2 / n_rtp));
+  prefetch_l2_bulk(s2e + (size_t)rp * (s2b / n_rtp), (uint32_t)(s2b / n_rtp));
+}
 
-  uint4 qv[8];
-  uint32_t sv[8];
-  auto load_group = [&](int ks0) {
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      if (ks0 + j < S) {
-        qv[j] = ldg_nc_v4(qt + (size_t)(ks0 + j) * 16 * 512 + lane * 16);
-        sv[j] = ldg_u16(st + (size_t)(ks0 + j) * 16 * 64 + lane * 2);
-      }
-    }
-  };
-  // Plan data (complete before the W13 grid started) is read before waiting on
-  // the W13 grid: the weights, the first row chunk's pairs and combine scales,
-  // and which pairs of the batch are valid (for the fused combine).
-  __shared__ int s_pair[NT * 8];
-  __shared__ float s_wsc[NT * 8];
-  __shared__ unsigned char s_valid[kDtabEntries];
-  load_group(0);
-  const int P_all = __ldcg(&pv.hdr->M) * d.k_eff;
-  for (int p = tid; p < P_all; p += 256) s_valid[p] = __ldcg(pv.inv + p) >= 0;
-  if (tid < min(count, NT * 8)) {
-    const int pair = __ldcg(pv.perm + base + tid);
-    s_pair[tid] = pair;
-    s_wsc[tid] = gsc * __ldcg(pv.w + pair);
+template <int NT>
+__global__ void __launch_bounds__(256, NT == 1 ? 3 : 2) decode_w13_kernel(const DecodeArgs p) {
+  extern __shared__ __align__(16) char dsm[];  // staged token rows, then the reduction area
+  __shared__ int s_tok[16];
+  __shared__ int s_ent[kDtabInts];
+  __shared__ int s_nact;
+  MOE_TL(kTlW13);
+  const LayerDims& d = p.d;
+  const int H = d.H, I = d.I;
+  const int tid = threadIdx.x;
+  char* xs = dsm;
+  const int xstride = H * 2 + 16, cpr = H / 8;
+  float* red = reinterpret_cast<float*>(dsm + align_up((size_t)p.M * xstride, 16));
+  // token rows: inputs of the layer, staged before waiting on the plan grid
+  for (int i = tid; i < p.M * cpr; i += 256) {
+    const int n = i / cpr, c = i - n * cpr;
+    cp_async16(smem_u32(xs + n * xstride + c * 16), p.x + (int64_t)n * H + c * 8, 16u);
   }
+  cp_async_commit();
   pdl_wait();
   MOE_TL_WAITED();
   pdl_launch_dependents();
-
-  for (int n0 = 0; n0 < count; n0 += NT * 8) {
-    const int n_e = min(count - n0, NT * 8);
-    const int pos0 = base + n0;
-    if (n0 > 0) {
+  const int n_rtp = I / 16;
+  if (tid == 0) s_nact = min(__ldcg(&p.pv.hdr->n_active), p.max_active);
+  if (tid < kDtabInts && blockIdx.x < p.max_active * n_rtp)
+    s_ent[tid] = __ldcg(p.pv.dtab + (blockIdx.x / n_rtp) * kDtabInts + tid);
+  cp_async_wait<0>();
+  __syncthreads();
+  const int n13 = s_nact * n_rtp;
+  for (int i = blockIdx.x; i < n13; i += gridDim.x) {
+    const int a = i / n_rtp, rp = i - a * n_rtp;
+    if (i != (int)blockIdx.x) {
+      // w13_item ended with a barrier: s_ent of the previous item is no longer read
+      if (tid < kDtabInts) s_ent[tid] = __ldcg(p.pv.dtab + a * kDtabInts + tid);
       __syncthreads();
-      if (tid < n_e) {
-        const int pair = __ldcg(pv.perm + pos0 + tid);
-        s_pair[tid] = pair;
-        s_wsc[tid] = gsc * __ldcg(pv.w + pair);
+    }
+    if (tid == 0) w2_share_prefetch(p, s_ent, rp);
+    w13_item<NT>(p, s_ent, rp, xs, red, s_tok);
+  }
+}
+
+// W2 + combine.  grid = H / 16 (one 16-row tile of H per block), 512 threads.
+// Shared: o[P][16] FP32 (every pair's outputs for the tile), valid[P].
+constexpr int kW2Warps = 16;
+
+template <int NT>
+__global__ void __launch_bounds__(kW2Warps * 32, 1) decode_w2_kernel(const DecodeArgs p) {
+  extern __shared__ __align__(16) char dsm[];
+  MOE_TL(kTlW2);
+  const LayerDims& d = p.d;
+  const int H = d.H, I = d.I, k_eff = d.k_eff;
+  const int P = p.M * k_eff;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g = lane >> 2, t4 = lane & 3;
+  const int rt = blockIdx.x;  // 16-row tile of H: tile rt % 16 of 256-row group rt / 16
+  const int S = I / 64;
+  float* o_s = reinterpret_cast<float*>(dsm);                      // [P][16]
+  unsigned char* valid = reinterpret_cast<unsigned char*>(o_s + (size_t)P * 16);  // [P]
+  // ---- everything that comes from the plan grid (complete before W13 began) ----
+  for (int q = tid; q < P; q += kW2Warps * 32) valid[q] = __ldcg(p.pv.inv + q) >= 0;
+  const int n_act = min(__ldcg(&p.pv.hdr->n_active), p.max_active);
+  // this warp's experts: a = warp, warp + 16, ...; lanes 0..19 hold the entry
+  int a = warp;
+  int ent_v = (a < n_act && lane < kDtabInts) ? __ldcg(p.pv.dtab + a * kDtabInts + lane) : -1;
+  uint4 q[8];
+  uint32_t sc[8];
+  float wsc = 0.f;  // lane n < 16: g2 * combine weight of the entry's row n
+  int pair_l = -1;  // lane n < 16: pair id of row n
+  auto load_expert = [&]() {
+    const int e = __shfl_sync(0xffffffffu, ent_v, 0);
+    const int base = __shfl_sync(0xffffffffu, ent_v, 1);
+    const int count = __shfl_sync(0xffffffffu, ent_v, 2);
+    const int pr = __shfl_sync(0xffffffffu, ent_v, (4 + lane) & 31);
+    if (!entry_ok(p, e, base, count)) return false;
+    const bool sh = (e == d.E);
+    const uint8_t* qe = sh ? p.s2.q : p.w2.q + (size_t)e * H * I / 2;
+    const uint8_t* se = sh ? p.s2.s : p.w2.s + (size_t)e * H * I / 16;
+    const uint8_t* qt = qe + (size_t)(rt >> 4) * S * 16 * 512 + (rt & 15) * 512;
+    const uint8_t* st = se + (size_t)(rt >> 4) * S * 16 * 64 + (rt & 15) * 64;
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      if (j < S) {
+        q[j] = ldg_nc_v4(qt + (size_t)j * 16 * 512 + lane * 16);
+        sc[j] = ldg_u16(st + (size_t)j * 16 * 64 + lane * 2);
       }
+    const float gsc = sh ? p.s2.g[0] : p.w2.g[e];
+    pair_l = (lane < 16 && lane < count) ? pr : -1;
+    if (pair_l >= P) pair_l = -1;
+    wsc = pair_l >= 0 ? gsc * __ldcg(p.pv.w + pair_l) : 0.f;
+    return true;
+  };
+  bool have = (a < n_act) && load_expert();
+  pdl_wait();
+  MOE_TL_WAITED();
+  // ---- h rows (written by the W13 grid) ----
+  for (; a < n_act; a += kW2Warps) {
+    if (a != warp) {
+      ent_v = (lane < kDtabInts) ? __ldcg(p.pv.dtab + a * kDtabInts + lane) : -1;
+      have = load_expert();
     }
-    for (int i = tid; i < n_e * cpr; i += 256) {
-      const int n = i / cpr, c = i - n * cpr;
-      cp_async16(smem_u32(hs_raw + n * hstride + c * 16), h + (int64_t)(pos0 + n) * I + c * 8,
-                 16u);
-    }
-    cp_async_commit();
-    cp_async_wait<0>();
-    __syncthreads();
-
-    float acc[NT][4];
+    if (!have) continue;
+    const int e = __shfl_sync(0xffffffffu, ent_v, 0);
+    const int base = __shfl_sync(0xffffffffu, ent_v, 1);
+    const int count = __shfl_sync(0xffffffffu, ent_v, 2);
+    const bool sh = (e == d.E);
+    const uint8_t* qe = sh ? p.s2.q : p.w2.q + (size_t)e * H * I / 2;
+    const uint8_t* se = sh ? p.s2.s : p.w2.s + (size_t)e * H * I / 16;
+    const uint8_t* qt = qe + (size_t)(rt >> 4) * S * 16 * 512 + (rt & 15) * 512;
+    const uint8_t* st = se + (size_t)(rt >> 4) * S * 16 * 64 + (rt & 15) * 64;
+    const float gsc = sh ? p.s2.g[0] : p.w2.g[e];
+    for (int n0 = 0; n0 < count; n0 += 8) {
+      const int n = n0 + g;  // this lane's B column (token row of the expert)
+      // pair and scale of column n: rows below 16 come from the table (lanes
+      // n of pair_l / wsc), later rows from the plan
+      int pair_n = __shfl_sync(0xffffffffu, pair_l, n & 15);
+      float wsc_n = __shfl_sync(0xffffffffu, wsc, n & 15);
+      if (n >= 16 && n < count) {
+        pair_n = __ldcg(p.pv.perm + base + n);
+        if (pair_n < 0 || pair_n >= P) pair_n = -1;
+        wsc_n = pair_n >= 0 ? gsc * __ldcg(p.pv.w + pair_n) : 0.f;
+      }
+      if (n >= count) pair_n = -1;
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      for (int ks0 = 0; ks0 < S; ks0 += 8) {
+        if (ks0 > 0 || n0 > 0) {
 #pragma unroll
-    for (int n = 0; n < NT; ++n)
+          for (int j = 0; j < 8; ++j)
+            if (ks0 + j < S) {
+              q[j] = ldg_nc_v4(qt + (size_t)(ks0 + j) * 16 * 512 + lane * 16);
+              sc[j] = ldg_u16(st + (size_t)(ks0 + j) * 16 * 64 + lane * 2);
+            }
+        }
+        // B fragments: column n = row (base + n) of h, 16 K values per segment
+        uint4 hv[8][2];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) acc[n][c] = 0.f;
-
-    for (int ks0 = 0; ks0 < S; ks0 += 8) {
-      if (ks0 > 0 || n0 > 0) load_group(ks0);
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int ks = ks0 + j;
-        if (ks >= S) break;
-        uint32_t sg, sg8;
-        scale_splats(sv[j], &sg, &sg8);
-        uint32_t xw[NT][8];
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          const int n = nt * 8 + g;
-          if (n < n_e) {
-            const char* src = hs_raw + n * hstride + (ks * 64 + 16 * t4) * 2;
-            const uint4 v0 = *reinterpret_cast<const uint4*>(src);
-            const uint4 v1 = *reinterpret_cast<const uint4*>(src + 16);
-            xw[nt][0] = v0.x; xw[nt][1] = v0.y; xw[nt][2] = v0.z; xw[nt][3] = v0.w;
-            xw[nt][4] = v1.x; xw[nt][5] = v1.y; xw[nt][6] = v1.z; xw[nt][7] = v1.w;
+        for (int j = 0; j < 8; ++j) {
+          if (ks0 + j < S && n < count) {
+            const __half* src = p.h + (int64_t)(base + n) * I + (ks0 + j) * 64 + 16 * t4;
+            hv[j][0] = __ldcg(reinterpret_cast<const uint4*>(src));
+            hv[j][1] = __ldcg(reinterpret_cast<const uint4*>(src) + 1);
           } else {
-#pragma unroll
-            for (int u = 0; u < 8; ++u) xw[nt][u] = 0u;
+            hv[j][0] = hv[j][1] = make_uint4(0u, 0u, 0u, 0u);
           }
         }
 #pragma unroll
-        for (int s = 0; s < 4; ++s) {
-          uint32_t af[4];
-          a_frag(qv[j], sg, sg8, s, af);
+        for (int j = 0; j < 8; ++j) {
+          if (ks0 + j >= S) break;
+          uint32_t sg, sg8;
+          scale_splats(sc[j], &sg, &sg8);
+          const uint32_t xw[8] = {hv[j][0].x, hv[j][0].y, hv[j][0].z, hv[j][0].w,
+                                  hv[j][1].x, hv[j][1].y, hv[j][1].z, hv[j][1].w};
 #pragma unroll
-          for (int nt = 0; nt < NT; ++nt)
-            mma_16816(acc[nt], af, xw[nt][2 * s], xw[nt][2 * s + 1]);
+          for (int s = 0; s < 4; ++s) {
+            uint32_t af[4];
+            a_frag(q[j], sg, sg8, s, af);
+            mma_16816(acc, af, xw[2 * s], xw[2 * s + 1]);
+          }
         }
       }
-    }
-    // c0: (row g, col 2t4), c1: (g, 2t4+1), c2: (g+8, 2t4), c3: (g+8, 2t4+1)
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
+      // c0: (row g, col 2t4), c1: (g, 2t4+1), c2: (g+8, 2t4), c3: (g+8, 2t4+1)
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
-        const int n = nt * 8 + 2 * t4 + (c & 1);
-        if (n < n_e) {
-          const int row = rt * 16 + g + ((c & 2) ? 8 : 0);
-          partial[(int64_t)s_pair[n] * H + row] = acc[nt][c] * s_wsc[n];
-        }
+        const int col = 2 * t4 + (c & 1);
+        const int pr = __shfl_sync(0xffffffffu, pair_n, col * 4);
+        const float ws = __shfl_sync(0xffffffffu, wsc_n, col * 4);
+        if (pr >= 0) o_s[pr * 16 + g + ((c & 2) ? 8 : 0)] = acc[c] * ws;
       }
-    __syncthreads();  // hs reused by the next chunk
-  }
-  // The last of the n_active blocks of this row block sums the slots of every
-  // token in order: y[t][rows] = fp16(sum_j partial[t * k_eff + j][rows]).
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) {
-    const unsigned t = atomicAdd(&pv.tickets[16 + hb], 1u);
-    is_last = (t == (unsigned)n_active - 1);
-    if (is_last) pv.tickets[16 + hb] = 0u;
-  }
-  __syncthreads();
-  if (!is_last) return;
-  __threadfence();
-  const int k_eff = d.k_eff, M = P_all / k_eff;
-  for (int i = tid; i < M * 32; i += 256) {
-    const int t = i >> 5, c = hb * 128 + (i & 31) * 4;
-    float4 acc4 = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int j = 0; j < k_eff; ++j) {
-      const int64_t pair = (int64_t)t * k_eff + j;
-      if (!s_valid[pair]) continue;
-      const float4 v = __ldcg(reinterpret_cast<const float4*>(partial + pair * H + c));
-      acc4.x += v.x;
-      acc4.y += v.y;
-      acc4.z += v.z;
-      acc4.w += v.w;
     }
-    __half2 lo = __floats2half2_rn(acc4.x, acc4.y), hi = __floats2half2_rn(acc4.z, acc4.w);
-    uint2 out;
-    out.x = *reinterpret_cast<uint32_t*>(&lo);
-    out.y = *reinterpret_cast<uint32_t*>(&hi);
-    *reinterpret_cast<uint2*>(y + (int64_t)t * H + c) = out;
+  }
+  __syncthreads();
+  // ---- combine: y[t][tile] = fp16(sum_j o[t * k_eff + j]), slots in order ----
+  for (int i = tid; i < p.M * 16; i += kW2Warps * 32) {
+    const int t = i >> 4, r = i & 15;
+    float sum = 0.f;
+    for (int j = 0; j < k_eff; ++j) {
+      const int pr = t * k_eff + j;
+      if (valid[pr]) sum += o_s[pr * 16 + r];
+    }
+    p.y[(int64_t)t * H + rt * 16 + r] = __float2half_rn(sum);
   }
 }
 
@@ -424,47 +440,65 @@ cudaError_t launch_combine(const LayerDims& d, int64_t M, const PlanView& pv,
 template <int NT>
 static cudaError_t decode_impl(const LayerDims& d, int64_t M, const __half* x, const PlanView& pv,
                                Weights w13, Weights w2, Weights s13, Weights s2, __half* y,
-                               __half* h, float* partial, cudaStream_t stream) {
-  const int max_active = (int)((M * d.k_eff < d.e_eff) ? M * d.k_eff : d.e_eff);
-  const size_t xs_smem = (size_t)NT * 8 * (d.H * 2 + 16);
-  const size_t hs_smem = (size_t)NT * 8 * (d.I * 2 + 16);
-  static bool attr_done = false;
-  if (!attr_done) {
-    // the largest sizes the shape limits allow (H, I <= 4096)
-    const int big = NT * 8 * (4096 * 2 + 16);
+                               __half* h, cudaStream_t stream, int num_sms) {
+  DecodeArgs a;
+  a.d = d;
+  a.pv = pv;
+  a.x = x;
+  a.w13 = w13;
+  a.s13 = s13;
+  a.w2 = w2;
+  a.s2 = s2;
+  a.h = h;
+  a.y = y;
+  a.M = (int)M;
+  a.max_active = (int)((M * d.k_eff < d.e_eff) ? M * d.k_eff : d.e_eff);
+  const int P = (int)(M * d.k_eff);
+  const size_t smem13 = align_up((size_t)M * (d.H * 2 + 16), 16) + 8 * 2 * NT * 32 * 4 * sizeof(float);
+  const size_t smem2 = (size_t)P * 16 * sizeof(float) + P;
+  // once per process: shared-memory ceilings and the W13 blocks per SM
+  static int w13_per_sm[2] = {-1, -1};
+  int& bps = w13_per_sm[M <= 8 ? 0 : 1];
+  if (bps < 0) {
+    const int big13 = 16 * (4096 * 2 + 16) + 8 * 2 * NT * 32 * 4 * (int)sizeof(float);
     cudaError_t e = cudaFuncSetAttribute(decode_w13_kernel<NT>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, big);
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, big13);
     if (e != cudaSuccess) return e;
+    const int big2 = kDecodeMaxTokens * 33 * (16 * (int)sizeof(float) + 1);
     e = cudaFuncSetAttribute(decode_w2_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             big);
+                             big2);
     if (e != cudaSuccess) return e;
-    attr_done = true;
+    bps = 0;
   }
+  int per_sm = 0;
+  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_w13_kernel<NT>,
+                                                                256, smem13);
+  if (e != cudaSuccess) return e;
+  const int n_items = a.max_active * (d.I / 16);
+  const int g13 = std::max(1, std::min(n_items, num_sms * std::max(per_sm, 1)));
   const bool pdl = !trace_on();
   trace_mark(stream, kTraceW13, false);
-  cudaError_t e = launch_k(decode_w13_kernel<NT>, dim3(max_active * (d.I / 16)), dim3(256),
-                           xs_smem, stream, pdl, d, pv, x, w13, s13, w2, s2, h);
+  e = launch_k(decode_w13_kernel<NT>, dim3(g13), dim3(256), smem13, stream, pdl, a);
   if (e != cudaSuccess) return e;
   trace_mark(stream, kTraceW13, true);
   trace_mark(stream, kTraceW2, false);
-  e = launch_k(decode_w2_kernel<NT>, dim3(max_active * (d.H / 128)), dim3(256), hs_smem, stream,
-               pdl, d, pv, (const __half*)h, w2, s2, partial, y);
+  e = launch_k(decode_w2_kernel<NT>, dim3(d.H / 16), dim3(kW2Warps * 32), smem2, stream, pdl, a);
   if (e != cudaSuccess) return e;
   trace_mark(stream, kTraceW2, true);
-  // the combine is fused into the W2 kernel on this path
+  // the combine is part of the W2 kernel on this path
   trace_mark(stream, kTraceCombine, false);
   trace_mark(stream, kTraceCombine, true);
-  return e;
+  return cudaSuccess;
 }
 
 cudaError_t launch_decode_forward(const LayerDims& d, int64_t M, const __half* x,
                                   const PlanView& pv, Weights w13, Weights w2, Weights s13,
                                   Weights s2, __half* y, __half* h, float* partial,
                                   uint32_t* status, cudaStream_t stream, int num_sms) {
+  (void)partial;
   (void)status;
-  (void)num_sms;
-  if (M <= 8) return decode_impl<1>(d, M, x, pv, w13, w2, s13, s2, y, h, partial, stream);
-  return decode_impl<2>(d, M, x, pv, w13, w2, s13, s2, y, h, partial, stream);
+  if (M <= 8) return decode_impl<1>(d, M, x, pv, w13, w2, s13, s2, y, h, stream, num_sms);
+  return decode_impl<2>(d, M, x, pv, w13, w2, s13, s2, y, h, stream, num_sms);
 }
 
 }  // namespace moe

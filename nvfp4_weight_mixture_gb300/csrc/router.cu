@@ -261,7 +261,7 @@ __device__ void plan_small_block(const LayerDims& d, int M, const int* src, cons
       else if (f == 2)
         v = s_cnt[e];
       else if (f >= 4 && f - 4 < s_cnt[e])
-        v = s_perm[off + f - 4] / d.k_eff;
+        v = s_perm[off + f - 4];
     }
     pv.dtab[i] = v;
   }
@@ -400,9 +400,9 @@ __global__ void __launch_bounds__(256) router_small_kernel(LayerDims d, int M,
     if (d.shared && lane == 0) s_ids[m * d.k_eff + d.k] = d.E;
   }
   __syncthreads();
-  if (tid == 0) MOE_TL_MIN(24);
+  if (tid == 0) MOE_TL_MAX(24);
   plan_small_block(d, M, s_ids, pv, status);
-  if (tid == 0) MOE_TL_MAX(25);
+  if (tid == 0) MOE_TL_MIN(25);
 }
 
 // Caller-given ids and weights: copy into the plan (plus the shared slot).
