@@ -1,5 +1,5 @@
-// Decode path (M <= 16): the weight-streaming forward as one cooperative
-// kernel, and the fixed-order combine kernel of the prefill path.
+// Decode path (M <= 16): the weight-streaming forward (W13 + SwiGLU, then W2
+// with the fixed-order combine), and the combine kernel of the prefill path.
 //
 // The layer is HBM-bound here: every touched expert's NVFP4 bytes are read
 // once.  Weights are stored in the fragment layout, so each warp reads one
@@ -50,12 +50,12 @@ __device__ __forceinline__ uint16_t ldg_u16(const uint8_t* p) {
 //   W13 + SwiGLU: persistent blocks walk the items (active expert, pair of
 //     gate / up 16-row tiles); the block's 8 warps split K, reduce in shared
 //     memory in a fixed order and write h[pos][i] = fp16(silu(g13 G) * (g13 U)).
-//   W2 + combine: one block per 16-row tile of H; its 16 warps take the active
+//   W2 + combine: one block per 16-row tile of H; its warps take the active
 //     experts in turn, each computing o = g2 * W2[tile] . h for the expert's
 //     pairs into shared memory; the block then sums every token's slots in
-//     order, y[t][tile] = fp16(sum_j w_j o_j).  Weights, pair ids and combine
-//     weights of a warp's first expert are loaded before waiting on the W13
-//     grid, so only the h rows are read after it.
+//     order, y[t][tile] = fp16(sum_j w_j o_j).  Weights (TMA), pair ids and
+//     combine weights of a warp's first experts are fetched before waiting on
+//     the W13 grid, so only the h rows are read after it.
 // ---------------------------------------------------------------------------
 struct DecodeArgs {
   LayerDims d;
@@ -64,6 +64,7 @@ struct DecodeArgs {
   Weights w13, s13, w2, s2;
   __half* h;
   __half* y;
+  uint32_t* status;
   int M;
   int max_active;  // work-table entries that can be valid (min(M * k_eff, e_eff))
 };
@@ -257,13 +258,32 @@ __global__ void __launch_bounds__(256, NT == 1 ? 3 : 2) decode_w13_kernel(const 
   }
 }
 
-// W2 + combine.  grid = H / 16 (one 16-row tile of H per block), 512 threads.
-// Shared: o[P][16] FP32 (every pair's outputs for the tile), valid[P].
+// W2 + combine: grid = H / 16 (one 16-row tile of H per block), 512 threads.
 constexpr int kW2Warps = 16;
 
+// Rows of a fragment-layout tensor map: row (m * rows / 256 + G) * (k / 64) + ks
+// holds the 16 tile blocks of segment ks of 256-row group G of matrix m.
+__device__ __forceinline__ int frag_map_row(int m, int groups, int G, int S, int ks) {
+  return (m * groups + G) * S + ks;
+}
+
+// W2 + combine.  Warp w < w2_warps takes experts a = w, w + w2_warps, ...; the
+// expert's 16-row tile of W2 (codes and scales over the full K = I) arrives by
+// two 2-D tensor-map loads into one of the warp's two shared-memory stages,
+// the first two issued before waiting on the W13 grid.  Each expert's pairs
+// get o = g2 * w_pair * (W2[tile] . h) in shared memory; the block then sums
+// every token's slots in order, y[t][tile] = fp16(sum_j o_j).
 template <int NT>
-__global__ void __launch_bounds__(kW2Warps * 32, 1) decode_w2_kernel(const DecodeArgs p) {
-  extern __shared__ __align__(16) char dsm[];
+__global__ void __launch_bounds__(kW2Warps * 32, 1)
+    decode_w2_kernel(const DecodeArgs p, int w2_warps, int stage_bytes,
+                         const __grid_constant__ CUtensorMap mq,
+                         const __grid_constant__ CUtensorMap ms,
+                         const __grid_constant__ CUtensorMap mqs,
+                         const __grid_constant__ CUtensorMap mss) {
+  extern __shared__ __align__(1024) char dsm_raw[];
+  char* dsm = reinterpret_cast<char*>((reinterpret_cast<uintptr_t>(dsm_raw) + 1023) &
+                                      ~uintptr_t(1023));
+  __shared__ uint64_t full[kW2Warps][2];
   MOE_TL(kTlW2);
   const LayerDims& d = p.d;
   const int H = d.H, I = d.I, k_eff = d.k_eff;
@@ -271,118 +291,144 @@ __global__ void __launch_bounds__(kW2Warps * 32, 1) decode_w2_kernel(const Decod
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, t4 = lane & 3;
   const int rt = blockIdx.x;  // 16-row tile of H: tile rt % 16 of 256-row group rt / 16
-  const int S = I / 64;
-  float* o_s = reinterpret_cast<float*>(dsm);                      // [P][16]
-  unsigned char* valid = reinterpret_cast<unsigned char*>(o_s + (size_t)P * 16);  // [P]
+  const int S = I / 64, groups = H / 256;
+  char* wst = dsm + (size_t)warp * 2 * stage_bytes;  // this warp's two stages
+  float* o_s = reinterpret_cast<float*>(dsm + (size_t)w2_warps * 2 * stage_bytes);  // [P][16]
+  unsigned char* valid = reinterpret_cast<unsigned char*>(o_s + (size_t)P * 16);    // [P]
+  const bool worker = warp < w2_warps;
+  if (worker && lane == 0) {
+    mbar_init(&full[warp][0], 1);
+    mbar_init(&full[warp][1], 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
   // ---- everything that comes from the plan grid (complete before W13 began) ----
   for (int q = tid; q < P; q += kW2Warps * 32) valid[q] = __ldcg(p.pv.inv + q) >= 0;
   const int n_act = min(__ldcg(&p.pv.hdr->n_active), p.max_active);
-  // this warp's experts: a = warp, warp + 16, ...; lanes 0..19 hold the entry
-  int a = warp;
-  int ent_v = (a < n_act && lane < kDtabInts) ? __ldcg(p.pv.dtab + a * kDtabInts + lane) : -1;
-  uint4 q[8];
-  uint32_t sc[8];
-  float wsc = 0.f;  // lane n < 16: g2 * combine weight of the entry's row n
-  int pair_l = -1;  // lane n < 16: pair id of row n
-  auto load_expert = [&]() {
-    const int e = __shfl_sync(0xffffffffu, ent_v, 0);
-    const int base = __shfl_sync(0xffffffffu, ent_v, 1);
-    const int count = __shfl_sync(0xffffffffu, ent_v, 2);
-    const int pr = __shfl_sync(0xffffffffu, ent_v, (4 + lane) & 31);
-    if (!entry_ok(p, e, base, count)) return false;
-    const bool sh = (e == d.E);
-    const uint8_t* qe = sh ? p.s2.q : p.w2.q + (size_t)e * H * I / 2;
-    const uint8_t* se = sh ? p.s2.s : p.w2.s + (size_t)e * H * I / 16;
-    const uint8_t* qt = qe + (size_t)(rt >> 4) * S * 16 * 512 + (rt & 15) * 512;
-    const uint8_t* st = se + (size_t)(rt >> 4) * S * 16 * 64 + (rt & 15) * 64;
-#pragma unroll
-    for (int j = 0; j < 8; ++j)
-      if (j < S) {
-        q[j] = ldg_nc_v4(qt + (size_t)j * 16 * 512 + lane * 16);
-        sc[j] = ldg_u16(st + (size_t)j * 16 * 64 + lane * 2);
-      }
-    const float gsc = sh ? p.s2.g[0] : p.w2.g[e];
-    pair_l = (lane < 16 && lane < count) ? pr : -1;
-    if (pair_l >= P) pair_l = -1;
-    wsc = pair_l >= 0 ? gsc * __ldcg(p.pv.w + pair_l) : 0.f;
-    return true;
+  const uint32_t tx = (uint32_t)S * (512 + 64);
+  // chunk r of this warp = expert a = warp + r * w2_warps, in stage r % 2
+  auto entry = [&](int r) {
+    const int a = warp + r * w2_warps;
+    return (a < n_act && lane < kDtabInts) ? __ldcg(p.pv.dtab + a * kDtabInts + lane) : -1;
   };
-  bool have = (a < n_act) && load_expert();
+  // issues chunk r (entry values in lanes 0..19 of ev); returns, on every
+  // lane, whether a copy was issued
+  auto issue = [&](int r, int ev) {
+    const int e = __shfl_sync(0xffffffffu, ev, 0);
+    const int base = __shfl_sync(0xffffffffu, ev, 1);
+    const int count = __shfl_sync(0xffffffffu, ev, 2);
+    const bool go = warp + r * w2_warps < n_act && entry_ok(p, e, base, count);
+    if (go && lane == 0) {
+      const bool sh = (e == d.E);
+      const int row0 = frag_map_row(sh ? 0 : e, groups, rt >> 4, S, 0);
+      char* st = wst + (r & 1) * stage_bytes;
+      uint64_t* bar = &full[warp][r & 1];
+      mbar_expect_tx(bar, tx);
+      tma_load_2d(st, sh ? &mqs : &mq, (rt & 15) * 64, row0, bar);
+      tma_load_2d(st + S * 512, sh ? &mss : &ms, (rt & 15) * 8, row0, bar);
+    }
+    return go;
+  };
+  int ent_cur = -1, ent_next = -1;
+  float wsc = 0.f;
+  int pair_l = -1;
+  bool iss_cur = false, iss_next = false;  // chunk r / r + 1 has a copy in flight
+  if (worker) {
+    ent_cur = entry(0);
+    ent_next = entry(1);
+    iss_cur = issue(0, ent_cur);
+    iss_next = issue(1, ent_next);
+  }
+  auto pairs_of = [&](int ev) {
+    const int e = __shfl_sync(0xffffffffu, ev, 0);
+    const int count = __shfl_sync(0xffffffffu, ev, 2);
+    const int pr = __shfl_sync(0xffffffffu, ev, (4 + lane) & 31);
+    pair_l = (lane < 16 && lane < count && pr >= 0 && pr < P) ? pr : -1;
+    const bool sh = (e == d.E);
+    const float gsc = (e >= 0 && (e < d.E || (sh && d.shared))) ? (sh ? p.s2.g[0] : p.w2.g[e]) : 0.f;
+    wsc = pair_l >= 0 ? gsc * __ldcg(p.pv.w + pair_l) : 0.f;
+  };
+  if (worker) pairs_of(ent_cur);
   pdl_wait();
   MOE_TL_WAITED();
-  // ---- h rows (written by the W13 grid) ----
-  for (; a < n_act; a += kW2Warps) {
-    if (a != warp) {
-      ent_v = (lane < kDtabInts) ? __ldcg(p.pv.dtab + a * kDtabInts + lane) : -1;
-      have = load_expert();
-    }
-    if (!have) continue;
-    const int e = __shfl_sync(0xffffffffu, ent_v, 0);
-    const int base = __shfl_sync(0xffffffffu, ent_v, 1);
-    const int count = __shfl_sync(0xffffffffu, ent_v, 2);
-    const bool sh = (e == d.E);
-    const uint8_t* qe = sh ? p.s2.q : p.w2.q + (size_t)e * H * I / 2;
-    const uint8_t* se = sh ? p.s2.s : p.w2.s + (size_t)e * H * I / 16;
-    const uint8_t* qt = qe + (size_t)(rt >> 4) * S * 16 * 512 + (rt & 15) * 512;
-    const uint8_t* st = se + (size_t)(rt >> 4) * S * 16 * 64 + (rt & 15) * 64;
-    const float gsc = sh ? p.s2.g[0] : p.w2.g[e];
-    for (int n0 = 0; n0 < count; n0 += 8) {
-      const int n = n0 + g;  // this lane's B column (token row of the expert)
-      // pair and scale of column n: rows below 16 come from the table (lanes
-      // n of pair_l / wsc), later rows from the plan
-      int pair_n = __shfl_sync(0xffffffffu, pair_l, n & 15);
-      float wsc_n = __shfl_sync(0xffffffffu, wsc, n & 15);
-      if (n >= 16 && n < count) {
-        pair_n = __ldcg(p.pv.perm + base + n);
-        if (pair_n < 0 || pair_n >= P) pair_n = -1;
-        wsc_n = pair_n >= 0 ? gsc * __ldcg(p.pv.w + pair_n) : 0.f;
-      }
-      if (n >= count) pair_n = -1;
-      float acc[4] = {0.f, 0.f, 0.f, 0.f};
-      for (int ks0 = 0; ks0 < S; ks0 += 8) {
-        if (ks0 > 0 || n0 > 0) {
+  bool ok = true;
+  int r = 0;
+  if (worker) {
+    for (; warp + r * w2_warps < n_act; ++r) {
+      if (r > 0) pairs_of(ent_cur);
+      const int e = __shfl_sync(0xffffffffu, ent_cur, 0);
+      const int base = __shfl_sync(0xffffffffu, ent_cur, 1);
+      const int count = __shfl_sync(0xffffffffu, ent_cur, 2);
+      if (iss_cur) {
+        if (!mbar_wait(&full[warp][r & 1], (r >> 1) & 1, p.status)) {
+          ok = false;
+          break;
+        }
+        const bool sh = (e == d.E);
+        const float gsc = sh ? p.s2.g[0] : p.w2.g[e];
+        const char* sq = wst + (r & 1) * stage_bytes;
+        const char* ss = sq + S * 512;
+        for (int n0 = 0; n0 < count; n0 += 8) {
+          const int n = n0 + g;
+          int pair_n = __shfl_sync(0xffffffffu, pair_l, n & 15);
+          float wsc_n = __shfl_sync(0xffffffffu, wsc, n & 15);
+          if (n >= 16 && n < count) {
+            pair_n = __ldcg(p.pv.perm + base + n);
+            if (pair_n < 0 || pair_n >= P) pair_n = -1;
+            wsc_n = pair_n >= 0 ? gsc * __ldcg(p.pv.w + pair_n) : 0.f;
+          }
+          if (n >= count) pair_n = -1;
+          float acc[4] = {0.f, 0.f, 0.f, 0.f};
+          for (int ks0 = 0; ks0 < S; ks0 += 8) {
+            uint4 hv[8][2];
 #pragma unroll
-          for (int j = 0; j < 8; ++j)
-            if (ks0 + j < S) {
-              q[j] = ldg_nc_v4(qt + (size_t)(ks0 + j) * 16 * 512 + lane * 16);
-              sc[j] = ldg_u16(st + (size_t)(ks0 + j) * 16 * 64 + lane * 2);
+            for (int j = 0; j < 8; ++j) {
+              if (ks0 + j < S && n < count) {
+                const __half* src = p.h + (int64_t)(base + n) * I + (ks0 + j) * 64 + 16 * t4;
+                hv[j][0] = __ldcg(reinterpret_cast<const uint4*>(src));
+                hv[j][1] = __ldcg(reinterpret_cast<const uint4*>(src) + 1);
+              } else {
+                hv[j][0] = hv[j][1] = make_uint4(0u, 0u, 0u, 0u);
+              }
             }
-        }
-        // B fragments: column n = row (base + n) of h, 16 K values per segment
-        uint4 hv[8][2];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          if (ks0 + j < S && n < count) {
-            const __half* src = p.h + (int64_t)(base + n) * I + (ks0 + j) * 64 + 16 * t4;
-            hv[j][0] = __ldcg(reinterpret_cast<const uint4*>(src));
-            hv[j][1] = __ldcg(reinterpret_cast<const uint4*>(src) + 1);
-          } else {
-            hv[j][0] = hv[j][1] = make_uint4(0u, 0u, 0u, 0u);
+            for (int j = 0; j < 8; ++j) {
+              const int ks = ks0 + j;
+              if (ks >= S) break;
+              const uint4 q = *reinterpret_cast<const uint4*>(sq + ks * 512 + lane * 16);
+              const uint32_t sc = *reinterpret_cast<const unsigned short*>(ss + ks * 64 + lane * 2);
+              uint32_t sg, sg8;
+              scale_splats(sc, &sg, &sg8);
+              const uint32_t xw[8] = {hv[j][0].x, hv[j][0].y, hv[j][0].z, hv[j][0].w,
+                                      hv[j][1].x, hv[j][1].y, hv[j][1].z, hv[j][1].w};
+#pragma unroll
+              for (int s = 0; s < 4; ++s) {
+                uint32_t af[4];
+                a_frag(q, sg, sg8, s, af);
+                mma_16816(acc, af, xw[2 * s], xw[2 * s + 1]);
+              }
+            }
           }
-        }
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          if (ks0 + j >= S) break;
-          uint32_t sg, sg8;
-          scale_splats(sc[j], &sg, &sg8);
-          const uint32_t xw[8] = {hv[j][0].x, hv[j][0].y, hv[j][0].z, hv[j][0].w,
-                                  hv[j][1].x, hv[j][1].y, hv[j][1].z, hv[j][1].w};
-#pragma unroll
-          for (int s = 0; s < 4; ++s) {
-            uint32_t af[4];
-            a_frag(q[j], sg, sg8, s, af);
-            mma_16816(acc, af, xw[2 * s], xw[2 * s + 1]);
+          for (int c = 0; c < 4; ++c) {
+            const int col = 2 * t4 + (c & 1);
+            const int pr = __shfl_sync(0xffffffffu, pair_n, col * 4);
+            const float ws = __shfl_sync(0xffffffffu, wsc_n, col * 4);
+            if (pr >= 0) o_s[pr * 16 + g + ((c & 2) ? 8 : 0)] = acc[c] * ws;
           }
         }
       }
-      // c0: (row g, col 2t4), c1: (g, 2t4+1), c2: (g+8, 2t4), c3: (g+8, 2t4+1)
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const int col = 2 * t4 + (c & 1);
-        const int pr = __shfl_sync(0xffffffffu, pair_n, col * 4);
-        const float ws = __shfl_sync(0xffffffffu, wsc_n, col * 4);
-        if (pr >= 0) o_s[pr * 16 + g + ((c & 2) ? 8 : 0)] = acc[c] * ws;
-      }
+      __syncwarp();  // every lane is done with stage r & 1
+      ent_cur = ent_next;
+      iss_cur = iss_next;
+      ent_next = entry(r + 2);
+      iss_next = issue(r + 2, ent_next);
+    }
+    if (!ok && lane == 0) {
+      // timed out: let the copies already issued land before the block exits
+      // (each wait bounded by the same limit)
+      mbar_wait(&full[warp][r & 1], (r >> 1) & 1, p.status);
+      if (iss_next) mbar_wait(&full[warp][(r + 1) & 1], ((r + 1) >> 1) & 1, p.status);
     }
   }
   __syncthreads();
@@ -437,11 +483,14 @@ cudaError_t launch_combine(const LayerDims& d, int64_t M, const PlanView& pv,
                   (const int32_t*)pv.inv, partial, y);
 }
 
+static constexpr size_t kDecSmemLimit = 225 * 1024;
+
 template <int NT>
 static cudaError_t decode_impl(const LayerDims& d, int64_t M, const __half* x, const PlanView& pv,
                                Weights w13, Weights w2, Weights s13, Weights s2, __half* y,
-                               __half* h, cudaStream_t stream, int num_sms) {
+                               __half* h, uint32_t* status, cudaStream_t stream, int num_sms) {
   DecodeArgs a;
+  a.status = status;
   a.d = d;
   a.pv = pv;
   a.x = x;
@@ -454,25 +503,28 @@ static cudaError_t decode_impl(const LayerDims& d, int64_t M, const __half* x, c
   a.M = (int)M;
   a.max_active = (int)((M * d.k_eff < d.e_eff) ? M * d.k_eff : d.e_eff);
   const int P = (int)(M * d.k_eff);
-  const size_t smem13 = align_up((size_t)M * (d.H * 2 + 16), 16) + 8 * 2 * NT * 32 * 4 * sizeof(float);
-  const size_t smem2 = (size_t)P * 16 * sizeof(float) + P;
-  // once per process: shared-memory ceilings and the W13 blocks per SM
-  static int w13_per_sm[2] = {-1, -1};
-  int& bps = w13_per_sm[M <= 8 ? 0 : 1];
-  if (bps < 0) {
-    const int big13 = 16 * (4096 * 2 + 16) + 8 * 2 * NT * 32 * 4 * (int)sizeof(float);
-    cudaError_t e = cudaFuncSetAttribute(decode_w13_kernel<NT>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, big13);
-    if (e != cudaSuccess) return e;
-    const int big2 = kDecodeMaxTokens * 33 * (16 * (int)sizeof(float) + 1);
-    e = cudaFuncSetAttribute(decode_w2_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             big2);
-    if (e != cudaSuccess) return e;
-    bps = 0;
+  const int S2 = d.I / 64;
+  const size_t smem13 =
+      align_up((size_t)M * (d.H * 2 + 16), 16) + (size_t)8 * 2 * NT * 32 * 4 * sizeof(float);
+  const int st2 = (int)align_up((size_t)S2 * (512 + 64), 1024);
+  const size_t o_b = (size_t)P * 16 * sizeof(float) + P;
+  // W2: as many expert warps as two ring stages each allow (at least one:
+  // 2 x 37 KB + 34 KB at the largest I and M)
+  const int w2_warps =
+      (int)std::min<size_t>(kW2Warps, (kDecSmemLimit - 1024 - o_b) / (2 * (size_t)st2));
+  if (w2_warps < 1) return cudaErrorInvalidValue;
+  static bool attr_done = false;
+  if (!attr_done) {
+    for (auto f : {(const void*)decode_w13_kernel<NT>, (const void*)decode_w2_kernel<NT>}) {
+      cudaError_t e =
+          cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDecSmemLimit);
+      if (e != cudaSuccess) return e;
+    }
+    attr_done = true;
   }
   int per_sm = 0;
-  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_w13_kernel<NT>,
-                                                                256, smem13);
+  cudaError_t e =
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_w13_kernel<NT>, 256, smem13);
   if (e != cudaSuccess) return e;
   const int n_items = a.max_active * (d.I / 16);
   const int g13 = std::max(1, std::min(n_items, num_sms * std::max(per_sm, 1)));
@@ -482,7 +534,20 @@ static cudaError_t decode_impl(const LayerDims& d, int64_t M, const __half* x, c
   if (e != cudaSuccess) return e;
   trace_mark(stream, kTraceW13, true);
   trace_mark(stream, kTraceW2, false);
-  e = launch_k(decode_w2_kernel<NT>, dim3(d.H / 16), dim3(kW2Warps * 32), smem2, stream, pdl, a);
+  CUtensorMap mq, ms, mqs, mss;
+  const uint64_t rows = (uint64_t)d.E * (d.H / 256) * S2;
+  const uint64_t rows_sh = (uint64_t)(d.H / 256) * S2;
+  if ((e = make_rows_map(&mq, w2.q, 16 * 512, rows, 512, S2)) != cudaSuccess) return e;
+  if ((e = make_rows_map(&ms, w2.s, 16 * 64, rows, 64, S2)) != cudaSuccess) return e;
+  mqs = mq;
+  mss = ms;
+  if (d.shared) {
+    if ((e = make_rows_map(&mqs, s2.q, 16 * 512, rows_sh, 512, S2)) != cudaSuccess) return e;
+    if ((e = make_rows_map(&mss, s2.s, 16 * 64, rows_sh, 64, S2)) != cudaSuccess) return e;
+  }
+  const size_t smem2 = 1024 + (size_t)w2_warps * 2 * st2 + o_b;
+  e = launch_k(decode_w2_kernel<NT>, dim3(d.H / 16), dim3(kW2Warps * 32), smem2, stream, pdl, a,
+               w2_warps, st2, mq, ms, mqs, mss);
   if (e != cudaSuccess) return e;
   trace_mark(stream, kTraceW2, true);
   // the combine is part of the W2 kernel on this path
@@ -496,9 +561,8 @@ cudaError_t launch_decode_forward(const LayerDims& d, int64_t M, const __half* x
                                   Weights s2, __half* y, __half* h, float* partial,
                                   uint32_t* status, cudaStream_t stream, int num_sms) {
   (void)partial;
-  (void)status;
-  if (M <= 8) return decode_impl<1>(d, M, x, pv, w13, w2, s13, s2, y, h, stream, num_sms);
-  return decode_impl<2>(d, M, x, pv, w13, w2, s13, s2, y, h, stream, num_sms);
+  if (M <= 8) return decode_impl<1>(d, M, x, pv, w13, w2, s13, s2, y, h, status, stream, num_sms);
+  return decode_impl<2>(d, M, x, pv, w13, w2, s13, s2, y, h, status, stream, num_sms);
 }
 
 }  // namespace moe

@@ -2,6 +2,7 @@
 // kernel translation units.  Launchers assume validated arguments.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -44,6 +45,11 @@ cudaError_t launch_prefill_forward(const LayerDims& d, int64_t M, const __half* 
                                    uint32_t* status, cudaStream_t stream, int num_sms);
 cudaError_t launch_combine(const LayerDims& d, int64_t M, const PlanView& pv,
                            const float* partial, __half* y, cudaStream_t stream, bool pdl);
+
+// TMA tensor map over a byte matrix of `rows` x `row_bytes`, 8-byte elements,
+// box `box_bytes` x `box_rows` (tma.cu).
+cudaError_t make_rows_map(CUtensorMap* map, const void* base, uint64_t row_bytes, uint64_t rows,
+                          uint32_t box_bytes, uint32_t box_rows);
 
 // Diagnostic per-step event records (moe_nvfp4_set_trace_events).
 enum TraceStep { kTracePlan = 0, kTraceW13 = 1, kTraceW2 = 2, kTraceCombine = 3 };

@@ -193,6 +193,7 @@ __device__ void plan_small_block(const LayerDims& d, int M, const int* src, cons
   }
   if (bad) set_status(status, MOE_ST_INVALID_ID);
   __syncthreads();
+  if (tid == 0) MOE_TL_MAX(36);
   // experts [3 tid, 3 tid + 3): counts, active flags, tiles -> block scan
   int c3[3], sc = 0, sa = 0, st = 0;
 #pragma unroll
@@ -204,6 +205,7 @@ __device__ void plan_small_block(const LayerDims& d, int M, const int* src, cons
   }
   int tot[3];
   block_scan3(sc, sa, st, tot);
+  if (tid == 0) MOE_TL_MAX(38);
 #pragma unroll
   for (int j = 0; j < 3; ++j) {
     const int e = 3 * tid + j;
@@ -231,6 +233,7 @@ __device__ void plan_small_block(const LayerDims& d, int M, const int* src, cons
     pv.hdr->n_tiles = tot[2];
   }
   __syncthreads();
+  if (tid == 0) MOE_TL_MAX(40);
   for (int p = tid; p < P; p += nthr) {
     const int e = s_ids[p];
     if (e < 0) {
@@ -245,6 +248,7 @@ __device__ void plan_small_block(const LayerDims& d, int M, const int* src, cons
     pv.inv[p] = pos;
   }
   __syncthreads();
+  if (tid == 0) MOE_TL_MAX(42);
   // decode work table: every entry up to the largest active-expert count
   const int n_active = tot[1];
   const int max_active = min(P, ne);
@@ -393,6 +397,7 @@ __global__ void __launch_bounds__(256) router_small_kernel(LayerDims d, int M,
     int id;
     float l;
     warp_topk<true>(pv.logits + (int64_t)m * E, E, d.k, &id, &l);
+    if (m == 0 && lane == 0) MOE_TL_MAX(46);
     const float w = warp_topk_weight(l, d.k);
     const float gamma = d.shared ? warp_gate(x + (int64_t)m * H, wg, H) : 0.f;
     store_route(d, m, id, w, gamma, ids_user, w_user, pv);
@@ -727,6 +732,293 @@ __global__ void plan_scatter_kernel(LayerDims d, int64_t P, PlanView pv) {
 }
 
 // ---------------------------------------------------------------------------
+// Small-M router + plan as one thread-block cluster of C CTAs (C = 16, or 8
+// where 16 cannot be scheduled).  CTA r owns rows [r H / C, (r + 1) H / C) of
+// W_r: the rows arrive by bulk copies into padded shared-memory rows (a ring
+// of 32-row tiles) and meet the staged token rows in mma.sync (FP32
+// accumulate), giving partial logits for all experts.  After a cluster
+// barrier CTA r sums expert slice r over the C partials in a fixed order
+// through distributed shared memory (+ bias) into CTA 0; after a second
+// barrier CTA 0 runs top-k, the weights, the gate and the whole plan.
+// ---------------------------------------------------------------------------
+constexpr int kRcTileRows = 32;
+constexpr int kRcMaxStages = 4;
+constexpr int kRcThreads = 256;
+constexpr int kRcMaxClusterCtas = 16;
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_nctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::
+                   : "memory");
+}
+// Address of the same shared-memory location in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t dsmem_addr(const void* p, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ float ld_dsmem_f32(uint32_t a) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(a) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_dsmem_f32(uint32_t a, float v) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(a), "f"(v) : "memory");
+}
+
+struct RouterClusterSmem {
+  int stages;
+  size_t ring, xs, part, logits, gpart, total;
+};
+
+__host__ __device__ inline RouterClusterSmem router_cluster_smem(int H, int E, int C) {
+  RouterClusterSmem s;
+  const size_t tile = (size_t)kRcTileRows * (E + 8) * 2;
+  const int R = H / C;
+  const int ntiles = (R + kRcTileRows - 1) / kRcTileRows;
+  s.xs = align_up((size_t)kDecodeMaxTokens * (R + 8) * 2, 128);
+  s.part = (size_t)kDecodeMaxTokens * E * 4;
+  s.logits = (size_t)kDecodeMaxTokens * E * 4;
+  s.gpart = 128;
+  const size_t fixed = s.xs + s.part + s.logits + s.gpart;
+  const size_t budget = 200 * 1024;
+  int st = (int)((budget > fixed ? budget - fixed : 0) / tile);
+  st = st > kRcMaxStages ? kRcMaxStages : st;
+  st = st > ntiles ? ntiles : st;
+  s.stages = st;
+  s.ring = (size_t)st * tile;
+  s.total = 128 + s.ring + fixed;
+  return s;
+}
+
+__global__ void __launch_bounds__(kRcThreads, 1)
+    router_cluster_kernel(LayerDims d, int M, const __half* __restrict__ x,
+                          const __half* __restrict__ wr, const float* __restrict__ bias,
+                          const __half* __restrict__ wg, int32_t* ids_user, float* w_user,
+                          PlanView pv, uint32_t* status) {
+  extern __shared__ __align__(128) char rsm_raw[];
+  char* rsm = reinterpret_cast<char*>((reinterpret_cast<uintptr_t>(rsm_raw) + 127) &
+                                      ~uintptr_t(127));
+  __shared__ uint64_t full[kRcMaxStages];
+  __shared__ int s_ids[kDecodeMaxTokens * 33];
+  MOE_TL(kTlRouter);
+  const int E = d.E, H = d.H;
+  const uint32_t C = cluster_nctarank(), rank = cluster_ctarank();
+  const int R = H / (int)C, h0 = (int)rank * R;
+  const RouterClusterSmem L = router_cluster_smem(H, E, (int)C);
+  const int stages = L.stages;
+  const int ntiles = (R + kRcTileRows - 1) / kRcTileRows;
+  const int rstride = (E + 8) * 2;  // padded W_r row in shared memory, bytes
+  const size_t tile_b = (size_t)kRcTileRows * rstride;
+  char* ring = rsm;
+  __half* xs = reinterpret_cast<__half*>(rsm + L.ring);                 // [16][R + 8]
+  float* part = reinterpret_cast<float*>(rsm + L.ring + L.xs);          // [16][E]
+  float* logit = reinterpret_cast<float*>(rsm + L.ring + L.xs + L.part);  // [16][E] (CTA 0)
+  float* gpart = reinterpret_cast<float*>(rsm + L.ring + L.xs + L.part + L.logits);  // [16]
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g = lane >> 2, t4 = lane & 3;
+
+  if (tid == 0) {
+    for (int i = 0; i < stages; ++i) mbar_init(&full[i], 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  // tile t: rows [h0 + 32 t, +32) of W_r, one bulk copy per row (lane = row)
+  auto issue = [&](int t) {
+    const int s = t % stages;
+    const int r0 = t * kRcTileRows;
+    const int nr = min(kRcTileRows, R - r0);
+    if (lane == 0) mbar_expect_tx(&full[s], (uint32_t)(nr * E * 2));
+    __syncwarp();
+    if (lane < nr)
+      bulk_g2s(ring + s * tile_b + (size_t)lane * rstride, wr + (int64_t)(h0 + r0 + lane) * E,
+               (uint32_t)(E * 2), &full[s]);
+  };
+  if (warp == 0)
+    for (int t = 0; t < stages && t < ntiles; ++t) issue(t);
+  // token rows of the chunk (rows >= M are zero) and the gate's partial dot
+  for (int i = tid; i < kDecodeMaxTokens * R; i += kRcThreads) {
+    const int m = i / R, k = i - m * R;
+    xs[m * (R + 8) + k] = (m < M) ? x[(int64_t)m * H + h0 + k] : __float2half(0.f);
+  }
+  if (d.shared)
+    for (int m = warp; m < M; m += kRcThreads / 32) {
+      float z = 0.f;
+      for (int k = lane; k < R; k += 32)
+        z = fmaf(__half2float(x[(int64_t)m * H + h0 + k]), __half2float(wg[h0 + k]), z);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+      if (lane == 0) gpart[m] = z;
+    }
+  __syncthreads();
+
+  // ---- partial logits: [16 tokens] x [E experts] over this CTA's rows ----
+  // warp w takes expert pairs j = w, w + 8, ... (16 experts each; the padded
+  // columns E .. E + 7 of a final half pair are computed and ignored)
+  const int npairs = (E + 15) / 16;
+  constexpr int kMaxPairs = 4;  // E <= 512
+  float acc[kMaxPairs][2][4];
+#pragma unroll
+  for (int j = 0; j < kMaxPairs; ++j)
+#pragma unroll
+    for (int t = 0; t < 2; ++t)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) acc[j][t][c] = 0.f;
+  bool ok = true;
+  int t = 0;
+  for (; t < ntiles; ++t) {
+    const int s = t % stages;
+    const bool got = mbar_wait(&full[s], (t / stages) & 1, status);
+    if (__syncthreads_and(got ? 1 : 0) == 0) {
+      ok = false;
+      break;
+    }
+    const char* tb = ring + s * tile_b;
+    const int r0 = t * kRcTileRows;
+    const int nr = min(kRcTileRows, R - r0);
+    for (int k0 = 0; k0 < nr; k0 += 16) {
+      uint32_t a[4];
+      {
+        const int row = (lane & 7) + 8 * ((lane >> 3) & 1);
+        const int col = r0 + k0 + 8 * (lane >> 4);
+        ldsm_x4(a, xs + row * (R + 8) + col);
+      }
+#pragma unroll
+      for (int j = 0; j < kMaxPairs; ++j) {
+        const int pj = warp + 8 * j;
+        if (pj < npairs) {
+          uint32_t b[4];
+          const int krow = k0 + (lane & 7) + 8 * ((lane >> 3) & 1);
+          const int ncol = pj * 16 + 8 * (lane >> 4);
+          ldsm_x4_t(b, tb + (size_t)krow * rstride + ncol * 2);
+          mma_16816(acc[j][0], a, b[0], b[1]);
+          mma_16816(acc[j][1], a, b[2], b[3]);
+        }
+      }
+    }
+    __syncthreads();  // every warp is done with stage s
+    if (warp == 0 && t + stages < ntiles) issue(t + stages);
+  }
+  if (!ok && tid == 0) {
+    // a copy timed out: let the copies already issued land before leaving
+    // (each wait bounded by the same limit)
+    for (int tt = t; tt < ntiles && tt < t + stages; ++tt)
+      mbar_wait(&full[tt % stages], (tt / stages) & 1, status);
+  }
+  // c0: (token g, expert 2t4), c1: (g, 2t4+1), c2: (g+8, 2t4), c3: (g+8, 2t4+1)
+#pragma unroll
+  for (int j = 0; j < kMaxPairs; ++j) {
+    const int pj = warp + 8 * j;
+    if (pj < npairs)
+#pragma unroll
+      for (int t = 0; t < 2; ++t)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const int e = pj * 16 + t * 8 + 2 * t4 + (c & 1);
+          const int m = g + ((c & 2) ? 8 : 0);
+          if (e < E) part[m * E + e] = acc[j][t][c];
+        }
+  }
+  if (tid == 0) MOE_TL_MAX(20);
+  cluster_sync_all();  // every CTA's partial logits are complete
+  if (tid == 0) MOE_TL_MIN(21);
+
+  // ---- expert slice `rank`: fixed-order sum over the C partials, into CTA 0 ----
+  const int es = (E + (int)C - 1) / (int)C;
+  const int e0 = (int)rank * es;
+  for (int i = tid; i < M * es; i += kRcThreads) {
+    const int m = i / es, e = e0 + (i - m * es);
+    if (e >= E) continue;
+    float v[kRcMaxClusterCtas];
+#pragma unroll
+    for (int c = 0; c < kRcMaxClusterCtas; ++c)
+      if (c < (int)C) v[c] = ld_dsmem_f32(dsmem_addr(part + m * E + e, c));
+    float sum = 0.f;
+#pragma unroll
+    for (int c = 0; c < kRcMaxClusterCtas; ++c)
+      if (c < (int)C) sum += v[c];
+    if (bias) sum += bias[e];
+    st_dsmem_f32(dsmem_addr(logit + m * E + e, 0), sum);
+  }
+  float gamma = 0.f;
+  if (rank == 0 && d.shared && tid < M) {
+    float z = 0.f;
+    for (int c = 0; c < (int)C; ++c) z += ld_dsmem_f32(dsmem_addr(gpart + tid, c));
+    gamma = 1.f / (1.f + expf(-z));
+  }
+  cluster_sync_all();  // CTA 0 holds every logit; no CTA reads another's memory after this
+  if (tid == 0) MOE_TL_MIN(23);
+  if (rank != 0) return;
+  if (d.shared && tid < M) gpart[tid] = gamma;  // CTA 0's own copy: gate values now
+  __syncthreads();
+  if (tid == 0) MOE_TL_MAX(24);
+
+  // ---- top-k, weights, plan (CTA 0) ----
+  for (int m = warp; m < M; m += kRcThreads / 32) {
+    int id;
+    float l;
+    warp_topk<false>(logit + m * E, E, d.k, &id, &l);
+    const float w = warp_topk_weight(l, d.k);
+    store_route(d, m, id, w, d.shared ? gpart[m] : 0.f, ids_user, w_user, pv);
+    if (lane < d.k) s_ids[m * d.k_eff + lane] = id;
+    if (d.shared && lane == 0) s_ids[m * d.k_eff + d.k] = d.E;
+  }
+  __syncthreads();
+  plan_small_block(d, M, s_ids, pv, status);
+  if (tid == 0) MOE_TL_MIN(25);
+}
+
+// Cluster size for the small-M router: 16 CTAs where the device can co-schedule
+// such a cluster with this kernel's shared memory, else 8, else 0 (the
+// 128-block router is used).  Decided once per process and shape class.
+static int router_cluster_size(const LayerDims& d) {
+  static int cached[2] = {-1, -1};  // [E > 256]
+  int& c = cached[d.E > 256 ? 1 : 0];
+  if (c >= 0) return c;
+  c = 0;
+  if (cudaFuncSetAttribute(router_cluster_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed,
+                           1) != cudaSuccess ||
+      cudaFuncSetAttribute(router_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           200 * 1024 + 128) !=
+          cudaSuccess) {
+    cudaGetLastError();
+    return c;
+  }
+  for (int cand : {16, 8}) {
+    if (d.H % (cand * 16) != 0) continue;
+    const RouterClusterSmem L = router_cluster_smem(d.H, d.E, cand);
+    if (L.stages < 1) continue;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(cand);
+    cfg.blockDim = dim3(kRcThreads);
+    cfg.dynamicSmemBytes = L.total;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = cand;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, router_cluster_kernel, &cfg) == cudaSuccess && n >= 1) {
+      c = cand;
+      break;
+    }
+    cudaGetLastError();
+  }
+  return c;
+}
+
+// ---------------------------------------------------------------------------
 cudaError_t launch_plan(const LayerDims& d, int64_t M, const __half* x, const __half* w_router,
                         const float* bias, const __half* w_gate, int32_t* ids_user,
                         float* w_user, bool ids_given, const PlanView& pv, uint32_t* status,
@@ -738,6 +1030,23 @@ cudaError_t launch_plan(const LayerDims& d, int64_t M, const __half* x, const __
       route_given_kernel<<<(Mi + 7) / 8, 256, 0, stream>>>(d, Mi, x, w_gate, ids_user, w_user, pv);
       plan_small_kernel<<<1, 256, 0, stream>>>(d, Mi, pv, status);
     } else {
+      const int C = router_cluster_size(d);
+      if (C > 0) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(C);
+        cfg.blockDim = dim3(kRcThreads);
+        cfg.dynamicSmemBytes = router_cluster_smem(d.H, d.E, C).total;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = C;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        return cudaLaunchKernelEx(&cfg, router_cluster_kernel, d, Mi, x, w_router, bias, w_gate,
+                                  ids_user, w_user, pv, status);
+      }
       dim3 grid((d.E + 63) / 64, d.H / kRsRows);
       router_small_kernel<<<grid, 256, 0, stream>>>(d, Mi, x, w_router, bias, w_gate, ids_user,
                                                      w_user, pv, status);

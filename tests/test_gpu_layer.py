@@ -164,6 +164,14 @@ def test_forward_tiny_shared_expert():
     _forward_check(Case(wl))
 
 
+@pytest.mark.parametrize("M,H,E,k,I", [(4, 512, 16, 2, 1024), (16, 4096, 8, 2, 256),
+                                       (40, 512, 16, 2, 1024), (40, 4096, 8, 2, 256)])
+def test_forward_other_shapes(M, H, E, k, I):
+    """Shapes away from the benchmark: K = I of 16 segments in W2, H = 4096
+    (the largest hidden size), decode and prefill buckets."""
+    _forward_check(Case(synth.custom("shape", M, H, E, k, I)))
+
+
 def test_forward_decode_m1_full():
     _forward_check(Case(DEC1))
 
