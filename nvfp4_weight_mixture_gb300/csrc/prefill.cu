@@ -19,8 +19,9 @@
 //              A tiles (2-deep ring), then run the unit's epilogue;
 //   warps 4-7  gather the unit's token rows with 16-byte cp.async into the
 //              same swizzled layout, in chunks of 64 rows (a 12-slot ring);
-//              warp 4 + (c % 4) owns chunk c and keeps two of its own chunks
-//              in flight, so up to eight chunks load ahead of the MMAs;
+//              warp 4 + (c % 4) owns chunk c, and its lanes announce the
+//              chunk on the slot barrier as their copies land, so the whole
+//              ring loads ahead of the MMAs;
 //   warp 8     allocates tensor memory; one lane issues the MMAs: per K step and
 //              A tile one MMA with N = all of the tile's rows, split in two only
 //              where the step's chunks wrap around the end of the B ring.
@@ -249,6 +250,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             }
             if (!ok) break;
             MOE_PROF(PROF_ADD(poff + 5, t0); t0 = clock64());
+            // the chunks were written by cp.async (generic proxy) and are read
+            // by the MMA (async proxy)
+            fence_proxy_async();
             tc_fence_after();
             const int n = min(run * kBChunkRows, un.npad - ch * kBChunkRows);
             const uint32_t idesc = idesc_f16_f32(128, n);
@@ -279,13 +283,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
   } else if (warp >= 4) {
     // ---- B producer: gather the unit's rows with cp.async -------------------------
-    // Chunk kc (64 rows of one K step) belongs to warp 4 + kc % 4.  A warp
-    // announces its chunk j once chunk j + 2 is issued (its own two-deep
-    // cp.async window), after its copies landed and were fenced for tcgen05.
+    // Chunk kc (64 rows of one K step) belongs to warp 4 + kc % 4.  Each lane
+    // announces its copies of the chunk on the slot's barrier as they land
+    // (cp.async.mbarrier.arrive), so a warp never waits for its own data and
+    // the whole ring can be in flight.
     const int bw = warp - 4;
     uint32_t kc = 0, it = 0;
-    uint32_t pend[3];  // this warp's chunk slots not yet announced (oldest first)
-    int npend = 0;
     for (int u = blockIdx.x; u < n_units && !*abort; u += gridDim.x, ++it) {
       const Unit un = load_unit<kW13>(d, pv, w, ws, u, upt);
       int* src = sm->bsrc[it & 1];
@@ -320,16 +323,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
               p = bsrc + (int64_t)(in ? un.pos0 + row : 0) * d.I + ks * kBK + c * 8;
             cp_async16(bt + sw128_off(n, c), p, in ? 16u : 0u);
           }
-          cp_async_commit();
-          pend[npend++] = bs;
-          if (npend == 3) {
-            cp_async_wait<2>();
-            fence_proxy_async();
-            mbar_arrive(&sm->b_full[pend[0]]);
-            pend[0] = pend[1];
-            pend[1] = pend[2];
-            npend = 2;
-          }
+          cp_async_arrive_noinc(&sm->b_full[bs]);
           MOE_PROF(if (lane == 0) PROF_ADD(poff + 9, t0));
         }
       }
@@ -337,9 +331,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       named_bar_sync(2, 128);
       if (!ok) break;
     }
+    // every copy this thread issued lands before the block exits
     cp_async_wait<0>();
-    fence_proxy_async();
-    for (int i = 0; i < npend; ++i) mbar_arrive(&sm->b_full[pend[i]]);
   } else {
     // ---- warps 0-3: dequantise, then the unit's epilogue ---------------------------
     const int g = lane >> 2, c = lane & 3;
