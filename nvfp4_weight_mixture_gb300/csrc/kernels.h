@@ -50,6 +50,10 @@ cudaError_t launch_combine(const LayerDims& d, int64_t M, const PlanView& pv,
 // box `box_bytes` x `box_rows` (tma.cu).
 cudaError_t make_rows_map(CUtensorMap* map, const void* base, uint64_t row_bytes, uint64_t rows,
                           uint32_t box_bytes, uint32_t box_rows);
+// TMA tensor map over an FP16 matrix rows x cols, box box_cols x box_rows,
+// optionally 128-byte swizzled (tma.cu).
+cudaError_t make_fp16_map(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows,
+                          uint32_t box_cols, uint32_t box_rows, bool swizzle128);
 
 // Diagnostic per-step event records (moe_nvfp4_set_trace_events).
 enum TraceStep { kTracePlan = 0, kTraceW13 = 1, kTraceW2 = 2, kTraceCombine = 3 };

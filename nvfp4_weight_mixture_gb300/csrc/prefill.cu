@@ -17,11 +17,11 @@
 //              shared ring with two bulk asynchronous copies per K step;
 //   warps 0-3  dequantise each raw stage into 128-byte-swizzled K-major FP16
 //              A tiles (2-deep ring), then run the unit's epilogue;
-//   warps 4-7  gather the unit's token rows with 16-byte cp.async into the
-//              same swizzled layout, in chunks of 64 rows (a 12-slot ring);
-//              warp 4 + (c % 4) owns chunk c, and its lanes announce the
-//              chunk on the slot barrier as their copies land, so the whole
-//              ring loads ahead of the MMAs;
+//   warps 4-7  fill the token-row operand in chunks of 64 rows (a 12-slot
+//              ring, same swizzled layout): W13 gathers x rows with 16-byte
+//              cp.async, chunk c by warp 4 + c % 4, whose lanes announce it on
+//              the slot barrier as their copies land; W2 loads 64 consecutive
+//              h rows per chunk with one tensor-map load;
 //   warp 8     allocates tensor memory; one lane issues the MMAs: per K step and
 //              A tile one MMA with N = all of the tile's rows, split in two only
 //              where the step's chunks wrap around the end of the B ring.
@@ -134,8 +134,9 @@ __device__ __forceinline__ Unit load_unit(const LayerDims& d, const PlanView& pv
 
 template <bool kW13>
 __global__ void __launch_bounds__(kGemmThreads, 1)
-    grouped_gemm_kernel(LayerDims d, PlanView pv, const __half* __restrict__ bsrc, Weights w,
-                        Weights ws, __half* __restrict__ h_out, float* __restrict__ partial,
+    grouped_gemm_kernel(LayerDims d, PlanView pv, const __half* __restrict__ xsrc,
+                        const __grid_constant__ CUtensorMap hmap, Weights w, Weights ws,
+                        __half* __restrict__ h_out, float* __restrict__ partial,
                         uint32_t* status) {
   extern __shared__ __align__(1024) char smem_raw[];
   char* base = reinterpret_cast<char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -159,7 +160,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       mbar_init(&sm->a_empty[i], 1);
     }
     for (int i = 0; i < kBSlots; ++i) {
-      mbar_init(&sm->b_full[i], 32);   // the one gather warp that owns the chunk
+      // W13: the 32 lanes of the gather warp that owns the chunk; W2: the
+      // loading thread (plus the transaction bytes)
+      mbar_init(&sm->b_full[i], kW13 ? 32 : 1);
       mbar_init(&sm->b_empty[i], 1);
     }
     mbar_init(&sm->accf, 1);
@@ -250,9 +253,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             }
             if (!ok) break;
             MOE_PROF(PROF_ADD(poff + 5, t0); t0 = clock64());
-            // the chunks were written by cp.async (generic proxy) and are read
-            // by the MMA (async proxy)
-            fence_proxy_async();
+            // W13 chunks were written by cp.async (generic proxy); the MMA reads
+            // through the async proxy
+            if (kW13) fence_proxy_async();
             tc_fence_after();
             const int n = min(run * kBChunkRows, un.npad - ch * kBChunkRows);
             const uint32_t idesc = idesc_f16_f32(128, n);
@@ -282,13 +285,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
     }
   } else if (warp >= 4) {
-    // ---- B producer: gather the unit's rows with cp.async -------------------------
-    // Chunk kc (64 rows of one K step) belongs to warp 4 + kc % 4.  Each lane
-    // announces its copies of the chunk on the slot's barrier as they land
-    // (cp.async.mbarrier.arrive), so a warp never waits for its own data and
-    // the whole ring can be in flight.
+    // ---- B producer: the unit's token rows, 64-row chunks, 128-byte swizzle -------
+    // W13: warps 4-7 gather x rows with 16-byte cp.async; chunk kc belongs to
+    // warp 4 + kc % 4, whose lanes announce it on the slot barrier as their
+    // copies land (the whole ring loads ahead of the MMAs).  W2: one thread
+    // loads 64 consecutive h rows per chunk with a tensor-map load.
     const int bw = warp - 4;
     uint32_t kc = 0, it = 0;
+    const bool tma_thread = (warp == 4 && lane == 0);
     for (int u = blockIdx.x; u < n_units && !*abort; u += gridDim.x, ++it) {
       const Unit un = load_unit<kW13>(d, pv, w, ws, u, upt);
       int* src = sm->bsrc[it & 1];
@@ -298,41 +302,61 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       named_bar_sync(2, 128);
       const int nch = (un.npad + kBChunkRows - 1) / kBChunkRows;
       bool ok = true;
-      for (int ks = 0; ks < S && ok; ++ks) {
-        for (int ch = 0; ch < nch; ++ch, ++kc) {
-          if ((int)(kc & 3) != bw) continue;
-          const int bs = kc % kBSlots;
-          MOE_PROF(long long t0 = clock64());
-          if (!wait_or_abort(&sm->b_empty[bs], ((kc / kBSlots) & 1) ^ 1, status, abort)) {
-            ok = false;
-            break;
-          }
-          MOE_PROF(if (lane == 0) PROF_ADD(poff + 8, t0); t0 = clock64());
-          const uint32_t bt = smem_u32(base + kOffB + bs * kBChunk);
-          const int r0 = ch * kBChunkRows;
-          const int rows = min(kBChunkRows, un.npad - r0);
+      if (kW13) {
+        for (int ks = 0; ks < S && ok; ++ks) {
+          for (int ch = 0; ch < nch; ++ch, ++kc) {
+            if ((int)(kc & 3) != bw) continue;
+            const int bs = kc % kBSlots;
+            MOE_PROF(long long t0 = clock64());
+            if (!wait_or_abort(&sm->b_empty[bs], ((kc / kBSlots) & 1) ^ 1, status, abort)) {
+              ok = false;
+              break;
+            }
+            MOE_PROF(if (lane == 0) PROF_ADD(poff + 8, t0); t0 = clock64());
+            const uint32_t bt = smem_u32(base + kOffB + bs * kBChunk);
+            const int r0 = ch * kBChunkRows;
+            const int rows = min(kBChunkRows, un.npad - r0);
 #pragma unroll 4
-          for (int i = lane; i < rows * 8; i += 32) {
-            const int n = i >> 3, c = i & 7;
-            const int row = r0 + n;
-            const bool in = row < un.rows;
-            const __half* p;
-            if (kW13)
-              p = bsrc + (int64_t)(in ? src[row] : 0) * d.H + ks * kBK + c * 8;
-            else
-              p = bsrc + (int64_t)(in ? un.pos0 + row : 0) * d.I + ks * kBK + c * 8;
-            cp_async16(bt + sw128_off(n, c), p, in ? 16u : 0u);
+            for (int i = lane; i < rows * 8; i += 32) {
+              const int n = i >> 3, c = i & 7;
+              const int row = r0 + n;
+              const bool in = row < un.rows;
+              const __half* p = xsrc + (int64_t)(in ? src[row] : 0) * d.H + ks * kBK + c * 8;
+              cp_async16(bt + sw128_off(n, c), p, in ? 16u : 0u);
+            }
+            cp_async_arrive_noinc(&sm->b_full[bs]);
+            MOE_PROF(if (lane == 0) PROF_ADD(poff + 9, t0));
           }
-          cp_async_arrive_noinc(&sm->b_full[bs]);
-          MOE_PROF(if (lane == 0) PROF_ADD(poff + 9, t0));
+        }
+      } else if (tma_thread) {
+        for (int ks = 0; ks < S && ok; ++ks) {
+          for (int ch = 0; ch < nch; ++ch, ++kc) {
+            const int bs = kc % kBSlots;
+            MOE_PROF(long long t0 = clock64());
+            if (!wait_or_abort(&sm->b_empty[bs], ((kc / kBSlots) & 1) ^ 1, status, abort)) {
+              ok = false;
+              break;
+            }
+            MOE_PROF(PROF_ADD(poff + 8, t0); t0 = clock64());
+            mbar_expect_tx(&sm->b_full[bs], (uint32_t)kBChunk);
+            tma_load_2d(base + kOffB + bs * kBChunk, &hmap, ks * kBK, un.pos0 + ch * kBChunkRows,
+                        &sm->b_full[bs]);
+            MOE_PROF(PROF_ADD(poff + 9, t0));
+          }
         }
       }
+      __syncwarp();
       // the row list of this parity is rewritten two units later
       named_bar_sync(2, 128);
-      if (!ok) break;
+      if (!ok || *abort) break;
     }
-    // every copy this thread issued lands before the block exits
-    cp_async_wait<0>();
+    if (kW13) {
+      cp_async_wait<0>();  // every copy this thread issued lands before the block exits
+    } else if (tma_thread) {
+      // tensor-map loads still in flight land before the block exits (bounded waits)
+      for (uint32_t k = (kc > (uint32_t)kBSlots ? kc - kBSlots : 0); k < kc; ++k)
+        mbar_wait(&sm->b_full[k % kBSlots], (k / kBSlots) & 1, status);
+    }
   } else {
     // ---- warps 0-3: dequantise, then the unit's epilogue ---------------------------
     const int g = lane >> 2, c = lane & 3;
@@ -508,14 +532,19 @@ cudaError_t launch_prefill_forward(const LayerDims& d, int64_t M, const __half* 
   const int g13 = (int)std::min<int64_t>((int64_t)max_tiles * ((2 * d.I) / 256), num_sms);
   const int g2 = (int)std::min<int64_t>((int64_t)max_tiles * (d.H / 256), num_sms);
   const bool pdl = !trace_on();
+  // W2's token-row operand: 64 consecutive h rows per tensor-map load,
+  // 128-byte swizzled (the W13 kernel gathers x rows itself)
+  CUtensorMap hmap;
+  cudaError_t e = make_fp16_map(&hmap, h, d.I, (uint64_t)P, kBK, kBChunkRows, true);
+  if (e != cudaSuccess) return e;
   trace_mark(stream, kTraceW13, false);
-  cudaError_t e = launch_k(grouped_gemm_kernel<true>, dim3(g13), dim3(kGemmThreads), smem,
-                           stream, pdl, d, pv, x, w13, s13, h, partial, status);
+  e = launch_k(grouped_gemm_kernel<true>, dim3(g13), dim3(kGemmThreads), smem, stream, pdl, d, pv,
+               x, hmap, w13, s13, h, partial, status);
   if (e != cudaSuccess) return e;
   trace_mark(stream, kTraceW13, true);
   trace_mark(stream, kTraceW2, false);
   e = launch_k(grouped_gemm_kernel<false>, dim3(g2), dim3(kGemmThreads), smem, stream, pdl, d,
-               pv, (const __half*)h, w2, s2, h, partial, status);
+               pv, (const __half*)nullptr, hmap, w2, s2, h, partial, status);
   if (e != cudaSuccess) return e;
   trace_mark(stream, kTraceW2, true);
   trace_mark(stream, kTraceCombine, false);

@@ -55,4 +55,26 @@ cudaError_t make_rows_map(CUtensorMap* map, const void* base, uint64_t row_bytes
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// FP16 matrix of `rows` x `cols` (row pitch cols * 2 bytes, a multiple of 16),
+// box `box_cols` x `box_rows`, optionally with the 128-byte swizzle (then
+// box_cols * 2 must be 128).  Rows and columns past the end read as zeros.
+cudaError_t make_fp16_map(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows,
+                          uint32_t box_cols, uint32_t box_rows, bool swizzle128) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return cudaErrorNotSupported;
+  if ((reinterpret_cast<uintptr_t>(base) & 15u) || ((cols * 2) & 15u) || box_cols > 256 ||
+      box_rows > 256 || box_rows == 0 || ((box_cols * 2) & 15u) ||
+      (swizzle128 && box_cols * 2 != 128))
+    return cudaErrorInvalidValue;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * 2};
+  const cuuint32_t box[2] = {box_cols, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 }  // namespace moe
