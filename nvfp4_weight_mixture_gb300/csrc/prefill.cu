@@ -12,17 +12,19 @@
 // columns fill the 512 tensor-memory columns) and the tokens are N.  Blocks
 // are persistent (one per SM) and walk the units with a static stride.
 // Warp roles, each running ahead as far as its ring allows:
-//   warp 9     one lane streams the unit's raw NVFP4 blocks (fragment layout:
-//              16 blocks of 512 + 64 bytes per K step of 64) into a 6-deep
+//   warp 13    one lane streams the unit's raw NVFP4 blocks (fragment layout:
+//              16 blocks of 512 + 64 bytes per K step of 64) into a 4-deep
 //              shared ring with two bulk asynchronous copies per K step;
-//   warps 0-3  dequantise each raw stage into 128-byte-swizzled K-major FP16
-//              A tiles (2-deep ring), then run the unit's epilogue;
-//   warps 4-7  fill the token-row operand in chunks of 64 rows (a 12-slot
+//   warps 0-7  dequantise each raw stage into 128-byte-swizzled K-major FP16
+//              A tiles (2-deep ring; two fragment blocks per warp), then run
+//              the unit's epilogue, warp w on TMEM lanes 32 (w % 4) .. +31 of
+//              accumulator w / 4;
+//   warps 8-11 fill the token-row operand in chunks of 64 rows (a 12-slot
 //              ring, same swizzled layout): W13 gathers x rows with 16-byte
-//              cp.async, chunk c by warp 4 + c % 4, whose lanes announce it on
+//              cp.async, chunk c by warp 8 + c % 4, whose lanes announce it on
 //              the slot barrier as their copies land; W2 loads 64 consecutive
 //              h rows per chunk with one tensor-map load;
-//   warp 8     allocates tensor memory; one lane issues the MMAs: per K step and
+//   warp 12    allocates tensor memory; one lane issues the MMAs: per K step and
 //              A tile one MMA with N = all of the tile's rows, split in two only
 //              where the step's chunks wrap around the end of the B ring.
 //
@@ -47,10 +49,17 @@ constexpr int kAS = 2;                    // A (dequantised) stages
 constexpr int kBChunkRows = 64;           // B ring slot: 64 token rows x 128 bytes
 constexpr int kBChunk = kBChunkRows * 128;
 constexpr int kBSlots = 12;               // B ring slots (96 KiB)
-constexpr int kRS = 5;                    // raw weight stages
+constexpr int kRS = 4;                    // raw weight stages
 constexpr int kRawQ = 16 * 512;           // raw q bytes per K step (16 fragment blocks)
 constexpr int kRawBytes = kRawQ + 16 * 64;
-constexpr int kGemmThreads = 320;
+// Warp roles: 0-7 dequantise and run the epilogue, 8-11 fill the token-row
+// operand, 12 issues the MMAs (and owns tensor memory), 13 streams raw weights.
+constexpr int kDqWarps = 8;
+constexpr int kDqThreads = kDqWarps * 32;
+constexpr int kBWarp0 = 8;
+constexpr int kMmaWarp = 12;
+constexpr int kRawWarp = 13;
+constexpr int kGemmThreads = 14 * 32;
 constexpr int kTmemCols = 512;
 constexpr int kOffA = 0;
 constexpr int kOffB = kOffA + kAS * 2 * kATile;
@@ -70,12 +79,13 @@ struct GemmSmem {
   float ewsc[2][kTileRows];  // epilogue (W2): g2 * combine weight of each row
   // epilogue staging, 2 KiB per warp: W13 h values [32 tokens][16 i] (FP16),
   // W2 partial values [16 pairs][32 rows] (FP32)
-  __align__(16) float stage[4][512];
+  __align__(16) float stage[kDqWarps][512];
 };
 
 constexpr size_t gemm_smem_bytes() {
   return 1024 /* alignment slack */ + (size_t)kOffMeta + sizeof(GemmSmem);
 }
+static_assert(gemm_smem_bytes() <= 232448, "grouped GEMM shared memory above the sm_103 limit");
 
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, uint32_t* status,
                                               volatile int* abort) {
@@ -153,10 +163,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   if (tid == 0) {
     for (int i = 0; i < kRS; ++i) {
       mbar_init(&sm->raw_full[i], 1);
-      mbar_init(&sm->raw_empty[i], 128);
+      mbar_init(&sm->raw_empty[i], kDqThreads);
     }
     for (int i = 0; i < kAS; ++i) {
-      mbar_init(&sm->a_full[i], 128);
+      mbar_init(&sm->a_full[i], kDqThreads);
       mbar_init(&sm->a_empty[i], 1);
     }
     for (int i = 0; i < kBSlots; ++i) {
@@ -166,12 +176,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       mbar_init(&sm->b_empty[i], 1);
     }
     mbar_init(&sm->accf, 1);
-    mbar_init(&sm->tmem_empty, 128);
+    mbar_init(&sm->tmem_empty, kDqThreads);
     mbar_init(&sm->drain, 1);
     sm->abort = 0;
     fence_mbar_init();
   }
-  if (warp == 8) tmem_alloc(&sm->tmem, kTmemCols);
+  if (warp == kMmaWarp) tmem_alloc(&sm->tmem, kTmemCols);
   // everything above is independent of the previous grid's results
   pdl_wait();
   MOE_TL_WAITED();
@@ -183,7 +193,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const int n_units = sm->n_units;
   volatile int* abort = &sm->abort;
 
-  if (warp == 9) {
+  if (warp == kRawWarp) {
     // ---- raw weight producer (one lane) ---------------------------------------
     if (lane == 0) {
       uint32_t kr = 0;
@@ -215,7 +225,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       for (uint32_t k = (kr > (uint32_t)kRS ? kr - kRS : 0); k < kr; ++k)
         wait_or_abort(&sm->raw_full[k % kRS], (k / kRS) & 1, status, abort);
     }
-  } else if (warp == 8) {
+  } else if (warp == kMmaWarp) {
     // ---- MMA issuer (one lane) --------------------------------------------------
     if (lane == 0) {
       uint32_t ka = 0, kc = 0, it = 0;
@@ -284,20 +294,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       while (!mbar_try_wait(&sm->drain, 0) && globaltimer() - t0 < kWaitTimeoutNs) {
       }
     }
-  } else if (warp >= 4) {
+  } else if (warp >= kBWarp0) {
     // ---- B producer: the unit's token rows, 64-row chunks, 128-byte swizzle -------
-    // W13: warps 4-7 gather x rows with 16-byte cp.async; chunk kc belongs to
-    // warp 4 + kc % 4, whose lanes announce it on the slot barrier as their
+    // W13: warps 8-11 gather x rows with 16-byte cp.async; chunk kc belongs to
+    // warp 8 + kc % 4, whose lanes announce it on the slot barrier as their
     // copies land (the whole ring loads ahead of the MMAs).  W2: one thread
     // loads 64 consecutive h rows per chunk with a tensor-map load.
-    const int bw = warp - 4;
+    const int bw = warp - kBWarp0;
     uint32_t kc = 0, it = 0;
-    const bool tma_thread = (warp == 4 && lane == 0);
+    const bool tma_thread = (warp == kBWarp0 && lane == 0);
     for (int u = blockIdx.x; u < n_units && !*abort; u += gridDim.x, ++it) {
       const Unit un = load_unit<kW13>(d, pv, w, ws, u, upt);
       int* src = sm->bsrc[it & 1];
       if (kW13)
-        for (int n = tid - 128; n < un.rows; n += 128)
+        for (int n = tid - kBWarp0 * 32; n < un.rows; n += 128)
           src[n] = __ldcg(pv.perm + un.pos0 + n) / d.k_eff;
       named_bar_sync(2, 128);
       const int nch = (un.npad + kBChunkRows - 1) / kBChunkRows;
@@ -358,13 +368,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         mbar_wait(&sm->b_full[k % kBSlots], (k / kBSlots) & 1, status);
     }
   } else {
-    // ---- warps 0-3: dequantise, then the unit's epilogue ---------------------------
+    // ---- warps 0-7: dequantise, then the unit's epilogue ---------------------------
     const int g = lane >> 2, c = lane & 3;
     uint32_t kd = 0, it = 0;
     for (int u = blockIdx.x; u < n_units && !*abort; u += gridDim.x, ++it) {
       const Unit un = load_unit<kW13>(d, pv, w, ws, u, upt);
       if (!kW13) {
-        for (int n = tid; n < un.rows; n += 128) {
+        for (int n = tid; n < un.rows; n += kDqThreads) {
           const int pair = __ldcg(pv.perm + un.pos0 + n);
           sm->epair[it & 1][n] = pair;
           sm->ewsc[it & 1][n] = un.g * __ldcg(pv.w + pair);
@@ -387,8 +397,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const char* raw = base + kOffRaw + rs * kRawBytes;
         char* stage = base + kOffA + as * 2 * kATile;
 #pragma unroll
-        for (int jj = 0; jj < 4; ++jj) {
-          const int j = warp * 4 + jj;  // fragment block: A tile j / 8, local row tile j % 8
+        for (int jj = 0; jj < 16 / kDqWarps; ++jj) {
+          // fragment block j: A tile j / 8, local row tile j % 8
+          const int j = warp * (16 / kDqWarps) + jj;
           const uint4 q = *reinterpret_cast<const uint4*>(raw + j * 512 + lane * 16);
           const uint32_t sc =
               *reinterpret_cast<const unsigned short*>(raw + kRawQ + j * 64 + lane * 2);
@@ -415,8 +426,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         MOE_PROF(if (tid == 0) PROF_ADD(poff + 12, t0));
       }
       if (!ok) break;
-      // ---- epilogue of this unit (TMEM lanes 32*warp .. +31) ----
-      named_bar_sync(1, 128);  // epair / ewsc of this unit visible to all four warps
+      // ---- epilogue of this unit: warp w reads TMEM lanes 32 (w % 4) .. +31 of
+      // accumulator w / 4 ----
+      named_bar_sync(1, kDqThreads);  // epair / ewsc of this unit visible to every warp
+      const int q4 = warp & 3, at = warp >> 2;
       MOE_PROF(long long te = clock64());
       if (!wait_or_abort(&sm->accf, it & 1, status, abort)) break;
       MOE_PROF(if (tid == 0) PROF_ADD(poff + 13, te); te = clock64());
@@ -431,13 +444,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const int r16 = lane & 15;
         const bool is_gate = lane < 16;
         __half(*stg)[16] = reinterpret_cast<__half(*)[16]>(sm->stage[warp]);
-#pragma unroll 1
-        for (int at = 0; at < 2; ++at) {
-          const int i0 = un.sub * 128 + at * 64 + warp * 16;
+        {
+          const int i0 = un.sub * 128 + at * 64 + q4 * 16;
 #pragma unroll 1
           for (int c0 = 0; c0 < un.npad; c0 += 32) {
             uint32_t v[32];
-            tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + at * 256 + c0, v);
+            tmem_ld32(tmem + ((uint32_t)(q4 * 32) << 16) + at * 256 + c0, v);
 #pragma unroll
             for (int jj = 0; jj < 16; ++jj) {
               const float lo = __uint_as_float(v[jj]), hi = __uint_as_float(v[jj + 16]);
@@ -466,13 +478,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const int* pr = sm->epair[it & 1];
         const float* wsc = sm->ewsc[it & 1];
         float(*stg)[32] = reinterpret_cast<float(*)[32]>(sm->stage[warp]);
-#pragma unroll 1
-        for (int at = 0; at < 2; ++at) {
-          const int hd0 = un.sub * 256 + at * 128 + warp * 32;
+        {
+          const int hd0 = un.sub * 256 + at * 128 + q4 * 32;
 #pragma unroll 1
           for (int c0 = 0; c0 < un.npad; c0 += 32) {
             uint32_t v[32];
-            tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + at * 256 + c0, v);
+            tmem_ld32(tmem + ((uint32_t)(q4 * 32) << 16) + at * 256 + c0, v);
 #pragma unroll
             for (int hf = 0; hf < 2; ++hf) {
 #pragma unroll
@@ -506,7 +517,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 8) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
