@@ -15,6 +15,9 @@ constexpr int kDecodeMaxTokens = 16;     // M <= this runs the streaming GEMV pa
 constexpr int kTileRows = 256;           // plan tile height (N of the grouped MMAs)
 constexpr int kPlanChunk = 4096;         // pairs per histogram block in the plan
 constexpr uint64_t kWaitTimeoutNs = 200ull * 1000 * 1000;  // bounded spins: 200 ms
+// The same bound in SM clock cycles, for spins that time themselves with the
+// SM-local cycle counter (cheap to read): 200 ms at 2 GHz, longer if slower.
+constexpr long long kWaitTimeoutCycles = 400ll * 1000 * 1000;
 // Decode work table entry (one per active expert, M <= 16): expert, first plan
 // position, rows, then the pair id of each of the first 16 rows; entries past
 // the active experts hold expert -1.
@@ -186,11 +189,11 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // kWaitTimeoutNs, sets MOE_ST_TIMEOUT and returns false.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* status) {
   if (mbar_try_wait(bar, parity)) return true;
-  uint64_t t0 = globaltimer();
+  const long long t0 = clock64();
   while (true) {
     for (int i = 0; i < 64; ++i)
       if (mbar_try_wait(bar, parity)) return true;
-    if (globaltimer() - t0 > kWaitTimeoutNs) {
+    if (clock64() - t0 > kWaitTimeoutCycles) {
       set_status(status, MOE_ST_TIMEOUT);
       return false;
     }

@@ -90,12 +90,12 @@ static_assert(gemm_smem_bytes() <= 232448, "grouped GEMM shared memory above the
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, uint32_t* status,
                                               volatile int* abort) {
   if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer();
+  const long long t0 = clock64();
   while (true) {
     for (int i = 0; i < 32; ++i)
       if (mbar_try_wait(bar, parity)) return true;
     if (*abort) return false;
-    if (globaltimer() - t0 > kWaitTimeoutNs) {
+    if (clock64() - t0 > kWaitTimeoutCycles) {
       set_status(status, MOE_ST_TIMEOUT);
       *abort = 1;
       return false;
@@ -107,7 +107,8 @@ __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
-// Profiling cells (timeline build): [0..3] raw producer wait/issue, [4..7]
+// Profiling cells (timeline build): [0..1] raw producer wait/issue, [2..3]
+// MMA thread total / unit bookkeeping, [4..7]
 // MMA wait-A / wait-B / issue / wait-TMEM, [8..9] B wait/issue, [10..14]
 // dequant wait-raw / wait-A / work, epilogue wait / work; [16 + 2k] = calls.
 #ifdef MOE_TIMELINE
@@ -229,10 +230,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // ---- MMA issuer (one lane) --------------------------------------------------
     if (lane == 0) {
       uint32_t ka = 0, kc = 0, it = 0;
+      MOE_PROF(const long long t_all = clock64());
       for (int u = blockIdx.x; u < n_units && !*abort; u += gridDim.x, ++it) {
+        MOE_PROF(long long t0 = clock64());
         const Unit un = load_unit<kW13>(d, pv, w, ws, u, upt);
         const int nch = (un.npad + kBChunkRows - 1) / kBChunkRows;
-        MOE_PROF(long long t0 = clock64());
+        MOE_PROF(PROF_ADD(poff + 3, t0); t0 = clock64());
         if (it > 0 && !wait_or_abort(&sm->tmem_empty, (it - 1) & 1, status, abort)) break;
         MOE_PROF(PROF_ADD(poff + 7, t0));
         tc_fence_after();
@@ -288,10 +291,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         if (!ok) break;
         tc_commit(&sm->accf);
       }
+      MOE_PROF(PROF_ADD(poff + 2, t_all));
       // every MMA issued has completed before tensor memory is released
       tc_commit(&sm->drain);
-      const uint64_t t0 = globaltimer();
-      while (!mbar_try_wait(&sm->drain, 0) && globaltimer() - t0 < kWaitTimeoutNs) {
+      const long long t0 = clock64();
+      while (!mbar_try_wait(&sm->drain, 0) && clock64() - t0 < kWaitTimeoutCycles) {
       }
     }
   } else if (warp >= kBWarp0) {
