@@ -97,7 +97,9 @@ def kernel_accounting(wl, step, n_active, n_pairs, decode):
         b = n_active * w13_expert_bytes(wl) + M * H * 2 + n_pairs * I * 2
         f = n_pairs * 2 * H * 2 * I
     elif step == "w2":
-        b = n_active * w2_expert_bytes(wl) + n_pairs * I * 2 + n_pairs * H * 4
+        # decode: the combine runs inside the W2 kernel (writes y); prefill: FP32 partials
+        out = M * H * 2 if decode else n_pairs * H * 4
+        b = n_active * w2_expert_bytes(wl) + n_pairs * I * 2 + out
         f = n_pairs * 2 * I * H
     elif step == "combine":
         b = n_pairs * H * 4 + M * H * 2
@@ -375,7 +377,8 @@ def run_gpu(args, wl):
             flush.zero_()
             graphs[i % n_var].replay()
     stream.synchronize()
-    launches_per_step = 4 if decode else 7
+    # router + plan (1 kernel for M <= 16, 4 above), W13, W2 (+ combine above M = 16)
+    launches_per_step = 3 if decode else 7
 
     # ---- timed region: graph replays, L2 flushed before each step ------------------
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
