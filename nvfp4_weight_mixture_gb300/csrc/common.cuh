@@ -140,11 +140,23 @@ struct TlScope {
 #define MOE_TL_WAITED() tl_scope_.waited()
 // per-role cycle accounting of the grouped GEMM (summed over blocks)
 extern __device__ unsigned long long g_prof[32];
+// per-event clock64 stamps of block 0 of the grouped GEMM (timeline build):
+// [0, 2048) B chunk issued, [2048, 4096) B chunk seen ready by the MMA thread,
+// [4096, 6144) A stage seen ready, [6144, 8192) raw stage issued,
+// [8192, 10240) raw stage seen ready by the dequantisers
+extern __device__ unsigned long long g_dbg[10240];
+#define MOE_DBG(slot, idx)                                                   \
+  do {                                                                        \
+    if (blockIdx.x == 0 && (idx) < 2048) g_dbg[(slot) * 2048 + (idx)] = clock64(); \
+  } while (0)
 #define MOE_PROF(stmt) stmt
 // raw stamps on timeline cells 20..63 (earliest / latest over the threads that pass)
 #define MOE_TL_MIN(cell) atomicMin(&::moe::g_timeline[cell], (unsigned long long)::moe::globaltimer())
 #define MOE_TL_MAX(cell) atomicMax(&::moe::g_timeline[cell], (unsigned long long)::moe::globaltimer())
 #else
+#define MOE_DBG(slot, idx) \
+  do {                     \
+  } while (0)
 #define MOE_PROF(stmt)
 #define MOE_TL_MIN(cell) \
   do {                   \

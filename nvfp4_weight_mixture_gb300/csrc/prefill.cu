@@ -19,14 +19,16 @@
 //              A tiles (2-deep ring; two fragment blocks per warp), then run
 //              the unit's epilogue, warp w on TMEM lanes 32 (w % 4) .. +31 of
 //              accumulator w / 4;
-//   warps 8-11 fill the token-row operand in chunks of 64 rows (a 12-slot
-//              ring, same swizzled layout): W13 gathers x rows with 16-byte
-//              cp.async, chunk c by warp 8 + c % 4, whose lanes announce it on
-//              the slot barrier as their copies land; W2 loads 64 consecutive
-//              h rows per chunk with one tensor-map load;
-//   warp 12    allocates tensor memory; one lane issues the MMAs: per K step and
-//              A tile one MMA with N = all of the tile's rows, split in two only
-//              where the step's chunks wrap around the end of the B ring.
+//   warps 8-11 fill the token-row operand, one 3-deep ring stage per K step
+//              (same swizzled layout): W13 gathers x rows with 16-byte cp.async,
+//              64 rows per warp, each lane announcing the stage as its copies
+//              land; W2 loads 64-row chunks of h with tensor-map loads;
+//   warp 12    allocates tensor memory; one lane issues the MMAs: per K step
+//              one wait on each ring, then per A tile and 16-element K slice one
+//              MMA with N = all of the unit's rows, then one commit per ring.
+//              (The issuing thread shares its SM sub-partition with busy
+//              dequantise and gather warps, so its per-step instruction chain
+//              is kept short.)
 //
 // W13: the fragment layout interleaves 16-row gate and up tiles, so TMEM lanes
 // [32q, 32q+16) hold gate rows and [32q+16, 32q+32) the matching up rows; the
@@ -46,9 +48,10 @@ constexpr int kBK = 64;                   // K per step (128 bytes of FP16)
 constexpr int kATile = 128 * 128;         // one 128-row FP16 A tile, bytes
 constexpr int kBTile = kTileRows * 128;   // the B tile, bytes
 constexpr int kAS = 2;                    // A (dequantised) stages
-constexpr int kBChunkRows = 64;           // B ring slot: 64 token rows x 128 bytes
+constexpr int kBChunkRows = 64;           // one gather warp's share: 64 token rows x 128 bytes
 constexpr int kBChunk = kBChunkRows * 128;
-constexpr int kBSlots = 12;               // B ring slots (96 KiB)
+constexpr int kBStage = 4 * kBChunk;      // B ring stage: one K step of up to 256 rows
+constexpr int kBStages = 3;               // B ring stages (96 KiB)
 constexpr int kRS = 4;                    // raw weight stages
 constexpr int kRawQ = 16 * 512;           // raw q bytes per K step (16 fragment blocks)
 constexpr int kRawBytes = kRawQ + 16 * 64;
@@ -63,13 +66,13 @@ constexpr int kGemmThreads = 14 * 32;
 constexpr int kTmemCols = 512;
 constexpr int kOffA = 0;
 constexpr int kOffB = kOffA + kAS * 2 * kATile;
-constexpr int kOffRaw = kOffB + kBSlots * kBChunk;
+constexpr int kOffRaw = kOffB + kBStages * kBStage;
 constexpr int kOffMeta = kOffRaw + kRS * kRawBytes;
 
 struct GemmSmem {
   uint64_t raw_full[kRS], raw_empty[kRS];
   uint64_t a_full[kAS], a_empty[kAS];
-  uint64_t b_full[kBSlots], b_empty[kBSlots];
+  uint64_t b_full[kBStages], b_empty[kBStages];
   uint64_t accf, tmem_empty, drain;
   uint32_t tmem;
   int abort;
@@ -170,10 +173,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       mbar_init(&sm->a_full[i], kDqThreads);
       mbar_init(&sm->a_empty[i], 1);
     }
-    for (int i = 0; i < kBSlots; ++i) {
-      // W13: the 32 lanes of the gather warp that owns the chunk; W2: the
+    for (int i = 0; i < kBStages; ++i) {
+      // W13: every lane of the four gather warps, once per K step; W2: the
       // loading thread (plus the transaction bytes)
-      mbar_init(&sm->b_full[i], kW13 ? 32 : 1);
+      mbar_init(&sm->b_full[i], kW13 ? 128 : 1);
       mbar_init(&sm->b_empty[i], 1);
     }
     mbar_init(&sm->accf, 1);
@@ -229,64 +232,51 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   } else if (warp == kMmaWarp) {
     // ---- MMA issuer (one lane) --------------------------------------------------
     if (lane == 0) {
-      uint32_t ka = 0, kc = 0, it = 0;
+      uint32_t ka = 0, it = 0;
       MOE_PROF(const long long t_all = clock64());
       for (int u = blockIdx.x; u < n_units && !*abort; u += gridDim.x, ++it) {
         MOE_PROF(long long t0 = clock64());
         const Unit un = load_unit<kW13>(d, pv, w, ws, u, upt);
-        const int nch = (un.npad + kBChunkRows - 1) / kBChunkRows;
+        const uint32_t idesc = idesc_f16_f32(128, un.npad);
         MOE_PROF(PROF_ADD(poff + 3, t0); t0 = clock64());
         if (it > 0 && !wait_or_abort(&sm->tmem_empty, (it - 1) & 1, status, abort)) break;
         MOE_PROF(PROF_ADD(poff + 7, t0));
         tc_fence_after();
         bool ok = true;
-        for (int ks = 0; ks < S && ok; ++ks, ++ka) {
-          const int as = ka % kAS;
+        // per K step: one A stage (two 128-row tiles) and one B stage (all of
+        // the unit's token rows); one MMA per tile and 16-element K slice
+        for (int ks = 0; ks < S; ++ks, ++ka) {
+          const int as = ka % kAS, bs = ka % kBStages;
           MOE_PROF(t0 = clock64());
           if (!wait_or_abort(&sm->a_full[as], (ka / kAS) & 1, status, abort)) {
             ok = false;
             break;
           }
-          MOE_PROF(PROF_ADD(poff + 4, t0));
+          if (kW13) MOE_DBG(2, ka);
+          MOE_PROF(PROF_ADD(poff + 4, t0); t0 = clock64());
+          if (!wait_or_abort(&sm->b_full[bs], (ka / kBStages) & 1, status, abort)) {
+            ok = false;
+            break;
+          }
+          if (kW13) MOE_DBG(1, ka);
+          MOE_PROF(PROF_ADD(poff + 5, t0); t0 = clock64());
+          // W13 rows were written by cp.async (generic proxy); the MMA reads
+          // through the async proxy
+          if (kW13) fence_proxy_async();
           tc_fence_after();
           const uint64_t da0 = sdesc_sw128(smem_u32(base + kOffA + as * 2 * kATile));
           const uint64_t da1 = sdesc_sw128(smem_u32(base + kOffA + as * 2 * kATile + kATile));
-          // the step's chunks in runs of contiguous ring slots (at most two)
-          int ch = 0;
-          while (ch < nch && ok) {
-            const int slot0 = kc % kBSlots;
-            const int run = min(nch - ch, kBSlots - slot0);
-            MOE_PROF(t0 = clock64());
-            for (int r = 0; r < run; ++r) {
-              const uint32_t kcr = kc + r;
-              if (!wait_or_abort(&sm->b_full[kcr % kBSlots], (kcr / kBSlots) & 1, status, abort)) {
-                ok = false;
-                break;
-              }
-            }
-            if (!ok) break;
-            MOE_PROF(PROF_ADD(poff + 5, t0); t0 = clock64());
-            // W13 chunks were written by cp.async (generic proxy); the MMA reads
-            // through the async proxy
-            if (kW13) fence_proxy_async();
-            tc_fence_after();
-            const int n = min(run * kBChunkRows, un.npad - ch * kBChunkRows);
-            const uint32_t idesc = idesc_f16_f32(128, n);
-            const uint64_t db = sdesc_sw128(smem_u32(base + kOffB + slot0 * kBChunk));
-            const uint32_t col = ch * kBChunkRows;
+          const uint64_t db = sdesc_sw128(smem_u32(base + kOffB + bs * kBStage));
 #pragma unroll
-            for (int kk = 0; kk < kBK / 16; ++kk) {
-              const uint32_t acc = (ks | kk) ? 1u : 0u;
-              // +32 bytes along K inside the 128-byte swizzle atom: start address + 2
-              tc_mma_f16(tmem + col, da0 + 2 * kk, db + 2 * kk, idesc, acc);
-              tc_mma_f16(tmem + 256 + col, da1 + 2 * kk, db + 2 * kk, idesc, acc);
-            }
-            for (int r = 0; r < run; ++r) tc_commit(&sm->b_empty[(kc + r) % kBSlots]);
-            MOE_PROF(PROF_ADD(poff + 6, t0));
-            kc += run;
-            ch += run;
+          for (int kk = 0; kk < kBK / 16; ++kk) {
+            const uint32_t acc = (ks | kk) ? 1u : 0u;
+            // +32 bytes along K inside the 128-byte swizzle atom: start address + 2
+            tc_mma_f16(tmem, da0 + 2 * kk, db + 2 * kk, idesc, acc);
+            tc_mma_f16(tmem + 256, da1 + 2 * kk, db + 2 * kk, idesc, acc);
           }
-          if (ok) tc_commit(&sm->a_empty[as]);
+          tc_commit(&sm->b_empty[bs]);
+          tc_commit(&sm->a_empty[as]);
+          MOE_PROF(PROF_ADD(poff + 6, t0));
         }
         if (!ok) break;
         tc_commit(&sm->accf);
@@ -299,13 +289,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
     }
   } else if (warp >= kBWarp0) {
-    // ---- B producer: the unit's token rows, 64-row chunks, 128-byte swizzle -------
-    // W13: warps 8-11 gather x rows with 16-byte cp.async; chunk kc belongs to
-    // warp 8 + kc % 4, whose lanes announce it on the slot barrier as their
-    // copies land (the whole ring loads ahead of the MMAs).  W2: one thread
-    // loads 64 consecutive h rows per chunk with a tensor-map load.
-    const int bw = warp - kBWarp0;
-    uint32_t kc = 0, it = 0;
+    // ---- B producer: the unit's token rows, one ring stage per K step (up to 256
+    // rows, 128-byte swizzle).  W13: warp 8 + j gathers rows [64 j, 64 j + 64)
+    // of each stage from x with 16-byte cp.async, and every lane announces the
+    // stage on its barrier once its copies have landed (the whole ring loads
+    // ahead of the MMAs).  W2: one thread loads 64-row chunks of h (already in
+    // plan order) with tensor-map loads.
+    const int bw = warp - kBWarp0;  // W13: this warp fills rows [64 bw, 64 bw + 64) of each stage
+    uint32_t kb = 0, it = 0;
     const bool tma_thread = (warp == kBWarp0 && lane == 0);
     for (int u = blockIdx.x; u < n_units && !*abort; u += gridDim.x, ++it) {
       const Unit un = load_unit<kW13>(d, pv, w, ws, u, upt);
@@ -314,49 +305,47 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         for (int n = tid - kBWarp0 * 32; n < un.rows; n += 128)
           src[n] = __ldcg(pv.perm + un.pos0 + n) / d.k_eff;
       named_bar_sync(2, 128);
-      const int nch = (un.npad + kBChunkRows - 1) / kBChunkRows;
       bool ok = true;
       if (kW13) {
-        for (int ks = 0; ks < S && ok; ++ks) {
-          for (int ch = 0; ch < nch; ++ch, ++kc) {
-            if ((int)(kc & 3) != bw) continue;
-            const int bs = kc % kBSlots;
-            MOE_PROF(long long t0 = clock64());
-            if (!wait_or_abort(&sm->b_empty[bs], ((kc / kBSlots) & 1) ^ 1, status, abort)) {
-              ok = false;
-              break;
-            }
-            MOE_PROF(if (lane == 0) PROF_ADD(poff + 8, t0); t0 = clock64());
-            const uint32_t bt = smem_u32(base + kOffB + bs * kBChunk);
-            const int r0 = ch * kBChunkRows;
-            const int rows = min(kBChunkRows, un.npad - r0);
-#pragma unroll 4
-            for (int i = lane; i < rows * 8; i += 32) {
-              const int n = i >> 3, c = i & 7;
-              const int row = r0 + n;
-              const bool in = row < un.rows;
-              const __half* p = xsrc + (int64_t)(in ? src[row] : 0) * d.H + ks * kBK + c * 8;
-              cp_async16(bt + sw128_off(n, c), p, in ? 16u : 0u);
-            }
-            cp_async_arrive_noinc(&sm->b_full[bs]);
-            MOE_PROF(if (lane == 0) PROF_ADD(poff + 9, t0));
+        const int r0 = bw * kBChunkRows;
+        const int rows = max(0, min(kBChunkRows, un.npad - r0));
+        for (int ks = 0; ks < S; ++ks, ++kb) {
+          const int bs = kb % kBStages;
+          MOE_PROF(long long t0 = clock64());
+          if (!wait_or_abort(&sm->b_empty[bs], ((kb / kBStages) & 1) ^ 1, status, abort)) {
+            ok = false;
+            break;
           }
+          MOE_PROF(if (lane == 0) PROF_ADD(poff + 8, t0); t0 = clock64());
+          if (kW13 && lane == 0 && bw == 0) MOE_DBG(0, kb);
+          const uint32_t bt = smem_u32(base + kOffB + bs * kBStage + r0 * 128);
+#pragma unroll 4
+          for (int i = lane; i < rows * 8; i += 32) {
+            const int n = i >> 3, c = i & 7;
+            const int row = r0 + n;
+            const bool in = row < un.rows;
+            const __half* p = xsrc + (int64_t)(in ? src[row] : 0) * d.H + ks * kBK + c * 8;
+            cp_async16(bt + sw128_off(n, c), p, in ? 16u : 0u);
+          }
+          // every lane announces the stage once its copies (if any) have landed
+          cp_async_arrive_noinc(&sm->b_full[bs]);
+          MOE_PROF(if (lane == 0) PROF_ADD(poff + 9, t0));
         }
       } else if (tma_thread) {
-        for (int ks = 0; ks < S && ok; ++ks) {
-          for (int ch = 0; ch < nch; ++ch, ++kc) {
-            const int bs = kc % kBSlots;
-            MOE_PROF(long long t0 = clock64());
-            if (!wait_or_abort(&sm->b_empty[bs], ((kc / kBSlots) & 1) ^ 1, status, abort)) {
-              ok = false;
-              break;
-            }
-            MOE_PROF(PROF_ADD(poff + 8, t0); t0 = clock64());
-            mbar_expect_tx(&sm->b_full[bs], (uint32_t)kBChunk);
-            tma_load_2d(base + kOffB + bs * kBChunk, &hmap, ks * kBK, un.pos0 + ch * kBChunkRows,
-                        &sm->b_full[bs]);
-            MOE_PROF(PROF_ADD(poff + 9, t0));
+        const int nch = (un.npad + kBChunkRows - 1) / kBChunkRows;
+        for (int ks = 0; ks < S; ++ks, ++kb) {
+          const int bs = kb % kBStages;
+          MOE_PROF(long long t0 = clock64());
+          if (!wait_or_abort(&sm->b_empty[bs], ((kb / kBStages) & 1) ^ 1, status, abort)) {
+            ok = false;
+            break;
           }
+          MOE_PROF(PROF_ADD(poff + 8, t0); t0 = clock64());
+          mbar_expect_tx(&sm->b_full[bs], (uint32_t)(nch * kBChunk));
+          for (int ch = 0; ch < nch; ++ch)
+            tma_load_2d(base + kOffB + bs * kBStage + ch * kBChunk, &hmap, ks * kBK,
+                        un.pos0 + ch * kBChunkRows, &sm->b_full[bs]);
+          MOE_PROF(PROF_ADD(poff + 9, t0));
         }
       }
       __syncwarp();
@@ -368,8 +357,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       cp_async_wait<0>();  // every copy this thread issued lands before the block exits
     } else if (tma_thread) {
       // tensor-map loads still in flight land before the block exits (bounded waits)
-      for (uint32_t k = (kc > (uint32_t)kBSlots ? kc - kBSlots : 0); k < kc; ++k)
-        mbar_wait(&sm->b_full[k % kBSlots], (k / kBSlots) & 1, status);
+      for (uint32_t k = (kb > (uint32_t)kBStages ? kb - kBStages : 0); k < kb; ++k)
+        mbar_wait(&sm->b_full[k % kBStages], (k / kBStages) & 1, status);
     }
   } else {
     // ---- warps 0-7: dequantise, then the unit's epilogue ---------------------------
@@ -398,6 +387,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           break;
         }
         MOE_PROF(if (tid == 0) PROF_ADD(poff + 11, t0); t0 = clock64());
+        if (kW13 && lane == 0) MOE_DBG(3, kd * kDqWarps + warp);
         const char* raw = base + kOffRaw + rs * kRawBytes;
         char* stage = base + kOffA + as * 2 * kATile;
 #pragma unroll
@@ -425,6 +415,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
               make_uint4(o[0], o[1], o[2], o[3]);
         }
         fence_proxy_async();
+        if (kW13 && lane == 0) MOE_DBG(4, kd * kDqWarps + warp);
         mbar_arrive(&sm->a_full[as]);
         mbar_arrive(&sm->raw_empty[rs]);
         MOE_PROF(if (tid == 0) PROF_ADD(poff + 12, t0));
