@@ -19,10 +19,10 @@
 //              A tiles (2-deep ring; two fragment blocks per warp), then run
 //              the unit's epilogue, warp w on TMEM lanes 32 (w % 4) .. +31 of
 //              accumulator w / 4;
-//   warps 8-11 fill the token-row operand, one 3-deep ring stage per K step
-//              (same swizzled layout): W13 gathers x rows with 16-byte cp.async,
-//              64 rows per warp, each lane announcing the stage as its copies
-//              land; W2 loads 64-row chunks of h with tensor-map loads;
+//   warp 8     one lane fills the token-row operand, one 3-deep ring stage per
+//              K step (same swizzled layout), with 64-row tensor-map loads of
+//              the plan-ordered rows: x gathered beforehand for W13, h for W2
+//              (warps 9-11 are spare);
 //   warp 12    allocates tensor memory; one lane issues the MMAs: per K step
 //              one wait on each ring, then per A tile and 16-element K slice one
 //              MMA with N = all of the unit's rows, then one commit per ring.
@@ -77,7 +77,6 @@ struct GemmSmem {
   uint32_t tmem;
   int abort;
   int n_units;
-  int bsrc[2][kTileRows];    // B warps: token (W13) of each row, by unit parity
   int epair[2][kTileRows];   // epilogue (W2): pair id of each row
   float ewsc[2][kTileRows];  // epilogue (W2): g2 * combine weight of each row
   // epilogue staging, 2 KiB per warp: W13 h values [32 tokens][16 i] (FP16),
@@ -148,10 +147,9 @@ __device__ __forceinline__ Unit load_unit(const LayerDims& d, const PlanView& pv
 
 template <bool kW13>
 __global__ void __launch_bounds__(kGemmThreads, 1)
-    grouped_gemm_kernel(LayerDims d, PlanView pv, const __half* __restrict__ xsrc,
-                        const __grid_constant__ CUtensorMap hmap, Weights w, Weights ws,
-                        __half* __restrict__ h_out, float* __restrict__ partial,
-                        uint32_t* status) {
+    grouped_gemm_kernel(LayerDims d, PlanView pv, const __grid_constant__ CUtensorMap bmap,
+                        Weights w, Weights ws, __half* __restrict__ h_out,
+                        float* __restrict__ partial, uint32_t* status) {
   extern __shared__ __align__(1024) char smem_raw[];
   char* base = reinterpret_cast<char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                        ~uintptr_t(1023));
@@ -174,9 +172,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       mbar_init(&sm->a_empty[i], 1);
     }
     for (int i = 0; i < kBStages; ++i) {
-      // W13: every lane of the four gather warps, once per K step; W2: the
-      // loading thread (plus the transaction bytes)
-      mbar_init(&sm->b_full[i], kW13 ? 128 : 1);
+      mbar_init(&sm->b_full[i], 1);  // the loading thread, plus the transaction bytes
       mbar_init(&sm->b_empty[i], 1);
     }
     mbar_init(&sm->accf, 1);
@@ -260,9 +256,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           }
           if (kW13) MOE_DBG(1, ka);
           MOE_PROF(PROF_ADD(poff + 5, t0); t0 = clock64());
-          // W13 rows were written by cp.async (generic proxy); the MMA reads
-          // through the async proxy
-          if (kW13) fence_proxy_async();
           tc_fence_after();
           const uint64_t da0 = sdesc_sw128(smem_u32(base + kOffA + as * 2 * kATile));
           const uint64_t da1 = sdesc_sw128(smem_u32(base + kOffA + as * 2 * kATile + kATile));
@@ -288,50 +281,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       while (!mbar_try_wait(&sm->drain, 0) && clock64() - t0 < kWaitTimeoutCycles) {
       }
     }
-  } else if (warp >= kBWarp0) {
-    // ---- B producer: the unit's token rows, one ring stage per K step (up to 256
-    // rows, 128-byte swizzle).  W13: warp 8 + j gathers rows [64 j, 64 j + 64)
-    // of each stage from x with 16-byte cp.async, and every lane announces the
-    // stage on its barrier once its copies have landed (the whole ring loads
-    // ahead of the MMAs).  W2: one thread loads 64-row chunks of h (already in
-    // plan order) with tensor-map loads.
-    const int bw = warp - kBWarp0;  // W13: this warp fills rows [64 bw, 64 bw + 64) of each stage
-    uint32_t kb = 0, it = 0;
-    const bool tma_thread = (warp == kBWarp0 && lane == 0);
-    for (int u = blockIdx.x; u < n_units && !*abort; u += gridDim.x, ++it) {
-      const Unit un = load_unit<kW13>(d, pv, w, ws, u, upt);
-      int* src = sm->bsrc[it & 1];
-      if (kW13)
-        for (int n = tid - kBWarp0 * 32; n < un.rows; n += 128)
-          src[n] = __ldcg(pv.perm + un.pos0 + n) / d.k_eff;
-      named_bar_sync(2, 128);
+  } else if (warp == kBWarp0) {
+    // ---- B producer (one thread): the unit's token rows, one ring stage per K
+    // step (up to 256 rows, 128-byte swizzle), loaded as 64-row tiles of the
+    // plan-ordered operand (x rows gathered into plan order for W13, h for W2).
+    if (lane == 0) {
+      uint32_t kb = 0;
       bool ok = true;
-      if (kW13) {
-        const int r0 = bw * kBChunkRows;
-        const int rows = max(0, min(kBChunkRows, un.npad - r0));
-        for (int ks = 0; ks < S; ++ks, ++kb) {
-          const int bs = kb % kBStages;
-          MOE_PROF(long long t0 = clock64());
-          if (!wait_or_abort(&sm->b_empty[bs], ((kb / kBStages) & 1) ^ 1, status, abort)) {
-            ok = false;
-            break;
-          }
-          MOE_PROF(if (lane == 0) PROF_ADD(poff + 8, t0); t0 = clock64());
-          if (kW13 && lane == 0 && bw == 0) MOE_DBG(0, kb);
-          const uint32_t bt = smem_u32(base + kOffB + bs * kBStage + r0 * 128);
-#pragma unroll 4
-          for (int i = lane; i < rows * 8; i += 32) {
-            const int n = i >> 3, c = i & 7;
-            const int row = r0 + n;
-            const bool in = row < un.rows;
-            const __half* p = xsrc + (int64_t)(in ? src[row] : 0) * d.H + ks * kBK + c * 8;
-            cp_async16(bt + sw128_off(n, c), p, in ? 16u : 0u);
-          }
-          // every lane announces the stage once its copies (if any) have landed
-          cp_async_arrive_noinc(&sm->b_full[bs]);
-          MOE_PROF(if (lane == 0) PROF_ADD(poff + 9, t0));
-        }
-      } else if (tma_thread) {
+      for (int u = blockIdx.x; u < n_units && ok && !*abort; u += gridDim.x) {
+        const Unit un = load_unit<kW13>(d, pv, w, ws, u, upt);
         const int nch = (un.npad + kBChunkRows - 1) / kBChunkRows;
         for (int ks = 0; ks < S; ++ks, ++kb) {
           const int bs = kb % kBStages;
@@ -343,23 +301,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           MOE_PROF(PROF_ADD(poff + 8, t0); t0 = clock64());
           mbar_expect_tx(&sm->b_full[bs], (uint32_t)(nch * kBChunk));
           for (int ch = 0; ch < nch; ++ch)
-            tma_load_2d(base + kOffB + bs * kBStage + ch * kBChunk, &hmap, ks * kBK,
+            tma_load_2d(base + kOffB + bs * kBStage + ch * kBChunk, &bmap, ks * kBK,
                         un.pos0 + ch * kBChunkRows, &sm->b_full[bs]);
           MOE_PROF(PROF_ADD(poff + 9, t0));
         }
       }
-      __syncwarp();
-      // the row list of this parity is rewritten two units later
-      named_bar_sync(2, 128);
-      if (!ok || *abort) break;
-    }
-    if (kW13) {
-      cp_async_wait<0>();  // every copy this thread issued lands before the block exits
-    } else if (tma_thread) {
-      // tensor-map loads still in flight land before the block exits (bounded waits)
+      // loads still in flight land before the block exits (bounded waits)
       for (uint32_t k = (kb > (uint32_t)kBStages ? kb - kBStages : 0); k < kb; ++k)
         mbar_wait(&sm->b_full[k % kBStages], (k / kBStages) & 1, status);
     }
+  } else if (warp > kBWarp0) {
+    // spare warps
   } else {
     // ---- warps 0-7: dequantise, then the unit's epilogue ---------------------------
     const int g = lane >> 2, c = lane & 3;
@@ -518,6 +470,23 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   }
 }
 
+// xg[pos] = x[perm[pos] / k_eff]: the token rows in plan order, the operand of
+// the grouped W13 GEMM (positions past the valid pairs are left alone).
+// One warp per row, 16-byte loads and stores.
+__global__ void gather_rows_kernel(LayerDims d, PlanView pv, const __half* __restrict__ x,
+                                   __half* __restrict__ xg) {
+  MOE_TL(kTlPlan);
+  pdl_wait();
+  pdl_launch_dependents();
+  const int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= __ldcg(&pv.hdr->n_valid)) return;
+  const int t = __ldcg(pv.perm + row) / d.k_eff;
+  const uint4* src = reinterpret_cast<const uint4*>(x + (int64_t)t * d.H);
+  uint4* dst = reinterpret_cast<uint4*>(xg + row * d.H);
+  for (int c = lane; c < d.H / 8; c += 32) dst[c] = __ldg(src + c);
+}
+
 cudaError_t launch_prefill_forward(const LayerDims& d, int64_t M, const __half* x,
                                    const PlanView& pv, Weights w13, Weights w2, Weights s13,
                                    Weights s2, __half* y, __half* h, float* partial,
@@ -538,19 +507,26 @@ cudaError_t launch_prefill_forward(const LayerDims& d, int64_t M, const __half* 
   const int g13 = (int)std::min<int64_t>((int64_t)max_tiles * ((2 * d.I) / 256), num_sms);
   const int g2 = (int)std::min<int64_t>((int64_t)max_tiles * (d.H / 256), num_sms);
   const bool pdl = !trace_on();
-  // W2's token-row operand: 64 consecutive h rows per tensor-map load,
-  // 128-byte swizzled (the W13 kernel gathers x rows itself)
-  CUtensorMap hmap;
-  cudaError_t e = make_fp16_map(&hmap, h, d.I, (uint64_t)P, kBK, kBChunkRows, true);
+  // Token-row operands in plan order, read as 64-row tensor-map tiles (128-byte
+  // swizzled): W13 reads x rows gathered into the partials buffer (unused until
+  // the W2 grid, which starts after W13 has finished), W2 reads h.
+  __half* xg = reinterpret_cast<__half*>(partial);
+  CUtensorMap xmap, hmap;
+  cudaError_t e = make_fp16_map(&xmap, xg, d.H, (uint64_t)P, kBK, kBChunkRows, true);
+  if (e != cudaSuccess) return e;
+  e = make_fp16_map(&hmap, h, d.I, (uint64_t)P, kBK, kBChunkRows, true);
   if (e != cudaSuccess) return e;
   trace_mark(stream, kTraceW13, false);
+  e = launch_k(gather_rows_kernel, dim3((unsigned)((P + 7) / 8)), dim3(256), 0, stream, pdl, d, pv,
+               x, xg);
+  if (e != cudaSuccess) return e;
   e = launch_k(grouped_gemm_kernel<true>, dim3(g13), dim3(kGemmThreads), smem, stream, pdl, d, pv,
-               x, hmap, w13, s13, h, partial, status);
+               xmap, w13, s13, h, partial, status);
   if (e != cudaSuccess) return e;
   trace_mark(stream, kTraceW13, true);
   trace_mark(stream, kTraceW2, false);
   e = launch_k(grouped_gemm_kernel<false>, dim3(g2), dim3(kGemmThreads), smem, stream, pdl, d,
-               pv, (const __half*)nullptr, hmap, w2, s2, h, partial, status);
+               pv, hmap, w2, s2, h, partial, status);
   if (e != cudaSuccess) return e;
   trace_mark(stream, kTraceW2, true);
   trace_mark(stream, kTraceCombine, false);
