@@ -110,7 +110,7 @@ namespace moe {
 #ifdef MOE_TIMELINE
 __device__ unsigned long long g_timeline[64];
 __device__ unsigned long long g_prof[32];
-__device__ unsigned long long g_dbg[10240];
+__device__ unsigned long long g_dbg[20480];
 #endif
 bool trace_on() { return g_trace_events != nullptr; }
 void trace_mark(cudaStream_t stream, int step, bool end) {
@@ -142,7 +142,7 @@ int32_t moe_nvfp4_timeline_read(unsigned long long* out) {
   return cuda_status(cudaMemcpyFromSymbol(out, moe::g_timeline, sizeof(unsigned long long) * 64));
 }
 int32_t moe_nvfp4_dbg_read(unsigned long long* out) {
-  return cuda_status(cudaMemcpyFromSymbol(out, moe::g_dbg, sizeof(unsigned long long) * 10240));
+  return cuda_status(cudaMemcpyFromSymbol(out, moe::g_dbg, sizeof(unsigned long long) * 20480));
 }
 int32_t moe_nvfp4_prof_read(unsigned long long* out, int reset) {
   cudaError_t e = cudaMemcpyFromSymbol(out, moe::g_prof, sizeof(unsigned long long) * 32);

@@ -12,7 +12,7 @@
 namespace moe {
 
 constexpr int kDecodeMaxTokens = 16;     // M <= this runs the streaming GEMV path
-constexpr int kTileRows = 256;           // plan tile height (N of the grouped MMAs)
+constexpr int kTileRows = 192;           // plan tile height (N of the grouped MMAs)
 constexpr int kPlanChunk = 4096;         // pairs per histogram block in the plan
 constexpr uint64_t kWaitTimeoutNs = 200ull * 1000 * 1000;  // bounded spins: 200 ms
 // The same bound in SM clock cycles, for spins that time themselves with the
@@ -140,11 +140,13 @@ struct TlScope {
 #define MOE_TL_WAITED() tl_scope_.waited()
 // per-role cycle accounting of the grouped GEMM (summed over blocks)
 extern __device__ unsigned long long g_prof[32];
-// per-event clock64 stamps of block 0 of the grouped GEMM (timeline build):
-// [0, 2048) B chunk issued, [2048, 4096) B chunk seen ready by the MMA thread,
-// [4096, 6144) A stage seen ready, [6144, 8192) raw stage issued,
-// [8192, 10240) raw stage seen ready by the dequantisers
-extern __device__ unsigned long long g_dbg[10240];
+// per-event clock64 stamps of block 0 of the grouped GEMM (timeline build),
+// 2048 per kind: [0] MMA K step issued, [1] B stage seen ready by the MMA
+// thread, [2] A stage seen ready, [3] / [4] dequantise start / end (K step x 8
+// + warp), [5] B stage loads issued, [6] raw stage issued, [7] epilogue
+// accumulator seen ready / epilogue done (2 x unit, 2 x unit + 1), [8] raw
+// stage landed, [9] B stage landed
+extern __device__ unsigned long long g_dbg[20480];
 #define MOE_DBG(slot, idx)                                                   \
   do {                                                                        \
     if (blockIdx.x == 0 && (idx) < 2048) g_dbg[(slot) * 2048 + (idx)] = clock64(); \
@@ -344,6 +346,16 @@ __device__ __forceinline__ void tc_mma_f16(uint32_t d_tmem, uint64_t adesc, uint
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// D[tmem] (+)= A[tmem] * B[smem]^T, kind::f16, issued by one thread: A is
+// read from tensor memory (lane m = row m, column j = K elements 2j, 2j+1).
+__device__ __forceinline__ void tc_mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                              uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
 // Arrives once on `bar` when every MMA this thread issued before has completed.
 __device__ __forceinline__ void tc_commit(uint64_t* bar) {
   asm volatile(
@@ -364,6 +376,26 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t v[32]) {
         "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
       : "r"(taddr));
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// 16 lanes x 32 columns of 32-bit TMEM cells from the warp's registers, in the
+// layout of the mma.sync accumulator fragment repeated along the columns:
+// thread 4g + c writes, for repetition r (columns [8r, 8r + 8)), lane g columns
+// 8r + 2c and 8r + 2c + 1 from r[4r], r[4r + 1] and lane g + 8 the same two
+// columns from r[4r + 2], r[4r + 3].  `taddr` carries the first lane (the
+// warp's lane quadrant or its upper half) and the first column.
+__device__ __forceinline__ void tmem_st16x256_x4(uint32_t taddr, const uint32_t r[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.16x256b.x4.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+      "%13,%14,%15,%16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+      "r"(r[15])
+      : "memory");
+}
+// Waits until this thread's tensor-memory stores have completed.
+__device__ __forceinline__ void tmem_wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
 // Shared-memory matrix descriptor, K-major operand with the 128-byte swizzle:

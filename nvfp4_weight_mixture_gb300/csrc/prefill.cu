@@ -4,31 +4,39 @@
 // "[Kernel][SM70] Improve Qwen3.8 no-MTP concurrency", section "Scope and
 // related PRs": grouped W13 with SwiGLU and grouped W2 with the reduction,
 // both driven by the same integer plan.  A work unit is one plan tile (one
-// expert, up to 256 of its routed rows) times 256 weight rows:
+// expert, up to 192 of its routed rows) times 256 weight rows:
 //
 //   D[weight row][token] = sum_k W[weight row][k] * X[token][k]     (swap-AB)
 //
-// so the weight rows are the MMA's M = 128 (two accumulators of N <= 256
-// columns fill the 512 tensor-memory columns) and the tokens are N.  Blocks
-// are persistent (one per SM) and walk the units with a static stride.
+// so the weight rows are the MMA's M = 128 (two accumulators of N <= 192
+// columns) and the tokens are N.  The dequantised weights (A) go to tensor
+// memory, not shared memory: tensor memory holds the two accumulators
+// (384 columns) and two A stages of one K step each (2 x 64 columns), and the
+// shared-memory bandwidth is left to the token rows (B) and raw weights.
+// Blocks are persistent (one per SM) and walk the units with a static stride.
 // Warp roles, each running ahead as far as its ring allows:
 //   warp 13    one lane streams the unit's raw NVFP4 blocks (fragment layout:
-//              16 blocks of 512 + 64 bytes per K step of 64) into a 4-deep
-//              shared ring with two bulk asynchronous copies per K step;
-//   warps 0-7  dequantise each raw stage into 128-byte-swizzled K-major FP16
-//              A tiles (2-deep ring; two fragment blocks per warp), then run
-//              the unit's epilogue, warp w on TMEM lanes 32 (w % 4) .. +31 of
-//              accumulator w / 4;
-//   warp 8     one lane fills the token-row operand, one 3-deep ring stage per
-//              K step (same swizzled layout), with 64-row tensor-map loads of
+//              16 blocks of 512 + 64 bytes per K step of 64) into a shared
+//              ring with two bulk asynchronous copies per K step;
+//   warps 0-7  dequantise each raw stage into tensor memory (two fragment
+//              blocks per warp: warp w owns lanes 32 (w % 4) .. +31 of A tile
+//              w / 4, the lanes its sub-partition may access), then run the
+//              unit's epilogue on the same lanes of accumulator w / 4;
+//   warp 8     one lane fills the token-row operand, one ring stage per K step
+//              (128-byte swizzled, K-major), with 64-row tensor-map loads of
 //              the plan-ordered rows: x gathered beforehand for W13, h for W2
 //              (warps 9-11 are spare);
 //   warp 12    allocates tensor memory; one lane issues the MMAs: per K step
 //              one wait on each ring, then per A tile and 16-element K slice one
 //              MMA with N = all of the unit's rows, then one commit per ring.
-//              (The issuing thread shares its SM sub-partition with busy
-//              dequantise and gather warps, so its per-step instruction chain
-//              is kept short.)
+//
+// K order inside each 64-element K step.  A warp's dequantised values sit in
+// the mma.sync fragment order (thread 4g + c: rows g, g + 8, elements
+// [16c, 16c + 16)), and the 16x256b tensor-memory store puts that thread's
+// 4-element group r at K positions [16r + 4c, 16r + 4c + 4).  So position
+// 16r + 4c + e of A holds element 16c + 4r + e; the token-row operands are
+// written in the same order (the row gather for W13, the W13 epilogue for
+// h), and the products pair up as in the natural order.
 //
 // W13: the fragment layout interleaves 16-row gate and up tiles, so TMEM lanes
 // [32q, 32q+16) hold gate rows and [32q+16, 32q+32) the matching up rows; the
@@ -45,17 +53,15 @@
 namespace moe {
 
 constexpr int kBK = 64;                   // K per step (128 bytes of FP16)
-constexpr int kATile = 128 * 128;         // one 128-row FP16 A tile, bytes
-constexpr int kBTile = kTileRows * 128;   // the B tile, bytes
-constexpr int kAS = 2;                    // A (dequantised) stages
-constexpr int kBChunkRows = 64;           // one gather warp's share: 64 token rows x 128 bytes
+constexpr int kAS = 2;                    // A (dequantised) stages in tensor memory
+constexpr int kBChunkRows = 64;           // rows per tensor-map load: 64 token rows x 128 bytes
 constexpr int kBChunk = kBChunkRows * 128;
-constexpr int kBStage = 4 * kBChunk;      // B ring stage: one K step of up to 256 rows
-constexpr int kBStages = 3;               // B ring stages (96 KiB)
-constexpr int kRS = 4;                    // raw weight stages
+constexpr int kBStage = kTileRows * 128;  // B ring stage: one K step of up to 192 rows
+constexpr int kBStages = 4;               // B ring stages (96 KiB)
+constexpr int kRS = 8;                    // raw weight stages
 constexpr int kRawQ = 16 * 512;           // raw q bytes per K step (16 fragment blocks)
 constexpr int kRawBytes = kRawQ + 16 * 64;
-// Warp roles: 0-7 dequantise and run the epilogue, 8-11 fill the token-row
+// Warp roles: 0-7 dequantise and run the epilogue, 8 fills the token-row
 // operand, 12 issues the MMAs (and owns tensor memory), 13 streams raw weights.
 constexpr int kDqWarps = 8;
 constexpr int kDqThreads = kDqWarps * 32;
@@ -63,16 +69,27 @@ constexpr int kBWarp0 = 8;
 constexpr int kMmaWarp = 12;
 constexpr int kRawWarp = 13;
 constexpr int kGemmThreads = 14 * 32;
+// Tensor memory: accumulator t at column t * kTileRows, A stage s, tile t at
+// column kAOff + s * 64 + t * 32 (64 FP16 of K per row = 32 columns).
 constexpr int kTmemCols = 512;
-constexpr int kOffA = 0;
-constexpr int kOffB = kOffA + kAS * 2 * kATile;
+constexpr int kAOff = 2 * kTileRows;
+static_assert(kAOff + kAS * 2 * (kBK / 2) <= kTmemCols, "tensor memory over-committed");
+static_assert(kTileRows % kBChunkRows == 0 && kTileRows % 16 == 0 && kTileRows <= 256,
+              "plan tile height must be a multiple of 64 and a valid MMA N");
+constexpr int kOffB = 0;
 constexpr int kOffRaw = kOffB + kBStages * kBStage;
 constexpr int kOffMeta = kOffRaw + kRS * kRawBytes;
+static_assert(kBStage % 1024 == 0, "B stages must stay 1024-byte aligned for the swizzle");
+static_assert(kBStages % kAS == 0 && kBStages >= 2 * kAS,
+              "one barrier per K step serves both rings: B ring a multiple of, and at least twice, the A ring");
 
 struct GemmSmem {
   uint64_t raw_full[kRS], raw_empty[kRS];
-  uint64_t a_full[kAS], a_empty[kAS];
-  uint64_t b_full[kBStages], b_empty[kBStages];
+  // K step k: full[k % kBStages] completes when A stage k % kAS is in tensor
+  // memory (one arrival per dequantising warp) and B stage k % kBStages has
+  // landed (the loading thread's arrival plus the transaction bytes); the MMA
+  // thread commits K step k to empty[k % kBStages], which frees both.
+  uint64_t full[kBStages], empty[kBStages];
   uint64_t accf, tmem_empty, drain;
   uint32_t tmem;
   int abort;
@@ -112,9 +129,12 @@ __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
 // Profiling cells (timeline build): [0..1] raw producer wait/issue, [2..3]
 // MMA thread total / unit bookkeeping, [4..7]
 // MMA wait-A / wait-B / issue / wait-TMEM, [8..9] B wait/issue, [10..14]
-// dequant wait-raw / wait-A / work, epilogue wait / work; [16 + 2k] = calls.
+// dequant wait-raw / wait-A / work, epilogue wait / work (W13); W2 at 16 + the
+// same offsets.
+// Each thread sums its cells in registers and adds them to g_prof once, at
+// exit, so that no global atomic sits inside a pipeline loop.
 #ifdef MOE_TIMELINE
-#define PROF_ADD(cell, t0) atomicAdd(&g_prof[cell], (unsigned long long)(clock64() - (t0)))
+#define PROF_ADD(cell, t0) (pacc[(cell) - poff] += (unsigned long long)(clock64() - (t0)))
 #else
 #define PROF_ADD(cell, t0)
 #endif
@@ -157,6 +177,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   MOE_TL(kW13 ? kTlW13 : kTlW2);
   MOE_PROF(constexpr int poff = kW13 ? 0 : 16);
+  MOE_PROF(unsigned long long pacc[15] = {});
 
   const int K = kW13 ? d.H : d.I;           // reduction length
   const int S = K / kBK;                     // K steps per unit
@@ -165,18 +186,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   if (tid == 0) {
     for (int i = 0; i < kRS; ++i) {
       mbar_init(&sm->raw_full[i], 1);
-      mbar_init(&sm->raw_empty[i], kDqThreads);
-    }
-    for (int i = 0; i < kAS; ++i) {
-      mbar_init(&sm->a_full[i], kDqThreads);
-      mbar_init(&sm->a_empty[i], 1);
+      mbar_init(&sm->raw_empty[i], kDqWarps);
     }
     for (int i = 0; i < kBStages; ++i) {
-      mbar_init(&sm->b_full[i], 1);  // the loading thread, plus the transaction bytes
-      mbar_init(&sm->b_empty[i], 1);
+      mbar_init(&sm->full[i], kDqWarps + 1);
+      mbar_init(&sm->empty[i], 1);
     }
     mbar_init(&sm->accf, 1);
-    mbar_init(&sm->tmem_empty, kDqThreads);
+    mbar_init(&sm->tmem_empty, kDqWarps);
     mbar_init(&sm->drain, 1);
     sm->abort = 0;
     fence_mbar_init();
@@ -215,6 +232,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           const size_t blk = ((size_t)grp * S + ks) * 16;
           bulk_g2s(dst, un.q + blk * 512, kRawQ, &sm->raw_full[slot]);
           bulk_g2s(dst + kRawQ, un.s + blk * 64, kRawBytes - kRawQ, &sm->raw_full[slot]);
+          if (kW13) MOE_DBG(6, kr);
           MOE_PROF(PROF_ADD(poff + 1, t0));
           ++kr;
         }
@@ -239,36 +257,31 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         MOE_PROF(PROF_ADD(poff + 7, t0));
         tc_fence_after();
         bool ok = true;
-        // per K step: one A stage (two 128-row tiles) and one B stage (all of
-        // the unit's token rows); one MMA per tile and 16-element K slice
+        // per K step: one wait (A stage and B stage of the step), then per A
+        // tile and 16-element K slice one MMA with N = all of the unit's rows,
+        // then one commit that frees both stages
         for (int ks = 0; ks < S; ++ks, ++ka) {
           const int as = ka % kAS, bs = ka % kBStages;
           MOE_PROF(t0 = clock64());
-          if (!wait_or_abort(&sm->a_full[as], (ka / kAS) & 1, status, abort)) {
+          if (!wait_or_abort(&sm->full[bs], (ka / kBStages) & 1, status, abort)) {
             ok = false;
             break;
           }
           if (kW13) MOE_DBG(2, ka);
           MOE_PROF(PROF_ADD(poff + 4, t0); t0 = clock64());
-          if (!wait_or_abort(&sm->b_full[bs], (ka / kBStages) & 1, status, abort)) {
-            ok = false;
-            break;
-          }
-          if (kW13) MOE_DBG(1, ka);
-          MOE_PROF(PROF_ADD(poff + 5, t0); t0 = clock64());
           tc_fence_after();
-          const uint64_t da0 = sdesc_sw128(smem_u32(base + kOffA + as * 2 * kATile));
-          const uint64_t da1 = sdesc_sw128(smem_u32(base + kOffA + as * 2 * kATile + kATile));
+          const uint32_t ta = tmem + kAOff + as * kBK;
           const uint64_t db = sdesc_sw128(smem_u32(base + kOffB + bs * kBStage));
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk) {
             const uint32_t acc = (ks | kk) ? 1u : 0u;
-            // +32 bytes along K inside the 128-byte swizzle atom: start address + 2
-            tc_mma_f16(tmem, da0 + 2 * kk, db + 2 * kk, idesc, acc);
-            tc_mma_f16(tmem + 256, da1 + 2 * kk, db + 2 * kk, idesc, acc);
+            // B: +32 bytes along K inside the 128-byte swizzle atom (start
+            // address + 2); A: +8 tensor-memory columns; tile t in accumulator t
+            tc_mma_f16_ts(tmem, ta + 8 * kk, db + 2 * kk, idesc, acc);
+            tc_mma_f16_ts(tmem + kTileRows, ta + kBK / 2 + 8 * kk, db + 2 * kk, idesc, acc);
           }
-          tc_commit(&sm->b_empty[bs]);
-          tc_commit(&sm->a_empty[as]);
+          tc_commit(&sm->empty[bs]);
+          if (kW13) MOE_DBG(0, ka);
           MOE_PROF(PROF_ADD(poff + 6, t0));
         }
         if (!ok) break;
@@ -283,7 +296,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
   } else if (warp == kBWarp0) {
     // ---- B producer (one thread): the unit's token rows, one ring stage per K
-    // step (up to 256 rows, 128-byte swizzle), loaded as 64-row tiles of the
+    // step (up to 192 rows, 128-byte swizzle), loaded as 64-row tiles of the
     // plan-ordered operand (x rows gathered into plan order for W13, h for W2).
     if (lane == 0) {
       uint32_t kb = 0;
@@ -294,27 +307,46 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         for (int ks = 0; ks < S; ++ks, ++kb) {
           const int bs = kb % kBStages;
           MOE_PROF(long long t0 = clock64());
-          if (!wait_or_abort(&sm->b_empty[bs], ((kb / kBStages) & 1) ^ 1, status, abort)) {
+          if (!wait_or_abort(&sm->empty[bs], ((kb / kBStages) & 1) ^ 1, status, abort)) {
             ok = false;
             break;
           }
           MOE_PROF(PROF_ADD(poff + 8, t0); t0 = clock64());
-          mbar_expect_tx(&sm->b_full[bs], (uint32_t)(nch * kBChunk));
+          mbar_expect_tx(&sm->full[bs], (uint32_t)(nch * kBChunk));
           for (int ch = 0; ch < nch; ++ch)
             tma_load_2d(base + kOffB + bs * kBStage + ch * kBChunk, &bmap, ks * kBK,
-                        un.pos0 + ch * kBChunkRows, &sm->b_full[bs]);
+                        un.pos0 + ch * kBChunkRows, &sm->full[bs]);
+          if (kW13) MOE_DBG(5, kb);
           MOE_PROF(PROF_ADD(poff + 9, t0));
         }
       }
-      // loads still in flight land before the block exits (bounded waits)
+      // loads still in flight land before the block exits (bounded waits; each
+      // of these phases completes once the dequantisers have arrived too, or
+      // the wait gives up after an abort)
       for (uint32_t k = (kb > (uint32_t)kBStages ? kb - kBStages : 0); k < kb; ++k)
-        mbar_wait(&sm->b_full[k % kBStages], (k / kBStages) & 1, status);
+        mbar_wait(&sm->full[k % kBStages], (k / kBStages) & 1, status);
     }
   } else if (warp > kBWarp0) {
-    // spare warps
+    // spare warps (timeline build: two of them stamp when each raw and B stage
+    // lands, following the rings' phases without taking part in them)
+#ifdef MOE_TIMELINE
+    if (kW13 && blockIdx.x == 0 && lane == 0 && (warp == 9 || warp == 10)) {
+      const int n_mine = (n_units - 1 - (int)blockIdx.x) / (int)gridDim.x + 1;
+      const int nst = warp == 9 ? kRS : kBStages;
+      uint64_t* bars = warp == 9 ? sm->raw_full : sm->full;
+      for (int k = 0; k < n_mine * S && k < 2048 && !*abort; ++k) {
+        const long long t0 = clock64();
+        bool seen = false;
+        while (!(seen = mbar_try_wait(&bars[k % nst], (k / nst) & 1)) && !*abort &&
+               clock64() - t0 < (kWaitTimeoutCycles >> 4)) {
+        }
+        if (!seen) break;
+        g_dbg[(warp == 9 ? 8 : 9) * 2048 + k] = clock64();
+      }
+    }
+#endif
   } else {
     // ---- warps 0-7: dequantise, then the unit's epilogue ---------------------------
-    const int g = lane >> 2, c = lane & 3;
     uint32_t kd = 0, it = 0;
     for (int u = blockIdx.x; u < n_units && !*abort; u += gridDim.x, ++it) {
       const Unit un = load_unit<kW13>(d, pv, w, ws, u, upt);
@@ -326,6 +358,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
       }
       bool ok = true;
+      // this warp's two fragment blocks j = 2 warp + jj: rows 32 (warp % 4) + 16 jj
+      // .. + 15 of A tile warp / 4
+      const uint32_t ta_warp = ((uint32_t)(32 * (warp & 3)) << 16) + kAOff + (warp >> 2) * (kBK / 2);
       for (int ks = 0; ks < S; ++ks, ++kd) {
         const int rs = kd % kRS, as = kd % kAS;
         MOE_PROF(long long t0 = clock64());
@@ -334,42 +369,46 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           break;
         }
         MOE_PROF(if (tid == 0) PROF_ADD(poff + 10, t0); t0 = clock64());
-        if (!wait_or_abort(&sm->a_empty[as], ((kd / kAS) & 1) ^ 1, status, abort)) {
-          ok = false;
-          break;
+        const char* raw = base + kOffRaw + rs * kRawBytes;
+        uint4 q[2];
+        uint32_t sc[2];
+#pragma unroll
+        for (int jj = 0; jj < 2; ++jj) {
+          const int j = warp * 2 + jj;
+          q[jj] = *reinterpret_cast<const uint4*>(raw + j * 512 + lane * 16);
+          sc[jj] = *reinterpret_cast<const unsigned short*>(raw + kRawQ + j * 64 + lane * 2);
         }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm->raw_empty[rs]);  // the stage is in registers
+        // A stage kd % kAS was last read by the MMAs of K step kd - kAS
+        if (kd >= (uint32_t)kAS) {
+          const uint32_t kp = kd - kAS;
+          if (!wait_or_abort(&sm->empty[kp % kBStages], (kp / kBStages) & 1, status, abort)) {
+            ok = false;
+            break;
+          }
+        }
+        tc_fence_after();
         MOE_PROF(if (tid == 0) PROF_ADD(poff + 11, t0); t0 = clock64());
         if (kW13 && lane == 0) MOE_DBG(3, kd * kDqWarps + warp);
-        const char* raw = base + kOffRaw + rs * kRawBytes;
-        char* stage = base + kOffA + as * 2 * kATile;
 #pragma unroll
-        for (int jj = 0; jj < 16 / kDqWarps; ++jj) {
-          // fragment block j: A tile j / 8, local row tile j % 8
-          const int j = warp * (16 / kDqWarps) + jj;
-          const uint4 q = *reinterpret_cast<const uint4*>(raw + j * 512 + lane * 16);
-          const uint32_t sc =
-              *reinterpret_cast<const unsigned short*>(raw + kRawQ + j * 64 + lane * 2);
-          char* at = stage + (j >> 3) * kATile;
-          const int r = (j & 7) * 16 + g;
-          const uint32_t f = e4m3x2_to_f16x2(sc);
+        for (int jj = 0; jj < 2; ++jj) {
+          const uint32_t f = e4m3x2_to_f16x2(sc[jj]);
           const uint32_t sg = __byte_perm(f, f, 0x1010), sg8 = __byte_perm(f, f, 0x3232);
-          uint32_t o[4];
-          dequant8(q.x, sg, o);
-          *reinterpret_cast<uint4*>(at + sw128_off(r, 2 * c)) = make_uint4(o[0], o[1], o[2], o[3]);
-          dequant8(q.y, sg, o);
-          *reinterpret_cast<uint4*>(at + sw128_off(r, 2 * c + 1)) =
-              make_uint4(o[0], o[1], o[2], o[3]);
-          dequant8(q.z, sg8, o);
-          *reinterpret_cast<uint4*>(at + sw128_off(r + 8, 2 * c)) =
-              make_uint4(o[0], o[1], o[2], o[3]);
-          dequant8(q.w, sg8, o);
-          *reinterpret_cast<uint4*>(at + sw128_off(r + 8, 2 * c + 1)) =
-              make_uint4(o[0], o[1], o[2], o[3]);
+          uint32_t x[4], y[4], z[4], w4[4];
+          dequant8(q[jj].x, sg, x);   // row g,     elements 16c + 0..7
+          dequant8(q[jj].y, sg, y);   // row g,     elements 16c + 8..15
+          dequant8(q[jj].z, sg8, z);  // row g + 8, elements 16c + 0..7
+          dequant8(q[jj].w, sg8, w4); // row g + 8, elements 16c + 8..15
+          const uint32_t r[16] = {x[0], x[1], z[0], z[1], x[2], x[3], z[2], z[3],
+                                  y[0], y[1], w4[0], w4[1], y[2], y[3], w4[2], w4[3]};
+          tmem_st16x256_x4(tmem + ta_warp + ((uint32_t)(16 * jj) << 16) + as * kBK, r);
         }
-        fence_proxy_async();
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
         if (kW13 && lane == 0) MOE_DBG(4, kd * kDqWarps + warp);
-        mbar_arrive(&sm->a_full[as]);
-        mbar_arrive(&sm->raw_empty[rs]);
+        if (lane == 0) mbar_arrive(&sm->full[kd % kBStages]);
         MOE_PROF(if (tid == 0) PROF_ADD(poff + 12, t0));
       }
       if (!ok) break;
@@ -379,6 +418,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const int q4 = warp & 3, at = warp >> 2;
       MOE_PROF(long long te = clock64());
       if (!wait_or_abort(&sm->accf, it & 1, status, abort)) break;
+      if (kW13 && tid == 0) MOE_DBG(7, 2 * it);
       MOE_PROF(if (tid == 0) PROF_ADD(poff + 13, te); te = clock64());
       tc_fence_after();
       if (kW13) {
@@ -386,17 +426,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         // matching up row, for 32 token columns per load.  One exchange per
         // pair of columns gives each lane 16 (G, U) pairs: gate lanes take
         // columns 0-15, up lanes 16-31.  h goes through a per-warp staging
-        // tile so that each token row leaves as two 16-byte stores.
+        // tile; each token row's 16 values [16q, 16q + 16) of the 64-wide K
+        // step leave as four 8-byte groups, group r at position 16r + 4q (the
+        // K order of the W2 operand).
         const int I = d.I;
         const int r16 = lane & 15;
         const bool is_gate = lane < 16;
         __half(*stg)[16] = reinterpret_cast<__half(*)[16]>(sm->stage[warp]);
         {
-          const int i0 = un.sub * 128 + at * 64 + q4 * 16;
+          const int i64 = un.sub * 128 + at * 64;  // the 64-wide K step of W2
+          const int i0 = i64 + q4 * 4;
 #pragma unroll 1
           for (int c0 = 0; c0 < un.npad; c0 += 32) {
             uint32_t v[32];
-            tmem_ld32(tmem + ((uint32_t)(q4 * 32) << 16) + at * 256 + c0, v);
+            tmem_ld32(tmem + ((uint32_t)(q4 * 32) << 16) + at * kTileRows + c0, v);
 #pragma unroll
             for (int jj = 0; jj < 16; ++jj) {
               const float lo = __uint_as_float(v[jj]), hi = __uint_as_float(v[jj + 16]);
@@ -409,10 +452,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             __syncwarp();
             const int n = c0 + lane;
             if (n < un.rows) {
-              const uint4* s4 = reinterpret_cast<const uint4*>(stg[lane]);
-              uint4* dst = reinterpret_cast<uint4*>(h_out + (int64_t)(un.pos0 + n) * I + i0);
-              dst[0] = s4[0];
-              dst[1] = s4[1];
+              const uint2* s2 = reinterpret_cast<const uint2*>(stg[lane]);
+              __half* dst = h_out + (int64_t)(un.pos0 + n) * I + i0;
+#pragma unroll
+              for (int r = 0; r < 4; ++r) *reinterpret_cast<uint2*>(dst + 16 * r) = s2[r];
             }
             __syncwarp();
           }
@@ -430,7 +473,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 #pragma unroll 1
           for (int c0 = 0; c0 < un.npad; c0 += 32) {
             uint32_t v[32];
-            tmem_ld32(tmem + ((uint32_t)(q4 * 32) << 16) + at * 256 + c0, v);
+            tmem_ld32(tmem + ((uint32_t)(q4 * 32) << 16) + at * kTileRows + c0, v);
 #pragma unroll
             for (int hf = 0; hf < 2; ++hf) {
 #pragma unroll
@@ -458,7 +501,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
       }
       tc_fence_before();
-      mbar_arrive(&sm->tmem_empty);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm->tmem_empty);
+      if (kW13 && tid == 0) MOE_DBG(7, 2 * it + 1);
       MOE_PROF(if (tid == 0) PROF_ADD(poff + 14, te));
     }
   }
@@ -468,11 +513,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
+#ifdef MOE_TIMELINE
+#pragma unroll
+  for (int i = 0; i < 15; ++i)
+    if (pacc[i]) atomicAdd(&g_prof[poff + i], pacc[i]);
+#endif
 }
 
 // xg[pos] = x[perm[pos] / k_eff]: the token rows in plan order, the operand of
-// the grouped W13 GEMM (positions past the valid pairs are left alone).
-// One warp per row, 16-byte loads and stores.
+// the grouped W13 GEMM (positions past the valid pairs are left alone), with
+// each 64-element K step in the order of the tensor-memory A operand: output
+// position 16r + 4c + e takes element 16c + 4r + e.  One warp per row; each
+// lane writes 16 bytes (positions [8m, 8m + 8): r = m / 2, c = 2 (m % 2) and
+// 2 (m % 2) + 1) from two 8-byte loads.
 __global__ void gather_rows_kernel(LayerDims d, PlanView pv, const __half* __restrict__ x,
                                    __half* __restrict__ xg) {
   MOE_TL(kTlPlan);
@@ -482,9 +535,15 @@ __global__ void gather_rows_kernel(LayerDims d, PlanView pv, const __half* __res
   const int lane = threadIdx.x & 31;
   if (row >= __ldcg(&pv.hdr->n_valid)) return;
   const int t = __ldcg(pv.perm + row) / d.k_eff;
-  const uint4* src = reinterpret_cast<const uint4*>(x + (int64_t)t * d.H);
+  const __half* src = x + (int64_t)t * d.H;
   uint4* dst = reinterpret_cast<uint4*>(xg + row * d.H);
-  for (int c = lane; c < d.H / 8; c += 32) dst[c] = __ldg(src + c);
+  for (int ch = lane; ch < d.H / 8; ch += 32) {
+    const int k0 = (ch >> 3) * 64, m = ch & 7;
+    const int r = m >> 1, c = 2 * (m & 1);
+    const uint2 lo = __ldg(reinterpret_cast<const uint2*>(src + k0 + 16 * c + 4 * r));
+    const uint2 hi = __ldg(reinterpret_cast<const uint2*>(src + k0 + 16 * (c + 1) + 4 * r));
+    dst[ch] = make_uint4(lo.x, lo.y, hi.x, hi.y);
+  }
 }
 
 cudaError_t launch_prefill_forward(const LayerDims& d, int64_t M, const __half* x,
@@ -504,7 +563,7 @@ cudaError_t launch_prefill_forward(const LayerDims& d, int64_t M, const __half* 
     if (e != cudaSuccess) return e;
     attr_done = true;
   }
-  const int g13 = (int)std::min<int64_t>((int64_t)max_tiles * ((2 * d.I) / 256), num_sms);
+  const int g13 = (int)std::min<int64_t>((int64_t)max_tiles * ((2 * d.I) / 256), num_sms);  // 256 weight rows per unit
   const int g2 = (int)std::min<int64_t>((int64_t)max_tiles * (d.H / 256), num_sms);
   const bool pdl = !trace_on();
   // Token-row operands in plan order, read as 64-row tensor-map tiles (128-byte

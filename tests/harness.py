@@ -157,7 +157,7 @@ class Case:
                            self.wl.E + int(self.wl.shared), self.wl.E, self.wl.H)
 
 
-TILE_ROWS = 256
+TILE_ROWS = 192
 PLAN_CHUNK = 4096
 DECODE_MAX_TOKENS = 16
 
