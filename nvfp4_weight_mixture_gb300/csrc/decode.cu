@@ -445,8 +445,9 @@ __global__ void __launch_bounds__(kW2Warps * 32, 1)
 }
 
 // ---------------------------------------------------------------------------
-// y[t] = fp16( sum_{j < k_eff} partial[t * k_eff + j] ), slots in order; pairs
-// dropped from the plan (invalid ids) contribute nothing.
+// y[t] = fp16( sum_{j < k_eff} partial[inv[t * k_eff + j]] ), slots in order
+// (the partial rows sit at the pairs' plan positions); pairs dropped from the
+// plan (invalid ids) contribute nothing.
 // ---------------------------------------------------------------------------
 __global__ void combine_kernel(int M, int H, int k_eff, const int32_t* __restrict__ inv,
                                const float* __restrict__ partial, __half* __restrict__ y) {
@@ -460,9 +461,9 @@ __global__ void combine_kernel(int M, int H, int k_eff, const int32_t* __restric
   const int c = (int)(i * 4 - t * H);
   float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
   for (int j = 0; j < k_eff; ++j) {
-    const int64_t pair = t * k_eff + j;
-    if (__ldcg(inv + pair) < 0) continue;
-    const float4 v = __ldcs(reinterpret_cast<const float4*>(partial + pair * H + c));
+    const int64_t pos = __ldcg(inv + t * k_eff + j);  // the pair's plan position
+    if (pos < 0) continue;
+    const float4 v = __ldcs(reinterpret_cast<const float4*>(partial + pos * H + c));
     s.x += v.x;
     s.y += v.y;
     s.z += v.z;

@@ -34,7 +34,8 @@ cudaError_t launch_plan(const LayerDims& d, int64_t M, const __half* x, const __
                         float* w_user, bool ids_given, const PlanView& pv, uint32_t* status,
                         cudaStream_t stream, int num_sms);
 
-// Forward paths.  partial: FP32 [M * k_eff][H]; h: FP16 [M * k_eff][I].
+// Forward paths.  partial: FP32 [M * k_eff][H], one row per pair at its plan
+// position; h: FP16 [M * k_eff][I] in plan order.
 cudaError_t launch_decode_forward(const LayerDims& d, int64_t M, const __half* x,
                                   const PlanView& pv, Weights w13, Weights w2, Weights s13,
                                   Weights s2, __half* y, __half* h, float* partial,

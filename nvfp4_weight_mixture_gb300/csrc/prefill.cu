@@ -42,7 +42,8 @@
 // [32q, 32q+16) hold gate rows and [32q+16, 32q+32) the matching up rows; the
 // epilogue pairs them with one shuffle and writes h = fp16(silu(G) * U).
 // W2:  the epilogue scales by g2 and the pair's combine weight and writes the
-// FP32 partial row of each pair; a separate pass sums the slots in order.
+// FP32 partial row of each pair at its plan position (rows of a unit are
+// consecutive); a separate pass sums each token's slots in order.
 #include <math.h>
 
 #include <algorithm>
@@ -94,8 +95,7 @@ struct GemmSmem {
   uint32_t tmem;
   int abort;
   int n_units;
-  int epair[2][kTileRows];   // epilogue (W2): pair id of each row
-  float ewsc[2][kTileRows];  // epilogue (W2): g2 * combine weight of each row
+  __align__(16) float ewsc[2][kTileRows];  // epilogue (W2): g2 * combine weight of each row
   // epilogue staging, 2 KiB per warp: W13 h values [32 tokens][16 i] (FP16),
   // W2 partial values [16 pairs][32 rows] (FP32)
   __align__(16) float stage[kDqWarps][512];
@@ -353,7 +353,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       if (!kW13) {
         for (int n = tid; n < un.rows; n += kDqThreads) {
           const int pair = __ldcg(pv.perm + un.pos0 + n);
-          sm->epair[it & 1][n] = pair;
           sm->ewsc[it & 1][n] = un.g * __ldcg(pv.w + pair);
         }
       }
@@ -461,42 +460,41 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           }
         }
       } else {
-        // Lane r of warp q holds output row hd = ... + 32q + r for 32 pair
-        // columns per load; a per-warp staging tile turns 16 columns at a time
-        // into rows of 32 contiguous FP32 values, written as 16-byte stores.
+        // Lane r of warp q holds output row hd = sub * 256 + 128 at + 32 q + r
+        // for 32 pair columns per load; a per-warp staging tile turns 16
+        // columns at a time into rows of 32 contiguous FP32 values, written
+        // as 16-byte stores into the pairs' partial rows, which sit at the
+        // pairs' plan positions (consecutive for the unit).
         const int H = d.H;
-        const int* pr = sm->epair[it & 1];
         const float* wsc = sm->ewsc[it & 1];
         float(*stg)[32] = reinterpret_cast<float(*)[32]>(sm->stage[warp]);
-        {
-          const int hd0 = un.sub * 256 + at * 128 + q4 * 32;
+        float* pbase = partial + (int64_t)un.pos0 * H + un.sub * 256 + at * 128 + q4 * 32;
 #pragma unroll 1
-          for (int c0 = 0; c0 < un.npad; c0 += 32) {
-            uint32_t v[32];
-            tmem_ld32(tmem + ((uint32_t)(q4 * 32) << 16) + at * kTileRows + c0, v);
+        for (int c0 = 0; c0 < un.npad; c0 += 32) {
+          uint32_t v[32];
+          tmem_ld32(tmem + ((uint32_t)(q4 * 32) << 16) + at * kTileRows + c0, v);
 #pragma unroll
-            for (int hf = 0; hf < 2; ++hf) {
+          for (int hf = 0; hf < 2; ++hf) {
 #pragma unroll
-              for (int j = 0; j < 16; ++j) stg[j][lane] = __uint_as_float(v[16 * hf + j]);
-              __syncwarp();
-              // lanes 8p .. 8p+7 write column (pair) p0 + p: 8 x 16 bytes
-              const int cl = lane >> 3, part = lane & 7;
+            for (int j = 0; j < 16; ++j) stg[j][lane] = __uint_as_float(v[16 * hf + j]);
+            __syncwarp();
+            // lanes 8p .. 8p+7 write column (pair) p0 + p: 8 x 16 bytes
+            const int cl = lane >> 3, part = lane & 7;
 #pragma unroll
-              for (int p4 = 0; p4 < 4; ++p4) {
-                const int j = p4 * 4 + cl;
-                const int n = c0 + 16 * hf + j;
-                if (n < un.rows) {
-                  float4 o = reinterpret_cast<const float4*>(stg[j])[part];
-                  const float sc = wsc[n];
-                  o.x *= sc;
-                  o.y *= sc;
-                  o.z *= sc;
-                  o.w *= sc;
-                  __stcs(reinterpret_cast<float4*>(partial + (int64_t)pr[n] * H + hd0) + part, o);
-                }
+            for (int p4 = 0; p4 < 4; ++p4) {
+              const int j = p4 * 4 + cl;
+              const int n = c0 + 16 * hf + j;
+              if (n < un.rows) {
+                float4 o = reinterpret_cast<const float4*>(stg[j])[part];
+                const float sc = wsc[n];
+                o.x *= sc;
+                o.y *= sc;
+                o.z *= sc;
+                o.w *= sc;
+                __stcs(reinterpret_cast<float4*>(pbase + (int64_t)n * H) + part, o);
               }
-              __syncwarp();
             }
+            __syncwarp();
           }
         }
       }
