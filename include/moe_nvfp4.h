@@ -121,6 +121,12 @@ int32_t moe_nvfp4_abi_version(void);
 /* Static text for a return code or a single MOE_ST_* bit; never NULL. */
 const char* moe_nvfp4_status_string(int32_t code);
 
+/* Name of the CUDA runtime error behind the calling thread's most recent
+ * MOE_ERR_CUDA return (for example "cudaErrorLaunchOutOfResources"), or ""
+ * if no call on this thread has returned MOE_ERR_CUDA.  Static text; never
+ * NULL. */
+const char* moe_nvfp4_last_cuda_error(void);
+
 /* Sizes, in bytes, of the plan buffer (for moe_nvfp4_plan) and of the
  * forward workspace (for moe_nvfp4_forward) for any M <= max_tokens.
  * Host-only arithmetic; also checks that the current device is an sm_103

@@ -98,8 +98,11 @@ int32_t check_weights(const moe_nvfp4_weights* w, int32_t layout) {
 void* const* g_trace_events = nullptr;
 int32_t g_trace_steps = 0;
 
+thread_local cudaError_t g_last_cuda_error = cudaSuccess;
+
 int32_t cuda_status(cudaError_t e) {
   if (e == cudaSuccess) return MOE_OK;
+  g_last_cuda_error = e;
   cudaGetLastError();
   return MOE_ERR_CUDA;
 }
@@ -162,6 +165,10 @@ int32_t moe_nvfp4_set_trace_events(void* const* events, int32_t n_steps) {
 }
 
 int32_t moe_nvfp4_abi_version(void) { return MOE_NVFP4_ABI_VERSION; }
+
+const char* moe_nvfp4_last_cuda_error(void) {
+  return g_last_cuda_error == cudaSuccess ? "" : cudaGetErrorName(g_last_cuda_error);
+}
 
 const char* moe_nvfp4_status_string(int32_t code) {
   switch (code) {

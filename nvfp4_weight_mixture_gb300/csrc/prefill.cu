@@ -65,10 +65,10 @@ constexpr int kRawBytes = kRawQ + 16 * 64;
 // Warp roles: 0-7 dequantise and run the epilogue, 8 fills the token-row
 // operand, 12 issues the MMAs (and owns tensor memory), 13 streams raw weights.
 constexpr int kDqWarps = 8;
-constexpr int kDqThreads = kDqWarps * 32;
 constexpr int kBWarp0 = 8;
 constexpr int kMmaWarp = 12;
 constexpr int kRawWarp = 13;
+constexpr int kScaleWarp = 9;  // W2 only
 constexpr int kGemmThreads = 14 * 32;
 // Tensor memory: accumulator t at column t * kTileRows, A stage s, tile t at
 // column kAOff + s * 64 + t * 32 (64 FP16 of K per row = 32 columns).
@@ -92,10 +92,13 @@ struct GemmSmem {
   // thread commits K step k to empty[k % kBStages], which frees both.
   uint64_t full[kBStages], empty[kBStages];
   uint64_t accf, tmem_empty, drain;
+  // W2: g2 * combine weight of each row of unit it in wsc[it & 1], written by
+  // the scale warp one unit ahead; wsc_full[b] completes when it is there
+  __align__(16) float wsc[2][kTileRows];
+  uint64_t wsc_full[2];
   uint32_t tmem;
   int abort;
   int n_units;
-  __align__(16) float ewsc[2][kTileRows];  // epilogue (W2): g2 * combine weight of each row
   // epilogue staging, 2 KiB per warp: W13 h values [32 tokens][16 i] (FP16),
   // W2 partial values [16 pairs][32 rows] (FP32)
   __align__(16) float stage[kDqWarps][512];
@@ -122,8 +125,12 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, ui
   }
 }
 
-__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+// Every lane of the warp waits; the outcome is made the same for the whole
+// warp (the tensor-memory instructions that follow are warp-wide, so the
+// warp goes on, or leaves after an abort, together).
+__device__ __forceinline__ bool warp_wait_or_abort(uint64_t* bar, uint32_t parity,
+                                                   uint32_t* status, volatile int* abort) {
+  return __all_sync(0xffffffffu, wait_or_abort(bar, parity, status, abort));
 }
 
 // Profiling cells (timeline build): [0..1] raw producer wait/issue, [2..3]
@@ -194,6 +201,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
     mbar_init(&sm->accf, 1);
     mbar_init(&sm->tmem_empty, kDqWarps);
+    mbar_init(&sm->wsc_full[0], 1);
+    mbar_init(&sm->wsc_full[1], 1);
     mbar_init(&sm->drain, 1);
     sm->abort = 0;
     fence_mbar_init();
@@ -326,6 +335,27 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       for (uint32_t k = (kb > (uint32_t)kBStages ? kb - kBStages : 0); k < kb; ++k)
         mbar_wait(&sm->full[k % kBStages], (k / kBStages) & 1, status);
     }
+  } else if (!kW13 && warp == kScaleWarp) {
+    // ---- W2 scale warp: g2 * combine weight of each row of each unit, one
+    // unit ahead of the epilogue, double-buffered (buffer it & 1 is free once
+    // the epilogue of unit it - 2 has finished)
+    uint32_t it = 0;
+    for (int u = blockIdx.x; u < n_units && !*abort; u += gridDim.x, ++it) {
+      const Unit un = load_unit<kW13>(d, pv, w, ws, u, upt);
+      if (it >= 2 && !warp_wait_or_abort(&sm->tmem_empty, (it - 2) & 1, status, abort)) break;
+      float* wsc = sm->wsc[it & 1];
+      int pr[kTileRows / 32];
+#pragma unroll
+      for (int i = 0; i < kTileRows / 32; ++i) {
+        const int n = lane + 32 * i;
+        pr[i] = n < un.rows ? __ldcg(pv.perm + un.pos0 + n) : -1;
+      }
+#pragma unroll
+      for (int i = 0; i < kTileRows / 32; ++i)
+        if (pr[i] >= 0) wsc[lane + 32 * i] = un.g * __ldcg(pv.w + pr[i]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm->wsc_full[it & 1]);
+    }
   } else if (warp > kBWarp0) {
     // spare warps (timeline build: two of them stamp when each raw and B stage
     // lands, following the rings' phases without taking part in them)
@@ -350,12 +380,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     uint32_t kd = 0, it = 0;
     for (int u = blockIdx.x; u < n_units && !*abort; u += gridDim.x, ++it) {
       const Unit un = load_unit<kW13>(d, pv, w, ws, u, upt);
-      if (!kW13) {
-        for (int n = tid; n < un.rows; n += kDqThreads) {
-          const int pair = __ldcg(pv.perm + un.pos0 + n);
-          sm->ewsc[it & 1][n] = un.g * __ldcg(pv.w + pair);
-        }
-      }
       bool ok = true;
       // this warp's two fragment blocks j = 2 warp + jj: rows 32 (warp % 4) + 16 jj
       // .. + 15 of A tile warp / 4
@@ -363,7 +387,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       for (int ks = 0; ks < S; ++ks, ++kd) {
         const int rs = kd % kRS, as = kd % kAS;
         MOE_PROF(long long t0 = clock64());
-        if (!wait_or_abort(&sm->raw_full[rs], (kd / kRS) & 1, status, abort)) {
+        if (!warp_wait_or_abort(&sm->raw_full[rs], (kd / kRS) & 1, status, abort)) {
           ok = false;
           break;
         }
@@ -382,7 +406,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         // A stage kd % kAS was last read by the MMAs of K step kd - kAS
         if (kd >= (uint32_t)kAS) {
           const uint32_t kp = kd - kAS;
-          if (!wait_or_abort(&sm->empty[kp % kBStages], (kp / kBStages) & 1, status, abort)) {
+          if (!warp_wait_or_abort(&sm->empty[kp % kBStages], (kp / kBStages) & 1, status, abort)) {
             ok = false;
             break;
           }
@@ -413,13 +437,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       if (!ok) break;
       // ---- epilogue of this unit: warp w reads TMEM lanes 32 (w % 4) .. +31 of
       // accumulator w / 4 ----
-      named_bar_sync(1, kDqThreads);  // epair / ewsc of this unit visible to every warp
       const int q4 = warp & 3, at = warp >> 2;
       MOE_PROF(long long te = clock64());
-      if (!wait_or_abort(&sm->accf, it & 1, status, abort)) break;
+      if (!warp_wait_or_abort(&sm->accf, it & 1, status, abort)) break;
       if (kW13 && tid == 0) MOE_DBG(7, 2 * it);
       MOE_PROF(if (tid == 0) PROF_ADD(poff + 13, te); te = clock64());
       tc_fence_after();
+      const uint32_t tbase = tmem + ((uint32_t)(q4 * 32) << 16) + at * kTileRows;
       if (kW13) {
         // Lane r < 16 of warp q holds gate row (16q + r) and lane r + 16 the
         // matching up row, for 32 token columns per load.  One exchange per
@@ -432,32 +456,29 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const int r16 = lane & 15;
         const bool is_gate = lane < 16;
         __half(*stg)[16] = reinterpret_cast<__half(*)[16]>(sm->stage[warp]);
-        {
-          const int i64 = un.sub * 128 + at * 64;  // the 64-wide K step of W2
-          const int i0 = i64 + q4 * 4;
+        const int i0 = un.sub * 128 + at * 64 + q4 * 4;  // the 64-wide K step of W2, group q
 #pragma unroll 1
-          for (int c0 = 0; c0 < un.npad; c0 += 32) {
-            uint32_t v[32];
-            tmem_ld32(tmem + ((uint32_t)(q4 * 32) << 16) + at * kTileRows + c0, v);
+        for (int c0 = 0; c0 < un.npad; c0 += 32) {
+          uint32_t v[32];
+          tmem_ld32(tbase + c0, v);
 #pragma unroll
-            for (int jj = 0; jj < 16; ++jj) {
-              const float lo = __uint_as_float(v[jj]), hi = __uint_as_float(v[jj + 16]);
-              const float recv = __shfl_xor_sync(0xffffffffu, is_gate ? hi : lo, 16);
-              const float G = (is_gate ? lo : recv) * un.g;
-              const float U = (is_gate ? recv : hi) * un.g;
-              const float hv = __fdividef(G, 1.f + __expf(-G)) * U;
-              stg[is_gate ? jj : jj + 16][r16] = __float2half_rn(hv);
-            }
-            __syncwarp();
-            const int n = c0 + lane;
-            if (n < un.rows) {
-              const uint2* s2 = reinterpret_cast<const uint2*>(stg[lane]);
-              __half* dst = h_out + (int64_t)(un.pos0 + n) * I + i0;
-#pragma unroll
-              for (int r = 0; r < 4; ++r) *reinterpret_cast<uint2*>(dst + 16 * r) = s2[r];
-            }
-            __syncwarp();
+          for (int jj = 0; jj < 16; ++jj) {
+            const float lo = __uint_as_float(v[jj]), hi = __uint_as_float(v[jj + 16]);
+            const float recv = __shfl_xor_sync(0xffffffffu, is_gate ? hi : lo, 16);
+            const float G = (is_gate ? lo : recv) * un.g;
+            const float U = (is_gate ? recv : hi) * un.g;
+            const float hv = __fdividef(G, 1.f + __expf(-G)) * U;
+            stg[is_gate ? jj : jj + 16][r16] = __float2half_rn(hv);
           }
+          __syncwarp();
+          const int n = c0 + lane;
+          if (n < un.rows) {
+            const uint2* s2 = reinterpret_cast<const uint2*>(stg[lane]);
+            __half* dst = h_out + (int64_t)(un.pos0 + n) * I + i0;
+#pragma unroll
+            for (int r = 0; r < 4; ++r) *reinterpret_cast<uint2*>(dst + 16 * r) = s2[r];
+          }
+          __syncwarp();
         }
       } else {
         // Lane r of warp q holds output row hd = sub * 256 + 128 at + 32 q + r
@@ -466,13 +487,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         // as 16-byte stores into the pairs' partial rows, which sit at the
         // pairs' plan positions (consecutive for the unit).
         const int H = d.H;
-        const float* wsc = sm->ewsc[it & 1];
+        if (!warp_wait_or_abort(&sm->wsc_full[it & 1], (it >> 1) & 1, status, abort)) break;
+        const float* wsc = sm->wsc[it & 1];
         float(*stg)[32] = reinterpret_cast<float(*)[32]>(sm->stage[warp]);
         float* pbase = partial + (int64_t)un.pos0 * H + un.sub * 256 + at * 128 + q4 * 32;
 #pragma unroll 1
         for (int c0 = 0; c0 < un.npad; c0 += 32) {
           uint32_t v[32];
-          tmem_ld32(tmem + ((uint32_t)(q4 * 32) << 16) + at * kTileRows + c0, v);
+          tmem_ld32(tbase + c0, v);
 #pragma unroll
           for (int hf = 0; hf < 2; ++hf) {
 #pragma unroll

@@ -18,6 +18,7 @@ LIB_PATH = os.path.join(_HERE, "libmoe_nvfp4.so")
 ABI_VERSION = 1
 
 OK = 0
+ERR_CUDA = -6
 ERR = {
     -1: "MOE_ERR_INVALID_ARG", -2: "MOE_ERR_SHAPE", -3: "MOE_ERR_ALIGNMENT",
     -4: "MOE_ERR_WORKSPACE", -5: "MOE_ERR_UNSUPPORTED_DEVICE", -6: "MOE_ERR_CUDA",
@@ -53,7 +54,10 @@ class WeightsC(ctypes.Structure):
 class MoEError(RuntimeError):
     def __init__(self, fn, code):
         self.code = code
-        super().__init__(f"{fn} failed: {ERR.get(code, code)} ({status_string(code)})")
+        msg = f"{fn} failed: {ERR.get(code, code)} ({status_string(code)})"
+        if code == ERR_CUDA:
+            msg += f" [{load_library().moe_nvfp4_last_cuda_error().decode()}]"
+        super().__init__(msg)
 
 
 _lock = threading.Lock()
@@ -74,6 +78,8 @@ def load_library(path: str = LIB_PATH):
         lib.moe_nvfp4_abi_version.restype = I32
         lib.moe_nvfp4_status_string.argtypes = [I32]
         lib.moe_nvfp4_status_string.restype = ctypes.c_char_p
+        lib.moe_nvfp4_last_cuda_error.argtypes = []
+        lib.moe_nvfp4_last_cuda_error.restype = ctypes.c_char_p
         lib.moe_nvfp4_query.argtypes = [P, I64, ctypes.POINTER(SZ), ctypes.POINTER(SZ)]
         lib.moe_nvfp4_query.restype = I32
         lib.moe_nvfp4_quantize.argtypes = [P, I64, I64, I64, I32, P, P, P, P, P]
