@@ -55,6 +55,10 @@ cudaError_t make_rows_map(CUtensorMap* map, const void* base, uint64_t row_bytes
 // optionally 128-byte swizzled (tma.cu).
 cudaError_t make_fp16_map(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows,
                           uint32_t box_cols, uint32_t box_rows, bool swizzle128);
+// The same with a swizzle of 0 (none), 32, 64 or 128 bytes; a swizzled box is
+// exactly one swizzle span wide (box_cols * 2 == swizzle_bytes).
+cudaError_t make_fp16_map_swz(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows,
+                              uint32_t box_cols, uint32_t box_rows, int swizzle_bytes);
 
 // Diagnostic per-step event records (moe_nvfp4_set_trace_events).
 enum TraceStep { kTracePlan = 0, kTraceW13 = 1, kTraceW2 = 2, kTraceCombine = 3 };

@@ -732,28 +732,25 @@ __global__ void plan_scatter_kernel(LayerDims d, int64_t P, PlanView pv) {
 }
 
 // ---------------------------------------------------------------------------
-// Small-M router + plan as one thread-block cluster of C CTAs (C = 16, or 8
-// where 16 cannot be scheduled).  CTA r owns rows [r H / C, (r + 1) H / C) of
-// W_r: the rows arrive by bulk copies into padded shared-memory rows (a ring
-// of 32-row tiles) and meet the staged token rows in mma.sync (FP32
-// accumulate), giving partial logits for all experts.  After a cluster
-// barrier CTA r sums expert slice r over the C partials in a fixed order
-// through distributed shared memory (+ bias) into CTA 0; after a second
-// barrier CTA 0 runs top-k, the weights, the gate and the whole plan.
+// Small-M router + plan as one thread-block cluster of C CTAs (C <= 16).  CTA
+// r owns the expert slice [r Es, (r + 1) Es) (Es a multiple of 16) and
+// computes those experts' complete logits: each of its 8 warps takes one
+// eighth of K, loads its W_r tiles ([K rows][Es experts], swizzled) with 2-D
+// tensor-map copies and multiplies them with the staged token rows on
+// mma.sync (FP32 accumulate); the 8 partial sums are added in warp order.
+// The CTA's own top-k candidates per token then go to CTA 0 through
+// distributed shared memory, and CTA 0 merges them (the global top-k is the
+// top-k of the slices' top-k), computes the weights and the gate and builds
+// the whole plan.
 // ---------------------------------------------------------------------------
-constexpr int kRcTileRows = 32;
-constexpr int kRcMaxStages = 4;
 constexpr int kRcThreads = 256;
-constexpr int kRcMaxClusterCtas = 16;
+constexpr int kRcWarps = kRcThreads / 32;
+constexpr int kRcTileBytes = 8192;  // W_r bytes per tensor-map load (at most)
+constexpr size_t kRcSmemBudget = 200 * 1024;  // dynamic; the plan builder adds ~15 KB static
 
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-__device__ __forceinline__ uint32_t cluster_nctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
   return r;
 }
 __device__ __forceinline__ void cluster_sync_all() {
@@ -766,106 +763,102 @@ __device__ __forceinline__ uint32_t dsmem_addr(const void* p, uint32_t rank) {
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
   return r;
 }
-__device__ __forceinline__ float ld_dsmem_f32(uint32_t a) {
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(a) : "memory");
-  return v;
-}
-__device__ __forceinline__ void st_dsmem_f32(uint32_t a, float v) {
-  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(a), "f"(v) : "memory");
+__device__ __forceinline__ void st_dsmem_u32x2(uint32_t a, uint32_t v0, uint32_t v1) {
+  asm volatile("st.shared::cluster.v2.u32 [%0], {%1, %2};" ::"r"(a), "r"(v0), "r"(v1) : "memory");
 }
 
-struct RouterClusterSmem {
-  int stages;
-  size_t ring, xs, part, logits, gpart, total;
+// Shape of one cluster launch: experts per CTA, W_r tile rows, ring depth and
+// the shared-memory carve (all offsets 1024-byte aligned).
+struct RouterClusterPlan {
+  int C, Es, tr, ntw, stages;
+  size_t xs, ring, stage, lg, total;
 };
 
-__host__ __device__ inline RouterClusterSmem router_cluster_smem(int H, int E, int C) {
-  RouterClusterSmem s;
-  const size_t tile = (size_t)kRcTileRows * (E + 8) * 2;
-  const int R = H / C;
-  const int ntiles = (R + kRcTileRows - 1) / kRcTileRows;
-  s.xs = align_up((size_t)kDecodeMaxTokens * (R + 8) * 2, 128);
-  s.part = (size_t)kDecodeMaxTokens * E * 4;
-  s.logits = (size_t)kDecodeMaxTokens * E * 4;
-  s.gpart = 128;
-  const size_t fixed = s.xs + s.part + s.logits + s.gpart;
-  const size_t budget = 200 * 1024;
-  int st = (int)((budget > fixed ? budget - fixed : 0) / tile);
-  st = st > kRcMaxStages ? kRcMaxStages : st;
-  st = st > ntiles ? ntiles : st;
-  s.stages = st;
-  s.ring = (size_t)st * tile;
-  s.total = 128 + s.ring + fixed;
-  return s;
+__host__ __device__ inline RouterClusterPlan router_cluster_plan(int H, int E, int k, int M,
+                                                                 int cmax) {
+  RouterClusterPlan p;
+  p.Es = 16 * ((E + 16 * cmax - 1) / (16 * cmax));
+  p.C = (E + p.Es - 1) / p.Es;
+  // K rows per warp (a multiple of 32) in ntw tiles of tr rows (tr a multiple
+  // of 16 dividing per_warp, at most one tensor-map load of kRcTileBytes)
+  const int per_warp = H / kRcWarps;
+  const int tr_max = kRcTileBytes / (2 * p.Es);
+  int n = (per_warp + tr_max - 1) / tr_max;
+  while (per_warp % n != 0 || (per_warp / n) % 16 != 0) ++n;
+  p.tr = per_warp / n;
+  p.ntw = n;
+  // token rows (M x (H + 8) halves) and a 16-byte zero row; after the first
+  // cluster barrier CTA 0 reuses the region for the candidates (M x C x k)
+  const size_t xs = (size_t)M * (H + 8) * 2 + 16;
+  const size_t cand = (size_t)M * p.C * k * 8;
+  p.xs = align_up(xs > cand ? xs : cand, 1024);
+  p.lg = align_up((size_t)kDecodeMaxTokens * p.Es * 4, 1024);
+  // a stage also holds the warp's partial sums ([16][Es] FP32) at the end
+  const size_t tile = (size_t)p.tr * p.Es * 2, red = (size_t)kDecodeMaxTokens * p.Es * 4;
+  p.stage = align_up(tile > red ? tile : red, 1024);
+  const size_t fixed = 1024 + p.xs + p.lg;
+  int st = (int)((kRcSmemBudget > fixed ? kRcSmemBudget - fixed : 0) / (kRcWarps * p.stage));
+  if (st > 2) st = 2;
+  if (st > p.ntw) st = p.ntw;
+  p.stages = st;
+  p.ring = (size_t)kRcWarps * st * p.stage;
+  p.total = fixed + p.ring;
+  return p;
 }
 
 __global__ void __launch_bounds__(kRcThreads, 1)
     router_cluster_kernel(LayerDims d, int M, const __half* __restrict__ x,
-                          const __half* __restrict__ wr, const float* __restrict__ bias,
+                          const __grid_constant__ CUtensorMap wrmap, const float* __restrict__ bias,
                           const __half* __restrict__ wg, int32_t* ids_user, float* w_user,
-                          PlanView pv, uint32_t* status) {
-  extern __shared__ __align__(128) char rsm_raw[];
-  char* rsm = reinterpret_cast<char*>((reinterpret_cast<uintptr_t>(rsm_raw) + 127) &
-                                      ~uintptr_t(127));
-  __shared__ uint64_t full[kRcMaxStages];
+                          PlanView pv, uint32_t* status, int cmax) {
+  extern __shared__ __align__(1024) char rsm_raw[];
+  char* rsm = reinterpret_cast<char*>((reinterpret_cast<uintptr_t>(rsm_raw) + 1023) &
+                                      ~uintptr_t(1023));
+  __shared__ uint64_t full[kRcWarps][2];
   __shared__ int s_ids[kDecodeMaxTokens * 33];
   MOE_TL(kTlRouter);
-  const int E = d.E, H = d.H;
-  const uint32_t C = cluster_nctarank(), rank = cluster_ctarank();
-  const int R = H / (int)C, h0 = (int)rank * R;
-  const RouterClusterSmem L = router_cluster_smem(H, E, (int)C);
-  const int stages = L.stages;
-  const int ntiles = (R + kRcTileRows - 1) / kRcTileRows;
-  const int rstride = (E + 8) * 2;  // padded W_r row in shared memory, bytes
-  const size_t tile_b = (size_t)kRcTileRows * rstride;
-  char* ring = rsm;
-  __half* xs = reinterpret_cast<__half*>(rsm + L.ring);                 // [16][R + 8]
-  float* part = reinterpret_cast<float*>(rsm + L.ring + L.xs);          // [16][E]
-  float* logit = reinterpret_cast<float*>(rsm + L.ring + L.xs + L.part);  // [16][E] (CTA 0)
-  float* gpart = reinterpret_cast<float*>(rsm + L.ring + L.xs + L.part + L.logits);  // [16]
+  const int E = d.E, H = d.H, k = d.k;
+  const uint32_t rank = cluster_ctarank();
+  const RouterClusterPlan L = router_cluster_plan(H, E, k, M, cmax);
+  const int C = L.C, Es = L.Es, tr = L.tr, ntw = L.ntw, stages = L.stages;
+  const int rb = Es * 2;  // bytes of one W_r tile row
+  __half* xs = reinterpret_cast<__half*>(rsm);
+  const char* zero_row = rsm + (size_t)M * (H + 8) * 2;
+  float* lg = reinterpret_cast<float*>(rsm + L.xs);  // [16][Es] logits of the slice
+  char* ring = rsm + L.xs + L.lg;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, t4 = lane & 3;
+  char* my_ring = ring + (size_t)warp * stages * L.stage;
+  const int kw0 = warp * (H / kRcWarps);  // this warp's first K row
 
   if (tid == 0) {
-    for (int i = 0; i < stages; ++i) mbar_init(&full[i], 1);
+    for (int w = 0; w < kRcWarps; ++w) {
+      mbar_init(&full[w][0], 1);
+      mbar_init(&full[w][1], 1);
+    }
     fence_mbar_init();
   }
   __syncthreads();
-  // tile t: rows [h0 + 32 t, +32) of W_r, one bulk copy per row (lane = row)
-  auto issue = [&](int t) {
-    const int s = t % stages;
-    const int r0 = t * kRcTileRows;
-    const int nr = min(kRcTileRows, R - r0);
-    if (lane == 0) mbar_expect_tx(&full[s], (uint32_t)(nr * E * 2));
-    __syncwarp();
-    if (lane < nr)
-      bulk_g2s(ring + s * tile_b + (size_t)lane * rstride, wr + (int64_t)(h0 + r0 + lane) * E,
-               (uint32_t)(E * 2), &full[s]);
-  };
-  if (warp == 0)
-    for (int t = 0; t < stages && t < ntiles; ++t) issue(t);
-  // token rows of the chunk (rows >= M are zero) and the gate's partial dot
-  for (int i = tid; i < kDecodeMaxTokens * R; i += kRcThreads) {
-    const int m = i / R, k = i - m * R;
-    xs[m * (R + 8) + k] = (m < M) ? x[(int64_t)m * H + h0 + k] : __float2half(0.f);
-  }
-  if (d.shared)
-    for (int m = warp; m < M; m += kRcThreads / 32) {
-      float z = 0.f;
-      for (int k = lane; k < R; k += 32)
-        z = fmaf(__half2float(x[(int64_t)m * H + h0 + k]), __half2float(wg[h0 + k]), z);
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
-      if (lane == 0) gpart[m] = z;
+  if (lane == 0)
+    for (int i = 0; i < stages; ++i) {
+      mbar_expect_tx(&full[warp][i], (uint32_t)(tr * rb));
+      tma_load_2d(my_ring + i * L.stage, &wrmap, (int)rank * Es, kw0 + i * tr, &full[warp][i]);
     }
+  // token rows and the zero row (rows >= M of the MMA read it)
+  {
+    const int rv = H / 8;  // 16-byte vectors per row
+    for (int i = tid; i < M * rv; i += kRcThreads) {
+      const int m = i / rv, c = i - m * rv;
+      reinterpret_cast<uint4*>(xs + (size_t)m * (H + 8))[c] =
+          __ldg(reinterpret_cast<const uint4*>(x + (size_t)m * H) + c);
+    }
+    if (tid == 0) *reinterpret_cast<uint4*>(const_cast<char*>(zero_row)) = make_uint4(0, 0, 0, 0);
+  }
   __syncthreads();
 
-  // ---- partial logits: [16 tokens] x [E experts] over this CTA's rows ----
-  // warp w takes expert pairs j = w, w + 8, ... (16 experts each; the padded
-  // columns E .. E + 7 of a final half pair are computed and ignored)
-  const int npairs = (E + 15) / 16;
-  constexpr int kMaxPairs = 4;  // E <= 512
+  // ---- this warp's K rows: [16 tokens] x [Es experts] ----
+  constexpr int kMaxPairs = 4;  // Es <= 64
+  const int npairs = Es / 16;
   float acc[kMaxPairs][2][4];
 #pragma unroll
   for (int j = 0; j < kMaxPairs; ++j)
@@ -873,134 +866,182 @@ __global__ void __launch_bounds__(kRcThreads, 1)
     for (int t = 0; t < 2; ++t)
 #pragma unroll
       for (int c = 0; c < 4; ++c) acc[j][t][c] = 0.f;
+  const int arow = (lane & 7) + 8 * ((lane >> 3) & 1);
+  const char* arow_p =
+      arow < M ? reinterpret_cast<const char*>(xs + (size_t)arow * (H + 8)) : nullptr;
+  int it = 0;
   bool ok = true;
-  int t = 0;
-  for (; t < ntiles; ++t) {
-    const int s = t % stages;
-    const bool got = mbar_wait(&full[s], (t / stages) & 1, status);
-    if (__syncthreads_and(got ? 1 : 0) == 0) {
-      ok = false;
-      break;
-    }
-    const char* tb = ring + s * tile_b;
-    const int r0 = t * kRcTileRows;
-    const int nr = min(kRcTileRows, R - r0);
-    for (int k0 = 0; k0 < nr; k0 += 16) {
+  for (; it < ntw && ok; ++it) {
+    const int st = it % stages;
+    ok = mbar_wait(&full[warp][st], (it / stages) & 1, status);
+    if (!ok) break;
+    const char* tb = my_ring + st * L.stage;
+    for (int k0 = 0; k0 < tr; k0 += 16) {
       uint32_t a[4];
       {
-        const int row = (lane & 7) + 8 * ((lane >> 3) & 1);
-        const int col = r0 + k0 + 8 * (lane >> 4);
-        ldsm_x4(a, xs + row * (R + 8) + col);
+        const int col = kw0 + it * tr + k0 + 8 * (lane >> 4);
+        ldsm_x4(a, arow_p ? arow_p + (size_t)col * 2 : zero_row);
       }
+      const int krow = k0 + arow;
+      const int swz = ((krow * rb) >> 7) & (rb / 16 - 1);
 #pragma unroll
       for (int j = 0; j < kMaxPairs; ++j) {
-        const int pj = warp + 8 * j;
-        if (pj < npairs) {
+        if (j < npairs) {
           uint32_t b[4];
-          const int krow = k0 + (lane & 7) + 8 * ((lane >> 3) & 1);
-          const int ncol = pj * 16 + 8 * (lane >> 4);
-          ldsm_x4_t(b, tb + (size_t)krow * rstride + ncol * 2);
+          const int cn = 2 * j + (lane >> 4);
+          ldsm_x4_t(b, tb + (size_t)krow * rb + ((cn ^ swz) << 4));
           mma_16816(acc[j][0], a, b[0], b[1]);
           mma_16816(acc[j][1], a, b[2], b[3]);
         }
       }
     }
-    __syncthreads();  // every warp is done with stage s
-    if (warp == 0 && t + stages < ntiles) issue(t + stages);
+    __syncwarp();  // every lane is done with the stage
+    if (lane == 0 && it + stages < ntw) {
+      mbar_expect_tx(&full[warp][st], (uint32_t)(tr * rb));
+      tma_load_2d(my_ring + st * L.stage, &wrmap, (int)rank * Es, kw0 + (it + stages) * tr,
+                  &full[warp][st]);
+    }
   }
-  if (!ok && tid == 0) {
-    // a copy timed out: let the copies already issued land before leaving
-    // (each wait bounded by the same limit)
-    for (int tt = t; tt < ntiles && tt < t + stages; ++tt)
-      mbar_wait(&full[tt % stages], (tt / stages) & 1, status);
+  if (!ok && lane == 0) {
+    // a copy timed out: let the copies already issued land before the ring is
+    // reused (each wait bounded by the same limit)
+    for (int jt = it; jt < ntw && jt < it + stages; ++jt)
+      mbar_wait(&full[warp][jt % stages], (jt / stages) & 1, status);
   }
-  // c0: (token g, expert 2t4), c1: (g, 2t4+1), c2: (g+8, 2t4), c3: (g+8, 2t4+1)
+  __syncwarp();
+  // this warp's partial sums into its own (now idle) first ring stage:
+  // c0 (token g, expert 2 t4), c1 (g, 2 t4 + 1), c2 (g + 8, 2 t4), c3 (g + 8, 2 t4 + 1)
+  float* red = reinterpret_cast<float*>(my_ring);
 #pragma unroll
-  for (int j = 0; j < kMaxPairs; ++j) {
-    const int pj = warp + 8 * j;
-    if (pj < npairs)
+  for (int j = 0; j < kMaxPairs; ++j)
+    if (j < npairs)
 #pragma unroll
       for (int t = 0; t < 2; ++t)
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-          const int e = pj * 16 + t * 8 + 2 * t4 + (c & 1);
+          const int e = j * 16 + t * 8 + 2 * t4 + (c & 1);
           const int m = g + ((c & 2) ? 8 : 0);
-          if (e < E) part[m * E + e] = acc[j][t][c];
+          red[m * Es + e] = acc[j][t][c];
         }
-  }
   if (tid == 0) MOE_TL_MAX(20);
-  cluster_sync_all();  // every CTA's partial logits are complete
-  if (tid == 0) MOE_TL_MIN(21);
-
-  // ---- expert slice `rank`: fixed-order sum over the C partials, into CTA 0 ----
-  const int es = (E + (int)C - 1) / (int)C;
-  const int e0 = (int)rank * es;
-  for (int i = tid; i < M * es; i += kRcThreads) {
-    const int m = i / es, e = e0 + (i - m * es);
-    if (e >= E) continue;
-    float v[kRcMaxClusterCtas];
-#pragma unroll
-    for (int c = 0; c < kRcMaxClusterCtas; ++c)
-      if (c < (int)C) v[c] = ld_dsmem_f32(dsmem_addr(part + m * E + e, c));
+  __syncthreads();
+  // ---- logits of the slice: the 8 warps' partials in warp order (+ bias) ----
+  for (int i = tid; i < M * Es; i += kRcThreads) {
+    const int m = i / Es, e = i - m * Es;
     float sum = 0.f;
 #pragma unroll
-    for (int c = 0; c < kRcMaxClusterCtas; ++c)
-      if (c < (int)C) sum += v[c];
-    if (bias) sum += bias[e];
-    st_dsmem_f32(dsmem_addr(logit + m * E + e, 0), sum);
+    for (int w = 0; w < kRcWarps; ++w)
+      sum += reinterpret_cast<const float*>(ring + (size_t)w * stages * L.stage)[m * Es + e];
+    const int ge = (int)rank * Es + e;
+    if (bias && ge < E) sum += bias[ge];
+    lg[m * Es + e] = sum;
   }
-  float gamma = 0.f;
-  if (rank == 0 && d.shared && tid < M) {
-    float z = 0.f;
-    for (int c = 0; c < (int)C; ++c) z += ld_dsmem_f32(dsmem_addr(gpart + tid, c));
-    gamma = 1.f / (1.f + expf(-z));
+  __syncthreads();
+  // ---- the slice's top-k per token (lane j < k holds the j-th), as keys ----
+  uint32_t ckey[2] = {0u, 0u};
+  int cid[2] = {-1, -1};
+#pragma unroll
+  for (int mm = 0; mm < 2; ++mm) {
+    const int m = warp + kRcWarps * mm;
+    if (m >= M) continue;
+    uint32_t v[2];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const int e = lane + 32 * i, ge = (int)rank * Es + e;
+      v[i] = (e < Es && ge < E) ? f2key(lg[m * Es + e]) : 0u;
+    }
+    for (int j = 0; j < k; ++j) {
+      const uint32_t gm = __reduce_max_sync(0xffffffffu, max(v[0], v[1]));
+      uint32_t li = 0xffffffffu;
+      if (v[1] == gm) li = (uint32_t)(lane + 32);
+      if (v[0] == gm) li = (uint32_t)lane;
+      const uint32_t gi = __reduce_min_sync(0xffffffffu, li);
+      if ((uint32_t)lane == gi) v[0] = 0u;
+      if ((uint32_t)(lane + 32) == gi) v[1] = 0u;
+      if (lane == j) {
+        ckey[mm] = gm;
+        cid[mm] = (int)rank * Es + (int)gi;
+      }
+    }
   }
-  cluster_sync_all();  // CTA 0 holds every logit; no CTA reads another's memory after this
+  if (tid == 0) MOE_TL_MIN(21);
+  cluster_sync_all();  // CTA 0 no longer reads its token rows: they become the candidates
+  // ---- candidates into CTA 0: cand[(m C + rank) k + j] = (key, id) ----
+#pragma unroll
+  for (int mm = 0; mm < 2; ++mm) {
+    const int m = warp + kRcWarps * mm;
+    if (m < M && lane < k)
+      st_dsmem_u32x2(dsmem_addr(rsm + (((size_t)m * C + rank) * k + lane) * 8, 0), ckey[mm],
+                     (uint32_t)cid[mm]);
+  }
+  cluster_sync_all();  // every candidate is in CTA 0
   if (tid == 0) MOE_TL_MIN(23);
   if (rank != 0) return;
-  if (d.shared && tid < M) gpart[tid] = gamma;  // CTA 0's own copy: gate values now
-  __syncthreads();
   if (tid == 0) MOE_TL_MAX(24);
 
-  // ---- top-k, weights, plan (CTA 0) ----
-  for (int m = warp; m < M; m += kRcThreads / 32) {
-    int id;
-    float l;
-    warp_topk<false>(logit + m * E, E, d.k, &id, &l);
-    const float w = warp_topk_weight(l, d.k);
-    store_route(d, m, id, w, d.shared ? gpart[m] : 0.f, ids_user, w_user, pv);
-    if (lane < d.k) s_ids[m * d.k_eff + lane] = id;
-    if (d.shared && lane == 0) s_ids[m * d.k_eff + d.k] = d.E;
+  // ---- merge, weights, gate, plan (CTA 0) ----
+  const uint2* cand = reinterpret_cast<const uint2*>(rsm);
+  const int nc = C * k;
+  for (int m = warp; m < M; m += kRcWarps) {
+    uint32_t v[16];
+    int ids[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const int q = lane + 32 * i;
+      const uint2 c = q < nc ? cand[(size_t)m * nc + q] : make_uint2(0u, 0u);
+      v[i] = c.x;
+      ids[i] = q < nc ? (int)c.y : 0x7fffffff;
+    }
+    int my_id = -1;
+    float my_l = -INFINITY;
+    for (int j = 0; j < k; ++j) {
+      uint32_t lm = 0u;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) lm = max(lm, v[i]);
+      const uint32_t gm = __reduce_max_sync(0xffffffffu, lm);
+      int li = 0x7fffffff;
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+        if (v[i] == gm && ids[i] < li) li = ids[i];
+      const int gi = (int)__reduce_min_sync(0xffffffffu, (uint32_t)li);
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+        if (ids[i] == gi) v[i] = 0u;
+      if (lane == j) {
+        my_id = gi;
+        my_l = key2f(gm);
+      }
+    }
+    const float w = warp_topk_weight(my_l, k);
+    const float gamma = d.shared ? warp_gate(x + (size_t)m * H, wg, H) : 0.f;
+    store_route(d, m, my_id, w, gamma, ids_user, w_user, pv);
+    if (lane < k) s_ids[m * d.k_eff + lane] = my_id;
+    if (d.shared && lane == 0) s_ids[m * d.k_eff + k] = d.E;
   }
   __syncthreads();
   plan_small_block(d, M, s_ids, pv, status);
   if (tid == 0) MOE_TL_MIN(25);
 }
 
-// Cluster size for the small-M router: 16 CTAs where the device can co-schedule
-// such a cluster with this kernel's shared memory, else 8, else 0 (the
-// 128-block router is used).  Decided once per process and shape class.
-static int router_cluster_size(const LayerDims& d) {
-  static int cached[2] = {-1, -1};  // [E > 256]
-  int& c = cached[d.E > 256 ? 1 : 0];
+// Largest cluster (16, else 8, else 0: the 128-block router is used) that the
+// device can co-schedule with this kernel at its largest shared-memory use.
+// Decided once per process.
+static int router_cluster_max() {
+  static int c = -1;
   if (c >= 0) return c;
   c = 0;
   if (cudaFuncSetAttribute(router_cluster_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed,
                            1) != cudaSuccess ||
       cudaFuncSetAttribute(router_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           200 * 1024 + 128) !=
-          cudaSuccess) {
+                           (int)kRcSmemBudget) != cudaSuccess) {
     cudaGetLastError();
     return c;
   }
   for (int cand : {16, 8}) {
-    if (d.H % (cand * 16) != 0) continue;
-    const RouterClusterSmem L = router_cluster_smem(d.H, d.E, cand);
-    if (L.stages < 1) continue;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(cand);
     cfg.blockDim = dim3(kRcThreads);
-    cfg.dynamicSmemBytes = L.total;
+    cfg.dynamicSmemBytes = kRcSmemBudget;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = cand;
@@ -1030,22 +1071,27 @@ cudaError_t launch_plan(const LayerDims& d, int64_t M, const __half* x, const __
       route_given_kernel<<<(Mi + 7) / 8, 256, 0, stream>>>(d, Mi, x, w_gate, ids_user, w_user, pv);
       plan_small_kernel<<<1, 256, 0, stream>>>(d, Mi, pv, status);
     } else {
-      const int C = router_cluster_size(d);
-      if (C > 0) {
+      const int cmax = router_cluster_max();
+      const RouterClusterPlan L = router_cluster_plan(d.H, d.E, d.k, Mi, cmax > 0 ? cmax : 1);
+      if (cmax > 0 && L.stages >= 1 && L.total <= kRcSmemBudget) {
+        CUtensorMap wrmap;
+        cudaError_t e = make_fp16_map_swz(&wrmap, w_router, (uint64_t)d.E, (uint64_t)d.H,
+                                          (uint32_t)L.Es, (uint32_t)L.tr, L.Es * 2);
+        if (e != cudaSuccess) return e;
         cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(C);
+        cfg.gridDim = dim3(L.C);
         cfg.blockDim = dim3(kRcThreads);
-        cfg.dynamicSmemBytes = router_cluster_smem(d.H, d.E, C).total;
+        cfg.dynamicSmemBytes = L.total;
         cfg.stream = stream;
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = C;
+        attr[0].val.clusterDim.x = L.C;
         attr[0].val.clusterDim.y = 1;
         attr[0].val.clusterDim.z = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        return cudaLaunchKernelEx(&cfg, router_cluster_kernel, d, Mi, x, w_router, bias, w_gate,
-                                  ids_user, w_user, pv, status);
+        return cudaLaunchKernelEx(&cfg, router_cluster_kernel, d, Mi, x, wrmap, bias, w_gate,
+                                  ids_user, w_user, pv, status, cmax);
       }
       dim3 grid((d.E + 63) / 64, d.H / kRsRows);
       router_small_kernel<<<grid, 256, 0, stream>>>(d, Mi, x, w_router, bias, w_gate, ids_user,

@@ -77,4 +77,30 @@ cudaError_t make_fp16_map(CUtensorMap* map, const void* base, uint64_t cols, uin
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+cudaError_t make_fp16_map_swz(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows,
+                              uint32_t box_cols, uint32_t box_rows, int swizzle_bytes) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return cudaErrorNotSupported;
+  CUtensorMapSwizzle sw;
+  switch (swizzle_bytes) {
+    case 0: sw = CU_TENSOR_MAP_SWIZZLE_NONE; break;
+    case 32: sw = CU_TENSOR_MAP_SWIZZLE_32B; break;
+    case 64: sw = CU_TENSOR_MAP_SWIZZLE_64B; break;
+    case 128: sw = CU_TENSOR_MAP_SWIZZLE_128B; break;
+    default: return cudaErrorInvalidValue;
+  }
+  if ((reinterpret_cast<uintptr_t>(base) & 15u) || ((cols * 2) & 15u) || box_cols > 256 ||
+      box_rows > 256 || box_rows == 0 || ((box_cols * 2) & 15u) ||
+      (swizzle_bytes && box_cols * 2 != (uint32_t)swizzle_bytes))
+    return cudaErrorInvalidValue;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * 2};
+  const cuuint32_t box[2] = {box_cols, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 }  // namespace moe
