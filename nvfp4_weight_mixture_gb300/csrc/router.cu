@@ -980,35 +980,25 @@ __global__ void __launch_bounds__(kRcThreads, 1)
   if (tid == 0) MOE_TL_MAX(24);
 
   // ---- merge, weights, gate, plan (CTA 0) ----
+  // Each slice's candidates are in descending order (ties: lower id first),
+  // so the merge keeps one head per slice (lane c < C) and, k times, takes
+  // the largest head (ties: the lower id) and advances that slice.
   const uint2* cand = reinterpret_cast<const uint2*>(rsm);
-  const int nc = C * k;
   for (int m = warp; m < M; m += kRcWarps) {
-    uint32_t v[16];
-    int ids[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const int q = lane + 32 * i;
-      const uint2 c = q < nc ? cand[(size_t)m * nc + q] : make_uint2(0u, 0u);
-      v[i] = c.x;
-      ids[i] = q < nc ? (int)c.y : 0x7fffffff;
-    }
+    const uint2* lst = cand + ((size_t)m * C + lane) * k;
+    int ptr = 0;
+    uint2 head = lane < C ? lst[0] : make_uint2(0u, 0x7fffffffu);
     int my_id = -1;
     float my_l = -INFINITY;
     for (int j = 0; j < k; ++j) {
-      uint32_t lm = 0u;
-#pragma unroll
-      for (int i = 0; i < 16; ++i) lm = max(lm, v[i]);
-      const uint32_t gm = __reduce_max_sync(0xffffffffu, lm);
-      int li = 0x7fffffff;
-#pragma unroll
-      for (int i = 0; i < 16; ++i)
-        if (v[i] == gm && ids[i] < li) li = ids[i];
-      const int gi = (int)__reduce_min_sync(0xffffffffu, (uint32_t)li);
-#pragma unroll
-      for (int i = 0; i < 16; ++i)
-        if (ids[i] == gi) v[i] = 0u;
+      const uint32_t gm = __reduce_max_sync(0xffffffffu, head.x);
+      const uint32_t gi = __reduce_min_sync(0xffffffffu, head.x == gm ? head.y : 0x7fffffffu);
+      if (lane < C && head.x == gm && head.y == gi) {
+        ++ptr;
+        head = ptr < k ? lst[ptr] : make_uint2(0u, 0x7fffffffu);
+      }
       if (lane == j) {
-        my_id = gi;
+        my_id = (int)gi;
         my_l = key2f(gm);
       }
     }
