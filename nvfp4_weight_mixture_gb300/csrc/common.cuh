@@ -14,6 +14,7 @@ namespace moe {
 constexpr int kDecodeMaxTokens = 16;     // M <= this runs the streaming GEMV path
 constexpr int kTileRows = 192;           // plan tile height (N of the grouped MMAs)
 constexpr int kPlanChunk = 4096;         // pairs per histogram block in the plan
+constexpr int kRouterChunk = 8192;       // tokens per large-M router logits pass
 constexpr uint64_t kWaitTimeoutNs = 200ull * 1000 * 1000;  // bounded spins: 200 ms
 // The same bound in SM clock cycles, for spins that time themselves with the
 // SM-local cycle counter (cheap to read): 200 ms at 2 GHz, longer if slower.
@@ -55,6 +56,8 @@ struct PlanView {
   uint32_t* tickets;  // [64] self-resetting arrival counters: [0, 8) router slices,
                       // [48, 51) decode forward grid barriers, 63 router finaliser
   int32_t* dtab;      // [kDecodeMaxTokens * 33][kDtabInts] decode work table (M <= 16)
+  float* rlogits;     // [min(M, kRouterChunk)][n_experts] router logits (M > 16)
+  __half* wrt;        // [n_experts][hidden] transposed router weight (M > 16)
 };
 
 __host__ __device__ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
@@ -93,6 +96,9 @@ __host__ __device__ inline size_t plan_layout(char* base, int64_t M, int k_eff, 
   t.partial = (float*)take(sizeof(float) * (size_t)n_hchunks * kDecodeMaxTokens * n_experts);
   t.logits = (float*)take(sizeof(float) * (size_t)kDecodeMaxTokens * n_experts);
   t.dtab = (int32_t*)take(sizeof(int32_t) * kDtabEntries * kDtabInts);
+  const int64_t Mr = M > kDecodeMaxTokens ? (M < kRouterChunk ? M : kRouterChunk) : 0;
+  t.rlogits = (float*)take(sizeof(float) * (size_t)Mr * n_experts);
+  t.wrt = (__half*)take(Mr > 0 ? sizeof(__half) * (size_t)n_experts * hidden : 0);
   if (v) *v = t;
   return off;
 }

@@ -732,6 +732,192 @@ __global__ void plan_scatter_kernel(LayerDims d, int64_t P, PlanView pv) {
 }
 
 // ---------------------------------------------------------------------------
+// Large-M router on the 5th-generation tensor cores.  The logits are a plain
+// FP16 GEMM, D[token][expert] = sum_h x[token][h] W_r[h][expert], with both
+// operands K-major: W_r is transposed once per call into the plan buffer.
+// One CTA computes 128 tokens x 256 experts: a producer thread loads the
+// K steps (64 along H) of both operands by 128-byte-swizzled tensor maps into
+// a 4-stage ring, one thread issues tcgen05.mma (M 128, N <= 256, FP32
+// accumulator in tensor memory), and four warps move the accumulator (+ bias)
+// to the logits rows.  A second kernel, one warp per token over all SMs,
+// takes the top-k, the weights and the gate from the logits (resident in L2).
+// ---------------------------------------------------------------------------
+constexpr int kRlTokens = 128;      // tokens (MMA M) per CTA
+constexpr int kRlExperts = 256;     // experts (MMA N) per CTA
+constexpr int kRlStages = 4;
+constexpr int kRlXBytes = kRlTokens * 128;   // one K step of the token rows
+constexpr int kRlWBytes = kRlExperts * 128;  // one K step of the expert rows
+constexpr size_t kRlSmem = 1024 + (size_t)kRlStages * (kRlXBytes + kRlWBytes);
+
+// W_r [H][E] -> W_r^T [E][H] through 32 x 32 shared-memory tiles.
+__global__ void __launch_bounds__(256) transpose_wr_kernel(const __half* __restrict__ wr, int H,
+                                                           int E, __half* __restrict__ wrt) {
+  __shared__ __half tile[32][34];
+  const int e0 = blockIdx.x * 32, h0 = blockIdx.y * 32;
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+  for (int i = ty; i < 32; i += 8) {
+    const int e = e0 + tx;
+    tile[i][tx] = e < E ? wr[(size_t)(h0 + i) * E + e] : __float2half(0.f);
+  }
+  __syncthreads();
+  for (int i = ty; i < 32; i += 8) {
+    const int e = e0 + i;
+    if (e < E) wrt[(size_t)e * H + h0 + tx] = tile[tx][i];
+  }
+}
+
+__global__ void __launch_bounds__(256, 1)
+    router_logits_kernel(LayerDims d, int M0, int Mc, const __grid_constant__ CUtensorMap xmap,
+                         const __grid_constant__ CUtensorMap wmap, const float* __restrict__ bias,
+                         float* __restrict__ logits, uint32_t* status) {
+  extern __shared__ __align__(1024) char rl_raw[];
+  char* base = reinterpret_cast<char*>((reinterpret_cast<uintptr_t>(rl_raw) + 1023) &
+                                       ~uintptr_t(1023));
+  __shared__ uint64_t full[kRlStages], empty[kRlStages], accf;
+  __shared__ uint32_t tmem_slot;
+  MOE_TL(kTlRouter);
+  const int E = d.E, H = d.H, S = H / 64;
+  const int m0 = blockIdx.x * kRlTokens, e0 = blockIdx.y * kRlExperts;
+  const int ne = min(kRlExperts, E - e0);           // experts of this CTA (a multiple of 16)
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  char* xs = base;
+  char* ws = base + kRlStages * kRlXBytes;
+  if (tid == 0) {
+    for (int i = 0; i < kRlStages; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    mbar_init(&accf, 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) tmem_alloc(&tmem_slot, kRlExperts);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+  if (warp == 0) {
+    // ---- producer: both operands of each K step into the ring ----
+    if (lane == 0) {
+      int ks = 0;
+      for (; ks < S; ++ks) {
+        const int st = ks % kRlStages;
+        if (!mbar_wait(&empty[st], ((ks / kRlStages) & 1) ^ 1, status)) break;
+        mbar_expect_tx(&full[st], kRlXBytes + kRlWBytes);
+        tma_load_2d(xs + st * kRlXBytes, &xmap, ks * 64, M0 + m0, &full[st]);
+        tma_load_2d(ws + st * kRlWBytes, &wmap, ks * 64, e0, &full[st]);
+      }
+      // the copies of the last stages land before the CTA may leave
+      for (int k = ks > kRlStages ? ks - kRlStages : 0; k < ks; ++k)
+        mbar_wait(&full[k % kRlStages], (k / kRlStages) & 1, status);
+    }
+  } else if (warp == 1) {
+    // ---- MMA issuer: per K step one wait, 4 MMAs of K 16, one commit ----
+    if (lane == 0) {
+      const uint32_t idesc = idesc_f16_f32(kRlTokens, ne);
+      for (int ks = 0; ks < S; ++ks) {
+        const int st = ks % kRlStages;
+        if (!mbar_wait(&full[st], (ks / kRlStages) & 1, status)) break;
+        tc_fence_after();
+        const uint64_t dx = sdesc_sw128(smem_u32(xs + st * kRlXBytes));
+        const uint64_t dw = sdesc_sw128(smem_u32(ws + st * kRlWBytes));
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          tc_mma_f16(tmem, dx + 2 * kk, dw + 2 * kk, idesc, (ks | kk) ? 1u : 0u);
+        tc_commit(&empty[st]);
+      }
+      tc_commit(&accf);  // also after an abort: every MMA issued completes first
+    }
+  } else if (warp >= 4) {
+    // ---- epilogue: lane r of warp q holds token 32 q + r of the tile ----
+    const int q = warp & 3;
+    if (mbar_wait(&accf, 0, status)) {
+      tc_fence_after();
+      const int t = m0 + q * 32 + lane;  // token within the chunk
+      float* row = logits + (size_t)t * E + e0;
+      for (int c0 = 0; c0 < ne; c0 += 32) {
+        uint32_t v[32];
+        tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + c0, v);
+        if (t < Mc) {
+#pragma unroll
+          for (int j4 = 0; j4 < 8; ++j4) {
+            const int e = c0 + 4 * j4;
+            if (e < ne) {
+              float4 o;
+              o.x = __uint_as_float(v[4 * j4 + 0]) + (bias ? bias[e0 + e + 0] : 0.f);
+              o.y = __uint_as_float(v[4 * j4 + 1]) + (bias ? bias[e0 + e + 1] : 0.f);
+              o.z = __uint_as_float(v[4 * j4 + 2]) + (bias ? bias[e0 + e + 2] : 0.f);
+              o.w = __uint_as_float(v[4 * j4 + 3]) + (bias ? bias[e0 + e + 3] : 0.f);
+              *reinterpret_cast<float4*>(row + e) = o;
+            }
+          }
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kRlExperts);
+  }
+}
+
+// One warp per token of the chunk: top-k of the logits row, renormalised
+// weights, the shared expert's gate, the route.
+__global__ void __launch_bounds__(256) router_topk_kernel(LayerDims d, int M0, int Mc,
+                                                          const float* __restrict__ logits,
+                                                          const __half* __restrict__ x,
+                                                          const __half* __restrict__ wg,
+                                                          int32_t* ids_user, float* w_user,
+                                                          PlanView pv) {
+  MOE_TL(kTlPlan);
+  const int r = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (r >= Mc) return;
+  const int t = M0 + r;
+  int id;
+  float l;
+  warp_topk<true>(logits + (size_t)r * d.E, d.E, d.k, &id, &l);
+  const float w = warp_topk_weight(l, d.k);
+  const float gamma = d.shared ? warp_gate(x + (int64_t)t * d.H, wg, d.H) : 0.f;
+  store_route(d, t, id, w, gamma, ids_user, w_user, pv);
+}
+
+// The tensor-core router covers E >= 256 (a multiple of 16) and M >= 128.
+static bool router_tc_ok(const LayerDims& d, int64_t M) {
+  return d.E >= kRlExperts && d.E % 16 == 0 && M >= kRlTokens;
+}
+
+static cudaError_t launch_router_tc(const LayerDims& d, int64_t M, const __half* x,
+                                    const __half* w_router, const float* bias,
+                                    const __half* w_gate, int32_t* ids_user, float* w_user,
+                                    const PlanView& pv, uint32_t* status, cudaStream_t stream) {
+  static bool attr_done = false;
+  if (!attr_done) {
+    cudaError_t e = cudaFuncSetAttribute(router_logits_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kRlSmem);
+    if (e != cudaSuccess) return e;
+    attr_done = true;
+  }
+  transpose_wr_kernel<<<dim3((d.E + 31) / 32, d.H / 32), 256, 0, stream>>>(w_router, d.H, d.E,
+                                                                             pv.wrt);
+  CUtensorMap xmap, wmap;
+  cudaError_t e = make_fp16_map(&xmap, x, (uint64_t)d.H, (uint64_t)M, 64, kRlTokens, true);
+  if (e != cudaSuccess) return e;
+  e = make_fp16_map(&wmap, pv.wrt, (uint64_t)d.H, (uint64_t)d.E, 64, kRlExperts, true);
+  if (e != cudaSuccess) return e;
+  for (int64_t M0 = 0; M0 < M; M0 += kRouterChunk) {
+    const int Mc = (int)std::min<int64_t>(kRouterChunk, M - M0);
+    const dim3 grid((unsigned)((Mc + kRlTokens - 1) / kRlTokens),
+                    (unsigned)((d.E + kRlExperts - 1) / kRlExperts));
+    router_logits_kernel<<<grid, 256, kRlSmem, stream>>>(d, (int)M0, Mc, xmap, wmap, bias,
+                                                        pv.rlogits, status);
+    router_topk_kernel<<<(Mc + 7) / 8, 256, 0, stream>>>(d, (int)M0, Mc, pv.rlogits, x, w_gate,
+                                                         ids_user, w_user, pv);
+  }
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
 // Small-M router + plan as one thread-block cluster of C CTAs (C <= 16).  CTA
 // r owns the expert slice [r Es, (r + 1) Es) (Es a multiple of 16) and
 // computes those experts' complete logits: each of its 8 warps takes one
@@ -1091,6 +1277,10 @@ cudaError_t launch_plan(const LayerDims& d, int64_t M, const __half* x, const __
   }
   if (ids_given) {
     route_given_kernel<<<(Mi + 7) / 8, 256, 0, stream>>>(d, Mi, x, w_gate, ids_user, w_user, pv);
+  } else if (router_tc_ok(d, M)) {
+    cudaError_t e = launch_router_tc(d, M, x, w_router, bias, w_gate, ids_user, w_user, pv, status,
+                                     stream);
+    if (e != cudaSuccess) return e;
   } else {
     const size_t smem = router_mma_smem(d.E);
     static bool attr_done = false;
