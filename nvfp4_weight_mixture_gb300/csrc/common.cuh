@@ -13,7 +13,7 @@ namespace moe {
 
 constexpr int kDecodeMaxTokens = 16;     // M <= this runs the streaming GEMV path
 constexpr int kTileRows = 192;           // plan tile height (N of the grouped MMAs)
-constexpr int kPlanChunk = 4096;         // pairs per histogram block in the plan
+constexpr int kPlanChunk = 2048;         // pairs per histogram block in the plan
 constexpr int kRouterChunk = 8192;       // tokens per large-M router logits pass
 constexpr uint64_t kWaitTimeoutNs = 200ull * 1000 * 1000;  // bounded spins: 200 ms
 // The same bound in SM clock cycles, for spins that time themselves with the

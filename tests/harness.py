@@ -158,7 +158,7 @@ class Case:
 
 
 TILE_ROWS = 192
-PLAN_CHUNK = 4096
+PLAN_CHUNK = 2048
 DECODE_MAX_TOKENS = 16
 
 
