@@ -85,6 +85,58 @@ def test_router_full_prefill_sampled():
     _check_router(case, tok)
 
 
+class _RouteCase:
+    """Router-only case: seeded x, W_r, bias; no expert weights (route() needs none)."""
+
+    def __init__(self, wl):
+        self.wl = wl
+        self.x = synth.activations(wl)
+        self.wr = synth.router_weight(wl)
+        self.bias = synth.router_bias(wl)
+        dev = torch.device("cuda")
+        self.x_t = torch.from_numpy(self.x).to(dev)
+        self.layer = moe.MoELayer(
+            wl.H, wl.E, wl.k, wl.I, torch.from_numpy(self.wr).to(dev), None, None,
+            bias=None if self.bias is None else torch.from_numpy(self.bias).to(dev),
+            max_tokens=max(wl.M, 1))
+
+    def gpu_route(self):
+        ids, w = self.layer.route(self.x_t)
+        return ids.cpu().numpy(), w.cpu().numpy()
+
+    def oracle_route(self, tokens=None):
+        x = self.x if tokens is None else self.x[np.asarray(tokens)]
+        logits, ids, w = oracle.router(x, self.wr, self.bias, self.wl.k)
+        return logits, ids, w, None
+
+
+@pytest.mark.parametrize("M,H,E,k", [(300, 2048, 256, 8), (300, 1024, 384, 10),
+                                     (128, 512, 256, 4), (8300, 2048, 512, 10)])
+def test_router_tensor_core_shapes(M, H, E, k):
+    """The tcgen05 router (M >= 128, E >= 256): a partial last expert slice
+    (E 384), M exactly one token tile, and M above one 8192-token logits chunk
+    (sampled tokens from both chunks)."""
+    case = _RouteCase(synth.custom("rt", M, H, E, k, 128))
+    tok = None
+    if M > 1000:
+        rng = np.random.default_rng(11)
+        tok = np.sort(np.concatenate([rng.choice(8192, 128, replace=False),
+                                      8192 + rng.choice(M - 8192, 64, replace=False)]))
+    _check_router(case, tok)
+    assert int(case.layer.status.item()) == 0
+
+
+@pytest.mark.parametrize("M,H,E,k", [(3, 256, 24, 2), (16, 4096, 512, 10), (1, 1024, 512, 32),
+                                     (7, 768, 64, 6), (16, 2048, 512, 10)])
+def test_router_cluster_shapes(M, H, E, k):
+    """The small-M cluster router: a partial last expert slice (E 24), the
+    largest hidden size with 16 tokens (one ring stage), k = 32, K rows per
+    warp that are not a power of two (H 768)."""
+    case = _RouteCase(synth.custom("rc", M, H, E, k, 128))
+    _check_router(case)
+    assert int(case.layer.status.item()) == 0
+
+
 # ---- plan ------------------------------------------------------------------------------
 
 @pytest.mark.parametrize("wl,M", [(TINY, 8), (TINY, 16), (TINY, 500), (DEC16, 16),
