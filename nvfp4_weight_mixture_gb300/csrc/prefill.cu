@@ -540,6 +540,299 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 #endif
 }
 
+// ---------------------------------------------------------------------------
+// Grouped W2.  A unit is one plan tile times 128 output rows (one A tile), so
+// that tensor memory holds two accumulator buffers (2 x 192 columns) beside
+// four A stages (4 x 32 columns): the epilogue of unit u drains one buffer
+// while the MMAs of unit u + 1 fill the other.  20 warps:
+//   warps 0-7    dequantise one fragment block each per K step (warp w owns
+//                lanes 16 (2 (w % 4) + w / 4) .. + 15 of the A tile);
+//   warps 8-15   epilogue: warp 8 + q + 4 p reads lanes 32 q .. + 31 of the
+//                unit's buffer, the 32-column chunks of parity p;
+//   warp 16      tensor memory owner, one lane issues the MMAs;
+//   warp 17      raw NVFP4 bulk copies (8 fragment blocks per K step);
+//   warp 18      token rows (h) by 64-row tensor-map loads;
+//   warp 19      g2 x combine weight of each row, one unit ahead.
+// ---------------------------------------------------------------------------
+constexpr int kW2Threads = 20 * 32;
+constexpr int kW2AS = 4;          // A stages of one tile
+constexpr int kW2EpiWarp0 = 8;
+constexpr int kW2MmaWarp = 16;
+constexpr int kW2RawWarp = 17;
+constexpr int kW2BWarp = 18;
+constexpr int kW2ScaleWarp = 19;
+constexpr int kW2RawQ = 8 * 512;  // raw q bytes per K step (8 fragment blocks)
+constexpr int kW2RawS = 8 * 64;
+static_assert(kAOff + kW2AS * (kBK / 2) <= kTmemCols, "W2 tensor memory over-committed");
+static_assert(kBStages >= kW2AS, "the B ring serves the A stages' barriers");
+
+struct W2Smem {
+  uint64_t raw_full[kRS], raw_empty[kRS];
+  uint64_t full[kBStages], empty[kBStages];
+  // per accumulator buffer b: accf[b] completes when a unit's MMAs into b are
+  // done, tmem_empty[b] when its epilogue has read b, wsc_full[b] when the
+  // unit's scales are in wsc[b]
+  uint64_t accf[2], tmem_empty[2], wsc_full[2], drain;
+  __align__(16) float wsc[2][kTileRows];
+  uint32_t tmem;
+  int abort;
+  int n_units;
+  __align__(16) float stage[8][512];  // epilogue staging, [16 pairs][32 rows] per warp
+};
+
+constexpr size_t w2_smem_bytes() { return 1024 + (size_t)kOffMeta + sizeof(W2Smem); }
+static_assert(w2_smem_bytes() <= 232448, "grouped W2 shared memory above the sm_103 limit");
+
+__global__ void __launch_bounds__(kW2Threads, 1)
+    grouped_w2_kernel(LayerDims d, PlanView pv, const __grid_constant__ CUtensorMap bmap,
+                      Weights w, Weights ws, float* __restrict__ partial, uint32_t* status) {
+  extern __shared__ __align__(1024) char smem_raw[];
+  char* base = reinterpret_cast<char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                       ~uintptr_t(1023));
+  W2Smem* sm = reinterpret_cast<W2Smem*>(base + kOffMeta);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  MOE_TL(kTlW2);
+  const int S = d.I / kBK;     // K steps per unit
+  const int upt = d.H / 128;   // units per plan tile
+
+  if (tid == 0) {
+    for (int i = 0; i < kRS; ++i) {
+      mbar_init(&sm->raw_full[i], 1);
+      mbar_init(&sm->raw_empty[i], kDqWarps);
+    }
+    for (int i = 0; i < kBStages; ++i) {
+      mbar_init(&sm->full[i], kDqWarps + 1);
+      mbar_init(&sm->empty[i], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&sm->accf[b], 1);
+      mbar_init(&sm->tmem_empty[b], 8);
+      mbar_init(&sm->wsc_full[b], 1);
+    }
+    mbar_init(&sm->drain, 1);
+    sm->abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == kW2MmaWarp) tmem_alloc(&sm->tmem, kTmemCols);
+  pdl_wait();
+  MOE_TL_WAITED();
+  if (tid == 0) sm->n_units = __ldcg(&pv.hdr->n_tiles) * upt;
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm->tmem;
+  const int n_units = sm->n_units;
+  volatile int* abort = &sm->abort;
+
+  if (warp == kW2RawWarp) {
+    // ---- raw weights: the unit's 8 fragment blocks of each K step ----
+    if (lane == 0) {
+      uint32_t kr = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < n_units && ok && !*abort; u += gridDim.x) {
+        const Unit un = load_unit<false>(d, pv, w, ws, u, upt);
+        const int grp = un.sub >> 1, half = un.sub & 1;
+        for (int ks = 0; ks < S; ++ks, ++kr) {
+          const int slot = kr % kRS;
+          if (!wait_or_abort(&sm->raw_empty[slot], ((kr / kRS) & 1) ^ 1, status, abort)) {
+            ok = false;
+            break;
+          }
+          char* dst = base + kOffRaw + slot * kRawBytes;
+          mbar_expect_tx(&sm->raw_full[slot], kW2RawQ + kW2RawS);
+          const size_t blk = ((size_t)grp * S + ks) * 16 + 8 * half;
+          bulk_g2s(dst, un.q + blk * 512, kW2RawQ, &sm->raw_full[slot]);
+          bulk_g2s(dst + kRawQ, un.s + blk * 64, kW2RawS, &sm->raw_full[slot]);
+        }
+      }
+      for (uint32_t k = (kr > (uint32_t)kRS ? kr - kRS : 0); k < kr; ++k)
+        wait_or_abort(&sm->raw_full[k % kRS], (k / kRS) & 1, status, abort);
+    }
+  } else if (warp == kW2MmaWarp) {
+    // ---- MMAs: per K step one wait, 4 MMAs (K 16 each), one commit ----
+    if (lane == 0) {
+      uint32_t ka = 0, it = 0;
+      for (int u = blockIdx.x; u < n_units && !*abort; u += gridDim.x, ++it) {
+        const Unit un = load_unit<false>(d, pv, w, ws, u, upt);
+        const uint32_t idesc = idesc_f16_f32(128, un.npad);
+        const int b = it & 1;
+        if (it >= 2 && !wait_or_abort(&sm->tmem_empty[b], ((it - 2) >> 1) & 1, status, abort))
+          break;
+        tc_fence_after();
+        bool ok = true;
+        for (int ks = 0; ks < S; ++ks, ++ka) {
+          const int st = ka % kBStages, as = ka % kW2AS;
+          if (!wait_or_abort(&sm->full[st], (ka / kBStages) & 1, status, abort)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t ta = tmem + kAOff + as * (kBK / 2);
+          const uint64_t db = sdesc_sw128(smem_u32(base + kOffB + st * kBStage));
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk)
+            tc_mma_f16_ts(tmem + b * kTileRows, ta + 8 * kk, db + 2 * kk, idesc,
+                          (ks | kk) ? 1u : 0u);
+          tc_commit(&sm->empty[st]);
+        }
+        if (!ok) break;
+        tc_commit(&sm->accf[b]);
+      }
+      tc_commit(&sm->drain);
+      const long long t0 = clock64();
+      while (!mbar_try_wait(&sm->drain, 0) && clock64() - t0 < kWaitTimeoutCycles) {
+      }
+    }
+  } else if (warp == kW2BWarp) {
+    // ---- token rows (h in plan order): one ring stage per K step ----
+    if (lane == 0) {
+      uint32_t kb = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < n_units && ok && !*abort; u += gridDim.x) {
+        const Unit un = load_unit<false>(d, pv, w, ws, u, upt);
+        const int nch = (un.npad + kBChunkRows - 1) / kBChunkRows;
+        for (int ks = 0; ks < S; ++ks, ++kb) {
+          const int bs = kb % kBStages;
+          if (!wait_or_abort(&sm->empty[bs], ((kb / kBStages) & 1) ^ 1, status, abort)) {
+            ok = false;
+            break;
+          }
+          mbar_expect_tx(&sm->full[bs], (uint32_t)(nch * kBChunk));
+          for (int ch = 0; ch < nch; ++ch)
+            tma_load_2d(base + kOffB + bs * kBStage + ch * kBChunk, &bmap, ks * kBK,
+                        un.pos0 + ch * kBChunkRows, &sm->full[bs]);
+        }
+      }
+      for (uint32_t k = (kb > (uint32_t)kBStages ? kb - kBStages : 0); k < kb; ++k)
+        mbar_wait(&sm->full[k % kBStages], (k / kBStages) & 1, status);
+    }
+  } else if (warp == kW2ScaleWarp) {
+    // ---- g2 x combine weight of each row, one unit ahead (buffer it & 1 is
+    // free once the epilogue of unit it - 2 is done) ----
+    uint32_t it = 0;
+    for (int u = blockIdx.x; u < n_units && !*abort; u += gridDim.x, ++it) {
+      const Unit un = load_unit<false>(d, pv, w, ws, u, upt);
+      if (it >= 2 &&
+          !warp_wait_or_abort(&sm->tmem_empty[it & 1], ((it - 2) >> 1) & 1, status, abort))
+        break;
+      float* wsc = sm->wsc[it & 1];
+      int pr[kTileRows / 32];
+#pragma unroll
+      for (int i = 0; i < kTileRows / 32; ++i) {
+        const int n = lane + 32 * i;
+        pr[i] = n < un.rows ? __ldcg(pv.perm + un.pos0 + n) : -1;
+      }
+#pragma unroll
+      for (int i = 0; i < kTileRows / 32; ++i)
+        if (pr[i] >= 0) wsc[lane + 32 * i] = un.g * __ldcg(pv.w + pr[i]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm->wsc_full[it & 1]);
+    }
+  } else if (warp >= kW2EpiWarp0 && warp < kW2EpiWarp0 + 8) {
+    // ---- epilogue: lane r of warp (q, p) holds output row 32 q + r of the
+    // unit (H row sub * 128 + 32 q + r) for the chunks c0 = 32 p, 32 p + 64, ...
+    // A per-warp staging tile turns 16 columns at a time into rows of 32
+    // contiguous FP32 values, written as 16-byte stores into the pairs'
+    // partial rows (at the pairs' plan positions) ----
+    const int q = warp & 3, pr = (warp - kW2EpiWarp0) >> 2;
+    const int H = d.H;
+    float(*stg)[32] = reinterpret_cast<float(*)[32]>(sm->stage[warp - kW2EpiWarp0]);
+    uint32_t it = 0;
+    for (int u = blockIdx.x; u < n_units && !*abort; u += gridDim.x, ++it) {
+      const Unit un = load_unit<false>(d, pv, w, ws, u, upt);
+      const int b = it & 1;
+      if (!warp_wait_or_abort(&sm->accf[b], (it >> 1) & 1, status, abort)) break;
+      if (!warp_wait_or_abort(&sm->wsc_full[b], (it >> 1) & 1, status, abort)) break;
+      tc_fence_after();
+      const float* wsc = sm->wsc[b];
+      float* pbase = partial + (int64_t)un.pos0 * H + un.sub * 128 + q * 32;
+      const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + b * kTileRows;
+#pragma unroll 1
+      for (int c0 = 32 * pr; c0 < un.npad; c0 += 64) {
+        uint32_t v[32];
+        tmem_ld32(tbase + c0, v);
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) stg[j][lane] = __uint_as_float(v[16 * hf + j]);
+          __syncwarp();
+          // lanes 8p .. 8p+7 write column (pair) p0 + p: 8 x 16 bytes
+          const int cl = lane >> 3, part = lane & 7;
+#pragma unroll
+          for (int p4 = 0; p4 < 4; ++p4) {
+            const int j = p4 * 4 + cl;
+            const int n = c0 + 16 * hf + j;
+            if (n < un.rows) {
+              float4 o = reinterpret_cast<const float4*>(stg[j])[part];
+              const float sc = wsc[n];
+              o.x *= sc;
+              o.y *= sc;
+              o.z *= sc;
+              o.w *= sc;
+              __stcs(reinterpret_cast<float4*>(pbase + (int64_t)n * H) + part, o);
+            }
+          }
+          __syncwarp();
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm->tmem_empty[b]);
+    }
+  } else if (warp < kDqWarps) {
+    // ---- dequantise: one fragment block per warp and K step into the A stage ----
+    const int jl = 2 * (warp & 3) + (warp >> 2);  // block of the unit's 8 (rows 16 jl ..)
+    const uint32_t ta_warp = ((uint32_t)(16 * jl) << 16) + kAOff;
+    uint32_t kd = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < n_units && ok && !*abort; u += gridDim.x) {
+      for (int ks = 0; ks < S; ++ks, ++kd) {
+        const int rs = kd % kRS, as = kd % kW2AS;
+        if (!warp_wait_or_abort(&sm->raw_full[rs], (kd / kRS) & 1, status, abort)) {
+          ok = false;
+          break;
+        }
+        const char* raw = base + kOffRaw + rs * kRawBytes;
+        const uint4 qv = *reinterpret_cast<const uint4*>(raw + jl * 512 + lane * 16);
+        const uint32_t sc =
+            *reinterpret_cast<const unsigned short*>(raw + kRawQ + jl * 64 + lane * 2);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm->raw_empty[rs]);  // the stage is in registers
+        // A stage kd % kW2AS was last read by the MMAs of K step kd - kW2AS
+        if (kd >= (uint32_t)kW2AS) {
+          const uint32_t kp = kd - kW2AS;
+          if (!warp_wait_or_abort(&sm->empty[kp % kBStages], (kp / kBStages) & 1, status,
+                                  abort)) {
+            ok = false;
+            break;
+          }
+        }
+        tc_fence_after();
+        const uint32_t f = e4m3x2_to_f16x2(sc);
+        const uint32_t sg = __byte_perm(f, f, 0x1010), sg8 = __byte_perm(f, f, 0x3232);
+        uint32_t x[4], y[4], z[4], w4[4];
+        dequant8(qv.x, sg, x);
+        dequant8(qv.y, sg, y);
+        dequant8(qv.z, sg8, z);
+        dequant8(qv.w, sg8, w4);
+        const uint32_t r[16] = {x[0], x[1], z[0], z[1], x[2], x[3], z[2], z[3],
+                                y[0], y[1], w4[0], w4[1], y[2], y[3], w4[2], w4[3]};
+        tmem_st16x256_x4(tmem + ta_warp + as * (kBK / 2), r);
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm->full[kd % kBStages]);
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kW2MmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
 // xg[pos] = x[perm[pos] / k_eff]: the token rows in plan order, the operand of
 // the grouped W13 GEMM (positions past the valid pairs are left alone), with
 // each 64-element K step in the order of the tensor-memory A operand: output
@@ -578,13 +871,13 @@ cudaError_t launch_prefill_forward(const LayerDims& d, int64_t M, const __half* 
     cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<true>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(grouped_gemm_kernel<false>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    e = cudaFuncSetAttribute(grouped_w2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)w2_smem_bytes());
     if (e != cudaSuccess) return e;
     attr_done = true;
   }
   const int g13 = (int)std::min<int64_t>((int64_t)max_tiles * ((2 * d.I) / 256), num_sms);  // 256 weight rows per unit
-  const int g2 = (int)std::min<int64_t>((int64_t)max_tiles * (d.H / 256), num_sms);
+  const int g2 = (int)std::min<int64_t>((int64_t)max_tiles * (d.H / 128), num_sms);
   const bool pdl = !trace_on();
   // Token-row operands in plan order, read as 64-row tensor-map tiles (128-byte
   // swizzled): W13 reads x rows gathered into the partials buffer (unused until
@@ -604,8 +897,8 @@ cudaError_t launch_prefill_forward(const LayerDims& d, int64_t M, const __half* 
   if (e != cudaSuccess) return e;
   trace_mark(stream, kTraceW13, true);
   trace_mark(stream, kTraceW2, false);
-  e = launch_k(grouped_gemm_kernel<false>, dim3(g2), dim3(kGemmThreads), smem, stream, pdl, d,
-               pv, hmap, w2, s2, h, partial, status);
+  e = launch_k(grouped_w2_kernel, dim3(g2), dim3(kW2Threads), w2_smem_bytes(), stream, pdl, d,
+               pv, hmap, w2, s2, partial, status);
   if (e != cudaSuccess) return e;
   trace_mark(stream, kTraceW2, true);
   trace_mark(stream, kTraceCombine, false);
