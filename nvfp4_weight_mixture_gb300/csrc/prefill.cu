@@ -4,31 +4,36 @@
 // "[Kernel][SM70] Improve Qwen3.8 no-MTP concurrency", section "Scope and
 // related PRs": grouped W13 with SwiGLU and grouped W2 with the reduction,
 // both driven by the same integer plan.  A work unit is one plan tile (one
-// expert, up to 192 of its routed rows) times 256 weight rows:
+// expert, up to 192 of its routed rows) times a block of weight rows:
 //
 //   D[weight row][token] = sum_k W[weight row][k] * X[token][k]     (swap-AB)
 //
-// so the weight rows are the MMA's M = 128 (two accumulators of N <= 192
-// columns) and the tokens are N.  The dequantised weights (A) go to tensor
-// memory, not shared memory: tensor memory holds the two accumulators
-// (384 columns) and two A stages of one K step each (2 x 64 columns), and the
-// shared-memory bandwidth is left to the token rows (B) and raw weights.
-// Blocks are persistent (one per SM) and walk the units with a static stride.
-// Warp roles, each running ahead as far as its ring allows:
+// so the weight rows are the MMA's M = 128 and the tokens are N (<= 192).  The
+// dequantised weights (A) go to tensor memory (`tcgen05.st`), not shared
+// memory, which leaves the shared-memory bandwidth to the token rows (B) and
+// the raw weights.  Blocks are persistent (one per SM) and walk the units with
+// a static stride; each role runs ahead as far as its ring allows.
+//
+// grouped_w13_kernel: units of 256 weight rows (two A tiles, gate and up
+// interleaved); tensor memory holds the two accumulators (2 x 192 columns)
+// and two A stages of one K step (2 x 64 columns).  Warp roles:
 //   warp 13    one lane streams the unit's raw NVFP4 blocks (fragment layout:
 //              16 blocks of 512 + 64 bytes per K step of 64) into a shared
 //              ring with two bulk asynchronous copies per K step;
 //   warps 0-7  dequantise each raw stage into tensor memory (two fragment
 //              blocks per warp: warp w owns lanes 32 (w % 4) .. +31 of A tile
 //              w / 4, the lanes its sub-partition may access), then run the
-//              unit's epilogue on the same lanes of accumulator w / 4;
+//              unit's SwiGLU epilogue on the same lanes of accumulator w / 4;
 //   warp 8     one lane fills the token-row operand, one ring stage per K step
 //              (128-byte swizzled, K-major), with 64-row tensor-map loads of
-//              the plan-ordered rows: x gathered beforehand for W13, h for W2
-//              (warps 9-11 are spare);
+//              the token rows gathered into plan order beforehand (warps 9-11
+//              are spare);
 //   warp 12    allocates tensor memory; one lane issues the MMAs: per K step
-//              one wait on each ring, then per A tile and 16-element K slice one
-//              MMA with N = all of the unit's rows, then one commit per ring.
+//              one wait (A and B stages share one barrier), then per A tile and
+//              16-element K slice one MMA with N = all of the unit's rows, then
+//              one commit that frees both stages.
+// grouped_w2_kernel (further below): units of 128 output rows with
+// double-buffered accumulators and separate epilogue warps.
 //
 // K order inside each 64-element K step.  A warp's dequantised values sit in
 // the mma.sync fragment order (thread 4g + c: rows g, g + 8, elements
@@ -68,7 +73,6 @@ constexpr int kDqWarps = 8;
 constexpr int kBWarp0 = 8;
 constexpr int kMmaWarp = 12;
 constexpr int kRawWarp = 13;
-constexpr int kScaleWarp = 9;  // W2 only
 constexpr int kGemmThreads = 14 * 32;
 // Tensor memory: accumulator t at column t * kTileRows, A stage s, tile t at
 // column kAOff + s * 64 + t * 32 (64 FP16 of K per row = 32 columns).
@@ -92,16 +96,11 @@ struct GemmSmem {
   // thread commits K step k to empty[k % kBStages], which frees both.
   uint64_t full[kBStages], empty[kBStages];
   uint64_t accf, tmem_empty, drain;
-  // W2: g2 * combine weight of each row of unit it in wsc[it & 1], written by
-  // the scale warp one unit ahead; wsc_full[b] completes when it is there
-  __align__(16) float wsc[2][kTileRows];
-  uint64_t wsc_full[2];
   uint32_t tmem;
   int abort;
   int n_units;
-  // epilogue staging, 2 KiB per warp: W13 h values [32 tokens][16 i] (FP16),
-  // W2 partial values [16 pairs][32 rows] (FP32)
-  __align__(16) float stage[kDqWarps][512];
+  // epilogue staging, 1 KiB per warp: h values [32 tokens][16 i] (FP16)
+  __align__(16) float stage[kDqWarps][256];
 };
 
 constexpr size_t gemm_smem_bytes() {
@@ -172,23 +171,21 @@ __device__ __forceinline__ Unit load_unit(const LayerDims& d, const PlanView& pv
   return un;
 }
 
-template <bool kW13>
 __global__ void __launch_bounds__(kGemmThreads, 1)
-    grouped_gemm_kernel(LayerDims d, PlanView pv, const __grid_constant__ CUtensorMap bmap,
-                        Weights w, Weights ws, __half* __restrict__ h_out,
-                        float* __restrict__ partial, uint32_t* status) {
+    grouped_w13_kernel(LayerDims d, PlanView pv, const __grid_constant__ CUtensorMap bmap,
+                       Weights w, Weights ws, __half* __restrict__ h_out, uint32_t* status) {
   extern __shared__ __align__(1024) char smem_raw[];
   char* base = reinterpret_cast<char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                        ~uintptr_t(1023));
   GemmSmem* sm = reinterpret_cast<GemmSmem*>(base + kOffMeta);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  MOE_TL(kW13 ? kTlW13 : kTlW2);
-  MOE_PROF(constexpr int poff = kW13 ? 0 : 16);
+  MOE_TL(kTlW13);
+  MOE_PROF(constexpr int poff = 0);
   MOE_PROF(unsigned long long pacc[15] = {});
 
-  const int K = kW13 ? d.H : d.I;           // reduction length
+  const int K = d.H;                        // reduction length
   const int S = K / kBK;                     // K steps per unit
-  const int upt = kW13 ? (2 * d.I) / 256 : d.H / 256;  // units per plan tile
+  const int upt = (2 * d.I) / 256;          // units per plan tile
 
   if (tid == 0) {
     for (int i = 0; i < kRS; ++i) {
@@ -201,8 +198,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
     mbar_init(&sm->accf, 1);
     mbar_init(&sm->tmem_empty, kDqWarps);
-    mbar_init(&sm->wsc_full[0], 1);
-    mbar_init(&sm->wsc_full[1], 1);
     mbar_init(&sm->drain, 1);
     sm->abort = 0;
     fence_mbar_init();
@@ -224,7 +219,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     if (lane == 0) {
       uint32_t kr = 0;
       for (int u = blockIdx.x; u < n_units && !*abort; u += gridDim.x) {
-        const Unit un = load_unit<kW13>(d, pv, w, ws, u, upt);
+        const Unit un = load_unit<true>(d, pv, w, ws, u, upt);
         const int grp = un.sub;  // the unit's 256 weight rows are one fragment group
         bool ok = true;
         for (int ks = 0; ks < S; ++ks) {
@@ -241,7 +236,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           const size_t blk = ((size_t)grp * S + ks) * 16;
           bulk_g2s(dst, un.q + blk * 512, kRawQ, &sm->raw_full[slot]);
           bulk_g2s(dst + kRawQ, un.s + blk * 64, kRawBytes - kRawQ, &sm->raw_full[slot]);
-          if (kW13) MOE_DBG(6, kr);
+          MOE_DBG(6, kr);
           MOE_PROF(PROF_ADD(poff + 1, t0));
           ++kr;
         }
@@ -259,7 +254,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       MOE_PROF(const long long t_all = clock64());
       for (int u = blockIdx.x; u < n_units && !*abort; u += gridDim.x, ++it) {
         MOE_PROF(long long t0 = clock64());
-        const Unit un = load_unit<kW13>(d, pv, w, ws, u, upt);
+        const Unit un = load_unit<true>(d, pv, w, ws, u, upt);
         const uint32_t idesc = idesc_f16_f32(128, un.npad);
         MOE_PROF(PROF_ADD(poff + 3, t0); t0 = clock64());
         if (it > 0 && !wait_or_abort(&sm->tmem_empty, (it - 1) & 1, status, abort)) break;
@@ -276,7 +271,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             ok = false;
             break;
           }
-          if (kW13) MOE_DBG(2, ka);
+          MOE_DBG(2, ka);
           MOE_PROF(PROF_ADD(poff + 4, t0); t0 = clock64());
           tc_fence_after();
           const uint32_t ta = tmem + kAOff + as * kBK;
@@ -290,7 +285,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             tc_mma_f16_ts(tmem + kTileRows, ta + kBK / 2 + 8 * kk, db + 2 * kk, idesc, acc);
           }
           tc_commit(&sm->empty[bs]);
-          if (kW13) MOE_DBG(0, ka);
+          MOE_DBG(0, ka);
           MOE_PROF(PROF_ADD(poff + 6, t0));
         }
         if (!ok) break;
@@ -311,7 +306,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       uint32_t kb = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < n_units && ok && !*abort; u += gridDim.x) {
-        const Unit un = load_unit<kW13>(d, pv, w, ws, u, upt);
+        const Unit un = load_unit<true>(d, pv, w, ws, u, upt);
         const int nch = (un.npad + kBChunkRows - 1) / kBChunkRows;
         for (int ks = 0; ks < S; ++ks, ++kb) {
           const int bs = kb % kBStages;
@@ -325,7 +320,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           for (int ch = 0; ch < nch; ++ch)
             tma_load_2d(base + kOffB + bs * kBStage + ch * kBChunk, &bmap, ks * kBK,
                         un.pos0 + ch * kBChunkRows, &sm->full[bs]);
-          if (kW13) MOE_DBG(5, kb);
+          MOE_DBG(5, kb);
           MOE_PROF(PROF_ADD(poff + 9, t0));
         }
       }
@@ -335,32 +330,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       for (uint32_t k = (kb > (uint32_t)kBStages ? kb - kBStages : 0); k < kb; ++k)
         mbar_wait(&sm->full[k % kBStages], (k / kBStages) & 1, status);
     }
-  } else if (!kW13 && warp == kScaleWarp) {
-    // ---- W2 scale warp: g2 * combine weight of each row of each unit, one
-    // unit ahead of the epilogue, double-buffered (buffer it & 1 is free once
-    // the epilogue of unit it - 2 has finished)
-    uint32_t it = 0;
-    for (int u = blockIdx.x; u < n_units && !*abort; u += gridDim.x, ++it) {
-      const Unit un = load_unit<kW13>(d, pv, w, ws, u, upt);
-      if (it >= 2 && !warp_wait_or_abort(&sm->tmem_empty, (it - 2) & 1, status, abort)) break;
-      float* wsc = sm->wsc[it & 1];
-      int pr[kTileRows / 32];
-#pragma unroll
-      for (int i = 0; i < kTileRows / 32; ++i) {
-        const int n = lane + 32 * i;
-        pr[i] = n < un.rows ? __ldcg(pv.perm + un.pos0 + n) : -1;
-      }
-#pragma unroll
-      for (int i = 0; i < kTileRows / 32; ++i)
-        if (pr[i] >= 0) wsc[lane + 32 * i] = un.g * __ldcg(pv.w + pr[i]);
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sm->wsc_full[it & 1]);
-    }
   } else if (warp > kBWarp0) {
     // spare warps (timeline build: two of them stamp when each raw and B stage
     // lands, following the rings' phases without taking part in them)
 #ifdef MOE_TIMELINE
-    if (kW13 && blockIdx.x == 0 && lane == 0 && (warp == 9 || warp == 10)) {
+    if (blockIdx.x == 0 && lane == 0 && (warp == 9 || warp == 10)) {
       const int n_mine = (n_units - 1 - (int)blockIdx.x) / (int)gridDim.x + 1;
       const int nst = warp == 9 ? kRS : kBStages;
       uint64_t* bars = warp == 9 ? sm->raw_full : sm->full;
@@ -379,7 +353,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // ---- warps 0-7: dequantise, then the unit's epilogue ---------------------------
     uint32_t kd = 0, it = 0;
     for (int u = blockIdx.x; u < n_units && !*abort; u += gridDim.x, ++it) {
-      const Unit un = load_unit<kW13>(d, pv, w, ws, u, upt);
+      const Unit un = load_unit<true>(d, pv, w, ws, u, upt);
       bool ok = true;
       // this warp's two fragment blocks j = 2 warp + jj: rows 32 (warp % 4) + 16 jj
       // .. + 15 of A tile warp / 4
@@ -413,7 +387,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
         tc_fence_after();
         MOE_PROF(if (tid == 0) PROF_ADD(poff + 11, t0); t0 = clock64());
-        if (kW13 && lane == 0) MOE_DBG(3, kd * kDqWarps + warp);
+        if (lane == 0) MOE_DBG(3, kd * kDqWarps + warp);
 #pragma unroll
         for (int jj = 0; jj < 2; ++jj) {
           const uint32_t f = e4m3x2_to_f16x2(sc[jj]);
@@ -430,7 +404,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (kW13 && lane == 0) MOE_DBG(4, kd * kDqWarps + warp);
+        if (lane == 0) MOE_DBG(4, kd * kDqWarps + warp);
         if (lane == 0) mbar_arrive(&sm->full[kd % kBStages]);
         MOE_PROF(if (tid == 0) PROF_ADD(poff + 12, t0));
       }
@@ -440,90 +414,49 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const int q4 = warp & 3, at = warp >> 2;
       MOE_PROF(long long te = clock64());
       if (!warp_wait_or_abort(&sm->accf, it & 1, status, abort)) break;
-      if (kW13 && tid == 0) MOE_DBG(7, 2 * it);
+      if (tid == 0) MOE_DBG(7, 2 * it);
       MOE_PROF(if (tid == 0) PROF_ADD(poff + 13, te); te = clock64());
       tc_fence_after();
       const uint32_t tbase = tmem + ((uint32_t)(q4 * 32) << 16) + at * kTileRows;
-      if (kW13) {
-        // Lane r < 16 of warp q holds gate row (16q + r) and lane r + 16 the
-        // matching up row, for 32 token columns per load.  One exchange per
-        // pair of columns gives each lane 16 (G, U) pairs: gate lanes take
-        // columns 0-15, up lanes 16-31.  h goes through a per-warp staging
-        // tile; each token row's 16 values [16q, 16q + 16) of the 64-wide K
-        // step leave as four 8-byte groups, group r at position 16r + 4q (the
-        // K order of the W2 operand).
-        const int I = d.I;
-        const int r16 = lane & 15;
-        const bool is_gate = lane < 16;
-        __half(*stg)[16] = reinterpret_cast<__half(*)[16]>(sm->stage[warp]);
-        const int i0 = un.sub * 128 + at * 64 + q4 * 4;  // the 64-wide K step of W2, group q
+      // Lane r < 16 of warp q holds gate row (16q + r) and lane r + 16 the
+      // matching up row, for 32 token columns per load.  One exchange per
+      // pair of columns gives each lane 16 (G, U) pairs: gate lanes take
+      // columns 0-15, up lanes 16-31.  h goes through a per-warp staging
+      // tile; each token row's 16 values [16q, 16q + 16) of the 64-wide K
+      // step leave as four 8-byte groups, group r at position 16r + 4q (the
+      // K order of the W2 operand).
+      const int I = d.I;
+      const int r16 = lane & 15;
+      const bool is_gate = lane < 16;
+      __half(*stg)[16] = reinterpret_cast<__half(*)[16]>(sm->stage[warp]);
+      const int i0 = un.sub * 128 + at * 64 + q4 * 4;  // the 64-wide K step of W2, group q
 #pragma unroll 1
-        for (int c0 = 0; c0 < un.npad; c0 += 32) {
-          uint32_t v[32];
-          tmem_ld32(tbase + c0, v);
+      for (int c0 = 0; c0 < un.npad; c0 += 32) {
+        uint32_t v[32];
+        tmem_ld32(tbase + c0, v);
 #pragma unroll
-          for (int jj = 0; jj < 16; ++jj) {
-            const float lo = __uint_as_float(v[jj]), hi = __uint_as_float(v[jj + 16]);
-            const float recv = __shfl_xor_sync(0xffffffffu, is_gate ? hi : lo, 16);
-            const float G = (is_gate ? lo : recv) * un.g;
-            const float U = (is_gate ? recv : hi) * un.g;
-            const float hv = __fdividef(G, 1.f + __expf(-G)) * U;
-            stg[is_gate ? jj : jj + 16][r16] = __float2half_rn(hv);
-          }
-          __syncwarp();
-          const int n = c0 + lane;
-          if (n < un.rows) {
-            const uint2* s2 = reinterpret_cast<const uint2*>(stg[lane]);
-            __half* dst = h_out + (int64_t)(un.pos0 + n) * I + i0;
-#pragma unroll
-            for (int r = 0; r < 4; ++r) *reinterpret_cast<uint2*>(dst + 16 * r) = s2[r];
-          }
-          __syncwarp();
+        for (int jj = 0; jj < 16; ++jj) {
+          const float lo = __uint_as_float(v[jj]), hi = __uint_as_float(v[jj + 16]);
+          const float recv = __shfl_xor_sync(0xffffffffu, is_gate ? hi : lo, 16);
+          const float G = (is_gate ? lo : recv) * un.g;
+          const float U = (is_gate ? recv : hi) * un.g;
+          const float hv = __fdividef(G, 1.f + __expf(-G)) * U;
+          stg[is_gate ? jj : jj + 16][r16] = __float2half_rn(hv);
         }
-      } else {
-        // Lane r of warp q holds output row hd = sub * 256 + 128 at + 32 q + r
-        // for 32 pair columns per load; a per-warp staging tile turns 16
-        // columns at a time into rows of 32 contiguous FP32 values, written
-        // as 16-byte stores into the pairs' partial rows, which sit at the
-        // pairs' plan positions (consecutive for the unit).
-        const int H = d.H;
-        if (!warp_wait_or_abort(&sm->wsc_full[it & 1], (it >> 1) & 1, status, abort)) break;
-        const float* wsc = sm->wsc[it & 1];
-        float(*stg)[32] = reinterpret_cast<float(*)[32]>(sm->stage[warp]);
-        float* pbase = partial + (int64_t)un.pos0 * H + un.sub * 256 + at * 128 + q4 * 32;
-#pragma unroll 1
-        for (int c0 = 0; c0 < un.npad; c0 += 32) {
-          uint32_t v[32];
-          tmem_ld32(tbase + c0, v);
+        __syncwarp();
+        const int n = c0 + lane;
+        if (n < un.rows) {
+          const uint2* s2 = reinterpret_cast<const uint2*>(stg[lane]);
+          __half* dst = h_out + (int64_t)(un.pos0 + n) * I + i0;
 #pragma unroll
-          for (int hf = 0; hf < 2; ++hf) {
-#pragma unroll
-            for (int j = 0; j < 16; ++j) stg[j][lane] = __uint_as_float(v[16 * hf + j]);
-            __syncwarp();
-            // lanes 8p .. 8p+7 write column (pair) p0 + p: 8 x 16 bytes
-            const int cl = lane >> 3, part = lane & 7;
-#pragma unroll
-            for (int p4 = 0; p4 < 4; ++p4) {
-              const int j = p4 * 4 + cl;
-              const int n = c0 + 16 * hf + j;
-              if (n < un.rows) {
-                float4 o = reinterpret_cast<const float4*>(stg[j])[part];
-                const float sc = wsc[n];
-                o.x *= sc;
-                o.y *= sc;
-                o.z *= sc;
-                o.w *= sc;
-                __stcs(reinterpret_cast<float4*>(pbase + (int64_t)n * H) + part, o);
-              }
-            }
-            __syncwarp();
-          }
+          for (int r = 0; r < 4; ++r) *reinterpret_cast<uint2*>(dst + 16 * r) = s2[r];
         }
+        __syncwarp();
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm->tmem_empty);
-      if (kW13 && tid == 0) MOE_DBG(7, 2 * it + 1);
+      if (tid == 0) MOE_DBG(7, 2 * it + 1);
       MOE_PROF(if (tid == 0) PROF_ADD(poff + 14, te));
     }
   }
@@ -868,7 +801,7 @@ cudaError_t launch_prefill_forward(const LayerDims& d, int64_t M, const __half* 
   const size_t smem = gemm_smem_bytes();
   static bool attr_done = false;
   if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<true>,
+    cudaError_t e = cudaFuncSetAttribute(grouped_w13_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(grouped_w2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -892,8 +825,8 @@ cudaError_t launch_prefill_forward(const LayerDims& d, int64_t M, const __half* 
   e = launch_k(gather_rows_kernel, dim3((unsigned)((P + 7) / 8)), dim3(256), 0, stream, pdl, d, pv,
                x, xg);
   if (e != cudaSuccess) return e;
-  e = launch_k(grouped_gemm_kernel<true>, dim3(g13), dim3(kGemmThreads), smem, stream, pdl, d, pv,
-               xmap, w13, s13, h, partial, status);
+  e = launch_k(grouped_w13_kernel, dim3(g13), dim3(kGemmThreads), smem, stream, pdl, d, pv,
+               xmap, w13, s13, h, status);
   if (e != cudaSuccess) return e;
   trace_mark(stream, kTraceW13, true);
   trace_mark(stream, kTraceW2, false);
