@@ -36,7 +36,8 @@ DECODE_MAX_TOKENS = 16
 
 EXPORTS = ["moe_nvfp4_abi_version", "moe_nvfp4_status_string", "moe_nvfp4_query",
            "moe_nvfp4_quantize", "moe_nvfp4_plan", "moe_nvfp4_forward", "moe_nvfp4_dequantize",
-           "moe_nvfp4_set_trace_events", "moe_nvfp4_forward_noalloc"]
+           "moe_nvfp4_set_trace_events", "moe_nvfp4_forward_noalloc",
+           "moe_nvfp4_last_cuda_error"]
 TRACE_STEPS = ("plan", "w13", "w2", "combine")
 
 

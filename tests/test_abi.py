@@ -38,6 +38,8 @@ def test_abi_version_and_status_strings(lib):
         s = moe.status_string(code)
         assert s and s != "unknown code"
     assert moe.status_string(12345) == "unknown code"
+    # no call on this thread has failed in CUDA: the error name is empty
+    assert lib.moe_nvfp4_last_cuda_error() == b""
 
 
 def _cfg(H=2048, E=512, k=10, I=512, flags=0):
