@@ -51,10 +51,10 @@ struct PlanView {
   int32_t* tiles;     // [max_tiles][4] (expert, first row, rows, 0)
   int32_t* chunk_hist;// [n_chunks][e_eff] scratch of the large-M plan
   int32_t* rank;      // [M * k_eff] scratch: rank of a pair inside its chunk
-  float* partial;     // [n_hchunks][kDecodeMaxTokens][n_experts] scratch (small-M router)
-  float* logits;      // [kDecodeMaxTokens][n_experts] scratch (small-M router)
-  uint32_t* tickets;  // [64] self-resetting arrival counters: [0, 8) router slices,
-                      // [48, 51) decode forward grid barriers, 63 router finaliser
+  float* partial;     // [n_hchunks][kDecodeMaxTokens][n_experts] scratch (128-block router)
+  float* logits;      // [kDecodeMaxTokens][n_experts] scratch (128-block router)
+  uint32_t* tickets;  // [64] self-resetting arrival counters of the 128-block small-M
+                      // router: [0, 8) expert slices, 63 finaliser
   int32_t* dtab;      // [kDecodeMaxTokens * 33][kDtabInts] decode work table (M <= 16)
   float* rlogits;     // [min(M, kRouterChunk)][n_experts] router logits (M > 16)
   __half* wrt;        // [n_experts][hidden] transposed router weight (M > 16)

@@ -6,13 +6,18 @@
 // related PRs": the router is batched, and one integer plan is built once and
 // reused by grouped W13 and grouped W2 ("avoids repeated planning").
 //
-// Two shapes:
-//  * M <= 16 (decode): one kernel.  Blocks own (64-expert slice, 256-row
-//    chunk of H) and stream W_r once; arrival tickets make the last block of
-//    each slice reduce the chunk partials in a fixed order, and the last slice
-//    finaliser runs top-k, the weights, the gate and the whole plan.
-//  * M > 16 (prefill): a 64-token x all-experts mma.sync GEMM with the top-k
-//    in its epilogue, then a three-kernel stable counting sort.
+// Shapes:
+//  * M <= 16 (decode): one thread-block cluster (router_cluster_kernel).  CTA
+//    r owns an expert slice and computes its complete logits; the slices'
+//    top-k candidates are merged in CTA 0, which also computes the weights,
+//    the gate and the whole plan, decode work table included.  Where such a
+//    cluster cannot be scheduled, a 128-block router with arrival tickets
+//    (router_small_kernel) does the same.
+//  * M > 16 (prefill): the logits as a tcgen05 GEMM (router_logits_kernel, W_r
+//    transposed once per call) and one warp per token for top-k, weights and
+//    gate (router_topk_kernel); an mma.sync router with the top-k in its
+//    epilogue (router_mma_kernel) covers E < 256 and M < 128.  Then a
+//    three-kernel stable counting sort builds the plan.
 #include <math.h>
 
 #include "common.cuh"
