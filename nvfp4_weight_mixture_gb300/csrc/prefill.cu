@@ -476,32 +476,38 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 // ---------------------------------------------------------------------------
 // Grouped W2.  A unit is one plan tile times 128 output rows (one A tile), so
 // that tensor memory holds two accumulator buffers (2 x 192 columns) beside
-// four A stages (4 x 32 columns): the epilogue of unit u drains one buffer
-// while the MMAs of unit u + 1 fill the other.  20 warps:
-//   warps 0-7    dequantise one fragment block each per K step (warp w owns
-//                lanes 16 (2 (w % 4) + w / 4) .. + 15 of the A tile);
+// two A stages of a 128-element K step (2 x 64 columns): the epilogue of unit
+// u drains one buffer while the MMAs of unit u + 1 fill the other.  A K step
+// is two 64-element fragment segments (8 MMAs per wait and commit).  20 warps:
+//   warps 0-7    dequantise one fragment block of each segment per K step
+//                (warp w owns lanes 16 (2 (w % 4) + w / 4) .. + 15 of the A tile);
 //   warps 8-15   epilogue: warp 8 + q + 4 p reads lanes 32 q .. + 31 of the
 //                unit's buffer, the 32-column chunks of parity p;
 //   warp 16      tensor memory owner, one lane issues the MMAs;
-//   warp 17      raw NVFP4 bulk copies (8 fragment blocks per K step);
-//   warp 18      token rows (h) by 64-row tensor-map loads;
+//   warp 17      raw NVFP4 bulk copies (8 fragment blocks per segment);
+//   warp 18      token rows (h) by 64-row tensor-map loads, one 24 KiB half
+//                stage per segment;
 //   warp 19      g2 x combine weight of each row, one unit ahead.
 // ---------------------------------------------------------------------------
 constexpr int kW2Threads = 20 * 32;
-constexpr int kW2AS = 4;          // A stages of one tile
+constexpr int kW2KS = 2 * kBK;     // K per W2 step: two fragment segments
+constexpr int kW2AS = 2;          // A stages of one tile and one step
+constexpr int kW2BStages = 2;     // B stages of one step (two 24 KiB halves each)
 constexpr int kW2EpiWarp0 = 8;
 constexpr int kW2MmaWarp = 16;
 constexpr int kW2RawWarp = 17;
 constexpr int kW2BWarp = 18;
 constexpr int kW2ScaleWarp = 19;
-constexpr int kW2RawQ = 8 * 512;  // raw q bytes per K step (8 fragment blocks)
+constexpr int kW2RawQ = 8 * 512;  // raw q bytes per segment (8 fragment blocks)
 constexpr int kW2RawS = 8 * 64;
-static_assert(kAOff + kW2AS * (kBK / 2) <= kTmemCols, "W2 tensor memory over-committed");
-static_assert(kBStages >= kW2AS, "the B ring serves the A stages' barriers");
+static_assert(2 * kW2RawQ <= kRawQ && 2 * kW2RawS <= kRawBytes - kRawQ, "W2 raw slot");
+static_assert(kAOff + kW2AS * (kW2KS / 2) <= kTmemCols, "W2 tensor memory over-committed");
+static_assert(kW2BStages == kW2AS, "one barrier per K step serves both rings");
+static_assert(kW2BStages * 2 * kBStage <= kBStages * kBStage, "W2 B ring inside the B region");
 
 struct W2Smem {
   uint64_t raw_full[kRS], raw_empty[kRS];
-  uint64_t full[kBStages], empty[kBStages];
+  uint64_t full[kW2BStages], empty[kW2BStages];
   // per accumulator buffer b: accf[b] completes when a unit's MMAs into b are
   // done, tmem_empty[b] when its epilogue has read b, wsc_full[b] when the
   // unit's scales are in wsc[b]
@@ -525,7 +531,7 @@ __global__ void __launch_bounds__(kW2Threads, 1)
   W2Smem* sm = reinterpret_cast<W2Smem*>(base + kOffMeta);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   MOE_TL(kTlW2);
-  const int S = d.I / kBK;     // K steps per unit
+  const int S = d.I / kW2KS;   // K steps per unit (I % 128 == 0)
   const int upt = d.H / 128;   // units per plan tile
 
   if (tid == 0) {
@@ -533,7 +539,7 @@ __global__ void __launch_bounds__(kW2Threads, 1)
       mbar_init(&sm->raw_full[i], 1);
       mbar_init(&sm->raw_empty[i], kDqWarps);
     }
-    for (int i = 0; i < kBStages; ++i) {
+    for (int i = 0; i < kW2BStages; ++i) {
       mbar_init(&sm->full[i], kDqWarps + 1);
       mbar_init(&sm->empty[i], 1);
     }
@@ -572,10 +578,15 @@ __global__ void __launch_bounds__(kW2Threads, 1)
             break;
           }
           char* dst = base + kOffRaw + slot * kRawBytes;
-          mbar_expect_tx(&sm->raw_full[slot], kW2RawQ + kW2RawS);
-          const size_t blk = ((size_t)grp * S + ks) * 16 + 8 * half;
-          bulk_g2s(dst, un.q + blk * 512, kW2RawQ, &sm->raw_full[slot]);
-          bulk_g2s(dst + kRawQ, un.s + blk * 64, kW2RawS, &sm->raw_full[slot]);
+          mbar_expect_tx(&sm->raw_full[slot], 2 * (kW2RawQ + kW2RawS));
+          // segments 2 ks and 2 ks + 1: q of segment c at c * kW2RawQ, s at
+          // kRawQ + c * kW2RawS
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            const size_t blk = ((size_t)grp * (2 * S) + 2 * ks + c) * 16 + 8 * half;
+            bulk_g2s(dst + c * kW2RawQ, un.q + blk * 512, kW2RawQ, &sm->raw_full[slot]);
+            bulk_g2s(dst + kRawQ + c * kW2RawS, un.s + blk * 64, kW2RawS, &sm->raw_full[slot]);
+          }
         }
       }
       for (uint32_t k = (kr > (uint32_t)kRS ? kr - kRS : 0); k < kr; ++k)
@@ -594,18 +605,23 @@ __global__ void __launch_bounds__(kW2Threads, 1)
         tc_fence_after();
         bool ok = true;
         for (int ks = 0; ks < S; ++ks, ++ka) {
-          const int st = ka % kBStages, as = ka % kW2AS;
-          if (!wait_or_abort(&sm->full[st], (ka / kBStages) & 1, status, abort)) {
+          const int st = ka % kW2BStages, as = ka % kW2AS;
+          if (!wait_or_abort(&sm->full[st], (ka / kW2BStages) & 1, status, abort)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t ta = tmem + kAOff + as * (kBK / 2);
-          const uint64_t db = sdesc_sw128(smem_u32(base + kOffB + st * kBStage));
+          const uint32_t ta = tmem + kAOff + as * (kW2KS / 2);
 #pragma unroll
-          for (int kk = 0; kk < kBK / 16; ++kk)
-            tc_mma_f16_ts(tmem + b * kTileRows, ta + 8 * kk, db + 2 * kk, idesc,
-                          (ks | kk) ? 1u : 0u);
+          for (int c = 0; c < 2; ++c) {
+            // segment c: A columns [32 c, 32 c + 32) of the stage, B half c
+            const uint64_t db =
+                sdesc_sw128(smem_u32(base + kOffB + (st * 2 + c) * kBStage));
+#pragma unroll
+            for (int kk = 0; kk < kBK / 16; ++kk)
+              tc_mma_f16_ts(tmem + b * kTileRows, ta + 32 * c + 8 * kk, db + 2 * kk, idesc,
+                            (ks | c | kk) ? 1u : 0u);
+          }
           tc_commit(&sm->empty[st]);
         }
         if (!ok) break;
@@ -625,19 +641,20 @@ __global__ void __launch_bounds__(kW2Threads, 1)
         const Unit un = load_unit<false>(d, pv, w, ws, u, upt);
         const int nch = (un.npad + kBChunkRows - 1) / kBChunkRows;
         for (int ks = 0; ks < S; ++ks, ++kb) {
-          const int bs = kb % kBStages;
-          if (!wait_or_abort(&sm->empty[bs], ((kb / kBStages) & 1) ^ 1, status, abort)) {
+          const int bs = kb % kW2BStages;
+          if (!wait_or_abort(&sm->empty[bs], ((kb / kW2BStages) & 1) ^ 1, status, abort)) {
             ok = false;
             break;
           }
-          mbar_expect_tx(&sm->full[bs], (uint32_t)(nch * kBChunk));
-          for (int ch = 0; ch < nch; ++ch)
-            tma_load_2d(base + kOffB + bs * kBStage + ch * kBChunk, &bmap, ks * kBK,
-                        un.pos0 + ch * kBChunkRows, &sm->full[bs]);
+          mbar_expect_tx(&sm->full[bs], (uint32_t)(2 * nch * kBChunk));
+          for (int c = 0; c < 2; ++c)
+            for (int ch = 0; ch < nch; ++ch)
+              tma_load_2d(base + kOffB + (bs * 2 + c) * kBStage + ch * kBChunk, &bmap,
+                          ks * kW2KS + c * kBK, un.pos0 + ch * kBChunkRows, &sm->full[bs]);
         }
       }
-      for (uint32_t k = (kb > (uint32_t)kBStages ? kb - kBStages : 0); k < kb; ++k)
-        mbar_wait(&sm->full[k % kBStages], (k / kBStages) & 1, status);
+      for (uint32_t k = (kb > (uint32_t)kW2BStages ? kb - kW2BStages : 0); k < kb; ++k)
+        mbar_wait(&sm->full[k % kW2BStages], (k / kW2BStages) & 1, status);
     }
   } else if (warp == kW2ScaleWarp) {
     // ---- g2 x combine weight of each row, one unit ahead (buffer it & 1 is
@@ -726,35 +743,43 @@ __global__ void __launch_bounds__(kW2Threads, 1)
           break;
         }
         const char* raw = base + kOffRaw + rs * kRawBytes;
-        const uint4 qv = *reinterpret_cast<const uint4*>(raw + jl * 512 + lane * 16);
-        const uint32_t sc =
-            *reinterpret_cast<const unsigned short*>(raw + kRawQ + jl * 64 + lane * 2);
+        uint4 qv[2];
+        uint32_t sc[2];
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          qv[c] = *reinterpret_cast<const uint4*>(raw + c * kW2RawQ + jl * 512 + lane * 16);
+          sc[c] = *reinterpret_cast<const unsigned short*>(raw + kRawQ + c * kW2RawS + jl * 64 +
+                                                           lane * 2);
+        }
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm->raw_empty[rs]);  // the stage is in registers
         // A stage kd % kW2AS was last read by the MMAs of K step kd - kW2AS
         if (kd >= (uint32_t)kW2AS) {
           const uint32_t kp = kd - kW2AS;
-          if (!warp_wait_or_abort(&sm->empty[kp % kBStages], (kp / kBStages) & 1, status,
+          if (!warp_wait_or_abort(&sm->empty[kp % kW2BStages], (kp / kW2BStages) & 1, status,
                                   abort)) {
             ok = false;
             break;
           }
         }
         tc_fence_after();
-        const uint32_t f = e4m3x2_to_f16x2(sc);
-        const uint32_t sg = __byte_perm(f, f, 0x1010), sg8 = __byte_perm(f, f, 0x3232);
-        uint32_t x[4], y[4], z[4], w4[4];
-        dequant8(qv.x, sg, x);
-        dequant8(qv.y, sg, y);
-        dequant8(qv.z, sg8, z);
-        dequant8(qv.w, sg8, w4);
-        const uint32_t r[16] = {x[0], x[1], z[0], z[1], x[2], x[3], z[2], z[3],
-                                y[0], y[1], w4[0], w4[1], y[2], y[3], w4[2], w4[3]};
-        tmem_st16x256_x4(tmem + ta_warp + as * (kBK / 2), r);
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          const uint32_t f = e4m3x2_to_f16x2(sc[c]);
+          const uint32_t sg = __byte_perm(f, f, 0x1010), sg8 = __byte_perm(f, f, 0x3232);
+          uint32_t x[4], y[4], z[4], w4[4];
+          dequant8(qv[c].x, sg, x);
+          dequant8(qv[c].y, sg, y);
+          dequant8(qv[c].z, sg8, z);
+          dequant8(qv[c].w, sg8, w4);
+          const uint32_t r[16] = {x[0], x[1], z[0], z[1], x[2], x[3], z[2], z[3],
+                                  y[0], y[1], w4[0], w4[1], y[2], y[3], w4[2], w4[3]};
+          tmem_st16x256_x4(tmem + ta_warp + as * (kW2KS / 2) + 32 * c, r);
+        }
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&sm->full[kd % kBStages]);
+        if (lane == 0) mbar_arrive(&sm->full[kd % kW2BStages]);
       }
     }
   }
