@@ -66,6 +66,22 @@ def dist_info():
 # ---------------------------------------------------------------------------
 # accounting (algorithmic bytes and FLOPs)
 # ---------------------------------------------------------------------------
+def max_over_ranks(value, dist, device):
+    """The largest value over the ranks (the slowest rank's time); the value
+    itself without a process group."""
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(world_size, tokens_per_rank_step, steps, total_ms):
+    """Whole-job throughput: every rank's tokens over the slowest rank's time."""
+    return world_size * tokens_per_rank_step * steps / (total_ms / 1e3)
+
+
 def w13_expert_bytes(wl):
     return 2 * wl.I * wl.H // 2 + 2 * wl.I * wl.H // 16 + 4
 
@@ -407,14 +423,11 @@ def run_gpu(args, wl):
     wall = time.perf_counter() - t_wall
     ck = clocks.stop()
     times = [a.elapsed_time(b) for a, b in ev]
-    total_ms = sum(times)
+    total_ms = max_over_ranks(sum(times), dist, dev)
     if dist:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
         dist.barrier()
     ms_per_step = total_ms / steps
-    value = ws * wl.M * steps / (total_ms / 1e3)
+    value = job_tokens_per_s(ws, wl.M, steps, total_ms)
 
     # ---- per-kernel durations (traced eager steps, same protocol) ----------------
     tr = [torch.cuda.Event(enable_timing=True) for _ in range(8)]
@@ -461,12 +474,8 @@ def run_gpu(args, wl):
             yh.copy_(yd, non_blocking=True)
             eev[i][1].record(stream)
     torch.cuda.synchronize()
-    e2e_ms = sum(a.elapsed_time(b) for a, b in eev)
-    if dist:
-        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_value = ws * wl.M * steps / (e2e_ms / 1e3)
+    e2e_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in eev), dist, dev)
+    e2e_value = job_tokens_per_s(ws, wl.M, steps, e2e_ms)
 
     if rank != 0:
         if dist:
