@@ -131,7 +131,12 @@ const char* moe_nvfp4_last_cuda_error(void);
  * forward workspace (for moe_nvfp4_forward) for any M <= max_tokens.
  * Host-only arithmetic; also checks that the current device is an sm_103
  * part (MOE_ERR_UNSUPPORTED_DEVICE otherwise) unless `plan_bytes` and
- * `ws_bytes` are both NULL, in which case only `cfg` is validated. */
+ * `ws_bytes` are both NULL, in which case only `cfg` is validated.
+ *
+ * The first call of any entry point on a device that checks the device also
+ * sets up the library's kernels there once (shared-memory limits, the
+ * router's cluster size; MOE_ERR_CUDA if that fails, retried on the next
+ * call).  The set-up is serialised across host threads and enqueues no work. */
 int32_t moe_nvfp4_query(const moe_nvfp4_config* cfg, int64_t max_tokens, size_t* plan_bytes,
                         size_t* ws_bytes);
 

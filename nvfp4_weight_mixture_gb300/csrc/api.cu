@@ -20,14 +20,18 @@ namespace {
 struct DevInfo {
   bool init = false;
   bool supported = false;
+  bool kernels_ready = false;
   int num_sms = 0;
 };
 
 std::mutex g_dev_mu;
 DevInfo g_dev[64];
 
-// Validates the current device (compute capability 10.3) and caches its SM
-// count.  Returns MOE_OK or an error code.
+thread_local cudaError_t g_last_cuda_error = cudaSuccess;
+
+// Validates the current device (compute capability 10.3), caches its SM count
+// and, once per device, sets up its kernels (shared-memory limits, the
+// router's cluster size).  Returns MOE_OK or an error code.
 int32_t current_device(int* num_sms) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) {
@@ -50,6 +54,17 @@ int32_t current_device(int* num_sms) {
     di.init = true;
   }
   if (!di.supported) return MOE_ERR_UNSUPPORTED_DEVICE;
+  if (!di.kernels_ready) {
+    cudaError_t e = router_device_init(dev);
+    if (e == cudaSuccess) e = prefill_device_init();
+    if (e == cudaSuccess) e = decode_device_init();
+    if (e != cudaSuccess) {
+      g_last_cuda_error = e;
+      cudaGetLastError();
+      return MOE_ERR_CUDA;
+    }
+    di.kernels_ready = true;
+  }
   *num_sms = di.num_sms;
   return MOE_OK;
 }
@@ -97,8 +112,6 @@ int32_t check_weights(const moe_nvfp4_weights* w, int32_t layout) {
 
 void* const* g_trace_events = nullptr;
 int32_t g_trace_steps = 0;
-
-thread_local cudaError_t g_last_cuda_error = cudaSuccess;
 
 int32_t cuda_status(cudaError_t e) {
   if (e == cudaSuccess) return MOE_OK;

@@ -28,6 +28,14 @@ cudaError_t launch_quantize(const float* w, int64_t n_mats, int64_t rows, int64_
 cudaError_t launch_dequantize(const uint8_t* q, const uint8_t* s, int64_t n_mats, int64_t rows,
                               int64_t k, int layout, void* out, cudaStream_t stream, int num_sms);
 
+// One-time set-up of a device's kernels (shared-memory limits, the router's
+// cluster size), run by the C-ABI layer under its device lock the first time
+// a call uses device `dev`, before any launch there.  Each returns the first
+// CUDA error; the set-up is retried on the next call after a failure.
+cudaError_t router_device_init(int dev);
+cudaError_t prefill_device_init();
+cudaError_t decode_device_init();
+
 // Router + plan.  ids_user / w_user are outputs unless ids_given.
 cudaError_t launch_plan(const LayerDims& d, int64_t M, const __half* x, const __half* w_router,
                         const float* bias, const __half* w_gate, int32_t* ids_user,

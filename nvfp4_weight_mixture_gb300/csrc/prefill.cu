@@ -817,6 +817,15 @@ __global__ void gather_rows_kernel(LayerDims d, PlanView pv, const __half* __res
   }
 }
 
+cudaError_t prefill_device_init() {
+  cudaError_t e = cudaFuncSetAttribute(grouped_w13_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)gemm_smem_bytes());
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(grouped_w2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)w2_smem_bytes());
+}
+
 cudaError_t launch_prefill_forward(const LayerDims& d, int64_t M, const __half* x,
                                    const PlanView& pv, Weights w13, Weights w2, Weights s13,
                                    Weights s2, __half* y, __half* h, float* partial,
@@ -824,16 +833,6 @@ cudaError_t launch_prefill_forward(const LayerDims& d, int64_t M, const __half* 
   const int64_t P = M * d.k_eff;
   const int max_tiles = max_tiles_for(P, d.e_eff);
   const size_t smem = gemm_smem_bytes();
-  static bool attr_done = false;
-  if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(grouped_w13_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(grouped_w2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)w2_smem_bytes());
-    if (e != cudaSuccess) return e;
-    attr_done = true;
-  }
   const int g13 = (int)std::min<int64_t>((int64_t)max_tiles * ((2 * d.I) / 256), num_sms);  // 256 weight rows per unit
   const int g2 = (int)std::min<int64_t>((int64_t)max_tiles * (d.H / 128), num_sms);
   const bool pdl = !trace_on();

@@ -896,13 +896,6 @@ static cudaError_t launch_router_tc(const LayerDims& d, int64_t M, const __half*
                                     const __half* w_router, const float* bias,
                                     const __half* w_gate, int32_t* ids_user, float* w_user,
                                     const PlanView& pv, uint32_t* status, cudaStream_t stream) {
-  static bool attr_done = false;
-  if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(router_logits_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kRlSmem);
-    if (e != cudaSuccess) return e;
-    attr_done = true;
-  }
   transpose_wr_kernel<<<dim3((d.E + 31) / 32, d.H / 32), 256, 0, stream>>>(w_router, d.H, d.E,
                                                                              pv.wrt);
   CUtensorMap xmap, wmap;
@@ -1204,19 +1197,19 @@ __global__ void __launch_bounds__(kRcThreads, 1)
   if (tid == 0) MOE_TL_MIN(25);
 }
 
-// Largest cluster (16, else 8, else 0: the 128-block router is used) that the
-// device can co-schedule with this kernel at its largest shared-memory use.
-// Decided once per process.
-static int router_cluster_max() {
-  static int c = -1;
-  if (c >= 0) return c;
-  c = 0;
+// Largest cluster (16, else 8, else 0: the 128-block router is used) that each
+// device can co-schedule with router_cluster_kernel at its largest
+// shared-memory use; written by router_device_init before the device's first
+// launch.
+static int g_cluster_max[64];
+
+static int router_cluster_probe() {
   if (cudaFuncSetAttribute(router_cluster_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed,
                            1) != cudaSuccess ||
       cudaFuncSetAttribute(router_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)kRcSmemBudget) != cudaSuccess) {
     cudaGetLastError();
-    return c;
+    return 0;
   }
   for (int cand : {16, 8}) {
     cudaLaunchConfig_t cfg = {};
@@ -1231,13 +1224,26 @@ static int router_cluster_max() {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, router_cluster_kernel, &cfg) == cudaSuccess && n >= 1) {
-      c = cand;
-      break;
-    }
+    if (cudaOccupancyMaxActiveClusters(&n, router_cluster_kernel, &cfg) == cudaSuccess && n >= 1)
+      return cand;
     cudaGetLastError();
   }
-  return c;
+  return 0;
+}
+
+cudaError_t router_device_init(int dev) {
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  cudaError_t e = cudaFuncSetAttribute(router_logits_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kRlSmem);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(router_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)router_mma_smem(512));
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(plan_hist_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)(sizeof(uint16_t) * 32 * kMaxEEff));
+  if (e != cudaSuccess) return e;
+  g_cluster_max[dev] = router_cluster_probe();
+  return cudaSuccess;
 }
 
 // ---------------------------------------------------------------------------
@@ -1246,13 +1252,16 @@ cudaError_t launch_plan(const LayerDims& d, int64_t M, const __half* x, const __
                         float* w_user, bool ids_given, const PlanView& pv, uint32_t* status,
                         cudaStream_t stream, int num_sms) {
   (void)num_sms;
+  int dev = 0;
+  cudaError_t de = cudaGetDevice(&dev);
+  if (de != cudaSuccess) return de;
   const int Mi = (int)M;
   if (M <= kDecodeMaxTokens) {
     if (ids_given) {
       route_given_kernel<<<(Mi + 7) / 8, 256, 0, stream>>>(d, Mi, x, w_gate, ids_user, w_user, pv);
       plan_small_kernel<<<1, 256, 0, stream>>>(d, Mi, pv, status);
     } else {
-      const int cmax = router_cluster_max();
+      const int cmax = (dev >= 0 && dev < 64) ? g_cluster_max[dev] : 0;
       const RouterClusterPlan L = router_cluster_plan(d.H, d.E, d.k, Mi, cmax > 0 ? cmax : 1);
       if (cmax > 0 && L.stages >= 1 && L.total <= kRcSmemBudget) {
         CUtensorMap wrmap;
@@ -1288,28 +1297,12 @@ cudaError_t launch_plan(const LayerDims& d, int64_t M, const __half* x, const __
     if (e != cudaSuccess) return e;
   } else {
     const size_t smem = router_mma_smem(d.E);
-    static bool attr_done = false;
-    if (!attr_done) {
-      cudaError_t e = cudaFuncSetAttribute(router_mma_kernel,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           (int)router_mma_smem(512));
-      if (e != cudaSuccess) return e;
-      attr_done = true;
-    }
     router_mma_kernel<<<(Mi + kRtTok - 1) / kRtTok, 512, smem, stream>>>(
         d, Mi, x, w_router, bias, w_gate, ids_user, w_user, pv);
   }
   const int64_t P = M * d.k_eff;
   const int n_chunks = (int)((P + kPlanChunk - 1) / kPlanChunk);
   const size_t hsmem = sizeof(uint16_t) * 32 * d.e_eff;
-  static bool attr_done = false;
-  if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(plan_hist_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)(sizeof(uint16_t) * 32 * 520));
-    if (e != cudaSuccess) return e;
-    attr_done = true;
-  }
   plan_hist_kernel<<<n_chunks, 1024, hsmem, stream>>>(d, P, pv, status);
   plan_scan_kernel<<<1, 1024, 0, stream>>>(d, Mi, n_chunks, pv);
   plan_scatter_kernel<<<(unsigned)((P + 255) / 256), 256, 0, stream>>>(d, P, pv);
