@@ -126,6 +126,16 @@ def test_router_tensor_core_shapes(M, H, E, k):
     assert int(case.layer.status.item()) == 0
 
 
+@pytest.mark.parametrize("M,H,E,k", [(40, 256, 32, 32), (200, 4096, 136, 10), (100, 512, 512, 3)])
+def test_router_mma_shapes(M, H, E, k):
+    """The mma.sync router (16 < M with E < 256, or M < 128): k = E = 32, the
+    largest hidden size with E not a multiple of 64 (136), and E = 512 below
+    the tensor-core router's 128-token minimum."""
+    case = _RouteCase(synth.custom("rm", M, H, E, k, 128))
+    _check_router(case)
+    assert int(case.layer.status.item()) == 0
+
+
 @pytest.mark.parametrize("M,H,E,k", [(3, 256, 24, 2), (16, 4096, 512, 10), (1, 1024, 512, 32),
                                      (7, 768, 64, 6), (16, 2048, 512, 10)])
 def test_router_cluster_shapes(M, H, E, k):
@@ -222,6 +232,42 @@ def test_forward_other_shapes(M, H, E, k, I):
     """Shapes away from the benchmark: K = I of 16 segments in W2, H = 4096
     (the largest hidden size), decode and prefill buckets."""
     _forward_check(Case(synth.custom("shape", M, H, E, k, I)))
+
+
+@pytest.fixture(scope="module")
+def largest_case():
+    """The largest hidden and intermediate sizes the ABI accepts together
+    (H = I = 4096: W13 of 8192 x 4096 and W2 of 4096 x 4096 per expert), 8
+    experts, top-2, 40 tokens."""
+    return Case(synth.custom("max", 40, 4096, 8, 2, 4096))
+
+
+def _forward_prefix(case, M):
+    """Plan + forward of the case's first M tokens with the oracle router's ids."""
+    tok = np.arange(M)
+    _, ids, w, _ = case.oracle_route(tok)
+    xs = case.x_t[:M]
+    case.layer.route(xs, torch.from_numpy(np.ascontiguousarray(ids, np.int32)).cuda(),
+                     torch.from_numpy(np.ascontiguousarray(w, np.float32)).cuda())
+    y = case.layer.forward_planned(xs)
+    torch.cuda.synchronize()
+    rel, mx = compare(y.cpu().numpy(), case.oracle_forward(tokens=tok))
+    assert rel <= REL_L2_TOL and mx <= MAX_ABS_TOL, (rel, mx)
+    assert int(case.layer.status.item()) == 0
+
+
+@pytest.mark.parametrize("M", [16, 40])
+def test_forward_largest_sizes(largest_case, M):
+    """H = I = 4096 in the decode bucket (the first 16 tokens: 64 K segments
+    of W2 per tensor-map copy) and in the grouped GEMMs (32 W2 K steps)."""
+    _forward_prefix(largest_case, M)
+
+
+@pytest.mark.parametrize("M", [16, 40])
+def test_forward_top32_every_expert(M):
+    """k = 32 = E, the largest top-k: every token uses every expert, so each
+    expert holds all M rows (16 per expert in the decode bucket)."""
+    _forward_check(Case(synth.custom("k32", M, 256, 32, 32, 512)))
 
 
 def test_forward_decode_m1_full():
