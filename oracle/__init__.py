@@ -77,7 +77,7 @@ def _load():
         lib.oracle_plan.argtypes = [P, I64, I64, I64, P, P, P, P, P, I64,
                                     ctypes.POINTER(ctypes.c_int64)]
         lib.oracle_plan.restype = ctypes.c_uint32
-        lib.oracle_forward.argtypes = [I64] * 5 + [P] * 15 + [P, P, I64, P, P]
+        lib.oracle_forward.argtypes = [I64] * 5 + [P] * 15 + [P, P, I64, ctypes.c_int, P, P]
         lib.oracle_forward.restype = ctypes.c_uint32
         _lib = lib
         return lib
@@ -202,8 +202,11 @@ def plan(ids, n_exp, bn):
                 inv=inv[:P].copy(), tiles=tiles[:nt.value].copy(), status=int(st))
 
 
-def forward(x, ids, w, w13, w2, shared=None, gamma=None, tokens=None, want_h=False):
-    """Layer output for the given tokens.
+def forward(x, ids, w, w13, w2, shared=None, gamma=None, tokens=None, want_h=False,
+            h_exact=False):
+    """Layer output for the given tokens.  h is rounded to FP16 between the
+    GEMMs (the reading the acceptance bar is stated against); with h_exact it
+    is not (the other reading of the same passage).
 
     w13 = (q [E,2I,H/2], s [E,2I,H/16], g [E]); w2 = (q [E,H,I/2], s [E,H,I/16], g [E]);
     shared = None or ((q13, s13, g13), (q2, s2, g2)) without the expert axis.
@@ -238,7 +241,7 @@ def forward(x, ids, w, w13, w2, shared=None, gamma=None, tokens=None, want_h=Fal
     st = _load().oracle_forward(M, H, E, k, I, _p(x), _p(ids), _p(w), _p(q13), _p(s13),
                                 _p(g13), _p(q2), _p(s2), _p(g2), _p(sq13), _p(ss13),
                                 _p(sg13), _p(sq2), _p(ss2), _p(sg2), _p(gm), _p(tok),
-                                n_tok, _p(y), _p(h))
+                                n_tok, int(bool(h_exact)), _p(y), _p(h))
     y = y.view(np.float16)
     if want_h:
         return y, int(st), h

@@ -456,10 +456,12 @@ static double wval(const uint8_t *q, const uint8_t *s, int64_t k, int64_t r, int
  * (READING of the name W13 = w1 (gate) stacked over w3 (up)); the one global
  * scale g13 covers both halves (READING: one tensor per expert and matrix).
  * Rounding h to FP16 is a READING: the second GEMM consumes FP16 operands.
+ * With h_exact the other reading is taken instead: h stays unrounded (a
+ * double), as if the two GEMMs were fused with no narrowing between them.
  */
 static void expert_mlp(const double *xt, int64_t H, int64_t I, const uint8_t *q13,
                        const uint8_t *s13, float g13, const uint8_t *q2,
-                       const uint8_t *s2, float g2, double *h, double *o)
+                       const uint8_t *s2, float g2, int h_exact, double *h, double *o)
 {
     for (int64_t i = 0; i < I; ++i) {
         double G = 0.0, U = 0.0;
@@ -470,7 +472,7 @@ static void expert_mlp(const double *xt, int64_t H, int64_t I, const uint8_t *q1
         G *= (double)g13;
         U *= (double)g13;
         double a = G / (1.0 + exp(-G)) * U;
-        h[i] = oracle_f16_to_double(oracle_f16_from_double(a));
+        h[i] = h_exact ? a : oracle_f16_to_double(oracle_f16_from_double(a));
     }
     for (int64_t n = 0; n < H; ++n) {
         double acc = 0.0;
@@ -495,7 +497,8 @@ static void expert_mlp(const double *xt, int64_t H, int64_t I, const uint8_t *q1
  *
  * Weights are canonical NVFP4: q13 [E][2I][H/2], s13 [E][2I][H/16], g13 [E];
  * q2 [E][H][I/2], s2 [E][H][I/16], g2 [E]; shared expert the same without E.
- * h_out (optional): the FP16-rounded h of each pair, [n_tok][k][I] as double.
+ * h_out (optional): the h of each pair, [n_tok][k][I] as double (FP16-rounded
+ * unless h_exact).
  */
 uint32_t oracle_forward(int64_t M, int64_t H, int64_t E, int64_t k, int64_t I,
                         const uint16_t *x, const int32_t *ids, const float *w,
@@ -504,7 +507,7 @@ uint32_t oracle_forward(int64_t M, int64_t H, int64_t E, int64_t k, int64_t I,
                         const uint8_t *sq13, const uint8_t *ss13, const float *sg13,
                         const uint8_t *sq2, const uint8_t *ss2, const float *sg2,
                         const float *gamma, const int64_t *tokens, int64_t n_tok,
-                        uint16_t *y, double *h_out)
+                        int h_exact, uint16_t *y, double *h_out)
 {
     init_tabs();
     uint32_t status = 0;
@@ -536,7 +539,7 @@ uint32_t oracle_forward(int64_t M, int64_t H, int64_t E, int64_t k, int64_t I,
                 continue;
             }
             expert_mlp(xt, H, I, q13 + e * b13, s13 + e * c13, g13[e], q2 + e * b2,
-                       s2 + e * c2, g2[e], h, o);
+                       s2 + e * c2, g2[e], h_exact, h, o);
             if (h_out)
                 for (int64_t i = 0; i < I; ++i)
                     h_out[(jt * k + j) * I + i] = h[i];
@@ -544,7 +547,7 @@ uint32_t oracle_forward(int64_t M, int64_t H, int64_t E, int64_t k, int64_t I,
                 acc[n] += (double)w[t * k + j] * o[n];
         }
         if (sq13) {
-            expert_mlp(xt, H, I, sq13, ss13, sg13[0], sq2, ss2, sg2[0], h, o);
+            expert_mlp(xt, H, I, sq13, ss13, sg13[0], sq2, ss2, sg2[0], h_exact, h, o);
             double gm = gamma ? (double)gamma[t] : 1.0;
             for (int64_t n = 0; n < H; ++n)
                 acc[n] += gm * o[n];

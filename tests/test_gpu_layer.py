@@ -270,6 +270,21 @@ def test_forward_top32_every_expert(M):
     _forward_check(Case(synth.custom("k32", M, 256, 32, 32, 512)))
 
 
+@pytest.mark.parametrize("wl,M", [(TINY, 40), (PRE, 300), (DEC16, 16)])
+def test_forward_within_bar_of_both_h_readings(wl, M):
+    """The pages leave open whether h is rounded to FP16 between the two
+    GEMMs; the kernels round it (kind::f16 operands).  The output also meets
+    the acceptance bar against the oracle that keeps h unrounded."""
+    case = Case(synth.with_tokens(wl, M))
+    y = case.gpu_forward(ids_from_oracle=True)
+    _, ids, w, _ = case.oracle_route()
+    o13, o2, _ = case.oracle_weights(set(int(e) for e in ids.ravel()))
+    ref, st = oracle.forward(case.x, ids, w, o13, o2, h_exact=True)
+    rel, mx = compare(y, ref)
+    assert rel <= REL_L2_TOL and mx <= MAX_ABS_TOL, (rel, mx)
+    assert st == 0 and int(case.layer.status.item()) == 0
+
+
 def test_forward_decode_m1_full():
     _forward_check(Case(DEC1))
 

@@ -334,3 +334,40 @@ def test_forward_h_is_fp16_rounded_swiglu():
     gu = W13 @ x[t].astype(np.float64)
     ref = gu[:128] / (1 + np.exp(-gu[:128])) * gu[128:]
     np.testing.assert_array_equal(h[t, j], ref.astype(np.float16).astype(np.float64))
+
+
+def test_forward_h_exact_reading():
+    """The other reading of the h hand-off (no FP16 rounding between the
+    GEMMs): h equals the FP64 SwiGLU itself, the single-expert layer equals
+    the dense MLP with unrounded h (torch.matmul), and on the tiny workload the
+    two readings' outputs sit well inside the acceptance bar of each other,
+    so that bar does not depend on which reading is taken."""
+    wl = TINY
+    x = synth.activations(wl)
+    w13, w2, _ = _quant_all(wl)
+    _, ids, w = oracle.router(x, synth.router_weight(wl), None, wl.k)
+    yx, st, h = oracle.forward(x, ids, w, w13, w2, want_h=True, h_exact=True)
+    assert st == 0
+    t, j = 2, 0
+    e = ids[t, j]
+    W13 = dequant_np(w13[0][e], w13[1][e]) * np.float64(w13[2][e])
+    gu = W13 @ x[t].astype(np.float64)
+    ref = gu[:128] / (1 + np.exp(-gu[:128])) * gu[128:]
+    np.testing.assert_allclose(h[t, j], ref, rtol=1e-12, atol=1e-15)
+    assert np.any(h[t, j] != ref.astype(np.float16).astype(np.float64))
+    y16, _ = oracle.forward(x, ids, w, w13, w2)
+    r = rel_l2(yx, y16)
+    assert 0 < r < 5e-4  # ~3.3e-4: the FP16 rounding of h, averaged over I terms
+    assert np.max(np.abs(yx.astype(np.float64) - y16.astype(np.float64))) < 1e-2
+
+    d = synth.custom("d", 6, 128, 1, 1, 64)
+    xd = synth.activations(d)
+    a13, a2, _ = _quant_all(d)
+    y1, _ = oracle.forward(xd, np.zeros((6, 1), np.int32), np.ones((6, 1), np.float32), a13, a2,
+                           h_exact=True)
+    W13 = torch.from_numpy(dequant_np(a13[0][0], a13[1][0]) * float(a13[2][0]))
+    W2 = torch.from_numpy(dequant_np(a2[0][0], a2[1][0]) * float(a2[2][0]))
+    gu = torch.matmul(torch.from_numpy(xd.astype(np.float64)), W13.T)
+    hh = torch.nn.functional.silu(gu[:, :64]) * gu[:, 64:]
+    np.testing.assert_allclose(y1.astype(np.float64), torch.matmul(hh, W2.T).numpy(),
+                               rtol=2 ** -10, atol=2 ** -24)
