@@ -162,51 +162,76 @@ def load_traffic(workload, kernel):
 # clocks sampler (nvidia-smi during the timed region)
 # ---------------------------------------------------------------------------
 class Clocks:
-    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi samples every 50 ms, each stamped; only the samples taken
+    between region_begin() and region_end() are reported (all of them, marked
+    "in_region": false, if the region was too short to catch one)."""
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
 
     def __init__(self, gpu_index):
         self.proc = None
         self.gpu = gpu_index
+        self.t0 = self.t1 = None
 
     def start(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.3)  # the first sample lands before the region opens
         except Exception:
             self.proc = None
+
+    def region_begin(self):
+        self.t0 = time.time()
+
+    def region_end(self):
+        self.t1 = time.time()
+
+    @staticmethod
+    def parse(out, t0=None, t1=None):
+        """(samples inside [t0, t1], all samples), each (sm, max_sm, reasons)."""
+        import datetime
+        inside, every = [], []
+        for line in out.splitlines():
+            v = [x.strip() for x in line.split(",")]
+            if len(v) < 9:
+                continue
+            try:
+                s = (float(v[1]), float(v[2]),
+                     {n for n, f in zip(Clocks.NAMES, v[5:9]) if f.lower() == "active"})
+            except ValueError:
+                continue
+            every.append(s)
+            try:
+                ts = datetime.datetime.strptime(v[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+            except ValueError:
+                continue
+            if t0 is not None and t1 is not None and t0 <= ts <= t1:
+                inside.append(s)
+        return inside, every
 
     def stop(self):
         if self.proc is None:
             return None
-        time.sleep(0.25)
+        time.sleep(0.1)
         self.proc.terminate()
         try:
             out, _ = self.proc.communicate(timeout=5)
         except Exception:
             self.proc.kill()
             out, _ = self.proc.communicate()
-        sm, mx, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in out.splitlines():
-            v = [x.strip() for x in line.split(",")]
-            if len(v) < 8:
-                continue
-            try:
-                sm.append(float(v[0]))
-                mx.append(float(v[1]))
-            except ValueError:
-                continue
-            for n, flag in zip(names, v[4:8]):
-                if flag.lower() == "active":
-                    reasons.add(n)
-        if not sm:
+        inside, every = self.parse(out, self.t0, self.t1)
+        use = inside or every
+        if not use:
             return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
-                "reasons": sorted(reasons), "samples": len(sm)}
+        return {"sm_mhz": statistics.median(s[0] for s in use),
+                "sm_max_mhz": max(s[1] for s in use),
+                "reasons": sorted(set().union(*(s[2] for s in use))),
+                "samples": len(use), "in_region": bool(inside)}
 
 
 # ---------------------------------------------------------------------------
@@ -366,7 +391,7 @@ def run_gpu(args, wl):
     dev = torch.device("cuda", local)
     moe.load_library()
     decode = wl.M <= moe.DECODE_MAX_TOKENS
-    steps = args.steps or (200 if decode else 30)
+    steps = args.steps or (5000 if decode else 300)
     warmup = max(3, args.warmup if args.warmup is not None else 10)
 
     layer = build_layer(wl, dev, moe, synth)
@@ -412,6 +437,7 @@ def run_gpu(args, wl):
         dist.barrier()
     torch.cuda.synchronize()
     clocks.start()
+    clocks.region_begin()
     t_wall = time.perf_counter()
     with torch.cuda.stream(stream):
         for i in range(steps):
@@ -421,6 +447,7 @@ def run_gpu(args, wl):
             ev[i][1].record(stream)
     torch.cuda.synchronize()
     wall = time.perf_counter() - t_wall
+    clocks.region_end()
     ck = clocks.stop()
     times = [a.elapsed_time(b) for a, b in ev]
     total_ms = max_over_ranks(sum(times), dist, dev)

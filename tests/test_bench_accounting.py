@@ -1,5 +1,5 @@
 """The bench's roofline arithmetic against figures worked out by hand from the
-layer's shapes (no GPU).
+layer's shapes, and its clock-sample filter (no GPU).
 
 Per expert, NVFP4 storage is half a byte per weight, one E4M3 byte per 16
 weights and one FP32 global scale per matrix: W13 (2I x H) and W2 (H x I) at
@@ -67,3 +67,18 @@ def test_shared_expert_layer():
     b, f = bench.layer_accounting(wl, 149, 81920 + 8192)
     assert b == 149 * PER_EXPERT + W_R + 2 * 8192 * 4096 + 512 * 4 + 2048 * 2
     assert f == 8192 * 2 * 2048 * 512 + (81920 + 8192) * PAIR_FLOPS + 8192 * 2 * 2048
+
+
+def test_clock_samples_outside_the_timed_region_are_dropped():
+    import datetime
+    def line(t, sm, reason="Not Active"):
+        ts = datetime.datetime.fromtimestamp(t).strftime("%Y/%m/%d %H:%M:%S.%f")[:-3]
+        return f"{ts}, {sm}, 2070, 900.5, 0x0, {reason}, Not Active, Not Active, Not Active"
+    t0 = 1_800_000_000.0
+    out = "\n".join([line(t0 - 0.2, 1000, "Active"),      # before: a slowdown, ignored
+                     line(t0 + 0.05, 2070), line(t0 + 0.10, 2050), line(t0 + 0.15, 2070),
+                     line(t0 + 0.6, 1200), "garbage line"])
+    inside, every = bench.Clocks.parse(out, t0, t0 + 0.3)
+    assert [s[0] for s in inside] == [2070.0, 2050.0, 2070.0]
+    assert len(every) == 5 and "hw_slowdown" in every[0][2]
+    assert all(not s[2] for s in inside)
