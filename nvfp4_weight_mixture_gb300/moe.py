@@ -131,6 +131,78 @@ def _need(t, dtype, name):
     return t
 
 
+def _on_current_device(named):
+    """Every given tensor lives on the current CUDA device (the one whose
+    stream the library enqueues on)."""
+    dev = torch.cuda.current_device()
+    for name, t in named:
+        if t is not None and t.device.index != dev:
+            raise ValueError(f"{name}: on {t.device}, but the current device is cuda:{dev}")
+
+
+def _expect(errors, name, t, dtype, n):
+    if t is None:
+        return
+    if t.dtype != dtype:
+        errors.append(f"{name}: expected {dtype}, got {t.dtype}")
+    elif t.numel() != n:
+        errors.append(f"{name}: expected {n} elements, got {t.numel()}")
+
+
+def _expect_weights(errors, name, w, rows, k, n_mats):
+    if w is None:
+        return
+    q, s, g = w
+    _expect(errors, name + ".q", q, torch.uint8, n_mats * rows * k // 2)
+    _expect(errors, name + ".s", s, torch.uint8, n_mats * rows * k // 16)
+    _expect(errors, name + ".g", g, torch.float32, n_mats)
+
+
+def _expect_status(errors, status):
+    if status is not None and (status.dtype != torch.int32 or status.numel() < 1):
+        errors.append("status: expected at least one int32 element")
+
+
+def plan_arg_errors(cfg, x, w_router, bias, w_gate, ids, topk_w, status=None):
+    """Sizes and dtypes the plan call reads and writes through plain pointers
+    (the C ABI cannot see them): x [M][H] FP16, W_r [H][E] FP16, bias [E] FP32,
+    w_g [H] FP16, ids [M][k] int32, weights [M][k] FP32.  Returns the list of
+    mismatches (empty when the arguments fit)."""
+    H, E, k = cfg.hidden, cfg.n_experts, cfg.top_k
+    M = x.shape[0] if x.dim() > 0 else 0
+    e = []
+    _expect(e, "x", x, torch.float16, M * H)
+    _expect(e, "w_router", w_router, torch.float16, H * E)
+    _expect(e, "bias", bias, torch.float32, E)
+    _expect(e, "w_gate", w_gate, torch.float16, H)
+    _expect(e, "ids", ids, torch.int32, M * k)
+    _expect(e, "topk_w", topk_w, torch.float32, M * k)
+    _expect_status(e, status)
+    return e
+
+
+def forward_arg_errors(cfg, x, w13, w2, shared13, shared2, y, status=None):
+    """As plan_arg_errors for the forward: x and y [M][H] FP16; W13 codes,
+    scales and global scales of E matrices of 2I x H, W2 of E matrices of
+    H x I (the shared expert's: one matrix each)."""
+    H, E, I = cfg.hidden, cfg.n_experts, cfg.intermediate
+    M = x.shape[0] if x.dim() > 0 else 0
+    e = []
+    _expect(e, "x", x, torch.float16, M * H)
+    _expect(e, "y", y, torch.float16, M * H)
+    _expect_weights(e, "w13", w13, 2 * I, H, E)
+    _expect_weights(e, "w2", w2, H, I, E)
+    _expect_weights(e, "shared13", shared13, 2 * I, H, 1)
+    _expect_weights(e, "shared2", shared2, H, I, 1)
+    _expect_status(e, status)
+    return e
+
+
+def _raise_if(fn, errors):
+    if errors:
+        raise ValueError(f"{fn}: " + "; ".join(errors))
+
+
 def make_config(hidden, n_experts, top_k, intermediate, shared=False, ids_given=False):
     c = Config()
     c.hidden, c.n_experts, c.top_k, c.intermediate = hidden, n_experts, top_k, intermediate
@@ -226,16 +298,39 @@ def plan(cfg: Config, x, w_router, bias, w_gate, ids, topk_w, plan_buf, status=N
     _need(ids, torch.int32, "ids")
     _need(topk_w, torch.float32, "topk_w")
     _need(plan_buf, torch.uint8, "plan")
+    for name, t in (("w_router", w_router), ("bias", bias), ("w_gate", w_gate),
+                    ("status", status)):
+        if t is not None:
+            _need(t, t.dtype, name)
+    _raise_if("plan", plan_arg_errors(cfg, x, w_router, bias, w_gate, ids, topk_w, status))
+    _on_current_device([("x", x), ("w_router", w_router), ("bias", bias), ("w_gate", w_gate),
+                        ("ids", ids), ("topk_w", topk_w), ("plan", plan_buf), ("status", status)])
     _check("moe_nvfp4_plan", load_library().moe_nvfp4_plan(
         ctypes.byref(cfg), M, _ptr(x), _ptr(w_router), _ptr(bias), _ptr(w_gate), _ptr(ids),
         _ptr(topk_w), _ptr(plan_buf), plan_buf.numel(), _ptr(status), _stream()))
 
 
-def forward(cfg: Config, x, plan_buf, w13, w2, shared13, shared2, y, ws, status=None):
-    M = x.shape[0]
+def _check_forward_args(fn, cfg, x, plan_buf, w13, w2, shared13, shared2, y, status, ws=None):
     _need(x, torch.float16, "x")
     _need(y, torch.float16, "y")
-    _need(ws, torch.uint8, "ws")
+    _need(plan_buf, torch.uint8, "plan")
+    if ws is not None:
+        _need(ws, torch.uint8, "ws")
+    named = [("x", x), ("y", y), ("plan", plan_buf), ("ws", ws), ("status", status)]
+    for wn, w in (("w13", w13), ("w2", w2), ("shared13", shared13), ("shared2", shared2)):
+        if w is not None:
+            for part, t in zip("qsg", w):
+                _need(t, t.dtype, f"{wn}.{part}")
+                named.append((f"{wn}.{part}", t))
+    if status is not None:
+        _need(status, torch.int32, "status")
+    _raise_if(fn, forward_arg_errors(cfg, x, w13, w2, shared13, shared2, y, status))
+    _on_current_device(named)
+
+
+def forward(cfg: Config, x, plan_buf, w13, w2, shared13, shared2, y, ws, status=None):
+    M = x.shape[0]
+    _check_forward_args("forward", cfg, x, plan_buf, w13, w2, shared13, shared2, y, status, ws)
     a = _weights_c(w13, LAYOUT_FRAGMENT_W13)
     b = _weights_c(w2, LAYOUT_FRAGMENT)
     c = _weights_c(shared13, LAYOUT_FRAGMENT_W13)
@@ -250,8 +345,8 @@ def forward_noalloc(cfg: Config, x, plan_buf, w13, w2, shared13, shared2, y, sta
     """moe_nvfp4_forward_noalloc: the forward with the library's own static
     workspace (for callers that cannot allocate; see the header)."""
     M = x.shape[0]
-    _need(x, torch.float16, "x")
-    _need(y, torch.float16, "y")
+    _check_forward_args("forward_noalloc", cfg, x, plan_buf, w13, w2, shared13, shared2, y,
+                        status)
     a = _weights_c(w13, LAYOUT_FRAGMENT_W13)
     b = _weights_c(w2, LAYOUT_FRAGMENT)
     c = _weights_c(shared13, LAYOUT_FRAGMENT_W13)

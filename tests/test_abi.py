@@ -106,3 +106,49 @@ def test_quantize_fail_closed(lib):
     assert qz(a, 1, 16, 64, 5, a, a, a, None, None) == -7
     assert qz(None, 1, 16, 64, 0, a, a, a, None, None) == -1
     assert qz(P(0x10008), 1, 16, 64, 0, a, a, a, None, None) == -3
+
+
+def test_binding_checks_sizes_the_abi_cannot_see():
+    """The C ABI takes plain pointers, so the binding checks every tensor's
+    dtype and element count against the configuration before a call (CPU
+    tensors stand in: only metadata is read)."""
+    import torch
+    from nvfp4_weight_mixture_gb300 import moe
+    H, E, k, I, M = 256, 16, 2, 128, 5
+    c = moe.make_config(H, E, k, I)
+    f16, f32, i32, u8 = torch.float16, torch.float32, torch.int32, torch.uint8
+    x = torch.zeros(M, H, dtype=f16)
+    ok = dict(x=x, w_router=torch.zeros(H, E, dtype=f16), bias=torch.zeros(E, dtype=f32),
+              w_gate=torch.zeros(H, dtype=f16), ids=torch.zeros(M, k, dtype=i32),
+              topk_w=torch.zeros(M, k, dtype=f32), status=torch.zeros(1, dtype=i32))
+    assert moe.plan_arg_errors(c, **ok) == []
+    assert moe.plan_arg_errors(c, **dict(ok, w_router=None, bias=None, w_gate=None)) == []
+    assert moe.plan_arg_errors(c, **dict(ok, x=x[:0], ids=ok["ids"][:0],
+                                          topk_w=ok["topk_w"][:0])) == []
+    for name, bad in (("ids", torch.zeros(M, k + 1, dtype=i32)),
+                      ("ids", torch.zeros(M, k, dtype=torch.int64)),
+                      ("topk_w", torch.zeros(M - 1, k, dtype=f32)),
+                      ("w_router", torch.zeros(E, H - 8, dtype=f16)),
+                      ("bias", torch.zeros(E, dtype=f16)),
+                      ("w_gate", torch.zeros(H + 1, dtype=f16)),
+                      ("x", torch.zeros(M, H // 2, dtype=f16)),
+                      ("status", torch.zeros(1, dtype=f32))):
+        errs = moe.plan_arg_errors(c, **dict(ok, **{name: bad}))
+        assert errs and errs[0].startswith(name), (name, errs)
+
+    def weights(rows, kk, n):
+        return (torch.zeros(n, rows * kk // 2, dtype=u8), torch.zeros(n, rows * kk // 16, dtype=u8),
+                torch.zeros(n, dtype=f32))
+    w13, w2 = weights(2 * I, H, E), weights(H, I, E)
+    fok = dict(x=x, w13=w13, w2=w2, shared13=None, shared2=None, y=torch.zeros(M, H, dtype=f16))
+    assert moe.forward_arg_errors(c, **fok) == []
+    assert moe.forward_arg_errors(c, **dict(fok, shared13=weights(2 * I, H, 1),
+                                            shared2=weights(H, I, 1))) == []
+    for name, bad, prefix in (("y", torch.zeros(M - 1, H, dtype=f16), "y"),
+                              ("y", torch.zeros(M, H, dtype=f32), "y"),
+                              ("w13", weights(2 * I, H, E - 1), "w13.q"),
+                              ("w2", weights(2 * I, H, E), "w2.q"),
+                              ("w2", (w2[0], w2[1], torch.zeros(E, dtype=f16)), "w2.g"),
+                              ("shared2", weights(H, I, 2), "shared2.q")):
+        errs = moe.forward_arg_errors(c, **dict(fok, **{name: bad}))
+        assert errs and errs[0].startswith(prefix), (name, errs)
