@@ -269,11 +269,22 @@ def quantize(w: torch.Tensor, layout: int, status: torch.Tensor | None = None, q
     return q, s, g
 
 
+def dequantize_arg_errors(q, s, n_mats, rows, k):
+    """q and s must hold the codes and scales of n_mats matrices of rows x k."""
+    e = []
+    _expect(e, "q", q, torch.uint8, n_mats * rows * k // 2)
+    _expect(e, "s", s, torch.uint8, n_mats * rows * k // 16)
+    return e
+
+
 def dequantize(q, s, n_mats, rows, k, layout):
+    _need(q, torch.uint8, "q")
+    _need(s, torch.uint8, "s")
+    _raise_if("dequantize", dequantize_arg_errors(q, s, n_mats, rows, k))
+    _on_current_device([("q", q), ("s", s)])
     out = torch.empty((n_mats, rows, k), dtype=torch.float16, device=q.device)
     _check("moe_nvfp4_dequantize", load_library().moe_nvfp4_dequantize(
-        _ptr(_need(q, torch.uint8, "q")), _ptr(_need(s, torch.uint8, "s")), n_mats, rows, k,
-        int(layout), _ptr(out), _stream()))
+        _ptr(q), _ptr(s), n_mats, rows, k, int(layout), _ptr(out), _stream()))
     return out
 
 

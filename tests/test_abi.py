@@ -152,3 +152,8 @@ def test_binding_checks_sizes_the_abi_cannot_see():
                               ("shared2", weights(H, I, 2), "shared2.q")):
         errs = moe.forward_arg_errors(c, **dict(fok, **{name: bad}))
         assert errs and errs[0].startswith(prefix), (name, errs)
+    # dequantise: codes and scales of n_mats x rows x k
+    q, s = torch.zeros(2 * 256 * 64 // 2, dtype=u8), torch.zeros(2 * 256 * 64 // 16, dtype=u8)
+    assert moe.dequantize_arg_errors(q, s, 2, 256, 64) == []
+    assert moe.dequantize_arg_errors(q[:-1], s, 2, 256, 64)[0].startswith("q")
+    assert moe.dequantize_arg_errors(q, s, 2, 256, 128)[0].startswith("q")
