@@ -79,6 +79,8 @@ def _load():
         lib.oracle_plan.restype = ctypes.c_uint32
         lib.oracle_forward.argtypes = [I64] * 5 + [P] * 15 + [P, P, I64, ctypes.c_int, P, P]
         lib.oracle_forward.restype = ctypes.c_uint32
+        lib.oracle_dense.argtypes = [I64, I64, I64, P, P, P, ctypes.c_float, P]
+        lib.oracle_dense.restype = None
         _lib = lib
         return lib
 
@@ -246,3 +248,18 @@ def forward(x, ids, w, w13, w2, shared=None, gamma=None, tokens=None, want_h=Fal
     if want_h:
         return y, int(st), h
     return y, int(st)
+
+
+def dense(x, q, s, g):
+    """Dense NVFP4 projection y = fp16(g * x . w16^T) of FP16 rows x [M, K]
+    with canonical NVFP4 weights q [N, K/2], s [N, K/16] and global scale g."""
+    x = _f16bits(x)
+    M, K = x.shape
+    q = _c(q, np.uint8)
+    s = _c(s, np.uint8)
+    N = q.shape[0]
+    if q.shape != (N, K // 2) or s.shape != (N, K // 16):
+        raise ValueError("dense: q must be [N, K/2] and s [N, K/16]")
+    y = np.empty((M, N), np.uint16)
+    _load().oracle_dense(M, N, K, _p(x), _p(q), _p(s), float(g), _p(y))
+    return y.view(np.float16)

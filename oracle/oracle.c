@@ -18,6 +18,10 @@
  *   [P1-QSA]    "[Perf][SM70] Optimize Qwen3.8 Flash Next prefill", section
  *               "SM70 QSA indexer hotspot update": the 8192-token, top-10
  *               NVFP4 MoE (W13 then W2).
+ *   [P2-QPN2]   "[SM70][Draft] Extend Qwen3.8 DFlash2 concurrency paths",
+ *               sections "Purpose" and "Test Result": the QPN2 NVFP4 dense
+ *               projection over a few rows (eight-row tiles, M <= 32),
+ *               compared against FP32.
  * The pages do not print the bit layout.  The format followed here is the
  * standard NVFP4 one: E2M1 elements, one E4M3 ("fn": no infinities, 0x7F and
  * 0xFF are NaN) block scale per 16 consecutive K elements of a row, and one
@@ -560,6 +564,31 @@ uint32_t oracle_forward(int64_t M, int64_t H, int64_t E, int64_t k, int64_t I,
         free(acc);
     }
     return status;
+}
+
+/*
+ * Dense NVFP4 projection of a few FP16 rows [P2-QPN2]:
+ *   y[m][n] = fp16( g * sum_K x[m][K] * w16[n][K] )
+ * accumulated in FP64 and rounded to FP16 once (READING: the pages print no
+ * formula for QPN2; this is the layer's own projection step, the same as the
+ * expert MLP's second GEMM, without routing).  Canonical NVFP4 weights:
+ * q [N][K/2], s [N][K/16], one FP32 global scale g.  x [M][K] and y [M][N]
+ * are FP16 bits.  Each row is computed on its own, so a row's output does not
+ * depend on the other rows of the call.
+ */
+void oracle_dense(int64_t M, int64_t N, int64_t K, const uint16_t *x, const uint8_t *q,
+                  const uint8_t *s, float g, uint16_t *y)
+{
+    init_tabs();
+#pragma omp parallel for schedule(static)
+    for (int64_t n = 0; n < N; ++n) {
+        for (int64_t m = 0; m < M; ++m) {
+            double acc = 0.0;
+            for (int64_t c = 0; c < K; ++c)
+                acc += oracle_f16_to_double(x[m * K + c]) * wval(q, s, K, n, c);
+            y[m * N + n] = oracle_f16_from_double(acc * (double)g);
+        }
+    }
 }
 
 int oracle_abi_version(void) { return 1; }
