@@ -8,12 +8,15 @@ cache is flushed (a 2x-L2 buffer is written) before every timed step, outside
 the step's events, and the routes change from step to step (16 different token
 batches), so weights stream from HBM as in a real layer stack.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workloads A,B,..]
+    python bench.py --workload NAME        # one workload only
     python bench.py --impl reference ...   # the CPU oracle arm
 
-Workloads (seeded; see nvfp4_weight_mixture_gb300/synth.py): decode_m1 (the
-default: 1 token, H 2048, 512 experts, top-10, I 512), decode_m16_bias,
-prefill_m8192, prefill_m8192_zipf_shared, tiny_m8.
+Workloads (seeded; see nvfp4_weight_mixture_gb300/synth.py).  The default run
+times all five in turn under the same protocol and prints one JSON line: the
+headline decode_m1 (1 token, H 2048, 512 experts, top-10, I 512), with
+decode_m16_bias, prefill_m8192, prefill_m8192_zipf_shared and tiny_m8 in its
+"configs" map (each with its own value, roofline, e2e and clocks).
 
 Under torchrun each rank runs the same workload on its own GPU (token-parallel
 replicas, no collective on the data path); value = all ranks' tokens / the
@@ -36,6 +39,10 @@ sys.path.insert(0, ROOT)
 import numpy as np  # noqa: E402
 
 METRIC = "MoE-layer tokens/s"
+# the headline (decode M = 1) first, then the other workloads the metric is
+# quoted on (M = 16, M = 8192) and the remaining seeded ones
+DEFAULT_WORKLOADS = ["decode_m1", "decode_m16_bias", "prefill_m8192",
+                     "prefill_m8192_zipf_shared", "tiny_m8"]
 UNIT = "tokens/s"
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
@@ -47,7 +54,10 @@ def parse_args():
     p.add_argument("--steps", type=int, default=None)
     p.add_argument("--warmup", type=int, default=None)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--workload", default="decode_m1")
+    p.add_argument("--workloads", default=",".join(DEFAULT_WORKLOADS),
+                   help="comma-separated workloads; the first is the headline line, the "
+                        "others are timed the same way into its \"configs\" map")
+    p.add_argument("--workload", default=None, help="time this one workload only")
     p.add_argument("--tokens", type=int, default=None,
                    help="override the workload's token count (same shapes and seeds)")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -378,18 +388,20 @@ def build_layer(wl, dev, moe, synth):
     return layer
 
 
-def run_gpu(args, wl):
+def _plan_stats(layer):
+    """(touched experts, valid pairs) of the plan in the layer's plan buffer."""
+    import torch
+    h = layer.plan_buf[:64].view(torch.int32).cpu().numpy()
+    return int(h[3]), int(h[5])
+
+
+def time_workload(wl, args, dist, dev, local, ws, rank):
+    """Times one workload under the bench protocol on this rank; returns the
+    per-workload record (rank 0 reads it; other ranks return after the
+    collectives)."""
     import torch
     from nvfp4_weight_mixture_gb300 import moe, synth
 
-    ws, rank, local = dist_info()
-    dist = None
-    if ws > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    moe.load_library()
     decode = wl.M <= moe.DECODE_MAX_TOKENS
     steps = args.steps or (5000 if decode else 300)
     warmup = max(3, args.warmup if args.warmup is not None else 10)
@@ -402,11 +414,18 @@ def run_gpu(args, wl):
     flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
     stream = torch.cuda.Stream(device=dev)
 
-    # warm-up (eager) and graph capture: one graph per token batch
+    # warm-up (eager), the plan statistics of every token batch, graph capture
+    touched, pairs = [], []
     with torch.cuda.stream(stream):
-        for i in range(warmup):
+        for i in range(max(warmup, n_var)):
             layer(xs[i % n_var], ys[i % n_var])
+            if i < n_var:
+                stream.synchronize()
+                a, p_ = _plan_stats(layer)
+                touched.append(a)
+                pairs.append(p_)
     stream.synchronize()
+    n_active, n_valid = statistics.mean(touched), statistics.mean(pairs)
     graphs = []
     for v in range(n_var):
         g = torch.cuda.CUDAGraph()
@@ -456,25 +475,42 @@ def run_gpu(args, wl):
     ms_per_step = total_ms / steps
     value = job_tokens_per_s(ws, wl.M, steps, total_ms)
 
-    # ---- per-kernel durations (traced eager steps, same protocol) ----------------
+    # ---- per-kernel durations inside graph-replayed steps ------------------------
+    # The library records caller events around each of its kernels; captured
+    # into the step's graph they become event nodes, so every kernel is timed
+    # as it runs in the replayed step (same flush protocol).  The event nodes
+    # order the kernels, so a traced step runs without programmatic-launch
+    # overlap: its kernels add up to a little more than the untraced step.
     tr = [torch.cuda.Event(enable_timing=True) for _ in range(8)]
     moe.set_trace_events(tr)
-    kt = {s: [] for s in moe.TRACE_STEPS}
-    n_tr = min(steps, 50)
+    tgraphs = []
+    for v in range(4):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            layer(xs[v], ys[v])
+        tgraphs.append(g)
+    kt = {s_: [] for s_ in moe.TRACE_STEPS}
+    span = []
+    n_tr = min(steps, 100)
     with torch.cuda.stream(stream):
         for i in range(n_tr):
             flush.zero_()
-            layer(xs[i % n_var], ys[i % n_var])
+            tgraphs[i % len(tgraphs)].replay()
             stream.synchronize()
-            for j, s in enumerate(moe.TRACE_STEPS):
-                kt[s].append(tr[2 * j].elapsed_time(tr[2 * j + 1]))
+            for j, s_ in enumerate(moe.TRACE_STEPS):
+                kt[s_].append(tr[2 * j].elapsed_time(tr[2 * j + 1]))
+            span.append(tr[0].elapsed_time(tr[7]))
     moe.set_trace_events(None)
-    kernel_ms = {s: statistics.mean(v) for s, v in kt.items()}
-
-    # plan statistics of the last traced step (read after timing)
-    k_eff = wl.k + int(wl.shared)
-    hdr = layer.plan_buf[:64].view(torch.int32).cpu().numpy()
-    n_active, n_valid = int(hdr[3]), int(hdr[5])
+    del tgraphs
+    kernel_ms = {s_: statistics.mean(v) for s_, v in kt.items()}
+    traced_step_ms = statistics.mean(span)
+    # On the decode path the combine runs inside the W2 kernel, so its record
+    # pair encloses no kernel: that pair's time is the cost of one pair of
+    # event nodes, taken off every traced kernel's duration.
+    event_pair_ms = kernel_ms["combine"] if decode else 0.0
+    kernel_ms_raw = dict(kernel_ms)
+    if decode:
+        kernel_ms = {s_: max(v - event_pair_ms, 0.0) for s_, v in kernel_ms.items()}
     st = int(layer.status.item())
 
     # ---- end to end through the public API: pinned H2D + layer + D2H ------------
@@ -503,15 +539,13 @@ def run_gpu(args, wl):
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in eev), dist, dev)
     e2e_value = job_tokens_per_s(ws, wl.M, steps, e2e_ms)
-
-    if rank != 0:
-        if dist:
-            dist.destroy_process_group()
-        return 0
+    del graphs, layer, xs, ys, flush, xh
+    torch.cuda.empty_cache()
 
     # ---- roofline of the dominant kernel -------------------------------------------
     hbm, tflops, peak_src = load_peaks()
-    dom = max(("w13", "w2", "combine", "plan"), key=lambda s: kernel_ms[s])
+    dom = max(("w13", "w2", "combine", "plan") if not decode else ("w13", "w2", "plan"),
+              key=lambda s_: kernel_ms[s_])
     bound, kb, kf = kernel_accounting(wl, dom, n_active, n_valid, decode)
     dur = kernel_ms[dom] / 1e3
     if bound == "hbm":
@@ -522,8 +556,7 @@ def run_gpu(args, wl):
     lb, lf = layer_accounting(wl, n_active, n_valid)
     step_s = ms_per_step / 1e3
     layer_roof = max(lb / (hbm * 1e9), lf / (tflops * 1e12))
-
-    line = {
+    return {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": steps,
         "warmup": warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
@@ -532,19 +565,52 @@ def run_gpu(args, wl):
                      "frac": achieved / peak, "traffic": traffic, "kernel": dom,
                      "peak_source": f"{peak_src} ({'hbm_gbs' if bound == 'hbm' else 'bf16_tflops'}"
                                     f"{', fp16 = bf16 nominal rate' if bound == 'tensor' else ''})",
+                     "kernel_timing": "event nodes captured in the replayed step graph",
                      "algorithmic": {"bytes": kb, "flops": kf, "kernel_ms": kernel_ms[dom]}},
         "layer": {"algorithmic_bytes": lb, "flops": lf, "touched_experts": n_active,
                   "pairs": n_valid, "roofline_us": layer_roof * 1e6,
                   "frac_of_roofline": layer_roof / step_s,
                   "hbm_gbs_achieved": lb / step_s / 1e9,
+                  "tensor_tflops_achieved": lf / step_s / 1e12,
                   "step_ms_p10_p50_p90": [float(np.percentile(times, q)) for q in (10, 50, 90)],
-                  "kernel_ms_traced": kernel_ms, "status": st},
+                  "kernel_ms_in_graph": kernel_ms, "kernel_ms_in_graph_raw": kernel_ms_raw,
+                  "event_pair_ms": event_pair_ms, "traced_step_ms": traced_step_ms,
+                  "status": st},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": wl.M * wl.H * 2,
                 "d2h_bytes_per_step": wl.M * wl.H * 2},
         "gpu_launches": launches_per_step * steps,
         "clocks": ck,
         "wall_s_timed_region": wall,
     }
+
+
+def run_gpu(args, workloads):
+    """Times every workload (the first is the headline line; the others go
+    into its "configs" map, each measured under the same protocol)."""
+    import torch
+    from nvfp4_weight_mixture_gb300 import moe
+
+    ws, rank, local = dist_info()
+    dist = None
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    moe.load_library()
+    recs = [time_workload(wl, args, dist, dev, local, ws, rank) for wl in workloads]
+    if rank != 0:
+        if dist:
+            dist.destroy_process_group()
+        return 0
+    line = recs[0]
+    if len(recs) > 1:
+        line["configs"] = {}
+        for wl, r in zip(workloads[1:], recs[1:]):
+            line["configs"][wl.name] = {k_: r[k_] for k_ in (
+                "value", "unit", "ms_per_step", "steps", "warmup", "config", "roofline", "layer",
+                "e2e", "gpu_launches", "clocks", "wall_s_timed_region")}
+    wl = workloads[0]
     if ws == 1 and not args.no_cpu_baseline:
         rate, cores, done, el = oracle_sample(wl, args.cpu_seconds)
         line["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle",
@@ -560,14 +626,16 @@ def run_gpu(args, wl):
 def main():
     args = parse_args()
     from nvfp4_weight_mixture_gb300 import synth
-    if args.workload not in synth.WORKLOADS:
-        raise SystemExit(f"unknown workload {args.workload}; one of {list(synth.WORKLOADS)}")
-    wl = synth.WORKLOADS[args.workload]
+    names = [args.workload] if args.workload else args.workloads.split(",")
+    for n in names:
+        if n not in synth.WORKLOADS:
+            raise SystemExit(f"unknown workload {n}; one of {list(synth.WORKLOADS)}")
+    wls = [synth.WORKLOADS[n] for n in names]
     if args.tokens is not None:
-        wl = synth.with_tokens(wl, args.tokens)
+        wls = [synth.with_tokens(w, args.tokens) for w in wls]
     if args.impl == "reference":
-        return run_reference(args, wl)
-    return run_gpu(args, wl)
+        return run_reference(args, wls[0])
+    return run_gpu(args, wls)
 
 
 if __name__ == "__main__":

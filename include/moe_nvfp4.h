@@ -114,21 +114,37 @@ typedef struct moe_nvfp4_weights {
   int32_t reserved; /* must be zero */
 } moe_nvfp4_weights;
 
-/* ABI capability check: returns MOE_NVFP4_ABI_VERSION.  Callers refuse to use
- * a library whose version differs from the header they were built with. */
+/* ABI capability check ("[SM70][Draft] Extend Qwen3.8 DFlash2 concurrency
+ * paths", section "Purpose": a new native route is admitted only after a
+ * native ABI capability check): returns MOE_NVFP4_ABI_VERSION.  Callers
+ * refuse to use a library whose version differs from the header they were
+ * built with.  Host-only; never fails. */
 int32_t moe_nvfp4_abi_version(void);
 
-/* Static text for a return code or a single MOE_ST_* bit; never NULL. */
+/* Static text for a return code or a single MOE_ST_* bit; never NULL ("unknown
+ * code" for anything else).  The codes are the outcomes of the host-side
+ * metadata gates that fail closed ("[Kernel][SM70] Improve Qwen3.8 no-MTP
+ * concurrency", section "Guarded production engine result": the CPU-integer
+ * metadata hardening fails closed for tensor metadata; section "Test Result":
+ * an unsafe launch request is refused rather than run).  Host-only. */
 const char* moe_nvfp4_status_string(int32_t code);
 
 /* Name of the CUDA runtime error behind the calling thread's most recent
  * MOE_ERR_CUDA return (for example "cudaErrorLaunchOutOfResources"), or ""
  * if no call on this thread has returned MOE_ERR_CUDA.  Static text; never
- * NULL. */
+ * NULL.  The detail of one fail-closed outcome (same passages as
+ * moe_nvfp4_status_string).  Host-only. */
 const char* moe_nvfp4_last_cuda_error(void);
 
 /* Sizes, in bytes, of the plan buffer (for moe_nvfp4_plan) and of the
- * forward workspace (for moe_nvfp4_forward) for any M <= max_tokens.
+ * forward workspace (for moe_nvfp4_forward) for any M <= max_tokens: the
+ * workspace gate of the pages ("[SM70][Draft] Extend Qwen3.8 DFlash2
+ * concurrency paths", section "Test Result": routing / workspace / ABI gates;
+ * "[Kernel][SM70] Improve Qwen3.8 no-MTP concurrency", section "Scope and
+ * related PRs": the plan and workspace are sized and owned outside the
+ * kernels, and calls with too small a buffer fail closed).
+ * Returns MOE_ERR_INVALID_ARG / MOE_ERR_SHAPE for a bad cfg or max_tokens
+ * outside [0, 2^20].
  * Host-only arithmetic; also checks that the current device is an sm_103
  * part (MOE_ERR_UNSUPPORTED_DEVICE otherwise) unless `plan_bytes` and
  * `ws_bytes` are both NULL, in which case only `cfg` is validated.
@@ -221,12 +237,16 @@ int32_t moe_nvfp4_forward(const moe_nvfp4_config* cfg, int64_t M, const void* x,
  * workspace is a 4 MiB array inside the library (allocated when the library
  * is loaded and held by every GPU that loads it until the process exits).
  * Calls whose workspace would exceed it (M * k_eff * (2*I + 4*H) bytes plus
- * alignment; e.g. M <= 16 at H 2048, I 512, top-10) return MOE_ERR_WORKSPACE
- * and launch nothing.  The first call on a device looks the array's device
- * address up (cudaGetSymbolAddress) with that device current; make that first
- * call before any stream capture.  All calls share the array and it keeps the
- * last call's contents (nothing in it needs to start at zero), so calls whose
- * GPU work overlaps race: order them on one stream.  Allocates nothing. */
+ * alignment) return MOE_ERR_WORKSPACE and launch nothing.  At H 2048, I 512,
+ * top-10 that admits M <= 16 (the decode kernels); at small layers larger M
+ * fits and runs the grouped kernels (e.g. H 256, I 128, top-2: M <= ~1600).
+ * The first call on a device looks the array's device address up
+ * (cudaGetSymbolAddress) with that device current and keeps it for the life
+ * of the process; make that first call before any stream capture.  A device
+ * reset between calls is not supported.  All calls share the array and it
+ * keeps the last call's contents (nothing in it needs to start at zero), so
+ * calls whose GPU work overlaps race: order them on one stream.  Allocates
+ * nothing. */
 int32_t moe_nvfp4_forward_noalloc(const moe_nvfp4_config* cfg, int64_t M, const void* x,
                                   const void* plan, const moe_nvfp4_weights* w13,
                                   const moe_nvfp4_weights* w2, const moe_nvfp4_weights* shared13,
@@ -241,7 +261,8 @@ int32_t moe_nvfp4_forward_noalloc(const moe_nvfp4_config* cfg, int64_t M, const 
 int32_t moe_nvfp4_dequantize(const uint8_t* q, const uint8_t* s, int64_t n_mats, int64_t rows,
                              int64_t k, int32_t layout, void* out, void* stream);
 
-/* Diagnostic kernel timing.  With `events` non-NULL, every later plan and
+/* Diagnostic kernel timing (no counterpart in the pages: a measurement aid).
+ * With `events` non-NULL, every later plan and
  * forward call records events[2*i] on its stream just before and
  * events[2*i+1] just after step i, for i < n_steps:
  *   i = 0  the whole plan call (router and plan kernels),
@@ -249,10 +270,20 @@ int32_t moe_nvfp4_dequantize(const uint8_t* q, const uint8_t* s, int64_t n_mats,
  *   i = 2  the W2 kernel,
  *   i = 3  the combine kernel.
  * `events` are cudaEvent_t handles created by the caller (with timing
- * enabled).  The records separate the kernels on the stream, so a traced call
+ * enabled).  The records are external event records, so a call captured in
+ * a CUDA graph records them at every replay.  The records separate the kernels on the stream, so a traced call
  * does not overlap its kernels through programmatic dependent launch.  NULL
  * turns tracing off.  Process-wide setting; not thread-safe. */
 int32_t moe_nvfp4_set_trace_events(void* const* events, int32_t n_steps);
+
+/* Diagnostic router selection for M <= 16 (no counterpart in the pages; a test
+ * aid).  mode 0: automatic (one thread-block cluster when the device can
+ * co-schedule it, else the 128-block router); mode 1: always the 128-block
+ * router with arrival tickets, the fallback of devices where a cluster of 8
+ * CTAs cannot be scheduled.  Both give bit-identical ids, weights and plans.
+ * Process-wide; takes effect at the next moe_nvfp4_plan call; not
+ * thread-safe.  Returns MOE_ERR_INVALID_ARG for another mode. */
+int32_t moe_nvfp4_set_small_router(int32_t mode);
 
 #ifdef __cplusplus
 }

@@ -129,9 +129,13 @@ __device__ unsigned long long g_prof[32];
 __device__ unsigned long long g_dbg[20480];
 #endif
 bool trace_on() { return g_trace_events != nullptr; }
+int32_t cuda_error_code(cudaError_t e) { return cuda_status(e); }
 void trace_mark(cudaStream_t stream, int step, bool end) {
   if (!g_trace_events || step >= g_trace_steps) return;
-  cudaEventRecord(static_cast<cudaEvent_t>(g_trace_events[2 * step + (end ? 1 : 0)]), stream);
+  // external: under stream capture the record becomes an event node of the
+  // graph (timed at every replay), not only a cross-stream dependency
+  cudaEventRecordWithFlags(static_cast<cudaEvent_t>(g_trace_events[2 * step + (end ? 1 : 0)]),
+                           stream, cudaEventRecordExternal);
 }
 }  // namespace moe
 
@@ -174,6 +178,12 @@ int32_t moe_nvfp4_set_trace_events(void* const* events, int32_t n_steps) {
   if (events && (n_steps < 1 || n_steps > 4)) return MOE_ERR_INVALID_ARG;
   g_trace_events = events;
   g_trace_steps = events ? n_steps : 0;
+  return MOE_OK;
+}
+
+int32_t moe_nvfp4_set_small_router(int32_t mode) {
+  if (mode != 0 && mode != 1) return MOE_ERR_INVALID_ARG;
+  set_force_small_router(mode == 1);
   return MOE_OK;
 }
 

@@ -315,6 +315,37 @@ __device__ __forceinline__ void dequant8(uint32_t word, uint32_t sc2, uint32_t o
   for (int b = 0; b < 4; ++b) out[b] = hmul2_u32(e2m1x2_to_f16x2((word >> (8 * b)) & 0xFF), sc2);
 }
 
+// Dequantised A fragment of k-step `s` (0..3) of a 16x64 fragment-layout block:
+// q = {row g codes 0-7, row g codes 8-15, row g+8 codes 0-7, row g+8 codes 8-15}
+// of this thread's 16-element run; sg / sg8 the FP16 scale splats.  The
+// m16n8k16 K index 2c + {0, 1} (c = lane % 4) holds element 16c + 4s + {0, 1}
+// of the run and 2c + 8 + {0, 1} element 16c + 4s + {2, 3}; the B operand
+// (token rows) is read in the same K order.
+__device__ __forceinline__ void a_frag(const uint4& q, uint32_t sg, uint32_t sg8, int s,
+                                       uint32_t a[4]) {
+  const uint32_t wg = (s < 2) ? q.x : q.y;
+  const uint32_t wg8 = (s < 2) ? q.z : q.w;
+  const int sh = 16 * (s & 1);
+  a[0] = hmul2_u32(e2m1x2_to_f16x2((wg >> sh) & 0xFF), sg);
+  a[2] = hmul2_u32(e2m1x2_to_f16x2((wg >> (sh + 8)) & 0xFF), sg);
+  a[1] = hmul2_u32(e2m1x2_to_f16x2((wg8 >> sh) & 0xFF), sg8);
+  a[3] = hmul2_u32(e2m1x2_to_f16x2((wg8 >> (sh + 8)) & 0xFF), sg8);
+}
+
+// FP16 scale splats of rows g (sg) and g + 8 (sg8) from their two E4M3 codes
+// (row g in the low byte).
+__device__ __forceinline__ void scale_splats(uint32_t sc16, uint32_t* sg, uint32_t* sg8) {
+  const uint32_t f = e4m3x2_to_f16x2(sc16);
+  *sg = __byte_perm(f, f, 0x1010);
+  *sg8 = __byte_perm(f, f, 0x3232);
+}
+
+// The same from two prepared FP16 scales (row g in the low half).
+__device__ __forceinline__ void scale_splats_f16(uint32_t f, uint32_t* sg, uint32_t* sg8) {
+  *sg = __byte_perm(f, f, 0x1010);
+  *sg8 = __byte_perm(f, f, 0x3232);
+}
+
 // ---- legacy warp MMA (decode GEMV and small router) --------------------------
 __device__ __forceinline__ void mma_16816(float c[4], const uint32_t a[4], uint32_t b0,
                                           uint32_t b1) {

@@ -21,26 +21,6 @@
 
 namespace moe {
 
-// Dequantised A fragment of k-step `s` (0..3) of a 16x64 fragment-layout block:
-// q = {row g codes 0-7, row g codes 8-15, row g+8 codes 0-7, row g+8 codes 8-15}
-// of this thread's 16-element run; sg / sg8 the FP16 scale splats.
-__device__ __forceinline__ void a_frag(const uint4& q, uint32_t sg, uint32_t sg8, int s,
-                                       uint32_t a[4]) {
-  const uint32_t wg = (s < 2) ? q.x : q.y;
-  const uint32_t wg8 = (s < 2) ? q.z : q.w;
-  const int sh = 16 * (s & 1);
-  a[0] = hmul2_u32(e2m1x2_to_f16x2((wg >> sh) & 0xFF), sg);
-  a[2] = hmul2_u32(e2m1x2_to_f16x2((wg >> (sh + 8)) & 0xFF), sg);
-  a[1] = hmul2_u32(e2m1x2_to_f16x2((wg8 >> sh) & 0xFF), sg8);
-  a[3] = hmul2_u32(e2m1x2_to_f16x2((wg8 >> (sh + 8)) & 0xFF), sg8);
-}
-
-__device__ __forceinline__ void scale_splats(uint32_t sc16, uint32_t* sg, uint32_t* sg8) {
-  const uint32_t f = e4m3x2_to_f16x2(sc16);
-  *sg = __byte_perm(f, f, 0x1010);
-  *sg8 = __byte_perm(f, f, 0x3232);
-}
-
 __device__ __forceinline__ uint16_t ldg_u16(const uint8_t* p) {
   return __ldg(reinterpret_cast<const unsigned short*>(p));
 }

@@ -68,6 +68,12 @@ cudaError_t make_fp16_map(CUtensorMap* map, const void* base, uint64_t cols, uin
 cudaError_t make_fp16_map_swz(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows,
                               uint32_t box_cols, uint32_t box_rows, int swizzle_bytes);
 
+// Diagnostic: M <= 16 routes through the 128-block router (router.cu).
+void set_force_small_router(bool on);
+// Records the CUDA error behind a MOE_ERR_CUDA return for
+// moe_nvfp4_last_cuda_error (api.cu) and clears the runtime's sticky error.
+int32_t cuda_error_code(cudaError_t e);
+
 // Diagnostic per-step event records (moe_nvfp4_set_trace_events).
 enum TraceStep { kTracePlan = 0, kTraceW13 = 1, kTraceW2 = 2, kTraceCombine = 3 };
 void trace_mark(cudaStream_t stream, int step, bool end);

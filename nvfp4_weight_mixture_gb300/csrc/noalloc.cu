@@ -32,20 +32,23 @@ void* g_noalloc_ptr[64] = {};
 
 // The device address of g_noalloc_ws on the current device.  The host-side
 // symbol is only a stand-in; the address is looked up once per device, with
-// that device current.
+// that device current, and kept for the life of the process: a device reset
+// (cudaDeviceReset, or a destroyed and re-created primary context) between
+// calls is not supported, as the kept address would then be stale.
 int32_t noalloc_workspace(void** out) {
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
-    cudaGetLastError();
+  const cudaError_t de = cudaGetDevice(&dev);
+  if (de != cudaSuccess) {
+    moe::cuda_error_code(de);
     return MOE_ERR_UNSUPPORTED_DEVICE;
   }
+  if (dev < 0 || dev >= 64) return MOE_ERR_UNSUPPORTED_DEVICE;
   std::lock_guard<std::mutex> lk(g_noalloc_mu);
   if (!g_noalloc_ptr[dev]) {
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_ws) != cudaSuccess || !p) {
-      cudaGetLastError();
-      return MOE_ERR_CUDA;
-    }
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_ws);
+    if (e != cudaSuccess) return moe::cuda_error_code(e);
+    if (!p) return MOE_ERR_CUDA;
     g_noalloc_ptr[dev] = p;
   }
   *out = g_noalloc_ptr[dev];

@@ -1202,6 +1202,10 @@ __global__ void __launch_bounds__(kRcThreads, 1)
 // shared-memory use; written by router_device_init before the device's first
 // launch.
 static int g_cluster_max[64];
+// Diagnostic override (moe_nvfp4_set_small_router): route M <= 16 through the
+// 128-block router even where a cluster could be scheduled.
+static bool g_force_small_router = false;
+void set_force_small_router(bool on) { g_force_small_router = on; }
 
 static int router_cluster_probe() {
   if (cudaFuncSetAttribute(router_cluster_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed,
@@ -1261,7 +1265,8 @@ cudaError_t launch_plan(const LayerDims& d, int64_t M, const __half* x, const __
       route_given_kernel<<<(Mi + 7) / 8, 256, 0, stream>>>(d, Mi, x, w_gate, ids_user, w_user, pv);
       plan_small_kernel<<<1, 256, 0, stream>>>(d, Mi, pv, status);
     } else {
-      const int cmax = (dev >= 0 && dev < 64) ? g_cluster_max[dev] : 0;
+      const int cmax =
+          (dev >= 0 && dev < 64 && !g_force_small_router) ? g_cluster_max[dev] : 0;
       const RouterClusterPlan L = router_cluster_plan(d.H, d.E, d.k, Mi, cmax > 0 ? cmax : 1);
       if (cmax > 0 && L.stages >= 1 && L.total <= kRcSmemBudget) {
         CUtensorMap wrmap;

@@ -37,7 +37,7 @@ DECODE_MAX_TOKENS = 16
 EXPORTS = ["moe_nvfp4_abi_version", "moe_nvfp4_status_string", "moe_nvfp4_query",
            "moe_nvfp4_quantize", "moe_nvfp4_plan", "moe_nvfp4_forward", "moe_nvfp4_dequantize",
            "moe_nvfp4_set_trace_events", "moe_nvfp4_forward_noalloc",
-           "moe_nvfp4_last_cuda_error"]
+           "moe_nvfp4_last_cuda_error", "moe_nvfp4_set_small_router"]
 TRACE_STEPS = ("plan", "w13", "w2", "combine")
 
 
@@ -95,6 +95,8 @@ def load_library(path: str = LIB_PATH):
         lib.moe_nvfp4_forward_noalloc.restype = I32
         lib.moe_nvfp4_set_trace_events.argtypes = [P, I32]
         lib.moe_nvfp4_set_trace_events.restype = I32
+        lib.moe_nvfp4_set_small_router.argtypes = [I32]
+        lib.moe_nvfp4_set_small_router.restype = I32
         v = lib.moe_nvfp4_abi_version()
         if v != ABI_VERSION:
             raise RuntimeError(f"libmoe_nvfp4 ABI version {v}, binding expects {ABI_VERSION}")
@@ -237,6 +239,13 @@ def set_trace_events(events):
     arr = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
     _trace_keep = (arr, events)
     _check("moe_nvfp4_set_trace_events", lib.moe_nvfp4_set_trace_events(arr, len(events) // 2))
+
+
+def set_small_router(force_ticket_router: bool):
+    """Diagnostic: route M <= 16 through the 128-block ticket router (True) or
+    choose automatically (False; the thread-block cluster where it fits)."""
+    _check("moe_nvfp4_set_small_router",
+           load_library().moe_nvfp4_set_small_router(1 if force_ticket_router else 0))
 
 
 # ---- quantise / dequantise ---------------------------------------------------------

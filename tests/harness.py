@@ -160,6 +160,8 @@ class Case:
 TILE_ROWS = 192
 PLAN_CHUNK = 2048
 DECODE_MAX_TOKENS = 16
+DTAB_INTS = 20
+DTAB_ENTRIES = DECODE_MAX_TOKENS * 33
 
 
 def _align(v, a=256):
@@ -192,7 +194,31 @@ def decode_plan(buf, M, k_eff, e_eff, E, H):
     perm = take(4 * Pc, np.int32, P)
     inv = take(4 * Pc, np.int32, P)
     tiles = take(16 * max_tiles, np.int32, 4 * max_tiles).reshape(-1, 4)
+    n_chunks = (Pc + PLAN_CHUNK - 1) // PLAN_CHUNK
+    take(4 * n_chunks * e_eff, np.int32, 0)                      # chunk histograms
+    take(4 * Pc, np.int32, 0)                                     # ranks
+    take(4 * ((H + 127) // 128) * DECODE_MAX_TOKENS * E, np.float32, 0)  # router partials
+    take(4 * DECODE_MAX_TOKENS * E, np.float32, 0)                # router logits
+    dtab = take(4 * DTAB_ENTRIES * DTAB_INTS, np.int32,
+                DTAB_ENTRIES * DTAB_INTS).reshape(DTAB_ENTRIES, DTAB_INTS)
     n_valid, n_active, n_tiles = int(hdr[5]), int(hdr[3]), int(hdr[4])
     return dict(hdr=hdr, ids=ids, w=w, counts=counts, offsets=offsets,
                 active=active[:n_active], perm=perm[:n_valid], inv=inv,
-                tiles=tiles[:n_tiles, :3])
+                tiles=tiles[:n_tiles, :3], dtab=dtab)
+
+
+def expected_work_table(ref, M, k_eff, e_eff):
+    """The decode work table an oracle plan implies (M <= 16): one entry per
+    active expert in ascending order, (expert, first plan position, rows, -1,
+    the pair ids of its first 16 rows, -1 past them); entries from n_active to
+    min(M * k_eff, e_eff) all -1.  Restated from the table's definition."""
+    P = M * k_eff
+    max_active = min(P, e_eff)
+    out = np.full((max_active, DTAB_INTS), -1, np.int32)
+    active = np.nonzero(ref["counts"])[0]
+    for a, e in enumerate(active):
+        off, cnt = int(ref["offsets"][e]), int(ref["counts"][e])
+        out[a, 0], out[a, 1], out[a, 2] = e, off, cnt
+        n = min(cnt, DTAB_INTS - 4)
+        out[a, 4:4 + n] = ref["perm"][off:off + n]
+    return out

@@ -157,3 +157,11 @@ def test_binding_checks_sizes_the_abi_cannot_see():
     assert moe.dequantize_arg_errors(q, s, 2, 256, 64) == []
     assert moe.dequantize_arg_errors(q[:-1], s, 2, 256, 64)[0].startswith("q")
     assert moe.dequantize_arg_errors(q, s, 2, 256, 128)[0].startswith("q")
+
+
+def test_small_router_switch_validates_mode(lib):
+    """The diagnostic router switch accepts modes 0 and 1 only (host-only)."""
+    assert lib.moe_nvfp4_set_small_router(2) == -1
+    assert lib.moe_nvfp4_set_small_router(-1) == -1
+    assert lib.moe_nvfp4_set_small_router(1) == 0
+    assert lib.moe_nvfp4_set_small_router(0) == 0

@@ -129,3 +129,46 @@ def test_e4m3_encode_brute_force_and_torch():
         else:
             assert got == 0x7E
     assert oracle.e4m3_encode(np.float32(-1.0)) == 0xB8
+
+
+# ---- oracle_dequant (canonical rows -> FP16) ---------------------------------------
+
+def _dequant_golden(golden_dir):
+    rows = parse_golden(os.path.join(golden_dir, "dequant_worked_rows.txt"))
+    q, s, y = {}, {}, {}
+    for r in rows:
+        vals = [int(t, 16) for t in r[2:]]
+        {"q": q, "s": s, "y": y}[r[0]][int(r[1])] = vals
+    n = len(q)
+    return (np.array([q[i] for i in range(n)], np.uint8), np.array([s[i] for i in range(n)], np.uint8),
+            np.array([y[i] for i in range(n)], np.uint16))
+
+
+def test_dequant_worked_rows(golden_dir):
+    """Hand-worked rows fix the nibble order (element 2i in the low nibble),
+    the scale index (element c uses scale c // 16) and the zero signs."""
+    q, s, y = _dequant_golden(golden_dir)
+    assert q.shape == (2, 16) and s.shape == (2, 2) and y.shape == (2, 32)
+    got = oracle.dequant(q, s).view(np.uint16)
+    np.testing.assert_array_equal(got, y)
+
+
+def test_dequant_matches_library_decode():
+    """Random canonical rows (every code and every finite scale) against the
+    test-side decode built from torch's float8_e4m3fn and the E2M1 closed
+    form; both are exact in FP16, so the bit patterns (zero signs included)
+    must agree."""
+    from helpers import dequant_np
+    rng = np.random.default_rng(7)
+    rows, k = 64, 256
+    q = rng.integers(0, 256, (rows, k // 2), dtype=np.uint8)
+    finite = np.array([c for c in range(256) if c not in (0x7F, 0xFF)], np.uint8)
+    s = finite[rng.integers(0, len(finite), (rows, k // 16))]
+    s[0, :len(finite) // 16] = finite[:len(finite) // 16]     # a run of distinct scales
+    got = oracle.dequant(q, s)
+    ref = dequant_np(q, s).astype(np.float16)
+    np.testing.assert_array_equal(got.view(np.uint16), ref.view(np.uint16))
+    # 3-D input (matrices x rows) keeps its leading shape
+    got3 = oracle.dequant(q.reshape(4, 16, k // 2), s.reshape(4, 16, k // 16))
+    assert got3.shape == (4, 16, k)
+    np.testing.assert_array_equal(got3.reshape(rows, k).view(np.uint16), ref.view(np.uint16))
