@@ -81,6 +81,12 @@ def _load():
         lib.oracle_forward.restype = ctypes.c_uint32
         lib.oracle_dense.argtypes = [I64, I64, I64, P, P, P, ctypes.c_float, P]
         lib.oracle_dense.restype = None
+        lib.oracle_prepare_scales.argtypes = [P, I64, P]
+        lib.oracle_prepare_scales.restype = ctypes.c_uint32
+        lib.oracle_fp8_quantize.argtypes = [P, I64, I64, P, P]
+        lib.oracle_fp8_quantize.restype = ctypes.c_uint32
+        lib.oracle_fp8_dense.argtypes = [I64, I64, I64, P, P, P, P]
+        lib.oracle_fp8_dense.restype = None
         _lib = lib
         return lib
 
@@ -262,4 +268,39 @@ def dense(x, q, s, g):
         raise ValueError("dense: q must be [N, K/2] and s [N, K/16]")
     y = np.empty((M, N), np.uint16)
     _load().oracle_dense(M, N, K, _p(x), _p(q), _p(s), float(g), _p(y))
+    return y.view(np.float16)
+
+
+def prepare_scales(s):
+    """E4M3 scale bytes -> FP16 bit patterns of their values, same shape
+    (the prepared-scale storage); returns (uint16 array, status)."""
+    s = _c(s, np.uint8)
+    out = np.empty(s.shape, np.uint16)
+    st = _load().oracle_prepare_scales(_p(s), s.size, _p(out))
+    return out, int(st)
+
+
+def fp8_quantize(w):
+    """FP32 [rows, k] -> (q [rows, k] E4M3 codes, cs [rows] FP32, status):
+    channel-FP8 (QPN8) weights."""
+    w = _c(w, np.float32)
+    rows, k = w.shape
+    q = np.empty((rows, k), np.uint8)
+    cs = np.empty((rows,), np.float32)
+    st = _load().oracle_fp8_quantize(_p(w), rows, k, _p(q), _p(cs))
+    return q, cs, int(st)
+
+
+def fp8_dense(x, q, cs):
+    """Dense channel-FP8 projection y = fp16(cs * x . E4M3(q)^T) of FP16 rows
+    x [M, K] with q [N, K] E4M3 codes and channel scales cs [N]."""
+    x = _f16bits(x)
+    M, K = x.shape
+    q = _c(q, np.uint8)
+    cs = _c(cs, np.float32)
+    N = q.shape[0]
+    if q.shape != (N, K) or cs.shape != (N,):
+        raise ValueError("fp8_dense: q must be [N, K] and cs [N]")
+    y = np.empty((M, N), np.uint16)
+    _load().oracle_fp8_dense(M, N, K, _p(x), _p(q), _p(cs), _p(y))
     return y.view(np.float16)

@@ -591,4 +591,103 @@ void oracle_dense(int64_t M, int64_t N, int64_t K, const uint16_t *x, const uint
     }
 }
 
+/* ------------------------------------------------------------------------ */
+/* Prepared-scale storage ("[Kernel][SM70] Improve Qwen3.8 no-MTP           */
+/* concurrency", sections "Purpose" and "Scope and related PRs": the        */
+/* prepared arm stores effective decode scales instead of raw E4M3 bytes;   */
+/* "Test Result": raw and prepared outputs are bitwise equal).              */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * out[i] = the FP16 bit pattern of E4M3(s[i]), for i < n, in the same order
+ * (READING: the prepared scale is the raw scale's value widened to the FP16
+ * operand type of the GEMM, exact since every finite E4M3 value is an FP16
+ * value; the global scale stays on the FP32 accumulator).  NaN codes give the
+ * FP16 NaN 0x7E00 and set ORACLE_ST_NONFINITE.
+ */
+uint32_t oracle_prepare_scales(const uint8_t *s, int64_t n, uint16_t *out)
+{
+    uint32_t status = 0;
+    for (int64_t i = 0; i < n; ++i) {
+        double v = oracle_e4m3_value(s[i]);
+        if (isnan(v)) {
+            out[i] = 0x7E00;
+            status |= ORACLE_ST_NONFINITE;
+        } else {
+            out[i] = oracle_f16_from_double(v);
+        }
+    }
+    return status;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Channel-FP8 weights (QPN8: "[SM70][Draft] Extend Qwen3.8 DFlash2         */
+/* concurrency paths", section "Follow-up: exact channel-FP8 QPN8           */
+/* concurrency paths and endpoint evidence").                               */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * w  : rows x k FP32, row-major (row = output channel).
+ * q  : rows x k E4M3 codes, row-major (canonical: one byte per element).
+ * cs : rows FP32 channel scales.
+ * READING: the pages name FP8 weights with one scale per output channel but
+ * print no recipe; the plainest one, with every step one correctly rounded
+ * FP32 operation, is
+ *   cs_r = amax(row r) / 448          (cs_r = 1 when the row is all zero)
+ *   q    = E4M3_rne_satfinite(x / cs_r)
+ * so that the row's largest magnitude maps to the largest E4M3 value.  NaN or
+ * infinite input sets ORACLE_ST_NONFINITE and is quantised as zero.
+ */
+uint32_t oracle_fp8_quantize(const float *w, int64_t rows, int64_t k, uint8_t *q, float *cs)
+{
+    uint32_t status = 0;
+    for (int64_t r = 0; r < rows; ++r) {
+        const float *wr = w + r * k;
+        float amax = 0.0f;
+        for (int64_t i = 0; i < k; ++i) {
+            if (!isfinite(wr[i])) {
+                status |= ORACLE_ST_NONFINITE;
+                continue;
+            }
+            float a = fabsf(wr[i]);
+            if (a > amax)
+                amax = a;
+        }
+        volatile float c = amax / 448.0f;
+        if (amax == 0.0f)
+            c = 1.0f;
+        cs[r] = c;
+        for (int64_t i = 0; i < k; ++i) {
+            float v = isfinite(wr[i]) ? wr[i] : 0.0f;
+            volatile float z = v / c;
+            q[r * k + i] = (uint8_t)oracle_e4m3_encode(z);
+        }
+    }
+    return status;
+}
+
+/*
+ * Dense channel-FP8 projection of a few FP16 rows:
+ *   y[m][n] = fp16( cs[n] * sum_K x[m][K] * E4M3(q[n][K]) )
+ * accumulated in FP64, one rounding to FP16.  READING: the channel scale
+ * multiplies the accumulated dot product (the pages only say that where the
+ * scale is applied changes the FP32 result; any exact placement gives the
+ * same real value, which is what the oracle computes).  x [M][K] and y
+ * [M][N] are FP16 bits, q [N][K] canonical, cs [N].  Rows are independent.
+ */
+void oracle_fp8_dense(int64_t M, int64_t N, int64_t K, const uint16_t *x, const uint8_t *q,
+                      const float *cs, uint16_t *y)
+{
+    init_tabs();
+#pragma omp parallel for schedule(static)
+    for (int64_t n = 0; n < N; ++n) {
+        for (int64_t m = 0; m < M; ++m) {
+            double acc = 0.0;
+            for (int64_t c = 0; c < K; ++c)
+                acc += oracle_f16_to_double(x[m * K + c]) * e4m3_tab[q[n * K + c]];
+            y[m * N + n] = oracle_f16_from_double(acc * (double)cs[n]);
+        }
+    }
+}
+
 int oracle_abi_version(void) { return 1; }
