@@ -88,11 +88,28 @@ extern "C" {
  *   fragment layout of the row-permuted matrix whose tile 2j is gate rows
  *   [16j, 16j+16) and tile 2j+1 is up rows [I+16j, I+16j+16).
  *
- * moe_nvfp4_forward needs W13 in layout 2 and W2 in layout 1.
+ * MOE_LAYOUT_FP8_FRAGMENT (3): channel-FP8 weights (moe_fp8_quantize,
+ *   moe_fp8_dense), one E4M3 code per byte, rows % 256 == 0, k % 64 == 0.
+ *   Tile rt, segment ks owns the 1024-byte block number
+ *       b = (G * k/64 + ks) * 16 + j      (G = rt / 16, j = rt % 16)
+ *   at byte 1024 * b; for L = 4*g + c, bytes [16L, 16L+16) are row 16*rt+g,
+ *   elements [64*ks+16*c, +16) in ascending order, and bytes [512+16L,
+ *   512+16L+16) the same elements of row 16*rt+g+8.  The canonical FP8 layout
+ *   is [rows][k], one byte per element.
+ *
+ * MOE_SCALES_PREPARED (0x100, OR-ed into moe_nvfp4_weights.layout): `s` holds
+ *   prepared scales (moe_nvfp4_prepare_scales): each E4M3 scale byte widened
+ *   to the 2-byte FP16 bit pattern of its value, in the same order, so the
+ *   scale array is twice as large.  Results are bitwise equal to raw scales.
+ *
+ * moe_nvfp4_forward needs W13 in layout 2 and W2 in layout 1 (either may add
+ * MOE_SCALES_PREPARED); moe_nvfp4_dense needs layout 1 (+ prepared).
  */
 #define MOE_LAYOUT_CANONICAL 0
 #define MOE_LAYOUT_FRAGMENT 1
 #define MOE_LAYOUT_FRAGMENT_W13 2
+#define MOE_LAYOUT_FP8_FRAGMENT 3
+#define MOE_SCALES_PREPARED 0x100
 
 typedef struct moe_nvfp4_config {
   int32_t hidden;       /* H: model width; H % 256 == 0, 256 <= H <= 4096 */
@@ -275,6 +292,74 @@ int32_t moe_nvfp4_dequantize(const uint8_t* q, const uint8_t* s, int64_t n_mats,
  * does not overlap its kernels through programmatic dependent launch.  NULL
  * turns tracing off.  Process-wide setting; not thread-safe. */
 int32_t moe_nvfp4_set_trace_events(void* const* events, int32_t n_steps);
+
+/* ---- dense few-row projections (M <= 32) ------------------------------------
+ *
+ * The QPN2 / QPN8 projections of "[SM70][Draft] Extend Qwen3.8 DFlash2
+ * concurrency paths" (section "Purpose": NVFP4 QPN2 in independent
+ * eight-row tiles, admitted through M <= 32; section "TP4-only NVFP4 verifier
+ * follow-up": split-K with the FP32 reduction order preserved, M9 / M15 / M16
+ * bitwise equal to concatenated M8 calls; section "Follow-up: exact
+ * channel-FP8 QPN8 concurrency paths": the same over FP8 weights with one
+ * scale per output channel):
+ *
+ *   y[m][n] = fp16( scale_n * sum_k x[m][k] * w16[n][k] )
+ *
+ * with FP32 accumulation.  Every output row is computed by the same
+ * operations whatever M is, so a call's rows are bitwise equal to the same
+ * rows computed in any other batch.  Shapes: 0 <= M <= 32 (M == 0 returns
+ * MOE_OK and touches nothing), N % 256 == 0 with 256 <= N <= 65536, K % 64 == 0
+ * with 64 <= K <= 65536; anything else MOE_ERR_SHAPE (larger M belongs to a
+ * GEMM, not to this weight-streaming path).  x is FP16 [M][K] and y FP16
+ * [M][N], row-major, device, 16-byte aligned. */
+
+/* Workspace bytes a dense call of this shape needs (0 when it needs none).
+ * Host-only; MOE_ERR_SHAPE as above, MOE_ERR_INVALID_ARG for a NULL out. */
+int32_t moe_nvfp4_dense_query(int64_t M, int64_t N, int64_t K, size_t* ws_bytes);
+
+/* NVFP4 dense projection (QPN2).  w: one N x K matrix in MOE_LAYOUT_FRAGMENT
+ * (optionally | MOE_SCALES_PREPARED), w->g one FP32 global scale (scale_n =
+ * g for all n).  ws: device workspace of at least moe_nvfp4_dense_query bytes
+ * (may be NULL when that is 0), borrowed for the call's stream work; it
+ * holds arrival counters and must be zero-filled before its first use (the
+ * library leaves the counters at zero after every call that completes; after
+ * a MOE_ST_TIMEOUT zero it again).  Dense calls on one workspace must not
+ * overlap on the GPU.  Returns
+ * MOE_ERR_LAYOUT for another layout, MOE_ERR_WORKSPACE for a short ws,
+ * MOE_ERR_ALIGNMENT / MOE_ERR_INVALID_ARG as usual.  Bounded device waits set
+ * MOE_ST_TIMEOUT in *status if they give up. */
+int32_t moe_nvfp4_dense(int64_t M, int64_t N, int64_t K, const void* x,
+                        const moe_nvfp4_weights* w, void* y, void* ws, size_t ws_bytes,
+                        uint32_t* status, void* stream);
+
+/* Channel-FP8 quantiser (the load-time step of QPN8, same section).  w:
+ * device FP32 [rows][k]; q: device out, rows * k E4M3 codes in `layout`
+ * (MOE_LAYOUT_CANONICAL: [rows][k]; MOE_LAYOUT_FP8_FRAGMENT: as above);
+ * channel_scale: device out FP32 [rows].  Per row, every step one correctly
+ * rounded FP32 operation: cs = amax / 448 (1 for an all-zero row),
+ * q = E4M3_rne_satfinite(x / cs).  NaN or infinite input is quantised as zero
+ * and sets MOE_ST_NONFINITE.  Requires k % 64 == 0 (64 <= k <= 65536),
+ * rows % 16 == 0 (rows % 256 == 0 for the fragment layout). */
+int32_t moe_fp8_quantize(const float* w, int64_t rows, int64_t k, int32_t layout, uint8_t* q,
+                         float* channel_scale, uint32_t* status, void* stream);
+
+/* Channel-FP8 dense projection (QPN8): q is N x K in MOE_LAYOUT_FP8_FRAGMENT,
+ * channel_scale FP32 [N] (scale_n), applied to the FP32 sum.  Otherwise as
+ * moe_nvfp4_dense. */
+int32_t moe_fp8_dense(int64_t M, int64_t N, int64_t K, const void* x, const uint8_t* q,
+                      const float* channel_scale, void* y, void* ws, size_t ws_bytes,
+                      uint32_t* status, void* stream);
+
+/* Prepared-scale storage ("[Kernel][SM70] Improve Qwen3.8 no-MTP
+ * concurrency", sections "Purpose" and "Scope and related PRs": prepared
+ * effective decode scales beside raw E4M3 scale residency; section "Test
+ * Result": raw and prepared outputs bitwise equal).  s16[i] = the FP16 bit
+ * pattern of E4M3 code s[i], for i < n, in the same order (any layout).  The
+ * NaN codes 0x7F / 0xFF give 0x7E00 and set MOE_ST_NONFINITE.  s: device n
+ * bytes; s16: device out, 2n bytes; both 16-byte aligned.  n == 0 returns
+ * MOE_OK. */
+int32_t moe_nvfp4_prepare_scales(const uint8_t* s, int64_t n, void* s16, uint32_t* status,
+                                 void* stream);
 
 /* Diagnostic router selection for M <= 16 (no counterpart in the pages; a test
  * aid).  mode 0: automatic (one thread-block cluster when the device can

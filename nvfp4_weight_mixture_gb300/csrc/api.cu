@@ -58,6 +58,7 @@ int32_t current_device(int* num_sms) {
     cudaError_t e = router_device_init(dev);
     if (e == cudaSuccess) e = prefill_device_init();
     if (e == cudaSuccess) e = decode_device_init();
+    if (e == cudaSuccess) e = dense_device_init();
     if (e != cudaSuccess) {
       g_last_cuda_error = e;
       cudaGetLastError();
@@ -337,6 +338,94 @@ int32_t moe_nvfp4_forward(const moe_nvfp4_config* cfg, int64_t M, const void* x,
     e = launch_prefill_forward(d, M, static_cast<const __half*>(x), pv, W13, W2, S13, S2,
                                static_cast<__half*>(y), h, partial, status, st, sms);
   return cuda_status(e);
+}
+
+// ---- dense few-row projections, channel-FP8 weights, prepared scales ----
+
+static int32_t check_dense_shape(int64_t M, int64_t N, int64_t K) {
+  if (M < 0 || M > kDenseMaxTokens) return MOE_ERR_SHAPE;
+  if (N < 256 || N > 65536 || N % 256) return MOE_ERR_SHAPE;
+  if (K < 64 || K > 65536 || K % 64) return MOE_ERR_SHAPE;
+  return MOE_OK;
+}
+
+int32_t moe_nvfp4_dense_query(int64_t M, int64_t N, int64_t K, size_t* ws_bytes) {
+  int32_t rc = check_dense_shape(M, N, K);
+  if (rc) return rc;
+  if (!ws_bytes) return MOE_ERR_INVALID_ARG;
+  *ws_bytes = dense_ws_bytes(M, N, K);
+  return MOE_OK;
+}
+
+static int32_t dense_common(int fmt, int64_t M, int64_t N, int64_t K, const void* x,
+                            const uint8_t* q, const uint8_t* s, const float* scale, void* y,
+                            void* ws, size_t ws_bytes, uint32_t* status, void* stream) {
+  int32_t rc = check_dense_shape(M, N, K);
+  if (rc) return rc;
+  if (M == 0) return MOE_OK;
+  if (!x || !q || !scale || !y || (fmt != kDenseFp8 && !s)) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(q) || !aligned16(y) || (s && !aligned16(s)) ||
+      !aligned16(scale))
+    return MOE_ERR_ALIGNMENT;
+  if (status && (reinterpret_cast<uintptr_t>(status) & 3u)) return MOE_ERR_ALIGNMENT;
+  const size_t need = dense_ws_bytes(M, N, K);
+  if (need > 0 && (!ws || ws_bytes < need)) return MOE_ERR_WORKSPACE;
+  if (ws && !aligned16(ws)) return MOE_ERR_ALIGNMENT;
+  int sms = 0;
+  rc = current_device(&sms);
+  if (rc) return rc;
+  return cuda_status(launch_dense(fmt, M, N, K, static_cast<const __half*>(x), q, s, scale, ws,
+                                  static_cast<__half*>(y), status,
+                                  static_cast<cudaStream_t>(stream)));
+}
+
+int32_t moe_nvfp4_dense(int64_t M, int64_t N, int64_t K, const void* x,
+                        const moe_nvfp4_weights* w, void* y, void* ws, size_t ws_bytes,
+                        uint32_t* status, void* stream) {
+  if (!w || w->reserved) return MOE_ERR_INVALID_ARG;
+  const int base = w->layout & ~MOE_SCALES_PREPARED;
+  if (base != MOE_LAYOUT_FRAGMENT || (w->layout & ~(MOE_LAYOUT_FRAGMENT | MOE_SCALES_PREPARED)))
+    return MOE_ERR_LAYOUT;
+  const int fmt = (w->layout & MOE_SCALES_PREPARED) ? kDenseNvfp4Prepared : kDenseNvfp4;
+  return dense_common(fmt, M, N, K, x, w->q, w->s, w->g, y, ws, ws_bytes, status, stream);
+}
+
+int32_t moe_fp8_dense(int64_t M, int64_t N, int64_t K, const void* x, const uint8_t* q,
+                      const float* channel_scale, void* y, void* ws, size_t ws_bytes,
+                      uint32_t* status, void* stream) {
+  return dense_common(kDenseFp8, M, N, K, x, q, nullptr, channel_scale, y, ws, ws_bytes, status,
+                      stream);
+}
+
+int32_t moe_fp8_quantize(const float* w, int64_t rows, int64_t k, int32_t layout, uint8_t* q,
+                         float* channel_scale, uint32_t* status, void* stream) {
+  if (!w || !q || !channel_scale) return MOE_ERR_INVALID_ARG;
+  if (layout != MOE_LAYOUT_CANONICAL && layout != MOE_LAYOUT_FP8_FRAGMENT) return MOE_ERR_LAYOUT;
+  if (rows < 1 || rows > (int64_t(1) << 24) || k < 64 || k > 65536 || k % 64)
+    return MOE_ERR_SHAPE;
+  if (layout == MOE_LAYOUT_FP8_FRAGMENT ? rows % 256 != 0 : rows % 16 != 0) return MOE_ERR_SHAPE;
+  if (!aligned16(w) || !aligned16(q) || (reinterpret_cast<uintptr_t>(channel_scale) & 3u))
+    return MOE_ERR_ALIGNMENT;
+  if (status && (reinterpret_cast<uintptr_t>(status) & 3u)) return MOE_ERR_ALIGNMENT;
+  int sms = 0;
+  int32_t rc = current_device(&sms);
+  if (rc) return rc;
+  return cuda_status(launch_fp8_quantize(w, rows, k, layout, q, channel_scale, status,
+                                         static_cast<cudaStream_t>(stream)));
+}
+
+int32_t moe_nvfp4_prepare_scales(const uint8_t* s, int64_t n, void* s16, uint32_t* status,
+                                 void* stream) {
+  if (n < 0 || n > (int64_t(1) << 40)) return MOE_ERR_SHAPE;
+  if (n == 0) return MOE_OK;
+  if (!s || !s16) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(s) || !aligned16(s16)) return MOE_ERR_ALIGNMENT;
+  if (status && (reinterpret_cast<uintptr_t>(status) & 3u)) return MOE_ERR_ALIGNMENT;
+  int sms = 0;
+  int32_t rc = current_device(&sms);
+  if (rc) return rc;
+  return cuda_status(launch_prepare_scales(s, n, static_cast<uint16_t*>(s16), status,
+                                           static_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"

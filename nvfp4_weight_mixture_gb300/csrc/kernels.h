@@ -63,10 +63,32 @@ cudaError_t make_rows_map(CUtensorMap* map, const void* base, uint64_t row_bytes
 // optionally 128-byte swizzled (tma.cu).
 cudaError_t make_fp16_map(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows,
                           uint32_t box_cols, uint32_t box_rows, bool swizzle128);
+// FP16 matrix rows x cols as 64-element K segments: box of box_segs
+// consecutive segments of box_rows rows, each a 128-byte-swizzled tile (tma.cu).
+cudaError_t make_fp16_segments_map(CUtensorMap* map, const void* base, uint64_t cols,
+                                   uint64_t rows, uint32_t box_rows, uint32_t box_segs);
 // The same with a swizzle of 0 (none), 32, 64 or 128 bytes; a swizzled box is
 // exactly one swizzle span wide (box_cols * 2 == swizzle_bytes).
 cudaError_t make_fp16_map_swz(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows,
                               uint32_t box_cols, uint32_t box_rows, int swizzle_bytes);
+
+// Dense few-row projection (dense.cu): weight formats, K split, launchers.
+enum DenseFormat { kDenseNvfp4 = 0, kDenseNvfp4Prepared = 1, kDenseFp8 = 2 };
+constexpr int kDenseMaxTokens = 32;
+struct DenseSplit {
+  int blocks;  // grid: equal contiguous ranges of the (group, K segment) pairs
+  int pieces;  // groups one block's range can touch
+};
+DenseSplit dense_split(int N, int K);
+size_t dense_ws_bytes(int64_t M, int64_t N, int64_t K);
+cudaError_t launch_dense(int fmt, int64_t M, int64_t N, int64_t K, const __half* x,
+                         const uint8_t* q, const uint8_t* s, const float* scale, void* ws,
+                         __half* y, uint32_t* status, cudaStream_t stream);
+cudaError_t launch_fp8_quantize(const float* w, int64_t rows, int64_t k, int layout, uint8_t* q,
+                                float* cs, uint32_t* status, cudaStream_t stream);
+cudaError_t launch_prepare_scales(const uint8_t* s, int64_t n, uint16_t* out, uint32_t* status,
+                                  cudaStream_t stream);
+cudaError_t dense_device_init();
 
 // Diagnostic: M <= 16 routes through the 128-block router (router.cu).
 void set_force_small_router(bool on);

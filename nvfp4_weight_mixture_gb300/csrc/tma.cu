@@ -77,6 +77,30 @@ cudaError_t make_fp16_map(CUtensorMap* map, const void* base, uint64_t cols, uin
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// FP16 matrix of `rows` x `cols` (cols % 64 == 0) seen as 64-element segments:
+// dimensions (64 elements, rows, cols / 64) with strides (2 cols, 128) bytes,
+// so that one box of 64 x box_rows x box_segs lands as box_segs consecutive K
+// segments, each a tile of box_rows rows of 128 bytes (row r of segment c at
+// row c * box_rows + r of the box, 128-byte swizzled).  Rows and segments
+// past the end read as zeros.
+cudaError_t make_fp16_segments_map(CUtensorMap* map, const void* base, uint64_t cols,
+                                   uint64_t rows, uint32_t box_rows, uint32_t box_segs) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return cudaErrorNotSupported;
+  if ((reinterpret_cast<uintptr_t>(base) & 15u) || (cols % 64) || box_rows > 256 ||
+      box_rows == 0 || box_segs == 0 || box_segs > 256)
+    return cudaErrorInvalidValue;
+  const cuuint64_t dims[3] = {64, rows, cols / 64};
+  const cuuint64_t strides[2] = {cols * 2, 128};
+  const cuuint32_t box[3] = {64, box_rows, box_segs};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 cudaError_t make_fp16_map_swz(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows,
                               uint32_t box_cols, uint32_t box_rows, int swizzle_bytes) {
   EncodeTiledFn fn = encode_fn();

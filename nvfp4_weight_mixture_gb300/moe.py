@@ -32,12 +32,17 @@ FLAG_SHARED = 0x2
 LAYOUT_CANONICAL = 0
 LAYOUT_FRAGMENT = 1
 LAYOUT_FRAGMENT_W13 = 2
+LAYOUT_FP8_FRAGMENT = 3
+SCALES_PREPARED = 0x100
+DENSE_MAX_TOKENS = 32
 DECODE_MAX_TOKENS = 16
 
 EXPORTS = ["moe_nvfp4_abi_version", "moe_nvfp4_status_string", "moe_nvfp4_query",
            "moe_nvfp4_quantize", "moe_nvfp4_plan", "moe_nvfp4_forward", "moe_nvfp4_dequantize",
            "moe_nvfp4_set_trace_events", "moe_nvfp4_forward_noalloc",
-           "moe_nvfp4_last_cuda_error", "moe_nvfp4_set_small_router"]
+           "moe_nvfp4_last_cuda_error", "moe_nvfp4_set_small_router",
+           "moe_nvfp4_dense_query", "moe_nvfp4_dense", "moe_fp8_quantize", "moe_fp8_dense",
+           "moe_nvfp4_prepare_scales"]
 TRACE_STEPS = ("plan", "w13", "w2", "combine")
 
 
@@ -97,6 +102,16 @@ def load_library(path: str = LIB_PATH):
         lib.moe_nvfp4_set_trace_events.restype = I32
         lib.moe_nvfp4_set_small_router.argtypes = [I32]
         lib.moe_nvfp4_set_small_router.restype = I32
+        lib.moe_nvfp4_dense_query.argtypes = [I64, I64, I64, ctypes.POINTER(SZ)]
+        lib.moe_nvfp4_dense_query.restype = I32
+        lib.moe_nvfp4_dense.argtypes = [I64, I64, I64, P, P, P, P, SZ, P, P]
+        lib.moe_nvfp4_dense.restype = I32
+        lib.moe_fp8_quantize.argtypes = [P, I64, I64, I32, P, P, P, P]
+        lib.moe_fp8_quantize.restype = I32
+        lib.moe_fp8_dense.argtypes = [I64, I64, I64, P, P, P, P, P, SZ, P, P]
+        lib.moe_fp8_dense.restype = I32
+        lib.moe_nvfp4_prepare_scales.argtypes = [P, I64, P, P, P]
+        lib.moe_nvfp4_prepare_scales.restype = I32
         v = lib.moe_nvfp4_abi_version()
         if v != ABI_VERSION:
             raise RuntimeError(f"libmoe_nvfp4 ABI version {v}, binding expects {ABI_VERSION}")
@@ -432,3 +447,98 @@ class MoELayer:
     def __call__(self, x, y=None):
         self.route(x)
         return self.forward_planned(x, y)
+
+
+# ---- dense few-row projections, channel-FP8 weights, prepared scales ---------------
+
+def dense_query(M, N, K):
+    wb = ctypes.c_size_t(0)
+    _check("moe_nvfp4_dense_query",
+           load_library().moe_nvfp4_dense_query(int(M), int(N), int(K), ctypes.byref(wb)))
+    return wb.value
+
+
+def _dense_ws(M, N, K, ws, device):
+    need = dense_query(M, N, K)
+    if ws is None and need > 0:
+        ws = torch.zeros(need, dtype=torch.uint8, device=device)   # counters start at zero
+    if ws is not None:
+        _need(ws, ws.dtype, "ws")
+    return ws, (ws.numel() * ws.element_size() if ws is not None else 0)
+
+
+def dense(x, w, N, prepared=False, y=None, ws=None, status=None):
+    """NVFP4 dense projection (QPN2): y [M, N] = fp16(g * x . w16^T).
+
+    w = (q, s, g) of one N x K matrix in the fragment layout; with prepared
+    the scales are FP16 (moe_nvfp4_prepare_scales)."""
+    _need(x, torch.float16, "x")
+    M, K = x.shape
+    q, s, g = w
+    for n_, t in (("q", q), ("s", s), ("g", g)):
+        _need(t, t.dtype, n_)
+    errs = []
+    _expect(errs, "q", q, torch.uint8, N * K // 2)
+    if s.numel() * s.element_size() != N * K // 16 * (2 if prepared else 1):
+        errs.append("s: wrong byte count for the scale format")
+    _expect(errs, "g", g, torch.float32, 1)
+    _expect_status(errs, status)
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float16, device=x.device)
+    _need(y, torch.float16, "y")
+    _expect(errs, "y", y, torch.float16, M * N)
+    _raise_if("dense", errs)
+    ws, wsb = _dense_ws(M, N, K, ws, x.device)
+    _on_current_device([("x", x), ("q", q), ("s", s), ("g", g), ("y", y), ("ws", ws),
+                        ("status", status)])
+    wc = _weights_c(w, LAYOUT_FRAGMENT | (SCALES_PREPARED if prepared else 0))
+    _check("moe_nvfp4_dense", load_library().moe_nvfp4_dense(
+        M, N, K, _ptr(x), ctypes.byref(wc), _ptr(y), _ptr(ws), wsb, _ptr(status), _stream()))
+    return y
+
+
+def fp8_quantize(w: torch.Tensor, layout: int = LAYOUT_FP8_FRAGMENT, status=None):
+    """FP32 CUDA [rows, k] -> (q uint8 [rows * k], channel scales float32 [rows])."""
+    _need(w, torch.float32, "w")
+    rows, k = w.shape
+    q = torch.empty((rows * k,), dtype=torch.uint8, device=w.device)
+    cs = torch.empty((rows,), dtype=torch.float32, device=w.device)
+    if status is not None:
+        _need(status, torch.int32, "status")
+    _check("moe_fp8_quantize", load_library().moe_fp8_quantize(
+        _ptr(w), rows, k, int(layout), _ptr(q), _ptr(cs), _ptr(status), _stream()))
+    return q, cs
+
+
+def fp8_dense(x, q, cs, y=None, ws=None, status=None):
+    """Channel-FP8 dense projection (QPN8): y [M, N] = fp16(cs * x . E4M3(q)^T),
+    q in the FP8 fragment layout."""
+    _need(x, torch.float16, "x")
+    _need(q, torch.uint8, "q")
+    _need(cs, torch.float32, "cs")
+    M, K = x.shape
+    N = cs.numel()
+    errs = []
+    _expect(errs, "q", q, torch.uint8, N * K)
+    _expect_status(errs, status)
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float16, device=x.device)
+    _need(y, torch.float16, "y")
+    _expect(errs, "y", y, torch.float16, M * N)
+    _raise_if("fp8_dense", errs)
+    ws, wsb = _dense_ws(M, N, K, ws, x.device)
+    _on_current_device([("x", x), ("q", q), ("cs", cs), ("y", y), ("ws", ws), ("status", status)])
+    _check("moe_fp8_dense", load_library().moe_fp8_dense(
+        M, N, K, _ptr(x), _ptr(q), _ptr(cs), _ptr(y), _ptr(ws), wsb, _ptr(status), _stream()))
+    return y
+
+
+def prepare_scales(s: torch.Tensor, status=None):
+    """E4M3 scale bytes -> prepared FP16 scales (as int16, same element order)."""
+    _need(s, torch.uint8, "s")
+    out = torch.empty(s.shape, dtype=torch.int16, device=s.device)
+    if status is not None:
+        _need(status, torch.int32, "status")
+    _check("moe_nvfp4_prepare_scales", load_library().moe_nvfp4_prepare_scales(
+        _ptr(s), s.numel(), _ptr(out), _ptr(status), _stream()))
+    return out

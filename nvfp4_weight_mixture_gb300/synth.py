@@ -141,6 +141,47 @@ def all_w2(wl: Workload, experts=None) -> np.ndarray:
     return np.stack([expert_w2(wl, e) for e in ex])
 
 
+# ---- dense few-row projections ---------------------------------------------------
+# The pages measure the QPN2 / QPN8 projections on a dense model's MLP split
+# four ways (gate/up and down projections, M = 8 / 16 / 32) without giving
+# the sizes; these stand-ins are hidden 5120 and intermediate 17408 split four
+# ways: gate+up N = 2 x 4352 = 8704 from K = 5120, down N = 5120 from K = 4352.
+
+@dataclass(frozen=True)
+class DenseWorkload:
+    name: str
+    index: int   # seed family
+    M: int       # token rows
+    N: int       # output channels
+    K: int       # reduction length
+
+
+DENSE_WORKLOADS = {
+    w.name: w
+    for w in [
+        DenseWorkload("dense_gate_up_m16", 50, 16, 8704, 5120),
+        DenseWorkload("dense_down_m16", 51, 16, 5120, 4352),
+        DenseWorkload("dense_small", 52, 8, 512, 256),
+    ]
+}
+
+
+def dense_with_tokens(wl: DenseWorkload, M: int) -> DenseWorkload:
+    return DenseWorkload(wl.name, wl.index, M, wl.N, wl.K)
+
+
+def dense_weight(wl: DenseWorkload) -> np.ndarray:
+    """FP32 [N, K] ~ N(0, 0.02)."""
+    r = np.random.Generator(np.random.PCG64(np.random.SeedSequence([1000 * wl.index + _W13, 0])))
+    return r.standard_normal((wl.N, wl.K), dtype=np.float32) * np.float32(0.02)
+
+
+def dense_activations(wl: DenseWorkload, variant: int = 0) -> np.ndarray:
+    """x: FP16 [M, K] ~ N(0, 1)."""
+    r = np.random.Generator(np.random.PCG64(np.random.SeedSequence([1000 * wl.index + _X, variant])))
+    return r.standard_normal((wl.M, wl.K), dtype=np.float32).astype(np.float16)
+
+
 def random_ids(wl: Workload, variant: int = 0) -> np.ndarray:
     """Random distinct expert ids per token, int32 [M, k] (for plan tests)."""
     r = _rng(wl, 20, variant)

@@ -19,7 +19,7 @@ def lib():
 
 def declared_symbols():
     text = open(HEADER).read()
-    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\**\s+\**(moe_nvfp4_\w+)\(", text, re.M)))
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\**\s+\**(moe_\w+)\(", text, re.M)))
 
 
 def test_exports_every_declared_symbol(lib):
@@ -165,3 +165,41 @@ def test_small_router_switch_validates_mode(lib):
     assert lib.moe_nvfp4_set_small_router(-1) == -1
     assert lib.moe_nvfp4_set_small_router(1) == 0
     assert lib.moe_nvfp4_set_small_router(0) == 0
+
+
+def test_dense_query_shapes_without_device(lib):
+    """The dense query is host-only arithmetic: shape gates and workspace size
+    (FP32 partial sums of every K split; none with a single split)."""
+    wb = ctypes.c_size_t(0)
+    R = ctypes.byref
+    assert lib.moe_nvfp4_dense_query(16, 8704, 5120, R(wb)) == 0 and wb.value > 0
+    assert lib.moe_nvfp4_dense_query(0, 8704, 5120, R(wb)) == 0 and wb.value == 0
+    assert lib.moe_nvfp4_dense_query(33, 8704, 5120, R(wb)) == -2   # M above the path
+    assert lib.moe_nvfp4_dense_query(8, 8704 + 16, 5120, R(wb)) == -2
+    assert lib.moe_nvfp4_dense_query(8, 8704, 5120 + 32, R(wb)) == -2
+    assert lib.moe_nvfp4_dense_query(8, 8704, 5120, None) == -1
+    # the split (and so the partial sums per token row) does not depend on M:
+    # 256 bytes of counters, then partial sums in proportion to M
+    a, b = ctypes.c_size_t(0), ctypes.c_size_t(0)
+    lib.moe_nvfp4_dense_query(8, 5120, 4352, R(a))
+    lib.moe_nvfp4_dense_query(32, 5120, 4352, R(b))
+    assert b.value - 256 == 4 * (a.value - 256)
+    # a shape whose block ranges fall on group boundaries needs no workspace:
+    # 152 groups of one 64-element segment each
+    assert lib.moe_nvfp4_dense_query(8, 152 * 256, 64, R(wb)) == 0 and wb.value == 0
+
+
+def test_dense_entry_points_fail_closed_without_device(lib):
+    """Argument checks come before any device use: NULL buffers, bad layouts
+    and M = 0 are answered on the host."""
+    from nvfp4_weight_mixture_gb300 import moe
+    R = ctypes.byref
+    w = moe.WeightsC(None, None, None, moe.LAYOUT_FRAGMENT, 0)
+    assert lib.moe_nvfp4_dense(0, 256, 64, None, R(w), None, None, 0, None, None) == 0
+    assert lib.moe_nvfp4_dense(4, 256, 64, None, R(w), None, None, 0, None, None) == -1
+    w.layout = moe.LAYOUT_FRAGMENT_W13
+    assert lib.moe_nvfp4_dense(4, 256, 64, None, R(w), None, None, 0, None, None) == -7
+    assert lib.moe_fp8_dense(4, 256, 64, None, None, None, None, None, 0, None, None) == -1
+    assert lib.moe_fp8_quantize(None, 256, 64, 3, None, None, None, None) == -1
+    assert lib.moe_nvfp4_prepare_scales(None, 0, None, None, None) == 0
+    assert lib.moe_nvfp4_prepare_scales(None, 16, None, None, None) == -1
