@@ -244,6 +244,21 @@ int32_t moe_nvfp4_forward(const moe_nvfp4_config* cfg, int64_t M, const void* x,
                           const moe_nvfp4_weights* shared13, const moe_nvfp4_weights* shared2,
                           void* y, void* ws, size_t ws_bytes, uint32_t* status, void* stream);
 
+/* The whole layer in one call: moe_nvfp4_plan followed by moe_nvfp4_forward
+ * on the same stream, with the same arguments and results (ids and topk_w
+ * written, the plan buffer holding the plan, y the layer output).  The
+ * forward's own buffers and weights are checked before the plan is enqueued,
+ * so a call that fails launches nothing.  The pages' complete MoE call
+ * ("[Kernel][SM70] Improve Qwen3.8 no-MTP concurrency", section "Latest
+ * grouped-MoE screen": the complete C16 call).  Returns the codes of
+ * moe_nvfp4_plan and moe_nvfp4_forward. */
+int32_t moe_nvfp4_layer(const moe_nvfp4_config* cfg, int64_t M, const void* x,
+                        const void* w_router, const float* bias, const void* w_gate, int32_t* ids,
+                        float* topk_w, void* plan, size_t plan_bytes, const moe_nvfp4_weights* w13,
+                        const moe_nvfp4_weights* w2, const moe_nvfp4_weights* shared13,
+                        const moe_nvfp4_weights* shared2, void* y, void* ws, size_t ws_bytes,
+                        uint32_t* status, void* stream);
+
 /* moe_nvfp4_forward without a workspace argument, for callers that cannot
  * allocate device memory (a host runtime that owns every allocation, a phase
  * in which a framework forbids allocation, a fixed C signature with no room

@@ -340,6 +340,38 @@ int32_t moe_nvfp4_forward(const moe_nvfp4_config* cfg, int64_t M, const void* x,
   return cuda_status(e);
 }
 
+// ---- the whole layer in one call ----
+
+int32_t moe_nvfp4_layer(const moe_nvfp4_config* cfg, int64_t M, const void* x,
+                        const void* w_router, const float* bias, const void* w_gate, int32_t* ids,
+                        float* topk_w, void* plan, size_t plan_bytes, const moe_nvfp4_weights* w13,
+                        const moe_nvfp4_weights* w2, const moe_nvfp4_weights* shared13,
+                        const moe_nvfp4_weights* shared2, void* y, void* ws, size_t ws_bytes,
+                        uint32_t* status, void* stream) {
+  LayerDims d;
+  int32_t rc = check_cfg(cfg, &d);
+  if (rc) return rc;
+  if (M < 0 || M > kMaxTokens) return MOE_ERR_SHAPE;
+  if (M == 0) return MOE_OK;
+  // plan then forward on the same stream; each validates everything it reads
+  // before enqueuing, and the forward's checks cannot fail for reasons the
+  // plan's did not (same cfg and M), except its own buffers: checked first
+  if (!y || !ws) return MOE_ERR_INVALID_ARG;
+  if ((rc = check_weights(w13, MOE_LAYOUT_FRAGMENT_W13))) return rc;
+  if ((rc = check_weights(w2, MOE_LAYOUT_FRAGMENT))) return rc;
+  if (d.shared) {
+    if ((rc = check_weights(shared13, MOE_LAYOUT_FRAGMENT_W13))) return rc;
+    if ((rc = check_weights(shared2, MOE_LAYOUT_FRAGMENT))) return rc;
+  }
+  if (!aligned16(y) || !aligned16(ws)) return MOE_ERR_ALIGNMENT;
+  if (ws_bytes < ws_bytes_for(d, M)) return MOE_ERR_WORKSPACE;
+  rc = moe_nvfp4_plan(cfg, M, x, w_router, bias, w_gate, ids, topk_w, plan, plan_bytes, status,
+                      stream);
+  if (rc) return rc;
+  return moe_nvfp4_forward(cfg, M, x, plan, w13, w2, shared13, shared2, y, ws, ws_bytes, status,
+                           stream);
+}
+
 // ---- dense few-row projections, channel-FP8 weights, prepared scales ----
 
 static int32_t check_dense_shape(int64_t M, int64_t N, int64_t K) {

@@ -266,6 +266,9 @@ __global__ void __launch_bounds__(kW2Warps * 32, 1)
                                       ~uintptr_t(1023));
   __shared__ uint64_t full[kW2Warps][2];
   MOE_TL(kTlW2);
+  // the next layer call's router may start its weight copies now (it waits
+  // for this whole grid before it reads anything this call writes)
+  pdl_launch_dependents();
   const LayerDims& d = p.d;
   const int H = d.H, I = d.I, k_eff = d.k_eff;
   const int P = p.M * k_eff;

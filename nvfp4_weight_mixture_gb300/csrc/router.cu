@@ -22,153 +22,9 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "route.cuh"
 
 namespace moe {
-
-constexpr int kMaxEEff = 520;  // >= 512 routed experts + the shared expert
-
-// A pair's expert id is valid if it names a routed expert in a routed slot,
-// or the shared expert in the shared slot.
-__device__ __forceinline__ bool pair_valid(int e, int slot, const LayerDims& d) {
-  return slot < d.k ? (e >= 0 && e < d.E) : (e == d.E);
-}
-
-// ---------------------------------------------------------------------------
-// Warp top-k over a row of E logits.  Lane j < k receives slot j: the j-th
-// largest logit, ties broken towards the lower expert id.  E <= 512.  Each
-// round takes the warp maximum of order-preserving integer keys and then the
-// lowest expert id holding it (two single-instruction warp reductions).
-// ---------------------------------------------------------------------------
-__device__ __forceinline__ uint32_t f2key(float f) {
-  const uint32_t b = __float_as_uint(f);
-  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
-}
-__device__ __forceinline__ float key2f(uint32_t k) {
-  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
-}
-
-template <bool kGlobal>
-__device__ __forceinline__ void warp_topk(const float* row, int E, int k, int* out_id,
-                                          float* out_l) {
-  const int lane = threadIdx.x & 31;
-  uint32_t v[16];  // key 0 = absent or taken (below every finite or infinite logit)
-#pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    const int e = lane + 32 * i;
-    v[i] = (e < E) ? f2key(kGlobal ? __ldcg(row + e) : row[e]) : 0u;
-  }
-  int my_id = -1;
-  float my_l = -INFINITY;
-  for (int j = 0; j < k; ++j) {
-    uint32_t m8[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) m8[i] = max(v[i], v[i + 8]);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) m8[i] = max(m8[i], m8[i + 4]);
-    const uint32_t lm = max(max(m8[0], m8[2]), max(m8[1], m8[3]));
-    const uint32_t gm = __reduce_max_sync(0xffffffffu, lm);
-    uint32_t li = 0xffffffffu;
-#pragma unroll
-    for (int i = 15; i >= 0; --i)
-      if (v[i] == gm) li = (uint32_t)(lane + 32 * i);
-    const uint32_t gi = __reduce_min_sync(0xffffffffu, li);
-#pragma unroll
-    for (int i = 0; i < 16; ++i)
-      if ((uint32_t)(lane + 32 * i) == gi) v[i] = 0u;
-    if (lane == j) {
-      my_id = (int)gi;
-      my_l = key2f(gm);
-    }
-  }
-  *out_id = my_id;
-  *out_l = my_l;
-}
-
-// softmax of the k selected logits held by lanes 0..k-1 (lane 0 holds the max)
-__device__ __forceinline__ float warp_topk_weight(float my_l, int k) {
-  const int lane = threadIdx.x & 31;
-  const float lmax = __shfl_sync(0xffffffffu, my_l, 0);
-  const float e = (lane < k) ? expf(my_l - lmax) : 0.f;
-  float s = e;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-  return e / s;
-}
-
-// gamma = sigmoid(x . w_g), one warp, x and w_g FP16 of length H (H % 64 == 0)
-__device__ __forceinline__ float warp_gate(const __half* xr, const __half* wg, int H) {
-  const int lane = threadIdx.x & 31;
-  float z = 0.f;
-  for (int c = 2 * lane; c < H; c += 64) {
-    const float2 a = __half22float2(*reinterpret_cast<const __half2*>(xr + c));
-    const float2 b = __half22float2(*reinterpret_cast<const __half2*>(wg + c));
-    z = fmaf(a.x, b.x, z);
-    z = fmaf(a.y, b.y, z);
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
-  return 1.f / (1.f + expf(-z));
-}
-
-// Writes slot values of token t (lanes < k), plus the shared slot.
-__device__ __forceinline__ void store_route(const LayerDims& d, int t, int id, float w,
-                                            float gamma, int32_t* ids_user, float* w_user,
-                                            const PlanView& pv) {
-  const int lane = threadIdx.x & 31;
-  if (lane < d.k) {
-    ids_user[(int64_t)t * d.k + lane] = id;
-    w_user[(int64_t)t * d.k + lane] = w;
-    pv.ids[(int64_t)t * d.k_eff + lane] = id;
-    pv.w[(int64_t)t * d.k_eff + lane] = w;
-  }
-  if (d.shared && lane == 0) {
-    pv.ids[(int64_t)t * d.k_eff + d.k] = d.E;
-    pv.w[(int64_t)t * d.k_eff + d.k] = gamma;
-  }
-}
-
-// Exclusive block scan of three counters (blockDim.x == 256).
-__device__ __forceinline__ void block_scan3(int& a, int& b, int& c, int* tot) {
-  __shared__ int ws[8][3];
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int ia = a, ib = b, ic = c;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int ta = __shfl_up_sync(0xffffffffu, ia, o);
-    const int tb = __shfl_up_sync(0xffffffffu, ib, o);
-    const int tc = __shfl_up_sync(0xffffffffu, ic, o);
-    if (lane >= o) {
-      ia += ta;
-      ib += tb;
-      ic += tc;
-    }
-  }
-  if (lane == 31) {
-    ws[warp][0] = ia;
-    ws[warp][1] = ib;
-    ws[warp][2] = ic;
-  }
-  __syncthreads();
-  int oa = 0, ob = 0, oc = 0, sa = 0, sb = 0, sc = 0;
-#pragma unroll
-  for (int w = 0; w < 8; ++w) {
-    if (w < warp) {
-      oa += ws[w][0];
-      ob += ws[w][1];
-      oc += ws[w][2];
-    }
-    sa += ws[w][0];
-    sb += ws[w][1];
-    sc += ws[w][2];
-  }
-  a = oa + ia - a;
-  b = ob + ib - b;
-  c = oc + ic - c;
-  tot[0] = sa;
-  tot[1] = sb;
-  tot[2] = sc;
-  __syncthreads();
-}
 
 // ---------------------------------------------------------------------------
 // Plan of up to kDecodeMaxTokens * (32 + 1) pairs by one block of 256 threads.
@@ -1028,6 +884,11 @@ __global__ void __launch_bounds__(kRcThreads, 1)
       mbar_expect_tx(&full[warp][i], (uint32_t)(tr * rb));
       tma_load_2d(my_ring + i * L.stage, &wrmap, (int)rank * Es, kw0 + i * tr, &full[warp][i]);
     }
+  // The router weight is an input of the layer, not of the previous kernel:
+  // its first copies are in flight before waiting for the preceding grid
+  // (programmatic dependent launch), whose outputs (the token rows) and
+  // buffers (the plan) are only touched after the wait.
+  pdl_wait();
   // token rows and the zero row (rows >= M of the MMA read it)
   {
     const int rv = H / 8;  // 16-byte vectors per row
@@ -1278,13 +1139,15 @@ cudaError_t launch_plan(const LayerDims& d, int64_t M, const __half* x, const __
         cfg.blockDim = dim3(kRcThreads);
         cfg.dynamicSmemBytes = L.total;
         cfg.stream = stream;
-        cudaLaunchAttribute attr[1];
+        cudaLaunchAttribute attr[2];
         attr[0].id = cudaLaunchAttributeClusterDimension;
         attr[0].val.clusterDim.x = L.C;
         attr[0].val.clusterDim.y = 1;
         attr[0].val.clusterDim.z = 1;
+        attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[1].val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = attr;
-        cfg.numAttrs = 1;
+        cfg.numAttrs = trace_on() ? 1 : 2;
         return cudaLaunchKernelEx(&cfg, router_cluster_kernel, d, Mi, x, wrmap, bias, w_gate,
                                   ids_user, w_user, pv, status, cmax);
       }

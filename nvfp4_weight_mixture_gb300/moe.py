@@ -42,7 +42,7 @@ EXPORTS = ["moe_nvfp4_abi_version", "moe_nvfp4_status_string", "moe_nvfp4_query"
            "moe_nvfp4_set_trace_events", "moe_nvfp4_forward_noalloc",
            "moe_nvfp4_last_cuda_error", "moe_nvfp4_set_small_router",
            "moe_nvfp4_dense_query", "moe_nvfp4_dense", "moe_fp8_quantize", "moe_fp8_dense",
-           "moe_nvfp4_prepare_scales"]
+           "moe_nvfp4_prepare_scales", "moe_nvfp4_layer"]
 TRACE_STEPS = ("plan", "w13", "w2", "combine")
 
 
@@ -96,6 +96,9 @@ def load_library(path: str = LIB_PATH):
         lib.moe_nvfp4_plan.restype = I32
         lib.moe_nvfp4_forward.argtypes = [P, I64, P, P, P, P, P, P, P, P, SZ, P, P]
         lib.moe_nvfp4_forward.restype = I32
+        lib.moe_nvfp4_layer.argtypes = [P, I64, P, P, P, P, P, P, P, SZ, P, P, P, P, P, P, SZ,
+                                        P, P]
+        lib.moe_nvfp4_layer.restype = I32
         lib.moe_nvfp4_forward_noalloc.argtypes = [P, I64, P, P, P, P, P, P, P, P, P]
         lib.moe_nvfp4_forward_noalloc.restype = I32
         lib.moe_nvfp4_set_trace_events.argtypes = [P, I32]
@@ -376,6 +379,30 @@ def forward(cfg: Config, x, plan_buf, w13, w2, shared13, shared2, y, ws, status=
         _ptr(y), _ptr(ws), ws.numel(), _ptr(status), _stream()))
 
 
+def layer(cfg: Config, x, w_router, bias, w_gate, ids, topk_w, plan_buf, w13, w2, shared13,
+          shared2, y, ws, status=None):
+    """moe_nvfp4_layer: router, plan and forward in one call."""
+    M = x.shape[0]
+    _need(ids, torch.int32, "ids")
+    _need(topk_w, torch.float32, "topk_w")
+    for name, t in (("w_router", w_router), ("bias", bias), ("w_gate", w_gate)):
+        if t is not None:
+            _need(t, t.dtype, name)
+    _raise_if("layer", plan_arg_errors(cfg, x, w_router, bias, w_gate, ids, topk_w, status))
+    _check_forward_args("layer", cfg, x, plan_buf, w13, w2, shared13, shared2, y, status, ws)
+    _on_current_device([("w_router", w_router), ("bias", bias), ("w_gate", w_gate),
+                        ("ids", ids), ("topk_w", topk_w)])
+    a = _weights_c(w13, LAYOUT_FRAGMENT_W13)
+    b = _weights_c(w2, LAYOUT_FRAGMENT)
+    c = _weights_c(shared13, LAYOUT_FRAGMENT_W13)
+    d = _weights_c(shared2, LAYOUT_FRAGMENT)
+    _check("moe_nvfp4_layer", load_library().moe_nvfp4_layer(
+        ctypes.byref(cfg), M, _ptr(x), _ptr(w_router), _ptr(bias), _ptr(w_gate), _ptr(ids),
+        _ptr(topk_w), _ptr(plan_buf), plan_buf.numel(), ctypes.byref(a), ctypes.byref(b),
+        ctypes.byref(c) if c is not None else None, ctypes.byref(d) if d is not None else None,
+        _ptr(y), _ptr(ws), ws.numel(), _ptr(status), _stream()))
+
+
 def forward_noalloc(cfg: Config, x, plan_buf, w13, w2, shared13, shared2, y, status=None):
     """moe_nvfp4_forward_noalloc: the forward with the library's own static
     workspace (for callers that cannot allocate; see the header)."""
@@ -444,9 +471,21 @@ class MoELayer:
                 self.ws, self.status)
         return y
 
-    def __call__(self, x, y=None):
-        self.route(x)
-        return self.forward_planned(x, y)
+    def __call__(self, x, y=None, ids=None, topk_w=None):
+        """The whole layer through moe_nvfp4_layer (router, plan, forward).
+        Returns y; the routes land in ids / topk_w (allocated when not given)
+        and the plan in the plan buffer."""
+        M = x.shape[0]
+        self.reserve(M)
+        y = y if y is not None else torch.empty((M, self.H), dtype=torch.float16, device=self.device)
+        ids = ids if ids is not None else torch.empty((M, self.k), dtype=torch.int32,
+                                                      device=self.device)
+        topk_w = topk_w if topk_w is not None else torch.empty((M, self.k), dtype=torch.float32,
+                                                               device=self.device)
+        layer(self.cfg, x, self.w_router, self.bias, self.w_gate, ids, topk_w, self.plan_buf,
+              self.w13, self.w2, self.shared13, self.shared2, y, self.ws, self.status)
+        self.last_ids, self.last_topk_w = ids, topk_w
+        return y
 
 
 # ---- dense few-row projections, channel-FP8 weights, prepared scales ---------------

@@ -344,15 +344,21 @@ def test_forward_repeat_bitwise_and_graph_replay():
 
 def test_decode_batch_invariance():
     """Inside the decode bucket a token's output does not depend on its batch:
-    M=16 equals two M=8 calls bitwise."""
+    M=16 equals two M=8 calls bitwise, through the plan + forward kernels and
+    through the fused single-kernel layer call alike."""
     case = Case(synth.with_tokens(DEC16, 16))
     y16 = case.gpu_forward()
     parts = []
     for sl in (slice(0, 8), slice(8, 16)):
         xs = case.x_t[sl].contiguous()
-        parts.append(case.layer(xs).cpu().numpy())
+        case.layer.route(xs)
+        parts.append(case.layer.forward_planned(xs).cpu().numpy())
     torch.cuda.synchronize()
     np.testing.assert_array_equal(y16.view(np.uint16), np.concatenate(parts).view(np.uint16))
+    f16 = case.layer(case.x_t).cpu().numpy()
+    fparts = [case.layer(case.x_t[sl].contiguous()).cpu().numpy()
+              for sl in (slice(0, 8), slice(8, 16))]
+    np.testing.assert_array_equal(f16.view(np.uint16), np.concatenate(fparts).view(np.uint16))
 
 
 @pytest.mark.parametrize("M", [16, 40])
