@@ -45,7 +45,7 @@ METRIC = "MoE-layer tokens/s"
 # the headline (decode M = 1) first, then the other workloads the metric is
 # quoted on (M = 16, M = 8192) and the remaining seeded ones
 DEFAULT_WORKLOADS = ["decode_m1", "decode_m16_bias", "prefill_m8192",
-                     "prefill_m8192_zipf_shared", "tiny_m8"]
+                     "prefill_m8192_zipf_shared", "prefill_m784", "tiny_m8"]
 UNIT = "tokens/s"
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
@@ -64,6 +64,9 @@ def parse_args():
     p.add_argument("--tokens", type=int, default=None,
                    help="override the workload's token count (same shapes and seeds)")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--crossover", default=None,
+                   help="comma-separated token counts: time the forward's decode and grouped "
+                        "paths at each M (one JSON line each) instead of the bench")
     p.add_argument("--cpu-seconds", type=float, default=12.0,
                    help="target CPU time of the oracle sample")
     return p.parse_args()
@@ -623,6 +626,64 @@ def time_workload(wl, args, dist, dev, local, ws, rank):
     }
 
 
+def run_crossover(args):
+    """The M crossover of the forward's two paths (the pages' M-bucketed
+    dispatch): per-call time of the layer in the 16-call stack for M tokens of
+    the prefill_m8192 layer (uniform routing) through the weight-streaming
+    decode kernels (M <= 16) and through the grouped tensor-core GEMMs (any
+    M).  Prints one JSON line per (M, path)."""
+    import torch
+    from nvfp4_weight_mixture_gb300 import moe, synth
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    moe.load_library()
+    base = synth.WORKLOADS["prefill_m8192"]
+    Ms = [int(v) for v in args.crossover.split(",")]
+    layer = build_layer(synth.with_tokens(base, max(Ms)), dev, moe, synth)
+    stack = [layer] + [clone_layer(layer, moe) for _ in range(STACK - 1)]
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    reps = args.steps or 20
+    for M in Ms:
+        wl = synth.with_tokens(base, M)
+        xs = [torch.from_numpy(synth.activations(wl, v)).to(dev) for v in range(STACK)]
+        ys = [torch.empty((M, wl.H), dtype=torch.float16, device=dev) for _ in range(STACK)]
+        for path, bucket in (("decode_gemv", 16), ("grouped_tcgen05", 0)):
+            if path == "decode_gemv" and M > moe.DECODE_MAX_TOKENS:
+                continue
+            moe.set_decode_max_tokens(bucket)
+            try:
+                with torch.cuda.stream(stream):
+                    for i in range(STACK):
+                        stack[i](xs[i], ys[i])
+                stream.synchronize()
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream):
+                    for i in range(STACK):
+                        stack[i](xs[i], ys[i])
+                ts = []
+                with torch.cuda.stream(stream):
+                    for r in range(reps + 3):
+                        flush.zero_()
+                        a = torch.cuda.Event(enable_timing=True)
+                        b = torch.cuda.Event(enable_timing=True)
+                        a.record(stream)
+                        g.replay()
+                        b.record(stream)
+                        stream.synchronize()
+                        if r >= 3:
+                            ts.append(a.elapsed_time(b) / STACK)
+                del g
+            finally:
+                moe.set_decode_max_tokens(16)
+            us = statistics.median(ts) * 1e3
+            print(json.dumps({"crossover": True, "M": M, "path": path, "us_per_call": us,
+                              "tokens_per_s": M / (us * 1e-6),
+                              "status": int(layer.status.item())}), flush=True)
+    return 0
+
+
 def run_gpu(args, workloads):
     """Times every workload (the first is the headline line; the others go
     into its "configs" map, each measured under the same protocol)."""
@@ -674,6 +735,8 @@ def main():
         wls = [synth.with_tokens(w, args.tokens) for w in wls]
     if args.impl == "reference":
         return run_reference(args, wls[0])
+    if args.crossover:
+        return run_crossover(args)
     return run_gpu(args, wls)
 
 

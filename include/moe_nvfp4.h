@@ -234,6 +234,11 @@ int32_t moe_nvfp4_plan(const moe_nvfp4_config* cfg, int64_t M, const void* x,
  *
  *   w13      routed W13, layout MOE_LAYOUT_FRAGMENT_W13, E matrices [2I][H].
  *   w2       routed W2, layout MOE_LAYOUT_FRAGMENT, E matrices [H][I].
+ *            Either storage of the scales: raw E4M3, or prepared FP16 with
+ *            MOE_SCALES_PREPARED OR-ed into every weight set's layout (all
+ *            of them alike, else MOE_ERR_LAYOUT); the output is bitwise the
+ *            same ("[Kernel][SM70] Improve Qwen3.8 no-MTP concurrency",
+ *            section "Test Result": raw and prepared outputs bitwise equal).
  *   shared13, shared2  shared expert (one matrix each, same layouts); required
  *            with MOE_FLAG_SHARED, else ignored.
  *   y        device FP16 [M][H] out.
@@ -384,6 +389,15 @@ int32_t moe_nvfp4_prepare_scales(const uint8_t* s, int64_t n, void* s16, uint32_
  * Process-wide; takes effect at the next moe_nvfp4_plan call; not
  * thread-safe.  Returns MOE_ERR_INVALID_ARG for another mode. */
 int32_t moe_nvfp4_set_small_router(int32_t mode);
+
+/* Diagnostic M bucket of moe_nvfp4_forward (no counterpart in the pages' text
+ * beyond their M-bucketed dispatch: "[Kernel][SM70] Improve Qwen3.8 no-MTP
+ * concurrency", section "Scope and related PRs", dynamic M2-M16 dispatch; a
+ * measurement aid).  Calls with M <= m run the weight-streaming decode
+ * kernels, larger M the grouped tensor-core GEMMs; 0 <= m <= 16 (default 16,
+ * the measured crossover), else MOE_ERR_INVALID_ARG.  Both give results
+ * within the acceptance bar of each other.  Process-wide; not thread-safe. */
+int32_t moe_nvfp4_set_decode_max_tokens(int32_t m);
 
 #ifdef __cplusplus
 }

@@ -102,10 +102,11 @@ size_t ws_bytes_for(const LayerDims& d, int64_t M) {
   return align_up((size_t)P * d.I * sizeof(__half), 256) + (size_t)P * d.H * sizeof(float);
 }
 
+// `layout`, optionally with MOE_SCALES_PREPARED.
 int32_t check_weights(const moe_nvfp4_weights* w, int32_t layout) {
   if (!w || !w->q || !w->s || !w->g) return MOE_ERR_INVALID_ARG;
   if (w->reserved) return MOE_ERR_INVALID_ARG;
-  if (w->layout != layout) return MOE_ERR_LAYOUT;
+  if ((w->layout & ~MOE_SCALES_PREPARED) != layout) return MOE_ERR_LAYOUT;
   if (!aligned16(w->q) || !aligned16(w->s) || (reinterpret_cast<uintptr_t>(w->g) & 3u))
     return MOE_ERR_ALIGNMENT;
   return MOE_OK;
@@ -113,6 +114,9 @@ int32_t check_weights(const moe_nvfp4_weights* w, int32_t layout) {
 
 void* const* g_trace_events = nullptr;
 int32_t g_trace_steps = 0;
+// forward: M <= this runs the weight-streaming decode kernels (diagnostic
+// moe_nvfp4_set_decode_max_tokens; the default is the measured crossover)
+int32_t g_decode_max_tokens = kDecodeMaxTokens;
 
 int32_t cuda_status(cudaError_t e) {
   if (e == cudaSuccess) return MOE_OK;
@@ -179,6 +183,12 @@ int32_t moe_nvfp4_set_trace_events(void* const* events, int32_t n_steps) {
   if (events && (n_steps < 1 || n_steps > 4)) return MOE_ERR_INVALID_ARG;
   g_trace_events = events;
   g_trace_steps = events ? n_steps : 0;
+  return MOE_OK;
+}
+
+int32_t moe_nvfp4_set_decode_max_tokens(int32_t m) {
+  if (m < 0 || m > kDecodeMaxTokens) return MOE_ERR_INVALID_ARG;
+  g_decode_max_tokens = m;
   return MOE_OK;
 }
 
@@ -310,6 +320,13 @@ int32_t moe_nvfp4_forward(const moe_nvfp4_config* cfg, int64_t M, const void* x,
     if ((rc = check_weights(shared13, MOE_LAYOUT_FRAGMENT_W13))) return rc;
     if ((rc = check_weights(shared2, MOE_LAYOUT_FRAGMENT))) return rc;
   }
+  // one scale storage for the whole layer
+  const int32_t sf = w13->layout & MOE_SCALES_PREPARED;
+  if ((w2->layout & MOE_SCALES_PREPARED) != sf ||
+      (d.shared && ((shared13->layout & MOE_SCALES_PREPARED) != sf ||
+                    (shared2->layout & MOE_SCALES_PREPARED) != sf)))
+    return MOE_ERR_LAYOUT;
+  const bool prepared = sf != 0;
   if (!aligned16(x) || !aligned16(plan) || !aligned16(y) || !aligned16(ws))
     return MOE_ERR_ALIGNMENT;
   if (status && (reinterpret_cast<uintptr_t>(status) & 3u)) return MOE_ERR_ALIGNMENT;
@@ -331,12 +348,12 @@ int32_t moe_nvfp4_forward(const moe_nvfp4_config* cfg, int64_t M, const void* x,
   }
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e;
-  if (M <= kDecodeMaxTokens)
+  if (M <= g_decode_max_tokens)
     e = launch_decode_forward(d, M, static_cast<const __half*>(x), pv, W13, W2, S13, S2,
-                              static_cast<__half*>(y), h, partial, status, st, sms);
+                              static_cast<__half*>(y), h, partial, status, st, sms, prepared);
   else
     e = launch_prefill_forward(d, M, static_cast<const __half*>(x), pv, W13, W2, S13, S2,
-                               static_cast<__half*>(y), h, partial, status, st, sms);
+                               static_cast<__half*>(y), h, partial, status, st, sms, prepared);
   return cuda_status(e);
 }
 

@@ -24,6 +24,36 @@ namespace moe {
 __device__ __forceinline__ uint16_t ldg_u16(const uint8_t* p) {
   return __ldg(reinterpret_cast<const unsigned short*>(p));
 }
+__device__ __forceinline__ uint32_t ldg_u32(const uint8_t* p) {
+  return __ldg(reinterpret_cast<const unsigned int*>(p));
+}
+
+// Scale storage: SB = 1 raw E4M3 bytes, SB = 2 prepared FP16 scales (each raw
+// byte widened to two bytes in place, so every scale offset doubles).  The
+// two scales of a fragment lane (rows g and g + 8) sit at raw byte offset
+// `off`: loaded as they are (no wait on the load here) ...
+template <int SB>
+__device__ __forceinline__ uint32_t lane_scales_ldg(const uint8_t* base, size_t off) {
+  if constexpr (SB == 1)
+    return ldg_u16(base + off);
+  else
+    return ldg_u32(base + 2 * off);
+}
+template <int SB>
+__device__ __forceinline__ uint32_t lane_scales_smem(const char* base, size_t off) {
+  if constexpr (SB == 1)
+    return *reinterpret_cast<const unsigned short*>(base + off);
+  else
+    return *reinterpret_cast<const uint32_t*>(base + 2 * off);
+}
+// ... and turned into the FP16 splats when they are used.
+template <int SB>
+__device__ __forceinline__ void lane_splats(uint32_t v, uint32_t* sg, uint32_t* sg8) {
+  if constexpr (SB == 1)
+    scale_splats(v, sg, sg8);
+  else
+    scale_splats_f16(v, sg, sg8);
+}
 
 // ---------------------------------------------------------------------------
 // Decode forward = two kernels in programmatic dependent launch:
@@ -47,6 +77,7 @@ struct DecodeArgs {
   uint32_t* status;
   int M;
   int max_active;  // work-table entries that can be valid (min(M * k_eff, e_eff))
+  int sb;          // bytes per stored scale (1 raw, 2 prepared)
 };
 
 // A work-table entry names a routed expert (or the shared one) and a run of
@@ -64,7 +95,7 @@ __device__ __forceinline__ void w2_share_prefetch(const DecodeArgs& p, const int
   const int e = en[0];
   if (!entry_ok(p, e, en[1], en[2])) return;
   const bool sh = (e == d.E);
-  const size_t q2 = (size_t)d.H * d.I / 2, s2b = (size_t)d.H * d.I / 16;
+  const size_t q2 = (size_t)d.H * d.I / 2, s2b = (size_t)d.H * d.I / 16 * p.sb;
   const int n_rtp = d.I / 16;
   const uint8_t* q2e = sh ? p.s2.q : p.w2.q + (size_t)e * q2;
   const uint8_t* s2e = sh ? p.s2.s : p.w2.s + (size_t)e * s2b;
@@ -74,7 +105,7 @@ __device__ __forceinline__ void w2_share_prefetch(const DecodeArgs& p, const int
 
 // W13 item (a, rp) for one block of 256 threads.  xs: staged token rows
 // (stride 2H + 16).
-template <int NT>
+template <int NT, int SB>
 __device__ __forceinline__ void w13_item(const DecodeArgs& p, const int* en, int rp,
                                          const char* xs, float* red, int* s_tok) {
   const LayerDims& d = p.d;
@@ -83,7 +114,7 @@ __device__ __forceinline__ void w13_item(const DecodeArgs& p, const int* en, int
   if (!entry_ok(p, e, base, count)) return;
   const bool sh = (e == d.E);
   const uint8_t* qe = sh ? p.s13.q : p.w13.q + (size_t)e * I * H;
-  const uint8_t* se = sh ? p.s13.s : p.w13.s + (size_t)e * I * H / 8;
+  const uint8_t* se = sh ? p.s13.s : p.w13.s + (size_t)e * I * H / 8 * SB;
   const float gsc = sh ? p.s13.g[0] : p.w13.g[e];
   const int ttid = threadIdx.x, warp = ttid >> 5, lane = ttid & 31;
   const int g = lane >> 2, t4 = lane & 3;
@@ -92,7 +123,7 @@ __device__ __forceinline__ void w13_item(const DecodeArgs& p, const int* en, int
   // block (tile j, segment ks) of a group is number ks * 16 + j within it
   const int j0 = 2 * (rp & 7);
   const uint8_t* qt = qe + (size_t)(rp >> 3) * S * 16 * 512 + j0 * 512;
-  const uint8_t* st = se + (size_t)(rp >> 3) * S * 16 * 64 + j0 * 64;
+  const size_t st = (size_t)(rp >> 3) * S * 16 * 64 + j0 * 64;  // raw scale offset
   const int xstride = H * 2 + 16;
 
   uint4 qv[4][2];
@@ -106,7 +137,7 @@ __device__ __forceinline__ void w13_item(const DecodeArgs& p, const int* en, int
 #pragma unroll
         for (int tt = 0; tt < 2; ++tt) {
           qv[j][tt] = ldg_nc_v4(qt + ((size_t)ks * 16 + tt) * 512 + lane * 16);
-          sv[j][tt] = ldg_u16(st + ((size_t)ks * 16 + tt) * 64 + lane * 2);
+          sv[j][tt] = lane_scales_ldg<SB>(se, st + ((size_t)ks * 16 + tt) * 64 + lane * 2);
         }
       }
     }
@@ -156,7 +187,7 @@ __device__ __forceinline__ void w13_item(const DecodeArgs& p, const int* en, int
 #pragma unroll
         for (int tt = 0; tt < 2; ++tt) {
           uint32_t sg, sg8;
-          scale_splats(sv[j][tt], &sg, &sg8);
+          lane_splats<SB>(sv[j][tt], &sg, &sg8);
 #pragma unroll
           for (int s = 0; s < 4; ++s) {
             uint32_t af[4];
@@ -199,7 +230,7 @@ __device__ __forceinline__ void w13_item(const DecodeArgs& p, const int* en, int
   }
 }
 
-template <int NT>
+template <int NT, int SB>
 __global__ void __launch_bounds__(256, NT == 1 ? 3 : 2) decode_w13_kernel(const DecodeArgs p) {
   extern __shared__ __align__(16) char dsm[];  // staged token rows, then the reduction area
   __shared__ int s_tok[16];
@@ -235,7 +266,7 @@ __global__ void __launch_bounds__(256, NT == 1 ? 3 : 2) decode_w13_kernel(const 
       if (tid < kDtabInts) s_ent[tid] = __ldcg(p.pv.dtab + a * kDtabInts + tid);
       __syncthreads();
     }
-    w13_item<NT>(p, s_ent, rp, xs, red, s_tok);
+    w13_item<NT, SB>(p, s_ent, rp, xs, red, s_tok);
   }
 }
 
@@ -254,7 +285,7 @@ __device__ __forceinline__ int frag_map_row(int m, int groups, int G, int S, int
 // the first two issued before waiting on the W13 grid.  Each expert's pairs
 // get o = g2 * w_pair * (W2[tile] . h) in shared memory; the block then sums
 // every token's slots in order, y[t][tile] = fp16(sum_j o_j).
-template <int NT>
+template <int NT, int SB>
 __global__ void __launch_bounds__(kW2Warps * 32, 1)
     decode_w2_kernel(const DecodeArgs p, int w2_warps, int stage_bytes,
                          const __grid_constant__ CUtensorMap mq,
@@ -289,7 +320,7 @@ __global__ void __launch_bounds__(kW2Warps * 32, 1)
   // ---- everything that comes from the plan grid (complete before W13 began) ----
   for (int q = tid; q < P; q += kW2Warps * 32) valid[q] = __ldcg(p.pv.inv + q) >= 0;
   const int n_act = min(__ldcg(&p.pv.hdr->n_active), p.max_active);
-  const uint32_t tx = (uint32_t)S * (512 + 64);
+  const uint32_t tx = (uint32_t)S * (512 + 64 * SB);
   // chunk r of this warp = expert a = warp + r * w2_warps, in stage r % 2
   auto entry = [&](int r) {
     const int a = warp + r * w2_warps;
@@ -309,7 +340,7 @@ __global__ void __launch_bounds__(kW2Warps * 32, 1)
       uint64_t* bar = &full[warp][r & 1];
       mbar_expect_tx(bar, tx);
       tma_load_2d(st, sh ? &mqs : &mq, (rt & 15) * 64, row0, bar);
-      tma_load_2d(st + S * 512, sh ? &mss : &ms, (rt & 15) * 8, row0, bar);
+      tma_load_2d(st + S * 512, sh ? &mss : &ms, (rt & 15) * 8 * SB, row0, bar);
     }
     return go;
   };
@@ -380,9 +411,8 @@ __global__ void __launch_bounds__(kW2Warps * 32, 1)
               const int ks = ks0 + j;
               if (ks >= S) break;
               const uint4 q = *reinterpret_cast<const uint4*>(sq + ks * 512 + lane * 16);
-              const uint32_t sc = *reinterpret_cast<const unsigned short*>(ss + ks * 64 + lane * 2);
               uint32_t sg, sg8;
-              scale_splats(sc, &sg, &sg8);
+              lane_splats<SB>(lane_scales_smem<SB>(ss, (size_t)ks * 64 + lane * 2), &sg, &sg8);
               const uint32_t xw[8] = {hv[j][0].x, hv[j][0].y, hv[j][0].z, hv[j][0].w,
                                       hv[j][1].x, hv[j][1].y, hv[j][1].z, hv[j][1].w};
 #pragma unroll
@@ -470,7 +500,7 @@ cudaError_t launch_combine(const LayerDims& d, int64_t M, const PlanView& pv,
 
 static constexpr size_t kDecSmemLimit = 225 * 1024;
 
-template <int NT>
+template <int NT, int SB>
 static cudaError_t decode_impl(const LayerDims& d, int64_t M, const __half* x, const PlanView& pv,
                                Weights w13, Weights w2, Weights s13, Weights s2, __half* y,
                                __half* h, uint32_t* status, cudaStream_t stream, int num_sms) {
@@ -487,11 +517,12 @@ static cudaError_t decode_impl(const LayerDims& d, int64_t M, const __half* x, c
   a.y = y;
   a.M = (int)M;
   a.max_active = (int)((M * d.k_eff < d.e_eff) ? M * d.k_eff : d.e_eff);
+  a.sb = SB;
   const int P = (int)(M * d.k_eff);
   const int S2 = d.I / 64;
   const size_t smem13 =
       align_up((size_t)M * (d.H * 2 + 16), 16) + (size_t)8 * 2 * NT * 32 * 4 * sizeof(float);
-  const int st2 = (int)align_up((size_t)S2 * (512 + 64), 1024);
+  const int st2 = (int)align_up((size_t)S2 * (512 + 64 * SB), 1024);
   const size_t o_b = (size_t)P * 16 * sizeof(float) + P;
   // W2: as many expert warps as two ring stages each allow (at least one:
   // 2 x 37 KB + 34 KB at the largest I and M)
@@ -500,13 +531,13 @@ static cudaError_t decode_impl(const LayerDims& d, int64_t M, const __half* x, c
   if (w2_warps < 1) return cudaErrorInvalidValue;
   int per_sm = 0;
   cudaError_t e =
-      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_w13_kernel<NT>, 256, smem13);
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_w13_kernel<NT, SB>, 256, smem13);
   if (e != cudaSuccess) return e;
   const int n_items = a.max_active * (d.I / 16);
   const int g13 = std::max(1, std::min(n_items, num_sms * std::max(per_sm, 1)));
   const bool pdl = !trace_on();
   trace_mark(stream, kTraceW13, false);
-  e = launch_k(decode_w13_kernel<NT>, dim3(g13), dim3(256), smem13, stream, pdl, a);
+  e = launch_k(decode_w13_kernel<NT, SB>, dim3(g13), dim3(256), smem13, stream, pdl, a);
   if (e != cudaSuccess) return e;
   trace_mark(stream, kTraceW13, true);
   trace_mark(stream, kTraceW2, false);
@@ -514,15 +545,15 @@ static cudaError_t decode_impl(const LayerDims& d, int64_t M, const __half* x, c
   const uint64_t rows = (uint64_t)d.E * (d.H / 256) * S2;
   const uint64_t rows_sh = (uint64_t)(d.H / 256) * S2;
   if ((e = make_rows_map(&mq, w2.q, 16 * 512, rows, 512, S2)) != cudaSuccess) return e;
-  if ((e = make_rows_map(&ms, w2.s, 16 * 64, rows, 64, S2)) != cudaSuccess) return e;
+  if ((e = make_rows_map(&ms, w2.s, 16 * 64 * SB, rows, 64 * SB, S2)) != cudaSuccess) return e;
   mqs = mq;
   mss = ms;
   if (d.shared) {
     if ((e = make_rows_map(&mqs, s2.q, 16 * 512, rows_sh, 512, S2)) != cudaSuccess) return e;
-    if ((e = make_rows_map(&mss, s2.s, 16 * 64, rows_sh, 64, S2)) != cudaSuccess) return e;
+    if ((e = make_rows_map(&mss, s2.s, 16 * 64 * SB, rows_sh, 64 * SB, S2)) != cudaSuccess) return e;
   }
   const size_t smem2 = 1024 + (size_t)w2_warps * 2 * st2 + o_b;
-  e = launch_k(decode_w2_kernel<NT>, dim3(d.H / 16), dim3(kW2Warps * 32), smem2, stream, pdl, a,
+  e = launch_k(decode_w2_kernel<NT, SB>, dim3(d.H / 16), dim3(kW2Warps * 32), smem2, stream, pdl, a,
                w2_warps, st2, mq, ms, mqs, mss);
   if (e != cudaSuccess) return e;
   trace_mark(stream, kTraceW2, true);
@@ -533,8 +564,10 @@ static cudaError_t decode_impl(const LayerDims& d, int64_t M, const __half* x, c
 }
 
 cudaError_t decode_device_init() {
-  for (auto f : {(const void*)decode_w13_kernel<1>, (const void*)decode_w2_kernel<1>,
-                 (const void*)decode_w13_kernel<2>, (const void*)decode_w2_kernel<2>}) {
+  for (auto f : {(const void*)decode_w13_kernel<1, 1>, (const void*)decode_w2_kernel<1, 1>,
+                 (const void*)decode_w13_kernel<2, 1>, (const void*)decode_w2_kernel<2, 1>,
+                 (const void*)decode_w13_kernel<1, 2>, (const void*)decode_w2_kernel<1, 2>,
+                 (const void*)decode_w13_kernel<2, 2>, (const void*)decode_w2_kernel<2, 2>}) {
     cudaError_t e =
         cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDecSmemLimit);
     if (e != cudaSuccess) return e;
@@ -545,10 +578,16 @@ cudaError_t decode_device_init() {
 cudaError_t launch_decode_forward(const LayerDims& d, int64_t M, const __half* x,
                                   const PlanView& pv, Weights w13, Weights w2, Weights s13,
                                   Weights s2, __half* y, __half* h, float* partial,
-                                  uint32_t* status, cudaStream_t stream, int num_sms) {
+                                  uint32_t* status, cudaStream_t stream, int num_sms,
+                                  bool prepared) {
   (void)partial;
-  if (M <= 8) return decode_impl<1>(d, M, x, pv, w13, w2, s13, s2, y, h, status, stream, num_sms);
-  return decode_impl<2>(d, M, x, pv, w13, w2, s13, s2, y, h, status, stream, num_sms);
+  if (prepared) {
+    if (M <= 8)
+      return decode_impl<1, 2>(d, M, x, pv, w13, w2, s13, s2, y, h, status, stream, num_sms);
+    return decode_impl<2, 2>(d, M, x, pv, w13, w2, s13, s2, y, h, status, stream, num_sms);
+  }
+  if (M <= 8) return decode_impl<1, 1>(d, M, x, pv, w13, w2, s13, s2, y, h, status, stream, num_sms);
+  return decode_impl<2, 1>(d, M, x, pv, w13, w2, s13, s2, y, h, status, stream, num_sms);
 }
 
 }  // namespace moe

@@ -66,7 +66,8 @@ constexpr int kBStage = kTileRows * 128;  // B ring stage: one K step of up to 1
 constexpr int kBStages = 4;               // B ring stages (96 KiB)
 constexpr int kRS = 8;                    // raw weight stages
 constexpr int kRawQ = 16 * 512;           // raw q bytes per K step (16 fragment blocks)
-constexpr int kRawBytes = kRawQ + 16 * 64;
+// + their scales: 16 x 64 bytes raw E4M3, 16 x 128 bytes prepared FP16
+constexpr int kRawBytes = kRawQ + 16 * 128;
 // Warp roles: 0-7 dequantise and run the epilogue, 8 fills the token-row
 // operand, 12 issues the MMAs (and owns tensor memory), 13 streams raw weights.
 constexpr int kDqWarps = 8;
@@ -152,7 +153,24 @@ struct Unit {
   float g;
 };
 
-template <bool kW13>
+// Scale storage: SB = 1 raw E4M3 bytes, SB = 2 prepared FP16 scales (every
+// scale offset doubles; the two scales of a fragment lane become one 32-bit word).
+template <int SB>
+__device__ __forceinline__ uint32_t lane_scale_word(const char* p) {
+  if constexpr (SB == 1)
+    return *reinterpret_cast<const unsigned short*>(p);
+  else
+    return *reinterpret_cast<const uint32_t*>(p);
+}
+template <int SB>
+__device__ __forceinline__ uint32_t lane_scale_f16x2(uint32_t v) {
+  if constexpr (SB == 1)
+    return e4m3x2_to_f16x2(v);
+  else
+    return v;
+}
+
+template <bool kW13, int SB>
 __device__ __forceinline__ Unit load_unit(const LayerDims& d, const PlanView& pv, Weights w,
                                           Weights ws, int u, int upt) {
   Unit un;
@@ -166,11 +184,12 @@ __device__ __forceinline__ Unit load_unit(const LayerDims& d, const PlanView& pv
   const bool sh = (un.e == d.E);
   const size_t mat_q = kW13 ? (size_t)d.I * d.H : (size_t)d.H * d.I / 2;
   un.q = sh ? ws.q : w.q + (size_t)un.e * mat_q;
-  un.s = sh ? ws.s : w.s + (size_t)un.e * mat_q / 8;
+  un.s = sh ? ws.s : w.s + (size_t)un.e * mat_q / 8 * SB;
   un.g = sh ? ws.g[0] : w.g[un.e];
   return un;
 }
 
+template <int SB>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     grouped_w13_kernel(LayerDims d, PlanView pv, const __grid_constant__ CUtensorMap bmap,
                        Weights w, Weights ws, __half* __restrict__ h_out, uint32_t* status) {
@@ -219,7 +238,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     if (lane == 0) {
       uint32_t kr = 0;
       for (int u = blockIdx.x; u < n_units && !*abort; u += gridDim.x) {
-        const Unit un = load_unit<true>(d, pv, w, ws, u, upt);
+        const Unit un = load_unit<true, SB>(d, pv, w, ws, u, upt);
         const int grp = un.sub;  // the unit's 256 weight rows are one fragment group
         bool ok = true;
         for (int ks = 0; ks < S; ++ks) {
@@ -231,11 +250,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           }
           MOE_PROF(PROF_ADD(poff + 0, t0); t0 = clock64());
           char* dst = base + kOffRaw + slot * kRawBytes;
-          mbar_expect_tx(&sm->raw_full[slot], kRawBytes);
+          mbar_expect_tx(&sm->raw_full[slot], kRawQ + 16 * 64 * SB);
           // the group's 16 tiles are contiguous for each segment: two copies
           const size_t blk = ((size_t)grp * S + ks) * 16;
           bulk_g2s(dst, un.q + blk * 512, kRawQ, &sm->raw_full[slot]);
-          bulk_g2s(dst + kRawQ, un.s + blk * 64, kRawBytes - kRawQ, &sm->raw_full[slot]);
+          bulk_g2s(dst + kRawQ, un.s + blk * 64 * SB, 16 * 64 * SB, &sm->raw_full[slot]);
           MOE_DBG(6, kr);
           MOE_PROF(PROF_ADD(poff + 1, t0));
           ++kr;
@@ -254,7 +273,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       MOE_PROF(const long long t_all = clock64());
       for (int u = blockIdx.x; u < n_units && !*abort; u += gridDim.x, ++it) {
         MOE_PROF(long long t0 = clock64());
-        const Unit un = load_unit<true>(d, pv, w, ws, u, upt);
+        const Unit un = load_unit<true, SB>(d, pv, w, ws, u, upt);
         const uint32_t idesc = idesc_f16_f32(128, un.npad);
         MOE_PROF(PROF_ADD(poff + 3, t0); t0 = clock64());
         if (it > 0 && !wait_or_abort(&sm->tmem_empty, (it - 1) & 1, status, abort)) break;
@@ -306,7 +325,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       uint32_t kb = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < n_units && ok && !*abort; u += gridDim.x) {
-        const Unit un = load_unit<true>(d, pv, w, ws, u, upt);
+        const Unit un = load_unit<true, SB>(d, pv, w, ws, u, upt);
         const int nch = (un.npad + kBChunkRows - 1) / kBChunkRows;
         for (int ks = 0; ks < S; ++ks, ++kb) {
           const int bs = kb % kBStages;
@@ -353,7 +372,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // ---- warps 0-7: dequantise, then the unit's epilogue ---------------------------
     uint32_t kd = 0, it = 0;
     for (int u = blockIdx.x; u < n_units && !*abort; u += gridDim.x, ++it) {
-      const Unit un = load_unit<true>(d, pv, w, ws, u, upt);
+      const Unit un = load_unit<true, SB>(d, pv, w, ws, u, upt);
       bool ok = true;
       // this warp's two fragment blocks j = 2 warp + jj: rows 32 (warp % 4) + 16 jj
       // .. + 15 of A tile warp / 4
@@ -373,7 +392,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         for (int jj = 0; jj < 2; ++jj) {
           const int j = warp * 2 + jj;
           q[jj] = *reinterpret_cast<const uint4*>(raw + j * 512 + lane * 16);
-          sc[jj] = *reinterpret_cast<const unsigned short*>(raw + kRawQ + j * 64 + lane * 2);
+          sc[jj] = lane_scale_word<SB>(raw + kRawQ + (j * 64 + lane * 2) * SB);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm->raw_empty[rs]);  // the stage is in registers
@@ -390,7 +409,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         if (lane == 0) MOE_DBG(3, kd * kDqWarps + warp);
 #pragma unroll
         for (int jj = 0; jj < 2; ++jj) {
-          const uint32_t f = e4m3x2_to_f16x2(sc[jj]);
+          const uint32_t f = lane_scale_f16x2<SB>(sc[jj]);
           const uint32_t sg = __byte_perm(f, f, 0x1010), sg8 = __byte_perm(f, f, 0x3232);
           uint32_t x[4], y[4], z[4], w4[4];
           dequant8(q[jj].x, sg, x);   // row g,     elements 16c + 0..7
@@ -499,8 +518,8 @@ constexpr int kW2RawWarp = 17;
 constexpr int kW2BWarp = 18;
 constexpr int kW2ScaleWarp = 19;
 constexpr int kW2RawQ = 8 * 512;  // raw q bytes per segment (8 fragment blocks)
-constexpr int kW2RawS = 8 * 64;
-static_assert(2 * kW2RawQ <= kRawQ && 2 * kW2RawS <= kRawBytes - kRawQ, "W2 raw slot");
+constexpr int kW2RawS = 8 * 64;   // their raw scale bytes (x 2 when prepared)
+static_assert(2 * kW2RawQ <= kRawQ && 2 * 2 * kW2RawS <= kRawBytes - kRawQ, "W2 raw slot");
 static_assert(kAOff + kW2AS * (kW2KS / 2) <= kTmemCols, "W2 tensor memory over-committed");
 static_assert(kW2BStages == kW2AS, "one barrier per K step serves both rings");
 static_assert(kW2BStages * 2 * kBStage <= kBStages * kBStage, "W2 B ring inside the B region");
@@ -522,6 +541,7 @@ struct W2Smem {
 constexpr size_t w2_smem_bytes() { return 1024 + (size_t)kOffMeta + sizeof(W2Smem); }
 static_assert(w2_smem_bytes() <= 232448, "grouped W2 shared memory above the sm_103 limit");
 
+template <int SB>
 __global__ void __launch_bounds__(kW2Threads, 1)
     grouped_w2_kernel(LayerDims d, PlanView pv, const __grid_constant__ CUtensorMap bmap,
                       Weights w, Weights ws, float* __restrict__ partial, uint32_t* status) {
@@ -569,7 +589,7 @@ __global__ void __launch_bounds__(kW2Threads, 1)
       uint32_t kr = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < n_units && ok && !*abort; u += gridDim.x) {
-        const Unit un = load_unit<false>(d, pv, w, ws, u, upt);
+        const Unit un = load_unit<false, SB>(d, pv, w, ws, u, upt);
         const int grp = un.sub >> 1, half = un.sub & 1;
         for (int ks = 0; ks < S; ++ks, ++kr) {
           const int slot = kr % kRS;
@@ -578,14 +598,15 @@ __global__ void __launch_bounds__(kW2Threads, 1)
             break;
           }
           char* dst = base + kOffRaw + slot * kRawBytes;
-          mbar_expect_tx(&sm->raw_full[slot], 2 * (kW2RawQ + kW2RawS));
+          mbar_expect_tx(&sm->raw_full[slot], 2 * (kW2RawQ + kW2RawS * SB));
           // segments 2 ks and 2 ks + 1: q of segment c at c * kW2RawQ, s at
           // kRawQ + c * kW2RawS
 #pragma unroll
           for (int c = 0; c < 2; ++c) {
             const size_t blk = ((size_t)grp * (2 * S) + 2 * ks + c) * 16 + 8 * half;
             bulk_g2s(dst + c * kW2RawQ, un.q + blk * 512, kW2RawQ, &sm->raw_full[slot]);
-            bulk_g2s(dst + kRawQ + c * kW2RawS, un.s + blk * 64, kW2RawS, &sm->raw_full[slot]);
+            bulk_g2s(dst + kRawQ + c * kW2RawS * SB, un.s + blk * 64 * SB, kW2RawS * SB,
+                     &sm->raw_full[slot]);
           }
         }
       }
@@ -597,7 +618,7 @@ __global__ void __launch_bounds__(kW2Threads, 1)
     if (lane == 0) {
       uint32_t ka = 0, it = 0;
       for (int u = blockIdx.x; u < n_units && !*abort; u += gridDim.x, ++it) {
-        const Unit un = load_unit<false>(d, pv, w, ws, u, upt);
+        const Unit un = load_unit<false, SB>(d, pv, w, ws, u, upt);
         const uint32_t idesc = idesc_f16_f32(128, un.npad);
         const int b = it & 1;
         if (it >= 2 && !wait_or_abort(&sm->tmem_empty[b], ((it - 2) >> 1) & 1, status, abort))
@@ -638,7 +659,7 @@ __global__ void __launch_bounds__(kW2Threads, 1)
       uint32_t kb = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < n_units && ok && !*abort; u += gridDim.x) {
-        const Unit un = load_unit<false>(d, pv, w, ws, u, upt);
+        const Unit un = load_unit<false, SB>(d, pv, w, ws, u, upt);
         const int nch = (un.npad + kBChunkRows - 1) / kBChunkRows;
         for (int ks = 0; ks < S; ++ks, ++kb) {
           const int bs = kb % kW2BStages;
@@ -661,7 +682,7 @@ __global__ void __launch_bounds__(kW2Threads, 1)
     // free once the epilogue of unit it - 2 is done) ----
     uint32_t it = 0;
     for (int u = blockIdx.x; u < n_units && !*abort; u += gridDim.x, ++it) {
-      const Unit un = load_unit<false>(d, pv, w, ws, u, upt);
+      const Unit un = load_unit<false, SB>(d, pv, w, ws, u, upt);
       if (it >= 2 &&
           !warp_wait_or_abort(&sm->tmem_empty[it & 1], ((it - 2) >> 1) & 1, status, abort))
         break;
@@ -689,7 +710,7 @@ __global__ void __launch_bounds__(kW2Threads, 1)
     float(*stg)[32] = reinterpret_cast<float(*)[32]>(sm->stage[warp - kW2EpiWarp0]);
     uint32_t it = 0;
     for (int u = blockIdx.x; u < n_units && !*abort; u += gridDim.x, ++it) {
-      const Unit un = load_unit<false>(d, pv, w, ws, u, upt);
+      const Unit un = load_unit<false, SB>(d, pv, w, ws, u, upt);
       const int b = it & 1;
       if (!warp_wait_or_abort(&sm->accf[b], (it >> 1) & 1, status, abort)) break;
       if (!warp_wait_or_abort(&sm->wsc_full[b], (it >> 1) & 1, status, abort)) break;
@@ -748,8 +769,7 @@ __global__ void __launch_bounds__(kW2Threads, 1)
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
           qv[c] = *reinterpret_cast<const uint4*>(raw + c * kW2RawQ + jl * 512 + lane * 16);
-          sc[c] = *reinterpret_cast<const unsigned short*>(raw + kRawQ + c * kW2RawS + jl * 64 +
-                                                           lane * 2);
+          sc[c] = lane_scale_word<SB>(raw + kRawQ + (c * kW2RawS + jl * 64 + lane * 2) * SB);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm->raw_empty[rs]);  // the stage is in registers
@@ -765,7 +785,7 @@ __global__ void __launch_bounds__(kW2Threads, 1)
         tc_fence_after();
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
-          const uint32_t f = e4m3x2_to_f16x2(sc[c]);
+          const uint32_t f = lane_scale_f16x2<SB>(sc[c]);
           const uint32_t sg = __byte_perm(f, f, 0x1010), sg8 = __byte_perm(f, f, 0x3232);
           uint32_t x[4], y[4], z[4], w4[4];
           dequant8(qv[c].x, sg, x);
@@ -818,18 +838,24 @@ __global__ void gather_rows_kernel(LayerDims d, PlanView pv, const __half* __res
 }
 
 cudaError_t prefill_device_init() {
-  cudaError_t e = cudaFuncSetAttribute(grouped_w13_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)gemm_smem_bytes());
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(grouped_w2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)w2_smem_bytes());
+  for (auto f : {(const void*)grouped_w13_kernel<1>, (const void*)grouped_w13_kernel<2>}) {
+    cudaError_t e =
+        cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)gemm_smem_bytes());
+    if (e != cudaSuccess) return e;
+  }
+  for (auto f : {(const void*)grouped_w2_kernel<1>, (const void*)grouped_w2_kernel<2>}) {
+    cudaError_t e =
+        cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)w2_smem_bytes());
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 cudaError_t launch_prefill_forward(const LayerDims& d, int64_t M, const __half* x,
                                    const PlanView& pv, Weights w13, Weights w2, Weights s13,
                                    Weights s2, __half* y, __half* h, float* partial,
-                                   uint32_t* status, cudaStream_t stream, int num_sms) {
+                                   uint32_t* status, cudaStream_t stream, int num_sms,
+                                   bool prepared) {
   const int64_t P = M * d.k_eff;
   const int max_tiles = max_tiles_for(P, d.e_eff);
   const size_t smem = gemm_smem_bytes();
@@ -849,13 +875,13 @@ cudaError_t launch_prefill_forward(const LayerDims& d, int64_t M, const __half* 
   e = launch_k(gather_rows_kernel, dim3((unsigned)((P + 7) / 8)), dim3(256), 0, stream, pdl, d, pv,
                x, xg);
   if (e != cudaSuccess) return e;
-  e = launch_k(grouped_w13_kernel, dim3(g13), dim3(kGemmThreads), smem, stream, pdl, d, pv,
-               xmap, w13, s13, h, status);
+  e = launch_k(prepared ? grouped_w13_kernel<2> : grouped_w13_kernel<1>, dim3(g13),
+               dim3(kGemmThreads), smem, stream, pdl, d, pv, xmap, w13, s13, h, status);
   if (e != cudaSuccess) return e;
   trace_mark(stream, kTraceW13, true);
   trace_mark(stream, kTraceW2, false);
-  e = launch_k(grouped_w2_kernel, dim3(g2), dim3(kW2Threads), w2_smem_bytes(), stream, pdl, d,
-               pv, hmap, w2, s2, partial, status);
+  e = launch_k(prepared ? grouped_w2_kernel<2> : grouped_w2_kernel<1>, dim3(g2),
+               dim3(kW2Threads), w2_smem_bytes(), stream, pdl, d, pv, hmap, w2, s2, partial, status);
   if (e != cudaSuccess) return e;
   trace_mark(stream, kTraceW2, true);
   trace_mark(stream, kTraceCombine, false);

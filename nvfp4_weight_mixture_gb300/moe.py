@@ -42,7 +42,7 @@ EXPORTS = ["moe_nvfp4_abi_version", "moe_nvfp4_status_string", "moe_nvfp4_query"
            "moe_nvfp4_set_trace_events", "moe_nvfp4_forward_noalloc",
            "moe_nvfp4_last_cuda_error", "moe_nvfp4_set_small_router",
            "moe_nvfp4_dense_query", "moe_nvfp4_dense", "moe_fp8_quantize", "moe_fp8_dense",
-           "moe_nvfp4_prepare_scales", "moe_nvfp4_layer"]
+           "moe_nvfp4_prepare_scales", "moe_nvfp4_layer", "moe_nvfp4_set_decode_max_tokens"]
 TRACE_STEPS = ("plan", "w13", "w2", "combine")
 
 
@@ -103,6 +103,8 @@ def load_library(path: str = LIB_PATH):
         lib.moe_nvfp4_forward_noalloc.restype = I32
         lib.moe_nvfp4_set_trace_events.argtypes = [P, I32]
         lib.moe_nvfp4_set_trace_events.restype = I32
+        lib.moe_nvfp4_set_decode_max_tokens.argtypes = [I32]
+        lib.moe_nvfp4_set_decode_max_tokens.restype = I32
         lib.moe_nvfp4_set_small_router.argtypes = [I32]
         lib.moe_nvfp4_set_small_router.restype = I32
         lib.moe_nvfp4_dense_query.argtypes = [I64, I64, I64, ctypes.POINTER(SZ)]
@@ -170,11 +172,14 @@ def _expect(errors, name, t, dtype, n):
 
 
 def _expect_weights(errors, name, w, rows, k, n_mats):
+    """Codes, scales (raw E4M3 bytes as uint8, or prepared FP16 scales as
+    int16) and global scales of n_mats matrices of rows x k."""
     if w is None:
         return
     q, s, g = w
     _expect(errors, name + ".q", q, torch.uint8, n_mats * rows * k // 2)
-    _expect(errors, name + ".s", s, torch.uint8, n_mats * rows * k // 16)
+    _expect(errors, name + ".s", s, torch.int16 if s.dtype == torch.int16 else torch.uint8,
+            n_mats * rows * k // 16)
     _expect(errors, name + ".g", g, torch.float32, n_mats)
 
 
@@ -259,6 +264,11 @@ def set_trace_events(events):
     _check("moe_nvfp4_set_trace_events", lib.moe_nvfp4_set_trace_events(arr, len(events) // 2))
 
 
+def set_decode_max_tokens(m: int):
+    """Diagnostic: the forward's largest M on the decode kernels (0..16)."""
+    _check("moe_nvfp4_set_decode_max_tokens", load_library().moe_nvfp4_set_decode_max_tokens(int(m)))
+
+
 def set_small_router(force_ticket_router: bool):
     """Diagnostic: route M <= 16 through the 128-block ticket router (True) or
     choose automatically (False; the thread-block cluster where it fits)."""
@@ -318,6 +328,7 @@ def dequantize(q, s, n_mats, rows, k, layout):
 # ---- plan / forward ---------------------------------------------------------------------
 
 def _weights_c(w, layout):
+    """The C weight set; int16 scales are prepared FP16 scales."""
     if w is None:
         return None
     q, s, g = w
@@ -325,7 +336,7 @@ def _weights_c(w, layout):
     wc.q = q.data_ptr()
     wc.s = s.data_ptr()
     wc.g = g.data_ptr()
-    wc.layout = layout
+    wc.layout = layout | (SCALES_PREPARED if s.dtype == torch.int16 else 0)
     wc.reserved = 0
     return wc
 

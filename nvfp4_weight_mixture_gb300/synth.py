@@ -58,6 +58,8 @@ WORKLOADS = {
         Workload("prefill_m8192", 3, 8192, 2048, 512, 10, 512),
         Workload("prefill_m8192_zipf_shared", 4, 8192, 2048, 512, 10, 512,
                  bias="zipf", shared=True),
+        # the pages' M784 point (a prefill chunk; the grouped path's lower range)
+        Workload("prefill_m784", 3, 784, 2048, 512, 10, 512),
     ]
 }
 

@@ -203,3 +203,11 @@ def test_dense_entry_points_fail_closed_without_device(lib):
     assert lib.moe_fp8_quantize(None, 256, 64, 3, None, None, None, None) == -1
     assert lib.moe_nvfp4_prepare_scales(None, 0, None, None, None) == 0
     assert lib.moe_nvfp4_prepare_scales(None, 16, None, None, None) == -1
+
+
+def test_decode_bucket_switch_validates(lib):
+    """The diagnostic decode-bucket switch accepts 0..16 only (host-only)."""
+    assert lib.moe_nvfp4_set_decode_max_tokens(17) == -1
+    assert lib.moe_nvfp4_set_decode_max_tokens(-1) == -1
+    assert lib.moe_nvfp4_set_decode_max_tokens(0) == 0
+    assert lib.moe_nvfp4_set_decode_max_tokens(16) == 0

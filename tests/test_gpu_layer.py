@@ -376,3 +376,19 @@ def test_forward_given_repeated_ids(M):
     ref = case.oracle_forward(ids=ids, w=w)
     rel, mx = compare(y, ref)
     assert rel <= REL_L2_TOL and mx <= MAX_ABS_TOL, (rel, mx)
+
+
+@pytest.mark.parametrize("M", [1, 8, 16])
+def test_forward_grouped_bucket_at_small_m(M):
+    """Below the crossover the grouped tensor-core path also meets the bar
+    (the M bucket only picks the faster path): the decode bucket lowered to
+    0 sends M <= 16 through the grouped GEMMs on the small-M plan."""
+    case = Case(synth.with_tokens(DEC16, M))
+    moe.set_decode_max_tokens(0)
+    try:
+        y = case.gpu_forward(ids_from_oracle=True)
+    finally:
+        moe.set_decode_max_tokens(16)
+    rel, mx = compare(y, case.oracle_forward())
+    assert rel <= REL_L2_TOL and mx <= MAX_ABS_TOL, (rel, mx)
+    assert int(case.layer.status.item()) == 0
