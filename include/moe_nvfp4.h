@@ -390,6 +390,20 @@ int32_t moe_nvfp4_prepare_scales(const uint8_t* s, int64_t n, void* s16, uint32_
  * thread-safe.  Returns MOE_ERR_INVALID_ARG for another mode. */
 int32_t moe_nvfp4_set_small_router(int32_t mode);
 
+/* Failure-path test switch (no counterpart in the pages beyond their safe
+ * fallback of an unsafe launch: "[Kernel][SM70] Improve Qwen3.8 no-MTP
+ * concurrency", section "Test Result").  With hold_raw_producer = 1 the
+ * grouped W13 kernel (the forward at M > 16) issues none of its raw weight
+ * copies, so its consumers' bounded waits run out: they set MOE_ST_TIMEOUT in
+ * *status, stop, let copies in flight land, free tensor memory and return;
+ * the output is then invalid, the context stays usable.  wait_limit_cycles
+ * sets the grouped GEMMs' wait limit in SM clock cycles (<= 0: the default,
+ * 4e8 ~ 200 ms).  Set on the current device through `stream`, synchronously;
+ * process-wide; call with (0, 0) to restore.  MOE_ERR_INVALID_ARG for another
+ * hold value. */
+int32_t moe_nvfp4_set_wait_test(int32_t hold_raw_producer, int64_t wait_limit_cycles,
+                                void* stream);
+
 /* Diagnostic M bucket of moe_nvfp4_forward (no counterpart in the pages' text
  * beyond their M-bucketed dispatch: "[Kernel][SM70] Improve Qwen3.8 no-MTP
  * concurrency", section "Scope and related PRs", dynamic M2-M16 dispatch; a

@@ -97,6 +97,25 @@ size_t plan_bytes_for(const LayerDims& d, int64_t M) {
   return plan_layout(nullptr, M, d.k_eff, d.e_eff, d.E, d.H, nullptr);
 }
 
+// The plan buffer for any M <= max_tokens.  Every array grows with M except
+// the split router's partial logits (splits x M rows), which are largest at
+// the top of a 64-token tile count and vanish where the tensor-core router
+// takes over, so the maximum is taken over those points.
+size_t plan_bytes_max(const LayerDims& d, int64_t max_tokens) {
+  size_t best = plan_bytes_for(d, max_tokens);
+  for (int64_t t = 1; t <= 128; ++t) {
+    for (int64_t m : {64 * t - 1, 64 * t}) {
+      const int64_t mm = m < max_tokens ? m : max_tokens;
+      if (mm > kDecodeMaxTokens) {
+        const size_t b = plan_bytes_for(d, mm);
+        if (b > best) best = b;
+      }
+    }
+    if (64 * t >= max_tokens) break;
+  }
+  return best;
+}
+
 size_t ws_bytes_for(const LayerDims& d, int64_t M) {
   const int64_t P = M * d.k_eff;
   return align_up((size_t)P * d.I * sizeof(__half), 256) + (size_t)P * d.H * sizeof(float);
@@ -186,6 +205,16 @@ int32_t moe_nvfp4_set_trace_events(void* const* events, int32_t n_steps) {
   return MOE_OK;
 }
 
+int32_t moe_nvfp4_set_wait_test(int32_t hold_raw_producer, int64_t wait_limit_cycles,
+                                void* stream) {
+  if (hold_raw_producer != 0 && hold_raw_producer != 1) return MOE_ERR_INVALID_ARG;
+  int sms = 0;
+  int32_t rc = current_device(&sms);
+  if (rc) return rc;
+  return cuda_status(prefill_set_wait_test(hold_raw_producer, (long long)wait_limit_cycles,
+                                           static_cast<cudaStream_t>(stream)));
+}
+
 int32_t moe_nvfp4_set_decode_max_tokens(int32_t m) {
   if (m < 0 || m > kDecodeMaxTokens) return MOE_ERR_INVALID_ARG;
   g_decode_max_tokens = m;
@@ -231,7 +260,7 @@ int32_t moe_nvfp4_query(const moe_nvfp4_config* cfg, int64_t max_tokens, size_t*
   int sms = 0;
   rc = current_device(&sms);
   if (rc) return rc;
-  if (plan_bytes) *plan_bytes = plan_bytes_for(d, max_tokens);
+  if (plan_bytes) *plan_bytes = plan_bytes_max(d, max_tokens);
   if (ws_bytes) *ws_bytes = ws_bytes_for(d, max_tokens);
   return MOE_OK;
 }

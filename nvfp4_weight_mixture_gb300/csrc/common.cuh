@@ -58,9 +58,25 @@ struct PlanView {
   int32_t* dtab;      // [kDecodeMaxTokens * 33][kDtabInts] decode work table (M <= 16)
   float* rlogits;     // [min(M, kRouterChunk)][n_experts] router logits (M > 16)
   __half* wrt;        // [n_experts][hidden] transposed router weight (M > 16)
+  float* rpart;       // [ksplit][M][n_experts] partial logits of the split mma.sync router
 };
 
 __host__ __device__ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// K splits of the mma.sync router (M > 16 where the tensor-core router does
+// not run: E < 256, E % 16 != 0 or M < 128): enough 32-row K splits that
+// token tiles of 64 x splits fill ~128 SMs; 1 = no split (top-k in the
+// router's epilogue).  The same for every call with this M, H, E.
+constexpr int kRouterSplitRows = 32;
+__host__ __device__ inline int router_ksplit(int64_t M, int H, int E) {
+  if (M <= kDecodeMaxTokens) return 1;
+  if (E >= 256 && E % 16 == 0 && M >= 128) return 1;  // tensor-core router
+  const int64_t tiles = (M + 63) / 64;
+  int64_t s = (128 + tiles - 1) / tiles;
+  const int64_t smax = H / kRouterSplitRows;
+  if (s > smax) s = smax;
+  return s < 1 ? 1 : (int)s;
+}
 
 __host__ __device__ inline int max_tiles_for(int64_t pairs, int e_eff) {
   return (int)(e_eff + (pairs + kTileRows - 1) / kTileRows);
@@ -99,6 +115,8 @@ __host__ __device__ inline size_t plan_layout(char* base, int64_t M, int k_eff, 
   const int64_t Mr = M > kDecodeMaxTokens ? (M < kRouterChunk ? M : kRouterChunk) : 0;
   t.rlogits = (float*)take(sizeof(float) * (size_t)Mr * n_experts);
   t.wrt = (__half*)take(Mr > 0 ? sizeof(__half) * (size_t)n_experts * hidden : 0);
+  const int ks = router_ksplit(M, hidden, n_experts);
+  t.rpart = (float*)take(ks > 1 ? sizeof(float) * (size_t)ks * M * n_experts : 0);
   if (v) *v = t;
   return off;
 }

@@ -93,6 +93,10 @@ cudaError_t launch_prepare_scales(const uint8_t* s, int64_t n, uint16_t* out, ui
                                   cudaStream_t stream);
 cudaError_t dense_device_init();
 
+// Test switch of the grouped GEMMs (prefill.cu): hold back W13's raw-weight
+// producer and set the bounded waits' limit (SM cycles; <= 0: the default).
+cudaError_t prefill_set_wait_test(int hold_raw, long long limit_cycles, cudaStream_t stream);
+
 // Diagnostic: M <= 16 routes through the 128-block router (router.cu).
 void set_force_small_router(bool on);
 // Records the CUDA error behind a MOE_ERR_CUDA return for

@@ -109,6 +109,13 @@ constexpr size_t gemm_smem_bytes() {
 }
 static_assert(gemm_smem_bytes() <= 232448, "grouped GEMM shared memory above the sm_103 limit");
 
+// Wait limit of the grouped GEMMs' bounded waits (SM cycles) and a test switch
+// that holds back W13's raw-weight producer (so that its consumers' waits run
+// out): both set only by moe_nvfp4_set_wait_test; the defaults are the
+// library's 200 ms bound and no hold.
+static __device__ long long g_pf_wait_limit = kWaitTimeoutCycles;
+static __device__ int g_pf_hold_raw = 0;
+
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, uint32_t* status,
                                               volatile int* abort) {
   if (mbar_try_wait(bar, parity)) return true;
@@ -117,11 +124,19 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, ui
     for (int i = 0; i < 32; ++i)
       if (mbar_try_wait(bar, parity)) return true;
     if (*abort) return false;
-    if (clock64() - t0 > kWaitTimeoutCycles) {
+    if (clock64() - t0 > g_pf_wait_limit) {
       set_status(status, MOE_ST_TIMEOUT);
       *abort = 1;
       return false;
     }
+  }
+}
+
+// Waits (bounded by the same limit) for a phase whose completion is only
+// awaited so that copies in flight land before the block leaves.
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity) && clock64() - t0 < g_pf_wait_limit) {
   }
 }
 
@@ -234,8 +249,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   volatile int* abort = &sm->abort;
 
   if (warp == kRawWarp) {
-    // ---- raw weight producer (one lane) ---------------------------------------
-    if (lane == 0) {
+    // ---- raw weight producer (one lane; held back only by the test switch) ---
+    if (lane == 0 && !g_pf_hold_raw) {
       uint32_t kr = 0;
       for (int u = blockIdx.x; u < n_units && !*abort; u += gridDim.x) {
         const Unit un = load_unit<true, SB>(d, pv, w, ws, u, upt);
@@ -314,7 +329,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       // every MMA issued has completed before tensor memory is released
       tc_commit(&sm->drain);
       const long long t0 = clock64();
-      while (!mbar_try_wait(&sm->drain, 0) && clock64() - t0 < kWaitTimeoutCycles) {
+      while (!mbar_try_wait(&sm->drain, 0) && clock64() - t0 < g_pf_wait_limit) {
       }
     }
   } else if (warp == kBWarp0) {
@@ -347,7 +362,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       // of these phases completes once the dequantisers have arrived too, or
       // the wait gives up after an abort)
       for (uint32_t k = (kb > (uint32_t)kBStages ? kb - kBStages : 0); k < kb; ++k)
-        mbar_wait(&sm->full[k % kBStages], (k / kBStages) & 1, status);
+        drain_wait(&sm->full[k % kBStages], (k / kBStages) & 1);
     }
   } else if (warp > kBWarp0) {
     // spare warps (timeline build: two of them stamp when each raw and B stage
@@ -650,7 +665,7 @@ __global__ void __launch_bounds__(kW2Threads, 1)
       }
       tc_commit(&sm->drain);
       const long long t0 = clock64();
-      while (!mbar_try_wait(&sm->drain, 0) && clock64() - t0 < kWaitTimeoutCycles) {
+      while (!mbar_try_wait(&sm->drain, 0) && clock64() - t0 < g_pf_wait_limit) {
       }
     }
   } else if (warp == kW2BWarp) {
@@ -675,7 +690,7 @@ __global__ void __launch_bounds__(kW2Threads, 1)
         }
       }
       for (uint32_t k = (kb > (uint32_t)kW2BStages ? kb - kW2BStages : 0); k < kb; ++k)
-        mbar_wait(&sm->full[k % kW2BStages], (k / kW2BStages) & 1, status);
+        drain_wait(&sm->full[k % kW2BStages], (k / kW2BStages) & 1);
     }
   } else if (warp == kW2ScaleWarp) {
     // ---- g2 x combine weight of each row, one unit ahead (buffer it & 1 is
@@ -835,6 +850,17 @@ __global__ void gather_rows_kernel(LayerDims d, PlanView pv, const __half* __res
     const uint2 hi = __ldg(reinterpret_cast<const uint2*>(src + k0 + 16 * (c + 1) + 4 * r));
     dst[ch] = make_uint4(lo.x, lo.y, hi.x, hi.y);
   }
+}
+
+cudaError_t prefill_set_wait_test(int hold_raw, long long limit_cycles, cudaStream_t stream) {
+  const long long lim = limit_cycles > 0 ? limit_cycles : kWaitTimeoutCycles;
+  cudaError_t e = cudaMemcpyToSymbolAsync(g_pf_hold_raw, &hold_raw, sizeof(int), 0,
+                                          cudaMemcpyHostToDevice, stream);
+  if (e != cudaSuccess) return e;
+  e = cudaMemcpyToSymbolAsync(g_pf_wait_limit, &lim, sizeof(long long), 0, cudaMemcpyHostToDevice,
+                              stream);
+  if (e != cudaSuccess) return e;
+  return cudaStreamSynchronize(stream);
 }
 
 cudaError_t prefill_device_init() {

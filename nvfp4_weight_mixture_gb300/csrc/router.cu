@@ -310,6 +310,7 @@ __global__ void __launch_bounds__(256) plan_small_kernel(LayerDims d, int M, Pla
 // ---------------------------------------------------------------------------
 constexpr int kRtTok = 64;
 constexpr int kRtK = 32;
+static_assert(kRtK == kRouterSplitRows, "router K split granularity");
 
 __device__ __forceinline__ void ldsm_x4(uint32_t r[4], const void* p) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
@@ -329,13 +330,18 @@ size_t router_mma_smem(int E) {
   return pipe > logits ? pipe : logits;
 }
 
+// blockIdx.y = K split: 32-row K steps [y * steps_per_split, ...).  With
+// `partial` the block writes its split's FP32 partial logits [split][M][E]
+// (no bias; router_split_topk_kernel adds the splits up); without it (one
+// split) the top-k runs in the epilogue.
 __global__ void __launch_bounds__(512) router_mma_kernel(LayerDims d, int M,
                                                          const __half* __restrict__ x,
                                                          const __half* __restrict__ wr,
                                                          const float* __restrict__ bias,
                                                          const __half* __restrict__ wg,
                                                          int32_t* ids_user, float* w_user,
-                                                         PlanView pv) {
+                                                         PlanView pv, int steps_per_split,
+                                                         float* __restrict__ partial) {
   extern __shared__ __align__(16) char smem[];
   MOE_TL(kTlRouter);
   const int E = d.E, H = d.H;
@@ -371,11 +377,12 @@ __global__ void __launch_bounds__(512) router_mma_kernel(LayerDims d, int M,
 #pragma unroll
       for (int c = 0; c < 4; ++c) acc[a][b][c] = 0.f;
 
-  const int nk = H / kRtK;
-  load_stage(0, 0);
+  const int k_first = blockIdx.y * steps_per_split;
+  const int nk = min(H / kRtK - k_first, steps_per_split);
+  load_stage(0, k_first * kRtK);
   cp_async_commit();
   for (int it = 0; it < nk; ++it) {
-    if (it + 1 < nk) load_stage((it + 1) & 1, (it + 1) * kRtK);
+    if (it + 1 < nk) load_stage((it + 1) & 1, (k_first + it + 1) * kRtK);
     cp_async_commit();
     cp_async_wait<1>();
     __syncthreads();
@@ -404,8 +411,32 @@ __global__ void __launch_bounds__(512) router_mma_kernel(LayerDims d, int M,
     }
     __syncthreads();
   }
-  // logits -> shared memory (the pipeline buffers are dead now)
   const int g = lane >> 2, t4 = lane & 3;
+  if (partial) {
+    // this split's partial logits, in the accumulator layout
+    if (eg * 64 < E) {
+#pragma unroll
+      for (int mi = 0; mi < 2; ++mi)
+#pragma unroll
+        for (int nt = 0; nt < 8; ++nt) {
+          const int e = eg * 64 + nt * 8 + 2 * t4;
+          const int r = tg * 32 + mi * 16 + g;
+          if (e < E) {
+            float* p0 = partial + ((size_t)blockIdx.y * M + t0 + r) * E + e;
+            if (t0 + r < M) {
+              p0[0] = acc[mi][nt][0];
+              p0[1] = acc[mi][nt][1];
+            }
+            if (t0 + r + 8 < M) {
+              p0[8 * (size_t)E] = acc[mi][nt][2];
+              p0[8 * (size_t)E + 1] = acc[mi][nt][3];
+            }
+          }
+        }
+    }
+    return;
+  }
+  // logits -> shared memory (the pipeline buffers are dead now)
   if (eg * 64 < E) {
 #pragma unroll
     for (int mi = 0; mi < 2; ++mi)
@@ -433,6 +464,44 @@ __global__ void __launch_bounds__(512) router_mma_kernel(LayerDims d, int M,
     const float gamma = d.shared ? warp_gate(x + (int64_t)t * H, wg, H) : 0.f;
     store_route(d, t, id, w, gamma, ids_user, w_user, pv);
   }
+}
+
+// One warp per token: its logits as the K splits' partial sums added in split
+// order (+ bias), then top-k, renormalised weights, gate and the route.
+// block = 256 (8 tokens), dynamic shared memory 8 x E floats.
+__global__ void __launch_bounds__(256) router_split_topk_kernel(
+    LayerDims d, int M, int n_split, const float* __restrict__ partial,
+    const float* __restrict__ bias, const __half* __restrict__ x, const __half* __restrict__ wg,
+    int32_t* ids_user, float* w_user, PlanView pv) {
+  extern __shared__ float rs_rows[];
+  MOE_TL(kTlPlan);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * 8 + warp;
+  if (t >= M) return;
+  const int E = d.E;
+  float* row = rs_rows + (size_t)warp * E;
+  for (int e = lane; e < E; e += 32) {
+    const float* src = partial + (size_t)t * E + e;
+    const size_t stride = (size_t)M * E;
+    float sum = 0.f;
+    int s0 = 0;
+    for (; s0 + 8 <= n_split; s0 += 8) {
+      float v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) v[u] = __ldcg(src + (s0 + u) * stride);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) sum += v[u];
+    }
+    for (; s0 < n_split; ++s0) sum += __ldcg(src + s0 * stride);
+    row[e] = bias ? sum + bias[e] : sum;
+  }
+  __syncwarp();
+  int id;
+  float l;
+  warp_topk<false>(row, E, d.k, &id, &l);
+  const float w = warp_topk_weight(l, d.k);
+  const float gamma = d.shared ? warp_gate(x + (int64_t)t * d.H, wg, d.H) : 0.f;
+  store_route(d, t, id, w, gamma, ids_user, w_user, pv);
 }
 
 // ---------------------------------------------------------------------------
@@ -1165,8 +1234,16 @@ cudaError_t launch_plan(const LayerDims& d, int64_t M, const __half* x, const __
     if (e != cudaSuccess) return e;
   } else {
     const size_t smem = router_mma_smem(d.E);
-    router_mma_kernel<<<(Mi + kRtTok - 1) / kRtTok, 512, smem, stream>>>(
-        d, Mi, x, w_router, bias, w_gate, ids_user, w_user, pv);
+    const int ks = router_ksplit(M, d.H, d.E);
+    const int nk = d.H / kRtK, spl = (nk + ks - 1) / ks;
+    const int n_split = (nk + spl - 1) / spl;
+    const dim3 grid((Mi + kRtTok - 1) / kRtTok, n_split);
+    router_mma_kernel<<<grid, 512, smem, stream>>>(d, Mi, x, w_router, bias, w_gate, ids_user,
+                                                   w_user, pv, spl,
+                                                   n_split > 1 ? pv.rpart : nullptr);
+    if (n_split > 1)
+      router_split_topk_kernel<<<(Mi + 7) / 8, 256, sizeof(float) * 8 * d.E, stream>>>(
+          d, Mi, n_split, pv.rpart, bias, x, w_gate, ids_user, w_user, pv);
   }
   const int64_t P = M * d.k_eff;
   const int n_chunks = (int)((P + kPlanChunk - 1) / kPlanChunk);

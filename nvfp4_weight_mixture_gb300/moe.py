@@ -42,7 +42,8 @@ EXPORTS = ["moe_nvfp4_abi_version", "moe_nvfp4_status_string", "moe_nvfp4_query"
            "moe_nvfp4_set_trace_events", "moe_nvfp4_forward_noalloc",
            "moe_nvfp4_last_cuda_error", "moe_nvfp4_set_small_router",
            "moe_nvfp4_dense_query", "moe_nvfp4_dense", "moe_fp8_quantize", "moe_fp8_dense",
-           "moe_nvfp4_prepare_scales", "moe_nvfp4_layer", "moe_nvfp4_set_decode_max_tokens"]
+           "moe_nvfp4_prepare_scales", "moe_nvfp4_layer", "moe_nvfp4_set_decode_max_tokens",
+           "moe_nvfp4_set_wait_test"]
 TRACE_STEPS = ("plan", "w13", "w2", "combine")
 
 
@@ -103,6 +104,8 @@ def load_library(path: str = LIB_PATH):
         lib.moe_nvfp4_forward_noalloc.restype = I32
         lib.moe_nvfp4_set_trace_events.argtypes = [P, I32]
         lib.moe_nvfp4_set_trace_events.restype = I32
+        lib.moe_nvfp4_set_wait_test.argtypes = [I32, I64, P]
+        lib.moe_nvfp4_set_wait_test.restype = I32
         lib.moe_nvfp4_set_decode_max_tokens.argtypes = [I32]
         lib.moe_nvfp4_set_decode_max_tokens.restype = I32
         lib.moe_nvfp4_set_small_router.argtypes = [I32]
@@ -262,6 +265,12 @@ def set_trace_events(events):
     arr = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
     _trace_keep = (arr, events)
     _check("moe_nvfp4_set_trace_events", lib.moe_nvfp4_set_trace_events(arr, len(events) // 2))
+
+
+def set_wait_test(hold_raw_producer: bool, wait_limit_cycles: int = 0):
+    """Failure-path test switch of the grouped GEMMs (see the header)."""
+    _check("moe_nvfp4_set_wait_test", load_library().moe_nvfp4_set_wait_test(
+        1 if hold_raw_producer else 0, int(wait_limit_cycles), _stream()))
 
 
 def set_decode_max_tokens(m: int):

@@ -211,3 +211,4 @@ def test_decode_bucket_switch_validates(lib):
     assert lib.moe_nvfp4_set_decode_max_tokens(-1) == -1
     assert lib.moe_nvfp4_set_decode_max_tokens(0) == 0
     assert lib.moe_nvfp4_set_decode_max_tokens(16) == 0
+

@@ -392,3 +392,17 @@ def test_forward_grouped_bucket_at_small_m(M):
     rel, mx = compare(y, case.oracle_forward())
     assert rel <= REL_L2_TOL and mx <= MAX_ABS_TOL, (rel, mx)
     assert int(case.layer.status.item()) == 0
+
+
+def test_query_plan_bytes_cover_every_smaller_m():
+    """The plan size the query returns for max_tokens covers every M up to it:
+    the split router's partial logits make the per-M layout non-monotonic
+    (M = 127 needs more than M = 128, where the tensor-core router runs)."""
+    for E in (512, 136):
+        cfg = moe.make_config(2048, E, 10, 512)
+        top = {n: moe.query(cfg, n)[0] for n in (128, 784, 8192)}
+        for M in (1, 16, 17, 64, 65, 100, 127, 128, 300, 784):
+            pb = moe.query(cfg, M)[0]
+            for n, v in top.items():
+                if M <= n:
+                    assert pb <= v, (E, M, n, pb, v)
