@@ -278,7 +278,8 @@ __global__ void __launch_bounds__(kDnThreads, 1)
     if (!whole) {
       // the block that brings the group's last piece adds them up in K order
       const int b_first = dn_block_of(gs0, W, B), b_last = dn_block_of(gs1 - 1, W, B);
-      __threadfence();  // this lane's partial sums are visible before the ticket
+      // the warps' partial sums reach warp 0 through the mbarrier (CTA scope);
+      // warp 0's device-scope fence then orders all of them before the ticket
       __syncwarp();
       if (lane == 0) mbar_arrive(&written);
       if (warp == 0) {
@@ -286,6 +287,7 @@ __global__ void __launch_bounds__(kDnThreads, 1)
         if (lane == 0) {
           s_last = 0;
           if (all_in) {
+            __threadfence();
             const uint32_t t = atomicAdd(&tickets[G], 1u);
             s_last = (t == (uint32_t)(b_last - b_first));
             if (s_last) tickets[G] = 0u;  // ready for the next call
