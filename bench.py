@@ -64,6 +64,8 @@ def parse_args():
     p.add_argument("--tokens", type=int, default=None,
                    help="override the workload's token count (same shapes and seeds)")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-dense", action="store_true",
+                   help="skip the dense QPN2 / QPN8 projection records")
     p.add_argument("--crossover", default=None,
                    help="comma-separated token counts: time the forward's decode and grouped "
                         "paths at each M (one JSON line each) instead of the bench")
@@ -684,6 +686,71 @@ def run_crossover(args):
     return 0
 
 
+def time_dense(wl, fmt, args, dev):
+    """The dense few-row projection (QPN2 NVFP4 or QPN8 channel-FP8) of a
+    dense workload under the same protocol as the layer: 16 calls per CUDA
+    graph over 16 distinct allocations of the same weights, a 2x-L2 buffer
+    written before every replay.  Returns the record for the configs map."""
+    import torch
+    from nvfp4_weight_mixture_gb300 import moe, synth
+    w = torch.from_numpy(synth.dense_weight(wl)).to(dev)
+    if fmt == "fp8":
+        q, cs = moe.fp8_quantize(w, moe.LAYOUT_FP8_FRAGMENT)
+        mats = [(q.clone(), cs.clone()) for _ in range(STACK)]
+        wbytes = wl.N * wl.K + 4 * wl.N
+    else:
+        q, sc, g = moe.quantize(w[None], moe.LAYOUT_FRAGMENT)
+        mats = [(q.reshape(-1).clone(), sc.reshape(-1).clone(), g.clone()) for _ in range(STACK)]
+        wbytes = wl.N * wl.K // 2 + wl.N * wl.K // 16 + 4
+    del w
+    xs = [torch.from_numpy(synth.dense_activations(wl, v)).to(dev) for v in range(STACK)]
+    ys = [torch.empty((wl.M, wl.N), dtype=torch.float16, device=dev) for _ in range(STACK)]
+    ws = torch.zeros(max(moe.dense_query(wl.M, wl.N, wl.K), 16), dtype=torch.uint8, device=dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    def call(i):
+        if fmt == "fp8":
+            moe.fp8_dense(xs[i], mats[i][0], mats[i][1], y=ys[i], ws=ws)
+        else:
+            moe.dense(xs[i], mats[i], wl.N, y=ys[i], ws=ws)
+    with torch.cuda.stream(stream):
+        for i in range(STACK):
+            call(i)
+    stream.synchronize()
+    g_ = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_, stream=stream):
+        for i in range(STACK):
+            call(i)
+    reps = max(3, (args.steps or 320) // STACK)
+    ts = []
+    with torch.cuda.stream(stream):
+        for r in range(reps + 3):
+            flush.zero_()
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            g_.replay()
+            b.record(stream)
+            stream.synchronize()
+            if r >= 3:
+                ts.append(a.elapsed_time(b) / STACK)
+    us = statistics.median(ts) * 1e3
+    hbm, _, peak_src = load_peaks()
+    byts = wbytes + wl.M * wl.K * 2 + wl.M * wl.N * 2
+    achieved = byts / (us * 1e-6) / 1e9
+    del g_, mats, xs, ys, flush
+    torch.cuda.empty_cache()
+    return {"value": wl.M / (us * 1e-6), "unit": "tokens/s", "us_per_call": us,
+            "calls": reps * STACK,
+            "config": {"workload": wl.name, "format": "NVFP4 (QPN2)" if fmt == "nvfp4"
+                       else "channel-FP8 (QPN8)", "M": wl.M, "N": wl.N, "K": wl.K},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                         "frac": achieved / hbm, "peak_source": f"{peak_src} (hbm_gbs)",
+                         "algorithmic": {"bytes": byts}}}
+
+
 def run_gpu(args, workloads):
     """Times every workload (the first is the headline line; the others go
     into its "configs" map, each measured under the same protocol)."""
@@ -699,6 +766,12 @@ def run_gpu(args, workloads):
     dev = torch.device("cuda", local)
     moe.load_library()
     recs = [time_workload(wl, args, dist, dev, local, ws, rank) for wl in workloads]
+    dense = {}
+    if args.workload is None and not args.no_dense:
+        from nvfp4_weight_mixture_gb300 import synth
+        for dn in ("dense_gate_up_m16", "dense_down_m16"):
+            for fmt in ("nvfp4", "fp8"):
+                dense[f"{dn}_{fmt}"] = time_dense(synth.DENSE_WORKLOADS[dn], fmt, args, dev)
     if rank != 0:
         if dist:
             dist.destroy_process_group()
@@ -710,6 +783,8 @@ def run_gpu(args, workloads):
             line["configs"][wl.name] = {k_: r[k_] for k_ in (
                 "value", "unit", "ms_per_step", "steps", "warmup", "config", "roofline", "layer",
                 "e2e", "gpu_launches", "clocks", "wall_s_timed_region")}
+    if dense:
+        line.setdefault("configs", {}).update(dense)
     wl = workloads[0]
     if ws == 1 and not args.no_cpu_baseline:
         rate, cores, done, el = oracle_sample(wl, args.cpu_seconds)

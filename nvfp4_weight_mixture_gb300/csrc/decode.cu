@@ -199,6 +199,10 @@ __device__ __forceinline__ void w13_item(const DecodeArgs& p, const int* en, int
         }
       }
     }
+    if (ttid == 0) {
+      MOE_TL_MAX(44);
+      MOE_TL_MIN(45);
+    }
     // red[warp][tt][nt][lane][c]
 #pragma unroll
     for (int tt = 0; tt < 2; ++tt)
@@ -258,6 +262,10 @@ __global__ void __launch_bounds__(256, NT == 1 ? 3 : 2) decode_w13_kernel(const 
     s_ent[tid] = __ldcg(p.pv.dtab + (blockIdx.x / n_rtp) * kDtabInts + tid);
   cp_async_wait<0>();
   __syncthreads();
+  if (tid == 0) {
+    MOE_TL_MAX(34);
+    MOE_TL_MIN(35);
+  }
   const int n13 = s_nact * n_rtp;
   for (int i = blockIdx.x; i < n13; i += gridDim.x) {
     const int a = i / n_rtp, rp = i - a * n_rtp;

@@ -42,6 +42,7 @@ __device__ void plan_small_block(const LayerDims& d, int M, const int* src, cons
   const int P = M * d.k_eff, ne = d.e_eff;
   for (int i = tid; i < 768; i += nthr) s_cnt[i] = 0;
   __syncthreads();
+  if (tid == 0) MOE_TL_MAX(32);
   bool bad = false;
   for (int p = tid; p < P; p += nthr) {
     const int e = src[p];
@@ -1116,13 +1117,16 @@ __global__ void __launch_bounds__(kRcThreads, 1)
         my_l = key2f(gm);
       }
     }
+    if (tid == 0) MOE_TL_MAX(26);
     const float w = warp_topk_weight(my_l, k);
     const float gamma = d.shared ? warp_gate(x + (size_t)m * H, wg, H) : 0.f;
     store_route(d, m, my_id, w, gamma, ids_user, w_user, pv);
+    if (tid == 0) MOE_TL_MAX(28);
     if (lane < k) s_ids[m * d.k_eff + lane] = my_id;
     if (d.shared && lane == 0) s_ids[m * d.k_eff + k] = d.E;
   }
   __syncthreads();
+  if (tid == 0) MOE_TL_MAX(30);
   plan_small_block(d, M, s_ids, pv, status);
   if (tid == 0) MOE_TL_MIN(25);
 }

@@ -378,6 +378,40 @@ def test_forward_given_repeated_ids(M):
     assert rel <= REL_L2_TOL and mx <= MAX_ABS_TOL, (rel, mx)
 
 
+def test_forward_repeated_ids_across_a_tile_boundary():
+    """A token whose two pairs of one expert fall on both sides of a 192-row
+    plan tile boundary (two W13 / W2 units) against the oracle: token 0
+    routes once to expert 3, every other token twice, so expert 3's rows 191
+    and 192 belong to token 96."""
+    M = 120
+    wl = synth.custom("rep_straddle", M, 256, 16, 2, 128)
+    case = Case(wl)
+    ids = np.full((M, 2), 3, np.int32)
+    ids[0, 1] = 7
+    w = np.full(ids.shape, 0.5, np.float32)
+    y = case.gpu_forward(ids=ids, w=w)
+    ref = case.oracle_forward(ids=ids, w=w)
+    rel, mx = compare(y, ref)
+    assert rel <= REL_L2_TOL and mx <= MAX_ABS_TOL, (rel, mx)
+    assert int(case.layer.status.item()) == 0
+
+
+def test_grouped_batch_invariance():
+    """On the grouped path a token's output does not depend on the other
+    tokens of its call (its pairs are summed in slot order whatever the
+    batch, and an MMA column does not depend on the tile's other columns):
+    the first 40 tokens of an 80-token call equal the 40-token call bitwise
+    (same ids)."""
+    case = Case(synth.with_tokens(TINY, 80))
+    _, ids, w, _ = case.oracle_route()
+    y80 = case.gpu_forward(ids=ids, w=w)
+    xs = case.x_t[:40].contiguous()
+    case.layer.route(xs, torch.from_numpy(np.ascontiguousarray(ids[:40])).cuda(),
+                     torch.from_numpy(np.ascontiguousarray(w[:40])).cuda())
+    y40 = case.layer.forward_planned(xs).cpu().numpy()
+    np.testing.assert_array_equal(y80[:40].view(np.uint16), y40.view(np.uint16))
+
+
 @pytest.mark.parametrize("M", [1, 8, 16])
 def test_forward_grouped_bucket_at_small_m(M):
     """Below the crossover the grouped tensor-core path also meets the bar
