@@ -25,7 +25,8 @@
 // one group).  A producer thread fills a ring of stages, each one K segment
 // of a group (the group's 16 fragment tiles, contiguous, by one or two bulk
 // copies) plus the same segment of every token row (one 128-byte-swizzled
-// tensor-map tile).  Eight warps own two 16-row tiles each, dequantise their
+// tensor-map tile).  Sixteen warps own one 16-row tile each (enough warps per
+// SM to overlap the dequantise / MMA dependency chains), dequantise their
 // fragments in registers straight into mma.sync A operands and multiply with
 // up to four 8-token column tiles.  A piece that is a whole group writes y;
 // otherwise it writes FP32 partial sums and takes a ticket of its group, and
@@ -41,7 +42,8 @@
 
 namespace moe {
 
-constexpr int kDnWarps = 8;                         // consumer warps (two 16-row tiles each)
+constexpr int kDnWarps = 16;                        // consumer warps
+constexpr int kDnTpw = 16 / kDnWarps;               // 16-row tiles of a group per consumer warp
 constexpr int kDnThreads = (kDnWarps + 1) * 32;     // + one producer warp
 constexpr int kDnBlocks = 152;                      // fixed grid (one block per SM of a GB300)
 constexpr int kDnRingBudget = 216 * 1024;
@@ -146,16 +148,30 @@ __global__ void __launch_bounds__(kDnThreads, 1)
     fence_mbar_init();
   }
   __syncthreads();
+  // Programmatic dependent launch: the next grid may start as soon as SMs
+  // free up.  The weights are inputs of the call, not results of the previous
+  // grid, so the first stages' weight copies go out before waiting for it;
+  // the token rows, the workspace and y are touched only after the wait.
+  pdl_launch_dependents();
 
   if (warp == kDnWarps) {
     // ---- producer: one stage per K segment of the block's range ----
     if (lane == 0) {
       uint32_t k = 0;
+      int pre_seg[R::kStages];  // first K segment of each stage issued before the wait
+      bool waited = false;
       for (int64_t i = r0, n; i < r1; i += n, ++k) {
         // up to kCH consecutive segments of one group: (group i / segs,
         // segments i % segs ..): their tiles are contiguous in the fragment layout
         n = min(min((int64_t)F::kCH, r1 - i), (int64_t)(segs - i % segs));
         const int st = k % R::kStages;
+        if (!waited && k == (uint32_t)R::kStages) {
+          // the ring is full: wait for the previous grid, then the deferred token rows
+          pdl_wait();
+          waited = true;
+          for (uint32_t j = 0; j < k; ++j)
+            tma_load_3d(base + j * R::kStage + R::kX, &xmap, 0, 0, pre_seg[j], &full[j]);
+        }
         if (!mbar_wait(&empty[st], ((k / R::kStages) & 1) ^ 1, status)) break;
         char* dst = base + st * R::kStage;
         mbar_expect_tx(&full[st], (uint32_t)(n * (F::kQ + F::kS) + F::kCH * NT * 8 * 128));
@@ -163,7 +179,15 @@ __global__ void __launch_bounds__(kDnThreads, 1)
         if (F::kS)
           bulk_g2s(dst + R::kSOff, s + (size_t)i * F::kS, (uint32_t)(n * F::kS), &full[st]);
         // kCH segments of the token rows (those past K read as zeros, unused)
-        tma_load_3d(dst + R::kX, &xmap, 0, 0, (int)(i % segs), &full[st]);
+        if (waited)
+          tma_load_3d(dst + R::kX, &xmap, 0, 0, (int)(i % segs), &full[st]);
+        else
+          pre_seg[k] = (int)(i % segs);
+      }
+      if (!waited) {
+        pdl_wait();
+        for (uint32_t j = 0; j < k; ++j)
+          tma_load_3d(base + j * R::kStage + R::kX, &xmap, 0, 0, pre_seg[j], &full[j]);
       }
       // copies still in flight land before the block exits (bounded waits)
       for (uint32_t j = (k > (uint32_t)R::kStages ? k - R::kStages : 0); j < k; ++j)
@@ -172,16 +196,17 @@ __global__ void __launch_bounds__(kDnThreads, 1)
     return;
   }
 
-  // ---- consumers: warp w owns tiles 2w and 2w + 1 of the group ----
-  const int tile0 = 2 * warp;
+  // ---- consumers: warp w owns tiles kDnTpw w .. kDnTpw w + kDnTpw - 1 of the group ----
+  pdl_wait();  // the workspace and y of the previous grid are free
+  const int tile0 = kDnTpw * warp;
   uint32_t k = 0, n_split = 0;
   int p = 0;
   for (int64_t i0 = r0; i0 < r1; ++p) {
     const int G = (int)(i0 / segs);
     const int64_t i1 = min(r1, (int64_t)(G + 1) * segs);  // this piece: [i0, i1)
-    float acc[2][NT][4];
+    float acc[kDnTpw][NT][4];
 #pragma unroll
-    for (int a = 0; a < 2; ++a)
+    for (int a = 0; a < kDnTpw; ++a)
 #pragma unroll
       for (int b = 0; b < NT; ++b)
 #pragma unroll
@@ -212,7 +237,7 @@ __global__ void __launch_bounds__(kDnThreads, 1)
         const char* qb = sb + c * F::kQ;
         const char* sc_b = sb + R::kSOff + c * F::kS;
 #pragma unroll
-        for (int tt = 0; tt < 2; ++tt) {
+        for (int tt = 0; tt < kDnTpw; ++tt) {
           const int j = tile0 + tt;
           if constexpr (FMT == kDenseFp8) {
             // block of 1024 bytes: row g's 16 codes at 16 L, row g + 8's at 512 + 16 L
@@ -259,7 +284,7 @@ __global__ void __launch_bounds__(kDnThreads, 1)
     // c0 (row g, token 2 t4), c1 (g, 2 t4 + 1), c2 (g + 8, 2 t4), c3 (g + 8, 2 t4 + 1)
     float* slot = part + ((size_t)blockIdx.x * pieces + p) * M * 256;
 #pragma unroll
-    for (int tt = 0; tt < 2; ++tt)
+    for (int tt = 0; tt < kDnTpw; ++tt)
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
@@ -290,7 +315,12 @@ __global__ void __launch_bounds__(kDnThreads, 1)
             __threadfence();
             const uint32_t t = atomicAdd(&tickets[G], 1u);
             s_last = (t == (uint32_t)(b_last - b_first));
-            if (s_last) tickets[G] = 0u;  // ready for the next call
+            if (s_last) {
+              tickets[G] = 0u;  // ready for the next call
+              // acquire side: the other blocks' pieces are visible to this
+              // block's threads, which are ordered after this fence by `decided`
+              __threadfence();
+            }
           }
           mbar_arrive(&decided);
         }
@@ -299,7 +329,6 @@ __global__ void __launch_bounds__(kDnThreads, 1)
       ++n_split;
       if (!__all_sync(0xffffffffu, dec)) break;
       if (s_last) {
-        __threadfence();
         for (int e = tid; e < M * 64; e += kDnWarps * 32) {  // one float4 of y each
           const int m = e >> 6, r = (e & 63) * 4;
           float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -354,7 +383,7 @@ static cudaError_t dense_go(int M, int N, int K, const DenseSplit& sp, const CUt
                             const uint8_t* q, const uint8_t* s, const float* scale, char* ws,
                             __half* y, uint32_t* status, cudaStream_t stream) {
   return launch_k(dense_kernel<FMT, NT>, dim3(sp.blocks), dim3(kDnThreads), DnRing<FMT>::kSmem,
-                  stream, false, M, N, K, sp.pieces, xmap, q, s, scale, ws, y, status);
+                  stream, !trace_on(), M, N, K, sp.pieces, xmap, q, s, scale, ws, y, status);
 }
 
 template <int FMT>
