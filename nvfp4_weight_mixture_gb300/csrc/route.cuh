@@ -72,11 +72,11 @@ __device__ __forceinline__ void warp_topk(const float* row, int E, int k, int* o
 __device__ __forceinline__ float warp_topk_weight(float my_l, int k) {
   const int lane = threadIdx.x & 31;
   const float lmax = __shfl_sync(0xffffffffu, my_l, 0);
-  const float e = (lane < k) ? expf(my_l - lmax) : 0.f;
+  const float e = (lane < k) ? __expf(my_l - lmax) : 0.f;
   float s = e;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-  return e / s;
+  return __fdividef(e, s);
 }
 
 // gamma = sigmoid(x . w_g), one warp, x and w_g FP16 of length H (H % 64 == 0)

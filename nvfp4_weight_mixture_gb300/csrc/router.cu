@@ -29,108 +29,189 @@ namespace moe {
 // ---------------------------------------------------------------------------
 // Plan of up to kDecodeMaxTokens * (32 + 1) pairs by one block of 256 threads.
 // `src` (shared memory) holds the M * k_eff expert ids of the pairs.  Also
-// writes the decode work table.
+// writes the decode work table.  Three steps separated by barriers:
+//   1. each pair's plan position, by direct comparison over the pairs (valid
+//      pairs of a lower expert, plus those of the same expert and a lower pair
+//      id): perm and inv; the first pair of each expert records the expert's
+//      row count;
+//   2. each active expert's rank and first tile: at up to 64 pairs by direct
+//      comparison over the experts' first pairs, above that by a block scan
+//      over the plan positions (an expert starts where the expert changes);
+//      active, tiles and the sorted active list in shared memory;
+//   3. counts and offsets of every expert (binary search in the active list),
+//      the header and the decode work table (16-byte stores).
 // ---------------------------------------------------------------------------
 __device__ void plan_small_block(const LayerDims& d, int M, const int* src, const PlanView& pv,
                                  uint32_t* status) {
-  __shared__ int s_ids[kDtabEntries];
-  __shared__ int s_perm[kDtabEntries];
-  __shared__ int s_cnt[768];
-  __shared__ int s_off[768];
-  __shared__ int s_act[kDtabEntries];
-  const int tid = threadIdx.x, nthr = blockDim.x;
+  __shared__ int s_ids[kDtabEntries];    // expert of each pair, -1 if invalid
+  __shared__ int s_perm[kDtabEntries];   // pair at each plan position
+  __shared__ int s_cnt1[kDtabEntries];   // rows of the pair's expert if it is the first, else 0
+  __shared__ int s_pos1[kDtabEntries];   // plan position of an expert's first pair
+  __shared__ int s_ae[kDtabEntries], s_aoff[kDtabEntries], s_acnt[kDtabEntries];
+  __shared__ int s_nv, s_na, s_nt;
+  const int tid = threadIdx.x, nthr = blockDim.x, lane = tid & 31;
   const int P = M * d.k_eff, ne = d.e_eff;
-  for (int i = tid; i < 768; i += nthr) s_cnt[i] = 0;
+  if (tid == 0) {
+    s_nv = 0;
+    s_na = 0;
+    s_nt = 0;
+  }
   __syncthreads();
-  if (tid == 0) MOE_TL_MAX(32);
   bool bad = false;
+  int nvalid = 0;
   for (int p = tid; p < P; p += nthr) {
     const int e = src[p];
     const bool ok = pair_valid(e, p % d.k_eff, d);
     s_ids[p] = ok ? e : -1;
-    if (ok)
-      atomicAdd(&s_cnt[e], 1);
-    else
-      bad = true;
+    bad = bad || !ok;
+    nvalid += ok;
   }
   if (bad) set_status(status, MOE_ST_INVALID_ID);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) nvalid += __shfl_xor_sync(0xffffffffu, nvalid, o);
+  if (lane == 0 && nvalid) atomicAdd(&s_nv, nvalid);
   __syncthreads();
   if (tid == 0) MOE_TL_MAX(36);
-  // experts [3 tid, 3 tid + 3): counts, active flags, tiles -> block scan
-  int c3[3], sc = 0, sa = 0, st = 0;
-#pragma unroll
-  for (int j = 0; j < 3; ++j) {
-    c3[j] = s_cnt[3 * tid + j];
-    sc += c3[j];
-    sa += c3[j] > 0;
-    st += (c3[j] + kTileRows - 1) / kTileRows;
-  }
-  int tot[3];
-  block_scan3(sc, sa, st, tot);
-  if (tid == 0) MOE_TL_MAX(38);
-#pragma unroll
-  for (int j = 0; j < 3; ++j) {
-    const int e = 3 * tid + j;
-    if (e < ne) {
-      s_off[e] = sc;
-      pv.counts[e] = c3[j];
-      pv.offsets[e] = sc;
-      if (c3[j] > 0) {
-        pv.active[sa] = e;
-        s_act[sa] = e;
-      }
-      for (int r0 = 0; r0 < c3[j]; r0 += kTileRows, ++st)
-        reinterpret_cast<int4*>(pv.tiles)[st] = make_int4(e, r0, min(kTileRows, c3[j] - r0), 0);
-    }
-    sc += c3[j];
-    sa += c3[j] > 0;
-  }
-  if (tid == 0) {
-    pv.offsets[ne] = tot[0];
-    pv.hdr->M = M;
-    pv.hdr->k_eff = d.k_eff;
-    pv.hdr->e_eff = ne;
-    pv.hdr->n_valid = tot[0];
-    pv.hdr->n_active = tot[1];
-    pv.hdr->n_tiles = tot[2];
-  }
-  __syncthreads();
-  if (tid == 0) MOE_TL_MAX(40);
+  const int nv = s_nv;
+  // 1. positions
   for (int p = tid; p < P; p += nthr) {
     const int e = s_ids[p];
+    s_cnt1[p] = 0;
     if (e < 0) {
       pv.inv[p] = -1;
       continue;
     }
-    int r = 0;
-    for (int q = 0; q < p; ++q) r += (s_ids[q] == e);
-    const int pos = s_off[e] + r;
+    int less = 0, before = 0, total = 0;
+    for (int q = 0; q < P; ++q) {
+      const int eq = s_ids[q];
+      less += (eq >= 0 && eq < e);
+      before += (eq == e && q < p);
+      total += (eq == e);
+    }
+    const int pos = less + before;
     pv.perm[pos] = p;
-    s_perm[pos] = p;
     pv.inv[p] = pos;
+    s_perm[pos] = p;
+    if (before == 0) {
+      s_cnt1[p] = total;
+      s_pos1[p] = pos;
+    }
   }
   __syncthreads();
-  if (tid == 0) MOE_TL_MAX(42);
-  // decode work table: every entry up to the largest active-expert count
-  const int n_active = tot[1];
-  const int max_active = min(P, ne);
-  for (int i = tid; i < max_active * kDtabInts; i += nthr) {
-    const int a = i / kDtabInts, f = i - a * kDtabInts;
-    int v = -1;
-    if (a < n_active) {
-      const int e = s_act[a];
-      const int off = s_off[e];
-      if (f == 0)
-        v = e;
-      else if (f == 1)
-        v = off;
-      else if (f == 2)
-        v = s_cnt[e];
-      else if (f >= 4 && f - 4 < s_cnt[e])
-        v = s_perm[off + f - 4];
+  if (tid == 0) MOE_TL_MAX(38);
+  // 2. active experts and tiles
+  if (P <= 64) {
+    // one pair per thread: the first pair of each expert counts the lower
+    // experts' first pairs and their tiles
+    const int p = tid;
+    const int c = p < P ? s_cnt1[p] : 0;
+    if (c != 0) {
+      const int e = s_ids[p];
+      int a = 0, t0 = 0, higher = 0;
+      for (int q = 0; q < P; ++q) {
+        const int cq = s_cnt1[q];
+        if (cq == 0) continue;
+        const int eq = s_ids[q];
+        if (eq < e) {
+          ++a;
+          t0 += (cq + kTileRows - 1) / kTileRows;
+        }
+        higher += eq > e;
+      }
+      s_ae[a] = e;
+      s_aoff[a] = s_pos1[p];
+      s_acnt[a] = c;
+      pv.active[a] = e;
+      const int nt_e = (c + kTileRows - 1) / kTileRows;
+      for (int r = 0; r < nt_e; ++r)
+        reinterpret_cast<int4*>(pv.tiles)[t0 + r] =
+            make_int4(e, r * kTileRows, min(kTileRows, c - r * kTileRows), 0);
+      if (higher == 0) {  // the highest active expert knows the totals
+        s_na = a + 1;
+        s_nt = t0 + nt_e;
+      }
     }
-    pv.dtab[i] = v;
+  } else {
+    // positions 3 tid .. 3 tid + 2: an expert starts at each position whose
+    // pair is its expert's first (the lowest pair id comes first)
+    int fl[3], cn[3], sa = 0, st = 0;
+#pragma unroll
+    for (int i = 0; i < 3; ++i) {
+      const int j = 3 * tid + i;
+      cn[i] = j < nv ? s_cnt1[s_perm[j]] : 0;
+      fl[i] = cn[i] != 0;
+      sa += fl[i];
+      st += fl[i] ? (cn[i] + kTileRows - 1) / kTileRows : 0;
+    }
+    int zero = 0, tot[3];
+    block_scan3(sa, st, zero, tot);
+#pragma unroll
+    for (int i = 0; i < 3; ++i) {
+      if (!fl[i]) continue;
+      const int j = 3 * tid + i, e = s_ids[s_perm[j]], c = cn[i];
+      s_ae[sa] = e;
+      s_aoff[sa] = j;
+      s_acnt[sa] = c;
+      pv.active[sa] = e;
+      for (int r0 = 0; r0 < c; r0 += kTileRows, ++st)
+        reinterpret_cast<int4*>(pv.tiles)[st] = make_int4(e, r0, min(kTileRows, c - r0), 0);
+      ++sa;
+    }
+    if (tid == 0) {
+      s_na = tot[0];
+      s_nt = tot[1];
+    }
   }
+  __syncthreads();
+  if (tid == 0) MOE_TL_MAX(40);
+  // 3. counts / offsets of every expert, header, work table
+  const int na = s_na;
+  for (int e = tid; e <= ne; e += nthr) {
+    int lo = 0, hi = na;  // first active expert >= e
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if (s_ae[mid] < e)
+        lo = mid + 1;
+      else
+        hi = mid;
+    }
+    if (e == ne) {
+      pv.offsets[ne] = nv;
+    } else {
+      pv.offsets[e] = lo < na ? s_aoff[lo] : nv;
+      pv.counts[e] = (lo < na && s_ae[lo] == e) ? s_acnt[lo] : 0;
+    }
+  }
+  if (tid == 0) {
+    pv.hdr->M = M;
+    pv.hdr->k_eff = d.k_eff;
+    pv.hdr->e_eff = ne;
+    pv.hdr->n_valid = nv;
+    pv.hdr->n_active = na;
+    pv.hdr->n_tiles = s_nt;
+  }
+  // decode work table: every entry up to the largest active-expert count, as
+  // five 16-byte groups (expert, first position, rows, -1 | first 16 pair ids)
+  static_assert(kDtabInts == 20, "a work-table entry is five 16-byte groups");
+  const int max_active = min(P, ne);
+  for (int i = tid; i < max_active * 5; i += nthr) {
+    const int a = i / 5, f4 = i - a * 5;
+    int4 v = make_int4(-1, -1, -1, -1);
+    if (a < na) {
+      const int off = s_aoff[a], cnt = s_acnt[a];
+      if (f4 == 0) {
+        v = make_int4(s_ae[a], off, cnt, -1);
+      } else {
+        const int r = 4 * (f4 - 1);
+        v.x = r < cnt ? s_perm[off + r] : -1;
+        v.y = r + 1 < cnt ? s_perm[off + r + 1] : -1;
+        v.z = r + 2 < cnt ? s_perm[off + r + 2] : -1;
+        v.w = r + 3 < cnt ? s_perm[off + r + 3] : -1;
+      }
+    }
+    reinterpret_cast<int4*>(pv.dtab)[i] = v;
+  }
+  if (tid == 0) MOE_TL_MAX(42);
 }
 
 // ---------------------------------------------------------------------------
@@ -881,7 +962,7 @@ __device__ __forceinline__ void st_dsmem_u32x2(uint32_t a, uint32_t v0, uint32_t
 // the shared-memory carve (all offsets 1024-byte aligned).
 struct RouterClusterPlan {
   int C, Es, tr, ntw, stages;
-  size_t xs, ring, stage, lg, total;
+  size_t xs, cand, ring, stage, lg, total;
 };
 
 __host__ __device__ inline RouterClusterPlan router_cluster_plan(int H, int E, int k, int M,
@@ -897,16 +978,16 @@ __host__ __device__ inline RouterClusterPlan router_cluster_plan(int H, int E, i
   while (per_warp % n != 0 || (per_warp / n) % 16 != 0) ++n;
   p.tr = per_warp / n;
   p.ntw = n;
-  // token rows (M x (H + 8) halves) and a 16-byte zero row; after the first
-  // cluster barrier CTA 0 reuses the region for the candidates (M x C x k)
-  const size_t xs = (size_t)M * (H + 8) * 2 + 16;
-  const size_t cand = (size_t)M * p.C * k * 8;
-  p.xs = align_up(xs > cand ? xs : cand, 1024);
+  // token rows (M x (H + 8) halves) and a 16-byte zero row, then the slices'
+  // top-k candidates (M x C x k), which the CTAs write into CTA 0 while it may
+  // still read its token rows
+  p.xs = align_up((size_t)M * (H + 8) * 2 + 16, 1024);
+  p.cand = align_up((size_t)M * p.C * k * 8, 1024);
   p.lg = align_up((size_t)kDecodeMaxTokens * p.Es * 4, 1024);
   // a stage also holds the warp's partial sums ([16][Es] FP32) at the end
   const size_t tile = (size_t)p.tr * p.Es * 2, red = (size_t)kDecodeMaxTokens * p.Es * 4;
   p.stage = align_up(tile > red ? tile : red, 1024);
-  const size_t fixed = 1024 + p.xs + p.lg;
+  const size_t fixed = 1024 + p.xs + p.cand + p.lg;
   int st = (int)((kRcSmemBudget > fixed ? kRcSmemBudget - fixed : 0) / (kRcWarps * p.stage));
   if (st > 2) st = 2;
   if (st > p.ntw) st = p.ntw;
@@ -934,8 +1015,9 @@ __global__ void __launch_bounds__(kRcThreads, 1)
   const int rb = Es * 2;  // bytes of one W_r tile row
   __half* xs = reinterpret_cast<__half*>(rsm);
   const char* zero_row = rsm + (size_t)M * (H + 8) * 2;
-  float* lg = reinterpret_cast<float*>(rsm + L.xs);  // [16][Es] logits of the slice
-  char* ring = rsm + L.xs + L.lg;
+  char* cand_region = rsm + L.xs;                           // [M][C][k] (key, id), CTA 0
+  float* lg = reinterpret_cast<float*>(rsm + L.xs + L.cand);  // [16][Es] logits of the slice
+  char* ring = rsm + L.xs + L.cand + L.lg;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, t4 = lane & 3;
   char* my_ring = ring + (size_t)warp * stages * L.stage;
@@ -1080,14 +1162,13 @@ __global__ void __launch_bounds__(kRcThreads, 1)
     }
   }
   if (tid == 0) MOE_TL_MIN(21);
-  cluster_sync_all();  // CTA 0 no longer reads its token rows: they become the candidates
   // ---- candidates into CTA 0: cand[(m C + rank) k + j] = (key, id) ----
 #pragma unroll
   for (int mm = 0; mm < 2; ++mm) {
     const int m = warp + kRcWarps * mm;
     if (m < M && lane < k)
-      st_dsmem_u32x2(dsmem_addr(rsm + (((size_t)m * C + rank) * k + lane) * 8, 0), ckey[mm],
-                     (uint32_t)cid[mm]);
+      st_dsmem_u32x2(dsmem_addr(cand_region + (((size_t)m * C + rank) * k + lane) * 8, 0),
+                     ckey[mm], (uint32_t)cid[mm]);
   }
   cluster_sync_all();  // every candidate is in CTA 0
   if (tid == 0) MOE_TL_MIN(23);
@@ -1098,7 +1179,7 @@ __global__ void __launch_bounds__(kRcThreads, 1)
   // Each slice's candidates are in descending order (ties: lower id first),
   // so the merge keeps one head per slice (lane c < C) and, k times, takes
   // the largest head (ties: the lower id) and advances that slice.
-  const uint2* cand = reinterpret_cast<const uint2*>(rsm);
+  const uint2* cand = reinterpret_cast<const uint2*>(cand_region);
   for (int m = warp; m < M; m += kRcWarps) {
     const uint2* lst = cand + ((size_t)m * C + lane) * k;
     int ptr = 0;
