@@ -14,6 +14,9 @@ outside its events.  Exactly --steps calls are timed (the remainder of a
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workloads A,B,..]
     python bench.py --workload NAME        # one workload only
     python bench.py --impl reference ...   # the CPU oracle arm
+    python bench.py --only-dense           # the dense projection records only
+    python bench.py --stack 1 ...          # one weight allocation (profiler captures
+                                           # that must hold little device memory)
 
 Workloads (seeded; see nvfp4_weight_mixture_gb300/synth.py).  The default run
 times all five in turn under the same protocol and prints one JSON line: the
@@ -66,6 +69,12 @@ def parse_args():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-dense", action="store_true",
                    help="skip the dense QPN2 / QPN8 projection records")
+    p.add_argument("--only-dense", action="store_true",
+                   help="time the dense QPN2 / QPN8 projection records only (one JSON line of "
+                        "them)")
+    p.add_argument("--stack", type=int, default=16,
+                   help="calls per CUDA graph, each on its own allocation of the weights (16: the "
+                        "pages' protocol; fewer holds less device memory, e.g. under a profiler)")
     p.add_argument("--crossover", default=None,
                    help="comma-separated token counts: time the forward's decode and grouped "
                         "paths at each M (one JSON line each) instead of the bench")
@@ -355,8 +364,9 @@ def workload_config(wl):
             "shared_expert": wl.shared,
             "weights": "NVFP4 (E2M1, E4M3 per 16 along K, FP32 per tensor) from N(0,0.02)",
             "activations": "FP16 N(0,1), 16 rotating token batches",
-            "l2": "16 complete layer calls per CUDA graph, call i on the i-th of 16 distinct "
-                  "allocations of the same weights; 2x L2 buffer written before every replay",
+            "l2": f"{STACK} complete layer calls per CUDA graph, call i on the i-th of {STACK} "
+                  "distinct allocations of the same weights; 2x L2 buffer written before every "
+                  "replay",
             "parallelism": "token-parallel replicas, no collective"}
 
 
@@ -437,7 +447,7 @@ def time_workload(wl, args, dist, dev, local, ws, rank):
     warmup = max(3, args.warmup if args.warmup is not None else 10)
 
     layer = build_layer(wl, dev, moe, synth)
-    n_var = STACK
+    n_var = max(16, STACK)  # token batches (the routes change from call to call)
     xs = [torch.from_numpy(synth.activations(wl, v)).to(dev) for v in range(n_var)]
     ys = [torch.empty((wl.M, wl.H), dtype=torch.float16, device=dev) for _ in range(n_var)]
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
@@ -751,6 +761,20 @@ def time_dense(wl, fmt, args, dev):
                          "algorithmic": {"bytes": byts}}}
 
 
+def run_dense_only(args):
+    """The dense projection records alone, one JSON line {"dense": {...}}."""
+    import torch
+    from nvfp4_weight_mixture_gb300 import moe, synth
+    dev = torch.device("cuda", 0)
+    moe.load_library()
+    out = {}
+    for dn in ("dense_gate_up_m16", "dense_down_m16"):
+        for fmt in ("nvfp4", "fp8"):
+            out[f"{dn}_{fmt}"] = time_dense(synth.DENSE_WORKLOADS[dn], fmt, args, dev)
+    print(json.dumps({"dense": out}), flush=True)
+    return 0
+
+
 def run_gpu(args, workloads):
     """Times every workload (the first is the headline line; the others go
     into its "configs" map, each measured under the same protocol)."""
@@ -799,7 +823,11 @@ def run_gpu(args, workloads):
 
 
 def main():
+    global STACK
     args = parse_args()
+    if args.stack < 1:
+        raise SystemExit("--stack must be at least 1")
+    STACK = args.stack
     from nvfp4_weight_mixture_gb300 import synth
     names = [args.workload] if args.workload else args.workloads.split(",")
     for n in names:
@@ -812,6 +840,8 @@ def main():
         return run_reference(args, wls[0])
     if args.crossover:
         return run_crossover(args)
+    if args.only_dense:
+        return run_dense_only(args)
     return run_gpu(args, wls)
 
 
