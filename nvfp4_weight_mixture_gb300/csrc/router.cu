@@ -1041,15 +1041,17 @@ __global__ void __launch_bounds__(kRcThreads, 1)
   // (programmatic dependent launch), whose outputs (the token rows) and
   // buffers (the plan) are only touched after the wait.
   pdl_wait();
-  // token rows and the zero row (rows >= M of the MMA read it)
+  // token rows (asynchronous copies, all in flight at once) and the zero row
+  // (rows >= M of the MMA read it)
   {
     const int rv = H / 8;  // 16-byte vectors per row
     for (int i = tid; i < M * rv; i += kRcThreads) {
       const int m = i / rv, c = i - m * rv;
-      reinterpret_cast<uint4*>(xs + (size_t)m * (H + 8))[c] =
-          __ldg(reinterpret_cast<const uint4*>(x + (size_t)m * H) + c);
+      cp_async16(smem_u32(xs + (size_t)m * (H + 8) + 8 * c), x + (size_t)m * H + 8 * c, 16u);
     }
+    cp_async_commit();
     if (tid == 0) *reinterpret_cast<uint4*>(const_cast<char*>(zero_row)) = make_uint4(0, 0, 0, 0);
+    cp_async_wait<0>();
   }
   __syncthreads();
 
