@@ -144,6 +144,17 @@ def _stream():
     return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
 
 
+_raw_stream_fn = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
+def _raw_stream(dev_index):
+    """The current stream of a device as an integer handle (the cheap query
+    where this torch build has it)."""
+    if _raw_stream_fn is not None:
+        return _raw_stream_fn(dev_index)
+    return torch.cuda.current_stream(dev_index).cuda_stream
+
+
 def _need(t, dtype, name):
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name}: expected a torch.Tensor")
@@ -457,7 +468,11 @@ class MoELayer:
         self.shared13, self.shared2, self.w_gate, self.bias = shared13, shared2, w_gate, bias
         self.max_tokens = 0
         self.device = torch.device(device)
+        self._dev_index = self.device.index if self.device.index is not None else \
+            torch.cuda.current_device()
         self.status = torch.zeros(1, dtype=torch.int32, device=self.device)
+        self._fast = None    # the call's fixed C arguments, once the full checks have passed
+        self._routes = {}    # M -> (ids, topk_w) reused by calls that pass none
         self.reserve(max_tokens)
 
     def reserve(self, max_tokens):
@@ -491,12 +506,59 @@ class MoELayer:
                 self.ws, self.status)
         return y
 
+    def _fast_key(self):
+        return (self.w13, self.w2, self.shared13, self.shared2, self.w_router, self.bias,
+                self.w_gate, self.plan_buf, self.ws, self.status)
+
+    def _build_fast(self):
+        """The fixed C arguments of moe_nvfp4_layer (config, weights, buffers),
+        built after a call whose arguments passed every check."""
+        wc = (_weights_c(self.w13, LAYOUT_FRAGMENT_W13), _weights_c(self.w2, LAYOUT_FRAGMENT),
+              _weights_c(self.shared13, LAYOUT_FRAGMENT_W13),
+              _weights_c(self.shared2, LAYOUT_FRAGMENT))
+        refs = tuple(None if w is None else ctypes.byref(w) for w in wc)
+        ptr = lambda t: None if t is None else t.data_ptr()
+        fixed = (ctypes.byref(self.cfg), ptr(self.w_router), ptr(self.bias), ptr(self.w_gate),
+                 self.plan_buf.data_ptr(), self.plan_buf.numel(), refs, self.ws.data_ptr(),
+                 self.ws.numel(), self.status.data_ptr())
+        self._fast = (self._fast_key(), fixed, wc)
+
+    def _fast_ready(self, t, M):
+        return (isinstance(t, torch.Tensor) and t.dtype is torch.float16 and t.dim() == 2
+                and t.shape[0] == M and t.shape[1] == self.H and t.is_contiguous()
+                and t.get_device() == self._dev_index)
+
     def __call__(self, x, y=None, ids=None, topk_w=None):
         """The whole layer through moe_nvfp4_layer (router, plan, forward).
-        Returns y; the routes land in ids / topk_w (allocated when not given)
-        and the plan in the plan buffer."""
+        Returns y; the routes land in ids / topk_w (when not given, in buffers
+        of the layer reused by the next call with as many tokens) and the plan
+        in the plan buffer.
+
+        After a first call with full argument checks, calls that pass no
+        routes and the same weights and buffers go straight to the library
+        with the checks that can change between calls (x and y: FP16, [M, H],
+        contiguous, on the layer's device); the library validates the rest."""
         M = x.shape[0]
         self.reserve(M)
+        f = self._fast
+        if (ids is None and topk_w is None and f is not None and self._fast_ready(x, M)
+                and (y is None or self._fast_ready(y, M))):
+            key = self._fast_key()
+            if all(a is b for a, b in zip(f[0], key)):
+                if y is None:
+                    y = torch.empty((M, self.H), dtype=torch.float16, device=self.device)
+                r = self._routes.get(M)
+                if r is None:
+                    r = (torch.empty((M, self.k), dtype=torch.int32, device=self.device),
+                         torch.empty((M, self.k), dtype=torch.float32, device=self.device))
+                    self._routes[M] = r
+                cfg_ref, wr, bias, wg, plan_p, plan_n, refs, ws_p, ws_n, st_p = f[1]
+                _check("moe_nvfp4_layer", load_library().moe_nvfp4_layer(
+                    cfg_ref, M, x.data_ptr(), wr, bias, wg, r[0].data_ptr(), r[1].data_ptr(),
+                    plan_p, plan_n, refs[0], refs[1], refs[2], refs[3], y.data_ptr(), ws_p, ws_n,
+                    st_p, _raw_stream(self._dev_index)))
+                self.last_ids, self.last_topk_w = r
+                return y
         y = y if y is not None else torch.empty((M, self.H), dtype=torch.float16, device=self.device)
         ids = ids if ids is not None else torch.empty((M, self.k), dtype=torch.int32,
                                                       device=self.device)
@@ -505,6 +567,8 @@ class MoELayer:
         layer(self.cfg, x, self.w_router, self.bias, self.w_gate, ids, topk_w, self.plan_buf,
               self.w13, self.w2, self.shared13, self.shared2, y, self.ws, self.status)
         self.last_ids, self.last_topk_w = ids, topk_w
+        if self._fast is None or not all(a is b for a, b in zip(self._fast[0], self._fast_key())):
+            self._build_fast()
         return y
 
 
