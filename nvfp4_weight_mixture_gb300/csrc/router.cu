@@ -8,11 +8,11 @@
 //
 // Shapes:
 //  * M <= 16 (decode): one thread-block cluster (router_cluster_kernel).  CTA
-//    r owns an expert slice and computes its complete logits; the slices'
-//    top-k candidates are merged in CTA 0, which also computes the weights,
-//    the gate and the whole plan, decode work table included.  Where such a
-//    cluster cannot be scheduled, a 128-block router with arrival tickets
-//    (router_small_kernel) does the same.
+//    r owns an expert slice and computes its complete logits, which it writes
+//    into CTA 0's shared memory; CTA 0 takes each token's top-k over all the
+//    experts and computes the weights, the gate and the whole plan, decode
+//    work table included.  Where such a cluster cannot be scheduled, a
+//    128-block router with arrival tickets (router_small_kernel) does the same.
 //  * M > 16 (prefill): the logits as a tcgen05 GEMM (router_logits_kernel, W_r
 //    transposed once per call) and one warp per token for top-k, weights and
 //    gate (router_topk_kernel); an mma.sync router with the top-k in its
@@ -929,10 +929,10 @@ static cudaError_t launch_router_tc(const LayerDims& d, int64_t M, const __half*
 // eighth of K, loads its W_r tiles ([K rows][Es experts], swizzled) with 2-D
 // tensor-map copies and multiplies them with the staged token rows on
 // mma.sync (FP32 accumulate); the 8 partial sums are added in warp order.
-// The CTA's own top-k candidates per token then go to CTA 0 through
-// distributed shared memory, and CTA 0 merges them (the global top-k is the
-// top-k of the slices' top-k), computes the weights and the gate and builds
-// the whole plan.
+// The slice's logits then go to CTA 0 through distributed shared memory (one
+// cluster barrier), and CTA 0 takes every token's top-k over all experts (one
+// warp per token), computes the weights and the gate and builds the whole
+// plan.
 // ---------------------------------------------------------------------------
 constexpr int kRcThreads = 256;
 constexpr int kRcWarps = kRcThreads / 32;
@@ -957,6 +957,9 @@ __device__ __forceinline__ uint32_t dsmem_addr(const void* p, uint32_t rank) {
 __device__ __forceinline__ void st_dsmem_u32x2(uint32_t a, uint32_t v0, uint32_t v1) {
   asm volatile("st.shared::cluster.v2.u32 [%0], {%1, %2};" ::"r"(a), "r"(v0), "r"(v1) : "memory");
 }
+__device__ __forceinline__ void st_dsmem_f32(uint32_t a, float v) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(a), "f"(v) : "memory");
+}
 
 // Shape of one cluster launch: experts per CTA, W_r tile rows, ring depth and
 // the shared-memory carve (all offsets 1024-byte aligned).
@@ -978,11 +981,12 @@ __host__ __device__ inline RouterClusterPlan router_cluster_plan(int H, int E, i
   while (per_warp % n != 0 || (per_warp / n) % 16 != 0) ++n;
   p.tr = per_warp / n;
   p.ntw = n;
-  // token rows (M x (H + 8) halves) and a 16-byte zero row, then the slices'
-  // top-k candidates (M x C x k), which the CTAs write into CTA 0 while it may
-  // still read its token rows
+  // token rows (M x (H + 8) halves) and a 16-byte zero row, then every
+  // expert's logit of every token (M x E), which the CTAs write into CTA 0
+  // while it may still read its token rows
+  (void)k;
   p.xs = align_up((size_t)M * (H + 8) * 2 + 16, 1024);
-  p.cand = align_up((size_t)M * p.C * k * 8, 1024);
+  p.cand = align_up((size_t)M * E * 4, 1024);
   p.lg = align_up((size_t)kDecodeMaxTokens * p.Es * 4, 1024);
   // a stage also holds the warp's partial sums ([16][Es] FP32) at the end
   const size_t tile = (size_t)p.tr * p.Es * 2, red = (size_t)kDecodeMaxTokens * p.Es * 4;
@@ -1011,11 +1015,11 @@ __global__ void __launch_bounds__(kRcThreads, 1)
   const int E = d.E, H = d.H, k = d.k;
   const uint32_t rank = cluster_ctarank();
   const RouterClusterPlan L = router_cluster_plan(H, E, k, M, cmax);
-  const int C = L.C, Es = L.Es, tr = L.tr, ntw = L.ntw, stages = L.stages;
+  const int Es = L.Es, tr = L.tr, ntw = L.ntw, stages = L.stages;
   const int rb = Es * 2;  // bytes of one W_r tile row
   __half* xs = reinterpret_cast<__half*>(rsm);
   const char* zero_row = rsm + (size_t)M * (H + 8) * 2;
-  char* cand_region = rsm + L.xs;                           // [M][C][k] (key, id), CTA 0
+  float* all_lg = reinterpret_cast<float*>(rsm + L.xs);      // [M][E] logits, CTA 0
   float* lg = reinterpret_cast<float*>(rsm + L.xs + L.cand);  // [16][Es] logits of the slice
   char* ring = rsm + L.xs + L.cand + L.lg;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -1136,70 +1140,23 @@ __global__ void __launch_bounds__(kRcThreads, 1)
     lg[m * Es + e] = sum;
   }
   __syncthreads();
-  // ---- the slice's top-k per token (lane j < k holds the j-th), as keys ----
-  uint32_t ckey[2] = {0u, 0u};
-  int cid[2] = {-1, -1};
-#pragma unroll
-  for (int mm = 0; mm < 2; ++mm) {
-    const int m = warp + kRcWarps * mm;
-    if (m >= M) continue;
-    uint32_t v[2];
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      const int e = lane + 32 * i, ge = (int)rank * Es + e;
-      v[i] = (e < Es && ge < E) ? f2key(lg[m * Es + e]) : 0u;
-    }
-    for (int j = 0; j < k; ++j) {
-      const uint32_t gm = __reduce_max_sync(0xffffffffu, max(v[0], v[1]));
-      uint32_t li = 0xffffffffu;
-      if (v[1] == gm) li = (uint32_t)(lane + 32);
-      if (v[0] == gm) li = (uint32_t)lane;
-      const uint32_t gi = __reduce_min_sync(0xffffffffu, li);
-      if ((uint32_t)lane == gi) v[0] = 0u;
-      if ((uint32_t)(lane + 32) == gi) v[1] = 0u;
-      if (lane == j) {
-        ckey[mm] = gm;
-        cid[mm] = (int)rank * Es + (int)gi;
-      }
-    }
+  // ---- the slice's logits into CTA 0: all_lg[m][rank Es + e] ----
+  for (int i = tid; i < M * Es; i += kRcThreads) {
+    const int m = i / Es, e = i - m * Es, ge = (int)rank * Es + e;
+    if (ge < E) st_dsmem_f32(dsmem_addr(all_lg + (size_t)m * E + ge, 0), lg[m * Es + e]);
   }
   if (tid == 0) MOE_TL_MIN(21);
-  // ---- candidates into CTA 0: cand[(m C + rank) k + j] = (key, id) ----
-#pragma unroll
-  for (int mm = 0; mm < 2; ++mm) {
-    const int m = warp + kRcWarps * mm;
-    if (m < M && lane < k)
-      st_dsmem_u32x2(dsmem_addr(cand_region + (((size_t)m * C + rank) * k + lane) * 8, 0),
-                     ckey[mm], (uint32_t)cid[mm]);
-  }
-  cluster_sync_all();  // every candidate is in CTA 0
+  cluster_sync_all();  // every logit is in CTA 0
   if (tid == 0) MOE_TL_MIN(23);
   if (rank != 0) return;
   if (tid == 0) MOE_TL_MAX(24);
 
-  // ---- merge, weights, gate, plan (CTA 0) ----
-  // Each slice's candidates are in descending order (ties: lower id first),
-  // so the merge keeps one head per slice (lane c < C) and, k times, takes
-  // the largest head (ties: the lower id) and advances that slice.
-  const uint2* cand = reinterpret_cast<const uint2*>(cand_region);
+  // ---- top-k, weights, gate, plan (CTA 0): one warp per token over all E
+  // logits (largest first; ties: the lower expert id) ----
   for (int m = warp; m < M; m += kRcWarps) {
-    const uint2* lst = cand + ((size_t)m * C + lane) * k;
-    int ptr = 0;
-    uint2 head = lane < C ? lst[0] : make_uint2(0u, 0x7fffffffu);
     int my_id = -1;
     float my_l = -INFINITY;
-    for (int j = 0; j < k; ++j) {
-      const uint32_t gm = __reduce_max_sync(0xffffffffu, head.x);
-      const uint32_t gi = __reduce_min_sync(0xffffffffu, head.x == gm ? head.y : 0x7fffffffu);
-      if (lane < C && head.x == gm && head.y == gi) {
-        ++ptr;
-        head = ptr < k ? lst[ptr] : make_uint2(0u, 0x7fffffffu);
-      }
-      if (lane == j) {
-        my_id = (int)gi;
-        my_l = key2f(gm);
-      }
-    }
+    warp_topk<false>(all_lg + (size_t)m * E, E, k, &my_id, &my_l);
     if (tid == 0) MOE_TL_MAX(26);
     const float w = warp_topk_weight(my_l, k);
     const float gamma = d.shared ? warp_gate(x + (size_t)m * H, wg, H) : 0.f;
