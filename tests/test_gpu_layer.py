@@ -440,3 +440,45 @@ def test_query_plan_bytes_cover_every_smaller_m():
             for n, v in top.items():
                 if M <= n:
                     assert pb <= v, (E, M, n, pb, v)
+
+
+def test_layer_repeated_calls_match_the_checked_call():
+    """MoELayer's repeated calls (the call's fixed C arguments built once,
+    after a fully checked call) give the bits of moe.layer with every check,
+    for other token counts too, and rebuild their arguments when the layer's
+    buffers or weights are replaced."""
+    case = Case(synth.with_tokens(TINY, 24))
+    L = case.layer
+    x = case.x_t
+
+    def checked(xx):
+        M = xx.shape[0]
+        y = torch.empty_like(xx)
+        ids = torch.empty((M, L.k), dtype=torch.int32, device="cuda")
+        tw = torch.empty((M, L.k), dtype=torch.float32, device="cuda")
+        moe.layer(L.cfg, xx, L.w_router, L.bias, L.w_gate, ids, tw, L.plan_buf, L.w13, L.w2,
+                  L.shared13, L.shared2, y, L.ws, L.status)
+        torch.cuda.synchronize()
+        return y.cpu().numpy(), ids.cpu().numpy()
+
+    def same(a, b):
+        np.testing.assert_array_equal(a.view(np.uint16), b.view(np.uint16))
+
+    ref, ref_ids = checked(x)
+    for _ in range(3):  # the first call is checked in full, the others take the short path
+        y = L(x)
+        torch.cuda.synchronize()
+        same(y.cpu().numpy(), ref)
+        np.testing.assert_array_equal(L.last_ids.cpu().numpy(), ref_ids)
+    assert L._fast is not None
+    x8 = x[:8].contiguous()
+    ref8, _ = checked(x8)
+    same(L(x8).cpu().numpy(), ref8)
+    # larger buffers, then another copy of the weights: the arguments follow
+    L.reserve(256)
+    same(L(x).cpu().numpy(), ref)
+    L.w13 = tuple(t.clone() for t in L.w13)
+    L.w2 = tuple(t.clone() for t in L.w2)
+    same(L(x).cpu().numpy(), ref)
+    assert L._fast[0][0] is L.w13
+    assert int(L.status.item()) == 0
