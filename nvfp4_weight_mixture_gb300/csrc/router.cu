@@ -27,6 +27,79 @@
 namespace moe {
 
 // ---------------------------------------------------------------------------
+// Plan of at most 32 pairs (M <= 16), with no block barrier.  Warp 0 holds
+// pair q in lane q: its validity, its rank among the pairs of its expert (a
+// match over the lanes), its plan position (valid pairs of a lower expert, by
+// comparison with the other lanes, plus that rank), perm and inv; the first
+// pair of each expert writes the expert's active entry, its tile (at most 32
+// rows: one), its decode work-table entry, and every pair its own id into
+// that entry.  The other warps write counts and offsets of every expert
+// straight from the pair list.  Same plan as the general path below.
+// ---------------------------------------------------------------------------
+__device__ void plan_tiny(const LayerDims& d, int M, const int* src, const PlanView& pv,
+                          uint32_t* status) {
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int P = M * d.k_eff, ne = d.e_eff;
+  if (tid < 32) {
+    const int e_in = lane < P ? src[lane] : -1;
+    const bool ok = lane < P && pair_valid(e_in, lane % d.k_eff, d);
+    if (__ballot_sync(0xffffffffu, lane < P && !ok) && lane == 0)
+      set_status(status, MOE_ST_INVALID_ID);
+    const uint32_t vmask = __ballot_sync(0xffffffffu, ok);
+    const int e = ok ? e_in : -1 - lane;  // lanes without a valid pair match only themselves
+    const uint32_t same = __match_any_sync(0xffffffffu, e);
+    const int before = __popc(same & ((1u << lane) - 1u)), total = __popc(same);
+    const uint32_t fmask = __ballot_sync(0xffffffffu, ok && before == 0);
+    int less = 0, a = 0;  // valid pairs / experts' first pairs of a lower expert
+    for (int q = 0; q < P; ++q) {
+      const int eq = __shfl_sync(0xffffffffu, e, q);
+      less += (int)((vmask >> q) & 1u) & (int)(eq < e);
+      a += (int)((fmask >> q) & 1u) & (int)(eq < e);
+    }
+    const int pos = less + before, na = __popc(fmask);
+    if (lane < P) pv.inv[lane] = ok ? pos : -1;
+    if (ok) {
+      pv.perm[pos] = lane;
+      int* ent = pv.dtab + (size_t)a * kDtabInts;
+      if (before < kDtabInts - 4) ent[4 + before] = lane;
+      if (before == 0) {
+        pv.active[a] = e;
+        reinterpret_cast<int4*>(pv.tiles)[a] = make_int4(e, 0, total, 0);
+        reinterpret_cast<int4*>(ent)[0] = make_int4(e, pos, total, -1);
+        for (int r = total; r < kDtabInts - 4; ++r) ent[4 + r] = -1;
+      }
+    }
+    // entries na .. min(P, ne) - 1 of the work table: unused, all -1
+    const int n_pad = (min(P, ne) - na) * 5;
+    for (int i = lane; i < n_pad; i += 32)
+      reinterpret_cast<int4*>(pv.dtab)[na * 5 + i] = make_int4(-1, -1, -1, -1);
+    if (lane == 0) {
+      pv.hdr->M = M;
+      pv.hdr->k_eff = d.k_eff;
+      pv.hdr->e_eff = ne;
+      pv.hdr->n_valid = __popc(vmask);
+      pv.hdr->n_active = na;
+      pv.hdr->n_tiles = na;
+    }
+  } else {
+    // offsets[e] = valid pairs of an expert below e (offsets[ne] = all valid
+    // pairs), counts[e] = valid pairs of expert e
+    for (int e = tid - 32; e <= ne; e += (int)blockDim.x - 32) {
+      int c = 0, l = 0, slot = 0;
+      for (int q = 0; q < P; ++q) {
+        const int eq = src[q];
+        const bool okq = pair_valid(eq, slot, d);
+        c += (int)(okq && eq == e);
+        l += (int)(okq && eq < e);
+        if (++slot == d.k_eff) slot = 0;
+      }
+      pv.offsets[e] = l;
+      if (e < ne) pv.counts[e] = c;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
 // Plan of up to kDecodeMaxTokens * (32 + 1) pairs by one block of 256 threads.
 // `src` (shared memory) holds the M * k_eff expert ids of the pairs.  Also
 // writes the decode work table.  Three steps separated by barriers:
@@ -51,6 +124,10 @@ __device__ void plan_small_block(const LayerDims& d, int M, const int* src, cons
   __shared__ int s_nv, s_na, s_nt;
   const int tid = threadIdx.x, nthr = blockDim.x, lane = tid & 31;
   const int P = M * d.k_eff, ne = d.e_eff;
+  if (P <= 32) {
+    plan_tiny(d, M, src, pv, status);
+    return;
+  }
   if (tid == 0) {
     s_nv = 0;
     s_na = 0;
@@ -929,10 +1006,11 @@ static cudaError_t launch_router_tc(const LayerDims& d, int64_t M, const __half*
 // eighth of K, loads its W_r tiles ([K rows][Es experts], swizzled) with 2-D
 // tensor-map copies and multiplies them with the staged token rows on
 // mma.sync (FP32 accumulate); the 8 partial sums are added in warp order.
-// The slice's logits then go to CTA 0 through distributed shared memory (one
-// cluster barrier), and CTA 0 takes every token's top-k over all experts (one
-// warp per token), computes the weights and the gate and builds the whole
-// plan.
+// The slice's logits then go straight into CTA 0's shared memory as
+// asynchronous remote stores that complete on one of its mbarriers (the
+// other CTAs exit after issuing them), and CTA 0 takes every token's top-k
+// over all experts (one warp per token), computes the weights and the gate
+// and builds the whole plan.
 // ---------------------------------------------------------------------------
 constexpr int kRcThreads = 256;
 constexpr int kRcWarps = kRcThreads / 32;
@@ -944,28 +1022,54 @@ __device__ __forceinline__ uint32_t cluster_ctarank() {
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
   return r;
 }
-__device__ __forceinline__ void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::
-                   : "memory");
-}
 // Address of the same shared-memory location in CTA `rank` of the cluster.
 __device__ __forceinline__ uint32_t dsmem_addr(const void* p, uint32_t rank) {
   uint32_t r;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
   return r;
 }
-__device__ __forceinline__ void st_dsmem_u32x2(uint32_t a, uint32_t v0, uint32_t v1) {
-  asm volatile("st.shared::cluster.v2.u32 [%0], {%1, %2};" ::"r"(a), "r"(v0), "r"(v1) : "memory");
+__device__ __forceinline__ void cluster_arrive() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
 }
-__device__ __forceinline__ void st_dsmem_f32(uint32_t a, float v) {
-  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(a), "f"(v) : "memory");
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Four FP32 values into the shared memory of another CTA of the cluster (16
+// bytes at cluster address `a`), completing as 16 transaction bytes on the
+// mbarrier at cluster address `bar` in that CTA.
+__device__ __forceinline__ void st_async_f32x4(uint32_t a, float4 v, uint32_t bar) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, "
+      "[%5];" ::"r"(a),
+      "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(bar)
+      : "memory");
+}
+// mbarrier wait with acquire at cluster scope (the data came from other CTAs
+// of the cluster); bounded like mbar_wait.
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity,
+                                                  uint32_t* status) {
+  const long long t0 = clock64();
+  while (true) {
+    uint32_t done;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], "
+        "%2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(done)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    if (done) return true;
+    if (clock64() - t0 > kWaitTimeoutCycles) {
+      set_status(status, MOE_ST_TIMEOUT);
+      return false;
+    }
+  }
 }
 
 // Shape of one cluster launch: experts per CTA, W_r tile rows, ring depth and
 // the shared-memory carve (all offsets 1024-byte aligned).
 struct RouterClusterPlan {
   int C, Es, tr, ntw, stages;
-  size_t xs, cand, ring, stage, lg, total;
+  size_t xs, cand, ring, stage, total;
 };
 
 __host__ __device__ inline RouterClusterPlan router_cluster_plan(int H, int E, int k, int M,
@@ -987,11 +1091,10 @@ __host__ __device__ inline RouterClusterPlan router_cluster_plan(int H, int E, i
   (void)k;
   p.xs = align_up((size_t)M * (H + 8) * 2 + 16, 1024);
   p.cand = align_up((size_t)M * E * 4, 1024);
-  p.lg = align_up((size_t)kDecodeMaxTokens * p.Es * 4, 1024);
   // a stage also holds the warp's partial sums ([16][Es] FP32) at the end
   const size_t tile = (size_t)p.tr * p.Es * 2, red = (size_t)kDecodeMaxTokens * p.Es * 4;
   p.stage = align_up(tile > red ? tile : red, 1024);
-  const size_t fixed = 1024 + p.xs + p.cand + p.lg;
+  const size_t fixed = 1024 + p.xs + p.cand;
   int st = (int)((kRcSmemBudget > fixed ? kRcSmemBudget - fixed : 0) / (kRcWarps * p.stage));
   if (st > 2) st = 2;
   if (st > p.ntw) st = p.ntw;
@@ -1010,6 +1113,8 @@ __global__ void __launch_bounds__(kRcThreads, 1)
   char* rsm = reinterpret_cast<char*>((reinterpret_cast<uintptr_t>(rsm_raw) + 1023) &
                                       ~uintptr_t(1023));
   __shared__ uint64_t full[kRcWarps][2];
+  __shared__ uint64_t xch;  // CTA 0: the logits of every slice have landed
+  __shared__ __align__(16) float s_bias[64];
   __shared__ int s_ids[kDecodeMaxTokens * 33];
   MOE_TL(kTlRouter);
   const int E = d.E, H = d.H, k = d.k;
@@ -1020,8 +1125,7 @@ __global__ void __launch_bounds__(kRcThreads, 1)
   __half* xs = reinterpret_cast<__half*>(rsm);
   const char* zero_row = rsm + (size_t)M * (H + 8) * 2;
   float* all_lg = reinterpret_cast<float*>(rsm + L.xs);      // [M][E] logits, CTA 0
-  float* lg = reinterpret_cast<float*>(rsm + L.xs + L.cand);  // [16][Es] logits of the slice
-  char* ring = rsm + L.xs + L.cand + L.lg;
+  char* ring = rsm + L.xs + L.cand;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, t4 = lane & 3;
   char* my_ring = ring + (size_t)warp * stages * L.stage;
@@ -1032,18 +1136,31 @@ __global__ void __launch_bounds__(kRcThreads, 1)
       mbar_init(&full[w][0], 1);
       mbar_init(&full[w][1], 1);
     }
+    if (rank == 0) {
+      // every expert's logit of every token arrives as transaction bytes
+      mbar_init(&xch, 1);
+      mbar_expect_tx(&xch, (uint32_t)(M * E * 4));
+    }
     fence_mbar_init();
   }
   __syncthreads();
+  // CTA 0's barrier is initialised before any CTA writes to it: the cluster
+  // barrier is arrived at here and waited on just before the first write
+  cluster_arrive();
   if (lane == 0)
     for (int i = 0; i < stages; ++i) {
       mbar_expect_tx(&full[warp][i], (uint32_t)(tr * rb));
       tma_load_2d(my_ring + i * L.stage, &wrmap, (int)rank * Es, kw0 + i * tr, &full[warp][i]);
     }
-  // The router weight is an input of the layer, not of the previous kernel:
-  // its first copies are in flight before waiting for the preceding grid
-  // (programmatic dependent launch), whose outputs (the token rows) and
-  // buffers (the plan) are only touched after the wait.
+  // The router weight and bias are inputs of the layer, not of the previous
+  // kernel: the first weight copies and the bias slice are in flight before
+  // waiting for the preceding grid (programmatic dependent launch), whose
+  // outputs (the token rows) and buffers (the plan) are only touched after
+  // the wait.
+  if (tid < Es) {
+    const int ge = (int)rank * Es + tid;
+    s_bias[tid] = (bias && ge < E) ? bias[ge] : 0.f;
+  }
   pdl_wait();
   // token rows (asynchronous copies, all in flight at once) and the zero row
   // (rows >= M of the MMA read it)
@@ -1128,28 +1245,44 @@ __global__ void __launch_bounds__(kRcThreads, 1)
         }
   if (tid == 0) MOE_TL_MAX(20);
   __syncthreads();
-  // ---- logits of the slice: the 8 warps' partials in warp order (+ bias) ----
-  for (int i = tid; i < M * Es; i += kRcThreads) {
-    const int m = i / Es, e = i - m * Es;
-    float sum = 0.f;
+  cluster_wait();  // CTA 0's barrier is initialised
+  // ---- logits of the slice, four experts per thread: the 8 warps' partials
+  // in warp order (+ bias), stored straight into CTA 0 (all_lg[m][rank Es +
+  // e]); E % 8 == 0 and Es % 16 == 0, so four experts are all valid or all
+  // past E ----
+  {
+    const uint32_t xbar = dsmem_addr(&xch, 0);
+    const int q4 = Es / 4;
+    for (int i = tid; i < M * q4; i += kRcThreads) {
+      const int m = i / q4, e = 4 * (i - m * q4), ge = (int)rank * Es + e;
+      if (ge >= E) continue;
+      float4 sum = *reinterpret_cast<const float4*>(s_bias + e);
+      float4 p[kRcWarps];
 #pragma unroll
-    for (int w = 0; w < kRcWarps; ++w)
-      sum += reinterpret_cast<const float*>(ring + (size_t)w * stages * L.stage)[m * Es + e];
-    const int ge = (int)rank * Es + e;
-    if (bias && ge < E) sum += bias[ge];
-    lg[m * Es + e] = sum;
-  }
-  __syncthreads();
-  // ---- the slice's logits into CTA 0: all_lg[m][rank Es + e] ----
-  for (int i = tid; i < M * Es; i += kRcThreads) {
-    const int m = i / Es, e = i - m * Es, ge = (int)rank * Es + e;
-    if (ge < E) st_dsmem_f32(dsmem_addr(all_lg + (size_t)m * E + ge, 0), lg[m * Es + e]);
+      for (int w = 0; w < kRcWarps; ++w)
+        p[w] = *reinterpret_cast<const float4*>(
+            reinterpret_cast<const float*>(ring + (size_t)w * stages * L.stage) + m * Es + e);
+      float4 a = p[0];
+#pragma unroll
+      for (int w = 1; w < kRcWarps; ++w) {
+        a.x += p[w].x;
+        a.y += p[w].y;
+        a.z += p[w].z;
+        a.w += p[w].w;
+      }
+      sum.x += a.x;
+      sum.y += a.y;
+      sum.z += a.z;
+      sum.w += a.w;
+      st_async_f32x4(dsmem_addr(all_lg + (size_t)m * E + ge, 0), sum, xbar);
+    }
   }
   if (tid == 0) MOE_TL_MIN(21);
-  cluster_sync_all();  // every logit is in CTA 0
-  if (tid == 0) MOE_TL_MIN(23);
-  if (rank != 0) return;
+  if (rank != 0) return;  // nothing reads the other CTAs' shared memory
+  // every expert's logit of every token is in CTA 0
+  const bool have = mbar_wait_cluster(&xch, 0, status);
   if (tid == 0) MOE_TL_MAX(24);
+  if (!have) return;
 
   // ---- top-k, weights, gate, plan (CTA 0): one warp per token over all E
   // logits (largest first; ties: the lower expert id) ----

@@ -11,8 +11,8 @@ import pytest
 import torch
 
 import oracle
-from harness import (MAX_ABS_TOL, REL_L2_TOL, ROUTER_GAP, ROUTER_W_TOL, TILE_ROWS, Case,
-                     compare)
+from harness import (DECODE_MAX_TOKENS, MAX_ABS_TOL, REL_L2_TOL, ROUTER_GAP, ROUTER_W_TOL,
+                     TILE_ROWS, Case, compare, expected_work_table)
 from nvfp4_weight_mixture_gb300 import moe, synth
 
 pytestmark = pytest.mark.gpu
@@ -65,6 +65,10 @@ def _check_plan(case, ids):
     np.testing.assert_array_equal(got["tiles"], ref["tiles"])
     np.testing.assert_array_equal(got["active"], np.nonzero(ref["counts"])[0])
     assert int(got["hdr"][0]) == wl.M and int(got["hdr"][1]) == k_eff
+    if wl.M <= DECODE_MAX_TOKENS:
+        # the decode work table the oracle plan implies
+        exp_tab = expected_work_table(ref, wl.M, k_eff, e_eff)
+        np.testing.assert_array_equal(got["dtab"][:len(exp_tab)], exp_tab)
     return ref
 
 
@@ -182,7 +186,7 @@ def test_plan_edge_cases(M):
     assert int(case.layer.status.item()) & moe.ST_INVALID_ID
 
 
-@pytest.mark.parametrize("M", [12, 600])
+@pytest.mark.parametrize("M", [8, 12, 600])
 def test_plan_with_shared_expert(M):
     wl = synth.custom("sh", M, 256, 16, 2, 128, bias="zipf", shared=True)
     case = Case(wl)
