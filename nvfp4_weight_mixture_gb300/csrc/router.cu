@@ -99,10 +99,54 @@ __device__ void plan_tiny(const LayerDims& d, int M, const int* src, const PlanV
   }
 }
 
+// The plan header and the decode work table from the sorted active list
+// (expert, first position, rows) and the pair at each plan position, all in
+// shared memory.  Work table: every entry up to the largest active-expert
+// count, as five 16-byte groups (expert, first position, rows, -1 | first 16
+// pair ids, -1 past the expert's rows); entries past the active experts -1.
+__device__ void plan_header_and_table(const LayerDims& d, int M, int nv, int na, int nt,
+                                      const int* s_ae, const int* s_aoff, const int* s_acnt,
+                                      const int* s_perm, const PlanView& pv) {
+  const int tid = threadIdx.x, nthr = blockDim.x;
+  const int P = M * d.k_eff, ne = d.e_eff;
+  if (tid == 0) {
+    pv.hdr->M = M;
+    pv.hdr->k_eff = d.k_eff;
+    pv.hdr->e_eff = ne;
+    pv.hdr->n_valid = nv;
+    pv.hdr->n_active = na;
+    pv.hdr->n_tiles = nt;
+  }
+  static_assert(kDtabInts == 20, "a work-table entry is five 16-byte groups");
+  const int max_active = min(P, ne);
+  for (int i = tid; i < max_active * 5; i += nthr) {
+    const int a = i / 5, f4 = i - a * 5;
+    int4 v = make_int4(-1, -1, -1, -1);
+    if (a < na) {
+      const int off = s_aoff[a], cnt = s_acnt[a];
+      if (f4 == 0) {
+        v = make_int4(s_ae[a], off, cnt, -1);
+      } else {
+        const int r = 4 * (f4 - 1);
+        v.x = r < cnt ? s_perm[off + r] : -1;
+        v.y = r + 1 < cnt ? s_perm[off + r + 1] : -1;
+        v.z = r + 2 < cnt ? s_perm[off + r + 2] : -1;
+        v.w = r + 3 < cnt ? s_perm[off + r + 3] : -1;
+      }
+    }
+    reinterpret_cast<int4*>(pv.dtab)[i] = v;
+  }
+}
+
 // ---------------------------------------------------------------------------
 // Plan of up to kDecodeMaxTokens * (32 + 1) pairs by one block of 256 threads.
 // `src` (shared memory) holds the M * k_eff expert ids of the pairs.  Also
-// writes the decode work table.  Three steps separated by barriers:
+// writes the decode work table.  Up to 32 pairs: plan_tiny.  Otherwise each
+// expert's token set is gathered first (one bit per token); where no token
+// lists an expert twice, one block scan over the experts gives counts,
+// offsets, active ranks and tiles, and a pair's position is its expert's
+// offset plus the earlier tokens in the expert's set.  Where a token does
+// list an expert twice, three steps separated by barriers:
 //   1. each pair's plan position, by direct comparison over the pairs (valid
 //      pairs of a lower expert, plus those of the same expert and a lower pair
 //      id): perm and inv; the first pair of each expert records the expert's
@@ -121,7 +165,12 @@ __device__ void plan_small_block(const LayerDims& d, int M, const int* src, cons
   __shared__ int s_cnt1[kDtabEntries];   // rows of the pair's expert if it is the first, else 0
   __shared__ int s_pos1[kDtabEntries];   // plan position of an expert's first pair
   __shared__ int s_ae[kDtabEntries], s_aoff[kDtabEntries], s_acnt[kDtabEntries];
-  __shared__ int s_nv, s_na, s_nt;
+  __shared__ int s_nv, s_na, s_nt, s_dup;
+  static_assert(kDtabEntries >= kMaxEEff, "per-expert arrays share the per-pair ones");
+  // the token set of each expert (bit m for token m) and each expert's first
+  // plan position share s_cnt1 / s_pos1, which only the step-by-step path uses
+  uint32_t* s_mask = reinterpret_cast<uint32_t*>(s_cnt1);
+  int* s_off = s_pos1;
   const int tid = threadIdx.x, nthr = blockDim.x, lane = tid & 31;
   const int P = M * d.k_eff, ne = d.e_eff;
   if (P <= 32) {
@@ -132,9 +181,11 @@ __device__ void plan_small_block(const LayerDims& d, int M, const int* src, cons
     s_nv = 0;
     s_na = 0;
     s_nt = 0;
+    s_dup = 0;
   }
+  for (int e = tid; e < ne; e += nthr) s_mask[e] = 0u;
   __syncthreads();
-  bool bad = false;
+  bool bad = false, dup = false;
   int nvalid = 0;
   for (int p = tid; p < P; p += nthr) {
     const int e = src[p];
@@ -142,14 +193,76 @@ __device__ void plan_small_block(const LayerDims& d, int M, const int* src, cons
     s_ids[p] = ok ? e : -1;
     bad = bad || !ok;
     nvalid += ok;
+    if (ok) {
+      const uint32_t bit = 1u << (p / d.k_eff);
+      dup = dup || (atomicOr(&s_mask[e], bit) & bit);
+    }
   }
   if (bad) set_status(status, MOE_ST_INVALID_ID);
+  if (dup) s_dup = 1;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) nvalid += __shfl_xor_sync(0xffffffffu, nvalid, o);
   if (lane == 0 && nvalid) atomicAdd(&s_nv, nvalid);
   __syncthreads();
   if (tid == 0) MOE_TL_MAX(36);
   const int nv = s_nv;
+  if (!s_dup) {
+    // No token lists an expert twice (every routed call: the top-k ids are
+    // distinct): an expert's pairs come one per token, in token order, so a
+    // pair's rank inside its expert is the number of earlier tokens in the
+    // expert's token set.  Experts 3 tid .. 3 tid + 2 take their counts,
+    // offsets, active ranks and tiles from one block scan.
+    int c[3], sa = 0, st = 0, so = 0;
+#pragma unroll
+    for (int i = 0; i < 3; ++i) {
+      const int e = 3 * tid + i;
+      c[i] = e < ne ? __popc(s_mask[e]) : 0;
+      sa += c[i] != 0;
+      st += (c[i] + kTileRows - 1) / kTileRows;
+      so += c[i];
+    }
+    int tot[3];
+    block_scan3(sa, st, so, tot);
+#pragma unroll
+    for (int i = 0; i < 3; ++i) {
+      const int e = 3 * tid + i;
+      if (e >= ne) break;
+      pv.counts[e] = c[i];
+      pv.offsets[e] = so;
+      s_off[e] = so;
+      if (c[i] != 0) {
+        s_ae[sa] = e;
+        s_aoff[sa] = so;
+        s_acnt[sa] = c[i];
+        pv.active[sa] = e;
+        for (int r0 = 0; r0 < c[i]; r0 += kTileRows, ++st)
+          reinterpret_cast<int4*>(pv.tiles)[st] = make_int4(e, r0, min(kTileRows, c[i] - r0), 0);
+        ++sa;
+      }
+      so += c[i];
+    }
+    if (tid == 0) {
+      pv.offsets[ne] = nv;
+      s_na = tot[0];
+      s_nt = tot[1];
+    }
+    __syncthreads();
+    for (int p = tid; p < P; p += nthr) {
+      const int e = s_ids[p];
+      if (e < 0) {
+        pv.inv[p] = -1;
+        continue;
+      }
+      const int m = p / d.k_eff;
+      const int pos = s_off[e] + __popc(s_mask[e] & ((1u << m) - 1u));
+      pv.perm[pos] = p;
+      pv.inv[p] = pos;
+      s_perm[pos] = p;
+    }
+    __syncthreads();
+    plan_header_and_table(d, M, nv, s_na, s_nt, s_ae, s_aoff, s_acnt, s_perm, pv);
+    return;
+  }
   // 1. positions
   for (int p = tid; p < P; p += nthr) {
     const int e = s_ids[p];
@@ -259,35 +372,7 @@ __device__ void plan_small_block(const LayerDims& d, int M, const int* src, cons
       pv.counts[e] = (lo < na && s_ae[lo] == e) ? s_acnt[lo] : 0;
     }
   }
-  if (tid == 0) {
-    pv.hdr->M = M;
-    pv.hdr->k_eff = d.k_eff;
-    pv.hdr->e_eff = ne;
-    pv.hdr->n_valid = nv;
-    pv.hdr->n_active = na;
-    pv.hdr->n_tiles = s_nt;
-  }
-  // decode work table: every entry up to the largest active-expert count, as
-  // five 16-byte groups (expert, first position, rows, -1 | first 16 pair ids)
-  static_assert(kDtabInts == 20, "a work-table entry is five 16-byte groups");
-  const int max_active = min(P, ne);
-  for (int i = tid; i < max_active * 5; i += nthr) {
-    const int a = i / 5, f4 = i - a * 5;
-    int4 v = make_int4(-1, -1, -1, -1);
-    if (a < na) {
-      const int off = s_aoff[a], cnt = s_acnt[a];
-      if (f4 == 0) {
-        v = make_int4(s_ae[a], off, cnt, -1);
-      } else {
-        const int r = 4 * (f4 - 1);
-        v.x = r < cnt ? s_perm[off + r] : -1;
-        v.y = r + 1 < cnt ? s_perm[off + r + 1] : -1;
-        v.z = r + 2 < cnt ? s_perm[off + r + 2] : -1;
-        v.w = r + 3 < cnt ? s_perm[off + r + 3] : -1;
-      }
-    }
-    reinterpret_cast<int4*>(pv.dtab)[i] = v;
-  }
+  plan_header_and_table(d, M, nv, na, s_nt, s_ae, s_aoff, s_acnt, s_perm, pv);
   if (tid == 0) MOE_TL_MAX(42);
 }
 

@@ -186,6 +186,27 @@ def test_plan_edge_cases(M):
     assert int(case.layer.status.item()) & moe.ST_INVALID_ID
 
 
+@pytest.mark.parametrize("dup", [False, True])
+def test_plan_decode_bucket_repeats_and_invalid(dup):
+    """64 pairs in the decode bucket (M 16, k 4) with invalid ids: distinct
+    experts per token (the per-expert token-set plan) and an expert repeated
+    inside some tokens (the step-by-step plan), bit-exact against the oracle
+    plan, work table included."""
+    wl = synth.custom("dq", 16, 256, 64, 4, 128)
+    case = Case(wl)
+    ids = synth.random_ids(wl, variant=4)
+    if dup:
+        ids[::3, 2] = ids[::3, 0]
+    ids[1, 3] = -1
+    ids[14, 0] = 64
+    w = np.full(ids.shape, 0.25, np.float32)
+    case.layer.status.zero_()
+    case.layer.route(case.x_t, torch.from_numpy(ids).cuda(), torch.from_numpy(w).cuda())
+    torch.cuda.synchronize()
+    _check_plan(case, ids)
+    assert int(case.layer.status.item()) & moe.ST_INVALID_ID
+
+
 @pytest.mark.parametrize("M", [8, 12, 600])
 def test_plan_with_shared_expert(M):
     wl = synth.custom("sh", M, 256, 16, 2, 128, bias="zipf", shared=True)
