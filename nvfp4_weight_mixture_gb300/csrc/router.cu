@@ -1129,6 +1129,11 @@ __device__ __forceinline__ void st_async_f32x4(uint32_t a, float4 v, uint32_t ba
       "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(bar)
       : "memory");
 }
+__device__ __forceinline__ void st_async_s32(uint32_t a, int v, uint32_t bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.s32 [%0], %1, [%2];" ::"r"(a),
+               "r"(v), "r"(bar)
+               : "memory");
+}
 // mbarrier wait with acquire at cluster scope (the data came from other CTAs
 // of the cluster); bounded like mbar_wait.
 __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity,
@@ -1198,7 +1203,8 @@ __global__ void __launch_bounds__(kRcThreads, 1)
   char* rsm = reinterpret_cast<char*>((reinterpret_cast<uintptr_t>(rsm_raw) + 1023) &
                                       ~uintptr_t(1023));
   __shared__ uint64_t full[kRcWarps][2];
-  __shared__ uint64_t xch;  // CTA 0: the logits of every slice have landed
+  __shared__ uint64_t xch;  // the logits of this CTA's tokens have landed
+  __shared__ uint64_t idb;  // CTA 0: the other CTAs' tokens' expert ids have landed
   __shared__ __align__(16) float s_bias[64];
   __shared__ int s_ids[kDecodeMaxTokens * 33];
   MOE_TL(kTlRouter);
@@ -1221,16 +1227,21 @@ __global__ void __launch_bounds__(kRcThreads, 1)
       mbar_init(&full[w][0], 1);
       mbar_init(&full[w][1], 1);
     }
+    // token m belongs to CTA m % C: every expert's logit of its tokens, and
+    // to CTA 0 the other CTAs' tokens' expert ids, arrive as transaction bytes
+    const int own = (M > (int)rank) ? (M - 1 - (int)rank) / (int)gridDim.x + 1 : 0;
+    mbar_init(&xch, 1);
+    mbar_expect_tx(&xch, (uint32_t)(own * E * 4));
     if (rank == 0) {
-      // every expert's logit of every token arrives as transaction bytes
-      mbar_init(&xch, 1);
-      mbar_expect_tx(&xch, (uint32_t)(M * E * 4));
+      mbar_init(&idb, 1);
+      mbar_expect_tx(&idb, (uint32_t)((M - own) * k * 4));
     }
     fence_mbar_init();
   }
   __syncthreads();
-  // CTA 0's barrier is initialised before any CTA writes to it: the cluster
-  // barrier is arrived at here and waited on just before the first write
+  // every CTA's barriers are initialised before any CTA writes to them: the
+  // cluster barrier is arrived at here and waited on just before the first
+  // write
   cluster_arrive();
   if (lane == 0)
     for (int i = 0; i < stages; ++i) {
@@ -1330,13 +1341,13 @@ __global__ void __launch_bounds__(kRcThreads, 1)
         }
   if (tid == 0) MOE_TL_MAX(20);
   __syncthreads();
-  cluster_wait();  // CTA 0's barrier is initialised
+  cluster_wait();  // every CTA's barriers are initialised
   // ---- logits of the slice, four experts per thread: the 8 warps' partials
-  // in warp order (+ bias), stored straight into CTA 0 (all_lg[m][rank Es +
-  // e]); E % 8 == 0 and Es % 16 == 0, so four experts are all valid or all
-  // past E ----
+  // in warp order (+ bias), stored straight into the CTA that owns the token
+  // (all_lg[m / C][rank Es + e] of CTA m % C); E % 8 == 0 and Es % 16 == 0,
+  // so four experts are all valid or all past E ----
+  const int C = (int)gridDim.x;
   {
-    const uint32_t xbar = dsmem_addr(&xch, 0);
     const int q4 = Es / 4;
     for (int i = tid; i < M * q4; i += kRcThreads) {
       const int m = i / q4, e = 4 * (i - m * q4), ge = (int)rank * Es + e;
@@ -1359,30 +1370,44 @@ __global__ void __launch_bounds__(kRcThreads, 1)
       sum.y += a.y;
       sum.z += a.z;
       sum.w += a.w;
-      st_async_f32x4(dsmem_addr(all_lg + (size_t)m * E + ge, 0), sum, xbar);
+      const uint32_t owner = (uint32_t)(m % C);
+      st_async_f32x4(dsmem_addr(all_lg + (size_t)(m / C) * E + ge, owner), sum,
+                     dsmem_addr(&xch, owner));
     }
   }
   if (tid == 0) MOE_TL_MIN(21);
-  if (rank != 0) return;  // nothing reads the other CTAs' shared memory
-  // every expert's logit of every token is in CTA 0
-  const bool have = mbar_wait_cluster(&xch, 0, status);
+  const int own = (M > (int)rank) ? (M - 1 - (int)rank) / C + 1 : 0;
+  if (own == 0) return;  // nothing writes to this CTA's shared memory
+  // every expert's logit of this CTA's tokens is here
+  if (!mbar_wait_cluster(&xch, 0, status)) return;
   if (tid == 0) MOE_TL_MAX(24);
-  if (!have) return;
 
-  // ---- top-k, weights, gate, plan (CTA 0): one warp per token over all E
-  // logits (largest first; ties: the lower expert id) ----
-  for (int m = warp; m < M; m += kRcWarps) {
+  // ---- top-k, weights, gate and route stores of this CTA's tokens: one warp
+  // per token over all E logits (largest first; ties: the lower expert id);
+  // the expert ids go to CTA 0, which builds the plan ----
+  const uint32_t ids0 = dsmem_addr(s_ids, 0), idbar = dsmem_addr(&idb, 0);
+  for (int lm = warp; lm < own; lm += kRcWarps) {
+    const int m = (int)rank + lm * C;
     int my_id = -1;
     float my_l = -INFINITY;
-    warp_topk<false>(all_lg + (size_t)m * E, E, k, &my_id, &my_l);
+    warp_topk<false>(all_lg + (size_t)lm * E, E, k, &my_id, &my_l);
     if (tid == 0) MOE_TL_MAX(26);
     const float w = warp_topk_weight(my_l, k);
     const float gamma = d.shared ? warp_gate(x + (size_t)m * H, wg, H) : 0.f;
     store_route(d, m, my_id, w, gamma, ids_user, w_user, pv);
     if (tid == 0) MOE_TL_MAX(28);
-    if (lane < k) s_ids[m * d.k_eff + lane] = my_id;
-    if (d.shared && lane == 0) s_ids[m * d.k_eff + k] = d.E;
+    if (lane < k) {
+      if (rank == 0)
+        s_ids[m * d.k_eff + lane] = my_id;
+      else
+        st_async_s32(ids0 + 4u * (uint32_t)(m * d.k_eff + lane), my_id, idbar);
+    }
   }
+  if (rank != 0) return;
+  // the other CTAs' tokens' ids; the shared expert's slot of every token
+  if (M > own && !mbar_wait_cluster(&idb, 0, status)) return;
+  if (d.shared)
+    for (int m = tid; m < M; m += kRcThreads) s_ids[m * d.k_eff + k] = d.E;
   __syncthreads();
   if (tid == 0) MOE_TL_MAX(30);
   plan_small_block(d, M, s_ids, pv, status);
