@@ -158,14 +158,29 @@ __device__ void plan_header_and_table(const LayerDims& d, int M, int nv, int na,
 //   3. counts and offsets of every expert (binary search in the active list),
 //      the header and the decode work table (16-byte stores).
 // ---------------------------------------------------------------------------
+// Shared-memory scratch of plan_small_block (its caller places it).
+struct PlanScratch {
+  int ids[kDtabEntries];   // expert of each pair, -1 if invalid
+  int perm[kDtabEntries];  // pair at each plan position
+  int cnt1[kDtabEntries];  // rows of the pair's expert if it is the first, else 0
+  int pos1[kDtabEntries];  // plan position of an expert's first pair
+  int ae[kDtabEntries], aoff[kDtabEntries], acnt[kDtabEntries];  // sorted active list
+  int nv, na, nt, dup;
+};
+
 __device__ void plan_small_block(const LayerDims& d, int M, const int* src, const PlanView& pv,
-                                 uint32_t* status) {
-  __shared__ int s_ids[kDtabEntries];    // expert of each pair, -1 if invalid
-  __shared__ int s_perm[kDtabEntries];   // pair at each plan position
-  __shared__ int s_cnt1[kDtabEntries];   // rows of the pair's expert if it is the first, else 0
-  __shared__ int s_pos1[kDtabEntries];   // plan position of an expert's first pair
-  __shared__ int s_ae[kDtabEntries], s_aoff[kDtabEntries], s_acnt[kDtabEntries];
-  __shared__ int s_nv, s_na, s_nt, s_dup;
+                                 uint32_t* status, PlanScratch* ps) {
+  int* const s_ids = ps->ids;
+  int* const s_perm = ps->perm;
+  int* const s_cnt1 = ps->cnt1;
+  int* const s_pos1 = ps->pos1;
+  int* const s_ae = ps->ae;
+  int* const s_aoff = ps->aoff;
+  int* const s_acnt = ps->acnt;
+  int& s_nv = ps->nv;
+  int& s_na = ps->na;
+  int& s_nt = ps->nt;
+  int& s_dup = ps->dup;
   static_assert(kDtabEntries >= kMaxEEff, "per-expert arrays share the per-pair ones");
   // the token set of each expert (bit m for token m) and each expert's first
   // plan position share s_cnt1 / s_pos1, which only the step-by-step path uses
@@ -511,7 +526,8 @@ __global__ void __launch_bounds__(256) router_small_kernel(LayerDims d, int M,
   }
   __syncthreads();
   if (tid == 0) MOE_TL_MAX(24);
-  plan_small_block(d, M, s_ids, pv, status);
+  __shared__ PlanScratch ps;
+  plan_small_block(d, M, s_ids, pv, status, &ps);
   if (tid == 0) MOE_TL_MIN(25);
 }
 
@@ -544,7 +560,8 @@ __global__ void __launch_bounds__(256) plan_small_kernel(LayerDims d, int M, Pla
   pdl_launch_dependents();
   for (int p = threadIdx.x; p < M * d.k_eff; p += blockDim.x) s_src[p] = pv.ids[p];
   __syncthreads();
-  plan_small_block(d, M, s_src, pv, status);
+  __shared__ PlanScratch ps;
+  plan_small_block(d, M, s_src, pv, status, &ps);
 }
 
 // ---------------------------------------------------------------------------
@@ -1189,7 +1206,9 @@ __host__ __device__ inline RouterClusterPlan router_cluster_plan(int H, int E, i
   if (st > 2) st = 2;
   if (st > p.ntw) st = p.ntw;
   p.stages = st;
-  p.ring = (size_t)kRcWarps * st * p.stage;
+  // the ring also holds CTA 0's plan scratch once the partial sums are read
+  const size_t ring = (size_t)kRcWarps * st * p.stage, scratch = align_up(sizeof(PlanScratch), 1024);
+  p.ring = ring > scratch ? ring : scratch;
   p.total = fixed + p.ring;
   return p;
 }
@@ -1410,7 +1429,8 @@ __global__ void __launch_bounds__(kRcThreads, 1)
     for (int m = tid; m < M; m += kRcThreads) s_ids[m * d.k_eff + k] = d.E;
   __syncthreads();
   if (tid == 0) MOE_TL_MAX(30);
-  plan_small_block(d, M, s_ids, pv, status);
+  // the plan's scratch takes the W_r ring, whose partial sums are all read
+  plan_small_block(d, M, s_ids, pv, status, reinterpret_cast<PlanScratch*>(ring));
   if (tid == 0) MOE_TL_MIN(25);
 }
 
