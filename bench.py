@@ -140,12 +140,12 @@ def kernel_accounting(wl, step, n_active, n_pairs, decode):
         b = n_active * w13_expert_bytes(wl) + M * H * 2 + n_pairs * I * 2
         f = n_pairs * 2 * H * 2 * I
     elif step == "w2":
-        # decode: the combine runs inside the W2 kernel (writes y); prefill: FP32 partials
-        out = M * H * 2 if decode else n_pairs * H * 4
+        # decode: the combine runs inside the W2 kernel (writes y); prefill: FP16 partials
+        out = M * H * 2 if decode else n_pairs * H * 2
         b = n_active * w2_expert_bytes(wl) + n_pairs * I * 2 + out
         f = n_pairs * 2 * I * H
     elif step == "combine":
-        b = n_pairs * H * 4 + M * H * 2
+        b = n_pairs * H * 2 + M * H * 2
         f = n_pairs * H
     else:  # plan: router weight + x + ids / weights
         b = H * wl.E * 2 + M * H * 2 + n_pairs * 8

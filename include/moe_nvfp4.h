@@ -273,10 +273,11 @@ int32_t moe_nvfp4_layer(const moe_nvfp4_config* cfg, int64_t M, const void* x,
  * Same arguments, results and rules as moe_nvfp4_forward, except that the
  * workspace is a 4 MiB array inside the library (allocated when the library
  * is loaded and held by every GPU that loads it until the process exits).
- * Calls whose workspace would exceed it (M * k_eff * (2*I + 4*H) bytes plus
+ * Calls whose workspace would exceed it (M * k_eff * (2*I + 2*H) bytes plus
  * alignment) return MOE_ERR_WORKSPACE and launch nothing.  At H 2048, I 512,
- * top-10 that admits M <= 16 (the decode kernels); at small layers larger M
- * fits and runs the grouped kernels (e.g. H 256, I 128, top-2: M <= ~1600).
+ * top-10 that admits M <= 81 (M <= 16 on the decode kernels, above that the
+ * grouped kernels); at small layers larger M fits (e.g. H 256, I 128, top-2:
+ * M <= 2730).
  * The first call on a device looks the array's device address up
  * (cudaGetSymbolAddress) with that device current and keeps it for the life
  * of the process; make that first call before any stream capture.  A device

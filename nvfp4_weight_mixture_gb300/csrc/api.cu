@@ -118,7 +118,7 @@ size_t plan_bytes_max(const LayerDims& d, int64_t max_tokens) {
 
 size_t ws_bytes_for(const LayerDims& d, int64_t M) {
   const int64_t P = M * d.k_eff;
-  return align_up((size_t)P * d.I * sizeof(__half), 256) + (size_t)P * d.H * sizeof(float);
+  return align_up((size_t)P * d.I * sizeof(__half), 256) + (size_t)P * d.H * sizeof(__half);
 }
 
 // `layout`, optionally with MOE_SCALES_PREPARED.
@@ -367,8 +367,8 @@ int32_t moe_nvfp4_forward(const moe_nvfp4_config* cfg, int64_t M, const void* x,
   plan_layout(static_cast<char*>(const_cast<void*>(plan)), M, d.k_eff, d.e_eff, d.E, d.H, &pv);
   const int64_t P = M * d.k_eff;
   __half* h = static_cast<__half*>(ws);
-  float* partial = reinterpret_cast<float*>(static_cast<char*>(ws) +
-                                            align_up((size_t)P * d.I * sizeof(__half), 256));
+  __half* partial = reinterpret_cast<__half*>(static_cast<char*>(ws) +
+                                              align_up((size_t)P * d.I * sizeof(__half), 256));
   Weights W13{w13->q, w13->s, w13->g}, W2{w2->q, w2->s, w2->g};
   Weights S13{nullptr, nullptr, nullptr}, S2{nullptr, nullptr, nullptr};
   if (d.shared) {

@@ -467,12 +467,12 @@ __global__ void __launch_bounds__(kW2Warps * 32, 1)
 }
 
 // ---------------------------------------------------------------------------
-// y[t] = fp16( sum_{j < k_eff} partial[inv[t * k_eff + j]] ), slots in order
-// (the partial rows sit at the pairs' plan positions); pairs dropped from the
-// plan (invalid ids) contribute nothing.
+// y[t] = fp16( sum_{j < k_eff} partial[inv[t * k_eff + j]] ), slots in order,
+// FP32 sums of the FP16 partial rows (which sit at the pairs' plan
+// positions); pairs dropped from the plan (invalid ids) contribute nothing.
 // ---------------------------------------------------------------------------
 __global__ void combine_kernel(int M, int H, int k_eff, const int32_t* __restrict__ inv,
-                               const float* __restrict__ partial, __half* __restrict__ y) {
+                               const __half* __restrict__ partial, __half* __restrict__ y) {
   MOE_TL(kTlCombine);
   pdl_wait();
   MOE_TL_WAITED();
@@ -485,11 +485,13 @@ __global__ void combine_kernel(int M, int H, int k_eff, const int32_t* __restric
   for (int j = 0; j < k_eff; ++j) {
     const int64_t pos = __ldcg(inv + t * k_eff + j);  // the pair's plan position
     if (pos < 0) continue;
-    const float4 v = __ldcs(reinterpret_cast<const float4*>(partial + pos * H + c));
-    s.x += v.x;
-    s.y += v.y;
-    s.z += v.z;
-    s.w += v.w;
+    const uint2 u = __ldcs(reinterpret_cast<const uint2*>(partial + pos * H + c));
+    const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
+    const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
+    s.x += a.x;
+    s.y += a.y;
+    s.z += b.x;
+    s.w += b.y;
   }
   __half2 lo = __floats2half2_rn(s.x, s.y), hi = __floats2half2_rn(s.z, s.w);
   uint2 out;
@@ -499,7 +501,7 @@ __global__ void combine_kernel(int M, int H, int k_eff, const int32_t* __restric
 }
 
 cudaError_t launch_combine(const LayerDims& d, int64_t M, const PlanView& pv,
-                           const float* partial, __half* y, cudaStream_t stream, bool pdl) {
+                           const __half* partial, __half* y, cudaStream_t stream, bool pdl) {
   const int64_t n4 = M * d.H / 4;
   const unsigned blocks = (unsigned)((n4 + 255) / 256);
   return launch_k(combine_kernel, dim3(blocks), dim3(256), 0, stream, pdl, (int)M, d.H, d.k_eff,
@@ -585,7 +587,7 @@ cudaError_t decode_device_init() {
 
 cudaError_t launch_decode_forward(const LayerDims& d, int64_t M, const __half* x,
                                   const PlanView& pv, Weights w13, Weights w2, Weights s13,
-                                  Weights s2, __half* y, __half* h, float* partial,
+                                  Weights s2, __half* y, __half* h, __half* partial,
                                   uint32_t* status, cudaStream_t stream, int num_sms,
                                   bool prepared) {
   (void)partial;

@@ -42,21 +42,21 @@ cudaError_t launch_plan(const LayerDims& d, int64_t M, const __half* x, const __
                         float* w_user, bool ids_given, const PlanView& pv, uint32_t* status,
                         cudaStream_t stream, int num_sms);
 
-// Forward paths.  partial: FP32 [M * k_eff][H], one row per pair at its plan
+// Forward paths.  partial: FP16 [M * k_eff][H], one row per pair at its plan
 // position; h: FP16 [M * k_eff][I] in plan order.
 // prepared: the scale arrays hold prepared FP16 scales (MOE_SCALES_PREPARED).
 cudaError_t launch_decode_forward(const LayerDims& d, int64_t M, const __half* x,
                                   const PlanView& pv, Weights w13, Weights w2, Weights s13,
-                                  Weights s2, __half* y, __half* h, float* partial,
+                                  Weights s2, __half* y, __half* h, __half* partial,
                                   uint32_t* status, cudaStream_t stream, int num_sms,
                                   bool prepared);
 cudaError_t launch_prefill_forward(const LayerDims& d, int64_t M, const __half* x,
                                    const PlanView& pv, Weights w13, Weights w2, Weights s13,
-                                   Weights s2, __half* y, __half* h, float* partial,
+                                   Weights s2, __half* y, __half* h, __half* partial,
                                    uint32_t* status, cudaStream_t stream, int num_sms,
                                    bool prepared);
 cudaError_t launch_combine(const LayerDims& d, int64_t M, const PlanView& pv,
-                           const float* partial, __half* y, cudaStream_t stream, bool pdl);
+                           const __half* partial, __half* y, cudaStream_t stream, bool pdl);
 
 // TMA tensor map over a byte matrix of `rows` x `row_bytes`, 8-byte elements,
 // box `box_bytes` x `box_rows` (tma.cu).

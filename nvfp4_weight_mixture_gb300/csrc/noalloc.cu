@@ -6,7 +6,7 @@
 // allocations are forbidden while a framework is capturing a CUDA graph, and C
 // callers behind a fixed signature with no workspace argument.  For them,
 // moe_nvfp4_forward_noalloc runs the same forward with its workspace (the h
-// rows and the per-pair FP32 partial rows) taken from g_noalloc_ws below: a
+// rows and the per-pair FP16 partial rows) taken from g_noalloc_ws below: a
 // file-scope device array of kNoAllocBytes that every GPU which loads this
 // library holds until the process exits.
 //

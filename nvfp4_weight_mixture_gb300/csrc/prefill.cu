@@ -46,9 +46,10 @@
 // W13: the fragment layout interleaves 16-row gate and up tiles, so TMEM lanes
 // [32q, 32q+16) hold gate rows and [32q+16, 32q+32) the matching up rows; the
 // epilogue pairs them with one shuffle and writes h = fp16(silu(G) * U).
-// W2:  the epilogue scales by g2 and the pair's combine weight and writes the
-// FP32 partial row of each pair at its plan position (rows of a unit are
-// consecutive); a separate pass sums each token's slots in order.
+// W2:  the epilogue scales the FP32 sums by g2 and the pair's combine weight
+// and writes each pair's partial row, rounded to FP16 (the activations' type),
+// at its plan position (rows of a unit are consecutive); a separate pass adds
+// each token's slots in order in FP32.
 #include <math.h>
 
 #include <algorithm>
@@ -559,7 +560,7 @@ static_assert(w2_smem_bytes() <= 232448, "grouped W2 shared memory above the sm_
 template <int SB>
 __global__ void __launch_bounds__(kW2Threads, 1)
     grouped_w2_kernel(LayerDims d, PlanView pv, const __grid_constant__ CUtensorMap bmap,
-                      Weights w, Weights ws, float* __restrict__ partial, uint32_t* status) {
+                      Weights w, Weights ws, __half* __restrict__ partial, uint32_t* status) {
   extern __shared__ __align__(1024) char smem_raw[];
   char* base = reinterpret_cast<char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                        ~uintptr_t(1023));
@@ -718,8 +719,8 @@ __global__ void __launch_bounds__(kW2Threads, 1)
     // ---- epilogue: lane r of warp (q, p) holds output row 32 q + r of the
     // unit (H row sub * 128 + 32 q + r) for the chunks c0 = 32 p, 32 p + 64, ...
     // A per-warp staging tile turns 16 columns at a time into rows of 32
-    // contiguous FP32 values, written as 16-byte stores into the pairs'
-    // partial rows (at the pairs' plan positions) ----
+    // contiguous FP32 values, scaled and written as FP16 (8-byte stores) into
+    // the pairs' partial rows (at the pairs' plan positions) ----
     const int q = warp & 3, pr = (warp - kW2EpiWarp0) >> 2;
     const int H = d.H;
     float(*stg)[32] = reinterpret_cast<float(*)[32]>(sm->stage[warp - kW2EpiWarp0]);
@@ -731,7 +732,7 @@ __global__ void __launch_bounds__(kW2Threads, 1)
       if (!warp_wait_or_abort(&sm->wsc_full[b], (it >> 1) & 1, status, abort)) break;
       tc_fence_after();
       const float* wsc = sm->wsc[b];
-      float* pbase = partial + (int64_t)un.pos0 * H + un.sub * 128 + q * 32;
+      __half* pbase = partial + (int64_t)un.pos0 * H + un.sub * 128 + q * 32;
       const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + b * kTileRows;
 #pragma unroll 1
       for (int c0 = 32 * pr; c0 < un.npad; c0 += 64) {
@@ -749,13 +750,14 @@ __global__ void __launch_bounds__(kW2Threads, 1)
             const int j = p4 * 4 + cl;
             const int n = c0 + 16 * hf + j;
             if (n < un.rows) {
-              float4 o = reinterpret_cast<const float4*>(stg[j])[part];
+              const float4 o = reinterpret_cast<const float4*>(stg[j])[part];
               const float sc = wsc[n];
-              o.x *= sc;
-              o.y *= sc;
-              o.z *= sc;
-              o.w *= sc;
-              __stcs(reinterpret_cast<float4*>(pbase + (int64_t)n * H) + part, o);
+              const __half2 lo = __floats2half2_rn(o.x * sc, o.y * sc);
+              const __half2 hi = __floats2half2_rn(o.z * sc, o.w * sc);
+              uint2 hv;
+              hv.x = *reinterpret_cast<const uint32_t*>(&lo);
+              hv.y = *reinterpret_cast<const uint32_t*>(&hi);
+              __stcs(reinterpret_cast<uint2*>(pbase + (int64_t)n * H) + part, hv);
             }
           }
           __syncwarp();
@@ -879,7 +881,7 @@ cudaError_t prefill_device_init() {
 
 cudaError_t launch_prefill_forward(const LayerDims& d, int64_t M, const __half* x,
                                    const PlanView& pv, Weights w13, Weights w2, Weights s13,
-                                   Weights s2, __half* y, __half* h, float* partial,
+                                   Weights s2, __half* y, __half* h, __half* partial,
                                    uint32_t* status, cudaStream_t stream, int num_sms,
                                    bool prepared) {
   const int64_t P = M * d.k_eff;
@@ -891,7 +893,7 @@ cudaError_t launch_prefill_forward(const LayerDims& d, int64_t M, const __half* 
   // Token-row operands in plan order, read as 64-row tensor-map tiles (128-byte
   // swizzled): W13 reads x rows gathered into the partials buffer (unused until
   // the W2 grid, which starts after W13 has finished), W2 reads h.
-  __half* xg = reinterpret_cast<__half*>(partial);
+  __half* xg = partial;
   CUtensorMap xmap, hmap;
   cudaError_t e = make_fp16_map(&xmap, xg, d.H, (uint64_t)P, kBK, kBChunkRows, true);
   if (e != cudaSuccess) return e;

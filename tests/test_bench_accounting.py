@@ -54,10 +54,10 @@ def test_prefill_m8192_layer_and_kernels():
     assert b13 == 512 * 1_179_652 + 8192 * 4096 + 81920 * 1024
     bound, b2, f2 = bench.kernel_accounting(wl, "w2", 512, 81920, decode=False)
     assert bound == "tensor" and f2 == 81920 * 2 * 512 * 2048
-    # W2 weights, h, FP32 partial rows
-    assert b2 == 512 * 589_828 + 81920 * 1024 + 81920 * 8192
+    # W2 weights, h, FP16 partial rows
+    assert b2 == 512 * 589_828 + 81920 * 1024 + 81920 * 4096
     bound, bc, _ = bench.kernel_accounting(wl, "combine", 512, 81920, decode=False)
-    assert bound == "hbm" and bc == 81920 * 8192 + 8192 * 4096
+    assert bound == "hbm" and bc == 81920 * 4096 + 8192 * 4096
 
 
 def test_shared_expert_layer():
