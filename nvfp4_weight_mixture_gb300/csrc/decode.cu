@@ -476,34 +476,37 @@ __global__ void combine_kernel(int M, int H, int k_eff, const int32_t* __restric
   MOE_TL(kTlCombine);
   pdl_wait();
   MOE_TL_WAITED();
-  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;  // one float4 of y
-  const int64_t n4 = (int64_t)M * H / 4;
-  if (i >= n4) return;
-  const int64_t t = (i * 4) / H;
-  const int c = (int)(i * 4 - t * H);
-  float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;  // 8 elements of y
+  const int64_t n8 = (int64_t)M * H / 8;
+  if (i >= n8) return;
+  const int64_t t = (i * 8) / H;
+  const int c = (int)(i * 8 - t * H);
+  float s[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
   for (int j = 0; j < k_eff; ++j) {
     const int64_t pos = __ldcg(inv + t * k_eff + j);  // the pair's plan position
     if (pos < 0) continue;
-    const uint2 u = __ldcs(reinterpret_cast<const uint2*>(partial + pos * H + c));
-    const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
-    const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
-    s.x += a.x;
-    s.y += a.y;
-    s.z += b.x;
-    s.w += b.y;
+    const uint4 u = __ldcs(reinterpret_cast<const uint4*>(partial + pos * H + c));
+    const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w4[q]));
+      s[2 * q] += f.x;
+      s[2 * q + 1] += f.y;
+    }
   }
-  __half2 lo = __floats2half2_rn(s.x, s.y), hi = __floats2half2_rn(s.z, s.w);
-  uint2 out;
-  out.x = *reinterpret_cast<uint32_t*>(&lo);
-  out.y = *reinterpret_cast<uint32_t*>(&hi);
-  *reinterpret_cast<uint2*>(y + t * H + c) = out;
+  uint32_t o[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const __half2 hq = __floats2half2_rn(s[2 * q], s[2 * q + 1]);
+    o[q] = *reinterpret_cast<const uint32_t*>(&hq);
+  }
+  *reinterpret_cast<uint4*>(y + t * H + c) = make_uint4(o[0], o[1], o[2], o[3]);
 }
 
 cudaError_t launch_combine(const LayerDims& d, int64_t M, const PlanView& pv,
                            const __half* partial, __half* y, cudaStream_t stream, bool pdl) {
-  const int64_t n4 = M * d.H / 4;
-  const unsigned blocks = (unsigned)((n4 + 255) / 256);
+  const int64_t n8 = M * d.H / 8;
+  const unsigned blocks = (unsigned)((n8 + 255) / 256);
   return launch_k(combine_kernel, dim3(blocks), dim3(256), 0, stream, pdl, (int)M, d.H, d.k_eff,
                   (const int32_t*)pv.inv, partial, y);
 }
