@@ -334,21 +334,20 @@ int32_t moe_nvfp4_set_trace_events(void* const* events, int32_t n_steps);
  * GEMM, not to this weight-streaming path).  x is FP16 [M][K] and y FP16
  * [M][N], row-major, device, 16-byte aligned. */
 
-/* Workspace bytes a dense call of this shape needs (0 when it needs none).
+/* Workspace bytes a dense call of this shape needs: 0 for every shape (each
+ * block of the kernel owns whole 16-row output tiles over all of K, so no
+ * partial sums are kept between blocks); the query and the ws arguments stay
+ * so that callers need not change if a later kernel asks for one.
  * Host-only; MOE_ERR_SHAPE as above, MOE_ERR_INVALID_ARG for a NULL out. */
 int32_t moe_nvfp4_dense_query(int64_t M, int64_t N, int64_t K, size_t* ws_bytes);
 
 /* NVFP4 dense projection (QPN2).  w: one N x K matrix in MOE_LAYOUT_FRAGMENT
  * (optionally | MOE_SCALES_PREPARED), w->g one FP32 global scale (scale_n =
  * g for all n).  ws: device workspace of at least moe_nvfp4_dense_query bytes
- * (may be NULL when that is 0), borrowed for the call's stream work; it
- * holds arrival counters and must be zero-filled before its first use (the
- * library leaves the counters at zero after every call that completes; after
- * a MOE_ST_TIMEOUT zero it again).  Dense calls on one workspace must not
- * overlap on the GPU.  Returns
- * MOE_ERR_LAYOUT for another layout, MOE_ERR_WORKSPACE for a short ws,
- * MOE_ERR_ALIGNMENT / MOE_ERR_INVALID_ARG as usual.  Bounded device waits set
- * MOE_ST_TIMEOUT in *status if they give up. */
+ * (NULL when that is 0, as it is for every shape), borrowed for the call's
+ * stream work.  Returns MOE_ERR_LAYOUT for another layout, MOE_ERR_WORKSPACE
+ * for a short ws, MOE_ERR_ALIGNMENT / MOE_ERR_INVALID_ARG as usual.  Bounded
+ * device waits set MOE_ST_TIMEOUT in *status if they give up. */
 int32_t moe_nvfp4_dense(int64_t M, int64_t N, int64_t K, const void* x,
                         const moe_nvfp4_weights* w, void* y, void* ws, size_t ws_bytes,
                         uint32_t* status, void* stream);

@@ -18,23 +18,20 @@
 // channel scale (FP8).
 //
 // Design.  The weights are the only large operand (HBM-bound), so the kernel
-// streams them once.  The work is the (256-row group, 64-element K segment)
-// pairs of the fragment layout, G-major; a fixed grid of kDnBlocks blocks
-// takes equal contiguous ranges of it, so every block streams the same number
-// of bytes.  A block's range falls into one or two "pieces" (the part inside
-// one group).  A producer thread fills a ring of stages, each one K segment
-// of a group (the group's 16 fragment tiles, contiguous, by one or two bulk
-// copies) plus the same segment of every token row (one 128-byte-swizzled
-// tensor-map tile).  Sixteen warps own one 16-row tile each (enough warps per
-// SM to overlap the dequantise / MMA dependency chains), dequantise their
-// fragments in registers straight into mma.sync A operands and multiply with
-// up to four 8-token column tiles.  A piece that is a whole group writes y;
-// otherwise it writes FP32 partial sums and takes a ticket of its group, and
-// the block that completes the group adds the group's pieces in K order and
-// writes y.  The ranges depend on N and K only, and a token's column of the
-// MMA does not depend on the other columns, so every output row is computed
-// by the same operations whatever M is: results are bitwise independent of
-// the batch.
+// streams them once.  Each of a fixed grid of up to kDnBlocks blocks owns a
+// contiguous range of the N / 16 output tiles (16 rows each) over the whole
+// of K, so no output is split between blocks.  It takes its tiles kDnTG at a
+// time: a producer thread fills a ring of stages, each up to kCH K segments
+// of those tiles (two 2-D tensor-map copies per tile: codes and scales) plus
+// the same segments of every token row (one 128-byte-swizzled tensor-map
+// copy).  The 16 consumer warps split the tiles evenly (16 / T warps per
+// tile, T the tiles in hand); warp r of a tile multiplies the tile's K
+// segments s with s % (16 / T) == r, dequantising its fragments in registers
+// straight into mma.sync A operands with up to four 8-token column tiles.
+// The tile's warps then add their sums in warp order and write y.  The tile
+// ranges depend on N only and a token's column of the MMA does not depend on
+// the other columns, so every output row is computed by the same operations
+// whatever M is: results are bitwise independent of the batch.
 #include <algorithm>
 
 #include "common.cuh"
@@ -42,152 +39,140 @@
 
 namespace moe {
 
-constexpr int kDnWarps = 16;                        // consumer warps
-constexpr int kDnTpw = 16 / kDnWarps;               // 16-row tiles of a group per consumer warp
-constexpr int kDnThreads = (kDnWarps + 1) * 32;     // + one producer warp
-constexpr int kDnBlocks = 152;                      // fixed grid (one block per SM of a GB300)
-constexpr int kDnRingBudget = 216 * 1024;
+constexpr int kDnWarps = 16;                     // consumer warps
+constexpr int kDnThreads = (kDnWarps + 1) * 32;  // + one producer warp
+constexpr int kDnBlocks = 152;                   // fixed grid (one block per SM of a GB300)
+constexpr int kDnTG = 4;                         // tiles in hand at a time
+constexpr int kDnSmemBudget = 216 * 1024;
 
-// Per weight format: bytes of one (group, segment) of codes (kQ) and scales
-// (kS), and kCH, the most consecutive segments one ring stage carries (one
-// bulk copy each for codes and scales, one tensor-map copy for the token rows:
-// few large copies keep many bytes in flight per SM).
+// Per weight format: bytes of one (tile, K segment) of codes (kQ) and scales
+// (kS) in the fragment layout, and kCH, the K segments of a stage (more for
+// the NVFP4 formats, whose expansion costs more instructions per byte: each
+// warp then takes more segments per stage wait).
 template <int FMT>
 struct DnFmt;
 template <>
 struct DnFmt<kDenseNvfp4> {  // E2M1 codes + raw E4M3 scales
-  static constexpr int kQ = 16 * 512, kS = 16 * 64, kCH = 4;
+  static constexpr int kQ = 512, kS = 64, kCH = 8;
 };
 template <>
 struct DnFmt<kDenseNvfp4Prepared> {  // E2M1 codes + prepared FP16 scales
-  static constexpr int kQ = 16 * 512, kS = 16 * 128, kCH = 4;
+  static constexpr int kQ = 512, kS = 128, kCH = 8;
 };
 template <>
 struct DnFmt<kDenseFp8> {  // E4M3 codes, channel scales applied to the sum
-  static constexpr int kQ = 16 * 1024, kS = 0, kCH = 2;
+  static constexpr int kQ = 1024, kS = 0, kCH = 8;
 };
-// Ring stage: codes of kCH segments | their scales | token rows (kCH tiles of
-// up to 32 rows x 128 bytes, 1024-byte aligned for the swizzle).
-template <int FMT>
+// Shared memory: the reduction area (the 16 warps' sums, [warp][NT][32][4]
+// FP32), then the ring.  A stage: codes [tile][segment][kQ] | scales
+// [tile][segment][kS] | token rows (kCH segments of NT x 8 rows x 128 bytes,
+// 1024-byte aligned for the swizzle).
+template <int FMT, int NT>
 struct DnRing {
   using F = DnFmt<FMT>;
-  static constexpr int kSOff = F::kCH * F::kQ;
-  static constexpr int kX = (int)((F::kCH * (F::kQ + F::kS) + 1023) / 1024 * 1024);
-  static constexpr int kStage = kX + F::kCH * 32 * 128;
-  static constexpr int kStages = std::min(8, kDnRingBudget / kStage);
-  static constexpr size_t kSmem = 1024 + (size_t)kStages * kStage;
+  // FP8 with 24 or 32 token rows keeps 4 segments a stage (room for 3 stages)
+  static constexpr int kCH = (FMT == kDenseFp8 && NT > 2) ? 4 : F::kCH;
+  static constexpr int kSOff = kDnTG * kCH * F::kQ;
+  static constexpr int kX = (kSOff + kDnTG * kCH * F::kS + 1023) / 1024 * 1024;
+  static constexpr int kStage = kX + kCH * NT * 8 * 128;
+  static constexpr int kRed = kDnWarps * NT * 32 * 4 * 4;
+  static constexpr int kStages = std::min(8, (kDnSmemBudget - kRed) / kStage);
+  static constexpr size_t kSmem = 1024 + kRed + (size_t)kStages * kStage;
+  static_assert(kSmem + 512 <= 232448, "dense ring above the shared-memory limit");
+  static_assert(kStages >= 3, "dense ring too shallow");
 };
-static_assert(DnRing<kDenseNvfp4>::kSmem + 256 <= 232448 &&
-                  DnRing<kDenseFp8>::kSmem + 256 <= 232448 &&
-                  DnRing<kDenseNvfp4Prepared>::kSmem + 256 <= 232448,
-              "dense ring above the shared-memory limit");
-static_assert(DnRing<kDenseNvfp4>::kStages >= 3 && DnRing<kDenseFp8>::kStages >= 3 &&
-                  DnRing<kDenseNvfp4Prepared>::kStages >= 3,
-              "dense ring too shallow");
 
-// Block b of the grid covers the flattened (group, segment) range
-// [b W / B, (b + 1) W / B), W = groups x segments, B = min(W, kDnBlocks).
-DenseSplit dense_split(int N, int K) {
-  DenseSplit p;
-  const int64_t W = (int64_t)(N / 256) * (K / 64);
-  p.blocks = (int)std::min<int64_t>(W, kDnBlocks);
-  const int len_max = (int)((W + p.blocks - 1) / p.blocks);
-  p.pieces = (len_max + (K / 64) - 1) / (K / 64) + 1;  // groups a range can touch
-  return p;
-}
+int dense_blocks(int N) { return std::min(N / 16, kDnBlocks); }
 
-// Workspace: one ticket per group (zero between calls), then FP32 [M][256]
-// partial sums per (block, piece).
-static size_t dense_tickets_bytes(int64_t N) { return align_up((size_t)(N / 256) * 4, 256); }
-
+// No output is split between blocks: no workspace.
 size_t dense_ws_bytes(int64_t M, int64_t N, int64_t K) {
-  if (M == 0) return 0;  // nothing is launched
-  const DenseSplit p = dense_split((int)N, (int)K);
-  const int64_t segs = K / 64, W = (N / 256) * segs;
-  bool whole = true;  // every range boundary on a group boundary: no piece to add up
-  for (int b = 0; b <= p.blocks; ++b) whole = whole && ((int64_t)b * W / p.blocks) % segs == 0;
-  if (whole) return 0;
-  return dense_tickets_bytes(N) + (size_t)p.blocks * p.pieces * M * 256 * sizeof(float);
-}
-
-__device__ __forceinline__ int dn_block_of(int64_t i, int64_t W, int B) {
-  return (int)(((i + 1) * B + W - 1) / W) - 1;  // the block whose range holds index i
+  (void)M;
+  (void)N;
+  (void)K;
+  return 0;
 }
 
 template <int FMT, int NT>
 __global__ void __launch_bounds__(kDnThreads, 1)
-    dense_kernel(int M, int N, int K, int pieces, const __grid_constant__ CUtensorMap xmap,
-                 const uint8_t* __restrict__ q, const uint8_t* __restrict__ s,
-                 const float* __restrict__ scale, char* __restrict__ ws, __half* __restrict__ y,
-                 uint32_t* status) {
+    dense_kernel(int M, int N, int K, const __grid_constant__ CUtensorMap xmap,
+                 const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap smap,
+                 const float* __restrict__ scale, __half* __restrict__ y, uint32_t* status) {
   using F = DnFmt<FMT>;
-  using R = DnRing<FMT>;
+  using R = DnRing<FMT, NT>;
   extern __shared__ __align__(1024) char dn_raw[];
   char* base = reinterpret_cast<char*>((reinterpret_cast<uintptr_t>(dn_raw) + 1023) &
                                        ~uintptr_t(1023));
+  float* red = reinterpret_cast<float*>(base);
+  char* ring = base + R::kRed;
   __shared__ uint64_t full[R::kStages], empty[R::kStages];
-  // per split piece: `written` completes when the 8 consumer warps have stored
-  // their partial sums, `decided` when warp 0 has taken the group's ticket
-  __shared__ uint64_t written, decided;
-  __shared__ int s_last;
+  __shared__ int s_abort;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, t4 = lane & 3;
-  const int segs = K >> 6;
-  const int B = gridDim.x;
-  const int64_t W = (int64_t)(N >> 8) * segs;
-  const int64_t r0 = (int64_t)blockIdx.x * W / B, r1 = (int64_t)(blockIdx.x + 1) * W / B;
-  uint32_t* tickets = reinterpret_cast<uint32_t*>(ws);
-  float* part = reinterpret_cast<float*>(ws + align_up((size_t)(N >> 8) * 4, 256));
+  const int S = K >> 6;
+  const int nt_all = N >> 4, B = gridDim.x;
+  const int t_begin = (int)((int64_t)blockIdx.x * nt_all / B);
+  const int t_end = (int)((int64_t)(blockIdx.x + 1) * nt_all / B);
+  const int n_chunks = (S + R::kCH - 1) / R::kCH;  // stages per group of tiles
   if (tid == 0) {
     for (int i = 0; i < R::kStages; ++i) {
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], kDnWarps);
     }
-    mbar_init(&written, kDnWarps);
-    mbar_init(&decided, 1);
+    s_abort = 0;
     fence_mbar_init();
   }
   __syncthreads();
   // Programmatic dependent launch: the next grid may start as soon as SMs
   // free up.  The weights are inputs of the call, not results of the previous
   // grid, so the first stages' weight copies go out before waiting for it;
-  // the token rows, the workspace and y are touched only after the wait.
+  // the token rows and y are touched only after the wait.
   pdl_launch_dependents();
 
   if (warp == kDnWarps) {
-    // ---- producer: one stage per K segment of the block's range ----
+    // ---- producer: stage k = (group of tiles, K chunk), in order ----
     if (lane == 0) {
       uint32_t k = 0;
       int pre_seg[R::kStages];  // first K segment of each stage issued before the wait
-      bool waited = false;
-      for (int64_t i = r0, n; i < r1; i += n, ++k) {
-        // up to kCH consecutive segments of one group: (group i / segs,
-        // segments i % segs ..): their tiles are contiguous in the fragment layout
-        n = min(min((int64_t)F::kCH, r1 - i), (int64_t)(segs - i % segs));
-        const int st = k % R::kStages;
-        if (!waited && k == (uint32_t)R::kStages) {
-          // the ring is full: wait for the previous grid, then the deferred token rows
-          pdl_wait();
-          waited = true;
-          for (uint32_t j = 0; j < k; ++j)
-            tma_load_3d(base + j * R::kStage + R::kX, &xmap, 0, 0, pre_seg[j], &full[j]);
+      bool waited = false, ok = true;
+      for (int t0 = t_begin; ok && t0 < t_end; t0 += kDnTG) {
+        const int T = min(kDnTG, t_end - t0);
+        for (int ch = 0; ch < n_chunks; ++ch, ++k) {
+          const int s0 = ch * R::kCH;
+          const int st = k % R::kStages;
+          if (!waited && k == (uint32_t)R::kStages) {
+            // the ring is full: wait for the previous grid, then the deferred token rows
+            pdl_wait();
+            waited = true;
+            for (uint32_t j = 0; j < k; ++j)
+              tma_load_3d(ring + j * R::kStage + R::kX, &xmap, 0, 0, pre_seg[j], &full[j]);
+          }
+          if (!mbar_wait(&empty[st], ((k / R::kStages) & 1) ^ 1, status)) {
+            ok = false;
+            break;
+          }
+          char* dst = ring + st * R::kStage;
+          // every copy moves its whole box (segments past K read as zeros)
+          mbar_expect_tx(&full[st],
+                         (uint32_t)(T * R::kCH * (F::kQ + F::kS) + R::kCH * NT * 8 * 128));
+          for (int t = 0; t < T; ++t) {
+            const int tile = t0 + t;
+            const int row = (tile >> 4) * S + s0;  // (group, segment) row of the fragment layout
+            tma_load_2d(dst + t * R::kCH * F::kQ, &qmap, (tile & 15) * (F::kQ / 8), row,
+                        &full[st]);
+            if (F::kS)
+              tma_load_2d(dst + R::kSOff + t * R::kCH * F::kS, &smap, (tile & 15) * (F::kS / 8),
+                          row, &full[st]);
+          }
+          if (waited)
+            tma_load_3d(dst + R::kX, &xmap, 0, 0, s0, &full[st]);
+          else
+            pre_seg[k] = s0;
         }
-        if (!mbar_wait(&empty[st], ((k / R::kStages) & 1) ^ 1, status)) break;
-        char* dst = base + st * R::kStage;
-        mbar_expect_tx(&full[st], (uint32_t)(n * (F::kQ + F::kS) + F::kCH * NT * 8 * 128));
-        bulk_g2s(dst, q + (size_t)i * F::kQ, (uint32_t)(n * F::kQ), &full[st]);
-        if (F::kS)
-          bulk_g2s(dst + R::kSOff, s + (size_t)i * F::kS, (uint32_t)(n * F::kS), &full[st]);
-        // kCH segments of the token rows (those past K read as zeros, unused)
-        if (waited)
-          tma_load_3d(dst + R::kX, &xmap, 0, 0, (int)(i % segs), &full[st]);
-        else
-          pre_seg[k] = (int)(i % segs);
       }
       if (!waited) {
         pdl_wait();
         for (uint32_t j = 0; j < k; ++j)
-          tma_load_3d(base + j * R::kStage + R::kX, &xmap, 0, 0, pre_seg[j], &full[j]);
+          tma_load_3d(ring + j * R::kStage + R::kX, &xmap, 0, 0, pre_seg[j], &full[j]);
       }
       // copies still in flight land before the block exits (bounded waits)
       for (uint32_t j = (k > (uint32_t)R::kStages ? k - R::kStages : 0); j < k; ++j)
@@ -196,53 +181,44 @@ __global__ void __launch_bounds__(kDnThreads, 1)
     return;
   }
 
-  // ---- consumers: warp w owns tiles kDnTpw w .. kDnTpw w + kDnTpw - 1 of the group ----
-  pdl_wait();  // the workspace and y of the previous grid are free
-  const int tile0 = kDnTpw * warp;
-  uint32_t k = 0, n_split = 0;
-  int p = 0;
-  for (int64_t i0 = r0; i0 < r1; ++p) {
-    const int G = (int)(i0 / segs);
-    const int64_t i1 = min(r1, (int64_t)(G + 1) * segs);  // this piece: [i0, i1)
-    float acc[kDnTpw][NT][4];
+  // ---- consumers ----
+  pdl_wait();  // y of the previous grid is free
+  uint32_t k = 0;
+  for (int t0 = t_begin; t0 < t_end; t0 += kDnTG) {
+    const int T = min(kDnTG, t_end - t0);
+    const int wpt = kDnWarps / T;  // warps per tile
+    const int tl = warp / wpt, r = warp - tl * wpt;
+    const bool active = tl < T;
+    float acc[NT][4];
 #pragma unroll
-    for (int a = 0; a < kDnTpw; ++a)
+    for (int b = 0; b < NT; ++b)
 #pragma unroll
-      for (int b = 0; b < NT; ++b)
-#pragma unroll
-        for (int c = 0; c < 4; ++c) acc[a][b][c] = 0.f;
-    bool ok = true;
-    for (int64_t i = i0, n; i < i1; i += n, ++k) {
-      n = min((int64_t)F::kCH, i1 - i);
+      for (int c = 0; c < 4; ++c) acc[b][c] = 0.f;
+    for (int ch = 0; ch < n_chunks; ++ch, ++k) {
       const int st = k % R::kStages;
       if (!mbar_wait(&full[st], (k / R::kStages) & 1, status)) {
-        ok = false;
-        break;
-      }
-      const char* sb = base + st * R::kStage;
+        if (lane == 0) s_abort = 1;
+      } else if (active) {
+        const char* sb = ring + st * R::kStage;
+        const int s0 = ch * R::kCH;
+        // this warp's segments of the stage: s % wpt == r
+        for (int c = ((r - s0) % wpt + wpt) % wpt; c < R::kCH && s0 + c < S; c += wpt) {
+          // token rows of segment c: lane (g, t4) reads elements [16 t4, 16 t4 + 16)
+          // of token nt * 8 + g (16-byte chunks 2 t4 and 2 t4 + 1, swizzled by row)
+          uint32_t xw[NT][8];
 #pragma unroll
-      for (int c = 0; c < F::kCH; ++c) {
-        if (c >= n) break;
-        // token rows of segment c: lane (g, t4) reads elements [16 t4, 16 t4 + 16)
-        // of token nt * 8 + g (16-byte chunks 2 t4 and 2 t4 + 1, swizzled by row)
-        uint32_t xw[NT][8];
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          const char* xr = sb + R::kX + (c * NT * 8 + nt * 8 + g) * 128;
-          const uint4 v0 = *reinterpret_cast<const uint4*>(xr + (((2 * t4) ^ g) << 4));
-          const uint4 v1 = *reinterpret_cast<const uint4*>(xr + (((2 * t4 + 1) ^ g) << 4));
-          xw[nt][0] = v0.x; xw[nt][1] = v0.y; xw[nt][2] = v0.z; xw[nt][3] = v0.w;
-          xw[nt][4] = v1.x; xw[nt][5] = v1.y; xw[nt][6] = v1.z; xw[nt][7] = v1.w;
-        }
-        const char* qb = sb + c * F::kQ;
-        const char* sc_b = sb + R::kSOff + c * F::kS;
-#pragma unroll
-        for (int tt = 0; tt < kDnTpw; ++tt) {
-          const int j = tile0 + tt;
+          for (int nt = 0; nt < NT; ++nt) {
+            const char* xr = sb + R::kX + (c * NT * 8 + nt * 8 + g) * 128;
+            const uint4 v0 = *reinterpret_cast<const uint4*>(xr + (((2 * t4) ^ g) << 4));
+            const uint4 v1 = *reinterpret_cast<const uint4*>(xr + (((2 * t4 + 1) ^ g) << 4));
+            xw[nt][0] = v0.x; xw[nt][1] = v0.y; xw[nt][2] = v0.z; xw[nt][3] = v0.w;
+            xw[nt][4] = v1.x; xw[nt][5] = v1.y; xw[nt][6] = v1.z; xw[nt][7] = v1.w;
+          }
+          const char* qb = sb + (tl * R::kCH + c) * F::kQ;
           if constexpr (FMT == kDenseFp8) {
             // block of 1024 bytes: row g's 16 codes at 16 L, row g + 8's at 512 + 16 L
-            const uint4 qa = *reinterpret_cast<const uint4*>(qb + j * 1024 + lane * 16);
-            const uint4 qc = *reinterpret_cast<const uint4*>(qb + j * 1024 + 512 + lane * 16);
+            const uint4 qa = *reinterpret_cast<const uint4*>(qb + lane * 16);
+            const uint4 qc = *reinterpret_cast<const uint4*>(qb + 512 + lane * 16);
             const uint32_t wa[4] = {qa.x, qa.y, qa.z, qa.w}, wb[4] = {qc.x, qc.y, qc.z, qc.w};
 #pragma unroll
             for (int s4 = 0; s4 < 4; ++s4) {
@@ -253,24 +229,23 @@ __global__ void __launch_bounds__(kDnThreads, 1)
               af[3] = e4m3x2_to_f16x2(wb[s4] >> 16);
 #pragma unroll
               for (int nt = 0; nt < NT; ++nt)
-                mma_16816(acc[tt][nt], af, xw[nt][2 * s4], xw[nt][2 * s4 + 1]);
+                mma_16816(acc[nt], af, xw[nt][2 * s4], xw[nt][2 * s4 + 1]);
             }
           } else {
-            const uint4 qv = *reinterpret_cast<const uint4*>(qb + j * 512 + lane * 16);
+            const char* sc_b = sb + R::kSOff + (tl * R::kCH + c) * F::kS;
+            const uint4 qv = *reinterpret_cast<const uint4*>(qb + lane * 16);
             uint32_t sg, sg8;
             if constexpr (FMT == kDenseNvfp4Prepared)
-              scale_splats_f16(*reinterpret_cast<const uint32_t*>(sc_b + j * 128 + lane * 4),
-                               &sg, &sg8);
+              scale_splats_f16(*reinterpret_cast<const uint32_t*>(sc_b + lane * 4), &sg, &sg8);
             else
-              scale_splats(*reinterpret_cast<const unsigned short*>(sc_b + j * 64 + lane * 2),
-                           &sg, &sg8);
+              scale_splats(*reinterpret_cast<const unsigned short*>(sc_b + lane * 2), &sg, &sg8);
 #pragma unroll
             for (int s4 = 0; s4 < 4; ++s4) {
               uint32_t af[4];
               a_frag(qv, sg, sg8, s4, af);
 #pragma unroll
               for (int nt = 0; nt < NT; ++nt)
-                mma_16816(acc[tt][nt], af, xw[nt][2 * s4], xw[nt][2 * s4 + 1]);
+                mma_16816(acc[nt], af, xw[nt][2 * s4], xw[nt][2 * s4 + 1]);
             }
           }
         }
@@ -278,142 +253,73 @@ __global__ void __launch_bounds__(kDnThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[st]);
     }
-    if (!__all_sync(0xffffffffu, ok)) break;
-    const int64_t gs0 = (int64_t)G * segs, gs1 = gs0 + segs;
-    const bool whole = (i0 == gs0 && i1 == gs1);
-    // c0 (row g, token 2 t4), c1 (g, 2 t4 + 1), c2 (g + 8, 2 t4), c3 (g + 8, 2 t4 + 1)
-    float* slot = part + ((size_t)blockIdx.x * pieces + p) * M * 256;
+    // ---- the tile's warps' sums in warp order: red[warp][nt][lane][c] ----
 #pragma unroll
-    for (int tt = 0; tt < kDnTpw; ++tt)
+    for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const int m = nt * 8 + 2 * t4 + (c & 1);
-          const int r = 16 * (tile0 + tt) + g + ((c & 2) ? 8 : 0);  // row inside the group
-          if (m < M) {
-            if (whole) {
-              const float sc = (FMT == kDenseFp8) ? scale[G * 256 + r] : scale[0];
-              y[(size_t)m * N + G * 256 + r] = __float2half_rn(acc[tt][nt][c] * sc);
-            } else {
-              slot[m * 256 + r] = acc[tt][nt][c];
-            }
-          }
-        }
-    if (!whole) {
-      // the block that brings the group's last piece adds them up in K order
-      const int b_first = dn_block_of(gs0, W, B), b_last = dn_block_of(gs1 - 1, W, B);
-      // the warps' partial sums reach warp 0 through the mbarrier (CTA scope);
-      // warp 0's device-scope fence then orders all of them before the ticket
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&written);
-      if (warp == 0) {
-        const bool all_in = mbar_wait(&written, n_split & 1, status);
-        if (lane == 0) {
-          s_last = 0;
-          if (all_in) {
-            __threadfence();
-            const uint32_t t = atomicAdd(&tickets[G], 1u);
-            s_last = (t == (uint32_t)(b_last - b_first));
-            if (s_last) {
-              tickets[G] = 0u;  // ready for the next call
-              // acquire side: the other blocks' pieces are visible to this
-              // block's threads, which are ordered after this fence by `decided`
-              __threadfence();
-            }
-          }
-          mbar_arrive(&decided);
-        }
-      }
-      const bool dec = mbar_wait(&decided, n_split & 1, status);
-      ++n_split;
-      if (!__all_sync(0xffffffffu, dec)) break;
-      if (s_last) {
-        for (int e = tid; e < M * 64; e += kDnWarps * 32) {  // one float4 of y each
-          const int m = e >> 6, r = (e & 63) * 4;
-          float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-          // the pieces in K order, eight loads in flight at a time
-          for (int b0 = b_first; b0 <= b_last; b0 += 8) {
-            float4 v[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-              const int b = b0 + u;
-              if (b <= b_last) {
-                const int pb = G - (int)(((int64_t)b * W / B) / segs);  // piece of block b in G
-                v[u] = __ldcg(reinterpret_cast<const float4*>(
-                    part + ((size_t)b * pieces + pb) * M * 256 + m * 256 + r));
-              }
-            }
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-              const int b = b0 + u;
-              if (b > b_last) break;
-              if (b == b_first) {
-                a = v[u];
-              } else {
-                a.x += v[u].x;
-                a.y += v[u].y;
-                a.z += v[u].z;
-                a.w += v[u].w;
-              }
-            }
-          }
-          float4 sc;
-          if (FMT == kDenseFp8) {
-            sc = *reinterpret_cast<const float4*>(scale + G * 256 + r);
-          } else {
-            const float s0 = scale[0];
-            sc = make_float4(s0, s0, s0, s0);
-          }
-          const __half2 lo = __floats2half2_rn(a.x * sc.x, a.y * sc.y);
-          const __half2 hi = __floats2half2_rn(a.z * sc.z, a.w * sc.w);
-          uint2 out;
-          out.x = *reinterpret_cast<const uint32_t*>(&lo);
-          out.y = *reinterpret_cast<const uint32_t*>(&hi);
-          *reinterpret_cast<uint2*>(y + (size_t)m * N + G * 256 + r) = out;
-        }
-      }
+      for (int c = 0; c < 4; ++c) red[((warp * NT + nt) * 32 + lane) * 4 + c] = acc[nt][c];
+    asm volatile("bar.sync 1, %0;" ::"r"(kDnWarps * 32) : "memory");
+    if (s_abort) break;
+    // thread: tile i < T, output element (nt, lane, c) of it
+    for (int e = tid; e < T * NT * 128; e += kDnWarps * 32) {
+      const int ti = e / (NT * 128), rem = e - ti * (NT * 128);
+      const int nt = rem >> 7, ln = (rem >> 2) & 31, c = rem & 3;
+      const int m = nt * 8 + 2 * (ln & 3) + (c & 1);
+      if (m >= M) continue;
+      float a = 0.f;
+      for (int rr = 0; rr < wpt; ++rr) a += red[(((ti * wpt + rr) * NT + nt) * 32 + ln) * 4 + c];
+      // c0 (row g, token 2 t4), c1 (g, 2 t4 + 1), c2 (g + 8, 2 t4), c3 (g + 8, 2 t4 + 1)
+      const int row = 16 * (t0 + ti) + (ln >> 2) + ((c & 2) ? 8 : 0);
+      const float sc = (FMT == kDenseFp8) ? scale[row] : scale[0];
+      y[(size_t)m * N + row] = __float2half_rn(a * sc);
     }
-    i0 = i1;
+    asm volatile("bar.sync 1, %0;" ::"r"(kDnWarps * 32) : "memory");  // red is reused
   }
 }
 
 template <int FMT, int NT>
-static cudaError_t dense_go(int M, int N, int K, const DenseSplit& sp, const CUtensorMap& xmap,
-                            const uint8_t* q, const uint8_t* s, const float* scale, char* ws,
-                            __half* y, uint32_t* status, cudaStream_t stream) {
-  return launch_k(dense_kernel<FMT, NT>, dim3(sp.blocks), dim3(kDnThreads), DnRing<FMT>::kSmem,
-                  stream, !trace_on(), M, N, K, sp.pieces, xmap, q, s, scale, ws, y, status);
+static cudaError_t dense_go(int M, int N, int K, const __half* x, const uint8_t* q,
+                            const uint8_t* s, const float* scale, __half* y, uint32_t* status,
+                            cudaStream_t stream) {
+  using F = DnFmt<FMT>;
+  constexpr int kCH = DnRing<FMT, NT>::kCH;
+  // the fragment layout as rows of (256-row group, K segment): 16 tiles of kQ
+  // code bytes (kS scale bytes); a box is one tile over kCH segments
+  const uint64_t rows = (uint64_t)(N / 256) * (K / 64);
+  CUtensorMap xmap, qmap, smap;
+  cudaError_t e = make_fp16_segments_map(&xmap, x, (uint64_t)K, (uint64_t)M, (uint32_t)(NT * 8),
+                                         (uint32_t)kCH);
+  if (e != cudaSuccess) return e;
+  if ((e = make_rows_map(&qmap, q, 16 * F::kQ, rows, F::kQ, kCH)) != cudaSuccess) return e;
+  smap = qmap;
+  if (F::kS && (e = make_rows_map(&smap, s, 16 * F::kS, rows, F::kS, kCH)) != cudaSuccess)
+    return e;
+  return launch_k(dense_kernel<FMT, NT>, dim3(dense_blocks(N)), dim3(kDnThreads),
+                  DnRing<FMT, NT>::kSmem, stream, !trace_on(), M, N, K, xmap, qmap, smap, scale,
+                  y, status);
 }
 
 template <int FMT>
-static cudaError_t dense_fmt(int M, int N, int K, const DenseSplit& sp, const CUtensorMap& xmap,
-                             const uint8_t* q, const uint8_t* s, const float* scale, char* ws,
-                             __half* y, uint32_t* status, cudaStream_t stream) {
+static cudaError_t dense_fmt(int M, int N, int K, const __half* x, const uint8_t* q,
+                             const uint8_t* s, const float* scale, __half* y, uint32_t* status,
+                             cudaStream_t stream) {
   switch ((M + 7) / 8) {
-    case 1: return dense_go<FMT, 1>(M, N, K, sp, xmap, q, s, scale, ws, y, status, stream);
-    case 2: return dense_go<FMT, 2>(M, N, K, sp, xmap, q, s, scale, ws, y, status, stream);
-    case 3: return dense_go<FMT, 3>(M, N, K, sp, xmap, q, s, scale, ws, y, status, stream);
-    default: return dense_go<FMT, 4>(M, N, K, sp, xmap, q, s, scale, ws, y, status, stream);
+    case 1: return dense_go<FMT, 1>(M, N, K, x, q, s, scale, y, status, stream);
+    case 2: return dense_go<FMT, 2>(M, N, K, x, q, s, scale, y, status, stream);
+    case 3: return dense_go<FMT, 3>(M, N, K, x, q, s, scale, y, status, stream);
+    default: return dense_go<FMT, 4>(M, N, K, x, q, s, scale, y, status, stream);
   }
 }
 
 cudaError_t launch_dense(int fmt, int64_t M, int64_t N, int64_t K, const __half* x,
                          const uint8_t* q, const uint8_t* s, const float* scale, void* ws,
                          __half* y, uint32_t* status, cudaStream_t stream) {
+  (void)ws;
   const int Mi = (int)M, Ni = (int)N, Ki = (int)K;
-  const DenseSplit sp = dense_split(Ni, Ki);
-  const int nt = (Mi + 7) / 8;
-  CUtensorMap xmap;
-  const uint32_t ch = fmt == kDenseFp8 ? DnFmt<kDenseFp8>::kCH : DnFmt<kDenseNvfp4>::kCH;
-  cudaError_t e = make_fp16_segments_map(&xmap, x, (uint64_t)K, (uint64_t)M, (uint32_t)(nt * 8), ch);
-  if (e != cudaSuccess) return e;
-  char* w = static_cast<char*>(ws);
-  if (fmt == kDenseFp8)
-    return dense_fmt<kDenseFp8>(Mi, Ni, Ki, sp, xmap, q, s, scale, w, y, status, stream);
+  if (fmt == kDenseFp8) return dense_fmt<kDenseFp8>(Mi, Ni, Ki, x, q, s, scale, y, status, stream);
   if (fmt == kDenseNvfp4Prepared)
-    return dense_fmt<kDenseNvfp4Prepared>(Mi, Ni, Ki, sp, xmap, q, s, scale, w, y, status, stream);
-  return dense_fmt<kDenseNvfp4>(Mi, Ni, Ki, sp, xmap, q, s, scale, w, y, status, stream);
+    return dense_fmt<kDenseNvfp4Prepared>(Mi, Ni, Ki, x, q, s, scale, y, status, stream);
+  return dense_fmt<kDenseNvfp4>(Mi, Ni, Ki, x, q, s, scale, y, status, stream);
 }
 
 // ---------------------------------------------------------------------------
@@ -546,7 +452,7 @@ cudaError_t dense_device_init() {
   {                                                                                         \
     cudaError_t e = cudaFuncSetAttribute(dense_kernel<F, T>,                                \
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,       \
-                                         (int)DnRing<F>::kSmem);                            \
+                                         (int)DnRing<F, T>::kSmem);                         \
     if (e != cudaSuccess) return e;                                                         \
   }
   MOE_DN_ATTR(kDenseNvfp4, 1) MOE_DN_ATTR(kDenseNvfp4, 2) MOE_DN_ATTR(kDenseNvfp4, 3)

@@ -75,14 +75,9 @@ cudaError_t make_fp16_segments_map(CUtensorMap* map, const void* base, uint64_t 
 cudaError_t make_fp16_map_swz(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows,
                               uint32_t box_cols, uint32_t box_rows, int swizzle_bytes);
 
-// Dense few-row projection (dense.cu): weight formats, K split, launchers.
+// Dense few-row projection (dense.cu): weight formats, launchers.
 enum DenseFormat { kDenseNvfp4 = 0, kDenseNvfp4Prepared = 1, kDenseFp8 = 2 };
 constexpr int kDenseMaxTokens = 32;
-struct DenseSplit {
-  int blocks;  // grid: equal contiguous ranges of the (group, K segment) pairs
-  int pieces;  // groups one block's range can touch
-};
-DenseSplit dense_split(int N, int K);
 size_t dense_ws_bytes(int64_t M, int64_t N, int64_t K);
 cudaError_t launch_dense(int fmt, int64_t M, int64_t N, int64_t K, const __half* x,
                          const uint8_t* q, const uint8_t* s, const float* scale, void* ws,
