@@ -148,6 +148,27 @@ def test_dense_batch_invariance(fmt, wl):
     np.testing.assert_array_equal(y1.view(np.uint16), parts[5:6].view(np.uint16))
 
 
+# Shapes the layer workloads do not reach: one 256-row group (16 blocks of one
+# tile), K of 5 and 17 segments (stages only partly used), and 1024 tiles over
+# the 152 blocks (6 or 7 each: more than one group of 4 tiles in hand).
+ODD = [synth.DenseWorkload("dense_one_group", 53, 8, 256, 320),
+       synth.DenseWorkload("dense_many_tiles", 54, 8, 16384, 1088)]
+
+
+@pytest.mark.parametrize("fmt", ["nvfp4", "fp8", "prepared"])
+@pytest.mark.parametrize("wl", ODD, ids=[w.name for w in ODD])
+def test_dense_other_shapes_vs_oracle_and_batch(fmt, wl):
+    d = _mat(wl)
+    x = d.x(20, variant=2)
+    y = d.gpu(fmt, x)
+    rel, mx = compare(y, d.ref("fp8" if fmt == "fp8" else "nvfp4", x))
+    assert rel <= REL_L2_TOL and mx <= MAX_ABS_TOL, (rel, mx)
+    # rows equal to the same rows of smaller calls (M 20 against 8 + 12)
+    a = d.gpu(fmt, np.ascontiguousarray(x[:8]))
+    b = d.gpu(fmt, np.ascontiguousarray(x[8:]))
+    np.testing.assert_array_equal(y.view(np.uint16), np.concatenate([a, b]).view(np.uint16))
+
+
 @pytest.mark.parametrize("wl,M", [(GU, 1), (GU, 16), (DN, 8), (DN, 32), (SMALL, 3)])
 def test_dense_prepared_scales_bitwise_equal_raw(wl, M):
     d = _mat(wl)
