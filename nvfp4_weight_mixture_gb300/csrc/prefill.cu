@@ -98,11 +98,15 @@ struct GemmSmem {
   // thread commits K step k to empty[k % kBStages], which frees both.
   uint64_t full[kBStages], empty[kBStages];
   uint64_t accf, tmem_empty, drain;
+  // W13 epilogue chunks: every dequantising warp has staged its tile
+  // (ep_staged) / has copied its token rows out (ep_free)
+  uint64_t ep_staged, ep_free;
   uint32_t tmem;
   int abort;
   int n_units;
-  // epilogue staging, 1 KiB per warp: h values [32 tokens][16 i] (FP16)
-  __align__(16) float stage[kDqWarps][256];
+  // epilogue staging, 1 KiB per warp (+16 bytes, so that the eight warps'
+  // tiles start on different banks): h values [32 tokens][16 i] (FP16)
+  __align__(16) float stage[kDqWarps][260];
 };
 
 constexpr size_t gemm_smem_bytes() {
@@ -233,6 +237,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
     mbar_init(&sm->accf, 1);
     mbar_init(&sm->tmem_empty, kDqWarps);
+    mbar_init(&sm->ep_staged, kDqWarps);
+    mbar_init(&sm->ep_free, kDqWarps);
     mbar_init(&sm->drain, 1);
     sm->abort = 0;
     fence_mbar_init();
@@ -386,7 +392,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 #endif
   } else {
     // ---- warps 0-7: dequantise, then the unit's epilogue ---------------------------
-    uint32_t kd = 0, it = 0;
+    uint32_t kd = 0, it = 0, ch = 0;  // ch: epilogue chunks so far
     for (int u = blockIdx.x; u < n_units && !*abort; u += gridDim.x, ++it) {
       const Unit un = load_unit<true, SB>(d, pv, w, ws, u, upt);
       bool ok = true;
@@ -457,16 +463,27 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       // matching up row, for 32 token columns per load.  One exchange per
       // pair of columns gives each lane 16 (G, U) pairs: gate lanes take
       // columns 0-15, up lanes 16-31.  h goes through a per-warp staging
-      // tile; each token row's 16 values [16q, 16q + 16) of the 64-wide K
-      // step leave as four 8-byte groups, group r at position 16r + 4q (the
-      // K order of the W2 operand).
+      // tile: a token row's 16 values of warp (q, t) belong at positions
+      // 64 t + 16 r + 4 q + (0..3), r = 0..3, of the unit's 128 h values
+      // (the K order of the W2 operand).  Once the eight warps have staged a
+      // chunk, each writes four whole token rows (256 bytes, one 8-byte store
+      // per lane) gathered from the eight tiles.
       const int I = d.I;
       const int r16 = lane & 15;
       const bool is_gate = lane < 16;
       __half(*stg)[16] = reinterpret_cast<__half(*)[16]>(sm->stage[warp]);
-      const int i0 = un.sub * 128 + at * 64 + q4 * 4;  // the 64-wide K step of W2, group q
+      // copy-out: lane l carries positions 4 l .. 4 l + 3 of a token row, held
+      // by warp (q = l % 4, t = l / 16) at values 4 ((l % 16) / 4) .. + 3
+      const char* src_tile = reinterpret_cast<const char*>(sm->stage[(lane & 3) + 4 * (lane >> 4)]) +
+                             8 * ((lane & 15) >> 2);
+      bool ep_ok = true;
 #pragma unroll 1
-      for (int c0 = 0; c0 < un.npad; c0 += 32) {
+      for (int c0 = 0; c0 < un.npad; c0 += 32, ++ch) {
+        // the eight tiles are free again once every warp has copied the last chunk out
+        if (ch > 0 && !warp_wait_or_abort(&sm->ep_free, (ch - 1) & 1, status, abort)) {
+          ep_ok = false;
+          break;
+        }
         uint32_t v[32];
         tmem_ld32(tbase + c0, v);
 #pragma unroll
@@ -479,15 +496,24 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           stg[is_gate ? jj : jj + 16][r16] = __float2half_rn(hv);
         }
         __syncwarp();
-        const int n = c0 + lane;
-        if (n < un.rows) {
-          const uint2* s2 = reinterpret_cast<const uint2*>(stg[lane]);
-          __half* dst = h_out + (int64_t)(un.pos0 + n) * I + i0;
+        if (lane == 0) mbar_arrive(&sm->ep_staged);
+        if (!warp_wait_or_abort(&sm->ep_staged, ch & 1, status, abort)) {
+          ep_ok = false;
+          break;
+        }
 #pragma unroll
-          for (int r = 0; r < 4; ++r) *reinterpret_cast<uint2*>(dst + 16 * r) = s2[r];
+        for (int rr = 0; rr < 32 / kDqWarps; ++rr) {
+          const int row = warp * (32 / kDqWarps) + rr, n = c0 + row;
+          if (n < un.rows) {
+            const uint2 v2 = *reinterpret_cast<const uint2*>(src_tile + row * 32);
+            *reinterpret_cast<uint2*>(h_out + (int64_t)(un.pos0 + n) * I + un.sub * 128 + 4 * lane) =
+                v2;
+          }
         }
         __syncwarp();
+        if (lane == 0) mbar_arrive(&sm->ep_free);
       }
+      if (!ep_ok) break;
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm->tmem_empty);
