@@ -593,6 +593,8 @@ __global__ void __launch_bounds__(kW2Threads, 1)
   W2Smem* sm = reinterpret_cast<W2Smem*>(base + kOffMeta);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   MOE_TL(kTlW2);
+  MOE_PROF(constexpr int poff = 16);
+  MOE_PROF(unsigned long long pacc[15] = {});
   const int S = d.I / kW2KS;   // K steps per unit (I % 128 == 0)
   const int upt = d.H / 128;   // units per plan tile
 
@@ -659,20 +661,25 @@ __global__ void __launch_bounds__(kW2Threads, 1)
     // ---- MMAs: per K step one wait, 4 MMAs (K 16 each), one commit ----
     if (lane == 0) {
       uint32_t ka = 0, it = 0;
+      MOE_PROF(const long long t_all = clock64());
       for (int u = blockIdx.x; u < n_units && !*abort; u += gridDim.x, ++it) {
         const Unit un = load_unit<false, SB>(d, pv, w, ws, u, upt);
         const uint32_t idesc = idesc_f16_f32(128, un.npad);
         const int b = it & 1;
+        MOE_PROF(long long t0 = clock64());
         if (it >= 2 && !wait_or_abort(&sm->tmem_empty[b], ((it - 2) >> 1) & 1, status, abort))
           break;
+        MOE_PROF(PROF_ADD(poff + 7, t0));
         tc_fence_after();
         bool ok = true;
         for (int ks = 0; ks < S; ++ks, ++ka) {
           const int st = ka % kW2BStages, as = ka % kW2AS;
+          MOE_PROF(t0 = clock64());
           if (!wait_or_abort(&sm->full[st], (ka / kW2BStages) & 1, status, abort)) {
             ok = false;
             break;
           }
+          MOE_PROF(PROF_ADD(poff + 4, t0); t0 = clock64());
           tc_fence_after();
           const uint32_t ta = tmem + kAOff + as * (kW2KS / 2);
 #pragma unroll
@@ -686,10 +693,12 @@ __global__ void __launch_bounds__(kW2Threads, 1)
                             (ks | c | kk) ? 1u : 0u);
           }
           tc_commit(&sm->empty[st]);
+          MOE_PROF(PROF_ADD(poff + 6, t0));
         }
         if (!ok) break;
         tc_commit(&sm->accf[b]);
       }
+      MOE_PROF(PROF_ADD(poff + 2, t_all));
       tc_commit(&sm->drain);
       const long long t0 = clock64();
       while (!mbar_try_wait(&sm->drain, 0) && clock64() - t0 < g_pf_wait_limit) {
@@ -705,10 +714,12 @@ __global__ void __launch_bounds__(kW2Threads, 1)
         const int nch = (un.npad + kBChunkRows - 1) / kBChunkRows;
         for (int ks = 0; ks < S; ++ks, ++kb) {
           const int bs = kb % kW2BStages;
+          MOE_PROF(long long t0 = clock64());
           if (!wait_or_abort(&sm->empty[bs], ((kb / kW2BStages) & 1) ^ 1, status, abort)) {
             ok = false;
             break;
           }
+          MOE_PROF(PROF_ADD(poff + 8, t0));
           mbar_expect_tx(&sm->full[bs], (uint32_t)(2 * nch * kBChunk));
           for (int c = 0; c < 2; ++c)
             for (int ch = 0; ch < nch; ++ch)
@@ -754,8 +765,10 @@ __global__ void __launch_bounds__(kW2Threads, 1)
     for (int u = blockIdx.x; u < n_units && !*abort; u += gridDim.x, ++it) {
       const Unit un = load_unit<false, SB>(d, pv, w, ws, u, upt);
       const int b = it & 1;
+      MOE_PROF(long long te = clock64());
       if (!warp_wait_or_abort(&sm->accf[b], (it >> 1) & 1, status, abort)) break;
       if (!warp_wait_or_abort(&sm->wsc_full[b], (it >> 1) & 1, status, abort)) break;
+      MOE_PROF(if (tid == kW2EpiWarp0 * 32) PROF_ADD(poff + 13, te); te = clock64());
       tc_fence_after();
       const float* wsc = sm->wsc[b];
       __half* pbase = partial + (int64_t)un.pos0 * H + un.sub * 128 + q * 32;
@@ -792,6 +805,7 @@ __global__ void __launch_bounds__(kW2Threads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm->tmem_empty[b]);
+      MOE_PROF(if (tid == kW2EpiWarp0 * 32) PROF_ADD(poff + 14, te));
     }
   } else if (warp < kDqWarps) {
     // ---- dequantise: one fragment block per warp and K step into the A stage ----
@@ -802,10 +816,12 @@ __global__ void __launch_bounds__(kW2Threads, 1)
     for (int u = blockIdx.x; u < n_units && ok && !*abort; u += gridDim.x) {
       for (int ks = 0; ks < S; ++ks, ++kd) {
         const int rs = kd % kRS, as = kd % kW2AS;
+        MOE_PROF(long long t0 = clock64());
         if (!warp_wait_or_abort(&sm->raw_full[rs], (kd / kRS) & 1, status, abort)) {
           ok = false;
           break;
         }
+        MOE_PROF(if (tid == 0) PROF_ADD(poff + 10, t0); t0 = clock64());
         const char* raw = base + kOffRaw + rs * kRawBytes;
         uint4 qv[2];
         uint32_t sc[2];
@@ -825,6 +841,7 @@ __global__ void __launch_bounds__(kW2Threads, 1)
             break;
           }
         }
+        MOE_PROF(if (tid == 0) PROF_ADD(poff + 11, t0); t0 = clock64());
         tc_fence_after();
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
@@ -843,6 +860,7 @@ __global__ void __launch_bounds__(kW2Threads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm->full[kd % kW2BStages]);
+        MOE_PROF(if (tid == 0) PROF_ADD(poff + 12, t0));
       }
     }
   }
@@ -852,6 +870,11 @@ __global__ void __launch_bounds__(kW2Threads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
+#ifdef MOE_TIMELINE
+#pragma unroll
+  for (int i = 0; i < 15; ++i)
+    if (pacc[i]) atomicAdd(&g_prof[poff + i], pacc[i]);
+#endif
 }
 
 // xg[pos] = x[perm[pos] / k_eff]: the token rows in plan order, the operand of
