@@ -48,7 +48,7 @@ struct PlanView {
   int32_t* active;    // [e_eff] experts with count > 0, ascending
   int32_t* perm;      // [M * k_eff] plan position -> pair id
   int32_t* inv;       // [M * k_eff] pair id -> plan position, -1 if dropped
-  int32_t* tiles;     // [max_tiles][4] (expert, first row, rows, 0)
+  int32_t* tiles;     // [max_tiles][4] (expert, first row, rows, first plan position)
   int32_t* chunk_hist;// [n_chunks][e_eff] scratch of the large-M plan
   int32_t* rank;      // [M * k_eff] scratch: rank of a pair inside its chunk
   float* partial;     // [n_hchunks][kDecodeMaxTokens][n_experts] scratch (128-block router)

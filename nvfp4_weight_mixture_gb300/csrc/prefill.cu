@@ -190,17 +190,28 @@ __device__ __forceinline__ uint32_t lane_scale_f16x2(uint32_t v) {
     return v;
 }
 
+// The tile entry of unit u (all zero past the last unit).  Every role walks
+// the units u = blockIdx.x, + gridDim.x, ... and loads the entry of its next
+// unit while it works on the current one, so that the entry's L2 latency
+// hides behind the unit instead of stalling the role at each unit boundary.
+__device__ __forceinline__ int4 unit_tile(const PlanView& pv, int u, int upt, int n_units) {
+  return u < n_units ? __ldcg(reinterpret_cast<const int4*>(pv.tiles) + u / upt)
+                     : make_int4(0, 0, 0, 0);
+}
+
+// Unit u from its tile entry tl = (expert, first row, rows, first plan
+// position); nxt receives the entry of the role's next unit.
 template <bool kW13, int SB>
 __device__ __forceinline__ Unit load_unit(const LayerDims& d, const PlanView& pv, Weights w,
-                                          Weights ws, int u, int upt) {
+                                          Weights ws, int u, int upt, int n_units, int4& nxt) {
   Unit un;
-  const int tile = u / upt;
-  un.sub = u - tile * upt;
-  const int4 tl = __ldcg(reinterpret_cast<const int4*>(pv.tiles) + tile);
+  const int4 tl = nxt;
+  nxt = unit_tile(pv, u + (int)gridDim.x, upt, n_units);
+  un.sub = u - (u / upt) * upt;
   un.e = tl.x;
   un.rows = tl.z;
   un.npad = (tl.z + 15) & ~15;
-  un.pos0 = __ldcg(pv.offsets + tl.x) + tl.y;
+  un.pos0 = tl.w;
   const bool sh = (un.e == d.E);
   const size_t mat_q = kW13 ? (size_t)d.I * d.H : (size_t)d.H * d.I / 2;
   un.q = sh ? ws.q : w.q + (size_t)un.e * mat_q;
@@ -259,8 +270,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // ---- raw weight producer (one lane; held back only by the test switch) ---
     if (lane == 0 && !g_pf_hold_raw) {
       uint32_t kr = 0;
+      int4 nxt = unit_tile(pv, blockIdx.x, upt, n_units);
       for (int u = blockIdx.x; u < n_units && !*abort; u += gridDim.x) {
-        const Unit un = load_unit<true, SB>(d, pv, w, ws, u, upt);
+        const Unit un = load_unit<true, SB>(d, pv, w, ws, u, upt, n_units, nxt);
         const int grp = un.sub;  // the unit's 256 weight rows are one fragment group
         bool ok = true;
         for (int ks = 0; ks < S; ++ks) {
@@ -293,9 +305,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     if (lane == 0) {
       uint32_t ka = 0, it = 0;
       MOE_PROF(const long long t_all = clock64());
+      int4 nxt = unit_tile(pv, blockIdx.x, upt, n_units);
       for (int u = blockIdx.x; u < n_units && !*abort; u += gridDim.x, ++it) {
         MOE_PROF(long long t0 = clock64());
-        const Unit un = load_unit<true, SB>(d, pv, w, ws, u, upt);
+        const Unit un = load_unit<true, SB>(d, pv, w, ws, u, upt, n_units, nxt);
         const uint32_t idesc = idesc_f16_f32(128, un.npad);
         MOE_PROF(PROF_ADD(poff + 3, t0); t0 = clock64());
         if (it > 0 && !wait_or_abort(&sm->tmem_empty, (it - 1) & 1, status, abort)) break;
@@ -346,8 +359,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     if (lane == 0) {
       uint32_t kb = 0;
       bool ok = true;
+      int4 nxt = unit_tile(pv, blockIdx.x, upt, n_units);
       for (int u = blockIdx.x; u < n_units && ok && !*abort; u += gridDim.x) {
-        const Unit un = load_unit<true, SB>(d, pv, w, ws, u, upt);
+        const Unit un = load_unit<true, SB>(d, pv, w, ws, u, upt, n_units, nxt);
         const int nch = (un.npad + kBChunkRows - 1) / kBChunkRows;
         for (int ks = 0; ks < S; ++ks, ++kb) {
           const int bs = kb % kBStages;
@@ -393,8 +407,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   } else {
     // ---- warps 0-7: dequantise, then the unit's epilogue ---------------------------
     uint32_t kd = 0, it = 0, ch = 0;  // ch: epilogue chunks so far
+    int4 nxt = unit_tile(pv, blockIdx.x, upt, n_units);
     for (int u = blockIdx.x; u < n_units && !*abort; u += gridDim.x, ++it) {
-      const Unit un = load_unit<true, SB>(d, pv, w, ws, u, upt);
+      const Unit un = load_unit<true, SB>(d, pv, w, ws, u, upt, n_units, nxt);
       bool ok = true;
       // this warp's two fragment blocks j = 2 warp + jj: rows 32 (warp % 4) + 16 jj
       // .. + 15 of A tile warp / 4
@@ -632,8 +647,9 @@ __global__ void __launch_bounds__(kW2Threads, 1)
     if (lane == 0) {
       uint32_t kr = 0;
       bool ok = true;
+      int4 nxt = unit_tile(pv, blockIdx.x, upt, n_units);
       for (int u = blockIdx.x; u < n_units && ok && !*abort; u += gridDim.x) {
-        const Unit un = load_unit<false, SB>(d, pv, w, ws, u, upt);
+        const Unit un = load_unit<false, SB>(d, pv, w, ws, u, upt, n_units, nxt);
         const int grp = un.sub >> 1, half = un.sub & 1;
         for (int ks = 0; ks < S; ++ks, ++kr) {
           const int slot = kr % kRS;
@@ -662,11 +678,13 @@ __global__ void __launch_bounds__(kW2Threads, 1)
     if (lane == 0) {
       uint32_t ka = 0, it = 0;
       MOE_PROF(const long long t_all = clock64());
+      int4 nxt = unit_tile(pv, blockIdx.x, upt, n_units);
       for (int u = blockIdx.x; u < n_units && !*abort; u += gridDim.x, ++it) {
-        const Unit un = load_unit<false, SB>(d, pv, w, ws, u, upt);
+        MOE_PROF(long long t0 = clock64());
+        const Unit un = load_unit<false, SB>(d, pv, w, ws, u, upt, n_units, nxt);
         const uint32_t idesc = idesc_f16_f32(128, un.npad);
         const int b = it & 1;
-        MOE_PROF(long long t0 = clock64());
+        MOE_PROF(PROF_ADD(poff + 3, t0); t0 = clock64());
         if (it >= 2 && !wait_or_abort(&sm->tmem_empty[b], ((it - 2) >> 1) & 1, status, abort))
           break;
         MOE_PROF(PROF_ADD(poff + 7, t0));
@@ -709,8 +727,9 @@ __global__ void __launch_bounds__(kW2Threads, 1)
     if (lane == 0) {
       uint32_t kb = 0;
       bool ok = true;
+      int4 nxt = unit_tile(pv, blockIdx.x, upt, n_units);
       for (int u = blockIdx.x; u < n_units && ok && !*abort; u += gridDim.x) {
-        const Unit un = load_unit<false, SB>(d, pv, w, ws, u, upt);
+        const Unit un = load_unit<false, SB>(d, pv, w, ws, u, upt, n_units, nxt);
         const int nch = (un.npad + kBChunkRows - 1) / kBChunkRows;
         for (int ks = 0; ks < S; ++ks, ++kb) {
           const int bs = kb % kW2BStages;
@@ -734,8 +753,9 @@ __global__ void __launch_bounds__(kW2Threads, 1)
     // ---- g2 x combine weight of each row, one unit ahead (buffer it & 1 is
     // free once the epilogue of unit it - 2 is done) ----
     uint32_t it = 0;
+    int4 nxt = unit_tile(pv, blockIdx.x, upt, n_units);
     for (int u = blockIdx.x; u < n_units && !*abort; u += gridDim.x, ++it) {
-      const Unit un = load_unit<false, SB>(d, pv, w, ws, u, upt);
+      const Unit un = load_unit<false, SB>(d, pv, w, ws, u, upt, n_units, nxt);
       if (it >= 2 &&
           !warp_wait_or_abort(&sm->tmem_empty[it & 1], ((it - 2) >> 1) & 1, status, abort))
         break;
@@ -762,8 +782,9 @@ __global__ void __launch_bounds__(kW2Threads, 1)
     const int H = d.H;
     float(*stg)[32] = reinterpret_cast<float(*)[32]>(sm->stage[warp - kW2EpiWarp0]);
     uint32_t it = 0;
+    int4 nxt = unit_tile(pv, blockIdx.x, upt, n_units);
     for (int u = blockIdx.x; u < n_units && !*abort; u += gridDim.x, ++it) {
-      const Unit un = load_unit<false, SB>(d, pv, w, ws, u, upt);
+      const Unit un = load_unit<false, SB>(d, pv, w, ws, u, upt, n_units, nxt);
       const int b = it & 1;
       MOE_PROF(long long te = clock64());
       if (!warp_wait_or_abort(&sm->accf[b], (it >> 1) & 1, status, abort)) break;

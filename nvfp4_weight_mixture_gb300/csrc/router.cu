@@ -64,7 +64,7 @@ __device__ void plan_tiny(const LayerDims& d, int M, const int* src, const PlanV
       if (before < kDtabInts - 4) ent[4 + before] = lane;
       if (before == 0) {
         pv.active[a] = e;
-        reinterpret_cast<int4*>(pv.tiles)[a] = make_int4(e, 0, total, 0);
+        reinterpret_cast<int4*>(pv.tiles)[a] = make_int4(e, 0, total, pos);
         reinterpret_cast<int4*>(ent)[0] = make_int4(e, pos, total, -1);
         for (int r = total; r < kDtabInts - 4; ++r) ent[4 + r] = -1;
       }
@@ -251,7 +251,8 @@ __device__ void plan_small_block(const LayerDims& d, int M, const int* src, cons
         s_acnt[sa] = c[i];
         pv.active[sa] = e;
         for (int r0 = 0; r0 < c[i]; r0 += kTileRows, ++st)
-          reinterpret_cast<int4*>(pv.tiles)[st] = make_int4(e, r0, min(kTileRows, c[i] - r0), 0);
+          reinterpret_cast<int4*>(pv.tiles)[st] =
+              make_int4(e, r0, min(kTileRows, c[i] - r0), so + r0);
         ++sa;
       }
       so += c[i];
@@ -330,7 +331,8 @@ __device__ void plan_small_block(const LayerDims& d, int M, const int* src, cons
       const int nt_e = (c + kTileRows - 1) / kTileRows;
       for (int r = 0; r < nt_e; ++r)
         reinterpret_cast<int4*>(pv.tiles)[t0 + r] =
-            make_int4(e, r * kTileRows, min(kTileRows, c - r * kTileRows), 0);
+            make_int4(e, r * kTileRows, min(kTileRows, c - r * kTileRows),
+                      s_pos1[p] + r * kTileRows);
       if (higher == 0) {  // the highest active expert knows the totals
         s_na = a + 1;
         s_nt = t0 + nt_e;
@@ -359,7 +361,7 @@ __device__ void plan_small_block(const LayerDims& d, int M, const int* src, cons
       s_acnt[sa] = c;
       pv.active[sa] = e;
       for (int r0 = 0; r0 < c; r0 += kTileRows, ++st)
-        reinterpret_cast<int4*>(pv.tiles)[st] = make_int4(e, r0, min(kTileRows, c - r0), 0);
+        reinterpret_cast<int4*>(pv.tiles)[st] = make_int4(e, r0, min(kTileRows, c - r0), j + r0);
       ++sa;
     }
     if (tid == 0) {
@@ -822,6 +824,7 @@ __global__ void __launch_bounds__(1024) plan_scan_kernel(LayerDims d, int M, int
                                                          PlanView pv) {
   __shared__ int s_cnt[kMaxEEff];
   __shared__ int s_tb[kMaxEEff];
+  __shared__ int s_ob[kMaxEEff];
   __shared__ int s_tot[3];
   MOE_TL(kTlPlan);
   const int tid = threadIdx.x, ne = d.e_eff;
@@ -879,6 +882,7 @@ __global__ void __launch_bounds__(1024) plan_scan_kernel(LayerDims d, int M, int
     for (int i = b; i < end; ++i) {
       const int c = s_cnt[i];
       s_tb[i] = ti;
+      s_ob[i] = ci;
       pv.counts[i] = c;
       pv.offsets[i] = ci;
       if (c > 0) pv.active[ai] = i;
@@ -898,10 +902,10 @@ __global__ void __launch_bounds__(1024) plan_scan_kernel(LayerDims d, int M, int
     pv.hdr->n_tiles = s_tot[2];
   }
   for (int e = tid; e < ne; e += 1024) {
-    const int c = s_cnt[e];
+    const int c = s_cnt[e], o = s_ob[e];
     int t = s_tb[e];
     for (int r0 = 0; r0 < c; r0 += kTileRows, ++t)
-      reinterpret_cast<int4*>(pv.tiles)[t] = make_int4(e, r0, min(kTileRows, c - r0), 0);
+      reinterpret_cast<int4*>(pv.tiles)[t] = make_int4(e, r0, min(kTileRows, c - r0), o + r0);
   }
 }
 

@@ -204,7 +204,14 @@ def decode_plan(buf, M, k_eff, e_eff, E, H):
     n_valid, n_active, n_tiles = int(hdr[5]), int(hdr[3]), int(hdr[4])
     return dict(hdr=hdr, ids=ids, w=w, counts=counts, offsets=offsets,
                 active=active[:n_active], perm=perm[:n_valid], inv=inv,
-                tiles=tiles[:n_tiles, :3], dtab=dtab)
+                tiles=tiles[:n_tiles, :3], tile_pos=tiles[:n_tiles, 3], dtab=dtab)
+
+
+def expected_tile_pos(ref):
+    """The first plan position of each tile of an oracle plan: its expert's
+    offset plus the tile's first row (the fourth field of a tile entry)."""
+    t = np.asarray(ref["tiles"]).reshape(-1, 3)
+    return (np.asarray(ref["offsets"])[t[:, 0]] + t[:, 1]).astype(np.int32)
 
 
 def expected_work_table(ref, M, k_eff, e_eff):

@@ -25,7 +25,7 @@ import torch
 
 import oracle
 from harness import (MAX_ABS_TOL, REL_L2_TOL, ROUTER_GAP, ROUTER_W_TOL, TILE_ROWS, Case,
-                     compare, expected_work_table)
+                     compare, expected_tile_pos, expected_work_table)
 from nvfp4_weight_mixture_gb300 import moe, synth
 
 pytestmark = pytest.mark.gpu
@@ -87,6 +87,7 @@ def test_gpu_routed_decode_vs_oracle(router_mode, name, wl):
     np.testing.assert_array_equal(got["ids"], ids_eff.reshape(-1))
     for key in ("counts", "offsets", "perm", "inv", "tiles"):
         np.testing.assert_array_equal(got[key], ref[key], err_msg=key)
+    np.testing.assert_array_equal(got["tile_pos"], expected_tile_pos(ref))
     np.testing.assert_array_equal(got["active"], np.nonzero(ref["counts"])[0])
     assert int(got["hdr"][0]) == wl.M and int(got["hdr"][1]) == k_eff
     assert int(got["hdr"][3]) == len(np.nonzero(ref["counts"])[0])
@@ -122,7 +123,7 @@ def test_ticket_router_matches_cluster_router(M):
             moe.set_small_router(False)
     np.testing.assert_array_equal(out[False][0], out[True][0])
     assert np.max(np.abs(out[False][1] - out[True][1])) <= ROUTER_W_TOL
-    for key in ("counts", "offsets", "perm", "inv", "tiles", "active", "dtab"):
+    for key in ("counts", "offsets", "perm", "inv", "tiles", "tile_pos", "active", "dtab"):
         np.testing.assert_array_equal(out[False][2][key], out[True][2][key], err_msg=key)
 
 

@@ -12,7 +12,7 @@ import torch
 
 import oracle
 from harness import (DECODE_MAX_TOKENS, MAX_ABS_TOL, REL_L2_TOL, ROUTER_GAP, ROUTER_W_TOL,
-                     TILE_ROWS, Case, compare, expected_work_table)
+                     TILE_ROWS, Case, compare, expected_tile_pos, expected_work_table)
 from nvfp4_weight_mixture_gb300 import moe, synth
 
 pytestmark = pytest.mark.gpu
@@ -63,6 +63,7 @@ def _check_plan(case, ids):
     np.testing.assert_array_equal(got["perm"], ref["perm"])
     np.testing.assert_array_equal(got["inv"], ref["inv"])
     np.testing.assert_array_equal(got["tiles"], ref["tiles"])
+    np.testing.assert_array_equal(got["tile_pos"], expected_tile_pos(ref))
     np.testing.assert_array_equal(got["active"], np.nonzero(ref["counts"])[0])
     assert int(got["hdr"][0]) == wl.M and int(got["hdr"][1]) == k_eff
     if wl.M <= DECODE_MAX_TOKENS:
