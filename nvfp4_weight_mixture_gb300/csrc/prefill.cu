@@ -70,9 +70,12 @@ constexpr int kRawQ = 16 * 512;           // raw q bytes per K step (16 fragment
 // + their scales: 16 x 64 bytes raw E4M3, 16 x 128 bytes prepared FP16
 constexpr int kRawBytes = kRawQ + 16 * 128;
 // Warp roles: 0-7 dequantise and run the epilogue, 8 fills the token-row
-// operand, 12 issues the MMAs (and owns tensor memory), 13 streams raw weights.
+// operand, 9-11 write the staged h rows out, 12 issues the MMAs (and owns
+// tensor memory), 13 streams raw weights.
 constexpr int kDqWarps = 8;
 constexpr int kBWarp0 = 8;
+constexpr int kOutWarp0 = 9;
+constexpr int kOutWarps = 3;
 constexpr int kMmaWarp = 12;
 constexpr int kRawWarp = 13;
 constexpr int kGemmThreads = 14 * 32;
@@ -90,6 +93,8 @@ static_assert(kBStage % 1024 == 0, "B stages must stay 1024-byte aligned for the
 static_assert(kBStages % kAS == 0 && kBStages >= 2 * kAS,
               "one barrier per K step serves both rings: B ring a multiple of, and at least twice, the A ring");
 
+constexpr int kHStageHalfs = kTileRows * 16 + 16;
+
 struct GemmSmem {
   uint64_t raw_full[kRS], raw_empty[kRS];
   // K step k: full[k % kBStages] completes when A stage k % kAS is in tensor
@@ -98,15 +103,17 @@ struct GemmSmem {
   // thread commits K step k to empty[k % kBStages], which frees both.
   uint64_t full[kBStages], empty[kBStages];
   uint64_t accf, tmem_empty, drain;
-  // W13 epilogue chunks: every dequantising warp has staged its tile
-  // (ep_staged) / has copied its token rows out (ep_free)
+  // W13 epilogue, once per unit: every dequantising warp has staged its tile
+  // of the unit's h (ep_staged) / the output warps have written the unit's
+  // token rows out (ep_free)
   uint64_t ep_staged, ep_free;
   uint32_t tmem;
   int abort;
   int n_units;
-  // epilogue staging, 1 KiB per warp (+16 bytes, so that the eight warps'
-  // tiles start on different banks): h values [32 tokens][16 i] (FP16)
-  __align__(16) float stage[kDqWarps][260];
+  // epilogue staging of a whole unit: per dequantising warp h values
+  // [kTileRows tokens][16 i] (FP16); the 32-byte pad after each tile makes
+  // the output warps' 8-byte reads of one half-warp hit 32 different banks
+  __align__(16) __half hstage[kDqWarps][kHStageHalfs];
 };
 
 constexpr size_t gemm_smem_bytes() {
@@ -249,7 +256,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     mbar_init(&sm->accf, 1);
     mbar_init(&sm->tmem_empty, kDqWarps);
     mbar_init(&sm->ep_staged, kDqWarps);
-    mbar_init(&sm->ep_free, kDqWarps);
+    mbar_init(&sm->ep_free, kOutWarps);
     mbar_init(&sm->drain, 1);
     sm->abort = 0;
     fence_mbar_init();
@@ -385,28 +392,31 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       for (uint32_t k = (kb > (uint32_t)kBStages ? kb - kBStages : 0); k < kb; ++k)
         drain_wait(&sm->full[k % kBStages], (k / kBStages) & 1);
     }
-  } else if (warp > kBWarp0) {
-    // spare warps (timeline build: two of them stamp when each raw and B stage
-    // lands, following the rings' phases without taking part in them)
-#ifdef MOE_TIMELINE
-    if (blockIdx.x == 0 && lane == 0 && (warp == 9 || warp == 10)) {
-      const int n_mine = (n_units - 1 - (int)blockIdx.x) / (int)gridDim.x + 1;
-      const int nst = warp == 9 ? kRS : kBStages;
-      uint64_t* bars = warp == 9 ? sm->raw_full : sm->full;
-      for (int k = 0; k < n_mine * S && k < 2048 && !*abort; ++k) {
-        const long long t0 = clock64();
-        bool seen = false;
-        while (!(seen = mbar_try_wait(&bars[k % nst], (k / nst) & 1)) && !*abort &&
-               clock64() - t0 < (kWaitTimeoutCycles >> 4)) {
-        }
-        if (!seen) break;
-        g_dbg[(warp == 9 ? 8 : 9) * 2048 + k] = clock64();
-      }
+  } else if (warp >= kOutWarp0 && warp < kOutWarp0 + kOutWarps) {
+    // ---- output warps: write each unit's staged h rows out (whole 256-byte
+    // token rows, one 8-byte store per lane); lane l carries positions
+    // 4 l .. 4 l + 3 of a row, held by dequantising warp (q = l % 4,
+    // t = l / 16) at values 4 ((l % 16) / 4) .. + 3 ----
+    const int I = d.I;
+    const char* src_tile = reinterpret_cast<const char*>(sm->hstage[(lane & 3) + 4 * (lane >> 4)]) +
+                           8 * ((lane & 15) >> 2);
+    uint32_t it = 0;
+    int4 nxt = unit_tile(pv, blockIdx.x, upt, n_units);
+    for (int u = blockIdx.x; u < n_units && !*abort; u += gridDim.x, ++it) {
+      const Unit un = load_unit<true, SB>(d, pv, w, ws, u, upt, n_units, nxt);
+      MOE_PROF(long long t0 = clock64());
+      if (!warp_wait_or_abort(&sm->ep_staged, it & 1, status, abort)) break;
+      MOE_PROF(if (lane == 0 && warp == kOutWarp0) PROF_ADD(poff + 5, t0));
+      __half* hrow = h_out + (int64_t)un.pos0 * I + un.sub * 128 + 4 * lane;
+      for (int n = warp - kOutWarp0; n < un.rows; n += kOutWarps)
+        *reinterpret_cast<uint2*>(hrow + (int64_t)n * I) =
+            *reinterpret_cast<const uint2*>(src_tile + n * 32);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm->ep_free);
     }
-#endif
   } else {
     // ---- warps 0-7: dequantise, then the unit's epilogue ---------------------------
-    uint32_t kd = 0, it = 0, ch = 0;  // ch: epilogue chunks so far
+    uint32_t kd = 0, it = 0;
     int4 nxt = unit_tile(pv, blockIdx.x, upt, n_units);
     for (int u = blockIdx.x; u < n_units && !*abort; u += gridDim.x, ++it) {
       const Unit un = load_unit<true, SB>(d, pv, w, ws, u, upt, n_units, nxt);
@@ -471,36 +481,32 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       MOE_PROF(long long te = clock64());
       if (!warp_wait_or_abort(&sm->accf, it & 1, status, abort)) break;
       if (tid == 0) MOE_DBG(7, 2 * it);
+      // the staging tiles are free once the output warps have written unit
+      // it - 1 out (long before, in the steady state: a unit's K loop)
+      if (it > 0 && !warp_wait_or_abort(&sm->ep_free, (it - 1) & 1, status, abort)) break;
       MOE_PROF(if (tid == 0) PROF_ADD(poff + 13, te); te = clock64());
       tc_fence_after();
       const uint32_t tbase = tmem + ((uint32_t)(q4 * 32) << 16) + at * kTileRows;
       // Lane r < 16 of warp q holds gate row (16q + r) and lane r + 16 the
       // matching up row, for 32 token columns per load.  One exchange per
       // pair of columns gives each lane 16 (G, U) pairs: gate lanes take
-      // columns 0-15, up lanes 16-31.  h goes through a per-warp staging
-      // tile: a token row's 16 values of warp (q, t) belong at positions
-      // 64 t + 16 r + 4 q + (0..3), r = 0..3, of the unit's 128 h values
-      // (the K order of the W2 operand).  Once the eight warps have staged a
-      // chunk, each writes four whole token rows (256 bytes, one 8-byte store
-      // per lane) gathered from the eight tiles.
-      const int I = d.I;
+      // columns 0-15, up lanes 16-31.  A token row's 16 values of warp (q, t)
+      // belong at positions 64 t + 16 r + 4 q + (0..3), r = 0..3, of the
+      // unit's 128 h values (the K order of the W2 operand).  Tensor memory
+      // is released right after the last read, so that the next unit's MMAs
+      // need not wait for the SwiGLU of the last chunk or the row writes.
       const int r16 = lane & 15;
       const bool is_gate = lane < 16;
-      __half(*stg)[16] = reinterpret_cast<__half(*)[16]>(sm->stage[warp]);
-      // copy-out: lane l carries positions 4 l .. 4 l + 3 of a token row, held
-      // by warp (q = l % 4, t = l / 16) at values 4 ((l % 16) / 4) .. + 3
-      const char* src_tile = reinterpret_cast<const char*>(sm->stage[(lane & 3) + 4 * (lane >> 4)]) +
-                             8 * ((lane & 15) >> 2);
-      bool ep_ok = true;
+      __half(*stg)[16] = reinterpret_cast<__half(*)[16]>(sm->hstage[warp]);
 #pragma unroll 1
-      for (int c0 = 0; c0 < un.npad; c0 += 32, ++ch) {
-        // the eight tiles are free again once every warp has copied the last chunk out
-        if (ch > 0 && !warp_wait_or_abort(&sm->ep_free, (ch - 1) & 1, status, abort)) {
-          ep_ok = false;
-          break;
-        }
+      for (int c0 = 0; c0 < un.npad; c0 += 32) {
         uint32_t v[32];
         tmem_ld32(tbase + c0, v);
+        if (c0 + 32 >= un.npad) {  // the unit's accumulators are read
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sm->tmem_empty);
+        }
 #pragma unroll
         for (int jj = 0; jj < 16; ++jj) {
           const float lo = __uint_as_float(v[jj]), hi = __uint_as_float(v[jj + 16]);
@@ -508,30 +514,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           const float G = (is_gate ? lo : recv) * un.g;
           const float U = (is_gate ? recv : hi) * un.g;
           const float hv = __fdividef(G, 1.f + __expf(-G)) * U;
-          stg[is_gate ? jj : jj + 16][r16] = __float2half_rn(hv);
+          stg[c0 + (is_gate ? jj : jj + 16)][r16] = __float2half_rn(hv);
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sm->ep_staged);
-        if (!warp_wait_or_abort(&sm->ep_staged, ch & 1, status, abort)) {
-          ep_ok = false;
-          break;
-        }
-#pragma unroll
-        for (int rr = 0; rr < 32 / kDqWarps; ++rr) {
-          const int row = warp * (32 / kDqWarps) + rr, n = c0 + row;
-          if (n < un.rows) {
-            const uint2 v2 = *reinterpret_cast<const uint2*>(src_tile + row * 32);
-            *reinterpret_cast<uint2*>(h_out + (int64_t)(un.pos0 + n) * I + un.sub * 128 + 4 * lane) =
-                v2;
-          }
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sm->ep_free);
       }
-      if (!ep_ok) break;
-      tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&sm->tmem_empty);
+      if (lane == 0) mbar_arrive(&sm->ep_staged);
       if (tid == 0) MOE_DBG(7, 2 * it + 1);
       MOE_PROF(if (tid == 0) PROF_ADD(poff + 14, te));
     }
@@ -566,9 +553,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 //   warp 19      g2 x combine weight of each row, one unit ahead.
 // ---------------------------------------------------------------------------
 constexpr int kW2Threads = 20 * 32;
-constexpr int kW2KS = 2 * kBK;     // K per W2 step: two fragment segments
-constexpr int kW2AS = 2;          // A stages of one tile and one step
-constexpr int kW2BStages = 2;     // B stages of one step (two 24 KiB halves each)
+constexpr int kW2Seg = 2;              // 64-element fragment segments per W2 K step
+constexpr int kW2KS = kW2Seg * kBK;    // K per W2 step
+constexpr int kW2AS = 4 / kW2Seg;      // A stages (128 tensor-memory columns in all)
+constexpr int kW2BStages = kW2AS;      // B stages of one step (kW2Seg 24 KiB halves each)
 constexpr int kW2EpiWarp0 = 8;
 constexpr int kW2MmaWarp = 16;
 constexpr int kW2RawWarp = 17;
@@ -576,13 +564,16 @@ constexpr int kW2BWarp = 18;
 constexpr int kW2ScaleWarp = 19;
 constexpr int kW2RawQ = 8 * 512;  // raw q bytes per segment (8 fragment blocks)
 constexpr int kW2RawS = 8 * 64;   // their raw scale bytes (x 2 when prepared)
-static_assert(2 * kW2RawQ <= kRawQ && 2 * 2 * kW2RawS <= kRawBytes - kRawQ, "W2 raw slot");
+// raw slot of one K step: the segments' q, then their scales (room for FP16)
+constexpr int kW2RawSlot = kW2Seg * (kW2RawQ + 2 * kW2RawS);
+constexpr int kW2RS = kRS * kRawBytes / kW2RawSlot;  // raw stages in the raw region
+static_assert(kW2RawSlot % 16 == 0 && kW2RS * kW2RawSlot <= kRS * kRawBytes, "W2 raw slot");
 static_assert(kAOff + kW2AS * (kW2KS / 2) <= kTmemCols, "W2 tensor memory over-committed");
 static_assert(kW2BStages == kW2AS, "one barrier per K step serves both rings");
-static_assert(kW2BStages * 2 * kBStage <= kBStages * kBStage, "W2 B ring inside the B region");
+static_assert(kW2BStages * kW2Seg * kBStage <= kBStages * kBStage, "W2 B ring inside the B region");
 
 struct W2Smem {
-  uint64_t raw_full[kRS], raw_empty[kRS];
+  uint64_t raw_full[kW2RS], raw_empty[kW2RS];
   uint64_t full[kW2BStages], empty[kW2BStages];
   // per accumulator buffer b: accf[b] completes when a unit's MMAs into b are
   // done, tmem_empty[b] when its epilogue has read b, wsc_full[b] when the
@@ -611,10 +602,11 @@ __global__ void __launch_bounds__(kW2Threads, 1)
   MOE_PROF(constexpr int poff = 16);
   MOE_PROF(unsigned long long pacc[15] = {});
   const int S = d.I / kW2KS;   // K steps per unit (I % 128 == 0)
+  static_assert(128 % kW2KS == 0, "W2 K step divides 128");
   const int upt = d.H / 128;   // units per plan tile
 
   if (tid == 0) {
-    for (int i = 0; i < kRS; ++i) {
+    for (int i = 0; i < kW2RS; ++i) {
       mbar_init(&sm->raw_full[i], 1);
       mbar_init(&sm->raw_empty[i], kDqWarps);
     }
@@ -652,26 +644,26 @@ __global__ void __launch_bounds__(kW2Threads, 1)
         const Unit un = load_unit<false, SB>(d, pv, w, ws, u, upt, n_units, nxt);
         const int grp = un.sub >> 1, half = un.sub & 1;
         for (int ks = 0; ks < S; ++ks, ++kr) {
-          const int slot = kr % kRS;
-          if (!wait_or_abort(&sm->raw_empty[slot], ((kr / kRS) & 1) ^ 1, status, abort)) {
+          const int slot = kr % kW2RS;
+          if (!wait_or_abort(&sm->raw_empty[slot], ((kr / kW2RS) & 1) ^ 1, status, abort)) {
             ok = false;
             break;
           }
-          char* dst = base + kOffRaw + slot * kRawBytes;
-          mbar_expect_tx(&sm->raw_full[slot], 2 * (kW2RawQ + kW2RawS * SB));
-          // segments 2 ks and 2 ks + 1: q of segment c at c * kW2RawQ, s at
-          // kRawQ + c * kW2RawS
+          char* dst = base + kOffRaw + slot * kW2RawSlot;
+          mbar_expect_tx(&sm->raw_full[slot], kW2Seg * (kW2RawQ + kW2RawS * SB));
+          // segments kW2Seg ks + c: q of segment c at c * kW2RawQ, s at
+          // kW2Seg * kW2RawQ + c * kW2RawS
 #pragma unroll
-          for (int c = 0; c < 2; ++c) {
-            const size_t blk = ((size_t)grp * (2 * S) + 2 * ks + c) * 16 + 8 * half;
+          for (int c = 0; c < kW2Seg; ++c) {
+            const size_t blk = ((size_t)grp * (kW2Seg * S) + kW2Seg * ks + c) * 16 + 8 * half;
             bulk_g2s(dst + c * kW2RawQ, un.q + blk * 512, kW2RawQ, &sm->raw_full[slot]);
-            bulk_g2s(dst + kRawQ + c * kW2RawS * SB, un.s + blk * 64 * SB, kW2RawS * SB,
-                     &sm->raw_full[slot]);
+            bulk_g2s(dst + kW2Seg * kW2RawQ + c * kW2RawS * SB, un.s + blk * 64 * SB,
+                     kW2RawS * SB, &sm->raw_full[slot]);
           }
         }
       }
-      for (uint32_t k = (kr > (uint32_t)kRS ? kr - kRS : 0); k < kr; ++k)
-        wait_or_abort(&sm->raw_full[k % kRS], (k / kRS) & 1, status, abort);
+      for (uint32_t k = (kr > (uint32_t)kW2RS ? kr - kW2RS : 0); k < kr; ++k)
+        wait_or_abort(&sm->raw_full[k % kW2RS], (k / kW2RS) & 1, status, abort);
     }
   } else if (warp == kW2MmaWarp) {
     // ---- MMAs: per K step one wait, 4 MMAs (K 16 each), one commit ----
@@ -701,10 +693,10 @@ __global__ void __launch_bounds__(kW2Threads, 1)
           tc_fence_after();
           const uint32_t ta = tmem + kAOff + as * (kW2KS / 2);
 #pragma unroll
-          for (int c = 0; c < 2; ++c) {
+          for (int c = 0; c < kW2Seg; ++c) {
             // segment c: A columns [32 c, 32 c + 32) of the stage, B half c
             const uint64_t db =
-                sdesc_sw128(smem_u32(base + kOffB + (st * 2 + c) * kBStage));
+                sdesc_sw128(smem_u32(base + kOffB + (st * kW2Seg + c) * kBStage));
 #pragma unroll
             for (int kk = 0; kk < kBK / 16; ++kk)
               tc_mma_f16_ts(tmem + b * kTileRows, ta + 32 * c + 8 * kk, db + 2 * kk, idesc,
@@ -739,10 +731,10 @@ __global__ void __launch_bounds__(kW2Threads, 1)
             break;
           }
           MOE_PROF(PROF_ADD(poff + 8, t0));
-          mbar_expect_tx(&sm->full[bs], (uint32_t)(2 * nch * kBChunk));
-          for (int c = 0; c < 2; ++c)
+          mbar_expect_tx(&sm->full[bs], (uint32_t)(kW2Seg * nch * kBChunk));
+          for (int c = 0; c < kW2Seg; ++c)
             for (int ch = 0; ch < nch; ++ch)
-              tma_load_2d(base + kOffB + (bs * 2 + c) * kBStage + ch * kBChunk, &bmap,
+              tma_load_2d(base + kOffB + (bs * kW2Seg + c) * kBStage + ch * kBChunk, &bmap,
                           ks * kW2KS + c * kBK, un.pos0 + ch * kBChunkRows, &sm->full[bs]);
         }
       }
@@ -836,20 +828,20 @@ __global__ void __launch_bounds__(kW2Threads, 1)
     bool ok = true;
     for (int u = blockIdx.x; u < n_units && ok && !*abort; u += gridDim.x) {
       for (int ks = 0; ks < S; ++ks, ++kd) {
-        const int rs = kd % kRS, as = kd % kW2AS;
+        const int rs = kd % kW2RS, as = kd % kW2AS;
         MOE_PROF(long long t0 = clock64());
-        if (!warp_wait_or_abort(&sm->raw_full[rs], (kd / kRS) & 1, status, abort)) {
+        if (!warp_wait_or_abort(&sm->raw_full[rs], (kd / kW2RS) & 1, status, abort)) {
           ok = false;
           break;
         }
         MOE_PROF(if (tid == 0) PROF_ADD(poff + 10, t0); t0 = clock64());
-        const char* raw = base + kOffRaw + rs * kRawBytes;
-        uint4 qv[2];
-        uint32_t sc[2];
+        const char* raw = base + kOffRaw + rs * kW2RawSlot;
+        uint4 qv[kW2Seg];
+        uint32_t sc[kW2Seg];
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
+        for (int c = 0; c < kW2Seg; ++c) {
           qv[c] = *reinterpret_cast<const uint4*>(raw + c * kW2RawQ + jl * 512 + lane * 16);
-          sc[c] = lane_scale_word<SB>(raw + kRawQ + (c * kW2RawS + jl * 64 + lane * 2) * SB);
+          sc[c] = lane_scale_word<SB>(raw + kW2Seg * kW2RawQ + (c * kW2RawS + jl * 64 + lane * 2) * SB);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm->raw_empty[rs]);  // the stage is in registers
@@ -865,7 +857,7 @@ __global__ void __launch_bounds__(kW2Threads, 1)
         MOE_PROF(if (tid == 0) PROF_ADD(poff + 11, t0); t0 = clock64());
         tc_fence_after();
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
+        for (int c = 0; c < kW2Seg; ++c) {
           const uint32_t f = lane_scale_f16x2<SB>(sc[c]);
           const uint32_t sg = __byte_perm(f, f, 0x1010), sg8 = __byte_perm(f, f, 0x3232);
           uint32_t x[4], y[4], z[4], w4[4];
