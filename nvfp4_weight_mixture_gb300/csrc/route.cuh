@@ -68,6 +68,98 @@ __device__ __forceinline__ void warp_topk(const float* row, int E, int k, int* o
   *out_l = my_l;
 }
 
+// The same selection for throughput (one warp per row, many rows): every
+// element of the top k is at least T, the k-th largest of the 32 lane maxima
+// counted with multiplicity (those k maxima are k distinct elements).  The
+// elements >= T, at least k of them and usually few more, are gathered one
+// per lane through `slot` (32 entries of this warp), so that the k rounds
+// reduce single values instead of selecting over 16 keys per lane.  More than
+// 32 such elements (heavy ties) take the rounds of warp_topk.  Lane j < k
+// receives the same slot j as from warp_topk.
+__device__ __forceinline__ void warp_topk_gathered(const float* row, int E, int k,
+                                                   uint32_t (*slot)[2], int* out_id,
+                                                   float* out_l) {
+  const int lane = threadIdx.x & 31;
+  uint32_t v[16];  // key 0 = absent (below every finite or infinite logit)
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const int e = lane + 32 * i;
+    v[i] = (e < E) ? f2key(__ldcg(row + e)) : 0u;
+  }
+  uint32_t lm = v[0];
+#pragma unroll
+  for (int i = 1; i < 16; ++i) lm = max(lm, v[i]);
+  // T: the k-th largest lane maximum (lanes holding the round's maximum all
+  // leave together; their number counts towards k)
+  uint32_t rest = lm, T = 0u;
+  for (int seen = 0; seen < k;) {
+    const uint32_t gm = __reduce_max_sync(0xffffffffu, rest);
+    seen += __popc(__ballot_sync(0xffffffffu, rest == gm));
+    T = gm;
+    if (rest == gm) rest = 0u;
+  }
+  const uint32_t Tq = max(T, 1u);
+  int c = 0;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) c += (int)(v[i] >= Tq);
+  const int C = (int)__reduce_add_sync(0xffffffffu, (uint32_t)c);
+  int my_id = -1;
+  float my_l = -INFINITY;
+  if (C <= 32) {
+    int off = c;  // exclusive prefix of the lanes' counts
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(0xffffffffu, off, o);
+      if (lane >= o) off += n;
+    }
+    off -= c;
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      if (v[i] >= Tq) {
+        slot[off][0] = v[i];
+        slot[off][1] = (uint32_t)(lane + 32 * i);
+        ++off;
+      }
+    __syncwarp();
+    uint32_t key = lane < C ? slot[lane][0] : 0u;
+    const uint32_t idx = lane < C ? slot[lane][1] : 0xffffffffu;
+    __syncwarp();
+    for (int j = 0; j < k; ++j) {
+      const uint32_t gm = __reduce_max_sync(0xffffffffu, key);
+      const uint32_t gi = __reduce_min_sync(0xffffffffu, key == gm ? idx : 0xffffffffu);
+      if (idx == gi) key = 0u;
+      if (lane == j) {
+        my_id = (int)gi;
+        my_l = key2f(gm);
+      }
+    }
+  } else {
+    for (int j = 0; j < k; ++j) {
+      uint32_t m8[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) m8[i] = max(v[i], v[i + 8]);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) m8[i] = max(m8[i], m8[i + 4]);
+      const uint32_t l2 = max(max(m8[0], m8[2]), max(m8[1], m8[3]));
+      const uint32_t gm = __reduce_max_sync(0xffffffffu, l2);
+      uint32_t li = 0xffffffffu;
+#pragma unroll
+      for (int i = 15; i >= 0; --i)
+        if (v[i] == gm) li = (uint32_t)(lane + 32 * i);
+      const uint32_t gi = __reduce_min_sync(0xffffffffu, li);
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+        if ((uint32_t)(lane + 32 * i) == gi) v[i] = 0u;
+      if (lane == j) {
+        my_id = (int)gi;
+        my_l = key2f(gm);
+      }
+    }
+  }
+  *out_id = my_id;
+  *out_l = my_l;
+}
+
 // softmax of the k selected logits held by lanes 0..k-1 (lane 0 holds the max)
 __device__ __forceinline__ float warp_topk_weight(float my_l, int k) {
   const int lane = threadIdx.x & 31;

@@ -831,6 +831,17 @@ __global__ void __launch_bounds__(1024) plan_scan_kernel(LayerDims d, int M, int
   for (int e = tid; e < ne; e += 1024) {
     int r = 0;
     int c = 0;
+    // loads in groups of 16, then 8: one dependent round trip per group
+    for (; c + 16 <= n_chunks; c += 16) {
+      int h[16];
+#pragma unroll
+      for (int u = 0; u < 16; ++u) h[u] = pv.chunk_hist[(int64_t)(c + u) * ne + e];
+#pragma unroll
+      for (int u = 0; u < 16; ++u) {
+        pv.chunk_hist[(int64_t)(c + u) * ne + e] = r;
+        r += h[u];
+      }
+    }
     for (; c + 8 <= n_chunks; c += 8) {
       int h[8];
 #pragma unroll
@@ -1065,13 +1076,14 @@ __global__ void __launch_bounds__(256) router_topk_kernel(LayerDims d, int M0, i
                                                           const __half* __restrict__ wg,
                                                           int32_t* ids_user, float* w_user,
                                                           PlanView pv) {
+  __shared__ uint32_t s_slot[8][32][2];  // each warp's gathered candidates
   MOE_TL(kTlPlan);
   const int r = blockIdx.x * 8 + (threadIdx.x >> 5);
   if (r >= Mc) return;
   const int t = M0 + r;
   int id;
   float l;
-  warp_topk<true>(logits + (size_t)r * d.E, d.E, d.k, &id, &l);
+  warp_topk_gathered(logits + (size_t)r * d.E, d.E, d.k, s_slot[threadIdx.x >> 5], &id, &l);
   const float w = warp_topk_weight(l, d.k);
   const float gamma = d.shared ? warp_gate(x + (int64_t)t * d.H, wg, d.H) : 0.f;
   store_route(d, t, id, w, gamma, ids_user, w_user, pv);

@@ -131,6 +131,34 @@ def test_router_tensor_core_shapes(M, H, E, k):
     assert int(case.layer.status.item()) == 0
 
 
+def test_router_tensor_core_ties():
+    """Exact ties in the tcgen05 router's top-k (M >= 128).  Experts 2j and
+    2j + 1 share their router column, so every logit appears twice and the
+    lower id must come first (candidates gathered one per lane).  Tokens
+    0..63 are zero rows: all 512 logits tie, the top-k is experts 0..k-1
+    with equal weights (more than 32 candidates: the general rounds)."""
+    wl = synth.custom("rt_ties", 256, 512, 512, 10, 128)
+    case = _RouteCase(wl)
+    case.x = case.x.copy()
+    case.x[:64] = 0
+    case.wr = case.wr.copy()
+    case.wr[:, 1::2] = case.wr[:, 0::2]
+    dev = torch.device("cuda")
+    case.x_t = torch.from_numpy(case.x).to(dev)
+    case.layer = moe.MoELayer(wl.H, wl.E, wl.k, wl.I, torch.from_numpy(case.wr).to(dev), None,
+                              None, max_tokens=wl.M)
+    ids_g, w_g = _check_router(case)
+    np.testing.assert_array_equal(ids_g[:64], np.tile(np.arange(wl.k, dtype=np.int32), (64, 1)))
+    assert np.max(np.abs(w_g[:64] - 1.0 / wl.k)) <= 1e-6
+    for t in range(64, wl.M):
+        sel = [int(e) for e in ids_g[t]]
+        for pos, e in enumerate(sel):
+            twin = e ^ 1
+            if e & 1:  # an odd expert is taken only after its even twin
+                assert twin in sel[:pos], (t, sel)
+    assert int(case.layer.status.item()) == 0
+
+
 @pytest.mark.parametrize("M,H,E,k", [(40, 256, 32, 32), (200, 4096, 136, 10), (100, 512, 512, 3)])
 def test_router_mma_shapes(M, H, E, k):
     """The mma.sync router (16 < M with E < 256, or M < 128): k = E = 32, the
