@@ -88,21 +88,6 @@ __device__ __forceinline__ bool entry_ok(const DecodeArgs& p, int e, int base, i
          base + count <= P;
 }
 
-// Starts the item's share (1 / n_rtp) of its expert's W2 bytes towards L2,
-// so that the W2 kernel finds them there (one thread).
-__device__ __forceinline__ void w2_share_prefetch(const DecodeArgs& p, const int* en, int rp) {
-  const LayerDims& d = p.d;
-  const int e = en[0];
-  if (!entry_ok(p, e, en[1], en[2])) return;
-  const bool sh = (e == d.E);
-  const size_t q2 = (size_t)d.H * d.I / 2, s2b = (size_t)d.H * d.I / 16 * p.sb;
-  const int n_rtp = d.I / 16;
-  const uint8_t* q2e = sh ? p.s2.q : p.w2.q + (size_t)e * q2;
-  const uint8_t* s2e = sh ? p.s2.s : p.w2.s + (size_t)e * s2b;
-  prefetch_l2_bulk(q2e + (size_t)rp * (q2 / n_rtp), (uint32_t)(q2 / n_rtp));
-  prefetch_l2_bulk(s2e + (size_t)rp * (s2b / n_rtp), (uint32_t)(s2b / n_rtp));
-}
-
 // W13 item (a, rp) for one block of 256 threads.  xs: staged token rows
 // (stride 2H + 16).
 template <int NT, int SB>
@@ -149,8 +134,6 @@ __device__ __forceinline__ void w13_item(const DecodeArgs& p, const int* en, int
     const int n_e = min(count - n0, NT * 8);
     const int pos0 = base + n0;
     load_group(warp);
-    // after this thread's own weight loads are in flight, not before them
-    if (n0 == 0 && ttid == 0) w2_share_prefetch(p, en, rp);
     if (ttid < n_e) {
       const int pair = (n0 + ttid < 16) ? en[4 + n0 + ttid] : __ldcg(p.pv.perm + pos0 + ttid);
       s_tok[ttid] = min(max(pair / d.k_eff, 0), p.M - 1);
