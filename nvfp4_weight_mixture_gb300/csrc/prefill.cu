@@ -23,11 +23,14 @@
 //   warps 0-7  dequantise each raw stage into tensor memory (two fragment
 //              blocks per warp: warp w owns lanes 32 (w % 4) .. +31 of A tile
 //              w / 4, the lanes its sub-partition may access), then run the
-//              unit's SwiGLU epilogue on the same lanes of accumulator w / 4;
+//              unit's SwiGLU epilogue on the same lanes of accumulator w / 4,
+//              staging the unit's h in shared memory and releasing tensor
+//              memory right after their last read;
 //   warp 8     one lane fills the token-row operand, one ring stage per K step
 //              (128-byte swizzled, K-major), with 64-row tensor-map loads of
-//              the token rows gathered into plan order beforehand (warps 9-11
-//              are spare);
+//              the token rows gathered into plan order beforehand;
+//   warps 9-11 write each unit's staged h rows out (whole 256-byte token
+//              rows), while the dequantising warps go on with the next unit;
 //   warp 12    allocates tensor memory; one lane issues the MMAs: per K step
 //              one wait (A and B stages share one barrier), then per A tile and
 //              16-element K slice one MMA with N = all of the unit's rows, then
