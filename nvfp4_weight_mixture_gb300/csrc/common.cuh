@@ -313,6 +313,11 @@ __device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) 
 }
 
 // ---- NVFP4 decode ----------------------------------------------------------
+// Byte b (0..3, a compile-time constant at every call) of w, zero-extended,
+// with one byte permute.
+__device__ __forceinline__ uint32_t byte_of(uint32_t w, int b) {
+  return __byte_perm(w, 0u, 0x4440u | (uint32_t)b);
+}
 // Two E2M1 codes (low nibble -> low half) to an FP16 pair.
 __device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte) {
   uint32_t r;
@@ -339,7 +344,7 @@ __device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b) {
 // of an E2M1 value and an E4M3 value is representable in FP16.
 __device__ __forceinline__ void dequant8(uint32_t word, uint32_t sc2, uint32_t out[4]) {
 #pragma unroll
-  for (int b = 0; b < 4; ++b) out[b] = hmul2_u32(e2m1x2_to_f16x2((word >> (8 * b)) & 0xFF), sc2);
+  for (int b = 0; b < 4; ++b) out[b] = hmul2_u32(e2m1x2_to_f16x2(byte_of(word, b)), sc2);
 }
 
 // Dequantised A fragment of k-step `s` (0..3) of a 16x64 fragment-layout block:
@@ -353,10 +358,11 @@ __device__ __forceinline__ void a_frag(const uint4& q, uint32_t sg, uint32_t sg8
   const uint32_t wg = (s < 2) ? q.x : q.y;
   const uint32_t wg8 = (s < 2) ? q.z : q.w;
   const int sh = 16 * (s & 1);
-  a[0] = hmul2_u32(e2m1x2_to_f16x2((wg >> sh) & 0xFF), sg);
-  a[2] = hmul2_u32(e2m1x2_to_f16x2((wg >> (sh + 8)) & 0xFF), sg);
-  a[1] = hmul2_u32(e2m1x2_to_f16x2((wg8 >> sh) & 0xFF), sg8);
-  a[3] = hmul2_u32(e2m1x2_to_f16x2((wg8 >> (sh + 8)) & 0xFF), sg8);
+  const int b0 = sh >> 3;
+  a[0] = hmul2_u32(e2m1x2_to_f16x2(byte_of(wg, b0)), sg);
+  a[2] = hmul2_u32(e2m1x2_to_f16x2(byte_of(wg, b0 + 1)), sg);
+  a[1] = hmul2_u32(e2m1x2_to_f16x2(byte_of(wg8, b0)), sg8);
+  a[3] = hmul2_u32(e2m1x2_to_f16x2(byte_of(wg8, b0 + 1)), sg8);
 }
 
 // FP16 scale splats of rows g (sg) and g + 8 (sg8) from their two E4M3 codes
